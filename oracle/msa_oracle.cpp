@@ -1,0 +1,182 @@
+// MSA forward oracle: plain, slow, fp64 CPU restatement of what the sparse
+// attention path computes. TEST INFRASTRUCTURE ONLY: the tests, the smoke check
+// and the bench's CPU-baseline / reference leg call it; the product library
+// never does. It shares no code, header or helper with the CUDA path.
+//
+// Sources (MiniMax Sparse Attention; three pages describing one method):
+//  * "MiniMax Sparse Attention" summary (hyper.ai, paper 2606.13392), section
+//    "方法" (Method): an Index Branch run per GQA group scores every causally
+//    visible key with the dot product of an index query and an index key,
+//    pools the token scores to blocks by max (Block Max Pooling), keeps the
+//    Top-K blocks, and always includes the block that holds the current query;
+//    the Main Branch then runs standard scaled-dot-product softmax attention
+//    over only the keys/values of the selected blocks.
+//  * quant_prune_distill post 751 (tgviewer), section "Метод" (Method): one
+//    index query head per query group and a single index key head for the
+//    whole layer; pre-softmax score, block maximum, top-K blocks by that
+//    maximum; the last block (sliding window) is always added.
+//  * same post, section "Эксперименты": 16 blocks of 128 tokens = 2048 tokens,
+//    i.e. the forced block counts toward K.
+//
+// Readings taken where the pages are silent:
+//  blocks are aligned to absolute position 0 (block t = keys [t*Bs, (t+1)*Bs));
+//  ties in the block maximum go to the lower block index; when a row sees at
+//  most K blocks all of them are selected and the list is padded with -1;
+//  the index score is the plain dot product (no scale: a positive scale
+//  cannot change a ranking); the attention scale is 1/sqrt(d) unless given;
+//  the causal mask keeps key j iff j <= pos, pos = q_offset[b] + i.
+//
+// Parity pins for every function here live in tests/test_oracle_pins.py.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+template <class F>
+void parallel_rows(int64_t nrows, int nthreads, F&& f) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 1024) nthreads = 1024;
+  if (nthreads == 1 || nrows < 2) {
+    for (int64_t r = 0; r < nrows; ++r) f(r);
+    return;
+  }
+  std::vector<std::thread> pool;
+  for (int t = 0; t < nthreads; ++t)
+    pool.emplace_back([&, t] {
+      for (int64_t r = t; r < nrows; r += nthreads) f(r);  // interleaved: cost grows with position
+    });
+  for (auto& th : pool) th.join();
+}
+
+// Index Branch for one (row, group): token scores, block maxima, selection.
+// Writes K entries of `sel` (ascending block ids, -1 padded) and, if given,
+// nblk entries of `bmax` (NaN where a block is not visible).
+void index_select_one(const float* iq_g, const float* ik_b, int di, int pos, int L, int Bs, int K, int nblk,
+                      int* sel, double* bmax) {
+  const int jmax = std::min(pos, L - 1);  // last causally visible key
+  const int loc = pos / Bs;               // block holding the query
+  std::vector<double> M(loc + 1, -std::numeric_limits<double>::infinity());
+  for (int j = 0; j <= jmax; ++j) {
+    double s = 0.0;  // pre-softmax index score: plain dot product
+    for (int c = 0; c < di; ++c) s += double(iq_g[c]) * double(ik_b[int64_t(j) * di + c]);
+    const int t = j / Bs;
+    if (s > M[t]) M[t] = s;  // block max pooling
+  }
+  if (bmax) {
+    for (int t = 0; t < nblk; ++t) bmax[t] = t <= loc ? M[t] : std::numeric_limits<double>::quiet_NaN();
+  }
+  std::vector<int> chosen;
+  if (loc + 1 <= K) {
+    for (int t = 0; t <= loc; ++t) chosen.push_back(t);  // every visible block
+  } else {
+    std::vector<int> cand(loc);
+    for (int t = 0; t < loc; ++t) cand[t] = t;
+    std::sort(cand.begin(), cand.end(), [&](int a, int b) {
+      if (M[a] != M[b]) return M[a] > M[b];  // higher block maximum first
+      return a < b;                          // tie: lower block index
+    });
+    for (int k = 0; k < K - 1; ++k) chosen.push_back(cand[k]);
+    chosen.push_back(loc);  // the query's own block is always kept
+    std::sort(chosen.begin(), chosen.end());
+  }
+  for (int k = 0; k < K; ++k) sel[k] = k < int(chosen.size()) ? chosen[k] : -1;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Index Branch for a list of query rows.
+//   iq_rows  [nrows, G, di]    index queries of the listed rows
+//   ik       [B, Nk, di]       the layer's single index key head
+//   row_b, row_i [nrows]       sequence and query index of each listed row
+//   q_offset, kv_len [B]       pos = q_offset[b] + i; keys j < kv_len[b]
+//   sel      [nrows, G, K]     out: ascending block ids, -1 padded
+//   block_max [nrows, G, nblk] out (optional): fp64 block maxima, NaN if not visible
+int msa_oracle_index_select(const float* iq_rows, const float* ik, const int32_t* row_b, const int32_t* row_i,
+                            int64_t nrows, const int32_t* q_offset, const int32_t* kv_len, int B, int Nk, int G,
+                            int di, int Bs, int K, int32_t* sel, double* block_max, int nthreads) {
+  if (!iq_rows || !ik || !row_b || !row_i || !q_offset || !kv_len || !sel) return 1;
+  if (B < 1 || Nk < 1 || G < 1 || di < 1 || Bs < 1 || K < 1 || nrows < 0) return 1;
+  const int nblk = (Nk + Bs - 1) / Bs;
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int b = row_b[r];
+    if (b < 0 || b >= B) return 1;
+    const int pos = q_offset[b] + row_i[r];
+    if (pos < 0 || kv_len[b] < 1 || kv_len[b] > Nk || pos >= kv_len[b]) return 1;
+  }
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    const int b = row_b[r];
+    const int pos = q_offset[b] + row_i[r];
+    for (int g = 0; g < G; ++g) {
+      index_select_one(iq_rows + (r * G + g) * di, ik + int64_t(b) * Nk * di, di, pos, kv_len[b], Bs, K, nblk,
+                       sel + (r * G + g) * K, block_max ? block_max + (r * G + g) * nblk : nullptr);
+    }
+  });
+  return 0;
+}
+
+// Main Branch for a list of query rows: exact softmax attention over the
+// tokens of the selected blocks, causally masked.
+//   q_rows [nrows, Hq, d]; k, v [B, Nk, Hkv, d]; sel_rows [nrows, G=Hkv, K]
+//   out [nrows, Hq, d] (fp64); lse [nrows, Hq] (fp64, optional)
+//   scale <= 0 selects 1/sqrt(d).
+int msa_oracle_sparse_attn(const float* q_rows, const float* k, const float* v, const int32_t* sel_rows,
+                           const int32_t* row_b, const int32_t* row_i, int64_t nrows, const int32_t* q_offset,
+                           const int32_t* kv_len, int B, int Nk, int Hq, int Hkv, int d, int Bs, int K,
+                           double scale, double* out, double* lse, int nthreads) {
+  if (!q_rows || !k || !v || !sel_rows || !row_b || !row_i || !q_offset || !kv_len || !out) return 1;
+  if (B < 1 || Nk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || Bs < 1 || K < 1) return 1;
+  if (scale <= 0.0) scale = 1.0 / std::sqrt(double(d));
+  const int nblk = (Nk + Bs - 1) / Bs;
+  const int heads_per_group = Hq / Hkv;
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    const int b = row_b[r];
+    const int pos = q_offset[b] + row_i[r];
+    const int L = kv_len[b];
+    std::vector<int> keys;
+    std::vector<double> s;
+    for (int h = 0; h < Hq; ++h) {
+      const int g = h / heads_per_group;  // GQA: query head h reads key/value head g
+      const int32_t* sl = sel_rows + (r * Hkv + g) * K;
+      keys.clear();
+      for (int kk = 0; kk < K; ++kk) {
+        const int t = sl[kk];
+        if (t < 0 || t >= nblk) continue;
+        for (int j = t * Bs; j < (t + 1) * Bs && j < L && j <= pos; ++j) keys.push_back(j);
+      }
+      const float* qh = q_rows + (r * Hq + h) * int64_t(d);
+      double* oh = out + (r * Hq + h) * int64_t(d);
+      for (int c = 0; c < d; ++c) oh[c] = 0.0;
+      if (keys.empty()) {
+        if (lse) lse[r * Hq + h] = -std::numeric_limits<double>::infinity();
+        continue;
+      }
+      s.assign(keys.size(), 0.0);
+      double m = -std::numeric_limits<double>::infinity();
+      for (size_t n = 0; n < keys.size(); ++n) {
+        const float* kj = k + ((int64_t(b) * Nk + keys[n]) * Hkv + g) * int64_t(d);
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += double(qh[c]) * double(kj[c]);
+        s[n] = acc * scale;
+        m = std::max(m, s[n]);
+      }
+      double l = 0.0;
+      for (size_t n = 0; n < keys.size(); ++n) {
+        const double w = std::exp(s[n] - m);
+        l += w;
+        const float* vj = v + ((int64_t(b) * Nk + keys[n]) * Hkv + g) * int64_t(d);
+        for (int c = 0; c < d; ++c) oh[c] += w * double(vj[c]);
+      }
+      for (int c = 0; c < d; ++c) oh[c] /= l;
+      if (lse) lse[r * Hq + h] = m + std::log(l);
+    }
+  });
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,315 @@
+"""Pins for the CPU oracle: each checks it against something other than itself.
+
+* a hand-worked example derived from the method's definition (tests/golden);
+* brute-force token scores via a library matmul (block max pooling);
+* the top-K optimality / structure invariants of the selection;
+* a second, differently written selection (repeated arg-max in pure Python);
+* closed forms: all-equal scores select blocks 0..K-2 plus the local block;
+  a planted block is selected by every row that can see it;
+* the dense special case (K >= visible blocks) equals textbook causal GQA
+  attention from torch's scaled_dot_product_attention in fp64;
+* the masked-dense restatement (selected blocks as an explicit attention mask)
+  equals torch's SDPA for partial selections, with ragged offsets / lengths;
+* decode at length L equals the prefill row at position L-1;
+* planted mistakes in a copy of the oracle source fail at least one pin.
+"""
+import math
+import os
+import re
+import shutil
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "handworked_msa.txt")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def rand_problem(seed, B=2, Nq=96, Nk=96, Hq=4, Hkv=2, d=16, di=8, a=3, q_offset=None, kv_len=None):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Nq, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((B, Nk, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, Nk, Hkv, d)).astype(np.float32)
+    iq = rng.integers(-a, a + 1, (B, Nq, Hkv, di)).astype(np.float32)
+    ik = rng.integers(-a, a + 1, (B, Nk, di)).astype(np.float32)
+    q_offset = np.zeros(B, np.int32) if q_offset is None else np.asarray(q_offset, np.int32)
+    kv_len = np.full(B, Nk, np.int32) if kv_len is None else np.asarray(kv_len, np.int32)
+    return q, k, v, iq, ik, q_offset, kv_len
+
+
+def sdpa_masked(q, k, v, allowed, scale):
+    """torch SDPA (fp64, CPU) with an explicit boolean mask.
+
+    q [B,Nq,Hq,d]; k,v [B,Nk,Hkv,d]; allowed [B,Nq,Hkv,Nk] bool (per group).
+    """
+    B, Nq, Hq, d = q.shape
+    Hkv = k.shape[2]
+    hpg = Hq // Hkv
+    qt = torch.from_numpy(q.astype(np.float64)).permute(0, 2, 1, 3)
+    kt = torch.from_numpy(k.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(hpg, dim=1)
+    vt = torch.from_numpy(v.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(hpg, dim=1)
+    m = torch.from_numpy(allowed).permute(0, 2, 1, 3).repeat_interleave(hpg, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=m, scale=scale)
+    s = torch.einsum("bhqc,bhkc->bhqk", qt, kt) * scale
+    lse = torch.logsumexp(s.masked_fill(~m, -math.inf), dim=-1)
+    return out.permute(0, 2, 1, 3).numpy(), lse.permute(0, 2, 1).numpy()
+
+
+def causal_allowed(B, Nq, Nk, Hkv, q_offset, kv_len):
+    j = np.arange(Nk)
+    al = np.zeros((B, Nq, Hkv, Nk), dtype=bool)
+    for b in range(B):
+        pos = q_offset[b] + np.arange(Nq)
+        al[b] = ((j[None, :] <= pos[:, None]) & (j[None, :] < kv_len[b]))[:, None, :]
+    return al
+
+
+def selected_allowed(sel, Bs, B, Nq, Nk, Hkv, q_offset, kv_len):
+    al = causal_allowed(B, Nq, Nk, Hkv, q_offset, kv_len)
+    blk = np.arange(Nk) // Bs
+    keep = np.zeros_like(al)
+    for b in range(B):
+        for i in range(Nq):
+            for g in range(Hkv):
+                s = sel[b, i, g]
+                keep[b, i, g] = np.isin(blk, s[s >= 0])
+    return al & keep
+
+
+def token_scores(iq, ik):
+    """[B,Nq,G,Nk] index scores by a library matmul (fp64)."""
+    return np.einsum("bigc,bjc->bigj", iq.astype(np.float64), ik.astype(np.float64))
+
+
+def argmax_selection(M, loc, K):
+    """Second implementation: K-1 rounds of arg-max (first max = lowest index)."""
+    if loc + 1 <= K:
+        return list(range(loc + 1)) + [-1] * (K - loc - 1)
+    avail = list(range(loc))
+    chosen = []
+    for _ in range(K - 1):
+        best = None
+        for t in avail:
+            if best is None or M[t] > M[best]:
+                best = t
+        chosen.append(best)
+        avail.remove(best)
+    return sorted(chosen + [loc])
+
+
+def oracle_all(q, k, v, iq, ik, Bs, K, q_offset, kv_len, lib=None, scale=0.0):
+    return oracle.msa_forward(q, k, v, iq, ik, Bs, K, q_offset=q_offset, kv_len=kv_len, scale=scale, lib=lib)
+
+
+# ---------------------------------------------------------------------------
+# pins (each takes an optional lib so the mutation test can rerun them)
+# ---------------------------------------------------------------------------
+def pin_golden(lib=None):
+    ik = None
+    attn_k = attn_v = expect = None
+    with open(GOLDEN) as f:
+        lines = [ln.split("#")[0].strip() for ln in f]
+    lines = [ln for ln in lines if ln]
+    ik = np.array([3, 1, 4, 1, 5, 9, 2, 6, 5, 3], np.float32).reshape(1, 10, 1)
+    Bs = 2
+    for ln in lines:
+        head, _, tail = ln.partition(":")
+        parts = head.split()
+        if parts[0] == "select":
+            iqv, pos, K = float(parts[1]), int(parts[2]), int(parts[3])
+            want = [int(x) for x in tail.split()]
+            sel = oracle.index_select(np.full((1, 1, 1), iqv, np.float32), ik, [0], [pos], [0], [10], Bs, K,
+                                      lib=lib)
+            assert sel[0, 0].tolist() == want, (ln, sel[0, 0].tolist())
+        elif parts[0] == "blockmax":
+            iqv, pos = float(parts[1]), int(parts[2])
+            want = [float(x) for x in tail.split()]
+            _, bm = oracle.index_select(np.full((1, 1, 1), iqv, np.float32), ik, [0], [pos], [0], [10], Bs, 2,
+                                        want_block_max=True, lib=lib)
+            assert bm[0, 0, :len(want)].tolist() == want, (ln, bm[0, 0].tolist())
+        elif parts[0] == "attend":
+            vals = [float(x) for x in parts[2:]]
+            if parts[1] == "k":
+                attn_k = np.array(vals, np.float32).reshape(1, 10, 1, 1)
+            elif parts[1] == "v":
+                attn_v = np.array(vals, np.float32).reshape(1, 10, 1, 1)
+            else:
+                expect = vals
+    out, lse = oracle.sparse_attn(np.ones((1, 1, 1), np.float32), attn_k, attn_v,
+                                  np.array([[[1, 2]]], np.int32), [0], [4], [0], [10], Bs, 2, scale=1.0, lib=lib)
+    assert abs(out[0, 0, 0] - expect[0]) < 1e-6 and abs(lse[0, 0] - expect[1]) < 1e-6, (out, lse)
+
+
+def pin_blockmax_bruteforce(lib=None):
+    q, k, v, iq, ik, _, _ = rand_problem(1)
+    Nq = 56
+    iq = iq[:, :Nq]
+    kl = np.array([96, 96], np.int32)
+    qo = np.array([0, 40], np.int32)
+    Bs, K = 8, 4
+    rb, ri = oracle.all_rows(2, Nq)
+    sel, bm = oracle.index_select(iq.reshape(-1, 2, 8), ik, rb, ri, qo, kl, Bs, K, want_block_max=True, lib=lib)
+    s = token_scores(iq, ik)
+    bm = bm.reshape(2, Nq, 2, -1)
+    for b in range(2):
+        for i in range(Nq):
+            pos = qo[b] + i
+            loc = pos // Bs
+            for g in range(2):
+                for t in range(loc + 1):
+                    hi = min((t + 1) * Bs, pos + 1)
+                    assert bm[b, i, g, t] == s[b, i, g, t * Bs:hi].max()
+                assert np.isnan(bm[b, i, g, loc + 1:]).all()
+
+
+def pin_selection_invariants(lib=None):
+    for seed, Bs, K in [(2, 8, 4), (3, 4, 7), (4, 16, 2), (5, 8, 1)]:
+        q, k, v, iq, ik, qo, kl = rand_problem(seed, q_offset=[0, 17], kv_len=[96, 96])
+        Nq = 79
+        iq = iq[:, :Nq]
+        rb, ri = oracle.all_rows(2, Nq)
+        sel, bm = oracle.index_select(iq.reshape(-1, 2, 8), ik, rb, ri, qo, kl, Bs, K, want_block_max=True,
+                                      lib=lib)
+        for r in range(len(rb)):
+            pos = qo[rb[r]] + ri[r]
+            loc = pos // Bs
+            for g in range(2):
+                s = sel[r, g]
+                valid = s[s >= 0]
+                assert (s[len(valid):] == -1).all()
+                assert len(valid) == min(K, loc + 1)
+                assert (np.diff(valid) > 0).all() and valid.min() >= 0 and valid.max() <= loc
+                assert loc in valid
+                M = bm[r, g]
+                others = [t for t in valid if t != loc]
+                unsel = [t for t in range(loc) if t not in valid]
+                if others and unsel:
+                    worst = min((M[t], -t) for t in others)
+                    best_out = max((M[t], -t) for t in unsel)
+                    assert worst > best_out
+                assert list(s) == argmax_selection(M, loc, K)
+
+
+def pin_closed_forms(lib=None):
+    # all-equal scores (index query zero): blocks 0..K-2 plus the local block
+    B, Nq, Nk, di, Bs, K = 1, 64, 64, 4, 4, 5
+    ik = np.random.default_rng(0).integers(-3, 4, (B, Nk, di)).astype(np.float32)
+    iq = np.zeros((B * Nq, 1, di), np.float32)
+    rb, ri = oracle.all_rows(B, Nq)
+    sel = oracle.index_select(iq, ik, rb, ri, [0], [Nk], Bs, K, lib=lib)
+    for i in range(Nq):
+        loc = i // Bs
+        want = list(range(loc + 1)) + [-1] * (K - loc - 1) if loc + 1 <= K else list(range(K - 1)) + [loc]
+        assert sel[i, 0].tolist() == want
+    # planted block: index query e0, index key dim 0 large on block t*
+    tstar = 6
+    ik2 = np.random.default_rng(1).integers(-3, 4, (B, Nk, di)).astype(np.float32)
+    ik2[0, tstar * Bs:(tstar + 1) * Bs, 0] = 100.0
+    iq2 = np.zeros((B * Nq, 1, di), np.float32)
+    iq2[:, 0, 0] = 1.0
+    sel2 = oracle.index_select(iq2, ik2, rb, ri, [0], [Nk], Bs, 2, lib=lib)
+    for i in range(Nq):
+        if i // Bs > tstar:
+            assert tstar in sel2[i, 0].tolist()
+
+
+def pin_dense_equals_sdpa(lib=None):
+    # K >= visible blocks: MSA equals dense causal GQA attention
+    q, k, v, iq, ik, qo, kl = rand_problem(7, B=2, Nq=40, Nk=96, q_offset=[56, 30], kv_len=[96, 70])
+    Bs, K = 8, 12
+    sel, out, lse = oracle_all(q, k, v, iq, ik, Bs, K, qo, kl, lib=lib)
+    al = causal_allowed(2, 40, 96, 2, qo, kl)
+    ref, ref_lse = sdpa_masked(q, k, v, al, 1.0 / math.sqrt(16))
+    assert np.abs(out - ref).max() < 1e-12
+    assert np.abs(lse - ref_lse).max() < 1e-12
+
+
+def pin_masked_dense_equals_sdpa(lib=None):
+    for seed, Bs, K in [(8, 8, 3), (9, 4, 5), (10, 16, 2)]:
+        q, k, v, iq, ik, qo, kl = rand_problem(seed, B=2, Nq=50, Nk=96, q_offset=[46, 20], kv_len=[96, 70])
+        sel, out, lse = oracle_all(q, k, v, iq, ik, Bs, K, qo, kl, lib=lib)
+        al = selected_allowed(sel, Bs, 2, 50, 96, 2, qo, kl)
+        ref, ref_lse = sdpa_masked(q, k, v, al, 1.0 / math.sqrt(16))
+        assert np.abs(out - ref).max() < 1e-12
+        assert np.abs(lse - ref_lse).max() < 1e-12
+
+
+def pin_attention_special_cases(lib=None):
+    q, k, v, iq, ik, qo, kl = rand_problem(11)
+    Bs, K = 8, 3
+    # position 0 attends only to key 0: output is v[0] of its group
+    sel, out, lse = oracle_all(q, k, v, iq, ik, Bs, K, [0, 0], [96, 96], lib=lib)
+    for h in range(4):
+        assert np.array_equal(out[:, 0, h], v[:, 0, h // 2].astype(np.float64))
+    # constant values: weights sum to one
+    ones = np.ones_like(v)
+    _, out1, _ = oracle_all(q, k, ones, iq, ik, Bs, K, [0, 0], [96, 96], lib=lib)
+    assert np.abs(out1 - 1.0).max() < 1e-12
+    # convex combination of the selected values
+    for b in range(2):
+        for i in range(0, 96, 7):
+            for h in range(4):
+                g = h // 2
+                s = sel[b, i, g]
+                keys = [j for t in s[s >= 0] for j in range(t * Bs, (t + 1) * Bs) if j <= i]
+                vv = v[b, keys, g].astype(np.float64)
+                assert (out[b, i, h] >= vv.min(0) - 1e-12).all() and (out[b, i, h] <= vv.max(0) + 1e-12).all()
+
+
+def pin_decode_equals_prefill_row(lib=None):
+    q, k, v, iq, ik, qo, kl = rand_problem(12, B=2, Nq=96, Nk=96)
+    Bs, K = 8, 4
+    sel, out, lse = oracle_all(q, k, v, iq, ik, Bs, K, [0, 0], [96, 96], lib=lib)
+    for L in (1, 9, 57, 96):
+        dsel, dout, dlse = oracle_all(q[:, L - 1:L], k, v, iq[:, L - 1:L], ik, Bs, K, [L - 1, L - 1], [L, L],
+                                      lib=lib)
+        assert np.array_equal(dsel[:, 0], sel[:, L - 1])
+        assert np.abs(dout[:, 0] - out[:, L - 1]).max() < 1e-12
+
+
+PINS = [pin_golden, pin_blockmax_bruteforce, pin_selection_invariants, pin_closed_forms, pin_dense_equals_sdpa,
+        pin_masked_dense_equals_sdpa, pin_attention_special_cases, pin_decode_equals_prefill_row]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: a broken copy of the oracle must fail some pin
+# ---------------------------------------------------------------------------
+MUTATIONS = {
+    "tie_to_higher_block": ("return a < b;", "return a > b;"),
+    "local_block_not_forced": ("chosen.push_back(loc);  // the query's own block is always kept",
+                               "chosen.push_back(cand[K - 1]);"),
+    "causal_excludes_diagonal": ("j < L && j <= pos; ++j", "j < L && j < pos; ++j"),
+    "gqa_head_map_modulo": ("const int g = h / heads_per_group;", "const int g = h % Hkv;"),
+    "scale_without_sqrt": ("scale = 1.0 / std::sqrt(double(d));", "scale = 1.0 / double(d);"),
+    "score_dim_off_by_one": ("for (int c = 0; c < di; ++c) s +=", "for (int c = 1; c < di; ++c) s +="),
+    "blockmax_keeps_min": ("if (s > M[t]) M[t] = s;", "if (s < M[t] || M[t] == -std::numeric_limits<double>::infinity()) M[t] = s;"),
+    "selects_lowest_maxima": ("if (M[a] != M[b]) return M[a] > M[b];", "if (M[a] != M[b]) return M[a] < M[b];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    src = os.path.join(os.path.dirname(oracle.__file__), "msa_oracle.cpp")
+    text = open(src).read()
+    old, new = MUTATIONS[name]
+    assert text.count(old) == 1, name
+    mut_src = tmp_path / "mut.cpp"
+    mut_src.write_text(text.replace(old, new))
+    lib = oracle.load(oracle.build(str(mut_src), str(tmp_path / "libmut.so")))
+    failed = []
+    for pin in PINS:
+        try:
+            pin(lib=lib)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"mutation {name} passed every pin"
