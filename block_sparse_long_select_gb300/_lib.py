@@ -1,0 +1,159 @@
+"""ctypes binding of libmsa.so: argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+from functools import lru_cache
+
+MSA_BF16, MSA_FP32 = 0, 1
+MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE = 0, 1, 2
+STATUS_NAMES = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
+                4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_BOUNDS"}
+
+# (name, restype, argtypes) of every symbol declared in include/msa.h
+_vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "msa_workspace_size": (_sz, [_i32] * 11),
+    "msa_index_select": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 8 + [_vp, _vp, _vp, _sz, _vp]),
+    "msa_sparse_attn_prefill": (_i32, [_vp] * 6 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "msa_sparse_attn_decode": (_i32, [_vp] * 5 + [_i32] * 7 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "msa_read_status": (_i32, [_vp, _vp]),
+    "msa_status_string": (ctypes.c_char_p, [_i32]),
+}
+
+
+class MsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+
+
+def lib_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsa.so")
+
+
+@lru_cache(maxsize=None)
+def load_library():
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with block_sparse_long_select_gb300.build() "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    return lib
+
+
+# ---------------------------------------------------------------------------
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return MSA_BF16
+    if t.dtype == torch.float32:
+        return MSA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise MsaError(code, where)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def msa_workspace_size(op, B, Nq, Nk, G, Hq, d, di, Bs, K, dtype) -> int:
+    return int(load_library().msa_workspace_size(op, B, Nq, Nk, G, Hq, d, di, Bs, K, dtype))
+
+
+def workspace(nbytes: int, device="cuda"):
+    """Zero-filled device scratch of ``nbytes`` (caching-allocator blocks are 512-byte aligned)."""
+    import torch
+
+    ws = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def msa_index_select(iq, ik, q_offset, kv_len, Bs, K, sel=None, block_max=None, ws=None, stream=None):
+    """iq [B,Nq,G,di], ik [B,Nk,di] -> sel [B,Nq,G,K] int32 (see include/msa.h)."""
+    import torch
+
+    _need_cuda(iq, ik, q_offset, kv_len, sel, block_max)
+    B, Nq, G, di = iq.shape
+    Nk = ik.shape[1]
+    dt = _dtype_code(iq)
+    if sel is None:
+        sel = torch.empty((B, Nq, G, K), dtype=torch.int32, device=iq.device)
+    if ws is None:
+        ws = workspace(msa_workspace_size(MSA_OP_INDEX_SELECT, B, Nq, Nk, G, 0, 0, di, Bs, K, dt), iq.device)
+    code = load_library().msa_index_select(_ptr(iq), _ptr(ik), _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, G, di, Bs,
+                                           K, dt, _ptr(sel), _ptr(block_max), _ptr(ws), ws.numel(),
+                                           _stream(stream, iq.device))
+    _check(code, "msa_index_select")
+    return sel
+
+
+def msa_sparse_attn_prefill(q, k, v, sel, q_offset, kv_len, Bs, K, scale=0.0, out=None, lse=None, ws=None,
+                            stream=None):
+    """q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d], sel [B,Nq,Hkv,K] -> out [B,Nq,Hq,d]."""
+    import torch
+
+    _need_cuda(q, k, v, sel, q_offset, kv_len, out, lse)
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(msa_workspace_size(MSA_OP_PREFILL, B, Nq, Nk, Hkv, Hq, d, 0, Bs, K, dt), q.device)
+    code = load_library().msa_sparse_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(sel), _ptr(q_offset),
+                                                  _ptr(kv_len), B, Nq, Nk, Hq, Hkv, d, Bs, K, float(scale), dt,
+                                                  _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                                  _stream(stream, q.device))
+    _check(code, "msa_sparse_attn_prefill")
+    return out
+
+
+def msa_sparse_attn_decode(q, k_cache, v_cache, sel, kv_len, Bs, K, scale=0.0, out=None, lse=None, ws=None,
+                           stream=None):
+    """q [B,Hq,d], caches [B,Lmax,Hkv,d], sel [B,Hkv,K] (or [B,1,Hkv,K]) -> out [B,Hq,d]."""
+    import torch
+
+    _need_cuda(q, k_cache, v_cache, sel, kv_len, out, lse)
+    B, Hq, d = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    dt = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(msa_workspace_size(MSA_OP_DECODE, B, 1, Lmax, Hkv, Hq, d, 0, Bs, K, dt), q.device)
+    code = load_library().msa_sparse_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(sel), _ptr(kv_len),
+                                                 B, Lmax, Hq, Hkv, d, Bs, K, float(scale), dt, _ptr(out), _ptr(lse),
+                                                 _ptr(ws), ws.numel(), _stream(stream, q.device))
+    _check(code, "msa_sparse_attn_decode")
+    return out
+
+
+def msa_read_status(ws, stream=None) -> int:
+    return int(load_library().msa_read_status(_ptr(ws), _stream(stream, ws.device)))
+
+
+def msa_status_string(code: int) -> str:
+    return load_library().msa_status_string(int(code)).decode()

@@ -1,0 +1,180 @@
+// C ABI of the MSA forward path: host-side validation, workspace planning and
+// dispatch to the kernels. Every entry point is asynchronous on its stream.
+#include <cstring>
+
+#include "msa_internal.cuh"
+
+namespace msa {
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool dtype_ok(int dtype) { return dtype == MSA_BF16 || dtype == MSA_FP32; }
+
+// ---- Index Branch planning ---------------------------------------------------
+struct IndexPlan {
+  bool ok = false;
+  msa_status_t err = MSA_ERR_INVALID_ARG;
+  size_t table_off = 0, table_bytes = 0;  // table region inside ws (0 if none)
+  size_t ws_bytes = 0;
+};
+
+IndexPlan plan_index(int B, int Nq, int Nk, int G, int di, int Bs, int K, int dtype, bool have_block_max) {
+  IndexPlan p;
+  if (B < 1 || Nq < 1 || Nk < 1 || G < 1 || di < 1 || Bs < 1 || K < 1 || !dtype_ok(dtype)) return p;
+  if (Nq > Nk) return p;
+  if (di != 32 && di != 64) {
+    p.err = MSA_ERR_UNSUPPORTED;
+    return p;
+  }
+  if (Bs > kMaxBs || K > kMaxK) {
+    p.err = MSA_ERR_UNSUPPORTED;
+    return p;
+  }
+  const int nblk = (Nk + Bs - 1) / Bs;
+  const size_t table = size_t(B) * Nq * G * nblk * sizeof(float);
+  p.table_off = kWsHeader;
+  p.table_bytes = have_block_max ? 0 : align256(table);
+  p.ws_bytes = kWsHeader + align256(table);  // size for the case without block_max
+  p.ok = true;
+  p.err = MSA_OK;
+  return p;
+}
+
+// ---- Main Branch planning ----------------------------------------------------
+struct AttnPlan {
+  bool ok = false;
+  msa_status_t err = MSA_ERR_INVALID_ARG;
+  size_t ws_bytes = 0;
+};
+
+AttnPlan plan_attn(int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K, int dtype) {
+  AttnPlan p;
+  if (B < 1 || Nq < 1 || Nk < 1 || Hq < 1 || Hkv < 1 || d < 1 || Bs < 1 || K < 1 || !dtype_ok(dtype)) return p;
+  if (Hq % Hkv != 0 || Nq > Nk) return p;
+  if ((d != 64 && d != 128) || Bs > kMaxBs || K > kMaxK) {
+    p.err = MSA_ERR_UNSUPPORTED;
+    return p;
+  }
+  p.ws_bytes = kWsHeader;
+  p.ok = true;
+  p.err = MSA_OK;
+  return p;
+}
+
+msa_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need) return MSA_ERR_WORKSPACE;
+  return MSA_OK;
+}
+
+inline msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+inline uint32_t* status_word(void* ws) { return &static_cast<WsHeader*>(ws)->status; }
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K,
+                                     int dtype) {
+  switch (op) {
+    case MSA_OP_INDEX_SELECT: {
+      IndexPlan p = plan_index(B, Nq, Nk, G, di, Bs, K, dtype, false);
+      return p.ok ? p.ws_bytes : 0;
+    }
+    case MSA_OP_PREFILL: {
+      AttnPlan p = plan_attn(B, Nq, Nk, Hq, G > 0 ? G : 1, d, Bs, K, dtype);
+      return p.ok ? p.ws_bytes : 0;
+    }
+    case MSA_OP_DECODE: {
+      AttnPlan p = plan_attn(B, 1, Nk, Hq, G > 0 ? G : 1, d, Bs, K, dtype);
+      return p.ok ? p.ws_bytes : 0;
+    }
+    default:
+      return 0;
+  }
+}
+
+extern "C" msa_status_t msa_index_select(const void* iq, const void* ik, const int32_t* q_offset,
+                                         const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs, int K,
+                                         int dtype, int32_t* sel, float* block_max, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream) {
+  if (!iq || !ik || !sel) return MSA_ERR_INVALID_ARG;
+  IndexPlan p = plan_index(B, Nq, Nk, G, di, Bs, K, dtype, block_max != nullptr);
+  if (!p.ok) return p.err;
+  msa_status_t w = check_ws(ws, ws_bytes, block_max ? kWsHeader : p.ws_bytes);
+  if (w != MSA_OK) return w;
+  uint32_t* status = status_word(ws);
+  float* table = block_max ? block_max : reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);
+  cudaError_t e = launch_index_blockmax_table(dtype, iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, table, status,
+                                              stream);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  e = launch_topk_from_table(table, q_offset, kv_len, B, Nq, Nk, G, Bs, K, sel, status, stream);
+  return cuda_status(e);
+}
+
+extern "C" msa_status_t msa_sparse_attn_prefill(const void* q, const void* k, const void* v, const int32_t* sel,
+                                                const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk,
+                                                int Hq, int Hkv, int d, int Bs, int K, float scale, int dtype,
+                                                void* out, float* lse, void* ws, size_t ws_bytes,
+                                                cudaStream_t stream) {
+  if (!q || !k || !v || !sel || !out) return MSA_ERR_INVALID_ARG;
+  AttnPlan p = plan_attn(B, Nq, Nk, Hq, Hkv, d, Bs, K, dtype);
+  if (!p.ok) return p.err;
+  msa_status_t w = check_ws(ws, ws_bytes, p.ws_bytes);
+  if (w != MSA_OK) return w;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
+  cudaError_t e = launch_attn_query_outer(dtype, q, k, v, sel, q_offset, kv_len, false, B, Nq, Nk, Hq, Hkv, d, Bs,
+                                          K, scale, out, lse, status_word(ws), stream);
+  return cuda_status(e);
+}
+
+extern "C" msa_status_t msa_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                                               const int32_t* sel, const int32_t* kv_len, int B, int Lmax, int Hq,
+                                               int Hkv, int d, int Bs, int K, float scale, int dtype, void* out,
+                                               float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!q || !k_cache || !v_cache || !sel || !kv_len || !out) return MSA_ERR_INVALID_ARG;
+  AttnPlan p = plan_attn(B, 1, Lmax, Hq, Hkv, d, Bs, K, dtype);
+  if (!p.ok) return p.err;
+  msa_status_t w = check_ws(ws, ws_bytes, p.ws_bytes);
+  if (w != MSA_OK) return w;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
+  cudaError_t e = launch_attn_query_outer(dtype, q, k_cache, v_cache, sel, nullptr, kv_len, true, B, 1, Lmax, Hq,
+                                          Hkv, d, Bs, K, scale, out, lse, status_word(ws), stream);
+  return cuda_status(e);
+}
+
+extern "C" msa_status_t msa_read_status(void* ws, cudaStream_t stream) {
+  if (!ws) return MSA_ERR_INVALID_ARG;
+  uint32_t host = 0;
+  if (cudaMemcpyAsync(&host, status_word(ws), sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MSA_ERR_CUDA;
+  if (host != 0) {
+    if (cudaMemsetAsync(status_word(ws), 0, sizeof(uint32_t), stream) != cudaSuccess) return MSA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  return static_cast<msa_status_t>(host);
+}
+
+extern "C" const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK:
+      return "MSA_OK";
+    case MSA_ERR_INVALID_ARG:
+      return "MSA_ERR_INVALID_ARG: invalid argument";
+    case MSA_ERR_UNSUPPORTED:
+      return "MSA_ERR_UNSUPPORTED: shape or dtype not built";
+    case MSA_ERR_WORKSPACE:
+      return "MSA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MSA_ERR_CUDA:
+      return "MSA_ERR_CUDA: CUDA launch or runtime error";
+    case MSA_ERR_TIMEOUT:
+      return "MSA_ERR_TIMEOUT: a bounded device wait ran out";
+    case MSA_ERR_BOUNDS:
+      return "MSA_ERR_BOUNDS: q_offset, kv_len or sel out of range";
+    default:
+      return "MSA status: unknown code";
+  }
+}

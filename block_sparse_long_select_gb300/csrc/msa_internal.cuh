@@ -1,0 +1,82 @@
+// Internal declarations shared by the MSA CUDA translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+namespace msa {
+
+constexpr int kNumSMs = 152;       // GB300: 2 dies x 76 SMs
+constexpr size_t kWsHeader = 256;  // status word + counters, then op regions
+constexpr int kMaxK = 64;
+constexpr int kMaxBs = 1024;
+
+// First 256 bytes of every workspace.
+struct WsHeader {
+  uint32_t status;        // sticky msa_status_t set by kernels
+  uint32_t work_counter;  // persistent-grid work queue head (reset per launch)
+  uint32_t reserved[62];
+};
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
+  atomicCAS(status, 0u, code);  // the first error wins
+}
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Order-preserving map of a float block maximum and its block id to one
+// unsigned 64-bit key: a larger key means a larger maximum, and among equal
+// maxima the lower block id. -0 is folded onto +0 so that the two compare
+// equal, as they do in floating point.
+__device__ __forceinline__ uint64_t rank_key(float m, int t) {
+  uint32_t u = __float_as_uint(m);
+  if (u == 0x80000000u) u = 0u;
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (uint64_t(u) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(t));
+}
+__device__ __forceinline__ int rank_key_block(uint64_t key) { return int(0xFFFFFFFFu - uint32_t(key)); }
+
+// Per-sequence position bounds, validated on the device.
+struct SeqView {
+  int q0;  // absolute position of query row 0
+  int L;   // valid keys
+  bool ok;
+};
+__device__ __forceinline__ SeqView seq_view(const int32_t* q_offset, const int32_t* kv_len, int b, int Nq, int Nk,
+                                            bool decode) {
+  SeqView s;
+  s.L = kv_len ? kv_len[b] : Nk;
+  s.q0 = decode ? s.L - 1 : (q_offset ? q_offset[b] : 0);
+  s.ok = s.L >= 1 && s.L <= Nk && s.q0 >= 0 && s.q0 + Nq <= s.L;
+  return s;
+}
+
+// ---- launchers (host) ------------------------------------------------------
+// Index Branch, CUDA-core table path: block maxima for every visible block.
+cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* ik, const int32_t* q_offset,
+                                        const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs,
+                                        float* table, uint32_t* status, cudaStream_t stream);
+// Exact top-K over a block-max table (warp per row).
+cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
+                                   int Nk, int G, int Bs, int K, int32_t* sel, uint32_t* status, cudaStream_t stream);
+// Main Branch, query-outer CUDA-core path (any dtype; prefill or decode).
+cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, const void* v, const int32_t* sel,
+                                    const int32_t* q_offset, const int32_t* kv_len, bool decode, int B, int Nq,
+                                    int Nk, int Hq, int Hkv, int d, int Bs, int K, float scale, void* out, float* lse,
+                                    uint32_t* status, cudaStream_t stream);
+
+}  // namespace msa

@@ -1,0 +1,144 @@
+/*
+ * msa.h -- C ABI of the MiniMax Sparse Attention (MSA) forward path on GB300.
+ *
+ * MSA is block-sparse attention layered on grouped-query attention (GQA). It
+ * has two branches (hyper.ai summary of paper 2606.13392, section "方法";
+ * quant_prune_distill post 751, section "Метод"):
+ *
+ *   Index Branch  one index query head per GQA group and one index key head
+ *                 for the whole layer; a pre-softmax dot-product score for
+ *                 every causally visible key, max-pooled per key block, then
+ *                 the Top-K blocks by that maximum, the block that holds the
+ *                 query always included            -> msa_index_select
+ *   Main Branch   exact softmax attention restricted to the keys/values of
+ *                 the selected blocks               -> msa_sparse_attn_prefill
+ *                                                     msa_sparse_attn_decode
+ *
+ * Notation: B sequences; Nq query rows per sequence; Nk key rows (capacity)
+ * per sequence; Hq query heads; Hkv key/value heads = G GQA groups (query
+ * head h belongs to group h / (Hq / Hkv)); d head dim; di index head dim;
+ * Bs key block size; K selected blocks per (query row, group), the forced
+ * local block included. Key block t holds keys [t*Bs, (t+1)*Bs). Query row i
+ * of sequence b sits at absolute position pos = q_offset[b] + i and sees keys
+ * j <= pos with j < kv_len[b]; its local block is loc = pos / Bs.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays
+ *    owned by the caller; the library allocates nothing and keeps no pointer
+ *    after the call returns. Work is enqueued on `stream` (0 = legacy default
+ *    stream) and runs asynchronously; nothing is synchronised.
+ *  - `dtype` (msa_dtype_t) is the element type of q, k, v, iq, ik and of the
+ *    attention output: MSA_BF16 (tensor-core path, fp32 accumulation) or
+ *    MSA_FP32 (CUDA-core path).
+ *  - `ws` is caller-owned DEVICE scratch of at least msa_workspace_size(...)
+ *    bytes, 256-byte aligned, zero-filled once before its first use. Its
+ *    first word is a sticky device status that kernels set when they detect a
+ *    bad index or a wait that ran out; msa_read_status() reads and clears it.
+ *    Calls that share one workspace must be ordered on one stream.
+ *  - Argument errors found on the host return before anything is enqueued.
+ *    Per-sequence values (q_offset, kv_len, sel entries) live on the device
+ *    and are checked there: an offending row is skipped (its sel row is -1,
+ *    its output row zero) and the status becomes MSA_ERR_BOUNDS.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1, /* a null pointer, a non-positive size, Hq % Hkv != 0, ... */
+  MSA_ERR_UNSUPPORTED = 2, /* a shape or dtype this build has no kernel for */
+  MSA_ERR_WORKSPACE = 3,   /* ws is NULL, misaligned or smaller than msa_workspace_size() */
+  MSA_ERR_CUDA = 4,        /* a launch or CUDA runtime call failed */
+  MSA_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out (the kernel returned early) */
+  MSA_ERR_BOUNDS = 6       /* device: a q_offset / kv_len / sel value was out of range */
+} msa_status_t;
+
+typedef enum { MSA_BF16 = 0, MSA_FP32 = 1 } msa_dtype_t;
+
+typedef enum { MSA_OP_INDEX_SELECT = 0, MSA_OP_PREFILL = 1, MSA_OP_DECODE = 2 } msa_op_t;
+
+/* Bytes of scratch `ws` the entry point `op` needs for these sizes (the same
+ * argument meanings as the entry points; unused ones may be 0: G and di for
+ * the attention ops, Hq and d for MSA_OP_INDEX_SELECT; for MSA_OP_DECODE, Nq
+ * is ignored and Nk is Lmax). Returns 0 when the arguments are invalid. */
+size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K, int dtype);
+
+/* Index Branch: block selection for every (query row, group).
+ * (hyper.ai summary, "方法": dot-product index scores over visible keys, Block
+ *  Max Pooling, Top-K per group, the query's own block always included;
+ *  quant_prune_distill post 751, "Метод"/"Эксперименты": one index query head
+ *  per group, one index key head per layer, 16 blocks x 128 = 2048 tokens.)
+ *
+ *  iq        [B, Nq, G, di]  index queries, one head per group (dtype)
+ *  ik        [B, Nk, di]     the layer's single index key head (dtype)
+ *  q_offset  [B] int32 or NULL (all 0): absolute position of query row 0
+ *  kv_len    [B] int32 or NULL (all Nk): valid keys per sequence;
+ *            need 0 <= q_offset[b], q_offset[b] + Nq <= kv_len[b] <= Nk
+ *  sel       [B, Nq, G, K] int32, out: selected block ids in ascending order.
+ *            Row (b,i,g) holds loc and the K-1 blocks t < loc with the highest
+ *            block maximum, ties to the lower t; if loc + 1 <= K it holds
+ *            0..loc and is padded with -1.
+ *  block_max [B, Nq, G, ceil(Nk/Bs)] fp32 or NULL, out (diagnostic): the
+ *            block maxima of the visible keys, NaN for blocks t > loc.
+ *  Supported: dtype BF16 or FP32; di in {32, 64}; 1 <= Bs <= 1024; 1 <= K <= 64.
+ *  Selection is exact when the index scores are exact in fp32 (for example
+ *  integer-valued index q/k with |score| < 2^24). */
+msa_status_t msa_index_select(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
+                              int Nq, int Nk, int G, int di, int Bs, int K, int dtype, int32_t* sel, float* block_max,
+                              void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Main Branch, prefill: exact softmax attention of every query row over the
+ * keys of its group's selected blocks, causally masked (j <= pos, j < kv_len).
+ * (hyper.ai summary, "方法": the Main Branch gathers the Key/Value vectors of
+ *  the selected blocks and computes standard scaled dot-product attention.)
+ *
+ *  q    [B, Nq, Hq, d] (dtype); k, v [B, Nk, Hkv, d] (dtype)
+ *  sel  [B, Nq, Hkv, K] int32: block ids per (row, group) as produced by
+ *       msa_index_select (ascending, -1 padded; -1 entries are skipped)
+ *  q_offset, kv_len: as for msa_index_select
+ *  scale  softmax scale; <= 0 selects 1/sqrt(d)
+ *  out  [B, Nq, Hq, d] (dtype), out; lse [B, Nq, Hq] fp32 or NULL, out:
+ *       natural-log sum of exp of the scaled scores over the attended keys
+ *  Supported: d in {64, 128}; BF16 or FP32; Bs and K as for msa_index_select. */
+msa_status_t msa_sparse_attn_prefill(const void* q, const void* k, const void* v, const int32_t* sel,
+                                     const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk, int Hq,
+                                     int Hkv, int d, int Bs, int K, float scale, int dtype, void* out, float* lse,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Main Branch, decode: one new query token per sequence attending to its KV
+ * cache through the selected blocks (the decode half of the pages' prefill /
+ * decode speedups, hyper.ai summary "一句话总结"). Same operation as
+ * msa_sparse_attn_prefill with Nq = 1 and pos = kv_len[b] - 1.
+ *
+ *  q        [B, Hq, d] (dtype)
+ *  k_cache, v_cache [B, Lmax, Hkv, d] (dtype); rows >= kv_len[b] are ignored
+ *  sel      [B, Hkv, K] int32: msa_index_select output for Nq = 1 and
+ *           q_offset[b] = kv_len[b] - 1
+ *  kv_len   [B] int32 (required): 1 <= kv_len[b] <= Lmax
+ *  out [B, Hq, d] (dtype); lse [B, Hq] fp32 or NULL */
+msa_status_t msa_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* sel,
+                                    const int32_t* kv_len, int B, int Lmax, int Hq, int Hkv, int d, int Bs, int K,
+                                    float scale, int dtype, void* out, float* lse, void* ws, size_t ws_bytes,
+                                    cudaStream_t stream);
+
+/* Synchronises `stream`, returns the sticky device status of workspace `ws`
+ * (MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_BOUNDS) and clears it. Returns
+ * MSA_ERR_CUDA if the stream reports an error. */
+msa_status_t msa_read_status(void* ws, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* msa_status_string(msa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -1,0 +1,81 @@
+"""C ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_long_select_gb300 as msa
+from block_sparse_long_select_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(msa_[a-z_]+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.lib_path()):
+        msa.build()
+    return msa.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"msa_index_select", "msa_sparse_attn_prefill", "msa_sparse_attn_decode", "msa_workspace_size",
+            "msa_read_status", "msa_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"binding lacks {n}"
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert msa.msa_status_string(code).startswith(name)
+
+
+def test_workspace_size(lib):
+    ws = msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, 1, 512, 512, 2, 0, 0, 32, 32, 4, msa.MSA_FP32)
+    assert ws >= 256 and ws % 256 == 0
+    assert msa.msa_workspace_size(msa.MSA_OP_PREFILL, 1, 8192, 8192, 8, 32, 128, 0, 128, 16, msa.MSA_BF16) >= 256
+    assert msa.msa_workspace_size(msa.MSA_OP_DECODE, 64, 1, 131072, 8, 32, 128, 0, 128, 16, msa.MSA_BF16) >= 256
+    # invalid: zero batch, Hq not a multiple of Hkv, unknown op
+    assert msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, 0, 512, 512, 2, 0, 0, 32, 32, 4, 1) == 0
+    assert msa.msa_workspace_size(msa.MSA_OP_PREFILL, 1, 64, 64, 3, 8, 64, 0, 32, 4, 1) == 0
+    assert msa.msa_workspace_size(7, 1, 64, 64, 2, 8, 64, 32, 32, 4, 1) == 0
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails host validation
+
+
+def test_host_validation_before_launch(lib):
+    P = lambda: FAKE  # noqa: E731
+    # null index tensors
+    assert lib.msa_index_select(None, P(), None, None, 1, 8, 8, 1, 32, 4, 2, 1, P(), None, P(), 4096, None) == 1
+    # unsupported index head dim
+    assert lib.msa_index_select(P(), P(), None, None, 1, 8, 8, 1, 48, 4, 2, 1, P(), None, P(), 1 << 20, None) == 2
+    # K beyond the built maximum
+    assert lib.msa_index_select(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 65, 1, P(), None, P(), 1 << 20, None) == 2
+    # workspace too small / misaligned
+    assert lib.msa_index_select(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 2, 1, P(), None, P(), 16, None) == 3
+    assert lib.msa_index_select(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 2, 1, P(), None,
+                                ctypes.c_void_p(0x1010), 1 << 20, None) == 3
+    # Hq % Hkv != 0; unsupported head dim; bad dtype
+    args = lambda Hq, Hkv, d, dt: (P(), P(), P(), P(), None, None, 1, 8, 8, Hq, Hkv, d, 4, 2, 0.0, dt, P(),  # noqa
+                                   None, P(), 1 << 20, None)
+    assert lib.msa_sparse_attn_prefill(*args(6, 4, 64, 1)) == 1
+    assert lib.msa_sparse_attn_prefill(*args(8, 2, 96, 1)) == 2
+    assert lib.msa_sparse_attn_prefill(*args(8, 2, 64, 9)) == 1
+    # decode needs kv_len
+    assert lib.msa_sparse_attn_decode(P(), P(), P(), P(), None, 1, 8, 8, 2, 64, 4, 2, 0.0, 1, P(), None, P(),
+                                      1 << 20, None) == 1
+    assert lib.msa_read_status(None, None) == 1
