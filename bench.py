@@ -1,0 +1,529 @@
+#!/usr/bin/env python
+"""MSA forward benchmark on GB300: prefill tokens/s at 128K and decode tokens/s.
+
+One step of the prefill workload is the whole hot path over one 131072-token
+sequence (block 128, top-16): msa_index_select then msa_sparse_attn_prefill.
+One decode step is 64 sequences x 1 new token over KV caches of 32K-128K:
+msa_index_select (Nq = 1) then msa_sparse_attn_decode. Inputs are synthetic
+(seeded, generated on the device) and resident in HBM when timing starts.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {msa,reference}]
+
+Prints ONE JSON line on rank 0. Under torchrun every rank runs the same
+workload on its own GPU (independent replicas; no collective on the data
+path) and `value` is the sum over ranks of tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MSA prefill tokens/s @128K and decode tokens/s (1 GB300) + % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {  # kernel name -> source file (for the ncu traffic freshness check)
+    "index_blockmax_table": "index_table.cu", "topk_from_table": "index_table.cu",
+    "attn_query_outer": "attn_query_outer.cu", "index_fused_tc": "index_fused_tc.cu",
+    "attn_kv_outer_tc": "attn_kv_outer_tc.cu", "attn_invert": "attn_kv_outer_tc.cu",
+    "attn_combine": "attn_kv_outer_tc.cu", "decode_index": "decode.cu", "decode_topk": "decode.cu",
+    "decode_attn": "decode.cu", "decode_combine": "decode.cu",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
+    ap.add_argument("--workload", default="prefill_128k_bs128")
+    ap.add_argument("--decode-workload", default="decode_b64")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = auto)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return reduce_scalar(self.pg, x, "max")
+
+    def sum(self, x: float) -> float:
+        return reduce_scalar(self.pg, x, "sum")
+
+
+def reduce_scalar(pg, x: float, op: str) -> float:
+    """Max / sum of one float over ranks (identity without a process group)."""
+    if pg is None:
+        return float(x)
+    import torch
+
+    dev = "cuda" if (torch.cuda.is_available() and pg.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX if op == "max" else pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def src_sha(kernel: str) -> str | None:
+    f = KERNEL_SOURCES.get(kernel)
+    if not f:
+        return None
+    path = os.path.join(ROOT, "block_sparse_long_select_gb300", "csrc", f)
+    if not os.path.exists(path):
+        return None
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel (profiles/*.md line:
+    `ncu-traffic <kernel> <workload> <bytes_per_launch> <src sha256[:16]>`)."""
+    sha = src_sha(kernel)
+    pdir = os.path.join(ROOT, "profiles")
+    if not sha or not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        for line in open(os.path.join(pdir, fn)):
+            m = re.match(r"\s*ncu-traffic\s+(\S+)\s+(\S+)\s+([0-9.eE+]+)\s+([0-9a-f]+)", line)
+            if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == sha:
+                return float(m.group(3))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (what the method must do, independent of the kernels)
+# ---------------------------------------------------------------------------
+def attended_keys(sel, q_offset, kv_len, Bs):
+    """Sum over (b, i, g) of the number of attended keys (selected blocks
+    intersected with j <= pos, j < kv_len)."""
+    import torch
+
+    B, Nq, G, K = sel.shape
+    dev = sel.device
+    pos = (torch.as_tensor(q_offset, device=dev).view(B, 1, 1, 1) +
+           torch.arange(Nq, device=dev).view(1, Nq, 1, 1))
+    L = torch.as_tensor(kv_len, device=dev).view(B, 1, 1, 1)
+    t = sel.long()
+    lo = t * Bs
+    hi = torch.minimum(torch.minimum(lo + Bs, pos + 1), L)
+    n = torch.clamp(hi - lo, min=0) * (t >= 0)
+    return int(n.sum().item())
+
+
+def prefill_work(w, sel, qo, kl):
+    pos = qo[:, None].astype(np.int64) + np.arange(w.Nq)[None, :]
+    visible = np.minimum(pos + 1, kl[:, None]).sum()
+    att = attended_keys(sel, qo, kl, w.Bs)
+    return {"index_flops": 2.0 * w.di * w.G * float(visible),
+            "attn_flops": 4.0 * w.d * (w.Hq // w.G) * float(att),
+            "attended_keys": att, "visible_keys": int(visible)}
+
+
+def decode_work(w, sel, kl):
+    att = attended_keys(sel, kl - 1, kl, w.Bs)  # summed over (b, g)
+    ik_bytes = float(kl.astype(np.int64).sum()) * w.di * 2
+    kv_bytes = float(att) * w.d * 2 * 2
+    small = w.B * (w.Hq * w.d * 2 * 2 + w.G * w.di * 2 + w.G * w.K * 4)
+    return {"index_bytes": ik_bytes, "attn_bytes": kv_bytes + w.B * w.Hq * w.d * 4, "total_bytes": ik_bytes +
+            kv_bytes + small, "index_flops": 2.0 * w.di * w.G * float(kl.sum()),
+            "attn_flops": 4.0 * w.d * (w.Hq // w.G) * float(att), "attended_keys": att}
+
+
+def roofline_for(kernel, prof, work, peaks, peak_src, workload, n_units, mode="prefill"):
+    """Roofline entry of one kernel: achieved = algorithmic work per launch /
+    mean launch duration (CUDA events on its stream inside the timed region).
+    Prefill kernels are contractions (tensor-bound); decode kernels stream
+    their inputs once (HBM-bound)."""
+    launches, total_ms = prof[kernel]
+    per_launch_s = total_ms / 1e3 / launches
+    if mode == "decode":
+        if "index" in kernel:
+            bound, unit, amount = "hbm", "GB/s", work["index_bytes"] / n_units
+        elif "attn" in kernel:
+            bound, unit, amount = "hbm", "GB/s", work["attn_bytes"] / n_units
+        else:
+            return None
+    elif kernel in ("index_fused_tc", "index_blockmax_table"):
+        bound, unit, amount = "tensor", "TFLOP/s", work["index_flops"] / n_units
+    elif kernel in ("attn_kv_outer_tc", "attn_query_outer"):
+        bound, unit, amount = "tensor", "TFLOP/s", work["attn_flops"] / n_units
+    elif kernel in ("decode_index",):
+        bound, unit, amount = "hbm", "GB/s", work["index_bytes"] / n_units
+    elif kernel in ("decode_attn",):
+        bound, unit, amount = "hbm", "GB/s", work["attn_bytes"] / n_units
+    else:
+        return None
+    if bound == "tensor":
+        achieved = amount / per_launch_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        peak_name = "bf16_tflops_sustained"
+    else:
+        achieved = amount / per_launch_s / 1e9
+        peak = peaks["hbm_gbs"]
+        peak_name = "hbm_gbs"
+    return {"kernel": kernel, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kernel, workload),
+            "algorithmic_per_launch": amount, "launch_ms": round(per_launch_s * 1e3, 4),
+            "peak_source": f"{peak_name} ({peak_src})"}
+
+
+# ---------------------------------------------------------------------------
+# the timed MSA arm
+# ---------------------------------------------------------------------------
+def run_msa(args, dist):
+    import torch
+
+    import block_sparse_long_select_gb300 as msa
+
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    msa.load_library()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+
+    def time_steps(step, K, W, profile=True):
+        for _ in range(W):
+            step()
+        torch.cuda.synchronize(dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        sampler = ClockSampler(dev.index if dev.index is not None else 0)
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler.start()
+        if profile:
+            msa.msa_profile_begin()
+        t0 = time.perf_counter()
+        for s in range(K):
+            flush.zero_()  # evict L2 between timed steps (outside the step events)
+            starts[s].record(stream)
+            step()
+            ends[s].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        prof = msa.msa_profile_end() if profile else {}
+        dist.barrier()
+        clocks = sampler.stop()
+        ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        return ms, prof, clocks, wall
+
+    # ----------------------------- prefill -----------------------------
+    w = synth.WORKLOADS[args.workload]
+    qo_np, kl_np = synth.q_offsets(w), synth.kv_lens(w)
+    t = {n: synth.device_tensor(w, n, dev) for n in ("q", "k", "v", "iq", "ik")}
+    qo = torch.from_numpy(qo_np).to(dev)
+    kl = torch.from_numpy(kl_np).to(dev)
+    sel = torch.empty((w.B, w.Nq, w.G, w.K), dtype=torch.int32, device=dev)
+    out = torch.empty_like(t["q"])
+    ws_i = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, w.B, w.Nq, w.Nk, w.G, 0, 0, w.di, w.Bs,
+                                                w.K, msa.MSA_BF16), dev)
+    ws_a = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_PREFILL, w.B, w.Nq, w.Nk, w.G, w.Hq, w.d, 0, w.Bs, w.K,
+                                                msa.MSA_BF16), dev)
+
+    def prefill_step():
+        msa.msa_index_select(t["iq"], t["ik"], qo, kl, w.Bs, w.K, sel=sel, ws=ws_i)
+        msa.msa_sparse_attn_prefill(t["q"], t["k"], t["v"], sel, qo, kl, w.Bs, w.K, out=out, ws=ws_a)
+
+    ms, prof, clocks, wall = time_steps(prefill_step, args.steps, args.warmup)
+    for ws in (ws_i, ws_a):
+        st = msa.msa_read_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status after prefill: {msa.msa_status_string(st)}")
+    work = prefill_work(w, sel, qo_np, kl_np)
+    step_ms = float(np.mean(ms))
+    tokens = w.B * w.Nq
+    max_total_s = dist.max(sum(ms) / 1e3)
+    all_tokens = dist.sum(tokens * args.steps)
+    value = all_tokens / max_total_s
+    launches = sum(v[0] for v in prof.values())
+    dom = max(prof, key=lambda k: prof[k][1]) if prof else None
+    roof = roofline_for(dom, prof, work, peaks, peak_src, w.name, 1) if dom else None
+    kernels = {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4),
+                   "share": round(v[1] / max(sum(x[1] for x in prof.values()), 1e-9), 4)} for k, v in prof.items()}
+    all_roofs = [r for r in (roofline_for(k, prof, work, peaks, peak_src, w.name, 1) for k in prof) if r]
+
+    # ---------------------------- e2e (host buffers) -------------------
+    e2e = None
+    if not args.no_e2e:
+        host = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in t}
+        for n in t:
+            host[n].copy_(t[n])
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(x.numel() * x.element_size() for x in host.values()) + 2 * qo.numel() * 4
+        d2h = out_h.numel() * out_h.element_size()
+        qo_h, kl_h = qo.cpu().pin_memory(), kl.cpu().pin_memory()
+
+        def e2e_step():
+            for n in t:
+                t[n].copy_(host[n], non_blocking=True)
+            qo.copy_(qo_h, non_blocking=True)
+            kl.copy_(kl_h, non_blocking=True)
+            prefill_step()
+            out_h.copy_(out, non_blocking=True)
+
+        ems, _, _, _ = time_steps(e2e_step, max(3, args.steps // 4), 1, profile=False)
+        e_tot = dist.max(sum(ems) / 1e3)
+        e2e = {"value": round(dist.sum(tokens * len(ems)) / e_tot, 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(float(np.mean(ems)), 4)}
+        del host, out_h
+
+    del t, out, sel, ws_i, ws_a
+    torch.cuda.empty_cache()
+
+    # ------------------------------ decode -----------------------------
+    decode = None
+    if not args.no_decode:
+        wd = synth.WORKLOADS[args.decode_workload]
+        kld_np = synth.kv_lens(wd)
+        td = {n: synth.device_tensor(wd, n, dev) for n in ("q", "k", "v", "iq", "ik")}
+        qd = td["q"][:, 0]
+        kld = torch.from_numpy(kld_np).to(dev)
+        qod = kld - 1
+        seld = torch.empty((wd.B, 1, wd.G, wd.K), dtype=torch.int32, device=dev)
+        outd = torch.empty_like(qd)
+        wsd_i = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, wd.B, 1, wd.Nk, wd.G, 0, 0, wd.di,
+                                                     wd.Bs, wd.K, msa.MSA_BF16), dev)
+        wsd_a = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_DECODE, wd.B, 1, wd.Nk, wd.G, wd.Hq, wd.d, 0, wd.Bs,
+                                                     wd.K, msa.MSA_BF16), dev)
+
+        def decode_step():
+            msa.msa_index_select(td["iq"], td["ik"], qod, kld, wd.Bs, wd.K, sel=seld, ws=wsd_i)
+            msa.msa_sparse_attn_decode(qd, td["k"], td["v"], seld, kld, wd.Bs, wd.K, out=outd, ws=wsd_a)
+
+        dsteps = max(args.steps, 50)
+        dms, dprof, dclocks, _ = time_steps(decode_step, dsteps, max(args.warmup, 5))
+        for ws in (wsd_i, wsd_a):
+            st = msa.msa_read_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status after decode: {msa.msa_status_string(st)}")
+        dwork = decode_work(wd, seld, kld_np)
+        d_tot = dist.max(sum(dms) / 1e3)
+        dval = dist.sum(wd.B * dsteps) / d_tot
+        dstep_s = float(np.mean(dms)) / 1e3
+        step_gbs = dwork["total_bytes"] / dstep_s / 1e9
+        ddom = max(dprof, key=lambda k: dprof[k][1]) if dprof else None
+        decode = {
+            "value": round(dval, 1), "unit": "tokens/s", "ms_per_step": round(float(np.mean(dms)), 4),
+            "steps": dsteps, "config": {"workload": wd.name, "batch": wd.B, "kv_len_range": list(wd.kv_len_range),
+                                        "Bs": wd.Bs, "K": wd.K, "l2": "flushed between steps"},
+            "step_roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": peaks["hbm_gbs"],
+                              "unit": "GB/s", "frac": round(step_gbs / peaks["hbm_gbs"], 4),
+                              "algorithmic_bytes_per_step": dwork["total_bytes"]},
+            "roofline": roofline_for(ddom, dprof, dwork, peaks, peak_src, wd.name, 1, "decode") if ddom else None,
+            "kernels": {k: {"launches": v[0], "ms_per_step": round(v[1] / dsteps, 4)} for k, v in dprof.items()},
+            "gpu_launches": sum(v[0] for v in dprof.values()), "clocks": dclocks,
+        }
+        del td, seld, outd, wsd_i, wsd_a
+        torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, device-generated)",
+        "config": {"workload": w.name, "batch": w.B, "seq_len": w.Nq, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "di": w.di, "Bs": w.Bs, "K": w.K, "hot_blocks": w.hot, "parallelism": f"replicas x{dist.world}",
+                   "l2": "flushed between timed steps (512 MB write)"},
+        "roofline": roof, "roofline_all": all_roofs, "kernels": kernels, "gpu_launches": launches,
+        "clocks": clocks, "e2e": e2e, "decode": decode,
+        "work": {"index_flops": work["index_flops"], "attn_flops": work["attn_flops"],
+                 "attended_keys": work["attended_keys"]},
+        "wall_s_timed_region": round(wall, 3),
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_prefill_rows(w, rows, ik_host):
+    """Oracle index select + attention for the listed rows of sequence 0.
+    Returns seconds spent inside the oracle (input generation excluded)."""
+    import oracle
+
+    rows = np.asarray(rows, np.int32)
+    rb = np.zeros(len(rows), np.int32)
+    iq = synth.host_rows(w, "iq", 0, rows)
+    q = synth.host_rows(w, "q", 0, rows)
+    qo, kl = synth.q_offsets(w), synth.kv_lens(w)
+    t0 = time.perf_counter()
+    sel = oracle.index_select(iq, ik_host, rb, rows, qo, kl, w.Bs, w.K)
+    t1 = time.perf_counter()
+    k = np.zeros((1, w.Nk, w.Hkv, w.d), np.float32)
+    v = np.zeros((1, w.Nk, w.Hkv, w.d), np.float32)
+    row = w.Hkv * w.d
+    for tb in sorted(set(int(x) for x in sel.reshape(-1) if x >= 0)):
+        j0, j1 = tb * w.Bs, min((tb + 1) * w.Bs, w.Nk)
+        k[0, j0:j1] = synth.host_range(w, "k", j0 * row, (j1 - j0) * row).reshape(j1 - j0, w.Hkv, w.d)
+        v[0, j0:j1] = synth.host_range(w, "v", j0 * row, (j1 - j0) * row).reshape(j1 - j0, w.Hkv, w.d)
+    t2 = time.perf_counter()
+    oracle.sparse_attn(q, k, v, sel, rb, rows, qo, kl, w.Bs, w.K)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2)
+
+
+def sample_rows(w, n, offset=0):
+    """n query rows evenly spaced over the sequence (their mean cost equals the
+    mean cost per token, which grows with position)."""
+    step = w.Nq / n
+    return np.array([int((k + 0.5) * step) + offset for k in range(n)], np.int32) % w.Nq
+
+
+def cpu_baseline(w, rows_n):
+    import oracle
+
+    ik = synth.host_tensor(w, "ik")
+    rows = sample_rows(w, rows_n)
+    secs = oracle_prefill_rows(w, rows, ik)
+    return {"value": round(len(rows) / secs, 2), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{len(rows)} query rows evenly spaced over the {w.Nq}-token sequence, all {w.G} groups / "
+                      f"{w.Hq} heads; index select + attention in fp64; tokens/s = rows / oracle seconds",
+            "seconds": round(secs, 2)}
+
+
+def run_reference(args, dist):
+    """The oracle as the reference arm: each step is a bounded sample of rows."""
+    import oracle
+
+    w = synth.WORKLOADS[args.workload]
+    ik = synth.host_tensor(w, "ik")
+    rows_per_step = 8
+    for s in range(args.warmup):
+        oracle_prefill_rows(w, sample_rows(w, rows_per_step, offset=s), ik)
+    secs = 0.0
+    for s in range(args.steps):
+        secs += oracle_prefill_rows(w, sample_rows(w, rows_per_step, offset=1000 + s), ik)
+    value = rows_per_step * args.steps / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "batch": w.B, "seq_len": w.Nq, "Bs": w.Bs, "K": w.K},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{rows_per_step} evenly spaced query rows per step (all groups/heads)"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    dist = Dist()
+    if args.impl == "reference":
+        if dist.rank == 0:
+            print(json.dumps(run_reference(args, dist)), flush=True)
+        return
+    line = run_msa(args, dist)
+    if dist.rank == 0:
+        if not args.no_cpu_baseline:
+            rows = args.cpu_rows or 4096
+            line["cpu_baseline"] = cpu_baseline(synth.WORKLOADS[args.workload], rows)
+        print(json.dumps(line), flush=True)
+    if dist.pg:
+        dist.pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

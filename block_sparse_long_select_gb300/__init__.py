@@ -21,6 +21,8 @@ from ._lib import (  # noqa: F401
     lib_path,
     load_library,
     msa_index_select,
+    msa_profile_begin,
+    msa_profile_end,
     msa_read_status,
     msa_sparse_attn_decode,
     msa_sparse_attn_prefill,

@@ -19,7 +19,13 @@ SIGNATURES = {
     "msa_sparse_attn_decode": (_i32, [_vp] * 5 + [_i32] * 7 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_read_status": (_i32, [_vp, _vp]),
     "msa_status_string": (ctypes.c_char_p, [_i32]),
+    "msa_profile_begin": (_i32, []),
+    "msa_profile_end": (_i32, [_vp, _i32]),
 }
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
 
 
 class MsaError(RuntimeError):
@@ -157,3 +163,16 @@ def msa_read_status(ws, stream=None) -> int:
 
 def msa_status_string(code: int) -> str:
     return load_library().msa_status_string(int(code)).decode()
+
+
+def msa_profile_begin() -> None:
+    load_library().msa_profile_begin()
+
+
+def msa_profile_end() -> dict:
+    """{kernel name: (launches, total device ms)} recorded since msa_profile_begin()."""
+    buf = (KernelTime * 64)()
+    n = load_library().msa_profile_end(ctypes.cast(buf, ctypes.c_void_p), 64)
+    if n < 0:
+        raise RuntimeError("msa_profile_end: event query failed")
+    return {buf[k].name.decode(): (buf[k].launches, buf[k].total_ms) for k in range(min(n, 64))}

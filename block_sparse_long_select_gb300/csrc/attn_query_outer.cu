@@ -132,6 +132,7 @@ cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, con
   const int64_t grid = int64_t(B) * Nq * Hkv;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  ProfScope prof("attn_query_outer", stream);
 #define MSA_QO(T, D)                                                                                         \
   attn_query_outer_kernel<T, D><<<unsigned(grid), kQoWarps * 32, 0, stream>>>(                             \
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), sel, q_offset, kv_len, \

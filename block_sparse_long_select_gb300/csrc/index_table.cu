@@ -234,6 +234,7 @@ cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* i
   const int64_t rows = int64_t(Nq) * G;
   dim3 grid(unsigned((rows + kTabRows - 1) / kTabRows), unsigned((nblk + kTabWarps - 1) / kTabWarps), unsigned(B));
   dim3 block(kTabWarps * 32);
+  ProfScope prof("index_blockmax_table", stream);
 #define MSA_TAB(T, DI)                                                                                            \
   index_blockmax_table_kernel<T, DI><<<grid, block, 0, stream>>>(static_cast<const T*>(iq), static_cast<const T*>(ik), \
                                                                  q_offset, kv_len, Nq, Nk, G, Bs, nblk, table, status)
@@ -263,6 +264,7 @@ cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, 
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = unsigned((rows + kTopkWarps - 1) / kTopkWarps);
+  ProfScope prof("topk_from_table", stream);
   topk_from_table_kernel<<<grid, kTopkWarps * 32, smem, stream>>>(table, q_offset, kv_len, B, Nq, Nk, G, Bs, K, nblk,
                                                                   sel, status);
   return cudaGetLastError();

@@ -65,6 +65,21 @@ __device__ __forceinline__ SeqView seq_view(const int32_t* q_offset, const int32
   return s;
 }
 
+// RAII bracket of one kernel launch with a CUDA event pair while profiling is
+// on (msa_profile_begin / msa_profile_end); a no-op otherwise.
+class ProfScope {
+ public:
+  ProfScope(const char* name, cudaStream_t stream);
+  ~ProfScope();
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+
+ private:
+  const char* name_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
 // ---- launchers (host) ------------------------------------------------------
 // Index Branch, CUDA-core table path: block maxima for every visible block.
 cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* ik, const int32_t* q_offset,
