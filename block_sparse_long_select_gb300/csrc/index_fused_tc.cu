@@ -1,0 +1,420 @@
+// Index Branch, fused tensor-core kernel (bf16, sm_103a):
+//   index scores  S = iq . ik^T on tcgen05 (TMA-fed shared-memory operands,
+//                 fp32 accumulators in TMEM),
+//   block max     pooled straight out of TMEM in the epilogue,
+//   top-K         a running exact top-(K-1) per row over the candidate blocks
+//                 t < loc, then the local block appended,
+// so neither the token-score matrix nor the block-max table ever reaches HBM.
+// (hyper.ai summary of paper 2606.13392, section "方法": per GQA group, dot-
+//  product scores of the index query against every visible key, Block Max
+//  Pooling, Top-K blocks, the block holding the query always included;
+//  quant_prune_distill post 751, "Метод": one index query head per group, one
+//  index key head for the layer.)
+//
+// Layout: the G index-query heads of a token are stacked along M, so one GEMM
+// of (Nq*G) x Nk per sequence serves every group (the index key is shared by
+// all groups). A work unit is 256 stacked rows (two 128-row MMA tiles that
+// share each key tile, which halves the key traffic per flop); it sweeps key
+// tiles of 128 keys over the blocks before its local block. Units are handed
+// out in a static serpentine order, longest first, over a persistent grid of
+// one CTA per SM.
+//
+// Warp roles (320 threads): warps 0-7 epilogue (warpgroup m reads TMEM lanes
+// of MMA tile m), warp 8 TMA producer, warp 9 TMEM owner + MMA issuer.
+// Pipelines: key tiles in an S-stage shared-memory ring; index-query tiles in
+// nA buffers; two TMEM accumulator sets of 2 x 128 columns (512 columns).
+// Every wait is bounded; on expiry the kernel records MSA_ERR_TIMEOUT, stops
+// issuing work, drains its copies and MMAs, frees TMEM and returns.
+#include <cmath>
+
+#include "msa_internal.cuh"
+#include "tc_utils.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kUnitRows = 256;  // stacked (token, group) rows per work unit
+constexpr int kTileN = 128;     // keys per key tile
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+
+struct Unit {
+  int b, row0, nrows, q0, nt;
+  bool ok;
+};
+
+__device__ __forceinline__ Unit get_unit(int u, int nunits, int nrb, int NqG, int G, int Nq, int Nk, int Bs, int K,
+                                         const int32_t* q_offset, const int32_t* kv_len) {
+  Unit U;
+  const int gu = nunits - 1 - u;  // longest units (latest rows) first
+  U.b = gu / nrb;
+  const int rb = gu % nrb;
+  U.row0 = rb * kUnitRows;
+  U.nrows = min(kUnitRows, NqG - U.row0);
+  const SeqView sv = seq_view(q_offset, kv_len, U.b, Nq, Nk, false);
+  U.ok = sv.ok;
+  U.q0 = sv.q0;
+  const int maxloc = sv.ok ? (sv.q0 + (U.row0 + U.nrows - 1) / G) / Bs : 0;
+  // key tiles are needed only if some row has more visible blocks than K
+  U.nt = (sv.ok && K > 1 && maxloc + 1 > K) ? (maxloc * Bs + kTileN - 1) / kTileN : 0;
+  return U;
+}
+
+// serpentine static schedule over the persistent grid
+__device__ __forceinline__ int unit_at(int round, int cta, int ncta) {
+  return round * ncta + ((round & 1) ? (ncta - 1 - cta) : cta);
+}
+
+template <int BS>
+__device__ __forceinline__ float block_max(const uint32_t* v) {
+  // four independent chains of 3-input max for instruction-level parallelism
+  static_assert(BS % 8 == 0, "block size must be a multiple of 8");
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < BS; c += 8) {
+    m0 = tc::fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+    m1 = tc::fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    m2 = tc::fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+    m3 = tc::fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+template <int DI, int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+    index_fused_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len, int B, int Nq,
+                          int Nk, int G, int K, int nA, int S, int32_t* __restrict__ sel, uint32_t* status) {
+  constexpr uint32_t kABytes = kUnitRows * DI * 2;   // one unit of index queries
+  constexpr uint32_t kATile = 128 * DI * 2;          // one 128-row MMA tile
+  constexpr uint32_t kBBytes = kTileN * DI * 2;      // one key tile
+  constexpr uint32_t kSbo = DI == 64 ? 1024 : 512;   // 8-row swizzle atom
+  constexpr uint32_t kSwz = DI == 64 ? 2 : 4;        // 128B / 64B swizzle
+  constexpr int kKSteps = DI / 16;
+  constexpr int kBlocksPerTile = kTileN / BS;
+  constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kTileN);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = tc::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* a_buf = smem;                                       // nA x kABytes
+  uint8_t* b_buf = a_buf + size_t(nA) * kABytes;               // S x kBBytes
+  const int Kc = K - 1;
+  uint64_t* lists = reinterpret_cast<uint64_t*>(b_buf + size_t(S) * kBBytes);  // [Kc][256]
+  uint64_t* bars = lists + size_t(Kc > 0 ? Kc : 1) * kUnitRows;
+  uint64_t* full = bars;
+  uint64_t* empty = full + S;
+  uint64_t* a_full = empty + S;
+  uint64_t* a_empty = a_full + nA;
+  uint64_t* acc_full = a_empty + nA;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NqG = Nq * G;
+  const int nrb = (NqG + kUnitRows - 1) / kUnitRows;
+  const int nunits = B * nrb;
+  const int ncta = gridDim.x, cta = blockIdx.x;
+  const int rounds = (nunits + ncta - 1) / ncta;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int x = 0; x < nA; ++x) {
+      tc::mbar_init(&a_full[x], 1);
+      tc::mbar_init(&a_empty[x], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&acc_full[a], 1);
+      tc::mbar_init(&acc_empty[a], kEpiWarps);
+    }
+    tc::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tc::tma_prefetch(&tmA);
+    tc::tma_prefetch(&tmB);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&](void) {
+    *abort_flag = 1;
+    set_status(status, MSA_ERR_TIMEOUT);
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      int kB = 0, jA = 0;
+      bool alive = true;
+      for (int r = 0; r < rounds && alive; ++r) {
+        const int u = unit_at(r, cta, ncta);
+        if (u >= nunits) continue;
+        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, q_offset, kv_len);
+        if (U.nt == 0) continue;
+        const int x = jA % nA;
+        if (!tc::mbar_wait(&a_empty[x], ((jA / nA) & 1) ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&a_full[x], kABytes);
+        tc::tma_load_3d(a_buf + size_t(x) * kABytes, &tmA, &a_full[x], 0, U.row0, U.b);
+        ++jA;
+        for (int n = 0; n < U.nt; ++n, ++kB) {
+          const int s = kB % S;
+          if (!tc::mbar_wait(&empty[s], ((kB / S) & 1) ^ 1, abort_flag)) {
+            fail();
+            alive = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&full[s], kBBytes);
+          tc::tma_load_3d(b_buf + size_t(s) * kBBytes, &tmB, &full[s], 0, n * kTileN, U.b);
+        }
+      }
+      // drain: every issued copy must land before the CTA exits
+      int zero = 0;
+      for (int s = 0; s < S && s < kB; ++s) {
+        const int last = kB - 1 - ((kB - 1 - s) % S);  // last tile index that used stage s
+        tc::mbar_wait(&full[s], (last / S) & 1, &zero);
+      }
+      for (int x = 0; x < nA && x < jA; ++x) {
+        const int last = jA - 1 - ((jA - 1 - x) % nA);
+        tc::mbar_wait(&a_full[x], (last / nA) & 1, &zero);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      int kB = 0, jA = 0, kAcc = 0;
+      bool alive = true;
+      for (int r = 0; r < rounds && alive; ++r) {
+        const int u = unit_at(r, cta, ncta);
+        if (u >= nunits) continue;
+        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, q_offset, kv_len);
+        if (U.nt == 0) continue;
+        const int x = jA % nA;
+        if (!tc::mbar_wait(&a_full[x], (jA / nA) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        ++jA;
+        const uint32_t a_addr = tc::smem_u32(a_buf + size_t(x) * kABytes);
+        for (int n = 0; n < U.nt; ++n, ++kB, ++kAcc) {
+          const int s = kB % S, a = kAcc & 1;
+          if (!tc::mbar_wait(&full[s], (kB / S) & 1, abort_flag) ||
+              !tc::mbar_wait(&acc_empty[a], ((kAcc >> 1) & 1) ^ 1, abort_flag)) {
+            fail();
+            alive = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t b_addr = tc::smem_u32(b_buf + size_t(s) * kBBytes);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const uint32_t d = tmem + uint32_t((a * 2 + m) * kTileN);
+#pragma unroll
+            for (int kk = 0; kk < kKSteps; ++kk) {
+              const uint64_t ad = tc::smem_desc(a_addr + m * kATile + kk * 32, 16, kSbo, kSwz);
+              const uint64_t bd = tc::smem_desc(b_addr + kk * 32, 16, kSbo, kSwz);
+              tc::mma_f16_ss(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            }
+          }
+          tc::mma_commit(&empty[s]);
+          tc::mma_commit(&acc_full[a]);
+          if (n == U.nt - 1) tc::mma_commit(&a_empty[x]);
+        }
+      }
+      // all issued MMAs complete before TMEM is released
+      int zero = 0;
+      tc::mma_commit(done_bar);
+      tc::mbar_wait(done_bar, 0, &zero);
+    }
+  } else {
+    // -------------------------------- epilogue --------------------------------
+    const int m = warp >> 2, quarter = warp & 3;
+    const int urow = m * 128 + quarter * 32 + lane;  // row within the unit = TMEM lane of tile m
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    int kAcc = 0;
+    bool alive = true;
+    uint64_t* my_list = lists + urow;  // entry k at my_list[k * 256]
+    for (int r = 0; r < rounds && alive; ++r) {
+      const int u = unit_at(r, cta, ncta);
+      if (u >= nunits) continue;
+      const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, q_offset, kv_len);
+      const bool active = urow < U.nrows;
+      const int row = U.row0 + urow;
+      const int pos = U.q0 + row / G;
+      const int loc = pos / BS;
+      const bool dense = loc + 1 <= K;
+      const bool cand_row = active && U.ok && !dense;
+      int cnt = 0;
+      uint64_t thr = 0;
+      for (int n = 0; n < U.nt; ++n, ++kAcc) {
+        const int a = kAcc & 1;
+        if (!tc::mbar_wait(&acc_full[a], (kAcc >> 1) & 1, abort_flag)) {
+          fail();
+          alive = false;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t v[kTileN];
+        const uint32_t taddr = tmem + lane_base + uint32_t((a * 2 + m) * kTileN);
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c) tc::tmem_ld_32x32b_x32(taddr + c * 32, v + c * 32);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
+        if (cand_row) {
+#pragma unroll
+          for (int bi = 0; bi < kBlocksPerTile; ++bi) {
+            const int t = n * kBlocksPerTile + bi;
+            const float mx = block_max<BS>(v + bi * BS);
+            if (t < loc) {
+              const uint64_t key = rank_key(mx, t);
+              if (cnt < Kc || key > thr) {
+                int p = cnt < Kc ? cnt++ : Kc - 1;
+                while (p > 0 && my_list[(p - 1) * kUnitRows] < key) {
+                  my_list[p * kUnitRows] = my_list[(p - 1) * kUnitRows];
+                  --p;
+                }
+                my_list[p * kUnitRows] = key;
+                if (cnt == Kc) thr = my_list[(Kc - 1) * kUnitRows];
+              }
+            }
+          }
+        }
+      }
+      if (!alive || !active) continue;
+      int32_t* out = sel + (int64_t(U.b) * NqG + row) * K;
+      if (!U.ok) {
+        for (int k = 0; k < K; ++k) out[k] = -1;
+        if (urow == 0) set_status(status, MSA_ERR_BOUNDS);
+      } else if (dense) {
+        for (int k = 0; k < K; ++k) out[k] = k <= loc ? k : -1;
+      } else {
+        // candidates -> block ids, ascending (insertion sort in this row's slots)
+        for (int k = 0; k < cnt; ++k) my_list[k * kUnitRows] = uint64_t(rank_key_block(my_list[k * kUnitRows]));
+        for (int k = 1; k < cnt; ++k) {
+          const uint64_t x = my_list[k * kUnitRows];
+          int p = k;
+          while (p > 0 && my_list[(p - 1) * kUnitRows] > x) {
+            my_list[p * kUnitRows] = my_list[(p - 1) * kUnitRows];
+            --p;
+          }
+          my_list[p * kUnitRows] = x;
+        }
+        for (int k = 0; k < K; ++k) out[k] = k < cnt ? int32_t(my_list[k * kUnitRows]) : (k == cnt ? loc : -1);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+int g_num_sms[64] = {0};
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return kNumSMs;
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMs;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+}  // namespace
+
+bool index_fused_supported(int dtype, int Nq, int G, int di, int Bs, int K) {
+  if (dtype != MSA_BF16 || (di != 32 && di != 64)) return false;
+  if (Bs != 32 && Bs != 64 && Bs != 128) return false;
+  if (K < 1 || K > kMaxK) return false;
+  if (int64_t(Nq) * G < 4 * kUnitRows || int64_t(Nq) * G > (int64_t(1) << 30)) return false;
+  return true;
+}
+
+cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len,
+                                  int B, int Nq, int Nk, int G, int di, int Bs, int K, int32_t* sel,
+                                  uint32_t* status, cudaStream_t stream) {
+  const int NqG = Nq * G;
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[3] = {uint64_t(di), uint64_t(NqG), uint64_t(B)};
+    const uint64_t strides[2] = {uint64_t(di) * 2, uint64_t(NqG) * di * 2};
+    const uint32_t box[3] = {uint32_t(di), uint32_t(kUnitRows), 1};
+    if (!make_tmap_bf16(&tmA, iq, 3, dims, strides, box,
+                        di == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {uint64_t(di), uint64_t(Nk), uint64_t(B)};
+    const uint64_t strides[2] = {uint64_t(di) * 2, uint64_t(Nk) * di * 2};
+    const uint32_t box[3] = {uint32_t(di), uint32_t(kTileN), 1};
+    if (!make_tmap_bf16(&tmB, ik, 3, dims, strides, box,
+                        di == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  }
+  const size_t a_bytes = size_t(kUnitRows) * di * 2, b_bytes = size_t(kTileN) * di * 2;
+  const int Kc = K - 1 > 0 ? K - 1 : 1;
+  const size_t lists = size_t(Kc) * kUnitRows * 8;
+  const size_t fixed = 1024 /*alignment slack*/ + lists + 256 /*barriers, flags*/;
+  const size_t budget = 227 * 1024;
+  int nA = 2, S = 8;
+  while (S > 2 && fixed + nA * a_bytes + S * b_bytes > budget) --S;
+  if (fixed + nA * a_bytes + S * b_bytes > budget) nA = 1;
+  while (S > 2 && fixed + nA * a_bytes + S * b_bytes > budget) --S;
+  const size_t smem = fixed + nA * a_bytes + S * b_bytes;
+  if (smem > budget) return cudaErrorInvalidValue;
+  // barriers must fit in the 256 reserved bytes
+  if ((2 * S + 2 * nA + 5) * 8 + 8 > 256) return cudaErrorInvalidValue;
+
+  const int nunits = B * ((NqG + kUnitRows - 1) / kUnitRows);
+  const int grid = nunits < num_sms() ? nunits : num_sms();
+  ProfScope prof("index_fused_tc", stream);
+#define MSA_FUSED(DI_, BS_)                                                                                     \
+  do {                                                                                                          \
+    auto kern = index_fused_tc_kernel<DI_, BS_>;                                                               \
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));      \
+    if (e != cudaSuccess) return e;                                                                            \
+    kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, q_offset, kv_len, B, Nq, Nk, G, K, nA, S, sel, status); \
+  } while (0)
+  if (di == 64) {
+    if (Bs == 128)
+      MSA_FUSED(64, 128);
+    else if (Bs == 64)
+      MSA_FUSED(64, 64);
+    else
+      MSA_FUSED(64, 32);
+  } else {
+    if (Bs == 128)
+      MSA_FUSED(32, 128);
+    else if (Bs == 64)
+      MSA_FUSED(32, 64);
+    else
+      MSA_FUSED(32, 32);
+  }
+#undef MSA_FUSED
+  return cudaGetLastError();
+}
+
+}  // namespace msa

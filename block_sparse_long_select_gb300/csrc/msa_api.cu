@@ -14,6 +14,7 @@ bool dtype_ok(int dtype) { return dtype == MSA_BF16 || dtype == MSA_FP32; }
 // ---- Index Branch planning ---------------------------------------------------
 struct IndexPlan {
   bool ok = false;
+  bool fused = false;  // tcgen05 kernel (no table) when no block_max is requested
   msa_status_t err = MSA_ERR_INVALID_ARG;
   size_t table_off = 0, table_bytes = 0;  // table region inside ws (0 if none)
   size_t ws_bytes = 0;
@@ -33,9 +34,11 @@ IndexPlan plan_index(int B, int Nq, int Nk, int G, int di, int Bs, int K, int dt
   }
   const int nblk = (Nk + Bs - 1) / Bs;
   const size_t table = size_t(B) * Nq * G * nblk * sizeof(float);
+  p.fused = index_fused_supported(dtype, Nq, G, di, Bs, K);
   p.table_off = kWsHeader;
-  p.table_bytes = have_block_max ? 0 : align256(table);
-  p.ws_bytes = kWsHeader + align256(table);  // size for the case without block_max
+  p.table_bytes = (have_block_max || p.fused) ? 0 : align256(table);
+  // size for the call without block_max
+  p.ws_bytes = kWsHeader + (p.fused ? 0 : align256(table));
   p.ok = true;
   p.err = MSA_OK;
   return p;
@@ -106,6 +109,10 @@ extern "C" msa_status_t msa_index_select(const void* iq, const void* ik, const i
   msa_status_t w = check_ws(ws, ws_bytes, block_max ? kWsHeader : p.ws_bytes);
   if (w != MSA_OK) return w;
   uint32_t* status = status_word(ws);
+  if (p.fused && !block_max) {
+    return cuda_status(launch_index_fused_tc(iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, K, sel, status,
+                                             stream));
+  }
   float* table = block_max ? block_max : reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);
   cudaError_t e = launch_index_blockmax_table(dtype, iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, table, status,
                                               stream);

@@ -85,6 +85,12 @@ class ProfScope {
 cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* ik, const int32_t* q_offset,
                                         const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs,
                                         float* table, uint32_t* status, cudaStream_t stream);
+// Index Branch, fused tcgen05 path (bf16): scores + block max + top-K in one
+// persistent kernel; no table.
+bool index_fused_supported(int dtype, int Nq, int G, int di, int Bs, int K);
+cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len,
+                                  int B, int Nq, int Nk, int G, int di, int Bs, int K, int32_t* sel,
+                                  uint32_t* status, cudaStream_t stream);
 // Exact top-K over a block-max table (warp per row).
 cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
                                    int Nk, int G, int Bs, int K, int32_t* sel, uint32_t* status, cudaStream_t stream);
