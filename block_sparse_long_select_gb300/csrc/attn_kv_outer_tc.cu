@@ -1,0 +1,795 @@
+// Main Branch, prefill, KV-outer on tcgen05 (bf16, sm_103a).
+// (hyper.ai summary of paper 2606.13392, "方法": exact softmax attention over
+//  the selected blocks with K/V gathered per block; "核心贡献": KV-outer sparse
+//  attention that raises tensor-core use at block granularity and handles
+//  skewed block popularity without atomic updates; quant_prune_distill post
+//  751, "Метод": a persistent grid for uneven, dynamic load.)
+//
+// Per query chunk (queries of one sequence, chunked to bound the scratch):
+//  1. attn_count    per (group, key block) number of (query, slot) entries that
+//                   selected it (shared-memory histograms, one global add per
+//                   non-empty bin and CTA)
+//  2. attn_scan     exclusive scans: entry offsets and 128-row tile offsets
+//  3. attn_tiles    the tile list: (bin, first entry, entry count)
+//  4. attn_fill     the inverted lists: bin -> (query, slot) entries
+//  5. attn_kv_outer persistent kernel. Each CTA takes a contiguous run of
+//                   tiles (ordered by bin, so K/V of a block is loaded once
+//                   per run of its tiles). Per tile: gather the 128 query rows
+//                   (128/hpg queries x hpg heads of the group), S = Q K^T on
+//                   tcgen05 into TMEM, exact softmax in registers (causal mask
+//                   only in the local block), P (bf16) to shared memory,
+//                   O = P V on tcgen05 into TMEM, then the per-slot partial
+//                   (O / l in bf16, lse in fp32) is written for the combine.
+//  6. attn_combine  per (query, head): log-sum-exp merge of the K slot
+//                   partials in slot order -> output row. Deterministic; no
+//                   atomics on any output.
+//
+// attn_kv_outer warp roles (448 threads): warp 0 K/V TMA producer, warps 1-4
+// query-row gather (cp.async, swizzled), warp 5 TMEM owner + MMA issuer,
+// warps 6-13 two epilogue warpgroups that alternate tiles (ping-pong), each
+// owning S (Bs columns) and O (D columns) in TMEM. All waits are bounded.
+#include <cmath>
+#include <cstdlib>
+
+#include "msa_internal.cuh"
+#include "tc_utils.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kRows = 128;  // query rows per tile (M of both MMAs)
+constexpr int kAttnThreads = 448;
+constexpr int kKvWarp = 0;
+constexpr int kGatherWarp0 = 1;  // warps 1..4
+constexpr int kMmaWarpA = 5;
+constexpr int kEpiWarp0 = 6;  // warps 6..13
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// inversion
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool entry_valid(int t, int pos, int Bs, int nblk) {
+  return t >= 0 && t < nblk && t * Bs <= pos;
+}
+
+// grid (row chunks, G); dynamic smem = nblk ints
+__global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
+                                  const int32_t* __restrict__ kv_len, int b, int Nq, int Nk, int G, int K, int Bs,
+                                  int nblk, int c0, int cq, int rows_per_cta, int* __restrict__ cnt,
+                                  uint32_t* status) {
+  extern __shared__ int hist[];
+  const int g = blockIdx.y;
+  for (int t = threadIdx.x; t < nblk; t += blockDim.x) hist[t] = 0;
+  __syncthreads();
+  const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
+  const int r0 = blockIdx.x * rows_per_cta;
+  const int r1 = min(cq, r0 + rows_per_cta);
+  if (sv.ok) {
+    for (int e = threadIdx.x; e < (r1 - r0) * K; e += blockDim.x) {
+      const int il = r0 + e / K, k = e % K;
+      const int i = c0 + il;
+      const int t = sel[((int64_t(b) * Nq + i) * G + g) * K + k];
+      if (t < -1 || t >= nblk) set_status(status, MSA_ERR_BOUNDS);
+      if (entry_valid(t, sv.q0 + i, Bs, nblk)) atomicAdd(&hist[t], 1);
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < nblk; t += blockDim.x)
+    if (hist[t]) atomicAdd(&cnt[g * nblk + t], hist[t]);
+}
+
+// single CTA of 1024 threads: entry offsets, tile offsets, tile total
+__global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__ cnt, int nbins, int per_tile,
+                                                         int* __restrict__ entry_off, int* __restrict__ tile_off,
+                                                         int* __restrict__ total_tiles) {
+  __shared__ int s_e[1024], s_t[1024];
+  const int tid = threadIdx.x;
+  const int per = (nbins + 1023) / 1024;
+  const int lo = min(nbins, tid * per), hi = min(nbins, lo + per);
+  int se = 0, st = 0;
+  for (int x = lo; x < hi; ++x) {
+    se += cnt[x];
+    st += (cnt[x] + per_tile - 1) / per_tile;
+  }
+  s_e[tid] = se;
+  s_t[tid] = st;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+    const int ve = tid >= off ? s_e[tid - off] : 0;
+    const int vt = tid >= off ? s_t[tid - off] : 0;
+    __syncthreads();
+    s_e[tid] += ve;
+    s_t[tid] += vt;
+    __syncthreads();
+  }
+  int be = s_e[tid] - se, bt = s_t[tid] - st;
+  for (int x = lo; x < hi; ++x) {
+    entry_off[x] = be;
+    tile_off[x] = bt;
+    be += cnt[x];
+    bt += (cnt[x] + per_tile - 1) / per_tile;
+  }
+  if (tid == 1023) {
+    entry_off[nbins] = s_e[1023];
+    tile_off[nbins] = s_t[1023];
+    *total_tiles = s_t[1023];
+  }
+}
+
+// one thread per bin: its tiles (bin, first entry, count)
+__global__ void attn_tiles_kernel(const int* __restrict__ cnt, const int* __restrict__ entry_off,
+                                  const int* __restrict__ tile_off, int nbins, int per_tile, int4* __restrict__ tiles) {
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= nbins) return;
+  const int c = cnt[x], e0 = entry_off[x], t0 = tile_off[x];
+  for (int j = 0; j * per_tile < c; ++j) tiles[t0 + j] = make_int4(x, e0 + j * per_tile, min(per_tile, c - j * per_tile), 0);
+}
+
+// grid (row chunks, G); dynamic smem = 2 * nblk ints. Entry = local query * 64 + slot.
+__global__ void attn_fill_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
+                                 const int32_t* __restrict__ kv_len, int b, int Nq, int Nk, int G, int K, int Bs,
+                                 int nblk, int c0, int cq, int rows_per_cta, const int* __restrict__ entry_off,
+                                 int* __restrict__ cursor, int* __restrict__ entries) {
+  extern __shared__ int sm[];
+  int* hist = sm;
+  int* base = sm + nblk;
+  const int g = blockIdx.y;
+  for (int t = threadIdx.x; t < nblk; t += blockDim.x) hist[t] = 0;
+  __syncthreads();
+  const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
+  const int r0 = blockIdx.x * rows_per_cta;
+  const int r1 = min(cq, r0 + rows_per_cta);
+  if (sv.ok) {
+    for (int e = threadIdx.x; e < (r1 - r0) * K; e += blockDim.x) {
+      const int il = r0 + e / K, k = e % K;
+      const int t = sel[((int64_t(b) * Nq + c0 + il) * G + g) * K + k];
+      if (entry_valid(t, sv.q0 + c0 + il, Bs, nblk)) atomicAdd(&hist[t], 1);
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < nblk; t += blockDim.x) {
+    const int h = hist[t];
+    base[t] = h ? entry_off[g * nblk + t] + atomicAdd(&cursor[g * nblk + t], h) : 0;
+    hist[t] = 0;
+  }
+  __syncthreads();
+  if (sv.ok) {
+    for (int e = threadIdx.x; e < (r1 - r0) * K; e += blockDim.x) {
+      const int il = r0 + e / K, k = e % K;
+      const int t = sel[((int64_t(b) * Nq + c0 + il) * G + g) * K + k];
+      if (entry_valid(t, sv.q0 + c0 + il, Bs, nblk)) {
+        const int slot = atomicAdd(&hist[t], 1);
+        entries[base[t] + slot] = il * 64 + k;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// attention
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+struct AttnParams {
+  const __nv_bfloat16* q;  // [B, Nq, Hq, D]
+  const int* entries;      // chunk entries
+  const int4* tiles;       // chunk tiles
+  const int* total_tiles;  // device count
+  const int32_t* q_offset;
+  const int32_t* kv_len;
+  __nv_bfloat16* part_o;  // [cq, K, Hq, D]
+  float* part_lse;        // [cq, K, Hq]
+  uint32_t* status;
+  int b, Nq, Nk, Hq, G, Bs, K, nblk, c0, hpg;
+  float scale_log2;  // softmax scale * log2(e)
+  float scale;
+};
+
+template <int D, int BS>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const AttnParams p) {
+  constexpr int NH = D / 64;                        // 64-element (128 B) halves of a row
+  constexpr uint32_t kQBytes = kRows * D * 2;       // one gathered query tile
+  constexpr uint32_t kKVHalf = BS * 128;            // one 64-wide half of a K or V block
+  constexpr uint32_t kKBytes = BS * D * 2;
+  constexpr bool kP128 = BS >= 64;                  // P rows: 128B swizzle halves, else 64B swizzle
+  constexpr uint32_t kPBytes = kRows * BS * 2;
+  constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, BS, false);
+  constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, D, true);  // B = V is MN-major
+  constexpr int kSCols = BS < 32 ? 32 : BS;
+  // TMEM columns: warpgroup w owns S at [256 w, 256 w + BS) and O at [256 w + 128, 256 w + 128 + D)
+  static_assert(kSCols <= 128 && D <= 128, "TMEM plan: S <= 128 and O <= 128 columns per warpgroup");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = tc::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* k_buf = smem;                    // [NH][BS][128 B]
+  uint8_t* v_buf = k_buf + kKBytes;         // [NH][BS][128 B]
+  uint8_t* q_buf = v_buf + kKBytes;         // 2 x [NH][128][128 B]
+  uint8_t* p_buf = q_buf + 2 * kQBytes;     // 2 x P tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p_buf + 2 * kPBytes);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;     // [2]
+  uint64_t* q_empty = bars + 4;    // [2]
+  uint64_t* s_full = bars + 6;     // [2]
+  uint64_t* p_full = bars + 8;     // [2]
+  uint64_t* o_full = bars + 10;    // [2]
+  uint64_t* o_empty = bars + 12;   // [2]
+  uint64_t* done_bar = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(kv_full, 1);
+    tc::mbar_init(kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&q_full[s], 4);
+      tc::mbar_init(&q_empty[s], 1);
+      tc::mbar_init(&s_full[s], 1);
+      tc::mbar_init(&p_full[s], 4);
+      tc::mbar_init(&o_full[s], 1);
+      tc::mbar_init(&o_empty[s], 4);
+    }
+    tc::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == kMmaWarpA) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == kKvWarp && lane == 0) {
+    tc::tma_prefetch(&tmK);
+    tc::tma_prefetch(&tmV);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  // this CTA's contiguous run of tiles
+  const int T = *p.total_tiles;
+  const int z0 = int((int64_t(T) * blockIdx.x) / gridDim.x);
+  const int z1 = int((int64_t(T) * (blockIdx.x + 1)) / gridDim.x);
+  const int n = z1 - z0;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, MSA_ERR_TIMEOUT);
+  };
+
+  if (warp == kKvWarp) {
+    // ----------------------------- K/V producer -----------------------------
+    if (lane == 0) {
+      int prev_bin = -1, loads = 0;
+      for (int z = 0; z < n; ++z) {
+        const int bin = p.tiles[z0 + z].x;
+        if (bin == prev_bin) continue;
+        prev_bin = bin;
+        if (!tc::mbar_wait(kv_empty, (loads & 1) ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        const int g = bin / p.nblk, t = bin % p.nblk;
+        tc::mbar_arrive_expect_tx(kv_full, 2 * kKBytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          tc::tma_load_4d(k_buf + h * kKVHalf, &tmK, kv_full, h * 64, g, t * BS, p.b);
+          tc::tma_load_4d(v_buf + h * kKVHalf, &tmV, kv_full, h * 64, g, t * BS, p.b);
+        }
+        ++loads;
+      }
+      int zero = 0;
+      if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // drain the last copy
+    }
+  } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 4) {
+    // --------------------------- query-row gather ---------------------------
+    const int r = (warp - kGatherWarp0) * 32 + lane;  // tile row
+    const int e = r / p.hpg, hh = r % p.hpg;
+    const uint32_t swz = uint32_t(r & 7);
+    for (int z = 0; z <= n; ++z) {
+      if (z < n) {
+        const int s = z & 1;
+        if (!tc::mbar_wait(&q_empty[s], ((z >> 1) & 1) ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        const int4 tl = p.tiles[z0 + z];
+        const bool valid = e < tl.z;
+        const int g = tl.x / p.nblk;
+        const int il = valid ? (p.entries[tl.y + e] >> 6) : 0;
+        const __nv_bfloat16* src = p.q + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + hh) * D;
+        const uint32_t dst = tc::smem_u32(q_buf + s * kQBytes) + uint32_t(r) * 128;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint32_t h = c >> 3, cc = c & 7;
+          cp_async16(dst + h * (kRows * 128) + ((cc ^ swz) << 4), src + c * 8, valid ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      if (z > 0) {
+        // the previous tile's rows have landed: publish them to the tensor core
+        cp_async_wait<1>();
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&q_full[(z - 1) & 1]);
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp == kMmaWarpA) {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      int prev_bin = -1, kv_uses = 0;
+      bool alive = true;
+      auto issue_pv = [&](int z, bool last_of_bin) -> bool {
+        const int s = z & 1;
+        if (!tc::mbar_wait(&p_full[s], (z >> 1) & 1, abort_flag) ||
+            !tc::mbar_wait(&o_empty[s], ((z >> 1) & 1) ^ 1, abort_flag))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t pa = tc::smem_u32(p_buf + s * kPBytes);
+        const uint32_t va = tc::smem_u32(v_buf);
+#pragma unroll
+        for (int kk = 0; kk < BS / 16; ++kk) {
+          uint64_t ad;
+          if (kP128)
+            ad = tc::smem_desc(pa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024, 2);
+          else
+            ad = tc::smem_desc(pa + kk * 32, 16, 512, 4);
+          const uint64_t bd = tc::smem_desc(va + kk * 16 * 128, kKVHalf, 1024, 2);
+          tc::mma_f16_ss(tmem + uint32_t(s) * 256u + 128u, ad, bd, kIdescPV, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&o_full[s]);
+        if (last_of_bin) tc::mma_commit(kv_empty);
+        return true;
+      };
+      for (int z = 0; z < n && alive; ++z) {
+        const int s = z & 1;
+        const int bin = p.tiles[z0 + z].x;
+        if (bin != prev_bin) {
+          if (z > 0 && !issue_pv(z - 1, true)) {
+            fail();
+            break;
+          }
+          if (!tc::mbar_wait(kv_full, kv_uses & 1, abort_flag)) {
+            fail();
+            break;
+          }
+          ++kv_uses;
+        }
+        if (!tc::mbar_wait(&q_full[s], (z >> 1) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t qa = tc::smem_u32(q_buf + s * kQBytes);
+        const uint32_t ka = tc::smem_u32(k_buf);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t ad = tc::smem_desc(qa + (kk >> 2) * (kRows * 128) + off, 16, 1024, 2);
+          const uint64_t bd = tc::smem_desc(ka + (kk >> 2) * kKVHalf + off, 16, 1024, 2);
+          tc::mma_f16_ss(tmem + uint32_t(s) * 256u, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&q_empty[s]);
+        tc::mma_commit(&s_full[s]);
+        if (bin == prev_bin && z > 0) {
+          if (!issue_pv(z - 1, false)) {
+            fail();
+            alive = false;
+            break;
+          }
+        }
+        prev_bin = bin;
+      }
+      if (alive && n > 0 && !*abort_flag) {
+        if (!issue_pv(n - 1, true)) fail();
+      }
+      int zero = 0;
+      tc::mma_commit(done_bar);
+      tc::mbar_wait(done_bar, 0, &zero);
+    }
+  } else {
+    // -------------------------------- epilogue --------------------------------
+    const int w = (warp - kEpiWarp0) >> 2;         // warpgroup: tiles z with z % 2 == w
+    const int quarter = warp & 3;                  // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;             // tile row
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const int e = r / p.hpg, hh = r % p.hpg;
+    const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
+    for (int z = w; z < n; z += 2) {
+      const int s = z & 1;  // == w
+      const int4 tl = p.tiles[z0 + z];
+      const bool valid = e < tl.z;
+      const int g = tl.x / p.nblk, t = tl.x % p.nblk;
+      const int packed = valid ? p.entries[tl.y + e] : 0;
+      const int il = packed >> 6, kslot = packed & 63;
+      const int pos = sv.q0 + p.c0 + il;
+      const int nvalid = valid ? min(BS, pos - t * BS + 1) : BS;  // keys j <= pos inside the block
+      if (!tc::mbar_wait(&s_full[s], (z >> 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t s_addr = tmem + lane_base + uint32_t(s) * 256u;
+      // pass 1: row maximum over the visible keys
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BS / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(s_addr + c * 32, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c * 32 + j < nvalid) mx = fmaxf(mx, __uint_as_float(v[j]));
+      }
+      // pass 2: probabilities (bf16) into the P tile, row sum
+      const float mneg = -mx * p.scale_log2;
+      float l = 0.f;
+      const uint32_t p_addr = tc::smem_u32(p_buf + s * kPBytes);
+#pragma unroll
+      for (int c = 0; c < BS / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(s_addr + c * 32, v);
+        tc::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = (c * 32 + j < nvalid) ? ex2(fmaf(__uint_as_float(v[j]), p.scale_log2, mneg)) : 0.f;
+          const float p1 = (c * 32 + j + 1 < nvalid) ? ex2(fmaf(__uint_as_float(v[j + 1]), p.scale_log2, mneg)) : 0.f;
+          l += p0 + p1;
+          pk[j >> 1] = pack_bf16(p0, p1);
+        }
+        // 32 keys = 4 chunks of 16 B
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = c * 4 + q4;  // 16-byte chunk index within the row (8 keys each)
+          uint32_t addr;
+          if (kP128) {
+            const int hf = chunk >> 3, cc = chunk & 7;
+            addr = p_addr + hf * (kRows * 128) + r * 128 + ((cc ^ (r & 7)) << 4);
+          } else {
+            addr = p_addr + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4);
+          }
+          st_shared_v4(addr, pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&p_full[s]);
+      // output: O / l as bf16 partial, lse
+      if (!tc::mbar_wait(&o_full[s], (z >> 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int h = g * p.hpg + hh;
+      const int64_t prow = (int64_t(il) * p.K + kslot) * p.Hq + h;
+      __nv_bfloat16* dst = p.part_o + prow * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(o_addr + c * 32, v);
+        tc::tmem_ld_wait();
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 o;
+            o.x = pack_bf16(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv);
+            o.y = pack_bf16(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv);
+            o.z = pack_bf16(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv);
+            o.w = pack_bf16(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv);
+            d4[q4] = o;
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&o_empty[s]);
+      if (valid) p.part_lse[prow] = mx * p.scale + logf(l);
+    }
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarpA) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine: one warp per (query, head); lanes own D/32 output elements each
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void attn_combine_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
+                                    const int32_t* __restrict__ kv_len, const __nv_bfloat16* __restrict__ part_o,
+                                    const float* __restrict__ part_lse, int b, int Nq, int Nk, int Hq, int G, int K,
+                                    int Bs, int nblk, int c0, int cq, __nv_bfloat16* __restrict__ out,
+                                    float* __restrict__ lse_out) {
+  constexpr int U = D / 32;
+  const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= int64_t(cq) * Hq) return;
+  const int il = int(wid / Hq), h = int(wid % Hq);
+  const int hpg = Hq / G, g = h / hpg;
+  const int i = c0 + il;
+  const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
+  const int pos = sv.q0 + i;
+  const int32_t* srow = sel + ((int64_t(b) * Nq + i) * G + g) * K;
+  float m = -INFINITY;
+  for (int k = 0; k < K; ++k) {
+    const int t = srow[k];
+    if (sv.ok && entry_valid(t, pos, Bs, nblk)) m = fmaxf(m, part_lse[(int64_t(il) * K + k) * Hq + h]);
+  }
+  float acc[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) acc[u] = 0.f;
+  float wsum = 0.f;
+  if (m > -INFINITY) {
+    for (int k = 0; k < K; ++k) {
+      const int t = srow[k];
+      if (!entry_valid(t, pos, Bs, nblk)) continue;
+      const int64_t prow = (int64_t(il) * K + k) * Hq + h;
+      const float wk = expf(part_lse[prow] - m);
+      wsum += wk;
+      const __nv_bfloat16* src = part_o + prow * D + lane * U;
+      if constexpr (U == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        acc[0] = fmaf(wk, a.x, acc[0]);
+        acc[1] = fmaf(wk, a.y, acc[1]);
+        acc[2] = fmaf(wk, c.x, acc[2]);
+        acc[3] = fmaf(wk, c.y, acc[3]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = fmaf(wk, __bfloat162float(src[u]), acc[u]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = out + ((int64_t(b) * Nq + i) * Hq + h) * D + lane * U;
+#pragma unroll
+  for (int u = 0; u < U; ++u) dst[u] = __float2bfloat16_rn(acc[u] * inv);
+  if (lse_out && lane == 0) lse_out[(int64_t(b) * Nq + i) * Hq + h] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
+int g_sms = 0;
+int sm_count() {
+  if (g_sms == 0) {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMs;
+    g_sms = n;
+  }
+  return g_sms;
+}
+
+inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int chunk_tokens(int Nq, int Hq, int K, int d) {
+  static int env = -1;
+  if (env < 0) {
+    const char* s = getenv("MSA_PREFILL_CHUNK");
+    env = s ? atoi(s) : 0;
+  }
+  if (env > 0) return env < Nq ? env : Nq;
+  // bound the partial buffers to ~4 GiB
+  const size_t per_tok = size_t(Hq) * K * (size_t(d) * 2 + 4);
+  size_t c = (size_t(4) << 30) / per_tok;
+  if (c < 1024) c = 1024;
+  return int(c < size_t(Nq) ? c : size_t(Nq));
+}
+
+struct KvoLayout {
+  size_t cnt, cursor, entry_off, tile_off, total, entries, tiles, part_o, part_lse, end;
+};
+
+KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
+  const int nblk = (Nk + Bs - 1) / Bs;
+  const int cq = chunk_tokens(Nq, Hq, K, d);
+  const size_t nbins = size_t(G) * nblk;
+  const size_t max_entries = size_t(cq) * G * K;
+  const int hpg = Hq / G;
+  const size_t per_tile = size_t(kRows / hpg);
+  const size_t max_tiles = max_entries / per_tile + nbins + 1;
+  KvoLayout L;
+  size_t o = kWsHeader;
+  L.cnt = o;
+  o += a256(nbins * 4);
+  L.cursor = o;
+  o += a256(nbins * 4);
+  L.entry_off = o;
+  o += a256((nbins + 1) * 4);
+  L.tile_off = o;
+  o += a256((nbins + 1) * 4);
+  L.total = o;
+  o += 256;
+  L.entries = o;
+  o += a256(max_entries * 4);
+  L.tiles = o;
+  o += a256(max_tiles * 16);
+  L.part_o = o;
+  o += a256(size_t(cq) * K * Hq * d * 2);
+  L.part_lse = o;
+  o += a256(size_t(cq) * K * Hq * 4);
+  L.end = o;
+  return L;
+}
+
+size_t attn_smem_bytes(int d, int Bs) {
+  const size_t kv = size_t(Bs) * d * 2 * 2, q = size_t(kRows) * d * 2 * 2, pb = size_t(kRows) * Bs * 2 * 2;
+  return 1024 + kv + q + pb + 16 * 8 + 64;
+}
+
+}  // namespace
+
+bool attn_kv_outer_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K) {
+  if (dtype != MSA_BF16 || (d != 64 && d != 128)) return false;
+  if (Bs != 32 && Bs != 64 && Bs != 128) return false;
+  if (K < 1 || K > kMaxK) return false;
+  const int hpg = Hq / Hkv;
+  if (hpg < 1 || hpg > 128 || (hpg & (hpg - 1)) != 0) return false;
+  return attn_smem_bytes(d, Bs) <= 227 * 1024;
+}
+
+size_t attn_kv_outer_ws_bytes(int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K) {
+  return kvo_layout(Nq, Hq, Hkv, d, Bs, K, Nk).end;
+}
+
+cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, const int32_t* sel,
+                                 const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk, int Hq,
+                                 int Hkv, int d, int Bs, int K, float scale, void* out, float* lse, void* ws,
+                                 cudaStream_t stream) {
+  const int G = Hkv, hpg = Hq / Hkv, nblk = (Nk + Bs - 1) / Bs;
+  const int nbins = G * nblk;
+  const int per_tile = kRows / hpg;
+  const KvoLayout L = kvo_layout(Nq, Hq, G, d, Bs, K, Nk);
+  char* w = static_cast<char*>(ws);
+  uint32_t* status = &static_cast<WsHeader*>(ws)->status;
+  int* cnt = reinterpret_cast<int*>(w + L.cnt);
+  int* cursor = reinterpret_cast<int*>(w + L.cursor);
+  int* entry_off = reinterpret_cast<int*>(w + L.entry_off);
+  int* tile_off = reinterpret_cast<int*>(w + L.tile_off);
+  int* total = reinterpret_cast<int*>(w + L.total);
+  int* entries = reinterpret_cast<int*>(w + L.entries);
+  int4* tiles = reinterpret_cast<int4*>(w + L.tiles);
+  __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(w + L.part_o);
+  float* part_lse = reinterpret_cast<float*>(w + L.part_lse);
+  const int cq_max = chunk_tokens(Nq, Hq, K, d);
+
+  CUtensorMap tmK, tmV;
+  const uint64_t dims[4] = {uint64_t(d), uint64_t(Hkv), uint64_t(Nk), uint64_t(B)};
+  const uint64_t strides[3] = {uint64_t(d) * 2, uint64_t(Hkv) * d * 2, uint64_t(Nk) * Hkv * d * 2};
+  const uint32_t box[4] = {64, 1, uint32_t(Bs), 1};
+  if (!make_tmap_bf16(&tmK, k, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16(&tmV, v, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+
+  const size_t smem = attn_smem_bytes(d, Bs);
+  const size_t hist_smem = size_t(nblk) * 4 * 2;
+  if (hist_smem > 200 * 1024) return cudaErrorInvalidValue;
+  static bool attr_done[2][3] = {{false}};
+  auto set_attr = [&](auto kern) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  };
+  cudaError_t e = cudaSuccess;
+  if (hist_smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(attn_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem));
+    if (e != cudaSuccess) return e;
+  }
+  (void)attr_done;
+
+  AttnParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.entries = entries;
+  prm.tiles = tiles;
+  prm.total_tiles = total;
+  prm.q_offset = q_offset;
+  prm.kv_len = kv_len;
+  prm.part_o = part_o;
+  prm.part_lse = part_lse;
+  prm.status = status;
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.Hq = Hq;
+  prm.G = G;
+  prm.Bs = Bs;
+  prm.K = K;
+  prm.nblk = nblk;
+  prm.hpg = hpg;
+  prm.scale = scale;
+  prm.scale_log2 = scale * kLog2e;
+  const int grid = sm_count();
+  const int rows_per_cta = 1024;
+
+  for (int b = 0; b < B; ++b) {
+    for (int c0 = 0; c0 < Nq; c0 += cq_max) {
+      const int cq = Nq - c0 < cq_max ? Nq - c0 : cq_max;
+      const dim3 igrid((cq + rows_per_cta - 1) / rows_per_cta, G);
+      if ((e = cudaMemsetAsync(w + L.cnt, 0, L.entry_off - L.cnt, stream)) != cudaSuccess) return e;
+      {
+        ProfScope pf("attn_invert", stream);
+        attn_count_kernel<<<igrid, 256, size_t(nblk) * 4, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk,
+                                                                    c0, cq, rows_per_cta, cnt, status);
+        attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, nbins, per_tile, entry_off, tile_off, total);
+        attn_tiles_kernel<<<(nbins + 255) / 256, 256, 0, stream>>>(cnt, entry_off, tile_off, nbins, per_tile, tiles);
+        attn_fill_kernel<<<igrid, 256, hist_smem, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0, cq,
+                                                            rows_per_cta, entry_off, cursor, entries);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+      prm.b = b;
+      prm.c0 = c0;
+      {
+        ProfScope pf("attn_kv_outer_tc", stream);
+#define MSA_KVO(D_, BS_)                                                                  \
+  do {                                                                                    \
+    auto kern = attn_kv_outer_kernel<D_, BS_>;                                           \
+    if ((e = set_attr(kern)) != cudaSuccess) return e;                                   \
+    kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, prm);                            \
+  } while (0)
+        if (d == 128) {
+          if (Bs == 128)
+            MSA_KVO(128, 128);
+          else if (Bs == 64)
+            MSA_KVO(128, 64);
+          else
+            MSA_KVO(128, 32);
+        } else {
+          if (Bs == 128)
+            MSA_KVO(64, 128);
+          else if (Bs == 64)
+            MSA_KVO(64, 64);
+          else
+            MSA_KVO(64, 32);
+        }
+#undef MSA_KVO
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+      {
+        ProfScope pf("attn_combine", stream);
+        const int64_t warps = int64_t(cq) * Hq;
+        const unsigned cgrid = unsigned((warps * 32 + 255) / 256);
+        if (d == 128)
+          attn_combine_kernel<128><<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, b, Nq, Nk, Hq,
+                                                              G, K, Bs, nblk, c0, cq,
+                                                              static_cast<__nv_bfloat16*>(out), lse);
+        else
+          attn_combine_kernel<64><<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, b, Nq, Nk, Hq,
+                                                             G, K, Bs, nblk, c0, cq,
+                                                             static_cast<__nv_bfloat16*>(out), lse);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+    }
+  }
+  return cudaSuccess;
+}
+
+}  // namespace msa

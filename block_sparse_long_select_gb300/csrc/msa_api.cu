@@ -47,11 +47,12 @@ IndexPlan plan_index(int B, int Nq, int Nk, int G, int di, int Bs, int K, int dt
 // ---- Main Branch planning ----------------------------------------------------
 struct AttnPlan {
   bool ok = false;
+  bool kv_outer = false;  // tcgen05 KV-outer kernel (bf16 prefill)
   msa_status_t err = MSA_ERR_INVALID_ARG;
   size_t ws_bytes = 0;
 };
 
-AttnPlan plan_attn(int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K, int dtype) {
+AttnPlan plan_attn(int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K, int dtype, bool prefill) {
   AttnPlan p;
   if (B < 1 || Nq < 1 || Nk < 1 || Hq < 1 || Hkv < 1 || d < 1 || Bs < 1 || K < 1 || !dtype_ok(dtype)) return p;
   if (Hq % Hkv != 0 || Nq > Nk) return p;
@@ -59,7 +60,8 @@ AttnPlan plan_attn(int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K,
     p.err = MSA_ERR_UNSUPPORTED;
     return p;
   }
-  p.ws_bytes = kWsHeader;
+  p.kv_outer = prefill && attn_kv_outer_supported(dtype, Hq, Hkv, d, Bs, K);
+  p.ws_bytes = p.kv_outer ? attn_kv_outer_ws_bytes(Nq, Nk, Hq, Hkv, d, Bs, K) : kWsHeader;
   p.ok = true;
   p.err = MSA_OK;
   return p;
@@ -87,11 +89,11 @@ extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int H
       return p.ok ? p.ws_bytes : 0;
     }
     case MSA_OP_PREFILL: {
-      AttnPlan p = plan_attn(B, Nq, Nk, Hq, G > 0 ? G : 1, d, Bs, K, dtype);
+      AttnPlan p = plan_attn(B, Nq, Nk, Hq, G > 0 ? G : 1, d, Bs, K, dtype, true);
       return p.ok ? p.ws_bytes : 0;
     }
     case MSA_OP_DECODE: {
-      AttnPlan p = plan_attn(B, 1, Nk, Hq, G > 0 ? G : 1, d, Bs, K, dtype);
+      AttnPlan p = plan_attn(B, 1, Nk, Hq, G > 0 ? G : 1, d, Bs, K, dtype, false);
       return p.ok ? p.ws_bytes : 0;
     }
     default:
@@ -127,11 +129,14 @@ extern "C" msa_status_t msa_sparse_attn_prefill(const void* q, const void* k, co
                                                 void* out, float* lse, void* ws, size_t ws_bytes,
                                                 cudaStream_t stream) {
   if (!q || !k || !v || !sel || !out) return MSA_ERR_INVALID_ARG;
-  AttnPlan p = plan_attn(B, Nq, Nk, Hq, Hkv, d, Bs, K, dtype);
+  AttnPlan p = plan_attn(B, Nq, Nk, Hq, Hkv, d, Bs, K, dtype, true);
   if (!p.ok) return p.err;
   msa_status_t w = check_ws(ws, ws_bytes, p.ws_bytes);
   if (w != MSA_OK) return w;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
+  if (p.kv_outer)
+    return cuda_status(launch_attn_kv_outer(q, k, v, sel, q_offset, kv_len, B, Nq, Nk, Hq, Hkv, d, Bs, K, scale, out,
+                                            lse, ws, stream));
   cudaError_t e = launch_attn_query_outer(dtype, q, k, v, sel, q_offset, kv_len, false, B, Nq, Nk, Hq, Hkv, d, Bs,
                                           K, scale, out, lse, status_word(ws), stream);
   return cuda_status(e);
@@ -142,7 +147,7 @@ extern "C" msa_status_t msa_sparse_attn_decode(const void* q, const void* k_cach
                                                int Hkv, int d, int Bs, int K, float scale, int dtype, void* out,
                                                float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!q || !k_cache || !v_cache || !sel || !kv_len || !out) return MSA_ERR_INVALID_ARG;
-  AttnPlan p = plan_attn(B, 1, Lmax, Hq, Hkv, d, Bs, K, dtype);
+  AttnPlan p = plan_attn(B, 1, Lmax, Hq, Hkv, d, Bs, K, dtype, false);
   if (!p.ok) return p.err;
   msa_status_t w = check_ws(ws, ws_bytes, p.ws_bytes);
   if (w != MSA_OK) return w;

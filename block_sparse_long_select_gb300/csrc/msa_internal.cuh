@@ -94,6 +94,13 @@ cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t*
 // Exact top-K over a block-max table (warp per row).
 cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
                                    int Nk, int G, int Bs, int K, int32_t* sel, uint32_t* status, cudaStream_t stream);
+// Main Branch, prefill, KV-outer tcgen05 path (bf16).
+bool attn_kv_outer_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K);
+size_t attn_kv_outer_ws_bytes(int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K);
+cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, const int32_t* sel,
+                                 const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk, int Hq,
+                                 int Hkv, int d, int Bs, int K, float scale, void* out, float* lse, void* ws,
+                                 cudaStream_t stream);
 // Main Branch, query-outer CUDA-core path (any dtype; prefill or decode).
 cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, const void* v, const int32_t* sel,
                                     const int32_t* q_offset, const int32_t* kv_len, bool decode, int B, int Nq,
