@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     lib_path,
     load_library,
     msa_index_select,
+    msa_index_select_noalloc,
     msa_profile_begin,
     msa_profile_end,
     msa_read_status,

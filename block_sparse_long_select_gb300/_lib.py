@@ -19,6 +19,7 @@ SIGNATURES = {
     "msa_sparse_attn_decode": (_i32, [_vp] * 5 + [_i32] * 7 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_read_status": (_i32, [_vp, _vp]),
     "msa_status_string": (ctypes.c_char_p, [_i32]),
+    "msa_index_select_noalloc": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 8 + [_vp, _vp, _vp]),
     "msa_profile_begin": (_i32, []),
     "msa_profile_end": (_i32, [_vp, _i32]),
 }
@@ -113,6 +114,19 @@ def msa_index_select(iq, ik, q_offset, kv_len, Bs, K, sel=None, block_max=None, 
                                            K, dt, _ptr(sel), _ptr(block_max), _ptr(ws), ws.numel(),
                                            _stream(stream, iq.device))
     _check(code, "msa_index_select")
+    return sel
+
+
+def msa_index_select_noalloc(iq, ik, q_offset, kv_len, Bs, K, sel, block_max=None, stream=None):
+    """msa_index_select on the library's static scratch (no workspace; see include/msa.h).
+    ``sel`` must be given: this wrapper allocates nothing either."""
+    _need_cuda(iq, ik, q_offset, kv_len, sel, block_max)
+    B, Nq, G, di = iq.shape
+    Nk = ik.shape[1]
+    code = load_library().msa_index_select_noalloc(_ptr(iq), _ptr(ik), _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, G,
+                                                   di, Bs, K, _dtype_code(iq), _ptr(sel), _ptr(block_max),
+                                                   _stream(stream, iq.device))
+    _check(code, "msa_index_select_noalloc")
     return sel
 
 

@@ -95,6 +95,28 @@ msa_status_t msa_index_select(const void* iq, const void* ik, const int32_t* q_o
                               int Nq, int Nk, int G, int di, int Bs, int K, int dtype, int32_t* sel, float* block_max,
                               void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* msa_index_select without a workspace argument: the same selection (and the
+ * same optional block_max output) for callers that cannot allocate device
+ * memory -- code that runs under another framework's allocator or inside its
+ * plugin hooks, where a raw cudaMalloc is forbidden or would bypass that
+ * framework's memory accounting, or a process whose device memory is fixed up
+ * front. The paper has no counterpart of this entry point.
+ *
+ * It allocates nothing. Its scratch (a status word and the block-max table)
+ * is a file-scope static __device__ array of 32 MiB that every GPU which loads
+ * this library reserves until the process exits. The table needs
+ * B*Nq*G*ceil(Nk/Bs)*4 bytes (0 when block_max is given); a call needing more
+ * than 32 MiB - 256 B returns MSA_ERR_WORKSPACE before anything is enqueued.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture. Every call
+ * shares the one array and clears its status word first: calls whose work
+ * overlaps on the GPU (other streams, or other host threads) race on it. Rows
+ * that fail the device-side range checks come back as -1 rows; the status
+ * word is not reported. Arguments and errors otherwise as msa_index_select. */
+msa_status_t msa_index_select_noalloc(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len,
+                                      int B, int Nq, int Nk, int G, int di, int Bs, int K, int dtype, int32_t* sel,
+                                      float* block_max, cudaStream_t stream);
+
 /* Main Branch, prefill: exact softmax attention of every query row over the
  * keys of its group's selected blocks, causally masked (j <= pos, j < kv_len).
  * (hyper.ai summary, "方法": the Main Branch gathers the Key/Value vectors of
