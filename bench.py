@@ -227,42 +227,39 @@ def decode_work(w, sel, kl):
             "attn_flops": 4.0 * w.d * (w.Hq // w.G) * float(att), "attended_keys": att}
 
 
-def roofline_for(kernel, prof, work, peaks, peak_src, workload, n_units, mode="prefill"):
-    """Roofline entry of one kernel: achieved = algorithmic work per launch /
-    mean launch duration (CUDA events on its stream inside the timed region).
-    Prefill kernels are contractions (tensor-bound); decode kernels stream
-    their inputs once (HBM-bound)."""
+def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="prefill"):
+    """Roofline entry of one kernel. achieved = algorithmic work per launch /
+    mean launch duration, both from the timed region: the per-step work of the
+    step that kernel serves x steps / launches, over the summed CUDA-event
+    time of its launches (recorded on its own stream). Prefill kernels are
+    contractions (tensor-bound); decode kernels stream their inputs once
+    (HBM-bound)."""
     launches, total_ms = prof[kernel]
     per_launch_s = total_ms / 1e3 / launches
     if mode == "decode":
         if "index" in kernel:
-            bound, unit, amount = "hbm", "GB/s", work["index_bytes"] / n_units
+            bound, unit, per_step = "hbm", "GB/s", work["index_bytes"]
         elif "attn" in kernel:
-            bound, unit, amount = "hbm", "GB/s", work["attn_bytes"] / n_units
+            bound, unit, per_step = "hbm", "GB/s", work["attn_bytes"]
         else:
             return None
     elif kernel in ("index_fused_tc", "index_blockmax_table"):
-        bound, unit, amount = "tensor", "TFLOP/s", work["index_flops"] / n_units
+        bound, unit, per_step = "tensor", "TFLOP/s", work["index_flops"]
     elif kernel in ("attn_kv_outer_tc", "attn_query_outer"):
-        bound, unit, amount = "tensor", "TFLOP/s", work["attn_flops"] / n_units
-    elif kernel in ("decode_index",):
-        bound, unit, amount = "hbm", "GB/s", work["index_bytes"] / n_units
-    elif kernel in ("decode_attn",):
-        bound, unit, amount = "hbm", "GB/s", work["attn_bytes"] / n_units
+        bound, unit, per_step = "tensor", "TFLOP/s", work["attn_flops"]
     else:
         return None
+    amount = per_step * steps / launches
     if bound == "tensor":
         achieved = amount / per_launch_s / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        peak_name = "bf16_tflops_sustained"
+        peak, peak_name = peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
     else:
         achieved = amount / per_launch_s / 1e9
-        peak = peaks["hbm_gbs"]
-        peak_name = "hbm_gbs"
+        peak, peak_name = peaks["hbm_gbs"], "hbm_gbs"
     return {"kernel": kernel, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": ncu_traffic(kernel, workload),
-            "algorithmic_per_launch": amount, "launch_ms": round(per_launch_s * 1e3, 4),
-            "peak_source": f"{peak_name} ({peak_src})"}
+            "algorithmic_per_launch": amount, "launches_per_step": launches / steps,
+            "launch_ms": round(per_launch_s * 1e3, 4), "peak_source": f"{peak_name} ({peak_src})"}
 
 
 # ---------------------------------------------------------------------------
@@ -336,10 +333,10 @@ def run_msa(args, dist):
     value = all_tokens / max_total_s
     launches = sum(v[0] for v in prof.values())
     dom = max(prof, key=lambda k: prof[k][1]) if prof else None
-    roof = roofline_for(dom, prof, work, peaks, peak_src, w.name, 1) if dom else None
+    roof = roofline_for(dom, prof, work, peaks, peak_src, w.name, args.steps) if dom else None
     kernels = {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4),
                    "share": round(v[1] / max(sum(x[1] for x in prof.values()), 1e-9), 4)} for k, v in prof.items()}
-    all_roofs = [r for r in (roofline_for(k, prof, work, peaks, peak_src, w.name, 1) for k in prof) if r]
+    all_roofs = [r for r in (roofline_for(k, prof, work, peaks, peak_src, w.name, args.steps) for k in prof) if r]
 
     # ---------------------------- e2e (host buffers) -------------------
     e2e = None
@@ -409,7 +406,7 @@ def run_msa(args, dist):
             "step_roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": peaks["hbm_gbs"],
                               "unit": "GB/s", "frac": round(step_gbs / peaks["hbm_gbs"], 4),
                               "algorithmic_bytes_per_step": dwork["total_bytes"]},
-            "roofline": roofline_for(ddom, dprof, dwork, peaks, peak_src, wd.name, 1, "decode") if ddom else None,
+            "roofline": roofline_for(ddom, dprof, dwork, peaks, peak_src, wd.name, dsteps, "decode") if ddom else None,
             "kernels": {k: {"launches": v[0], "ms_per_step": round(v[1] / dsteps, 4)} for k, v in dprof.items()},
             "gpu_launches": sum(v[0] for v in dprof.values()), "clocks": dclocks,
         }
