@@ -25,10 +25,12 @@
 //                   atomics on any output.
 //
 // attn_kv_outer warp roles (448 threads): warp 0 K/V TMA producer, warps 1-4
-// query-row gather (cp.async, swizzled), warp 5 TMEM owner + MMA issuer,
+// query-row gather (one ring slot each; cp.async, swizzled), warp 5 TMEM owner
+// + MMA issuer,
 // warps 6-13 two epilogue warpgroups that alternate tiles (ping-pong), each
 // owning S (Bs columns) and O (D columns) in TMEM. All waits are bounded.
 #include <cmath>
+#include <algorithm>
 #include <cstdlib>
 
 #include "msa_internal.cuh"
@@ -79,7 +81,8 @@ __global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t
     if (hist[t]) atomicAdd(&cnt[g * nblk + t], hist[t]);
 }
 
-// single CTA of 1024 threads: entry offsets, tile offsets, tile total
+// single CTA of 1024 threads: tile offsets, entry offsets (= tile offset x
+// entries per tile: every tile owns a full slot range), tile total
 __global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__ cnt, int nbins, int per_tile,
                                                          int* __restrict__ entry_off, int* __restrict__ tile_off,
                                                          int* __restrict__ total_tiles) {
@@ -103,15 +106,14 @@ __global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__
     s_t[tid] += vt;
     __syncthreads();
   }
-  int be = s_e[tid] - se, bt = s_t[tid] - st;
+  int bt = s_t[tid] - st;
   for (int x = lo; x < hi; ++x) {
-    entry_off[x] = be;
+    entry_off[x] = bt * per_tile;  // a bin's entries start on a tile boundary
     tile_off[x] = bt;
-    be += cnt[x];
     bt += (cnt[x] + per_tile - 1) / per_tile;
   }
   if (tid == 1023) {
-    entry_off[nbins] = s_e[1023];
+    entry_off[nbins] = s_t[1023] * per_tile;
     tile_off[nbins] = s_t[1023];
     *total_tiles = s_t[1023];
   }
@@ -123,14 +125,16 @@ __global__ void attn_tiles_kernel(const int* __restrict__ cnt, const int* __rest
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= nbins) return;
   const int c = cnt[x], e0 = entry_off[x], t0 = tile_off[x];
-  for (int j = 0; j * per_tile < c; ++j) tiles[t0 + j] = make_int4(x, e0 + j * per_tile, min(per_tile, c - j * per_tile), 0);
+  for (int j = 0; j * per_tile < c; ++j)
+    tiles[t0 + j] = make_int4(x, e0 + j * per_tile, min(per_tile, c - j * per_tile), 0);
 }
 
-// grid (row chunks, G); dynamic smem = 2 * nblk ints. Entry = local query * 64 + slot.
+// grid (row chunks, G); dynamic smem = 2 * nblk ints. Entry = local query * 64 + slot;
+// rev[(query, group, slot)] = the entry's index (its partial's row block).
 __global__ void attn_fill_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
                                  const int32_t* __restrict__ kv_len, int b, int Nq, int Nk, int G, int K, int Bs,
                                  int nblk, int c0, int cq, int rows_per_cta, const int* __restrict__ entry_off,
-                                 int* __restrict__ cursor, int* __restrict__ entries) {
+                                 int* __restrict__ cursor, int* __restrict__ entries, int* __restrict__ rev) {
   extern __shared__ int sm[];
   int* hist = sm;
   int* base = sm + nblk;
@@ -161,6 +165,7 @@ __global__ void attn_fill_kernel(const int32_t* __restrict__ sel, const int32_t*
       if (entry_valid(t, sv.q0 + c0 + il, Bs, nblk)) {
         const int slot = atomicAdd(&hist[t], 1);
         entries[base[t] + slot] = il * 64 + k;
+        rev[(int64_t(il) * G + g) * K + k] = base[t] + slot;  // where this (query, slot) partial lands
       }
     }
   }
@@ -197,57 +202,70 @@ struct AttnParams {
   const int* total_tiles;  // device count
   const int32_t* q_offset;
   const int32_t* kv_len;
-  __nv_bfloat16* part_o;  // [cq, K, Hq, D]
-  float* part_lse;        // [cq, K, Hq]
+  float* part_lse;        // [entries, hpg]: row (entry * hpg + head in group)
   uint32_t* status;
   int b, Nq, Nk, Hq, G, Bs, K, nblk, c0, hpg;
   float scale_log2;  // softmax scale * log2(e)
   float scale;
 };
 
+constexpr int kRing = 3;  // gathered-query tile ring depth (one gather warp per slot)
+static_assert(kRing <= 4, "one gather warp per ring slot: warps 1..4");
+
+template <int NC>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* v) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) tc::tmem_ld_32x32b_x32(taddr + c * 32, v + c * 32);
+  tc::tmem_ld_wait();
+}
+
 template <int D, int BS>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const AttnParams p) {
-  constexpr int NH = D / 64;                        // 64-element (128 B) halves of a row
-  constexpr uint32_t kQBytes = kRows * D * 2;       // one gathered query tile
+                         const __grid_constant__ CUtensorMap tmO, const AttnParams p) {
+  constexpr uint32_t kQBytes = kRows * D * 2;       // one gathered query tile (= one bf16 O tile)
+  constexpr uint32_t kSlot = kQBytes;
   constexpr uint32_t kKVHalf = BS * 128;            // one 64-wide half of a K or V block
   constexpr uint32_t kKBytes = BS * D * 2;
-  constexpr bool kP128 = BS >= 64;                  // P rows: 128B swizzle halves, else 64B swizzle
-  constexpr uint32_t kPBytes = kRows * BS * 2;
+  constexpr int NH = D / 64;
   constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, BS, false);
   constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, D, true);  // B = V is MN-major
-  constexpr int kSCols = BS < 32 ? 32 : BS;
+  constexpr int kSC = BS / 32 > 2 ? 2 : BS / 32;   // 32-column chunks per TMEM load batch (S)
   // TMEM columns: warpgroup w owns S at [256 w, 256 w + BS) and O at [256 w + 128, 256 w + 128 + D)
-  static_assert(kSCols <= 128 && D <= 128, "TMEM plan: S <= 128 and O <= 128 columns per warpgroup");
+  static_assert(BS <= 128 && D <= 128, "TMEM plan: S <= 128 and O <= 128 columns per warpgroup");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* k_buf = smem;                    // [NH][BS][128 B]
   uint8_t* v_buf = k_buf + kKBytes;         // [NH][BS][128 B]
-  uint8_t* q_buf = v_buf + kKBytes;         // 2 x [NH][128][128 B]
-  uint8_t* p_buf = q_buf + 2 * kQBytes;     // 2 x P tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p_buf + 2 * kPBytes);
+  uint8_t* ring = v_buf + kKBytes;          // kRing x kSlot: gathered Q tiles
+  uint8_t* ostage = ring + kRing * kSlot;   // 2 x kQBytes: O staging per epilogue warpgroup
+  int* meta = reinterpret_cast<int*>(ostage + 2 * kQBytes);  // [kRing][<=128] tile entries (query*64+slot) or -1
+  // mbarriers need 8-byte alignment: round the barrier area up to 16 bytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(meta + kRing * kRows) + 15) & ~uintptr_t(15));
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;     // [2]
-  uint64_t* q_empty = bars + 4;    // [2]
-  uint64_t* s_full = bars + 6;     // [2]
-  uint64_t* p_full = bars + 8;     // [2]
-  uint64_t* o_full = bars + 10;    // [2]
-  uint64_t* o_empty = bars + 12;   // [2]
-  uint64_t* done_bar = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* q_full = bars + 2;                // [kRing]
+  uint64_t* q_empty = q_full + kRing;         // [kRing]
+  uint64_t* s_full = q_empty + kRing;         // [2]
+  uint64_t* p_full = s_full + 2;              // [2]
+  uint64_t* o_full = p_full + 2;              // [2]
+  uint64_t* o_empty = o_full + 2;             // [2]
+  uint64_t* done_bar = o_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
+    for (int r = 0; r < kRing; ++r) {
+      tc::mbar_init(&q_full[r], 1);
+      tc::mbar_init(&q_empty[r], 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&q_full[s], 4);
-      tc::mbar_init(&q_empty[s], 1);
       tc::mbar_init(&s_full[s], 1);
       tc::mbar_init(&p_full[s], 4);
       tc::mbar_init(&o_full[s], 1);
@@ -264,6 +282,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == kKvWarp && lane == 0) {
     tc::tma_prefetch(&tmK);
     tc::tma_prefetch(&tmV);
+    tc::tma_prefetch(&tmO);
   }
   __syncthreads();
   tc::fence_after_sync();
@@ -305,36 +324,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 4) {
     // --------------------------- query-row gather ---------------------------
-    const int r = (warp - kGatherWarp0) * 32 + lane;  // tile row
-    const int e = r / p.hpg, hh = r % p.hpg;
-    const uint32_t swz = uint32_t(r & 7);
-    for (int z = 0; z <= n; ++z) {
-      if (z < n) {
-        const int s = z & 1;
-        if (!tc::mbar_wait(&q_empty[s], ((z >> 1) & 1) ^ 1, abort_flag)) {
-          fail();
-          break;
-        }
-        const int4 tl = p.tiles[z0 + z];
-        const bool valid = e < tl.z;
-        const int g = tl.x / p.nblk;
-        const int il = valid ? (p.entries[tl.y + e] >> 6) : 0;
-        const __nv_bfloat16* src = p.q + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + hh) * D;
-        const uint32_t dst = tc::smem_u32(q_buf + s * kQBytes) + uint32_t(r) * 128;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint32_t h = c >> 3, cc = c & 7;
-          cp_async16(dst + h * (kRows * 128) + ((cc ^ swz) << 4), src + c * 8, valid ? 16u : 0u);
-        }
+    // Gather warp gw < kRing owns ring slot gw and gathers tiles z = gw, gw + kRing, ...
+    // whole: the tile's entries go to shared memory first, then every lane
+    // copies 16-byte chunks (a warp instruction covers whole 256-byte rows,
+    // coalesced) into the 128B-swizzled K-major layout, and the tile is
+    // published as soon as its own copies have landed.
+    const int gw = warp - kGatherWarp0;    // ring slot of this warp; warps beyond the ring idle
+    constexpr int kCpr = D / 8;            // 16-byte chunks per row
+    constexpr int kRowsPerIt = 32 / kCpr;  // rows per warp instruction
+    const int per_tile = kRows / p.hpg;
+    int* my_meta = meta + gw * kRows;
+    for (int z = gw; gw < kRing && z < n; z += kRing) {
+      const int4 tl = p.tiles[z0 + z];
+      if (!tc::mbar_wait(&q_empty[gw], ((z / kRing) & 1) ^ 1, abort_flag)) {
+        fail();
+        break;
+      }
+      for (int e = lane; e < per_tile; e += 32) my_meta[e] = e < tl.z ? p.entries[tl.y + e] : -1;
+      __syncwarp();
+      const int g = tl.x / p.nblk;
+      const uint32_t slot = tc::smem_u32(ring + gw * kSlot);
+      const int chunk = lane % kCpr, sub = lane / kCpr;
+      const uint32_t hf = chunk >> 3, cc = chunk & 7;
+#pragma unroll 8
+      for (int it = 0; it < kRows / kRowsPerIt; ++it) {
+        const int row = it * kRowsPerIt + sub;
+        const int ent = my_meta[row / p.hpg];
+        const int il = ent >= 0 ? (ent >> 6) : 0;
+        const __nv_bfloat16* src =
+            p.q + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg) * D + chunk * 8;
+        cp_async16(slot + hf * (kRows * 128) + row * 128 + ((cc ^ uint32_t(row & 7)) << 4), src, ent >= 0 ? 16u : 0u);
       }
       cp_async_commit();
-      if (z > 0) {
-        // the previous tile's rows have landed: publish them to the tensor core
-        cp_async_wait<1>();
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&q_full[(z - 1) & 1]);
-      }
+      cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&q_full[gw]);
     }
     cp_async_wait<0>();
   } else if (warp == kMmaWarpA) {
@@ -348,25 +373,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             !tc::mbar_wait(&o_empty[s], ((z >> 1) & 1) ^ 1, abort_flag))
           return false;
         tc::fence_after_sync();
-        const uint32_t pa = tc::smem_u32(p_buf + s * kPBytes);
         const uint32_t va = tc::smem_u32(v_buf);
 #pragma unroll
         for (int kk = 0; kk < BS / 16; ++kk) {
-          uint64_t ad;
-          if (kP128)
-            ad = tc::smem_desc(pa + (kk >> 2) * (kRows * 128) + (kk & 3) * 32, 16, 1024, 2);
-          else
-            ad = tc::smem_desc(pa + kk * 32, 16, 512, 4);
+          // P (bf16 pairs packed per 32-bit column) sits where S was: 16 keys = 8 columns
+          const uint32_t a_tmem = tmem + uint32_t(s) * 256u + uint32_t(kk) * 8u;
           const uint64_t bd = tc::smem_desc(va + kk * 16 * 128, kKVHalf, 1024, 2);
-          tc::mma_f16_ss(tmem + uint32_t(s) * 256u + 128u, ad, bd, kIdescPV, kk > 0 ? 1u : 0u);
+          tc::mma_f16_ts(tmem + uint32_t(s) * 256u + 128u, a_tmem, bd, kIdescPV, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&o_full[s]);
         if (last_of_bin) tc::mma_commit(kv_empty);
         return true;
       };
+      int bin_next = n > 0 ? p.tiles[z0].x : -1;
       for (int z = 0; z < n && alive; ++z) {
-        const int s = z & 1;
-        const int bin = p.tiles[z0 + z].x;
+        const int s = z & 1, rs = z % kRing;
+        const int bin = bin_next;
+        if (z + 1 < n) bin_next = p.tiles[z0 + z + 1].x;
         if (bin != prev_bin) {
           if (z > 0 && !issue_pv(z - 1, true)) {
             fail();
@@ -378,12 +401,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           ++kv_uses;
         }
-        if (!tc::mbar_wait(&q_full[s], (z >> 1) & 1, abort_flag)) {
+        if (!tc::mbar_wait(&q_full[rs], (z / kRing) & 1, abort_flag)) {
           fail();
           break;
         }
         tc::fence_after_sync();
-        const uint32_t qa = tc::smem_u32(q_buf + s * kQBytes);
+        const uint32_t qa = tc::smem_u32(ring + rs * kSlot);
         const uint32_t ka = tc::smem_u32(k_buf);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -392,8 +415,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint64_t bd = tc::smem_desc(ka + (kk >> 2) * kKVHalf + off, 16, 1024, 2);
           tc::mma_f16_ss(tmem + uint32_t(s) * 256u, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&q_empty[s]);
         tc::mma_commit(&s_full[s]);
+        tc::mma_commit(&q_empty[rs]);  // the gathered Q tile is consumed
         if (bin == prev_bin && z > 0) {
           if (!issue_pv(z - 1, false)) {
             fail();
@@ -416,103 +439,105 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int quarter = warp & 3;                  // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;             // tile row
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    const int e = r / p.hpg, hh = r % p.hpg;
     const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
     for (int z = w; z < n; z += 2) {
       const int s = z & 1;  // == w
+      // this tile's metadata straight from global memory (the Q ring slot and
+      // its staged metadata are recycled as soon as QK^T has consumed them);
+      // the loads are in flight while S is being computed
       const int4 tl = p.tiles[z0 + z];
-      const bool valid = e < tl.z;
-      const int g = tl.x / p.nblk, t = tl.x % p.nblk;
-      const int packed = valid ? p.entries[tl.y + e] : 0;
-      const int il = packed >> 6, kslot = packed & 63;
-      const int pos = sv.q0 + p.c0 + il;
-      const int nvalid = valid ? min(BS, pos - t * BS + 1) : BS;  // keys j <= pos inside the block
+      const int ent = r / p.hpg < tl.z ? p.entries[tl.y + r / p.hpg] : -1;
       if (!tc::mbar_wait(&s_full[s], (z >> 1) & 1, abort_flag)) {
         fail();
         break;
       }
       tc::fence_after_sync();
+      const int bin = tl.x;
+      const bool valid = ent >= 0;
+      const int t = bin % p.nblk;
+      const int il = ent >> 6;
+      const int pos = sv.q0 + p.c0 + il;
+      const int nvalid = valid ? min(BS, pos - t * BS + 1) : BS;  // keys j <= pos inside the block
       const uint32_t s_addr = tmem + lane_base + uint32_t(s) * 256u;
       // pass 1: row maximum over the visible keys
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BS / 32; ++c) {
-        uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(s_addr + c * 32, v);
-        tc::tmem_ld_wait();
+      for (int c0 = 0; c0 < BS / 32; c0 += kSC) {
+        uint32_t v[kSC * 32];
+        tmem_load_cols<kSC>(s_addr + c0 * 32, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c * 32 + j < nvalid) mx = fmaxf(mx, __uint_as_float(v[j]));
+        for (int j = 0; j < kSC * 32; ++j)
+          if (c0 * 32 + j < nvalid) mx = fmaxf(mx, __uint_as_float(v[j]));
       }
-      // pass 2: probabilities (bf16) into the P tile, row sum
+      // pass 2: probabilities as bf16 pairs written back over S in TMEM (the
+      // PV MMA reads its A operand from there), row sum in fp32
       const float mneg = -mx * p.scale_log2;
       float l = 0.f;
-      const uint32_t p_addr = tc::smem_u32(p_buf + s * kPBytes);
 #pragma unroll
-      for (int c = 0; c < BS / 32; ++c) {
-        uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(s_addr + c * 32, v);
-        tc::tmem_ld_wait();
-        uint32_t pk[16];
+      for (int c0 = 0; c0 < BS / 32; c0 += kSC) {
+        uint32_t v[kSC * 32];
+        tmem_load_cols<kSC>(s_addr + c0 * 32, v);
+        uint32_t pk[kSC * 16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = (c * 32 + j < nvalid) ? ex2(fmaf(__uint_as_float(v[j]), p.scale_log2, mneg)) : 0.f;
-          const float p1 = (c * 32 + j + 1 < nvalid) ? ex2(fmaf(__uint_as_float(v[j + 1]), p.scale_log2, mneg)) : 0.f;
+        for (int j = 0; j < kSC * 32; j += 2) {
+          const float p0 = (c0 * 32 + j < nvalid) ? ex2(fmaf(__uint_as_float(v[j]), p.scale_log2, mneg)) : 0.f;
+          const float p1 = (c0 * 32 + j + 1 < nvalid) ? ex2(fmaf(__uint_as_float(v[j + 1]), p.scale_log2, mneg)) : 0.f;
           l += p0 + p1;
-          pk[j >> 1] = pack_bf16(p0, p1);
+          pk[j >> 1] = pack_bf16(p0, p1);  // keys 2c (low half) and 2c+1 (high half) in column c
         }
-        // 32 keys = 4 chunks of 16 B
+        // S columns [c0*32, c0*32 + 32*kSC) were read above; P of those keys
+        // takes columns [c0*16, c0*16 + 16*kSC), all of which are already read
+        if (kSC == 2)
+          tc::tmem_st_32x32b_x32(s_addr + c0 * 16, pk);
+        else
+          tc::tmem_st_32x32b_x16(s_addr + c0 * 16, pk);
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&p_full[s]);
+      // output: O / l (bf16) staged in this warpgroup's buffer, stored as one
+      // contiguous 128-row block by TMA; lse per row.
+      if (!tc::mbar_wait(&o_full[s], (z >> 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      if (r == 0) tc::bulk_wait_read_all();  // the previous store has read the staging buffer
+      tc::named_bar_sync(1 + w, 128);
+      tc::fence_after_sync();
+      const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint8_t* stage = ostage + w * kQBytes;
+      const uint32_t stage_addr = tc::smem_u32(stage);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = c * 4 + q4;  // 16-byte chunk index within the row (8 keys each)
-          uint32_t addr;
-          if (kP128) {
-            const int hf = chunk >> 3, cc = chunk & 7;
-            addr = p_addr + hf * (kRows * 128) + r * 128 + ((cc ^ (r & 7)) << 4);
-          } else {
-            addr = p_addr + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4);
-          }
-          st_shared_v4(addr, pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+      for (int c0 = 0; c0 < D / 32; c0 += 2) {
+        uint32_t v[64];
+        tmem_load_cols<2>(o_addr + c0 * 32, v);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int chunk = c0 * 4 + q4;  // 16-byte chunk of the output row
+          const int hf = chunk >> 3, ch = chunk & 7;
+          st_shared_v4(stage_addr + hf * (kRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4),
+                       pack_bf16(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv),
+                       pack_bf16(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv),
+                       pack_bf16(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv),
+                       pack_bf16(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv));
         }
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&p_full[s]);
-      // output: O / l as bf16 partial, lse
-      if (!tc::mbar_wait(&o_full[s], (z >> 1) & 1, abort_flag)) {
-        fail();
-        break;
-      }
-      tc::fence_after_sync();
-      const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int h = g * p.hpg + hh;
-      const int64_t prow = (int64_t(il) * p.K + kslot) * p.Hq + h;
-      __nv_bfloat16* dst = p.part_o + prow * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(o_addr + c * 32, v);
-        tc::tmem_ld_wait();
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 o;
-            o.x = pack_bf16(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv);
-            o.y = pack_bf16(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv);
-            o.z = pack_bf16(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv);
-            o.w = pack_bf16(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv);
-            d4[q4] = o;
-          }
-        }
-      }
-      tc::fence_before_sync();
-      __syncwarp();
       if (lane == 0) tc::mbar_arrive(&o_empty[s]);
-      if (valid) p.part_lse[prow] = mx * p.scale + logf(l);
+      const int zg = z0 + z;  // tile index in the chunk = its partial row block
+      p.part_lse[int64_t(zg) * kRows + r] = valid ? mx * p.scale + logf(l) : 0.f;
+      tc::named_bar_sync(1 + w, 128);  // the whole tile is staged
+      if (r == 0) {
+#pragma unroll
+        for (int hf = 0; hf < NH; ++hf) tc::tma_store_2d(&tmO, stage + hf * (kRows * 128), hf * 64, zg * kRows);
+        tc::bulk_commit();
+      }
     }
+    if (r == 0) tc::bulk_wait_all();
   }
 
   __syncthreads();
@@ -523,60 +548,88 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// combine: one warp per (query, head); lanes own D/32 output elements each
+// combine: one warp per (query, group). A slot's partials of the group's
+// heads are contiguous (hpg rows of D bf16, found through the reverse map);
+// each lane owns NU 16-byte vectors of them. Slots are merged in slot order
+// with log-sum-exp weights.
 // ---------------------------------------------------------------------------
-template <int D>
+template <int NU>
 __global__ void attn_combine_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
                                     const int32_t* __restrict__ kv_len, const __nv_bfloat16* __restrict__ part_o,
-                                    const float* __restrict__ part_lse, int b, int Nq, int Nk, int Hq, int G, int K,
-                                    int Bs, int nblk, int c0, int cq, __nv_bfloat16* __restrict__ out,
+                                    const float* __restrict__ part_lse, const int* __restrict__ rev, int b, int Nq, int Nk, int Hq, int G, int K,
+                                    int Bs, int nblk, int D, int c0, int cq, __nv_bfloat16* __restrict__ out,
                                     float* __restrict__ lse_out) {
-  constexpr int U = D / 32;
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (wid >= int64_t(cq) * Hq) return;
-  const int il = int(wid / Hq), h = int(wid % Hq);
-  const int hpg = Hq / G, g = h / hpg;
+  if (wid >= int64_t(cq) * G) return;
+  const int il = int(wid / G), g = int(wid % G);
+  const int hpg = Hq / G;
+  const int nvec = hpg * D / 8;  // 16-byte vectors per slot
   const int i = c0 + il;
   const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
   const int pos = sv.q0 + i;
   const int32_t* srow = sel + ((int64_t(b) * Nq + i) * G + g) * K;
-  float m = -INFINITY;
-  for (int k = 0; k < K; ++k) {
-    const int t = srow[k];
-    if (sv.ok && entry_valid(t, pos, Bs, nblk)) m = fmaxf(m, part_lse[(int64_t(il) * K + k) * Hq + h]);
+  const int ta = lane < K ? srow[lane] : -1;
+  const int tb = lane + 32 < K ? srow[lane + 32] : -1;
+  const uint64_t mask = uint64_t(__ballot_sync(0xffffffffu, sv.ok && entry_valid(ta, pos, Bs, nblk))) |
+                        (uint64_t(__ballot_sync(0xffffffffu, sv.ok && entry_valid(tb, pos, Bs, nblk))) << 32);
+  int head[NU];
+  float m[NU], wsum[NU], acc[NU][8];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const int vi = lane + 32 * u;
+    head[u] = vi < nvec ? (vi * 8) / D : 0;
+    m[u] = -INFINITY;
+    wsum[u] = 0.f;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc[u][x] = 0.f;
   }
-  float acc[U];
+  // slot k's partial rows: entry E = rev[...], rows E * hpg .. E * hpg + hpg - 1
+  const int* rv = rev + (int64_t(il) * G + g) * K;
+  const int ea = lane < K ? rv[lane] : 0;
+  const int eb = lane + 32 < K ? rv[lane + 32] : 0;
+#pragma unroll 4
+  for (int k = 0; k < K; ++k) {
+    if (!((mask >> k) & 1)) continue;
+    const int64_t E = __shfl_sync(0xffffffffu, k < 32 ? ea : eb, k & 31);
 #pragma unroll
-  for (int u = 0; u < U; ++u) acc[u] = 0.f;
-  float wsum = 0.f;
-  if (m > -INFINITY) {
-    for (int k = 0; k < K; ++k) {
-      const int t = srow[k];
-      if (!entry_valid(t, pos, Bs, nblk)) continue;
-      const int64_t prow = (int64_t(il) * K + k) * Hq + h;
-      const float wk = expf(part_lse[prow] - m);
-      wsum += wk;
-      const __nv_bfloat16* src = part_o + prow * D + lane * U;
-      if constexpr (U == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(src);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        acc[0] = fmaf(wk, a.x, acc[0]);
-        acc[1] = fmaf(wk, a.y, acc[1]);
-        acc[2] = fmaf(wk, c.x, acc[2]);
-        acc[3] = fmaf(wk, c.y, acc[3]);
-      } else {
+    for (int u = 0; u < NU; ++u) m[u] = fmaxf(m[u], part_lse[E * hpg + head[u]]);
+  }
+#pragma unroll 4
+  for (int k = 0; k < K; ++k) {
+    if (!((mask >> k) & 1)) continue;
+    const int64_t E = __shfl_sync(0xffffffffu, k < 32 ? ea : eb, k & 31);
 #pragma unroll
-        for (int u = 0; u < U; ++u) acc[u] = fmaf(wk, __bfloat162float(src[u]), acc[u]);
+    for (int u = 0; u < NU; ++u) {
+      const int vi = lane + 32 * u;
+      if (vi >= nvec) continue;
+      const float wk = expf(part_lse[E * hpg + head[u]] - m[u]);
+      wsum[u] += wk;
+      const uint4 raw = *reinterpret_cast<const uint4*>(part_o + E * hpg * D + vi * 8);
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float2 f = __bfloat1622float2(h2[x]);
+        acc[u][2 * x] = fmaf(wk, f.x, acc[u][2 * x]);
+        acc[u][2 * x + 1] = fmaf(wk, f.y, acc[u][2 * x + 1]);
       }
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = out + ((int64_t(b) * Nq + i) * Hq + h) * D + lane * U;
+  __nv_bfloat16* dst = out + ((int64_t(b) * Nq + i) * Hq + g * hpg) * D;
 #pragma unroll
-  for (int u = 0; u < U; ++u) dst[u] = __float2bfloat16_rn(acc[u] * inv);
-  if (lse_out && lane == 0) lse_out[(int64_t(b) * Nq + i) * Hq + h] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+  for (int u = 0; u < NU; ++u) {
+    const int vi = lane + 32 * u;
+    if (vi >= nvec) continue;
+    const float inv = wsum[u] > 0.f ? 1.f / wsum[u] : 0.f;
+    uint4 o;
+    o.x = pack_bf16(acc[u][0] * inv, acc[u][1] * inv);
+    o.y = pack_bf16(acc[u][2] * inv, acc[u][3] * inv);
+    o.z = pack_bf16(acc[u][4] * inv, acc[u][5] * inv);
+    o.w = pack_bf16(acc[u][6] * inv, acc[u][7] * inv);
+    *reinterpret_cast<uint4*>(dst + vi * 8) = o;
+    if (lse_out && (vi * 8) % D == 0)
+      lse_out[(int64_t(b) * Nq + i) * Hq + g * hpg + head[u]] = wsum[u] > 0.f ? m[u] + logf(wsum[u]) : -INFINITY;
+  }
 }
 
 int g_sms = 0;
@@ -599,15 +652,17 @@ int chunk_tokens(int Nq, int Hq, int K, int d) {
     env = s ? atoi(s) : 0;
   }
   if (env > 0) return env < Nq ? env : Nq;
-  // bound the partial buffers to ~4 GiB
+  // bound the partial buffers to ~4 GiB, in equal chunks (no short tail chunk)
   const size_t per_tok = size_t(Hq) * K * (size_t(d) * 2 + 4);
-  size_t c = (size_t(4) << 30) / per_tok;
-  if (c < 1024) c = 1024;
-  return int(c < size_t(Nq) ? c : size_t(Nq));
+  size_t cap = (size_t(4) << 30) / per_tok;
+  if (cap < 1024) cap = 1024;
+  const size_t nchunks = (size_t(Nq) + cap - 1) / cap;
+  return int((size_t(Nq) + nchunks - 1) / nchunks);
 }
 
 struct KvoLayout {
-  size_t cnt, cursor, entry_off, tile_off, total, entries, tiles, part_o, part_lse, end;
+  size_t cnt, cursor, entry_off, tile_off, total, entries, rev, tiles, part_o, part_lse, end;
+  size_t max_tiles;
 };
 
 KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
@@ -630,21 +685,26 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   o += a256((nbins + 1) * 4);
   L.total = o;
   o += 256;
+  L.max_tiles = max_tiles;
   L.entries = o;
+  o += a256(max_tiles * per_tile * 4);  // bins padded to whole tiles
+  L.rev = o;
   o += a256(max_entries * 4);
   L.tiles = o;
   o += a256(max_tiles * 16);
-  L.part_o = o;
-  o += a256(size_t(cq) * K * Hq * d * 2);
-  L.part_lse = o;
-  o += a256(size_t(cq) * K * Hq * 4);
+  L.part_o = o;  // [tiles * 128 rows][d] bf16
+  o += a256(max_tiles * kRows * size_t(d) * 2);
+  L.part_lse = o;  // [tiles * 128 rows] fp32
+  o += a256(max_tiles * kRows * 4);
   L.end = o;
   return L;
 }
 
 size_t attn_smem_bytes(int d, int Bs) {
-  const size_t kv = size_t(Bs) * d * 2 * 2, q = size_t(kRows) * d * 2 * 2, pb = size_t(kRows) * Bs * 2 * 2;
-  return 1024 + kv + q + pb + 16 * 8 + 64;
+  const size_t kv = size_t(Bs) * d * 2 * 2;
+  const size_t slot = size_t(kRows) * d * 2;
+  const size_t meta = size_t(kRing) * kRows * 4 + 16;
+  return 1024 + kv + kRing * slot + 2 * slot + meta + (2 + 2 * kRing + 8 + 1) * 8 + 16;
 }
 
 }  // namespace
@@ -654,7 +714,7 @@ bool attn_kv_outer_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K) {
   if (Bs != 32 && Bs != 64 && Bs != 128) return false;
   if (K < 1 || K > kMaxK) return false;
   const int hpg = Hq / Hkv;
-  if (hpg < 1 || hpg > 128 || (hpg & (hpg - 1)) != 0) return false;
+  if (hpg < 1 || hpg > 128 || (hpg & (hpg - 1)) != 0 || hpg * d > 2048) return false;
   return attn_smem_bytes(d, Bs) <= 227 * 1024;
 }
 
@@ -678,6 +738,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   int* tile_off = reinterpret_cast<int*>(w + L.tile_off);
   int* total = reinterpret_cast<int*>(w + L.total);
   int* entries = reinterpret_cast<int*>(w + L.entries);
+  int* rev = reinterpret_cast<int*>(w + L.rev);
   int4* tiles = reinterpret_cast<int4*>(w + L.tiles);
   __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(w + L.part_o);
   float* part_lse = reinterpret_cast<float*>(w + L.part_lse);
@@ -690,11 +751,17 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   if (!make_tmap_bf16(&tmK, k, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16(&tmV, v, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  CUtensorMap tmO;  // partial rows: [tiles * 128][d], stored 128 rows x 64 columns at a time
+  {
+    const uint64_t odims[2] = {uint64_t(d), uint64_t(L.max_tiles) * kRows};
+    const uint64_t ostr[1] = {uint64_t(d) * 2};
+    const uint32_t obox[2] = {64, uint32_t(kRows)};
+    if (!make_tmap_bf16(&tmO, part_o, 2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
 
   const size_t smem = attn_smem_bytes(d, Bs);
   const size_t hist_smem = size_t(nblk) * 4 * 2;
   if (hist_smem > 200 * 1024) return cudaErrorInvalidValue;
-  static bool attr_done[2][3] = {{false}};
   auto set_attr = [&](auto kern) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   };
@@ -705,7 +772,6 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
       e = cudaFuncSetAttribute(attn_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem));
     if (e != cudaSuccess) return e;
   }
-  (void)attr_done;
 
   AttnParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -714,7 +780,6 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   prm.total_tiles = total;
   prm.q_offset = q_offset;
   prm.kv_len = kv_len;
-  prm.part_o = part_o;
   prm.part_lse = part_lse;
   prm.status = status;
   prm.Nq = Nq;
@@ -742,7 +807,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
         attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, nbins, per_tile, entry_off, tile_off, total);
         attn_tiles_kernel<<<(nbins + 255) / 256, 256, 0, stream>>>(cnt, entry_off, tile_off, nbins, per_tile, tiles);
         attn_fill_kernel<<<igrid, 256, hist_smem, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0, cq,
-                                                            rows_per_cta, entry_off, cursor, entries);
+                                                            rows_per_cta, entry_off, cursor, entries, rev);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
       prm.b = b;
@@ -753,7 +818,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   do {                                                                                    \
     auto kern = attn_kv_outer_kernel<D_, BS_>;                                           \
     if ((e = set_attr(kern)) != cudaSuccess) return e;                                   \
-    kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, prm);                            \
+    kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, tmO, prm);                       \
   } while (0)
         if (d == 128) {
           if (Bs == 128)
@@ -775,16 +840,22 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
       }
       {
         ProfScope pf("attn_combine", stream);
-        const int64_t warps = int64_t(cq) * Hq;
+        const int64_t warps = int64_t(cq) * G;
         const unsigned cgrid = unsigned((warps * 32 + 255) / 256);
-        if (d == 128)
-          attn_combine_kernel<128><<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, b, Nq, Nk, Hq,
-                                                              G, K, Bs, nblk, c0, cq,
-                                                              static_cast<__nv_bfloat16*>(out), lse);
+        const int nvec = hpg * d / 8;
+        __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(out);
+#define MSA_CMB(NU_)                                                                                            \
+  attn_combine_kernel<NU_><<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, rev, b, Nq, Nk, Hq, G, K, \
+                                                      Bs, nblk, d, c0, cq, o16, lse)
+        if (nvec <= 32)
+          MSA_CMB(1);
+        else if (nvec <= 64)
+          MSA_CMB(2);
+        else if (nvec <= 128)
+          MSA_CMB(4);
         else
-          attn_combine_kernel<64><<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, b, Nq, Nk, Hq,
-                                                             G, K, Bs, nblk, c0, cq,
-                                                             static_cast<__nv_bfloat16*>(out), lse);
+          MSA_CMB(8);
+#undef MSA_CMB
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
     }
