@@ -48,6 +48,7 @@ IndexPlan plan_index(int B, int Nq, int Nk, int G, int di, int Bs, int K, int dt
 struct AttnPlan {
   bool ok = false;
   bool kv_outer = false;  // tcgen05 KV-outer kernel (bf16 prefill)
+  bool split = false;     // split-over-blocks decode kernel (bf16 decode)
   msa_status_t err = MSA_ERR_INVALID_ARG;
   size_t ws_bytes = 0;
 };
@@ -61,7 +62,9 @@ AttnPlan plan_attn(int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K,
     return p;
   }
   p.kv_outer = prefill && attn_kv_outer_supported(dtype, Hq, Hkv, d, Bs, K);
-  p.ws_bytes = p.kv_outer ? attn_kv_outer_ws_bytes(Nq, Nk, Hq, Hkv, d, Bs, K) : kWsHeader;
+  p.split = !prefill && decode_attn_supported(dtype, Hq, Hkv, d, Bs, K);
+  p.ws_bytes = p.kv_outer ? attn_kv_outer_ws_bytes(Nq, Nk, Hq, Hkv, d, Bs, K)
+                          : (p.split ? kWsHeader + decode_ws_bytes(B, Hq, Hkv, d, K) : kWsHeader);
   p.ok = true;
   p.err = MSA_OK;
   return p;
@@ -115,6 +118,10 @@ extern "C" msa_status_t msa_index_select(const void* iq, const void* ik, const i
     return cuda_status(launch_index_fused_tc(iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, K, sel, status,
                                              stream));
   }
+  if (!block_max && decode_index_supported(dtype, B, Nq, G, di, Bs, K)) {
+    float* tab = reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);
+    return cuda_status(launch_decode_index(iq, ik, q_offset, kv_len, B, Nk, G, Bs, K, sel, tab, status, stream));
+  }
   float* table = block_max ? block_max : reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);
   cudaError_t e = launch_index_blockmax_table(dtype, iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, table, status,
                                               stream);
@@ -152,6 +159,9 @@ extern "C" msa_status_t msa_sparse_attn_decode(const void* q, const void* k_cach
   msa_status_t w = check_ws(ws, ws_bytes, p.ws_bytes);
   if (w != MSA_OK) return w;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
+  if (p.split)
+    return cuda_status(launch_decode_attn(q, k_cache, v_cache, sel, kv_len, B, Lmax, Hq, Hkv, d, Bs, K, scale, out,
+                                          lse, static_cast<char*>(ws) + kWsHeader, status_word(ws), stream));
   cudaError_t e = launch_attn_query_outer(dtype, q, k_cache, v_cache, sel, nullptr, kv_len, true, B, 1, Lmax, Hq,
                                           Hkv, d, Bs, K, scale, out, lse, status_word(ws), stream);
   return cuda_status(e);

@@ -101,6 +101,19 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
                                  const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk, int Hq,
                                  int Hkv, int d, int Bs, int K, float scale, void* out, float* lse, void* ws,
                                  cudaStream_t stream);
+// Index Branch for one query per sequence (decode): tcgen05 stream of the
+// index-key cache into a [B, G, nblk] block-max table, then exact top-K.
+bool decode_index_supported(int dtype, int B, int Nq, int G, int di, int Bs, int K);
+cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
+                                int Lmax, int G, int Bs, int K, int32_t* sel, float* table, uint32_t* status,
+                                cudaStream_t stream);
+// Main Branch, decode: split over selected blocks + combine (bf16).
+bool decode_attn_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K);
+size_t decode_ws_bytes(int B, int Hq, int Hkv, int d, int K);
+cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v_cache, const int32_t* sel,
+                               const int32_t* kv_len, int B, int Lmax, int Hq, int Hkv, int d, int Bs, int K,
+                               float scale, void* out, float* lse, void* scratch, uint32_t* status,
+                               cudaStream_t stream);
 // Main Branch, query-outer CUDA-core path (any dtype; prefill or decode).
 cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, const void* v, const int32_t* sel,
                                     const int32_t* q_offset, const int32_t* kv_len, bool decode, int B, int Nq,

@@ -108,3 +108,47 @@ def test_decode_b64_full():
     oout, olse = oracle_attention_rows(w, rb, ri, osel)
     assert_close(out.float().cpu().numpy(), oout, "bf16", w.name)
     assert_close(lse.cpu().numpy(), olse, "bf16", w.name, lse=True)
+
+
+DECODE_VARIANTS = {
+    "bs64_k8": dict(Bs=64, K=8),
+    "bs32_hpg8_d64": dict(Bs=32, K=12, Hq=16, Hkv=2, d=64),
+    "bs128_hpg1": dict(Bs=128, K=5, Hq=8, Hkv=8),
+    "bs128_hpg2_d64_di32": dict(Bs=128, K=6, Hq=8, Hkv=4, d=64, di=32),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_VARIANTS))
+def test_decode_variants(name):
+    """Decode with other block sizes, head maps and head dims (ragged lengths, some shorter than one block)."""
+    w = synth.scaled(synth.WORKLOADS["decode_b64"], B=6, Nk=3000, kv_len_range=(1, 3000), **DECODE_VARIANTS[name])
+    t = device_inputs(w, DEV)
+    sel, out, lse = gpu_decode(w, t, DEV)
+    h = host_inputs(w)
+    osel, oout, olse = oracle_full(w, h)
+    assert np.array_equal(sel.cpu().numpy(), osel), name
+    assert_close(out.float().cpu().numpy(), oout[:, 0], "bf16", name)
+    assert_close(lse.cpu().numpy(), olse[:, 0], "bf16", name, lse=True)
+
+
+def test_decode_query_offset_not_last():
+    """Index selection with one query per sequence at a position before the end of its keys."""
+    w = synth.scaled(synth.WORKLOADS["decode_b64"], B=4, Nk=4096, kv_len_range=(2000, 4096))
+    t = device_inputs(w, DEV)
+    kl = synth.kv_lens(w)
+    qo = (kl // 2).astype(np.int32)
+    sel = msa_index_select_dev(t, w, qo, kl)
+    h = host_inputs(w)
+    import oracle
+
+    osel = oracle.index_select(h["iq"].reshape(w.B, w.G, w.di), h["ik"], np.arange(w.B, dtype=np.int32),
+                               np.zeros(w.B, np.int32), qo, kl, w.Bs, w.K)
+    assert np.array_equal(sel[:, 0], osel)
+
+
+def msa_index_select_dev(t, w, qo, kl):
+    import block_sparse_long_select_gb300 as msa
+
+    s = msa.msa_index_select(t["iq"], t["ik"], torch.from_numpy(qo).to(DEV), torch.from_numpy(kl).to(DEV), w.Bs, w.K)
+    torch.cuda.synchronize()
+    return s.cpu().numpy()
