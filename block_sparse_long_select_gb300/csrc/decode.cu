@@ -6,17 +6,19 @@
 //  decode_index    Index Branch for one query per sequence: the index-key
 //                  cache streamed once by TMA in 128-key tiles, scores on
 //                  tcgen05 (keys along M, the G index-query heads along N),
-//                  block maxima straight from TMEM into a small
-//                  [B, G, nblk] table
-//  decode_topk     exact top-K per (sequence, group) over that table, the
-//                  query's own block forced, ascending output
+//                  32-key sub-block maxima straight from TMEM (one warp
+//                  redux each) into a small [B, G, Lmax/32] table
+//  decode_topk     exact top-K per (sequence, group): block maxima assembled
+//                  from the sub-block maxima, the query's own block forced,
+//                  ascending output
 //  decode_attn     one CTA per (sequence, group, selected block): the block's
 //                  K and V rows of that group are TMA-loaded (128B-swizzled,
 //                  so a thread reading "its" key row is bank-conflict free),
 //                  scores for the group's query heads, a block-local softmax,
 //                  P.V in fp32 -> per-slot partial (O unnormalised, max, sum)
-//  decode_combine  per (sequence, query head): log-sum-exp merge of the K
-//                  slot partials in slot order -> bf16 output row (+ lse)
+//                  The last of the K slot CTAs of a (sequence, group) (an
+//                  arrival counter, not an output atomic) merges the slot
+//                  partials in slot order by log-sum-exp -> bf16 rows (+ lse)
 //
 // The step streams each selected K/V block from HBM exactly once; partials
 // are small (B x G x K x hpg x (d + 2) fp32) and stay in L2.
@@ -28,7 +30,6 @@
 namespace msa {
 namespace {
 
-constexpr int kDecThreads = 128;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2eD = 1.4426950408889634f;
 
@@ -38,252 +39,282 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// smem: K [NH][BS][128 B] | V [NH][BS][128 B] (128B swizzle) | q [hpg][D] f32 | p [hpg][BS] f32 | ml [hpg][2]
+// ---------------------------------------------------------------------------
+// decode_attn (+ combine by the last CTA of each (sequence, group))
+// smem: K [NH][BS][128 B] | V [NH][BS][128 B] (TMA, 128B swizzle) |
+//       S [HPG][BS] f32 | P [HPG][BS + 8] bf16 | ml [HPG][2] | 2 mbarriers
+// Both products run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// accumulate): S^T = K q^T with keys along M and the group's heads along N
+// (padded to 8), O^T = V^T P^T with head dims along M; operands come straight
+// from the swizzled K/V tiles through ldmatrix (.trans for V).
+// ---------------------------------------------------------------------------
+constexpr int kDecThreads = 256;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// address of 16-byte chunk `ch` (8 columns) of row `row` in a 128B-swizzled [NH][rows][128 B] tile
+__device__ __forceinline__ uint32_t swz_addr(uint32_t base, uint32_t half_bytes, int row, int ch) {
+  return base + uint32_t(ch >> 3) * half_bytes + uint32_t(row) * 128u + ((uint32_t(ch & 7) ^ uint32_t(row & 7)) << 4);
+}
+
 template <int D, int BS, int HPG>
 __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const __nv_bfloat16* __restrict__ q,
     const int32_t* __restrict__ sel, const int32_t* __restrict__ kv_len, int Lmax, int Hq, int G, int K, int nblk,
-    float scale_log2, float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* status) {
+    float scale_log2, float* __restrict__ part_o, float* __restrict__ part_ml, int* __restrict__ arrivals,
+    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* status) {
   constexpr int NH = D / 64;
   constexpr uint32_t kHalf = BS * 128;
   constexpr uint32_t kTile = BS * D * 2;
-  constexpr int OPT = HPG * D / kDecThreads;  // output elements per thread
-  static_assert(OPT >= 1 && OPT <= 8 && (HPG * D) % kDecThreads == 0, "decode output mapping");
+  constexpr int kOut = HPG * D;  // outputs per (sequence, group)
+  constexpr int kPS = BS + 8;    // padded P row (bf16)
+  static_assert(HPG <= 8, "heads of a group must fit the N = 8 of one MMA");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* kt = smem;
   uint8_t* vt = kt + kTile;
-  float* qs = reinterpret_cast<float*>(vt + kTile);  // [HPG][D]
-  float* ps = qs + HPG * D;                          // [HPG][BS]
-  float* ml = ps + HPG * BS;                         // [HPG][2]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(ml + 2 * HPG);  // HPG*(D+BS+2) floats: 8-byte aligned
-  __shared__ int abort_s;
+  float* ss = reinterpret_cast<float*>(vt + kTile);                          // [HPG][BS] scores (log2 units)
+  __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(ss + HPG * BS);       // [HPG][kPS] probabilities
+  float* ml = reinterpret_cast<float*>(pb + HPG * kPS);                      // [HPG][2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(ml + 2 * HPG) + 15) & ~uintptr_t(15));
+  __shared__ int abort_s, last_s;
 
   const int item = blockIdx.x;  // (b, g, k)
   const int k = item % K;
-  const int g = (item / K) % G;
-  const int b = item / (K * G);
+  const int bg = item / K;
+  const int g = bg % G;
+  const int b = bg / G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
   const int L = kv_len[b];
   const int pos = L - 1;
-  const int t = sel[(int64_t(b) * G + g) * K + k];
+  const int t = sel[int64_t(bg) * K + k];
   const bool seq_ok = L >= 1 && L <= Lmax;
   const bool valid = seq_ok && t >= 0 && t < nblk && t * BS <= pos;
   if (tid == 0 && (!seq_ok || t < -1 || t >= nblk)) set_status(status, MSA_ERR_BOUNDS);
-  float* out_o = part_o + int64_t(item) * HPG * D;
+  float* out_o = part_o + int64_t(item) * kOut;
   float* out_ml = part_ml + int64_t(item) * HPG * 2;
-  if (!valid) {  // empty slot: contributes nothing to the combine
-    for (int x = tid; x < HPG * D; x += kDecThreads) out_o[x] = 0.f;
+
+  if (valid) {
+    if (tid == 0) {
+      abort_s = 0;
+      tc::mbar_init(&bars[0], 1);
+      tc::mbar_init(&bars[1], 1);
+      tc::fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0) {  // K and V on separate barriers: scores start while V is in flight
+      tc::mbar_arrive_expect_tx(&bars[0], kTile);
+      tc::mbar_arrive_expect_tx(&bars[1], kTile);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) tc::tma_load_4d(kt + h * kHalf, &tmK, &bars[0], h * 64, g, t * BS, b);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) tc::tma_load_4d(vt + h * kHalf, &tmV, &bars[1], h * 64, g, t * BS, b);
+    }
+    // q^T fragments (B operand of S^T = K q^T): column n = head gq, rows = head dims
+    uint32_t qf[D / 16][2];
+    {
+      const __nv_bfloat16* qh = q + (int64_t(b) * Hq + g * HPG + gq) * D;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        if (gq < HPG) {
+          qf[ks][0] = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 2 * tq);
+          qf[ks][1] = *reinterpret_cast<const uint32_t*>(qh + ks * 16 + 2 * tq + 8);
+        } else {
+          qf[ks][0] = qf[ks][1] = 0u;
+        }
+      }
+    }
+    const int nvalid = min(BS, pos - t * BS + 1);  // keys j <= pos in this block
+    bool ok = tc::mbar_wait(&bars[0], 0, &abort_s);
+    if (ok && warp < BS / 16) {
+      // S^T tile: keys [16 warp, 16 warp + 16) x heads
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t kbase = tc::smem_u32(kt);
+      const int row = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(swz_addr(kbase, kHalf, row, ks * 2 + (lane >> 4)), a0, a1, a2, a3);
+        mma_bf16_16816(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+      // acc: keys (gq, gq + 8) x heads (2 tq, 2 tq + 1)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = warp * 16 + gq + 8 * (e >> 1);
+        const int hh = 2 * tq + (e & 1);
+        if (hh < HPG) ss[hh * BS + key] = key < nvalid ? acc[e] * scale_log2 : -INFINITY;
+      }
+    }
+    __syncthreads();
+    if (ok) {
+      // block-local softmax per head (warp per head); P as bf16
+      for (int hh = warp; hh < HPG; hh += kDecThreads / 32) {
+        float m = -INFINITY;
+        for (int j = lane; j < BS; j += 32) m = fmaxf(m, ss[hh * BS + j]);
+        m = tc::warp_max_f32(m);
+        float l = 0.f;
+        for (int j = lane; j < BS; j += 32) {
+          const float e = j < nvalid ? ex2f(ss[hh * BS + j] - m) : 0.f;
+          pb[hh * kPS + j] = __float2bfloat16_rn(e);
+          l += e;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        if (lane == 0) {
+          ml[2 * hh] = m;
+          ml[2 * hh + 1] = l;
+        }
+      }
+    }
+    __syncthreads();
+    if (ok) ok = tc::mbar_wait(&bars[1], 0, &abort_s);
+    if (ok) {
+      // O^T tile: head dims [16 warp, 16 warp + 16) x heads, over all keys
+      if (warp < D / 16) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t vbase = tc::smem_u32(vt);
+        const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+        for (int ks = 0; ks < BS / 16; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          const int key = ks * 16 + r8 + 8 * (mi >> 1);
+          ldsm_x4_t(swz_addr(vbase, kHalf, key, warp * 2 + (mi & 1)), a0, a1, a2, a3);
+          uint32_t b0 = 0u, b1 = 0u;
+          if (gq < HPG) {
+            b0 = *reinterpret_cast<const uint32_t*>(pb + gq * kPS + ks * 16 + 2 * tq);
+            b1 = *reinterpret_cast<const uint32_t*>(pb + gq * kPS + ks * 16 + 2 * tq + 8);
+          }
+          mma_bf16_16816(acc, a0, a1, a2, a3, b0, b1);
+        }
+        // acc: head dims (gq, gq + 8) x heads (2 tq, 2 tq + 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = warp * 16 + gq + 8 * (e >> 1);
+          const int hh = 2 * tq + (e & 1);
+          if (hh < HPG) out_o[hh * D + c] = acc[e];
+        }
+      }
+      if (tid < HPG) {
+        out_ml[2 * tid] = ml[2 * tid];
+        out_ml[2 * tid + 1] = ml[2 * tid + 1];
+      }
+    } else {
+      if (tid == 0) set_status(status, MSA_ERR_TIMEOUT);
+      int zero = 0;  // copies may still land: wait (bounded) before the CTA gives up its smem
+      tc::mbar_wait(&bars[0], 0, &zero);
+      tc::mbar_wait(&bars[1], 0, &zero);
+    }
+  } else {  // empty slot: contributes nothing to the merge
+    for (int x = tid; x < kOut; x += kDecThreads) out_o[x] = 0.f;
     if (tid < HPG) {
       out_ml[2 * tid] = -INFINITY;
       out_ml[2 * tid + 1] = 0.f;
     }
-    return;
   }
-  if (tid == 0) {
-    abort_s = 0;
-    tc::mbar_init(bar, 1);
-    tc::fence_barrier_init();
-  }
+  // ---- the last of the K slot CTAs of (b, g) merges the partials ----
+  __threadfence();
   __syncthreads();
   if (tid == 0) {
-    tc::mbar_arrive_expect_tx(bar, 2 * kTile);
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      tc::tma_load_4d(kt + h * kHalf, &tmK, bar, h * 64, g, t * BS, b);
-      tc::tma_load_4d(vt + h * kHalf, &tmV, bar, h * 64, g, t * BS, b);
-    }
-  }
-  // the group's query heads, pre-scaled so that exp2 gives the softmax
-  for (int x = tid; x < HPG * D; x += kDecThreads) {
-    const int hh = x / D, c = x % D;
-    qs[x] = __bfloat162float(q[(int64_t(b) * Hq + g * HPG + hh) * D + c]) * scale_log2;
+    const int old = atomicAdd(&arrivals[bg], 1);
+    last_s = old == K - 1;
   }
   __syncthreads();
-  if (!tc::mbar_wait(bar, 0, &abort_s)) {
-    set_status(status, MSA_ERR_TIMEOUT);
-    // a copy may still land: wait (bounded) before the CTA gives up its smem
-    int zero = 0;
-    tc::mbar_wait(bar, 0, &zero);
-    return;
-  }
-  const int nvalid = min(BS, pos - t * BS + 1);  // keys j <= pos in this block
-
-  // scores: thread j owns key j (its K row: 16-byte chunks, swizzle-permuted)
-  for (int j = tid; j < BS; j += kDecThreads) {
-    float s[HPG];
-#pragma unroll
-    for (int hh = 0; hh < HPG; ++hh) s[hh] = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < D / 8; ++ch) {
-      const int hf = ch >> 3, cc = ch & 7;
-      const uint4 raw = *reinterpret_cast<const uint4*>(kt + hf * kHalf + j * 128 + ((cc ^ (j & 7)) << 4));
-      const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-      float kf[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(k2[e]);
-        kf[2 * e] = f.x;
-        kf[2 * e + 1] = f.y;
-      }
-#pragma unroll
-      for (int hh = 0; hh < HPG; ++hh) {
-        const float4 qa = *reinterpret_cast<const float4*>(qs + hh * D + ch * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(qs + hh * D + ch * 8 + 4);
-        s[hh] = fmaf(qa.x, kf[0], s[hh]);
-        s[hh] = fmaf(qa.y, kf[1], s[hh]);
-        s[hh] = fmaf(qa.z, kf[2], s[hh]);
-        s[hh] = fmaf(qa.w, kf[3], s[hh]);
-        s[hh] = fmaf(qb.x, kf[4], s[hh]);
-        s[hh] = fmaf(qb.y, kf[5], s[hh]);
-        s[hh] = fmaf(qb.z, kf[6], s[hh]);
-        s[hh] = fmaf(qb.w, kf[7], s[hh]);
+  if (!last_s) return;
+  __threadfence();
+  if (tid == 0) arrivals[bg] = 0;  // ready for the next call
+  const float* po = part_o + int64_t(bg) * K * kOut;
+  const float* pm = part_ml + int64_t(bg) * K * HPG * 2;
+  for (int o = tid; o < kOut; o += kDecThreads) {
+    const int hh = o / D, c = o % D;
+    float M = -INFINITY;
+    for (int kk = 0; kk < K; ++kk) M = fmaxf(M, __ldcg(pm + (kk * HPG + hh) * 2));
+    float acc = 0.f, den = 0.f;
+    if (M > -INFINITY) {
+      for (int kk = 0; kk < K; ++kk) {
+        const float w = ex2f(__ldcg(pm + (kk * HPG + hh) * 2) - M);  // 0 for empty slots
+        den = fmaf(w, __ldcg(pm + (kk * HPG + hh) * 2 + 1), den);
+        acc = fmaf(w, __ldcg(po + int64_t(kk) * kOut + o), acc);
       }
     }
-#pragma unroll
-    for (int hh = 0; hh < HPG; ++hh) ps[hh * BS + j] = j < nvalid ? s[hh] : -INFINITY;
-  }
-  __syncthreads();
-  // block-local softmax per head (warp per head)
-  for (int hh = warp; hh < HPG; hh += kDecThreads / 32) {
-    float m = -INFINITY;
-    for (int j = lane; j < BS; j += 32) m = fmaxf(m, ps[hh * BS + j]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float l = 0.f;
-    for (int j = lane; j < BS; j += 32) {
-      const float e = j < nvalid ? ex2f(ps[hh * BS + j] - m) : 0.f;
-      ps[hh * BS + j] = e;
-      l += e;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    if (lane == 0) {
-      ml[2 * hh] = m;
-      ml[2 * hh + 1] = l;
-    }
-  }
-  __syncthreads();
-  // O[h][c] = sum_j P[h][j] V[j][c]: thread -> (head, OPT consecutive columns)
-  {
-    const int o0 = tid * OPT;
-    const int hh = o0 / D, c0 = o0 % D;
-    const int ch = c0 >> 3, hf = ch >> 3, cc = ch & 7, within = (c0 & 7) * 2;
-    float acc[OPT];
-#pragma unroll
-    for (int x = 0; x < OPT; ++x) acc[x] = 0.f;
-    const float* prow = ps + hh * BS;
-    for (int j = 0; j < nvalid; ++j) {
-      const float pj = prow[j];
-      const uint8_t* src = vt + hf * kHalf + j * 128 + ((cc ^ (j & 7)) << 4) + within;
-      if constexpr (OPT == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(src);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        acc[0] = fmaf(pj, a.x, acc[0]);
-        acc[1] = fmaf(pj, a.y, acc[1]);
-        acc[2] = fmaf(pj, c.x, acc[2]);
-        acc[3] = fmaf(pj, c.y, acc[3]);
-      } else {
-        const __nv_bfloat16* v16 = reinterpret_cast<const __nv_bfloat16*>(src);
-#pragma unroll
-        for (int x = 0; x < OPT; ++x) acc[x] = fmaf(pj, __bfloat162float(v16[x]), acc[x]);
-      }
-    }
-#pragma unroll
-    for (int x = 0; x < OPT; ++x) out_o[o0 + x] = acc[x];
-  }
-  if (tid < HPG) {
-    out_ml[2 * tid] = ml[2 * tid];
-    out_ml[2 * tid + 1] = ml[2 * tid + 1];
+    const int h = g * HPG + hh;
+    out[(int64_t(b) * Hq + h) * D + c] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
+    if (lse && c == 0) lse[int64_t(b) * Hq + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
   }
 }
 
-// one warp per (sequence, query head); lanes own D/32 output columns
-template <int D>
-__global__ void decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml, int B,
-                                      int Hq, int G, int K, __nv_bfloat16* __restrict__ out,
-                                      float* __restrict__ lse) {
-  constexpr int U = D / 32;
-  const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= int64_t(B) * Hq) return;
-  const int b = int(wid / Hq), h = int(wid % Hq);
-  const int hpg = Hq / G, g = h / hpg, hh = h % hpg;
-  const int64_t item0 = (int64_t(b) * G + g) * K;
-  float M = -INFINITY;
-  for (int k = 0; k < K; ++k) M = fmaxf(M, part_ml[((item0 + k) * hpg + hh) * 2]);
-  float acc[U], den = 0.f;
-#pragma unroll
-  for (int u = 0; u < U; ++u) acc[u] = 0.f;
-  if (M > -INFINITY) {
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-      const float* mlk = part_ml + ((item0 + k) * hpg + hh) * 2;
-      const float w = ex2f(mlk[0] - M);  // 0 for empty slots (max -inf)
-      den = fmaf(w, mlk[1], den);
-      const float* ok = part_o + ((item0 + k) * hpg + hh) * D;
-#pragma unroll
-      for (int u = 0; u < U; ++u) acc[u] = fmaf(w, ok[lane + 32 * u], acc[u]);
-    }
-  }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  __nv_bfloat16* dst = out + (int64_t(b) * Hq + h) * D;
-#pragma unroll
-  for (int u = 0; u < U; ++u) dst[lane + 32 * u] = __float2bfloat16_rn(acc[u] * inv);
-  if (lse && lane == 0) lse[int64_t(b) * Hq + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+size_t dec_smem_bytes(int d, int Bs, int hpg) {
+  return 1024 + size_t(2) * Bs * d * 2 + size_t(hpg) * Bs * 4 + size_t(hpg) * (Bs + 8) * 2 + size_t(hpg) * 8 + 16 +
+         32;
 }
 
 // ---------------------------------------------------------------------------
-// decode_index: persistent; tiles = (sequence, 128-key tile) in sequence order
+// decode_index: persistent; tiles = (sequence, 128-key tile) in sequence order.
+// Warps: 0 TMA, 1 MMA + TMEM owner, 2-9 two epilogue warpgroups that take
+// alternate tiles (4 TMEM accumulators of 32 columns). Each warp reduces its
+// 32 keys per index-query head with one redux and writes the 32-key sub-block
+// maximum; the top-K pass assembles block maxima from those.
 // ---------------------------------------------------------------------------
-constexpr int kDiThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kDiThreads = 320;
 constexpr int kDiStages = 8;
 constexpr int kDiMaxB = 4096;
+constexpr int kDiAcc = 4;
 constexpr uint32_t kDiA = 128 * 64 * 2;  // 128 keys x 64 (bf16)
 constexpr uint32_t kDiB = 16 * 64 * 2;   // 16 index-query rows (G <= 16, padded)
 constexpr uint32_t kDiStage = kDiA + kDiB;
 
-template <int BS>
 __global__ void __launch_bounds__(kDiThreads, 1)
     decode_index_kernel(const __grid_constant__ CUtensorMap tmIK, const __grid_constant__ CUtensorMap tmIQ,
                         const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len, int B, int Lmax,
-                        int G, int nblk, float* __restrict__ table, uint32_t* status) {
+                        int G, int nsub, float* __restrict__ sub_max, uint32_t* status) {
   constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, 16);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* stages = smem;                                              // kDiStages x (A | B)
   int* prefix = reinterpret_cast<int*>(stages + kDiStages * kDiStage);  // [B + 1] tile prefix
-  float* red = reinterpret_cast<float*>(prefix + kDiMaxB + 1);          // [2][4][16]
-  // mbarriers need 8-byte alignment (the prefix array has an odd length): round up
-  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(red + 2 * 4 * 16) + 15) & ~uintptr_t(15));
+  int* qpos = prefix + kDiMaxB + 1;                                     // [B] query position
+  // mbarriers need 8-byte alignment: round up past the int arrays
+  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(qpos + kDiMaxB) + 15) & ~uintptr_t(15));
   uint64_t* full = bars;
   uint64_t* empty = full + kDiStages;
   uint64_t* acc_full = empty + kDiStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* done_bar = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + kDiAcc;
+  uint64_t* done_bar = acc_empty + kDiAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // tile prefix over sequences (every CTA builds its own copy)
+  __shared__ int scan_part[kDiThreads];
   if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int b = 0; b < B; ++b) {  // tiles cover keys 0..pos of each sequence
-      prefix[b] = acc;
-      const SeqView sv = seq_view(q_offset, kv_len, b, 1, Lmax, false);
-      if (!sv.ok) set_status(status, MSA_ERR_BOUNDS);
-      acc += sv.ok ? sv.q0 / 128 + 1 : 0;
-    }
-    prefix[B] = acc;
     for (int s = 0; s < kDiStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kDiAcc; ++a) {
       tc::mbar_init(&acc_full[a], 1);
       tc::mbar_init(&acc_empty[a], 4);
     }
@@ -291,8 +322,40 @@ __global__ void __launch_bounds__(kDiThreads, 1)
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
+  // per-sequence tile counts (tiles cover keys 0..pos), then their prefix
+  for (int b = threadIdx.x; b < B; b += kDiThreads) {
+    const SeqView sv = seq_view(q_offset, kv_len, b, 1, Lmax, false);
+    if (!sv.ok) set_status(status, MSA_ERR_BOUNDS);
+    qpos[b] = sv.ok ? sv.q0 : -1;
+    prefix[b] = sv.ok ? sv.q0 / 128 + 1 : 0;
+  }
+  __syncthreads();
+  {
+    const int per = (B + kDiThreads - 1) / kDiThreads;
+    const int lo = min(B, int(threadIdx.x) * per), hi = min(B, lo + per);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) local += prefix[b];
+    scan_part[threadIdx.x] = local;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int i = 0; i < kDiThreads; ++i) {
+        const int v = scan_part[i];
+        scan_part[i] = run;
+        run += v;
+      }
+      prefix[B] = run;
+    }
+    __syncthreads();
+    int base = scan_part[threadIdx.x];
+    for (int b = lo; b < hi; ++b) {
+      const int c = prefix[b];
+      prefix[b] = base;
+      base += c;
+    }
+  }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 64);
+    tc::tmem_alloc(tmem_slot, 128);
     tc::tmem_relinquish();
   }
   __syncthreads();
@@ -340,9 +403,9 @@ __global__ void __launch_bounds__(kDiThreads, 1)
     if (lane == 0) {
       int n = 0;
       for (int x = x0; x < x1; ++x, ++n) {
-        const int s = n % kDiStages, a = n & 1;
+        const int s = n % kDiStages, a = n % kDiAcc;
         if (!tc::mbar_wait(&full[s], (n / kDiStages) & 1, abort_flag) ||
-            !tc::mbar_wait(&acc_empty[a], ((n >> 1) & 1) ^ 1, abort_flag)) {
+            !tc::mbar_wait(&acc_empty[a], ((n / kDiAcc) & 1) ^ 1, abort_flag)) {
           fail();
           break;
         }
@@ -362,15 +425,14 @@ __global__ void __launch_bounds__(kDiThreads, 1)
       tc::mbar_wait(done_bar, 0, &zero);
     }
   } else {
-    // epilogue: thread = key row of the tile (TMEM lane)
-    const int q = warp & 3;  // lane quarter
-    const int etid = (warp - 2) * 32 + lane;
-    int n = 0;
-    for (int x = x0; x < x1; ++x, ++n) {
+    // epilogue: warpgroup w takes tiles n = w, w + 2, ...; thread = key row
+    const int w = (warp - 2) >> 2;
+    const int q = warp & 3;  // TMEM lane quarter
+    for (int n = w; x0 + n < x1; n += 2) {
       int b, kt;
-      locate(x, b, kt);
-      const int a = n & 1;
-      if (!tc::mbar_wait(&acc_full[a], (n >> 1) & 1, abort_flag)) {
+      locate(x0 + n, b, kt);
+      const int a = n % kDiAcc;
+      if (!tc::mbar_wait(&acc_full[a], (n / kDiAcc) & 1, abort_flag)) {
         fail();
         break;
       }
@@ -381,50 +443,67 @@ __global__ void __launch_bounds__(kDiThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
-      const int j = kt * 128 + q * 32 + lane;
-      const bool vis = j <= (q_offset ? q_offset[b] : 0);  // causal: keys up to the query's position
-      float* rbuf = red + (n & 1) * 64;
+      const int sblk = kt * 4 + q;           // 32-key sub-block of this warp
+      const bool vis = sblk * 32 + lane <= qpos[b];
+      float* dst = sub_max + int64_t(b) * G * nsub + sblk;
 #pragma unroll
       for (int g = 0; g < 16; ++g) {
         if (g < G) {
           const float m = tc::warp_max_f32(vis ? __uint_as_float(v[g]) : -INFINITY);
-          if (lane == g) rbuf[q * 16 + g] = m;
+          if (lane == g && sblk < nsub) dst[int64_t(g) * nsub] = m;
         }
-      }
-      tc::named_bar_sync(1, 128);
-      constexpr int kWarpsPerBlock = BS / 32, kBlocksPerTile = 128 / BS;
-      if (etid < G * kBlocksPerTile) {
-        const int bi = etid / G, g = etid % G;
-        float m = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarpsPerBlock; ++w) m = fmaxf(m, rbuf[(bi * kWarpsPerBlock + w) * 16 + g]);
-        const int t = kt * kBlocksPerTile + bi;
-        if (t < nblk) table[(int64_t(b) * G + g) * nblk + t] = m;
       }
     }
   }
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 64);
+    tc::tmem_dealloc(tmem, 128);
   }
 }
 
 // ---------------------------------------------------------------------------
-// decode_topk: one CTA per (sequence, group). Candidates are blocks t < loc
-// keyed by (block max, -t) as one unsigned 64-bit value; the (K-1)-th largest
-// key is found bit by bit with block-wide counts, the selected blocks are
-// compacted in ascending t, and loc is appended.
+// decode_topk: one CTA per (sequence, group). Block maxima of the candidates
+// t < loc are assembled from the 32-key sub-block maxima and cached in shared
+// memory as order-preserving 32-bit values. The (K-1)-th largest value v* is
+// found two bits per round with block-wide counts; then every candidate above
+// v* is selected, plus the lowest-t candidates equal to v* until K-1 are
+// chosen (ties go to the lower block). Selected blocks are compacted in
+// ascending t and the local block is appended.
 // ---------------------------------------------------------------------------
 constexpr int kTkThreads = 256;
+constexpr int kTkMaxCand = 16384;
 
-__global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __restrict__ table,
+__device__ __forceinline__ uint32_t ord_f32(float m) {
+  uint32_t u = __float_as_uint(m);
+  if (u == 0x80000000u) u = 0u;  // -0 == +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// exclusive block-wide scan of one int per thread (kTkThreads threads)
+__device__ __forceinline__ int block_exclusive_scan(int v, int* buf) {
+  const int tid = threadIdx.x;
+  buf[tid] = v;
+  __syncthreads();
+  for (int off = 1; off < kTkThreads; off <<= 1) {
+    const int x = tid >= off ? buf[tid - off] : 0;
+    __syncthreads();
+    buf[tid] += x;
+    __syncthreads();
+  }
+  const int incl = buf[tid];
+  __syncthreads();
+  return incl - v;
+}
+
+__global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __restrict__ sub_max,
                                                                  const int32_t* __restrict__ q_offset,
                                                                  const int32_t* __restrict__ kv_len, int Lmax, int G,
-                                                                 int Bs, int K, int nblk, int32_t* __restrict__ sel,
+                                                                 int Bs, int K, int nsub, int32_t* __restrict__ sel,
                                                                  uint32_t* status) {
-  __shared__ int wsum[2][kTkThreads / 32];
-  __shared__ int scan_s[kTkThreads];
+  extern __shared__ uint32_t vals[];  // [loc] order-preserving block maxima
+  __shared__ int wsum[2][kTkThreads / 32][3];
+  __shared__ int scan_buf[kTkThreads];
   const int row = blockIdx.x;  // b * G + g
   const int b = row / G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -440,62 +519,81 @@ __global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __
     for (int k = tid; k < K; k += kTkThreads) out[k] = k <= loc ? k : -1;
     return;
   }
-  const float* M = table + int64_t(row) * nblk;
+  const int R = Bs / 32;  // sub-blocks per block
+  const float* sm = sub_max + int64_t(row) * nsub;
   const int per = (loc + kTkThreads - 1) / kTkThreads;  // contiguous candidates per thread
   const int t0 = min(loc, tid * per), t1 = min(loc, t0 + per);
+  for (int t = t0; t < t1; ++t) {
+    float m = sm[t * R];
+    for (int r = 1; r < R; ++r) m = fmaxf(m, sm[t * R + r]);
+    vals[t] = ord_f32(m);
+  }
   const int need = K - 1;
-  uint64_t prefix = 0;
-  for (int bit = 63; bit >= 0; --bit) {
-    const uint64_t cand = prefix | (uint64_t(1) << bit);
-    int c = 0;
-    for (int t = t0; t < t1; ++t) c += rank_key(M[t], t) >= cand;
-    c = __reduce_add_sync(0xffffffffu, c);
-    const int par = bit & 1;
-    if (lane == 0) wsum[par][warp] = c;
-    __syncthreads();
-    int total = 0;
+  uint32_t prefix = 0;
+  for (int round = 0; round < 16; ++round) {
+    const int sh = 30 - 2 * round;
+    int c[3] = {0, 0, 0};
+    for (int t = t0; t < t1; ++t) {
+      const uint32_t v = vals[t];
 #pragma unroll
-    for (int w = 0; w < kTkThreads / 32; ++w) total += wsum[par][w];
-    if (total >= need) prefix = cand;  // the need-th largest key is >= cand
-  }
-  // keys >= prefix are exactly the top K-1 (keys are unique)
-  int c = 0;
-  for (int t = t0; t < t1; ++t) c += rank_key(M[t], t) >= prefix;
-  scan_s[tid] = c;
-  __syncthreads();
-  for (int off = 1; off < kTkThreads; off <<= 1) {
-    const int v = tid >= off ? scan_s[tid - off] : 0;
+      for (int x = 0; x < 3; ++x) c[x] += v >= (prefix | (uint32_t(x + 1) << sh));
+    }
+    const int par = round & 1;
+#pragma unroll
+    for (int x = 0; x < 3; ++x) {
+      const int w = __reduce_add_sync(0xffffffffu, c[x]);
+      if (lane == 0) wsum[par][warp][x] = w;
+    }
     __syncthreads();
-    scan_s[tid] += v;
-    __syncthreads();
+    int best = 0;
+#pragma unroll
+    for (int x = 0; x < 3; ++x) {
+      int total = 0;
+#pragma unroll
+      for (int w = 0; w < kTkThreads / 32; ++w) total += wsum[par][w][x];
+      if (total >= need) best = x + 1;  // counts fall as the candidate grows
+    }
+    prefix |= uint32_t(best) << sh;
   }
-  int o = scan_s[tid] - c;
-  for (int t = t0; t < t1; ++t)
-    if (rank_key(M[t], t) >= prefix) out[o++] = t;
+  // prefix = v*, the need-th largest value
+  int gt = 0, eq = 0;
+  for (int t = t0; t < t1; ++t) {
+    gt += vals[t] > prefix;
+    eq += vals[t] == prefix;
+  }
+  const int gt_total = block_exclusive_scan(gt, scan_buf) + gt;  // inclusive for the last thread only
+  __shared__ int gt_all;
+  if (tid == kTkThreads - 1) gt_all = gt_total;
+  const int eq_before = block_exclusive_scan(eq, scan_buf);
+  const int ties = need - gt_all;
+  const int take_eq = max(0, min(eq, ties - eq_before));  // the lowest-t equals go first
+  const int my = gt + take_eq;
+  int o = block_exclusive_scan(my, scan_buf);
+  int eq_seen = 0;
+  for (int t = t0; t < t1; ++t) {
+    const uint32_t v = vals[t];
+    if (v > prefix || (v == prefix && eq_seen++ < take_eq)) out[o++] = t;
+  }
   if (tid == 0) out[K - 1] = loc;
-}
-
-size_t dec_smem_bytes(int d, int Bs, int hpg) {
-  return 1024 + size_t(2) * Bs * d * 2 + size_t(hpg) * d * 4 + size_t(hpg) * Bs * 4 + size_t(hpg) * 8 + 64;
 }
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
 bool decode_attn_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K) {
   if (dtype != MSA_BF16 || (d != 64 && d != 128)) return false;
   if (Bs != 32 && Bs != 64 && Bs != 128) return false;
   if (K < 1 || K > kMaxK || Hq % Hkv != 0) return false;
   const int hpg = Hq / Hkv;
   if (hpg != 1 && hpg != 2 && hpg != 4 && hpg != 8) return false;
-  if ((hpg * d) % kDecThreads != 0 || hpg * d / kDecThreads > 8) return false;
   return dec_smem_bytes(d, Bs, hpg) <= 227 * 1024;
 }
 
+static size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
 size_t decode_ws_bytes(int B, int Hq, int Hkv, int d, int K) {
   const size_t items = size_t(B) * Hkv * K, hpg = size_t(Hq / Hkv);
-  const size_t o = (items * hpg * d * 4 + 255) & ~size_t(255);
-  const size_t m = (items * hpg * 2 * 4 + 255) & ~size_t(255);
-  return o + m;
+  return a256(items * hpg * d * 4) + a256(items * hpg * 2 * 4) + a256(size_t(B) * Hkv * 4);
 }
 
 cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v_cache, const int32_t* sel,
@@ -504,9 +602,10 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
                                cudaStream_t stream) {
   const int G = Hkv, hpg = Hq / Hkv, nblk = (Lmax + Bs - 1) / Bs;
   const size_t items = size_t(B) * G * K;
-  float* part_o = static_cast<float*>(scratch);
-  float* part_ml =
-      reinterpret_cast<float*>(static_cast<char*>(scratch) + ((items * hpg * d * 4 + 255) & ~size_t(255)));
+  char* sc = static_cast<char*>(scratch);
+  float* part_o = reinterpret_cast<float*>(sc);
+  float* part_ml = reinterpret_cast<float*>(sc + a256(items * hpg * d * 4));
+  int* arrivals = reinterpret_cast<int*>(sc + a256(items * hpg * d * 4) + a256(items * hpg * 2 * 4));
   CUtensorMap tmK, tmV;
   const uint64_t dims[4] = {uint64_t(d), uint64_t(Hkv), uint64_t(Lmax), uint64_t(B)};
   const uint64_t strides[3] = {uint64_t(d) * 2, uint64_t(Hkv) * d * 2, uint64_t(Lmax) * Hkv * d * 2};
@@ -517,8 +616,7 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
   const size_t smem = dec_smem_bytes(d, Bs, hpg);
   const float scale_log2 = scale * kLog2eD;
   cudaError_t e;
-  {
-    ProfScope pf("decode_attn", stream);
+  ProfScope pf("decode_attn", stream);
 #define MSA_DEC(D_, BS_, HPG_)                                                                                   \
   do {                                                                                                           \
     auto kern = decode_attn_kernel<D_, BS_, HPG_>;                                                              \
@@ -526,49 +624,39 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
       return e;                                                                                                  \
     kern<<<unsigned(items), kDecThreads, smem, stream>>>(tmK, tmV, static_cast<const __nv_bfloat16*>(q), sel,     \
                                                          kv_len, Lmax, Hq, G, K, nblk, scale_log2, part_o,        \
-                                                         part_ml, status);                                        \
+                                                         part_ml, arrivals, static_cast<__nv_bfloat16*>(out),     \
+                                                         lse, status);                                            \
   } while (0)
-#define MSA_DEC_BS(D_, HPG_)      \
-  do {                            \
-    if (Bs == 128)                \
-      MSA_DEC(D_, 128, HPG_);     \
-    else if (Bs == 64)            \
-      MSA_DEC(D_, 64, HPG_);      \
-    else                          \
-      MSA_DEC(D_, 32, HPG_);      \
+#define MSA_DEC_BS(D_, HPG_)  \
+  do {                        \
+    if (Bs == 128)            \
+      MSA_DEC(D_, 128, HPG_); \
+    else if (Bs == 64)        \
+      MSA_DEC(D_, 64, HPG_);  \
+    else                      \
+      MSA_DEC(D_, 32, HPG_);  \
   } while (0)
-    if (d == 128) {
-      if (hpg == 4)
-        MSA_DEC_BS(128, 4);
-      else if (hpg == 8)
-        MSA_DEC_BS(128, 8);
-      else if (hpg == 2)
-        MSA_DEC_BS(128, 2);
-      else
-        MSA_DEC_BS(128, 1);
-    } else {
-      if (hpg == 4)
-        MSA_DEC_BS(64, 4);
-      else if (hpg == 8)
-        MSA_DEC_BS(64, 8);
-      else
-        MSA_DEC_BS(64, 2);
-    }
+  if (d == 128) {
+    if (hpg == 4)
+      MSA_DEC_BS(128, 4);
+    else if (hpg == 8)
+      MSA_DEC_BS(128, 8);
+    else if (hpg == 2)
+      MSA_DEC_BS(128, 2);
+    else
+      MSA_DEC_BS(128, 1);
+  } else {
+    if (hpg == 4)
+      MSA_DEC_BS(64, 4);
+    else if (hpg == 8)
+      MSA_DEC_BS(64, 8);
+    else if (hpg == 2)
+      MSA_DEC_BS(64, 2);
+    else
+      MSA_DEC_BS(64, 1);
+  }
 #undef MSA_DEC_BS
 #undef MSA_DEC
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  {
-    ProfScope pf("decode_combine", stream);
-    const int64_t warps = int64_t(B) * Hq;
-    const unsigned grid = unsigned((warps * 32 + 255) / 256);
-    if (d == 128)
-      decode_combine_kernel<128><<<grid, 256, 0, stream>>>(part_o, part_ml, B, Hq, G, K,
-                                                          static_cast<__nv_bfloat16*>(out), lse);
-    else
-      decode_combine_kernel<64><<<grid, 256, 0, stream>>>(part_o, part_ml, B, Hq, G, K,
-                                                         static_cast<__nv_bfloat16*>(out), lse);
-  }
   return cudaGetLastError();
 }
 
@@ -577,14 +665,14 @@ bool decode_index_supported(int dtype, int B, int Nq, int G, int di, int Bs, int
          (Bs == 32 || Bs == 64 || Bs == 128) && K >= 1 && K <= kMaxK;
 }
 
-size_t decode_index_ws_bytes(int B, int G, int Nk, int Bs) {
-  return size_t(B) * G * ((Nk + Bs - 1) / Bs) * sizeof(float);
-}
+size_t decode_index_ws_bytes(int B, int G, int Nk) { return size_t(B) * G * ((Nk + 31) / 32) * sizeof(float); }
 
 cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
                                 int Lmax, int G, int Bs, int K, int32_t* sel, float* table, uint32_t* status,
                                 cudaStream_t stream) {
+  const int nsub = (Lmax + 31) / 32;
   const int nblk = (Lmax + Bs - 1) / Bs;
+  if (nblk > kTkMaxCand) return cudaErrorInvalidValue;
   CUtensorMap tmIK, tmIQ;
   {
     const uint64_t dims[3] = {64, uint64_t(Lmax), uint64_t(B)};
@@ -598,33 +686,30 @@ cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q
     const uint32_t box[3] = {64, 16, 1};
     if (!make_tmap_bf16(&tmIQ, iq, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   }
-  const size_t smem = 1024 + size_t(kDiStages) * kDiStage + (kDiMaxB + 1) * 4 + 2 * 4 * 16 * 4 + 16 +
-                      (2 * kDiStages + 5) * 8 + 16;
+  const size_t smem = 1024 + size_t(kDiStages) * kDiStage + (2 * kDiMaxB + 1) * 4 + 16 +
+                      (2 * kDiStages + 2 * kDiAcc + 1) * 8 + 16;
   int dev = 0, sms = kNumSMs;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaError_t e;
   {
     ProfScope pf("decode_index", stream);
-#define MSA_DI(BS_)                                                                                              \
-  do {                                                                                                           \
-    auto kern = decode_index_kernel<BS_>;                                                                       \
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess) \
-      return e;                                                                                                  \
-    kern<<<sms, kDiThreads, smem, stream>>>(tmIK, tmIQ, q_offset, kv_len, B, Lmax, G, nblk, table, status);     \
-  } while (0)
-    if (Bs == 128)
-      MSA_DI(128);
-    else if (Bs == 64)
-      MSA_DI(64);
-    else
-      MSA_DI(32);
-#undef MSA_DI
+    if ((e = cudaFuncSetAttribute(decode_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
+        cudaSuccess)
+      return e;
+    decode_index_kernel<<<sms, kDiThreads, smem, stream>>>(tmIK, tmIQ, q_offset, kv_len, B, Lmax, G, nsub, table,
+                                                           status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
     ProfScope pf("decode_topk", stream);
-    decode_topk_kernel<<<B * G, kTkThreads, 0, stream>>>(table, q_offset, kv_len, Lmax, G, Bs, K, nblk, sel, status);
+    const size_t tk_smem = size_t(nblk) * 4;
+    if (tk_smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(decode_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tk_smem))) !=
+            cudaSuccess)
+      return e;
+    decode_topk_kernel<<<B * G, kTkThreads, tk_smem, stream>>>(table, q_offset, kv_len, Lmax, G, Bs, K, nsub, sel,
+                                                               status);
   }
   return cudaGetLastError();
 }

@@ -1,5 +1,6 @@
 // C ABI of the MSA forward path: host-side validation, workspace planning and
 // dispatch to the kernels. Every entry point is asynchronous on its stream.
+#include <algorithm>
 #include <cstring>
 
 #include "msa_internal.cuh"
@@ -33,7 +34,9 @@ IndexPlan plan_index(int B, int Nq, int Nk, int G, int di, int Bs, int K, int dt
     return p;
   }
   const int nblk = (Nk + Bs - 1) / Bs;
-  const size_t table = size_t(B) * Nq * G * nblk * sizeof(float);
+  size_t table = size_t(B) * Nq * G * nblk * sizeof(float);
+  // the one-query (decode) path keeps 32-key sub-block maxima instead
+  if (decode_index_supported(dtype, B, Nq, G, di, Bs, K)) table = std::max(table, decode_index_ws_bytes(B, G, Nk));
   p.fused = index_fused_supported(dtype, Nq, G, di, Bs, K);
   p.table_off = kWsHeader;
   p.table_bytes = (have_block_max || p.fused) ? 0 : align256(table);

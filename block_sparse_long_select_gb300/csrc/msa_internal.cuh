@@ -104,6 +104,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
 // Index Branch for one query per sequence (decode): tcgen05 stream of the
 // index-key cache into a [B, G, nblk] block-max table, then exact top-K.
 bool decode_index_supported(int dtype, int B, int Nq, int G, int di, int Bs, int K);
+size_t decode_index_ws_bytes(int B, int G, int Nk);
 cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
                                 int Lmax, int G, int Bs, int K, int32_t* sel, float* table, uint32_t* status,
                                 cudaStream_t stream);
