@@ -279,8 +279,8 @@ size_t dec_smem_bytes(int d, int Bs, int hpg) {
 // maximum; the top-K pass assembles block maxima from those.
 // ---------------------------------------------------------------------------
 constexpr int kDiThreads = 320;
-constexpr int kDiStages = 8;
-constexpr int kDiMaxB = 4096;
+constexpr int kDiStages = 12;
+constexpr int kDiMaxB = 1024;
 constexpr int kDiAcc = 4;
 constexpr uint32_t kDiA = 128 * 64 * 2;  // 128 keys x 64 (bf16)
 constexpr uint32_t kDiB = 16 * 64 * 2;   // 16 index-query rows (G <= 16, padded)
@@ -358,6 +358,10 @@ __global__ void __launch_bounds__(kDiThreads, 1)
     tc::tmem_alloc(tmem_slot, 128);
     tc::tmem_relinquish();
   }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch(&tmIK);
+    tc::tma_prefetch(&tmIQ);
+  }
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
@@ -373,6 +377,11 @@ __global__ void __launch_bounds__(kDiThreads, 1)
     b = lo;
     kt = x - prefix[lo];
   };
+  // tiles are visited in increasing order: advance the sequence cursor instead of searching
+  auto advance = [&](int x, int& b, int& kt) {
+    while (b + 1 < B && prefix[b + 1] <= x) ++b;
+    kt = x - prefix[b];
+  };
   auto fail = [&]() {
     *abort_flag = 1;
     set_status(status, MSA_ERR_TIMEOUT);
@@ -380,10 +389,10 @@ __global__ void __launch_bounds__(kDiThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
+      int issued = 0, b = 0, kt = 0;
+      if (x0 < x1) locate(x0, b, kt);
       for (int x = x0; x < x1; ++x, ++issued) {
-        int b, kt;
-        locate(x, b, kt);
+        advance(x, b, kt);
         const int s = issued % kDiStages;
         if (!tc::mbar_wait(&empty[s], ((issued / kDiStages) & 1) ^ 1, abort_flag)) {
           fail();
@@ -428,9 +437,10 @@ __global__ void __launch_bounds__(kDiThreads, 1)
     // epilogue: warpgroup w takes tiles n = w, w + 2, ...; thread = key row
     const int w = (warp - 2) >> 2;
     const int q = warp & 3;  // TMEM lane quarter
+    int b = 0, kt = 0;
+    if (x0 + w < x1) locate(x0 + w, b, kt);
     for (int n = w; x0 + n < x1; n += 2) {
-      int b, kt;
-      locate(x0 + n, b, kt);
+      advance(x0 + n, b, kt);
       const int a = n % kDiAcc;
       if (!tc::mbar_wait(&acc_full[a], (n / kDiAcc) & 1, abort_flag)) {
         fail();
@@ -446,13 +456,16 @@ __global__ void __launch_bounds__(kDiThreads, 1)
       const int sblk = kt * 4 + q;           // 32-key sub-block of this warp
       const bool vis = sblk * 32 + lane <= qpos[b];
       float* dst = sub_max + int64_t(b) * G * nsub + sblk;
+      // all warp reductions first (independent), then one store per lane
+      float mine = -INFINITY;
 #pragma unroll
       for (int g = 0; g < 16; ++g) {
-        if (g < G) {
+        if (g < G) {  // uniform: the padding columns are skipped
           const float m = tc::warp_max_f32(vis ? __uint_as_float(v[g]) : -INFINITY);
-          if (lane == g && sblk < nsub) dst[int64_t(g) * nsub] = m;
+          mine = lane == g ? m : mine;
         }
       }
+      if (lane < G && sblk < nsub) dst[int64_t(lane) * nsub] = mine;
     }
   }
   __syncthreads();

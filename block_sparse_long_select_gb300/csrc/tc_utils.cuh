@@ -216,7 +216,7 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // warp-wide maximum of a float (sm_100+)
 __device__ __forceinline__ float warp_max_f32(float x) {
   float y;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(x));
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(x));
   return y;
 }
 
