@@ -57,6 +57,8 @@ WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", B=1, Nq=512, Nk=512, Hq=8, Hkv=2, d=64, di=32, Bs=32, K=4,
                           dtype="fp32", idx_a=4),
     "prefill_8k": Workload("prefill_8k", B=1, Nq=8192, Nk=8192, Bs=128, K=16, **_P),
+    # a 32K-token prefill: inputs well above the L2 size, a few GB on the device (profiling captures)
+    "prefill_32k": Workload("prefill_32k", B=1, Nq=32768, Nk=32768, Bs=128, K=16, hot="first4", **_P),
     "prefill_128k_bs128": Workload("prefill_128k_bs128", B=1, Nq=131072, Nk=131072, Bs=128, K=16,
                                    hot="first4", **_P),
     "prefill_128k_bs64": Workload("prefill_128k_bs64", B=1, Nq=131072, Nk=131072, Bs=64, K=32,

@@ -101,10 +101,10 @@ def check_structure(sel, q_offset, kv_len, Bs, K):
     sel = sel.astype(np.int64)
     B, Nq, G, _ = sel.shape
     pos = np.asarray(q_offset)[:, None] + np.arange(Nq)[None, :]
-    loc = (pos // Bs)[:, :, None]
+    loc = (pos // Bs)[:, :, None, None]  # [B, Nq, 1, 1]
     valid = sel >= 0
     cnt = valid.sum(-1)
-    assert np.array_equal(cnt, np.minimum(K, loc + 1).repeat(G, axis=2)), "selection count"
+    assert np.array_equal(cnt, np.broadcast_to(np.minimum(K, loc[..., 0] + 1), cnt.shape)), "selection count"
     # -1 only at the tail
     assert np.all(np.diff(valid.astype(np.int8), axis=-1) <= 0), "padding not at the tail"
     s = np.where(valid, sel, np.iinfo(np.int64).max)
