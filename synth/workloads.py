@@ -67,6 +67,9 @@ WORKLOADS = {
                                   hot="first4", **_P),
     "decode_b64": Workload("decode_b64", B=64, Nq=1, Nk=131072, Bs=128, K=16,
                            kv_len_range=(32768, 131072), **_P),
+    # a reduced decode batch (caches of 32K, ~4 GB on the device) for profiling captures
+    "decode_b32_32k": Workload("decode_b32_32k", B=32, Nq=1, Nk=32768, Bs=128, K=16,
+                               kv_len_range=(8192, 32768), **_P),
     "prefill_1m": Workload("prefill_1m", B=1, Nq=1048576, Nk=1048576, Bs=128, K=16, hot="pct1", **_P),
 }
 
