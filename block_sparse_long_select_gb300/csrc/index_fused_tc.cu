@@ -34,7 +34,7 @@ namespace msa {
 namespace {
 
 constexpr int kUnitRows = 256;  // stacked (token, group) rows per work unit
-constexpr int kTileN = 128;     // keys per key tile
+constexpr int kTileN = 256;     // keys per key tile (N of each MMA)
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kProducerWarp = 8;
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSbo = DI == 64 ? 1024 : 512;   // 8-row swizzle atom
   constexpr uint32_t kSwz = DI == 64 ? 2 : 4;        // 128B / 64B swizzle
   constexpr int kKSteps = DI / 16;
-  constexpr int kBlocksPerTile = kTileN / BS;
+  constexpr int kChunk = 128;  // TMEM columns read per epilogue step (one load round)
   constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kTileN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -130,9 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&a_full[x], 1);
       tc::mbar_init(&a_empty[x], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      tc::mbar_init(&acc_full[a], 1);
-      tc::mbar_init(&acc_empty[a], kEpiWarps);
+    for (int m = 0; m < 2; ++m) {  // one accumulator per MMA tile of the unit
+      tc::mbar_init(&acc_full[m], 1);
+      tc::mbar_init(&acc_empty[m], kEpiWarps / 2);
     }
     tc::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -213,27 +213,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++jA;
         const uint32_t a_addr = tc::smem_u32(a_buf + size_t(x) * kABytes);
         for (int n = 0; n < U.nt; ++n, ++kB, ++kAcc) {
-          const int s = kB % S, a = kAcc & 1;
-          if (!tc::mbar_wait(&full[s], (kB / S) & 1, abort_flag) ||
-              !tc::mbar_wait(&acc_empty[a], ((kAcc >> 1) & 1) ^ 1, abort_flag)) {
+          const int s = kB % S;
+          if (!tc::mbar_wait(&full[s], (kB / S) & 1, abort_flag)) {
             fail();
             alive = false;
             break;
           }
-          tc::fence_after_sync();
           const uint32_t b_addr = tc::smem_u32(b_buf + size_t(s) * kBBytes);
+          // ping-pong: tile m's accumulator is drained by warpgroup m while the
+          // tensor core works on the other tile
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            const uint32_t d = tmem + uint32_t((a * 2 + m) * kTileN);
+            if (!tc::mbar_wait(&acc_empty[m], (kAcc & 1) ^ 1, abort_flag)) {
+              fail();
+              alive = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t d = tmem + uint32_t(m * kTileN);
 #pragma unroll
             for (int kk = 0; kk < kKSteps; ++kk) {
               const uint64_t ad = tc::smem_desc(a_addr + m * kATile + kk * 32, 16, kSbo, kSwz);
               const uint64_t bd = tc::smem_desc(b_addr + kk * 32, 16, kSbo, kSwz);
               tc::mma_f16_ss(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
             }
+            tc::mma_commit(&acc_full[m]);
           }
+          if (!alive) break;
           tc::mma_commit(&empty[s]);
-          tc::mma_commit(&acc_full[a]);
           if (n == U.nt - 1) tc::mma_commit(&a_empty[x]);
         }
       }
@@ -262,39 +269,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool cand_row = active && U.ok && !dense;
       int cnt = 0;
       uint64_t thr = 0;
+      auto offer = [&](int t, float mx) {  // candidate block t with maximum mx
+        if (t >= loc) return;
+        const uint64_t key = rank_key(mx, t);
+        if (cnt < Kc || key > thr) {
+          int p = cnt < Kc ? cnt++ : Kc - 1;
+          while (p > 0 && my_list[(p - 1) * kUnitRows] < key) {
+            my_list[p * kUnitRows] = my_list[(p - 1) * kUnitRows];
+            --p;
+          }
+          my_list[p * kUnitRows] = key;
+          if (cnt == Kc) thr = my_list[(Kc - 1) * kUnitRows];
+        }
+      };
       for (int n = 0; n < U.nt; ++n, ++kAcc) {
-        const int a = kAcc & 1;
-        if (!tc::mbar_wait(&acc_full[a], (kAcc >> 1) & 1, abort_flag)) {
+        if (!tc::mbar_wait(&acc_full[m], kAcc & 1, abort_flag)) {
           fail();
           alive = false;
           break;
         }
         tc::fence_after_sync();
-        uint32_t v[kTileN];
-        const uint32_t taddr = tmem + lane_base + uint32_t((a * 2 + m) * kTileN);
+        const uint32_t taddr = tmem + lane_base + uint32_t(m * kTileN);
 #pragma unroll
-        for (int c = 0; c < kTileN / 32; ++c) tc::tmem_ld_32x32b_x32(taddr + c * 32, v + c * 32);
-        tc::tmem_ld_wait();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
-        if (cand_row) {
+        for (int c = 0; c < kTileN / kChunk; ++c) {
+          uint32_t v[kChunk];
 #pragma unroll
-          for (int bi = 0; bi < kBlocksPerTile; ++bi) {
-            const int t = n * kBlocksPerTile + bi;
-            const float mx = block_max<BS>(v + bi * BS);
-            if (t < loc) {
-              const uint64_t key = rank_key(mx, t);
-              if (cnt < Kc || key > thr) {
-                int p = cnt < Kc ? cnt++ : Kc - 1;
-                while (p > 0 && my_list[(p - 1) * kUnitRows] < key) {
-                  my_list[p * kUnitRows] = my_list[(p - 1) * kUnitRows];
-                  --p;
-                }
-                my_list[p * kUnitRows] = key;
-                if (cnt == Kc) thr = my_list[(Kc - 1) * kUnitRows];
-              }
-            }
+          for (int q = 0; q < kChunk / 32; ++q) tc::tmem_ld_32x32b_x32(taddr + c * kChunk + q * 32, v + q * 32);
+          tc::tmem_ld_wait();
+          if (c == kTileN / kChunk - 1) {  // the whole accumulator is in registers: release it
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty[m]);
+          }
+          if (cand_row) {
+#pragma unroll
+            for (int bi = 0; bi < kChunk / BS; ++bi)
+              offer(n * (kTileN / BS) + c * (kChunk / BS) + bi, block_max<BS>(v + bi * BS));
           }
         }
       }
