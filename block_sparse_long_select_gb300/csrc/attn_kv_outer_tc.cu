@@ -554,13 +554,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // with log-sum-exp weights.
 // ---------------------------------------------------------------------------
 template <int NU>
-__global__ void attn_combine_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
-                                    const int32_t* __restrict__ kv_len, const __nv_bfloat16* __restrict__ part_o,
-                                    const float* __restrict__ part_lse, const int* __restrict__ rev, int b, int Nq, int Nk, int Hq, int G, int K,
-                                    int Bs, int nblk, int D, int c0, int cq, __nv_bfloat16* __restrict__ out,
-                                    float* __restrict__ lse_out) {
+__global__ void __launch_bounds__(256) attn_combine_kernel(
+    const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
+    const __nv_bfloat16* __restrict__ part_o, const float* __restrict__ part_lse, const int* __restrict__ rev, int b,
+    int Nq, int Nk, int Hq, int G, int K, int Bs, int nblk, int D, int c0, int cq, __nv_bfloat16* __restrict__ out,
+    float* __restrict__ lse_out) {
+  constexpr int kBatch = NU <= 2 ? 8 : (NU == 4 ? 4 : 2);  // slots whose loads are in flight together
+  __shared__ int slot_e[256 / 32][kMaxK];
   const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   if (wid >= int64_t(cq) * G) return;
   const int il = int(wid / G), g = int(wid % G);
   const int hpg = Hq / G;
@@ -568,11 +570,18 @@ __global__ void attn_combine_kernel(const int32_t* __restrict__ sel, const int32
   const int i = c0 + il;
   const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
   const int pos = sv.q0 + i;
+  // valid slots in slot order, as partial-row entries (via the reverse map)
   const int32_t* srow = sel + ((int64_t(b) * Nq + i) * G + g) * K;
-  const int ta = lane < K ? srow[lane] : -1;
-  const int tb = lane + 32 < K ? srow[lane + 32] : -1;
-  const uint64_t mask = uint64_t(__ballot_sync(0xffffffffu, sv.ok && entry_valid(ta, pos, Bs, nblk))) |
-                        (uint64_t(__ballot_sync(0xffffffffu, sv.ok && entry_valid(tb, pos, Bs, nblk))) << 32);
+  const int* rv = rev + (int64_t(il) * G + g) * K;
+  int nvalid = 0;
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    const int k = k0 + lane;
+    const bool ok = k < K && sv.ok && entry_valid(srow[k], pos, Bs, nblk);
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (ok) slot_e[wl][nvalid + __popc(bal & ((1u << lane) - 1u))] = rv[k];
+    nvalid += __popc(bal);
+  }
+  __syncwarp();
   int head[NU];
   float m[NU], wsum[NU], acc[NU][8];
 #pragma unroll
@@ -584,35 +593,45 @@ __global__ void attn_combine_kernel(const int32_t* __restrict__ sel, const int32
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[u][x] = 0.f;
   }
-  // slot k's partial rows: entry E = rev[...], rows E * hpg .. E * hpg + hpg - 1
-  const int* rv = rev + (int64_t(il) * G + g) * K;
-  const int ea = lane < K ? rv[lane] : 0;
-  const int eb = lane + 32 < K ? rv[lane + 32] : 0;
-#pragma unroll 4
-  for (int k = 0; k < K; ++k) {
-    if (!((mask >> k) & 1)) continue;
-    const int64_t E = __shfl_sync(0xffffffffu, k < 32 ? ea : eb, k & 31);
+  // one pass, kBatch slots at a time: all their loads first, then a running
+  // log-sum-exp rescale (slot order is fixed: the result is deterministic)
+  for (int j0 = 0; j0 < nvalid; j0 += kBatch) {
+    float l[kBatch][NU];
+    uint4 raw[kBatch][NU];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) m[u] = fmaxf(m[u], part_lse[E * hpg + head[u]]);
-  }
-#pragma unroll 4
-  for (int k = 0; k < K; ++k) {
-    if (!((mask >> k) & 1)) continue;
-    const int64_t E = __shfl_sync(0xffffffffu, k < 32 ? ea : eb, k & 31);
+    for (int j = 0; j < kBatch; ++j) {
+      const bool have = j0 + j < nvalid;
+      const int64_t E = have ? slot_e[wl][j0 + j] : 0;
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        const int vi = lane + 32 * u;
+        l[j][u] = have ? part_lse[E * hpg + head[u]] : -INFINITY;
+        raw[j][u] = (have && vi < nvec) ? *reinterpret_cast<const uint4*>(part_o + E * hpg * D + vi * 8)
+                                        : make_uint4(0, 0, 0, 0);
+      }
+    }
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
-      const int vi = lane + 32 * u;
-      if (vi >= nvec) continue;
-      const float wk = expf(part_lse[E * hpg + head[u]] - m[u]);
-      wsum[u] += wk;
-      const uint4 raw = *reinterpret_cast<const uint4*>(part_o + E * hpg * D + vi * 8);
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      float mb = m[u];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float2 f = __bfloat1622float2(h2[x]);
-        acc[u][2 * x] = fmaf(wk, f.x, acc[u][2 * x]);
-        acc[u][2 * x + 1] = fmaf(wk, f.y, acc[u][2 * x + 1]);
+      for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, l[j][u]);
+      const float rescale = m[u] > -INFINITY ? expf(m[u] - mb) : 0.f;
+      wsum[u] *= rescale;
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[u][x] *= rescale;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float wk = l[j][u] > -INFINITY ? expf(l[j][u] - mb) : 0.f;
+        wsum[u] += wk;
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float2 f = __bfloat1622float2(h2[x]);
+          acc[u][2 * x] = fmaf(wk, f.x, acc[u][2 * x]);
+          acc[u][2 * x + 1] = fmaf(wk, f.y, acc[u][2 * x + 1]);
+        }
       }
+      m[u] = mb;
     }
   }
   __nv_bfloat16* dst = out + ((int64_t(b) * Nq + i) * Hq + g * hpg) * D;
