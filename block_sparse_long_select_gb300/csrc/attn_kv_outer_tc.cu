@@ -17,18 +17,23 @@
 //                   per run of its tiles). Per tile: gather the 128 query rows
 //                   (128/hpg queries x hpg heads of the group), S = Q K^T on
 //                   tcgen05 into TMEM, exact softmax in registers (causal mask
-//                   only in the local block), P (bf16) to shared memory,
-//                   O = P V on tcgen05 into TMEM, then the per-slot partial
-//                   (O / l in bf16, lse in fp32) is written for the combine.
+//                   only in the local block), P (bf16) written back over S in
+//                   TMEM, O = P V on tcgen05 into TMEM, then the per-slot
+//                   partial (O / l in bf16, lse in fp32) is stored for the
+//                   combine straight from registers (chunk-major rows, so a
+//                   warp store covers 512 contiguous bytes).
 //  6. attn_combine  per (query, head): log-sum-exp merge of the K slot
 //                   partials in slot order -> output row. Deterministic; no
 //                   atomics on any output.
 //
-// attn_kv_outer warp roles (448 threads): warp 0 K/V TMA producer, warps 1-4
-// query-row gather (one ring slot each; cp.async, swizzled), warp 5 TMEM owner
-// + MMA issuer,
-// warps 6-13 two epilogue warpgroups that alternate tiles (ping-pong), each
-// owning S (Bs columns) and O (D columns) in TMEM. All waits are bounded.
+// attn_kv_outer warp roles (512 threads): warp 0 K/V TMA producer, warps 1-4
+// query-row gather (one ring slot each; cp.async, swizzled; the next tile's
+// entries are fetched while the current copies are in flight), warp 5 TMEM
+// owner + MMA issuer, warps 6-7 idle; warps 8-15 two epilogue warpgroups that
+// alternate tiles (ping-pong), each owning S (Bs columns) and O (D columns) in
+// TMEM. Warpgroups 0-1 hand registers to the epilogue (88 -> 168 per thread)
+// so that a whole S row and a whole O row are read from TMEM at once. All
+// waits are bounded.
 #include <cmath>
 #include <algorithm>
 #include <cstdlib>
@@ -40,11 +45,14 @@ namespace msa {
 namespace {
 
 constexpr int kRows = 128;  // query rows per tile (M of both MMAs)
-constexpr int kAttnThreads = 448;
+constexpr int kAttnThreads = 512;
+constexpr int kLaunchRegs = 128;  // registers per thread at launch (checked on the host)
+constexpr int kProdRegs = 88, kEpiRegs = 168;
+static_assert(256 * kProdRegs + 256 * kEpiRegs <= kAttnThreads * kLaunchRegs, "register split");
 constexpr int kKvWarp = 0;
 constexpr int kGatherWarp0 = 1;  // warps 1..4
 constexpr int kMmaWarpA = 5;
-constexpr int kEpiWarp0 = 6;  // warps 6..13
+constexpr int kEpiWarp0 = 8;  // warps 8..15 (warpgroups 2 and 3)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -191,12 +199,10 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 struct AttnParams {
   const __nv_bfloat16* q;  // [B, Nq, Hq, D]
+  uint4* part_o;           // [tiles][D / 8 chunks][128 rows] x 16 bytes (8 bf16)
   const int* entries;      // chunk entries
   const int4* tiles;       // chunk tiles
   const int* total_tiles;  // device count
@@ -209,20 +215,14 @@ struct AttnParams {
   float scale;
 };
 
-constexpr int kRing = 3;  // gathered-query tile ring depth (one gather warp per slot)
+constexpr int kRing = 4;  // gathered-query tile ring depth (one gather warp per slot)
 static_assert(kRing <= 4, "one gather warp per ring slot: warps 1..4");
 
-template <int NC>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* v) {
-#pragma unroll
-  for (int c = 0; c < NC; ++c) tc::tmem_ld_32x32b_x32(taddr + c * 32, v + c * 32);
-  tc::tmem_ld_wait();
-}
 
 template <int D, int BS>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmO, const AttnParams p) {
+                         const AttnParams p) {
   constexpr uint32_t kQBytes = kRows * D * 2;       // one gathered query tile (= one bf16 O tile)
   constexpr uint32_t kSlot = kQBytes;
   constexpr uint32_t kKVHalf = BS * 128;            // one 64-wide half of a K or V block
@@ -230,7 +230,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr int NH = D / 64;
   constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, BS, false);
   constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, D, true);  // B = V is MN-major
-  constexpr int kSC = BS / 32 > 2 ? 2 : BS / 32;   // 32-column chunks per TMEM load batch (S)
   // TMEM columns: warpgroup w owns S at [256 w, 256 w + BS) and O at [256 w + 128, 256 w + 128 + D)
   static_assert(BS <= 128 && D <= 128, "TMEM plan: S <= 128 and O <= 128 columns per warpgroup");
 
@@ -240,8 +239,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* k_buf = smem;                    // [NH][BS][128 B]
   uint8_t* v_buf = k_buf + kKBytes;         // [NH][BS][128 B]
   uint8_t* ring = v_buf + kKBytes;          // kRing x kSlot: gathered Q tiles
-  uint8_t* ostage = ring + kRing * kSlot;   // 2 x kQBytes: O staging per epilogue warpgroup
-  int* meta = reinterpret_cast<int*>(ostage + 2 * kQBytes);  // [kRing][<=128] tile entries (query*64+slot) or -1
+  int* meta = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kRing][<=128] tile entries (query*64+slot) or -1
   // mbarriers need 8-byte alignment: round the barrier area up to 16 bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(meta + kRing * kRows) + 15) & ~uintptr_t(15));
@@ -282,7 +280,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == kKvWarp && lane == 0) {
     tc::tma_prefetch(&tmK);
     tc::tma_prefetch(&tmV);
-    tc::tma_prefetch(&tmO);
   }
   __syncthreads();
   tc::fence_after_sync();
@@ -298,6 +295,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     set_status(p.status, MSA_ERR_TIMEOUT);
   };
 
+  // Each register re-allocation sits at the top of its warpgroups' branch
+  // (one instruction for all warps of a warpgroup) so that the compiler
+  // budgets each branch with its own register count.
+  if (warp < kEpiWarp0) {
+  tc::regs_dec<kProdRegs>();
   if (warp == kKvWarp) {
     // ----------------------------- K/V producer -----------------------------
     if (lane == 0) {
@@ -332,21 +334,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int gw = warp - kGatherWarp0;    // ring slot of this warp; warps beyond the ring idle
     constexpr int kCpr = D / 8;            // 16-byte chunks per row
     constexpr int kRowsPerIt = 32 / kCpr;  // rows per warp instruction
+    constexpr int kEntPerLane = kRows / 32;
     const int per_tile = kRows / p.hpg;
     int* my_meta = meta + gw * kRows;
+    // a tile's (bin, first entry, count) and its entries, held in registers
+    // from one iteration to the next so their latency overlaps the copies
+    int4 tl = make_int4(0, 0, 0, 0);
+    int ev[kEntPerLane];
+    auto fetch = [&](int z) {
+      tl = p.tiles[z0 + z];
+#pragma unroll
+      for (int x = 0; x < kEntPerLane; ++x) {
+        const int e = lane + 32 * x;
+        ev[x] = (e < per_tile && e < tl.z) ? p.entries[tl.y + e] : -1;
+      }
+    };
+    if (gw < kRing && gw < n) fetch(gw);
     for (int z = gw; gw < kRing && z < n; z += kRing) {
-      const int4 tl = p.tiles[z0 + z];
       if (!tc::mbar_wait(&q_empty[gw], ((z / kRing) & 1) ^ 1, abort_flag)) {
         fail();
         break;
       }
-      for (int e = lane; e < per_tile; e += 32) my_meta[e] = e < tl.z ? p.entries[tl.y + e] : -1;
+#pragma unroll
+      for (int x = 0; x < kEntPerLane; ++x)
+        if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = ev[x];
       __syncwarp();
       const int g = tl.x / p.nblk;
       const uint32_t slot = tc::smem_u32(ring + gw * kSlot);
       const int chunk = lane % kCpr, sub = lane / kCpr;
       const uint32_t hf = chunk >> 3, cc = chunk & 7;
-#pragma unroll 8
+#pragma unroll 4
       for (int it = 0; it < kRows / kRowsPerIt; ++it) {
         const int row = it * kRowsPerIt + sub;
         const int ent = my_meta[row / p.hpg];
@@ -356,6 +373,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         cp_async16(slot + hf * (kRows * 128) + row * 128 + ((cc ^ uint32_t(row & 7)) << 4), src, ent >= 0 ? 16u : 0u);
       }
       cp_async_commit();
+      if (z + kRing < n) fetch(z + kRing);
       cp_async_wait<0>();
       tc::fence_proxy_async_smem();
       __syncwarp();
@@ -433,7 +451,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::mma_commit(done_bar);
       tc::mbar_wait(done_bar, 0, &zero);
     }
+  }  // warps 6-7: idle
   } else {
+    tc::regs_inc<kEpiRegs>();
     // -------------------------------- epilogue --------------------------------
     const int w = (warp - kEpiWarp0) >> 2;         // warpgroup: tiles z with z % 2 == w
     const int quarter = warp & 3;                  // TMEM lane quarter of this warp
@@ -459,85 +479,80 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int pos = sv.q0 + p.c0 + il;
       const int nvalid = valid ? min(BS, pos - t * BS + 1) : BS;  // keys j <= pos inside the block
       const uint32_t s_addr = tmem + lane_base + uint32_t(s) * 256u;
-      // pass 1: row maximum over the visible keys
-      float mx = -INFINITY;
+      const bool full = nvalid >= BS;  // all keys visible (every block but the local one)
+      // the whole S row in registers: one TMEM round trip
+      uint32_t v[BS];
 #pragma unroll
-      for (int c0 = 0; c0 < BS / 32; c0 += kSC) {
-        uint32_t v[kSC * 32];
-        tmem_load_cols<kSC>(s_addr + c0 * 32, v);
+      for (int c = 0; c < BS / 32; ++c) tc::tmem_ld_32x32b_x32(s_addr + c * 32, v + c * 32);
+      tc::tmem_ld_wait();
+      if (!full) {
 #pragma unroll
-        for (int j = 0; j < kSC * 32; ++j)
-          if (c0 * 32 + j < nvalid) mx = fmaxf(mx, __uint_as_float(v[j]));
+        for (int j = 0; j < BS; ++j)
+          if (j >= nvalid) v[j] = __float_as_uint(-INFINITY);  // exp2(-inf) = 0 below
       }
-      // pass 2: probabilities as bf16 pairs written back over S in TMEM (the
-      // PV MMA reads its A operand from there), row sum in fp32
+      // row maximum (four independent chains)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < BS; j += 2)
+        m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      // probabilities as bf16 pairs written back over S in TMEM (the PV MMA
+      // reads its A operand from there), row sum in fp32
       const float mneg = -mx * p.scale_log2;
-      float l = 0.f;
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c0 = 0; c0 < BS / 32; c0 += kSC) {
-        uint32_t v[kSC * 32];
-        tmem_load_cols<kSC>(s_addr + c0 * 32, v);
-        uint32_t pk[kSC * 16];
+      for (int c0 = 0; c0 < BS / 32; ++c0) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < kSC * 32; j += 2) {
-          const float p0 = (c0 * 32 + j < nvalid) ? ex2(fmaf(__uint_as_float(v[j]), p.scale_log2, mneg)) : 0.f;
-          const float p1 = (c0 * 32 + j + 1 < nvalid) ? ex2(fmaf(__uint_as_float(v[j + 1]), p.scale_log2, mneg)) : 0.f;
-          l += p0 + p1;
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j]), p.scale_log2, mneg));
+          const float p1 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j + 1]), p.scale_log2, mneg));
+          l4[(j >> 1) & 3] += p0 + p1;
           pk[j >> 1] = pack_bf16(p0, p1);  // keys 2c (low half) and 2c+1 (high half) in column c
         }
-        // S columns [c0*32, c0*32 + 32*kSC) were read above; P of those keys
-        // takes columns [c0*16, c0*16 + 16*kSC), all of which are already read
-        if (kSC == 2)
-          tc::tmem_st_32x32b_x32(s_addr + c0 * 16, pk);
-        else
-          tc::tmem_st_32x32b_x16(s_addr + c0 * 16, pk);
+        tc::tmem_st_32x32b_x16(s_addr + c0 * 16, pk);
       }
+      const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&p_full[s]);
-      // output: O / l (bf16) staged in this warpgroup's buffer, stored as one
-      // contiguous 128-row block by TMA; lse per row.
+      // output: O / l in bf16, stored from registers. Partial row r of tile zg
+      // keeps its 16-byte chunk c at part_o[(zg * D/8 + c) * 128 + r], so each
+      // warp store instruction writes 32 consecutive rows' chunk: 512 bytes.
       if (!tc::mbar_wait(&o_full[s], (z >> 1) & 1, abort_flag)) {
         fail();
         break;
       }
-      if (r == 0) tc::bulk_wait_read_all();  // the previous store has read the staging buffer
-      tc::named_bar_sync(1 + w, 128);
       tc::fence_after_sync();
       const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint8_t* stage = ostage + w * kQBytes;
-      const uint32_t stage_addr = tc::smem_u32(stage);
+      const int zg = z0 + z;  // tile index in the chunk = its partial row block
+      uint4* dst = p.part_o + int64_t(zg) * (D / 8) * kRows + r;
+      constexpr int kOH = D > 64 ? 64 : D;  // O columns per TMEM round trip
 #pragma unroll
-      for (int c0 = 0; c0 < D / 32; c0 += 2) {
-        uint32_t v[64];
-        tmem_load_cols<2>(o_addr + c0 * 32, v);
+      for (int h0 = 0; h0 < D; h0 += kOH) {
+        uint32_t ov[kOH];
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const int chunk = c0 * 4 + q4;  // 16-byte chunk of the output row
-          const int hf = chunk >> 3, ch = chunk & 7;
-          st_shared_v4(stage_addr + hf * (kRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4),
-                       pack_bf16(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv),
-                       pack_bf16(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv),
-                       pack_bf16(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv),
-                       pack_bf16(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv));
+        for (int c = 0; c < kOH / 32; ++c) tc::tmem_ld_32x32b_x32(o_addr + h0 + c * 32, ov + c * 32);
+        tc::tmem_ld_wait();
+        if (h0 + kOH >= D) {  // O is in registers: the next PV may overwrite it
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&o_empty[s]);
+        }
+#pragma unroll
+        for (int c = 0; c < kOH / 8; ++c) {
+          uint4 o;
+          o.x = pack_bf16(__uint_as_float(ov[c * 8 + 0]) * inv, __uint_as_float(ov[c * 8 + 1]) * inv);
+          o.y = pack_bf16(__uint_as_float(ov[c * 8 + 2]) * inv, __uint_as_float(ov[c * 8 + 3]) * inv);
+          o.z = pack_bf16(__uint_as_float(ov[c * 8 + 4]) * inv, __uint_as_float(ov[c * 8 + 5]) * inv);
+          o.w = pack_bf16(__uint_as_float(ov[c * 8 + 6]) * inv, __uint_as_float(ov[c * 8 + 7]) * inv);
+          dst[(h0 / 8 + c) * kRows] = o;
         }
       }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&o_empty[s]);
-      const int zg = z0 + z;  // tile index in the chunk = its partial row block
       p.part_lse[int64_t(zg) * kRows + r] = valid ? mx * p.scale + logf(l) : 0.f;
-      tc::named_bar_sync(1 + w, 128);  // the whole tile is staged
-      if (r == 0) {
-#pragma unroll
-        for (int hf = 0; hf < NH; ++hf) tc::tma_store_2d(&tmO, stage + hf * (kRows * 128), hf * 64, zg * kRows);
-        tc::bulk_commit();
-      }
     }
-    if (r == 0) tc::bulk_wait_all();
   }
 
   __syncthreads();
@@ -549,14 +564,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ---------------------------------------------------------------------------
 // combine: one warp per (query, group). A slot's partials of the group's
-// heads are contiguous (hpg rows of D bf16, found through the reverse map);
-// each lane owns NU 16-byte vectors of them. Slots are merged in slot order
-// with log-sum-exp weights.
+// heads are hpg consecutive partial rows (found through the reverse map),
+// stored chunk-major: 16-byte chunk c of row r in tile zg at
+// ((zg * D/8 + c) * 128 + r). Lane vector vi takes head vi % hpg and chunk
+// vi / hpg, so neighbouring lanes read neighbouring rows of one chunk. Each
+// lane owns NU vectors. Slots are merged in slot order with log-sum-exp
+// weights.
 // ---------------------------------------------------------------------------
 template <int NU>
 __global__ void __launch_bounds__(256) attn_combine_kernel(
     const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
-    const __nv_bfloat16* __restrict__ part_o, const float* __restrict__ part_lse, const int* __restrict__ rev, int b,
+    const uint4* __restrict__ part_o, const float* __restrict__ part_lse, const int* __restrict__ rev, int b,
     int Nq, int Nk, int Hq, int G, int K, int Bs, int nblk, int D, int c0, int cq, __nv_bfloat16* __restrict__ out,
     float* __restrict__ lse_out) {
   constexpr int kBatch = NU <= 2 ? 8 : (NU == 4 ? 4 : 2);  // slots whose loads are in flight together
@@ -582,12 +600,13 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
     nvalid += __popc(bal);
   }
   __syncwarp();
-  int head[NU];
+  int head[NU], voff[NU];
   float m[NU], wsum[NU], acc[NU][8];
 #pragma unroll
   for (int u = 0; u < NU; ++u) {
     const int vi = lane + 32 * u;
-    head[u] = vi < nvec ? (vi * 8) / D : 0;
+    head[u] = vi < nvec ? vi % hpg : 0;
+    voff[u] = vi < nvec ? (vi / hpg) * 128 + head[u] : 0;  // chunk-major offset from the slot's first row
     m[u] = -INFINITY;
     wsum[u] = 0.f;
 #pragma unroll
@@ -601,13 +620,13 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const bool have = j0 + j < nvalid;
-      const int64_t E = have ? slot_e[wl][j0 + j] : 0;
+      const int64_t R = have ? int64_t(slot_e[wl][j0 + j]) * hpg : 0;  // the slot's first partial row
+      const uint4* base = part_o + (R >> 7) * (D / 8) * 128 + (R & 127);
 #pragma unroll
       for (int u = 0; u < NU; ++u) {
         const int vi = lane + 32 * u;
-        l[j][u] = have ? part_lse[E * hpg + head[u]] : -INFINITY;
-        raw[j][u] = (have && vi < nvec) ? *reinterpret_cast<const uint4*>(part_o + E * hpg * D + vi * 8)
-                                        : make_uint4(0, 0, 0, 0);
+        l[j][u] = have ? part_lse[R + head[u]] : -INFINITY;
+        raw[j][u] = (have && vi < nvec) ? base[voff[u]] : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll
@@ -645,8 +664,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
     o.y = pack_bf16(acc[u][2] * inv, acc[u][3] * inv);
     o.z = pack_bf16(acc[u][4] * inv, acc[u][5] * inv);
     o.w = pack_bf16(acc[u][6] * inv, acc[u][7] * inv);
-    *reinterpret_cast<uint4*>(dst + vi * 8) = o;
-    if (lse_out && (vi * 8) % D == 0)
+    *reinterpret_cast<uint4*>(dst + head[u] * D + (vi / hpg) * 8) = o;
+    if (lse_out && vi < hpg)
       lse_out[(int64_t(b) * Nq + i) * Hq + g * hpg + head[u]] = wsum[u] > 0.f ? m[u] + logf(wsum[u]) : -INFINITY;
   }
 }
@@ -711,7 +730,7 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   o += a256(max_entries * 4);
   L.tiles = o;
   o += a256(max_tiles * 16);
-  L.part_o = o;  // [tiles * 128 rows][d] bf16
+  L.part_o = o;  // [tiles][d / 8 chunks][128 rows] x 8 bf16
   o += a256(max_tiles * kRows * size_t(d) * 2);
   L.part_lse = o;  // [tiles * 128 rows] fp32
   o += a256(max_tiles * kRows * 4);
@@ -723,7 +742,7 @@ size_t attn_smem_bytes(int d, int Bs) {
   const size_t kv = size_t(Bs) * d * 2 * 2;
   const size_t slot = size_t(kRows) * d * 2;
   const size_t meta = size_t(kRing) * kRows * 4 + 16;
-  return 1024 + kv + kRing * slot + 2 * slot + meta + (2 + 2 * kRing + 8 + 1) * 8 + 16;
+  return 1024 + kv + kRing * slot + meta + (2 + 2 * kRing + 8 + 1) * 8 + 16;
 }
 
 }  // namespace
@@ -759,7 +778,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   int* entries = reinterpret_cast<int*>(w + L.entries);
   int* rev = reinterpret_cast<int*>(w + L.rev);
   int4* tiles = reinterpret_cast<int4*>(w + L.tiles);
-  __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(w + L.part_o);
+  uint4* part_o = reinterpret_cast<uint4*>(w + L.part_o);
   float* part_lse = reinterpret_cast<float*>(w + L.part_lse);
   const int cq_max = chunk_tokens(Nq, Hq, K, d);
 
@@ -770,18 +789,18 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   if (!make_tmap_bf16(&tmK, k, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16(&tmV, v, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  CUtensorMap tmO;  // partial rows: [tiles * 128][d], stored 128 rows x 64 columns at a time
-  {
-    const uint64_t odims[2] = {uint64_t(d), uint64_t(L.max_tiles) * kRows};
-    const uint64_t ostr[1] = {uint64_t(d) * 2};
-    const uint32_t obox[2] = {64, uint32_t(kRows)};
-    if (!make_tmap_bf16(&tmO, part_o, 2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-  }
 
   const size_t smem = attn_smem_bytes(d, Bs);
   const size_t hist_smem = size_t(nblk) * 4 * 2;
   if (hist_smem > 200 * 1024) return cudaErrorInvalidValue;
   auto set_attr = [&](auto kern) {
+    // the register split re-allocates exactly the launch allocation: a build
+    // that launches with another register count must not run (the increase
+    // would wait for registers that are never released)
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+    if (err != cudaSuccess) return err;
+    if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kAttnThreads) return cudaErrorInvalidConfiguration;
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   };
   cudaError_t e = cudaSuccess;
@@ -794,6 +813,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
 
   AttnParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.part_o = part_o;
   prm.entries = entries;
   prm.tiles = tiles;
   prm.total_tiles = total;
@@ -837,7 +857,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   do {                                                                                    \
     auto kern = attn_kv_outer_kernel<D_, BS_>;                                           \
     if ((e = set_attr(kern)) != cudaSuccess) return e;                                   \
-    kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, tmO, prm);                       \
+    kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, prm);                            \
   } while (0)
         if (d == 128) {
           if (Bs == 128)

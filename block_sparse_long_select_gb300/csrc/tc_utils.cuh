@@ -220,6 +220,18 @@ __device__ __forceinline__ float warp_max_f32(float x) {
   return y;
 }
 
+// Per-warpgroup register re-allocation. Every warp of a warpgroup executes
+// the same call; the increases of some warpgroups must be covered by the
+// decreases of others out of the registers the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // max of three floats in one instruction (sm_100+)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
