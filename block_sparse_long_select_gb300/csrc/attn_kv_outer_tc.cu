@@ -27,9 +27,10 @@
 //                   atomics on any output.
 //
 // attn_kv_outer warp roles (512 threads): warp 0 K/V TMA producer, warps 1-4
-// query-row gather (one ring slot each; cp.async, swizzled; the next tile's
-// entries are fetched while the current copies are in flight), warp 5 TMEM
-// owner + MMA issuer, warps 6-7 idle; warps 8-15 two epilogue warpgroups that
+// query-row gather by cp.async (one ring slot each, rows 0-79), warp 6
+// query-row gather by four-row TMA gathers (rows 80-127 of every slot; the
+// next tile's entries are fetched while the current one is issued), warp 5
+// TMEM owner + MMA issuer, warp 7 idle; warps 8-15 two epilogue warpgroups that
 // alternate tiles (ping-pong), each owning S (Bs columns) and O (D columns) in
 // TMEM. Warpgroups 0-1 hand registers to the epilogue (88 -> 168 per thread)
 // so that a whole S row and a whole O row are read from TMEM at once. All
@@ -50,7 +51,8 @@ constexpr int kLaunchRegs = 128;  // registers per thread at launch (checked on 
 constexpr int kProdRegs = 88, kEpiRegs = 168;
 static_assert(256 * kProdRegs + 256 * kEpiRegs <= kAttnThreads * kLaunchRegs, "register split");
 constexpr int kKvWarp = 0;
-constexpr int kGatherWarp0 = 1;  // warps 1..4
+constexpr int kGatherWarp0 = 1;  // warps 1..4: cp.async gathers
+constexpr int kTmaGatherWarp = 6;  // TMA gathers
 constexpr int kMmaWarpA = 5;
 constexpr int kEpiWarp0 = 8;  // warps 8..15 (warpgroups 2 and 3)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -89,41 +91,92 @@ __global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t
     if (hist[t]) atomicAdd(&cnt[g * nblk + t], hist[t]);
 }
 
+// Relative cost of the attention kernel's work, fitted to per-CTA cycle
+// counts: a tile, the first tile of a bin (its K/V load and the pipeline
+// bubble around it), a tile holding rows whose local block this is (masked).
+constexpr int kCostTile = 32, kCostBin = 17, kCostMasked = 8;
+constexpr int kMaxGrid = 1024;  // persistent grid: one CTA per SM
+
 // single CTA of 1024 threads: tile offsets, entry offsets (= tile offset x
-// entries per tile: every tile owns a full slot range), tile total
-__global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__ cnt, int nbins, int per_tile,
-                                                         int* __restrict__ entry_off, int* __restrict__ tile_off,
-                                                         int* __restrict__ total_tiles) {
-  __shared__ int s_e[1024], s_t[1024];
+// entries per tile: every tile owns a full slot range), tile total, and the
+// persistent grid's split: CTA j takes tiles [cta_start[j], cta_start[j+1]),
+// contiguous runs of equal estimated cost.
+__global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__ cnt, const int32_t* __restrict__ q_offset,
+                                                         int b, int nblk, int nbins, int per_tile, int Bs, int c0,
+                                                         int cq, int grid, int* __restrict__ entry_off,
+                                                         int* __restrict__ tile_off, int* __restrict__ cost_off,
+                                                         int* __restrict__ total_tiles, int* __restrict__ cta_start) {
+  __shared__ int s_e[1024], s_t[1024], s_c[1024];
   const int tid = threadIdx.x;
   const int per = (nbins + 1023) / 1024;
   const int lo = min(nbins, tid * per), hi = min(nbins, lo + per);
-  int se = 0, st = 0;
+  const int q0 = q_offset ? q_offset[b] : 0;
+  auto bin_cost = [&](int x, int nt) {
+    // queries of the chunk whose local block is this bin's block
+    const int t = x % nblk;
+    const int a0 = max(c0, t * Bs - q0), a1 = min(c0 + cq, (t + 1) * Bs - q0);
+    const int nloc = max(0, a1 - a0);
+    return nt > 0 ? kCostTile * nt + kCostBin + kCostMasked * min(nt, nloc) : 0;
+  };
+  int se = 0, st = 0, sc = 0;
   for (int x = lo; x < hi; ++x) {
+    const int nt = (cnt[x] + per_tile - 1) / per_tile;
     se += cnt[x];
-    st += (cnt[x] + per_tile - 1) / per_tile;
+    st += nt;
+    sc += bin_cost(x, nt);
   }
   s_e[tid] = se;
   s_t[tid] = st;
+  s_c[tid] = sc;
   __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scans
     const int ve = tid >= off ? s_e[tid - off] : 0;
     const int vt = tid >= off ? s_t[tid - off] : 0;
+    const int vc = tid >= off ? s_c[tid - off] : 0;
     __syncthreads();
     s_e[tid] += ve;
     s_t[tid] += vt;
+    s_c[tid] += vc;
     __syncthreads();
   }
-  int bt = s_t[tid] - st;
+  int bt = s_t[tid] - st, bc = s_c[tid] - sc;
   for (int x = lo; x < hi; ++x) {
+    const int nt = (cnt[x] + per_tile - 1) / per_tile;
     entry_off[x] = bt * per_tile;  // a bin's entries start on a tile boundary
     tile_off[x] = bt;
-    bt += (cnt[x] + per_tile - 1) / per_tile;
+    cost_off[x] = bc;
+    bt += nt;
+    bc += bin_cost(x, nt);
   }
   if (tid == 1023) {
     entry_off[nbins] = s_t[1023] * per_tile;
     tile_off[nbins] = s_t[1023];
+    cost_off[nbins] = s_c[1023];
     *total_tiles = s_t[1023];
+  }
+  __syncthreads();
+  // CTA j starts at the tile where the cost prefix reaches total * j / grid
+  const int64_t ctot = s_c[1023];
+  const int ttot = s_t[1023];
+  for (int j = tid; j <= grid; j += 1024) {
+    if (j == grid) {
+      cta_start[j] = ttot;
+      continue;
+    }
+    const int64_t X = ctot * j / grid;
+    int lo_b = 0, hi_b = nbins - 1;  // the last bin with cost_off <= X
+    while (lo_b < hi_b) {
+      const int mid = (lo_b + hi_b + 1) >> 1;
+      if (cost_off[mid] <= X)
+        lo_b = mid;
+      else
+        hi_b = mid - 1;
+    }
+    const int nt = tile_off[lo_b + 1] - tile_off[lo_b];
+    const int64_t c = int64_t(cost_off[lo_b + 1]) - cost_off[lo_b];
+    const int64_t kq = c > 0 ? (X - cost_off[lo_b]) * nt / c : 0;
+    const int k = kq < nt ? int(kq) : nt;
+    cta_start[j] = tile_off[lo_b] + k;
   }
 }
 
@@ -205,7 +258,7 @@ struct AttnParams {
   uint4* part_o;           // [tiles][D / 8 chunks][128 rows] x 16 bytes (8 bf16)
   const int* entries;      // chunk entries
   const int4* tiles;       // chunk tiles
-  const int* total_tiles;  // device count
+  const int* cta_start;    // [grid + 1]: this CTA's tiles are [cta_start[j], cta_start[j + 1])
   const int32_t* q_offset;
   const int32_t* kv_len;
   float* part_lse;        // [entries, hpg]: row (entry * hpg + head in group)
@@ -215,14 +268,18 @@ struct AttnParams {
   float scale;
 };
 
-constexpr int kRing = 4;  // gathered-query tile ring depth (one gather warp per slot)
-static_assert(kRing <= 4, "one gather warp per ring slot: warps 1..4");
+constexpr int kRing = 4;  // gathered-query tile ring depth (one cp.async gather warp per slot)
+static_assert(kRing <= 4, "cp.async gather warps are warps 1..4");
+// Rows of a tile gathered by cp.async (the rest by four-row TMA gathers):
+// the two paths have separate in-flight limits, so they run side by side.
+constexpr int kRowsLsu = 80;
+static_assert(kRowsLsu % 8 == 0 && (kRows - kRowsLsu) % 4 == 0 && kRows - kRowsLsu <= 128, "row split");
 
 
 template <int D, int BS>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const AttnParams p) {
+                         const __grid_constant__ CUtensorMap tmQ, const AttnParams p) {
   constexpr uint32_t kQBytes = kRows * D * 2;       // one gathered query tile (= one bf16 O tile)
   constexpr uint32_t kSlot = kQBytes;
   constexpr uint32_t kKVHalf = BS * 128;            // one 64-wide half of a K or V block
@@ -239,10 +296,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* k_buf = smem;                    // [NH][BS][128 B]
   uint8_t* v_buf = k_buf + kKBytes;         // [NH][BS][128 B]
   uint8_t* ring = v_buf + kKBytes;          // kRing x kSlot: gathered Q tiles
-  int* meta = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kRing][<=128] tile entries (query*64+slot) or -1
+  int* meta = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kRing + 1][128] gathered tiles' entries (query*64+slot) or -1
   // mbarriers need 8-byte alignment: round the barrier area up to 16 bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(meta + kRing * kRows) + 15) & ~uintptr_t(15));
+      (reinterpret_cast<uintptr_t>(meta + (kRing + 1) * kRows) + 15) & ~uintptr_t(15));
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* q_full = bars + 2;                // [kRing]
@@ -260,7 +317,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
     for (int r = 0; r < kRing; ++r) {
-      tc::mbar_init(&q_full[r], 1);
+      tc::mbar_init(&q_full[r], 2);  // the slot's cp.async warp + the TMA gather warp
       tc::mbar_init(&q_empty[r], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -280,15 +337,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == kKvWarp && lane == 0) {
     tc::tma_prefetch(&tmK);
     tc::tma_prefetch(&tmV);
+    tc::tma_prefetch(&tmQ);
   }
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
   // this CTA's contiguous run of tiles
-  const int T = *p.total_tiles;
-  const int z0 = int((int64_t(T) * blockIdx.x) / gridDim.x);
-  const int z1 = int((int64_t(T) * (blockIdx.x + 1)) / gridDim.x);
+  const int z0 = p.cta_start[blockIdx.x];
+  const int z1 = p.cta_start[blockIdx.x + 1];
   const int n = z1 - z0;
   auto fail = [&]() {
     *abort_flag = 1;
@@ -324,47 +381,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int zero = 0;
       if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // drain the last copy
     }
-  } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 4) {
-    // --------------------------- query-row gather ---------------------------
-    // Gather warp gw < kRing owns ring slot gw and gathers tiles z = gw, gw + kRing, ...
-    // whole: the tile's entries go to shared memory first, then every lane
-    // copies 16-byte chunks (a warp instruction covers whole 256-byte rows,
-    // coalesced) into the 128B-swizzled K-major layout, and the tile is
-    // published as soon as its own copies have landed.
-    const int gw = warp - kGatherWarp0;    // ring slot of this warp; warps beyond the ring idle
+  } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kRing) {
+    // ------------------------ query-row gather, cp.async ------------------------
+    // Gather warp gw owns ring slot gw (tiles z = gw, gw + kRing, ...) and
+    // copies rows [0, kRowsLsu) of its tiles in 16-byte chunks (a warp
+    // instruction covers whole 256-byte rows) into the 128B-swizzled K-major
+    // layout; its arrival on the slot's barrier follows its own copies.
+    const int gw = warp - kGatherWarp0;
     constexpr int kCpr = D / 8;            // 16-byte chunks per row
     constexpr int kRowsPerIt = 32 / kCpr;  // rows per warp instruction
     constexpr int kEntPerLane = kRows / 32;
     const int per_tile = kRows / p.hpg;
     int* my_meta = meta + gw * kRows;
-    // a tile's (bin, first entry, count) and its entries, held in registers
-    // from one iteration to the next so their latency overlaps the copies
     int4 tl = make_int4(0, 0, 0, 0);
     int ev[kEntPerLane];
-    auto fetch = [&](int z) {
+    auto fetch = [&](int z) {  // independent loads: tile z's entries start at (z0 + z) * per_tile
       tl = p.tiles[z0 + z];
 #pragma unroll
       for (int x = 0; x < kEntPerLane; ++x) {
         const int e = lane + 32 * x;
-        ev[x] = (e < per_tile && e < tl.z) ? p.entries[tl.y + e] : -1;
+        ev[x] = e < per_tile ? p.entries[int64_t(z0 + z) * per_tile + e] : -1;
       }
     };
-    if (gw < kRing && gw < n) fetch(gw);
-    for (int z = gw; gw < kRing && z < n; z += kRing) {
+    if (gw < n) fetch(gw);
+    for (int z = gw; z < n; z += kRing) {
       if (!tc::mbar_wait(&q_empty[gw], ((z / kRing) & 1) ^ 1, abort_flag)) {
         fail();
         break;
       }
 #pragma unroll
       for (int x = 0; x < kEntPerLane; ++x)
-        if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = ev[x];
+        if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = lane + 32 * x < tl.z ? ev[x] : -1;
       __syncwarp();
       const int g = tl.x / p.nblk;
       const uint32_t slot = tc::smem_u32(ring + gw * kSlot);
       const int chunk = lane % kCpr, sub = lane / kCpr;
       const uint32_t hf = chunk >> 3, cc = chunk & 7;
 #pragma unroll 4
-      for (int it = 0; it < kRows / kRowsPerIt; ++it) {
+      for (int it = 0; it < kRowsLsu / kRowsPerIt; ++it) {
         const int row = it * kRowsPerIt + sub;
         const int ent = my_meta[row / p.hpg];
         const int il = ent >= 0 ? (ent >> 6) : 0;
@@ -380,6 +434,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) tc::mbar_arrive(&q_full[gw]);
     }
     cp_async_wait<0>();
+  } else if (warp == kTmaGatherWarp) {
+    // ------------------------ query-row gather, TMA ------------------------
+    // Rows [kRowsLsu, 128) of every tile, in ring order: lane l < kTmaLanes
+    // loads four rows with one four-row gather per 64-column half (same
+    // swizzled layout); the bytes are counted on the slot's barrier. Rows of
+    // padding entries read the chunk's first query (finite values; their
+    // outputs are never read).
+    constexpr int kTmaLanes = (kRows - kRowsLsu) / 4;
+    constexpr int kEntPerLane = kRows / 32;
+    const int per_tile = kRows / p.hpg;
+    int* my_meta = meta + kRing * kRows;
+    int4 tl_n = make_int4(0, 0, 0, 0);
+    int ev_n[kEntPerLane];
+    auto fetch = [&](int z) {
+      tl_n = p.tiles[z0 + z];
+#pragma unroll
+      for (int x = 0; x < kEntPerLane; ++x) {
+        const int e = lane + 32 * x;
+        ev_n[x] = e < per_tile ? p.entries[int64_t(z0 + z) * per_tile + e] : -1;
+      }
+    };
+    if (n > 0) fetch(0);
+    int issued = 0;
+    for (int z = 0; z < n; ++z) {
+      const int rs = z % kRing;
+      const int4 tl = tl_n;
+#pragma unroll
+      for (int x = 0; x < kEntPerLane; ++x)
+        if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = lane + 32 * x < tl.z ? ev_n[x] : -1;
+      if (z + 1 < n) fetch(z + 1);
+      __syncwarp();
+      const int g = tl.x / p.nblk;
+      int rows[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = kRowsLsu + (lane % kTmaLanes) * 4 + j;
+        const int ent = my_meta[row / p.hpg];
+        const int il = ent >= 0 ? (ent >> 6) : 0;
+        rows[j] = (p.b * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg;
+      }
+      if (!tc::mbar_wait(&q_empty[rs], ((z / kRing) & 1) ^ 1, abort_flag)) {
+        fail();
+        break;
+      }
+      if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[rs], uint32_t(kRows - kRowsLsu) * D * 2);
+      __syncwarp();
+      if (lane < kTmaLanes) {
+        uint8_t* dst = ring + rs * kSlot + (kRowsLsu + lane * 4) * 128;
+#pragma unroll
+        for (int hf = 0; hf < NH; ++hf)
+          tc::tma_gather4(dst + hf * (kRows * 128), &tmQ, &q_full[rs], hf * 64, rows[0], rows[1], rows[2], rows[3]);
+      }
+      ++issued;
+      __syncwarp();  // every lane has read my_meta before it is rewritten
+    }
+    // drain: no copy may still be landing in shared memory when the CTA exits
+    int zero = 0;
+    for (int z = issued > kRing ? issued - kRing : 0; z < issued; ++z)
+      tc::mbar_wait(&q_full[z % kRing], (z / kRing) & 1, &zero);
   } else if (warp == kMmaWarpA) {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0) {
@@ -466,7 +579,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // its staged metadata are recycled as soon as QK^T has consumed them);
       // the loads are in flight while S is being computed
       const int4 tl = p.tiles[z0 + z];
-      const int ent = r / p.hpg < tl.z ? p.entries[tl.y + r / p.hpg] : -1;
+      const int e_raw = p.entries[int64_t(z0 + z) * (kRows / p.hpg) + r / p.hpg];
+      const int ent = r / p.hpg < tl.z ? e_raw : -1;
       if (!tc::mbar_wait(&s_full[s], (z >> 1) & 1, abort_flag)) {
         fail();
         break;
@@ -699,7 +813,7 @@ int chunk_tokens(int Nq, int Hq, int K, int d) {
 }
 
 struct KvoLayout {
-  size_t cnt, cursor, entry_off, tile_off, total, entries, rev, tiles, part_o, part_lse, end;
+  size_t cnt, cursor, entry_off, tile_off, cost_off, total, cta_start, entries, rev, tiles, part_o, part_lse, end;
   size_t max_tiles;
 };
 
@@ -721,8 +835,12 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   o += a256((nbins + 1) * 4);
   L.tile_off = o;
   o += a256((nbins + 1) * 4);
+  L.cost_off = o;
+  o += a256((nbins + 1) * 4);
   L.total = o;
   o += 256;
+  L.cta_start = o;
+  o += a256(size_t(kMaxGrid + 1) * 4);
   L.max_tiles = max_tiles;
   L.entries = o;
   o += a256(max_tiles * per_tile * 4);  // bins padded to whole tiles
@@ -741,7 +859,7 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
 size_t attn_smem_bytes(int d, int Bs) {
   const size_t kv = size_t(Bs) * d * 2 * 2;
   const size_t slot = size_t(kRows) * d * 2;
-  const size_t meta = size_t(kRing) * kRows * 4 + 16;
+  const size_t meta = size_t(kRing + 1) * kRows * 4 + 16;
   return 1024 + kv + kRing * slot + meta + (2 + 2 * kRing + 8 + 1) * 8 + 16;
 }
 
@@ -775,6 +893,8 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   int* entry_off = reinterpret_cast<int*>(w + L.entry_off);
   int* tile_off = reinterpret_cast<int*>(w + L.tile_off);
   int* total = reinterpret_cast<int*>(w + L.total);
+  int* cost_off = reinterpret_cast<int*>(w + L.cost_off);
+  int* cta_start = reinterpret_cast<int*>(w + L.cta_start);
   int* entries = reinterpret_cast<int*>(w + L.entries);
   int* rev = reinterpret_cast<int*>(w + L.rev);
   int4* tiles = reinterpret_cast<int4*>(w + L.tiles);
@@ -789,6 +909,13 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   if (!make_tmap_bf16(&tmK, k, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16(&tmV, v, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  CUtensorMap tmQ;  // query rows (b, i, head) x d, gathered four rows at a time (one-row box)
+  {
+    const uint64_t qdims[2] = {uint64_t(d), uint64_t(B) * Nq * Hq};
+    const uint64_t qstr[1] = {uint64_t(d) * 2};
+    const uint32_t qbox[2] = {64, 1};
+    if (!make_tmap_bf16(&tmQ, q, 2, qdims, qstr, qbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
 
   const size_t smem = attn_smem_bytes(d, Bs);
   const size_t hist_smem = size_t(nblk) * 4 * 2;
@@ -816,7 +943,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   prm.part_o = part_o;
   prm.entries = entries;
   prm.tiles = tiles;
-  prm.total_tiles = total;
+  prm.cta_start = cta_start;
   prm.q_offset = q_offset;
   prm.kv_len = kv_len;
   prm.part_lse = part_lse;
@@ -831,7 +958,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   prm.hpg = hpg;
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
-  const int grid = sm_count();
+  const int grid = sm_count() < kMaxGrid ? sm_count() : kMaxGrid;
   const int rows_per_cta = 1024;
 
   for (int b = 0; b < B; ++b) {
@@ -843,7 +970,8 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
         ProfScope pf("attn_invert", stream);
         attn_count_kernel<<<igrid, 256, size_t(nblk) * 4, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk,
                                                                     c0, cq, rows_per_cta, cnt, status);
-        attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, nbins, per_tile, entry_off, tile_off, total);
+        attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, q_offset, b, nblk, nbins, per_tile, Bs, c0, cq, grid,
+                                                 entry_off, tile_off, cost_off, total, cta_start);
         attn_tiles_kernel<<<(nbins + 255) / 256, 256, 0, stream>>>(cnt, entry_off, tile_off, nbins, per_tile, tiles);
         attn_fill_kernel<<<igrid, 256, hist_smem, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0, cq,
                                                             rows_per_cta, entry_off, cursor, entries, rev);
@@ -857,7 +985,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   do {                                                                                    \
     auto kern = attn_kv_outer_kernel<D_, BS_>;                                           \
     if ((e = set_attr(kern)) != cudaSuccess) return e;                                   \
-    kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, prm);                            \
+    kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, tmQ, prm);                      \
   } while (0)
         if (d == 128) {
           if (Bs == 128)

@@ -64,7 +64,9 @@ AttnPlan plan_attn(int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K,
     p.err = MSA_ERR_UNSUPPORTED;
     return p;
   }
-  p.kv_outer = prefill && attn_kv_outer_supported(dtype, Hq, Hkv, d, Bs, K);
+  // the KV-outer kernel addresses query rows (b, i, head) with 32-bit TMA coordinates
+  p.kv_outer = prefill && attn_kv_outer_supported(dtype, Hq, Hkv, d, Bs, K) &&
+               int64_t(B) * Nq * Hq < (int64_t(1) << 31);
   p.split = !prefill && decode_attn_supported(dtype, Hq, Hkv, d, Bs, K);
   p.ws_bytes = p.kv_outer ? attn_kv_outer_ws_bytes(Nq, Nk, Hq, Hkv, d, Bs, K)
                           : (p.split ? kWsHeader + decode_ws_bytes(B, Hq, Hkv, d, K) : kWsHeader);
