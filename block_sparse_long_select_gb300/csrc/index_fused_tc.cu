@@ -267,19 +267,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int loc = pos / BS;
       const bool dense = loc + 1 <= K;
       const bool cand_row = active && U.ok && !dense;
+      // This row's best Kc candidates so far, as a binary min-heap of rank
+      // keys (unique: the block id is part of the key) in its shared-memory
+      // slots; the root is the acceptance threshold once the heap is full.
+      // An accepted candidate costs at most log2(Kc) levels.
       int cnt = 0;
       uint64_t thr = 0;
       auto offer = [&](int t, float mx) {  // candidate block t with maximum mx
         if (t >= loc) return;
         const uint64_t key = rank_key(mx, t);
-        if (cnt < Kc || key > thr) {
-          int p = cnt < Kc ? cnt++ : Kc - 1;
-          while (p > 0 && my_list[(p - 1) * kUnitRows] < key) {
-            my_list[p * kUnitRows] = my_list[(p - 1) * kUnitRows];
-            --p;
+        if (cnt < Kc) {  // fill: sift up
+          int i = cnt++;
+          while (i > 0) {
+            const int pi = (i - 1) >> 1;
+            const uint64_t pv = my_list[pi * kUnitRows];
+            if (pv < key) break;
+            my_list[i * kUnitRows] = pv;
+            i = pi;
           }
-          my_list[p * kUnitRows] = key;
-          if (cnt == Kc) thr = my_list[(Kc - 1) * kUnitRows];
+          my_list[i * kUnitRows] = key;
+          if (cnt == Kc) thr = my_list[0];
+        } else if (key > thr) {  // replace the minimum: sift down
+          int i = 0;
+          while (true) {
+            int c = 2 * i + 1;
+            if (c >= Kc) break;
+            uint64_t cv = my_list[c * kUnitRows];
+            if (c + 1 < Kc) {
+              const uint64_t c2 = my_list[(c + 1) * kUnitRows];
+              if (c2 < cv) {
+                cv = c2;
+                ++c;
+              }
+            }
+            if (key < cv) break;
+            my_list[i * kUnitRows] = cv;
+            i = c;
+          }
+          my_list[i * kUnitRows] = key;
+          thr = my_list[0];
         }
       };
       for (int n = 0; n < U.nt; ++n, ++kAcc) {
@@ -290,6 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         const uint32_t taddr = tmem + lane_base + uint32_t(m * kTileN);
+        // block maxima of the whole tile first (the accumulator is released
+        // as soon as its last columns are in registers), offers afterwards
+        float bm[kTileN / BS];
 #pragma unroll
         for (int c = 0; c < kTileN / kChunk; ++c) {
           uint32_t v[kChunk];
@@ -301,11 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[m]);
           }
-          if (cand_row) {
 #pragma unroll
-            for (int bi = 0; bi < kChunk / BS; ++bi)
-              offer(n * (kTileN / BS) + c * (kChunk / BS) + bi, block_max<BS>(v + bi * BS));
-          }
+          for (int bi = 0; bi < kChunk / BS; ++bi) bm[c * (kChunk / BS) + bi] = block_max<BS>(v + bi * BS);
+        }
+        if (cand_row) {
+#pragma unroll 1
+          for (int j = 0; j < kTileN / BS; ++j) offer(n * (kTileN / BS) + j, bm[j]);
         }
       }
       if (!alive || !active) continue;
