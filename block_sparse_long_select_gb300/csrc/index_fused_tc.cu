@@ -35,10 +35,14 @@ namespace {
 
 constexpr int kUnitRows = 256;  // stacked (token, group) rows per work unit
 constexpr int kTileN = 256;     // keys per key tile (N of each MMA)
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8;
+constexpr int kThreads = 384;
+constexpr int kEpiWarps = 8;       // warps 0-7 (warpgroups 0 and 1)
+constexpr int kProducerWarp = 8;   // warpgroup 2: TMA producer, MMA issuer, two idle warps
 constexpr int kMmaWarp = 9;
+constexpr int kLaunchRegs = 168;   // registers per thread at launch (checked on the host)
+constexpr int kProdRegs = 72, kEpiRegs = 216;
+static_assert(128 * kProdRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
+constexpr int kRegList = 15;       // candidates kept in registers when K - 1 <= 15
 
 struct Unit {
   int b, row0, nrows, q0, nt;
@@ -82,7 +86,7 @@ __device__ __forceinline__ float block_max(const uint32_t* v) {
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
-template <int DI, int BS>
+template <int DI, int BS, bool REG>
 __global__ void __launch_bounds__(kThreads, 1)
     index_fused_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len, int B, int Nq,
@@ -155,6 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     set_status(status, MSA_ERR_TIMEOUT);
   };
 
+  // Each register re-allocation sits at the top of its warpgroups' branch so
+  // that the compiler budgets each branch with its own register count.
+  if (warp >= kEpiWarps) {
+  tc::regs_dec<kProdRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
@@ -249,7 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(done_bar);
       tc::mbar_wait(done_bar, 0, &zero);
     }
+  }  // warps 10-11: idle
   } else {
+    tc::regs_inc<kEpiRegs>();
     // -------------------------------- epilogue --------------------------------
     const int m = warp >> 2, quarter = warp & 3;
     const int urow = m * 128 + quarter * 32 + lane;  // row within the unit = TMEM lane of tile m
@@ -273,6 +283,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // An accepted candidate costs at most log2(Kc) levels.
       int cnt = 0;
       uint64_t thr = 0;
+      // REG (K - 1 <= 15): the best candidates so far in registers, sorted
+      // descending and padded with key 0 (below every real key); an insertion
+      // is a branch-free compare-and-shift over the list, taken by the whole
+      // warp whenever one of its rows accepts (the others' lists stay as
+      // they are: their key is below every slot).
+      uint64_t L[kRegList];
+      int ncand = 0;
+#pragma unroll
+      for (int k = 0; k < kRegList; ++k) L[k] = 0;
+      auto offer_reg = [&](int t, float mx) {
+        const bool valid = cand_row && t < loc;
+        const uint64_t x = valid ? rank_key(mx, t) : 0ull;
+        ncand += valid ? 1 : 0;
+        if (__any_sync(0xffffffffu, x > L[kRegList - 1])) {
+#pragma unroll
+          for (int k = kRegList - 1; k > 0; --k) L[k] = x > L[k - 1] ? L[k - 1] : (x > L[k] ? x : L[k]);
+          L[0] = x > L[0] ? x : L[0];
+        }
+      };
       auto offer = [&](int t, float mx) {  // candidate block t with maximum mx
         if (t >= loc) return;
         const uint64_t key = rank_key(mx, t);
@@ -333,10 +362,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int bi = 0; bi < kChunk / BS; ++bi) bm[c * (kChunk / BS) + bi] = block_max<BS>(v + bi * BS);
         }
-        if (cand_row) {
+        if constexpr (REG) {
+#pragma unroll
+          for (int j = 0; j < kTileN / BS; ++j) offer_reg(n * (kTileN / BS) + j, bm[j]);
+        } else if (cand_row) {
 #pragma unroll 1
           for (int j = 0; j < kTileN / BS; ++j) offer(n * (kTileN / BS) + j, bm[j]);
         }
+      }
+      if constexpr (REG) {  // the best min(candidates, Kc) keys go to the row's slots
+        cnt = ncand < Kc ? ncand : Kc;
+#pragma unroll
+        for (int k = 0; k < kRegList; ++k)
+          if (k < cnt) my_list[k * kUnitRows] = L[k];
       }
       if (!alive || !active) continue;
       int32_t* out = sel + (int64_t(U.b) * NqG + row) * K;
@@ -431,28 +469,42 @@ cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t*
   const int nunits = B * ((NqG + kUnitRows - 1) / kUnitRows);
   const int grid = nunits < num_sms() ? nunits : num_sms();
   ProfScope prof("index_fused_tc", stream);
-#define MSA_FUSED(DI_, BS_)                                                                                     \
+  // The register split re-allocates exactly the launch allocation: a build
+  // that launches with another register count must not run (the increase
+  // would wait for registers that are never released).
+#define MSA_FUSED(DI_, BS_, REG_)                                                                               \
   do {                                                                                                          \
-    auto kern = index_fused_tc_kernel<DI_, BS_>;                                                               \
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));      \
+    auto kern = index_fused_tc_kernel<DI_, BS_, REG_>;                                                         \
+    cudaFuncAttributes fa;                                                                                      \
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);                                                           \
+    if (e != cudaSuccess) return e;                                                                            \
+    if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;  \
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));                    \
     if (e != cudaSuccess) return e;                                                                            \
     kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, q_offset, kv_len, B, Nq, Nk, G, K, nA, S, sel, status); \
   } while (0)
+#define MSA_FUSED_BS(DI_, REG_) \
+  do {                          \
+    if (Bs == 128)              \
+      MSA_FUSED(DI_, 128, REG_); \
+    else if (Bs == 64)          \
+      MSA_FUSED(DI_, 64, REG_);  \
+    else                        \
+      MSA_FUSED(DI_, 32, REG_);  \
+  } while (0)
+  const bool reg = K - 1 <= kRegList;
   if (di == 64) {
-    if (Bs == 128)
-      MSA_FUSED(64, 128);
-    else if (Bs == 64)
-      MSA_FUSED(64, 64);
+    if (reg)
+      MSA_FUSED_BS(64, true);
     else
-      MSA_FUSED(64, 32);
+      MSA_FUSED_BS(64, false);
   } else {
-    if (Bs == 128)
-      MSA_FUSED(32, 128);
-    else if (Bs == 64)
-      MSA_FUSED(32, 64);
+    if (reg)
+      MSA_FUSED_BS(32, true);
     else
-      MSA_FUSED(32, 32);
+      MSA_FUSED_BS(32, false);
   }
+#undef MSA_FUSED_BS
 #undef MSA_FUSED
   return cudaGetLastError();
 }
