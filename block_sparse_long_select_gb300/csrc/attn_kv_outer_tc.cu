@@ -677,13 +677,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// combine: one warp per (query, group). A slot's partials of the group's
-// heads are hpg consecutive partial rows (found through the reverse map),
-// stored chunk-major: 16-byte chunk c of row r in tile zg at
-// ((zg * D/8 + c) * 128 + r). Lane vector vi takes head vi % hpg and chunk
-// vi / hpg, so neighbouring lanes read neighbouring rows of one chunk. Each
-// lane owns NU vectors. Slots are merged in slot order with log-sum-exp
-// weights.
+// combine: persistent warps, each taking (query, group) items in a strided
+// loop. A slot's partials of the group's heads are hpg consecutive partial
+// rows (found through the reverse map), stored chunk-major: 16-byte chunk c
+// of row r in tile zg at ((zg * D/8 + c) * 128 + r). Lane vector vi takes
+// head vi % hpg and chunk vi / hpg, so neighbouring lanes read neighbouring
+// rows of one chunk. Each lane owns NU vectors. Slots are merged in slot
+// order with log-sum-exp weights. The next item's selection row and reverse
+// map row are loaded while the current item's partials are in flight.
 // ---------------------------------------------------------------------------
 template <int NU>
 __global__ void __launch_bounds__(256) attn_combine_kernel(
@@ -692,95 +693,125 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
     int Nq, int Nk, int Hq, int G, int K, int Bs, int nblk, int D, int c0, int cq, __nv_bfloat16* __restrict__ out,
     float* __restrict__ lse_out) {
   constexpr int kBatch = NU <= 2 ? 8 : (NU == 4 ? 4 : 2);  // slots whose loads are in flight together
-  __shared__ int slot_e[256 / 32][kMaxK];
-  const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  constexpr int kWarps = 256 / 32;
+  __shared__ int slot_e[kWarps][2][kMaxK];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  if (wid >= int64_t(cq) * G) return;
-  const int il = int(wid / G), g = int(wid % G);
+  const int64_t nitems = int64_t(cq) * G;
+  const int64_t stride = int64_t(gridDim.x) * kWarps;
   const int hpg = Hq / G;
   const int nvec = hpg * D / 8;  // 16-byte vectors per slot
-  const int i = c0 + il;
   const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
-  const int pos = sv.q0 + i;
-  // valid slots in slot order, as partial-row entries (via the reverse map)
-  const int32_t* srow = sel + ((int64_t(b) * Nq + i) * G + g) * K;
-  const int* rv = rev + (int64_t(il) * G + g) * K;
-  int nvalid = 0;
-  for (int k0 = 0; k0 < K; k0 += 32) {
-    const int k = k0 + lane;
-    const bool ok = k < K && sv.ok && entry_valid(srow[k], pos, Bs, nblk);
-    const unsigned bal = __ballot_sync(0xffffffffu, ok);
-    if (ok) slot_e[wl][nvalid + __popc(bal & ((1u << lane) - 1u))] = rv[k];
-    nvalid += __popc(bal);
-  }
-  __syncwarp();
   int head[NU], voff[NU];
-  float m[NU], wsum[NU], acc[NU][8];
 #pragma unroll
   for (int u = 0; u < NU; ++u) {
     const int vi = lane + 32 * u;
     head[u] = vi < nvec ? vi % hpg : 0;
     voff[u] = vi < nvec ? (vi / hpg) * 128 + head[u] : 0;  // chunk-major offset from the slot's first row
-    m[u] = -INFINITY;
-    wsum[u] = 0.f;
-#pragma unroll
-    for (int x = 0; x < 8; ++x) acc[u][x] = 0.f;
   }
-  // one pass, kBatch slots at a time: all their loads first, then a running
-  // log-sum-exp rescale (slot order is fixed: the result is deterministic)
-  for (int j0 = 0; j0 < nvalid; j0 += kBatch) {
-    float l[kBatch][NU];
-    uint4 raw[kBatch][NU];
+  // an item's selection and reverse-map entries for slots lane and lane + 32
+  int s_t[2], s_e[2];
+  auto meta_load = [&](int64_t it) {
+    const int il = int(it / G), g = int(it % G);
+    const int32_t* srow = sel + ((int64_t(b) * Nq + c0 + il) * G + g) * K;
+    const int* rv = rev + (int64_t(il) * G + g) * K;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const bool have = j0 + j < nvalid;
-      const int64_t R = have ? int64_t(slot_e[wl][j0 + j]) * hpg : 0;  // the slot's first partial row
-      const uint4* base = part_o + (R >> 7) * (D / 8) * 128 + (R & 127);
-#pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        const int vi = lane + 32 * u;
-        l[j][u] = have ? part_lse[R + head[u]] : -INFINITY;
-        raw[j][u] = (have && vi < nvec) ? base[voff[u]] : make_uint4(0, 0, 0, 0);
-      }
+    for (int h = 0; h < 2; ++h) {
+      const int k = lane + 32 * h;
+      s_t[h] = k < K ? srow[k] : -1;
+      s_e[h] = k < K ? rv[k] : 0;
     }
+  };
+  // valid slots in slot order, as partial-row entries, into slot_e[wl][buf]
+  auto meta_finish = [&](int64_t it, int buf) {
+    const int pos = sv.q0 + c0 + int(it / G);
+    int nv = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int k = lane + 32 * h;
+      const bool ok = k < K && sv.ok && entry_valid(s_t[h], pos, Bs, nblk);
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      if (ok) slot_e[wl][buf][nv + __popc(bal & ((1u << lane) - 1u))] = s_e[h];
+      nv += __popc(bal);
+    }
+    __syncwarp();
+    return nv;
+  };
+  int64_t item = int64_t(blockIdx.x) * kWarps + wl;
+  int buf = 0, nvalid = 0;
+  if (item < nitems) {
+    meta_load(item);
+    nvalid = meta_finish(item, buf);
+  }
+  for (; item < nitems; item += stride, buf ^= 1) {
+    const int64_t next = item + stride;
+    if (next < nitems) meta_load(next);
+    const int il = int(item / G), g = int(item % G);
+    const int i = c0 + il;
+    float m[NU], wsum[NU], acc[NU][8];
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
-      float mb = m[u];
+      m[u] = -INFINITY;
+      wsum[u] = 0.f;
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, l[j][u]);
-      const float rescale = m[u] > -INFINITY ? expf(m[u] - mb) : 0.f;
-      wsum[u] *= rescale;
-#pragma unroll
-      for (int x = 0; x < 8; ++x) acc[u][x] *= rescale;
+      for (int x = 0; x < 8; ++x) acc[u][x] = 0.f;
+    }
+    // kBatch slots at a time: all their loads first, then a running
+    // log-sum-exp rescale (slot order is fixed: the result is deterministic)
+    for (int j0 = 0; j0 < nvalid; j0 += kBatch) {
+      float l[kBatch][NU];
+      uint4 raw[kBatch][NU];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
-        const float wk = l[j][u] > -INFINITY ? expf(l[j][u] - mb) : 0.f;
-        wsum[u] += wk;
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
+        const bool have = j0 + j < nvalid;
+        const int64_t R = have ? int64_t(slot_e[wl][buf][j0 + j]) * hpg : 0;  // the slot's first partial row
+        const uint4* base = part_o + (R >> 7) * (D / 8) * 128 + (R & 127);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float2 f = __bfloat1622float2(h2[x]);
-          acc[u][2 * x] = fmaf(wk, f.x, acc[u][2 * x]);
-          acc[u][2 * x + 1] = fmaf(wk, f.y, acc[u][2 * x + 1]);
+        for (int u = 0; u < NU; ++u) {
+          const int vi = lane + 32 * u;
+          l[j][u] = have ? part_lse[R + head[u]] : -INFINITY;
+          raw[j][u] = (have && vi < nvec) ? base[voff[u]] : make_uint4(0, 0, 0, 0);
         }
       }
-      m[u] = mb;
-    }
-  }
-  __nv_bfloat16* dst = out + ((int64_t(b) * Nq + i) * Hq + g * hpg) * D;
 #pragma unroll
-  for (int u = 0; u < NU; ++u) {
-    const int vi = lane + 32 * u;
-    if (vi >= nvec) continue;
-    const float inv = wsum[u] > 0.f ? 1.f / wsum[u] : 0.f;
-    uint4 o;
-    o.x = pack_bf16(acc[u][0] * inv, acc[u][1] * inv);
-    o.y = pack_bf16(acc[u][2] * inv, acc[u][3] * inv);
-    o.z = pack_bf16(acc[u][4] * inv, acc[u][5] * inv);
-    o.w = pack_bf16(acc[u][6] * inv, acc[u][7] * inv);
-    *reinterpret_cast<uint4*>(dst + head[u] * D + (vi / hpg) * 8) = o;
-    if (lse_out && vi < hpg)
-      lse_out[(int64_t(b) * Nq + i) * Hq + g * hpg + head[u]] = wsum[u] > 0.f ? m[u] + logf(wsum[u]) : -INFINITY;
+      for (int u = 0; u < NU; ++u) {
+        float mb = m[u];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, l[j][u]);
+        const float rescale = m[u] > -INFINITY ? expf(m[u] - mb) : 0.f;
+        wsum[u] *= rescale;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) acc[u][x] *= rescale;
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const float wk = l[j][u] > -INFINITY ? expf(l[j][u] - mb) : 0.f;
+          wsum[u] += wk;
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float2 f = __bfloat1622float2(h2[x]);
+            acc[u][2 * x] = fmaf(wk, f.x, acc[u][2 * x]);
+            acc[u][2 * x + 1] = fmaf(wk, f.y, acc[u][2 * x + 1]);
+          }
+        }
+        m[u] = mb;
+      }
+    }
+    __nv_bfloat16* dst = out + ((int64_t(b) * Nq + i) * Hq + g * hpg) * D;
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+      const int vi = lane + 32 * u;
+      if (vi >= nvec) continue;
+      const float inv = wsum[u] > 0.f ? 1.f / wsum[u] : 0.f;
+      uint4 o;
+      o.x = pack_bf16(acc[u][0] * inv, acc[u][1] * inv);
+      o.y = pack_bf16(acc[u][2] * inv, acc[u][3] * inv);
+      o.z = pack_bf16(acc[u][4] * inv, acc[u][5] * inv);
+      o.w = pack_bf16(acc[u][6] * inv, acc[u][7] * inv);
+      *reinterpret_cast<uint4*>(dst + head[u] * D + (vi / hpg) * 8) = o;
+      if (lse_out && vi < hpg)
+        lse_out[(int64_t(b) * Nq + i) * Hq + g * hpg + head[u]] = wsum[u] > 0.f ? m[u] + logf(wsum[u]) : -INFINITY;
+    }
+    if (next < nitems) nvalid = meta_finish(next, buf ^ 1);
   }
 }
 
@@ -1007,13 +1038,21 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
       }
       {
         ProfScope pf("attn_combine", stream);
-        const int64_t warps = int64_t(cq) * G;
-        const unsigned cgrid = unsigned((warps * 32 + 255) / 256);
+        const int64_t items = int64_t(cq) * G;
         const int nvec = hpg * d / 8;
         __nv_bfloat16* o16 = static_cast<__nv_bfloat16*>(out);
-#define MSA_CMB(NU_)                                                                                            \
-  attn_combine_kernel<NU_><<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, rev, b, Nq, Nk, Hq, G, K, \
-                                                      Bs, nblk, d, c0, cq, o16, lse)
+        // persistent: as many CTAs as fit at once, each warp striding over items
+#define MSA_CMB(NU_)                                                                                           \
+  do {                                                                                                         \
+    auto kern = attn_combine_kernel<NU_>;                                                                      \
+    int per_sm = 0;                                                                                            \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)     \
+      per_sm = 1;                                                                                              \
+    const int64_t need = (items + 7) / 8;                                                                      \
+    const unsigned cgrid = unsigned(need < int64_t(per_sm) * grid ? need : int64_t(per_sm) * grid);            \
+    kern<<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, rev, b, Nq, Nk, Hq, G, K, Bs, nblk, d, \
+                                    c0, cq, o16, lse);                                                         \
+  } while (0)
         if (nvec <= 32)
           MSA_CMB(1);
         else if (nvec <= 64)
