@@ -68,10 +68,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 // address of 16-byte chunk `ch` (8 columns) of row `row` in a 128B-swizzled [NH][rows][128 B] tile
 __device__ __forceinline__ uint32_t swz_addr(uint32_t base, uint32_t half_bytes, int row, int ch) {
   return base + uint32_t(ch >> 3) * half_bytes + uint32_t(row) * 128u + ((uint32_t(ch & 7) ^ uint32_t(row & 7)) << 4);
@@ -475,6 +471,151 @@ __global__ void __launch_bounds__(kDiThreads, 1)
   }
 }
 
+__device__ __forceinline__ uint32_t ord_f32(float m) {
+  uint32_t u = __float_as_uint(m);
+  if (u == 0x80000000u) u = 0u;  // -0 == +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exact top-K of one (sequence, group) row by one warp, from the row's 32-key
+// sub-block maxima. Candidates are the blocks t < loc; their maxima become
+// order-preserving 32-bit values in registers (block t = lane + 32 j). The
+// (K-1)-th largest value v* is found two bits per round with warp sums; then
+// every candidate above v* is taken, plus the lowest-t candidates equal to v*
+// (ties go to the lower block), compacted in ascending t by ballots; the
+// local block loc closes the row. A row that sees at most K blocks takes them
+// all.
+constexpr int kWarpTopkPer = 32;  // candidates per lane: rows of up to 1024 blocks
+// R = sub-blocks per block (Bs / 32). The row's loc * R sub-block maxima are
+// first staged in the warp's shared-memory buffer (16-byte cp.async, all in
+// flight together), then each lane takes the maxima of its blocks.
+template <int R>
+__device__ void warp_topk_row(const float* __restrict__ sm, int loc, int K, int32_t* __restrict__ out, int lane,
+                              float* buf) {
+  if (loc + 1 <= K) {
+    for (int k = lane; k < K; k += 32) out[k] = k <= loc ? k : -1;
+    return;
+  }
+  const int n = loc * R;  // floats; the row starts on 16 bytes
+  const uint32_t sbuf = tc::smem_u32(buf);
+  for (int i = lane * 4; i < n; i += 128) {
+    const uint32_t bytes = uint32_t(min(4, n - i)) * 4u;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sbuf + uint32_t(i) * 4u), "l"(sm + i),
+                 "r"(bytes)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncwarp();
+  // Candidate values are >= 1 (an order-preserving key of 0 is raised to 1;
+  // only a NaN pattern has it) and padding is 0. Every threshold tested below
+  // is >= 1, so padding is never counted or taken and no loop needs a branch.
+  uint32_t v[kWarpTopkPer];
+#pragma unroll
+  for (int j = 0; j < kWarpTopkPer; ++j) {
+    const int t = lane + 32 * j;
+    float m = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < R; ++r) m = fmaxf(m, buf[(t < loc ? t : 0) * R + r]);
+    v[j] = t < loc ? max(ord_f32(m), 1u) : 0u;
+  }
+  const int need = K - 1;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  if (need <= 32) {
+    // The need-th largest lane maximum T bounds v* from below (need lanes
+    // hold a value >= T), so only candidates >= T can be selected. They are
+    // gathered in ascending t and ranked exactly by (value desc, t asc).
+    uint32_t lm = v[0];
+#pragma unroll
+    for (int j = 1; j < kWarpTopkPer; ++j) lm = max(lm, v[j]);
+    int lrank = 0;  // rank of this lane's maximum among the lanes' (ties to the lower lane)
+#pragma unroll
+    for (int o = 0; o < 32; ++o) {
+      const uint32_t x = __shfl_sync(0xffffffffu, lm, o);
+      lrank += (x > lm) || (x == lm && o < lane);
+    }
+    const unsigned at = __ballot_sync(0xffffffffu, lrank == need - 1);
+    const uint32_t T = max(__shfl_sync(0xffffffffu, lm, __ffs(at) - 1), 1u);
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < kWarpTopkPer; ++j) c += v[j] >= T;
+    const int C = __reduce_add_sync(0xffffffffu, c);
+    if (C <= 64) {
+      uint32_t* cv = reinterpret_cast<uint32_t*>(buf);  // the staged row is no longer needed
+      int* ct = reinterpret_cast<int*>(buf) + 64;
+      __syncwarp();
+      int base = 0;
+#pragma unroll
+      for (int j = 0; j < kWarpTopkPer; ++j) {
+        const bool f = v[j] >= T;
+        const unsigned fm = __ballot_sync(0xffffffffu, f);
+        if (f) {
+          const int q = base + __popc(fm & lt_mask);
+          cv[q] = v[j];
+          ct[q] = lane + 32 * j;
+        }
+        base += __popc(fm);
+      }
+      __syncwarp();
+      bool take[2];
+      int tt[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        const uint32_t vi = i < C ? cv[i] : 0u;
+        tt[h] = i < C ? ct[i] : 0;
+        int rank = 0;
+        for (int x = 0; x < C; ++x) rank += (cv[x] > vi) || (cv[x] == vi && x < i);  // candidate x has the lower t
+        take[h] = i < C && rank < need;
+      }
+      int o = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // candidates are in ascending t: compact the taken ones
+        const unsigned tm = __ballot_sync(0xffffffffu, take[h]);
+        if (take[h]) out[o + __popc(tm & lt_mask)] = tt[h];
+        o += __popc(tm);
+      }
+      if (lane == 0) out[K - 1] = loc;
+      return;
+    }
+  }
+  uint32_t prefix = 0;
+  for (int round = 0; round < 16; ++round) {
+    const int sh = 30 - 2 * round;
+    const uint32_t c1 = prefix | (1u << sh), c2 = prefix | (2u << sh), c3 = prefix | (3u << sh);
+    int n1 = 0, n2 = 0, n3 = 0;
+#pragma unroll
+    for (int j = 0; j < kWarpTopkPer; ++j) {
+      n1 += v[j] >= c1;
+      n2 += v[j] >= c2;
+      n3 += v[j] >= c3;
+    }
+    n1 = __reduce_add_sync(0xffffffffu, n1);
+    n2 = __reduce_add_sync(0xffffffffu, n2);
+    n3 = __reduce_add_sync(0xffffffffu, n3);
+    const uint32_t best = n3 >= need ? 3u : (n2 >= need ? 2u : (n1 >= need ? 1u : 0u));  // counts fall as the value grows
+    prefix |= best << sh;
+  }
+  // prefix = v* >= 1, the need-th largest value
+  int gt = 0;
+#pragma unroll
+  for (int j = 0; j < kWarpTopkPer; ++j) gt += v[j] > prefix;
+  const int ties = need - __reduce_add_sync(0xffffffffu, gt);
+  int base = 0, eq_seen = 0;
+#pragma unroll
+  for (int j = 0; j < kWarpTopkPer; ++j) {
+    const int t = lane + 32 * j;
+    const bool eqf = v[j] == prefix;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eqf);
+    const bool take = v[j] > prefix || (eqf && eq_seen + __popc(eqm & lt_mask) < ties);
+    const unsigned tm = __ballot_sync(0xffffffffu, take);
+    if (take) out[base + __popc(tm & lt_mask)] = t;
+    base += __popc(tm);
+    eq_seen += __popc(eqm);
+  }
+  if (lane == 0) out[K - 1] = loc;
+}
+
 // ---------------------------------------------------------------------------
 // decode_topk: one CTA per (sequence, group). Block maxima of the candidates
 // t < loc are assembled from the 32-key sub-block maxima and cached in shared
@@ -487,11 +628,6 @@ __global__ void __launch_bounds__(kDiThreads, 1)
 constexpr int kTkThreads = 256;
 constexpr int kTkMaxCand = 16384;
 
-__device__ __forceinline__ uint32_t ord_f32(float m) {
-  uint32_t u = __float_as_uint(m);
-  if (u == 0x80000000u) u = 0u;  // -0 == +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // exclusive block-wide scan of one int per thread (kTkThreads threads)
 __device__ __forceinline__ int block_exclusive_scan(int v, int* buf) {
@@ -590,6 +726,37 @@ __global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __
   if (tid == 0) out[K - 1] = loc;
 }
 
+// decode_topk for rows of at most 1024 blocks: one warp per (sequence,
+// group) row, eight rows per CTA, each warp staging its row's sub-block maxima
+// in its own 16 KB of shared memory (warp_topk_row).
+constexpr int kTkwRows = 8;
+constexpr uint32_t kTkwRowBytes = kWarpTopkPer * 32 * 4 * 4;  // 1024 blocks x 4 sub-blocks
+__global__ void __launch_bounds__(kTkwRows * 32) decode_topk_warp_kernel(
+    const float* __restrict__ sub_max, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
+    int Lmax, int G, int Bs, int K, int nsub, int rows, int32_t* __restrict__ sel, uint32_t* status) {
+  extern __shared__ __align__(16) uint8_t tkw_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kTkwRows + warp;  // b * G + g
+  if (row >= rows) return;
+  const int b = row / G;
+  int32_t* out = sel + int64_t(row) * K;
+  const SeqView sv = seq_view(q_offset, kv_len, b, 1, Lmax, false);
+  if (!sv.ok) {
+    for (int k = lane; k < K; k += 32) out[k] = -1;
+    if (lane == 0) set_status(status, MSA_ERR_BOUNDS);
+    return;
+  }
+  const int loc = sv.q0 / Bs;
+  const float* sm = sub_max + int64_t(row) * nsub;
+  float* buf = reinterpret_cast<float*>(tkw_smem + size_t(warp) * kTkwRowBytes);
+  if (Bs == 128)
+    warp_topk_row<4>(sm, loc, K, out, lane, buf);
+  else if (Bs == 64)
+    warp_topk_row<2>(sm, loc, K, out, lane, buf);
+  else
+    warp_topk_row<1>(sm, loc, K, out, lane, buf);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -678,12 +845,15 @@ bool decode_index_supported(int dtype, int B, int Nq, int G, int di, int Bs, int
          (Bs == 32 || Bs == 64 || Bs == 128) && K >= 1 && K <= kMaxK;
 }
 
-size_t decode_index_ws_bytes(int B, int G, int Nk) { return size_t(B) * G * ((Nk + 31) / 32) * sizeof(float); }
+// row stride of the sub-block maxima table: ceil(Lmax / 32) rounded up to 4
+// floats, so that every row starts on 16 bytes (16-byte copies of a row)
+static int decode_sub_stride(int Lmax) { return (((Lmax + 31) / 32) + 3) & ~3; }
+size_t decode_index_ws_bytes(int B, int G, int Nk) { return size_t(B) * G * decode_sub_stride(Nk) * sizeof(float); }
 
 cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
                                 int Lmax, int G, int Bs, int K, int32_t* sel, float* table, uint32_t* status,
                                 cudaStream_t stream) {
-  const int nsub = (Lmax + 31) / 32;
+  const int nsub = decode_sub_stride(Lmax);  // table row stride (>= sub-blocks per row)
   const int nblk = (Lmax + Bs - 1) / Bs;
   if (nblk > kTkMaxCand) return cudaErrorInvalidValue;
   CUtensorMap tmIK, tmIQ;
@@ -713,6 +883,17 @@ cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q
     decode_index_kernel<<<sms, kDiThreads, smem, stream>>>(tmIK, tmIQ, q_offset, kv_len, B, Lmax, G, nsub, table,
                                                            status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (nblk <= kWarpTopkPer * 32) {
+    ProfScope pf("decode_topk", stream);
+    const int rows = B * G;
+    const size_t tkw_smem = size_t(kTkwRows) * kTkwRowBytes;
+    if ((e = cudaFuncSetAttribute(decode_topk_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(tkw_smem))) != cudaSuccess)
+      return e;
+    decode_topk_warp_kernel<<<(rows + kTkwRows - 1) / kTkwRows, kTkwRows * 32, tkw_smem, stream>>>(
+        table, q_offset, kv_len, Lmax, G, Bs, K, nsub, rows, sel, status);
+    return cudaGetLastError();
   }
   {
     ProfScope pf("decode_topk", stream);

@@ -115,6 +115,8 @@ DECODE_VARIANTS = {
     "bs32_hpg8_d64": dict(Bs=32, K=12, Hq=16, Hkv=2, d=64),
     "bs128_hpg1": dict(Bs=128, K=5, Hq=8, Hkv=8),
     "bs128_hpg2_d64_di32": dict(Bs=128, K=6, Hq=8, Hkv=4, d=64, di=32),
+    # K - 1 > 32: the warp top-K takes its exact radix path instead of the lane-maximum filter
+    "bs32_k40_radix": dict(Bs=32, K=40),
 }
 
 
@@ -129,6 +131,18 @@ def test_decode_variants(name):
     assert np.array_equal(sel.cpu().numpy(), osel), name
     assert_close(out.float().cpu().numpy(), oout[:, 0], "bf16", name)
     assert_close(lse.cpu().numpy(), olse[:, 0], "bf16", name, lse=True)
+
+
+def test_decode_long_rows_cta_topk():
+    """Rows of more than 1024 blocks (Bs 32, caches of 40000 keys): the CTA-per-row top-K."""
+    w = synth.scaled(synth.WORKLOADS["decode_b64"], B=3, Nk=40000, kv_len_range=(33000, 40000), Bs=32, K=16)
+    t = device_inputs(w, DEV)
+    sel, out, lse = gpu_decode(w, t, DEV)
+    h = host_inputs(w)
+    osel, oout, olse = oracle_full(w, h)
+    assert np.array_equal(sel.cpu().numpy(), osel)
+    assert_close(out.float().cpu().numpy(), oout[:, 0], "bf16", w.name)
+    assert_close(lse.cpu().numpy(), olse[:, 0], "bf16", w.name, lse=True)
 
 
 def test_decode_query_offset_not_last():
