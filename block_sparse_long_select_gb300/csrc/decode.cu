@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
   const int gq = lane >> 2, tq = lane & 3;  // MMA fragment coordinates
   const int L = kv_len[b];
   const int pos = L - 1;
+  tc::griddep_launch_dependents();
+  tc::griddep_wait();  // launched early behind the top-K: sel is its output
   const int t = sel[int64_t(bg) * K + k];
   const bool seq_ok = L >= 1 && L <= Lmax;
   const bool valid = seq_ok && t >= 0 && t < nblk && t * BS <= pos;
@@ -303,6 +305,7 @@ __global__ void __launch_bounds__(kDiThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tc::griddep_launch_dependents();  // the top-K may launch now; it waits for this grid's maxima
 
   __shared__ int scan_part[kDiThreads];
   if (threadIdx.x == 0) {
@@ -656,6 +659,7 @@ __global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __
   const int row = blockIdx.x;  // b * G + g
   const int b = row / G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  tc::griddep_launch_dependents();  // attention may launch now; it waits for the selection
   int32_t* out = sel + int64_t(row) * K;
   const SeqView sv = seq_view(q_offset, kv_len, b, 1, Lmax, false);
   if (!sv.ok) {
@@ -670,6 +674,7 @@ __global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __
   }
   const int R = Bs / 32;  // sub-blocks per block
   const float* sm = sub_max + int64_t(row) * nsub;
+  tc::griddep_wait();  // the sub-block maxima come from the index kernel
   const int per = (loc + kTkThreads - 1) / kTkThreads;  // contiguous candidates per thread
   const int t0 = min(loc, tid * per), t1 = min(loc, t0 + per);
   for (int t = t0; t < t1; ++t) {
@@ -736,6 +741,7 @@ __global__ void __launch_bounds__(kTkwRows * 32) decode_topk_warp_kernel(
     int Lmax, int G, int Bs, int K, int nsub, int rows, int32_t* __restrict__ sel, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t tkw_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tc::griddep_launch_dependents();  // attention may launch now; it waits for the selection
   const int row = blockIdx.x * kTkwRows + warp;  // b * G + g
   if (row >= rows) return;
   const int b = row / G;
@@ -749,12 +755,32 @@ __global__ void __launch_bounds__(kTkwRows * 32) decode_topk_warp_kernel(
   const int loc = sv.q0 / Bs;
   const float* sm = sub_max + int64_t(row) * nsub;
   float* buf = reinterpret_cast<float*>(tkw_smem + size_t(warp) * kTkwRowBytes);
+  tc::griddep_wait();  // the sub-block maxima come from the index kernel
   if (Bs == 128)
     warp_topk_row<4>(sm, loc, K, out, lane, buf);
   else if (Bs == 64)
     warp_topk_row<2>(sm, loc, K, out, lane, buf);
   else
     warp_topk_row<1>(sm, loc, K, out, lane, buf);
+}
+
+// Launches `kern` with programmatic stream serialization: it may begin while
+// the previous kernel of the stream finishes, and waits (griddep_wait) before
+// it reads that kernel's output.
+template <typename... Params, typename... Args>
+cudaError_t launch_after_prev(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace
@@ -802,10 +828,11 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
     auto kern = decode_attn_kernel<D_, BS_, HPG_>;                                                              \
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess) \
       return e;                                                                                                  \
-    kern<<<unsigned(items), kDecThreads, smem, stream>>>(tmK, tmV, static_cast<const __nv_bfloat16*>(q), sel,     \
-                                                         kv_len, Lmax, Hq, G, K, nblk, scale_log2, part_o,        \
-                                                         part_ml, arrivals, static_cast<__nv_bfloat16*>(out),     \
-                                                         lse, status);                                            \
+    if ((e = launch_after_prev(kern, dim3(unsigned(items)), dim3(kDecThreads), smem, stream, tmK, tmV,              \
+                               static_cast<const __nv_bfloat16*>(q), sel, kv_len, Lmax, Hq, G, K, nblk, scale_log2,   \
+                               part_o, part_ml, arrivals, static_cast<__nv_bfloat16*>(out), lse, status)) !=         \
+        cudaSuccess)                                                                                             \
+      return e;                                                                                                  \
   } while (0)
 #define MSA_DEC_BS(D_, HPG_)  \
   do {                        \
@@ -891,8 +918,10 @@ cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q
     if ((e = cudaFuncSetAttribute(decode_topk_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(tkw_smem))) != cudaSuccess)
       return e;
-    decode_topk_warp_kernel<<<(rows + kTkwRows - 1) / kTkwRows, kTkwRows * 32, tkw_smem, stream>>>(
-        table, q_offset, kv_len, Lmax, G, Bs, K, nsub, rows, sel, status);
+    if ((e = launch_after_prev(decode_topk_warp_kernel, dim3((rows + kTkwRows - 1) / kTkwRows), dim3(kTkwRows * 32),
+                               tkw_smem, stream, static_cast<const float*>(table), q_offset, kv_len, Lmax, G, Bs, K,
+                               nsub, rows, sel, status)) != cudaSuccess)
+      return e;
     return cudaGetLastError();
   }
   {
@@ -902,8 +931,10 @@ cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q
         (e = cudaFuncSetAttribute(decode_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tk_smem))) !=
             cudaSuccess)
       return e;
-    decode_topk_kernel<<<B * G, kTkThreads, tk_smem, stream>>>(table, q_offset, kv_len, Lmax, G, Bs, K, nsub, sel,
-                                                               status);
+    if ((e = launch_after_prev(decode_topk_kernel, dim3(B * G), dim3(kTkThreads), tk_smem, stream,
+                               static_cast<const float*>(table), q_offset, kv_len, Lmax, G, Bs, K, nsub, sel, status)) !=
+        cudaSuccess)
+      return e;
   }
   return cudaGetLastError();
 }

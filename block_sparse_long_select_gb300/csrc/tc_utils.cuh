@@ -58,6 +58,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return true;
 }
 
+// ---- programmatic dependent launch --------------------------------------------
+// Waits until the grids this one depends on have completed and their writes
+// are visible (returns at once for a grid launched without programmatic
+// stream serialization).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allows the next grid of the stream, if it was launched with programmatic
+// stream serialization, to begin launching; it still waits (griddep_wait)
+// for this grid to complete before it reads what this grid writes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA --------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
