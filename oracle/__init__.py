@@ -43,6 +43,9 @@ def _load(path):
     lib.msa_oracle_index_select.argtypes = [vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp,
                                             i32]
     lib.msa_oracle_index_select.restype = i32
+    lib.msa_oracle_index_select_v.argtypes = [vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp,
+                                              vp, i32]
+    lib.msa_oracle_index_select_v.restype = i32
     lib.msa_oracle_sparse_attn.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32,
                                            i32, f64, vp, vp, i32]
     lib.msa_oracle_sparse_attn.restype = i32
@@ -65,10 +68,12 @@ def _c(a, dtype):
 
 
 def index_select(iq_rows, ik, row_b, row_i, q_offset, kv_len, Bs, K, want_block_max=False, nthreads=None,
-                 lib=None):
+                 lib=None, force_start=False):
     """Index Branch for listed rows.
 
     iq_rows [n, G, di]; ik [B, Nk, di]; row_b/row_i [n]; q_offset/kv_len [B].
+    force_start keeps block 0 as well as the local block (the experiments'
+    hard-coded sequence-start ablation; needs K >= 2).
     Returns sel [n, G, K] int32 (and block_max [n, G, nblk] fp64 if asked).
     """
     iq_rows = _c(iq_rows, np.float32)
@@ -81,10 +86,11 @@ def index_select(iq_rows, ik, row_b, row_i, q_offset, kv_len, Bs, K, want_block_
     nblk = (Nk + Bs - 1) // Bs
     sel = np.empty((n, G, K), dtype=np.int32)
     bmax = np.empty((n, G, nblk), dtype=np.float64) if want_block_max else None
-    rc = (lib or _lib()).msa_oracle_index_select(iq_rows.ctypes.data, ik.ctypes.data, row_b.ctypes.data,
-                                        row_i.ctypes.data, n, q_offset.ctypes.data, kv_len.ctypes.data, B, Nk, G,
-                                        di, Bs, K, sel.ctypes.data,
-                                        bmax.ctypes.data if bmax is not None else None, nthreads or threads())
+    rc = (lib or _lib()).msa_oracle_index_select_v(iq_rows.ctypes.data, ik.ctypes.data, row_b.ctypes.data,
+                                                   row_i.ctypes.data, n, q_offset.ctypes.data, kv_len.ctypes.data,
+                                                   B, Nk, G, di, Bs, K, 1 if force_start else 0, sel.ctypes.data,
+                                                   bmax.ctypes.data if bmax is not None else None,
+                                                   nthreads or threads())
     if rc != 0:
         raise ValueError("oracle index_select rejected its arguments")
     return (sel, bmax) if want_block_max else sel

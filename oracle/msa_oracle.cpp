@@ -26,6 +26,11 @@
 //  cannot change a ranking); the attention scale is 1/sqrt(d) unless given;
 //  the causal mask keeps key j iff j <= pos, pos = q_offset[b] + i.
 //
+// Variant (same summary, section "实验" (Experiments)): the ablation that
+// hard-codes the sequence-start block as well as the local window. With
+// force_start, block 0 is kept like the local block and the other K-2 come
+// from the ranking of blocks 1..loc-1.
+//
 // Parity pins for every function here live in tests/test_oracle_pins.py.
 #include <algorithm>
 #include <cmath>
@@ -56,7 +61,7 @@ void parallel_rows(int64_t nrows, int nthreads, F&& f) {
 // Writes K entries of `sel` (ascending block ids, -1 padded) and, if given,
 // nblk entries of `bmax` (NaN where a block is not visible).
 void index_select_one(const float* iq_g, const float* ik_b, int di, int pos, int L, int Bs, int K, int nblk,
-                      int* sel, double* bmax) {
+                      bool force_start, int* sel, double* bmax) {
   const int jmax = std::min(pos, L - 1);  // last causally visible key
   const int loc = pos / Bs;               // block holding the query
   std::vector<double> M(loc + 1, -std::numeric_limits<double>::infinity());
@@ -73,13 +78,16 @@ void index_select_one(const float* iq_g, const float* ik_b, int di, int pos, int
   if (loc + 1 <= K) {
     for (int t = 0; t <= loc; ++t) chosen.push_back(t);  // every visible block
   } else {
-    std::vector<int> cand(loc);
-    for (int t = 0; t < loc; ++t) cand[t] = t;
+    const int first = force_start ? 1 : 0;  // block 0 is kept outright in the variant
+    std::vector<int> cand;
+    for (int t = first; t < loc; ++t) cand.push_back(t);
     std::sort(cand.begin(), cand.end(), [&](int a, int b) {
       if (M[a] != M[b]) return M[a] > M[b];  // higher block maximum first
       return a < b;                          // tie: lower block index
     });
-    for (int k = 0; k < K - 1; ++k) chosen.push_back(cand[k]);
+    const int ranked = K - 1 - first;
+    for (int k = 0; k < ranked; ++k) chosen.push_back(cand[k]);
+    if (force_start) chosen.push_back(0);
     chosen.push_back(loc);  // the query's own block is always kept
     std::sort(chosen.begin(), chosen.end());
   }
@@ -97,11 +105,13 @@ extern "C" {
 //   q_offset, kv_len [B]       pos = q_offset[b] + i; keys j < kv_len[b]
 //   sel      [nrows, G, K]     out: ascending block ids, -1 padded
 //   block_max [nrows, G, nblk] out (optional): fp64 block maxima, NaN if not visible
-int msa_oracle_index_select(const float* iq_rows, const float* ik, const int32_t* row_b, const int32_t* row_i,
-                            int64_t nrows, const int32_t* q_offset, const int32_t* kv_len, int B, int Nk, int G,
-                            int di, int Bs, int K, int32_t* sel, double* block_max, int nthreads) {
+//   force_start              0: only the local block is forced; 1: block 0 too (K >= 2)
+int msa_oracle_index_select_v(const float* iq_rows, const float* ik, const int32_t* row_b, const int32_t* row_i,
+                              int64_t nrows, const int32_t* q_offset, const int32_t* kv_len, int B, int Nk, int G,
+                              int di, int Bs, int K, int force_start, int32_t* sel, double* block_max, int nthreads) {
   if (!iq_rows || !ik || !row_b || !row_i || !q_offset || !kv_len || !sel) return 1;
   if (B < 1 || Nk < 1 || G < 1 || di < 1 || Bs < 1 || K < 1 || nrows < 0) return 1;
+  if (force_start != 0 && (force_start != 1 || K < 2)) return 1;
   const int nblk = (Nk + Bs - 1) / Bs;
   for (int64_t r = 0; r < nrows; ++r) {
     const int b = row_b[r];
@@ -114,10 +124,17 @@ int msa_oracle_index_select(const float* iq_rows, const float* ik, const int32_t
     const int pos = q_offset[b] + row_i[r];
     for (int g = 0; g < G; ++g) {
       index_select_one(iq_rows + (r * G + g) * di, ik + int64_t(b) * Nk * di, di, pos, kv_len[b], Bs, K, nblk,
-                       sel + (r * G + g) * K, block_max ? block_max + (r * G + g) * nblk : nullptr);
+                       force_start != 0, sel + (r * G + g) * K, block_max ? block_max + (r * G + g) * nblk : nullptr);
     }
   });
   return 0;
+}
+
+int msa_oracle_index_select(const float* iq_rows, const float* ik, const int32_t* row_b, const int32_t* row_i,
+                            int64_t nrows, const int32_t* q_offset, const int32_t* kv_len, int B, int Nk, int G,
+                            int di, int Bs, int K, int32_t* sel, double* block_max, int nthreads) {
+  return msa_oracle_index_select_v(iq_rows, ik, row_b, row_i, nrows, q_offset, kv_len, B, Nk, G, di, Bs, K, 0, sel,
+                                   block_max, nthreads);
 }
 
 // Main Branch for a list of query rows: exact softmax attention over the

@@ -11,6 +11,9 @@
 * the masked-dense restatement (selected blocks as an explicit attention mask)
   equals torch's SDPA for partial selections, with ragged offsets / lengths;
 * decode at length L equals the prefill row at position L-1;
+* the forced sequence-start variant: structure, a second implementation, and
+  its equivalences with the plain selection when block 0 is the strongest or
+  the weakest block;
 * planted mistakes in a copy of the oracle source fail at least one pin.
 """
 import math
@@ -100,6 +103,23 @@ def argmax_selection(M, loc, K):
         chosen.append(best)
         avail.remove(best)
     return sorted(chosen + [loc])
+
+
+def argmax_selection_start(M, loc, K):
+    """Second implementation of the forced-start variant: blocks 0 and loc,
+    plus K-2 rounds of arg-max over blocks 1..loc-1."""
+    if loc + 1 <= K:
+        return list(range(loc + 1)) + [-1] * (K - loc - 1)
+    avail = list(range(1, loc))
+    chosen = []
+    for _ in range(K - 2):
+        best = None
+        for t in avail:
+            if best is None or M[t] > M[best]:
+                best = t
+        chosen.append(best)
+        avail.remove(best)
+    return sorted(chosen + [0, loc])
 
 
 def oracle_all(q, k, v, iq, ik, Bs, K, q_offset, kv_len, lib=None, scale=0.0):
@@ -272,8 +292,47 @@ def pin_decode_equals_prefill_row(lib=None):
         assert np.abs(dout[:, 0] - out[:, L - 1]).max() < 1e-12
 
 
+def pin_force_start(lib=None):
+    """Forced sequence-start variant: structure, a second implementation, and
+    two equivalences with the plain selection that fix its meaning: when block
+    0 is the strongest block the two selections agree; when it is the weakest,
+    the variant equals {0} plus the plain selection with one slot fewer."""
+    for seed, Bs, K in [(11, 8, 4), (12, 4, 7), (13, 16, 3)]:
+        q, k, v, iq, ik, qo, kl = rand_problem(seed, q_offset=[0, 17], kv_len=[96, 96])
+        Nq = 79
+        iq = iq[:, :Nq]
+        rb, ri = oracle.all_rows(2, Nq)
+        sel, bm = oracle.index_select(iq.reshape(-1, 2, 8), ik, rb, ri, qo, kl, Bs, K, want_block_max=True,
+                                      lib=lib, force_start=True)
+        for r in range(len(rb)):
+            loc = (qo[rb[r]] + ri[r]) // Bs
+            for g in range(2):
+                s = sel[r, g]
+                valid = s[s >= 0]
+                assert len(valid) == min(K, loc + 1) and (s[len(valid):] == -1).all()
+                assert (np.diff(valid) > 0).all() and 0 in valid and loc in valid
+                assert list(s) == argmax_selection_start(bm[r, g], loc, K)
+    # block 0 strongest / weakest: index query e0, index key dim 0 = +-100 on block 0
+    B, Nq, Nk, di, Bs, K = 1, 64, 64, 4, 4, 5
+    rb, ri = oracle.all_rows(B, Nq)
+    iq = np.random.default_rng(3).integers(-3, 4, (B * Nq, 1, di)).astype(np.float32)
+    iq[:, 0, 0] = 1.0
+    for big, rel in [(100.0, "equal"), (-100.0, "one_fewer")]:
+        ik = np.random.default_rng(4).integers(-3, 4, (B, Nk, di)).astype(np.float32)
+        ik[0, :Bs, 0] = big
+        forced = oracle.index_select(iq, ik, rb, ri, [0], [Nk], Bs, K, lib=lib, force_start=True)
+        if rel == "equal":
+            plain = oracle.index_select(iq, ik, rb, ri, [0], [Nk], Bs, K, lib=lib)
+            assert np.array_equal(forced, plain)
+        else:
+            plain = oracle.index_select(iq, ik, rb, ri, [0], [Nk], Bs, K - 1, lib=lib)
+            for i in range(Nq):
+                if i // Bs + 1 > K:
+                    assert forced[i, 0].tolist() == sorted([0] + plain[i, 0].tolist())
+
+
 PINS = [pin_golden, pin_blockmax_bruteforce, pin_selection_invariants, pin_closed_forms, pin_dense_equals_sdpa,
-        pin_masked_dense_equals_sdpa, pin_attention_special_cases, pin_decode_equals_prefill_row]
+        pin_masked_dense_equals_sdpa, pin_attention_special_cases, pin_decode_equals_prefill_row, pin_force_start]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -294,6 +353,8 @@ MUTATIONS = {
     "score_dim_off_by_one": ("for (int c = 0; c < di; ++c) s +=", "for (int c = 1; c < di; ++c) s +="),
     "blockmax_keeps_min": ("if (s > M[t]) M[t] = s;", "if (s < M[t] || M[t] == -std::numeric_limits<double>::infinity()) M[t] = s;"),
     "selects_lowest_maxima": ("if (M[a] != M[b]) return M[a] > M[b];", "if (M[a] != M[b]) return M[a] < M[b];"),
+    "start_variant_ranks_one_too_many": ("const int ranked = K - 1 - first;", "const int ranked = K - 1;"),
+    "start_variant_ranks_block_zero": ("const int first = force_start ? 1 : 0;", "const int first = 0;"),
 }
 
 
