@@ -5,14 +5,17 @@ Argument marshalling over the C ABI of ``libmsa.so`` (declared in
 PyTorch only provides device memory and the current stream. The functions
 carry the C names:
 
-    msa_workspace_size, msa_index_select, msa_sparse_attn_prefill,
-    msa_sparse_attn_decode, msa_read_status, msa_status_string
+    msa_workspace_size, msa_index_select, msa_index_select_v,
+    msa_sparse_attn_prefill, msa_sparse_attn_decode, msa_read_status,
+    msa_status_string
 
 There is no CPU fallback: if ``libmsa.so`` is missing or was not built for
 this GPU, every call raises.
 """
 from ._lib import (  # noqa: F401
     MSA_BF16,
+    MSA_FORCE_LOCAL,
+    MSA_FORCE_START,
     MSA_FP32,
     MSA_OP_DECODE,
     MSA_OP_INDEX_SELECT,
@@ -22,6 +25,7 @@ from ._lib import (  # noqa: F401
     load_library,
     msa_index_select,
     msa_index_select_noalloc,
+    msa_index_select_v,
     msa_profile_begin,
     msa_profile_end,
     msa_read_status,

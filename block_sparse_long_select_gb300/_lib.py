@@ -7,6 +7,7 @@ from functools import lru_cache
 
 MSA_BF16, MSA_FP32 = 0, 1
 MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE = 0, 1, 2
+MSA_FORCE_LOCAL, MSA_FORCE_START = 1, 2
 STATUS_NAMES = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
                 4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_BOUNDS"}
 
@@ -15,6 +16,7 @@ _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_s
 SIGNATURES = {
     "msa_workspace_size": (_sz, [_i32] * 11),
     "msa_index_select": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 8 + [_vp, _vp, _vp, _sz, _vp]),
+    "msa_index_select_v": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 9 + [_vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_attn_prefill": (_i32, [_vp] * 6 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_attn_decode": (_i32, [_vp] * 5 + [_i32] * 7 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_read_status": (_i32, [_vp, _vp]),
@@ -100,6 +102,12 @@ def workspace(nbytes: int, device="cuda"):
 
 def msa_index_select(iq, ik, q_offset, kv_len, Bs, K, sel=None, block_max=None, ws=None, stream=None):
     """iq [B,Nq,G,di], ik [B,Nk,di] -> sel [B,Nq,G,K] int32 (see include/msa.h)."""
+    return msa_index_select_v(iq, ik, q_offset, kv_len, Bs, K, MSA_FORCE_LOCAL, sel, block_max, ws, stream)
+
+
+def msa_index_select_v(iq, ik, q_offset, kv_len, Bs, K, force, sel=None, block_max=None, ws=None, stream=None):
+    """msa_index_select with a choice of forced blocks: force = MSA_FORCE_LOCAL,
+    or MSA_FORCE_LOCAL | MSA_FORCE_START to keep block 0 as well (see include/msa.h)."""
     import torch
 
     _need_cuda(iq, ik, q_offset, kv_len, sel, block_max)
@@ -110,10 +118,10 @@ def msa_index_select(iq, ik, q_offset, kv_len, Bs, K, sel=None, block_max=None, 
         sel = torch.empty((B, Nq, G, K), dtype=torch.int32, device=iq.device)
     if ws is None:
         ws = workspace(msa_workspace_size(MSA_OP_INDEX_SELECT, B, Nq, Nk, G, 0, 0, di, Bs, K, dt), iq.device)
-    code = load_library().msa_index_select(_ptr(iq), _ptr(ik), _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, G, di, Bs,
-                                           K, dt, _ptr(sel), _ptr(block_max), _ptr(ws), ws.numel(),
-                                           _stream(stream, iq.device))
-    _check(code, "msa_index_select")
+    code = load_library().msa_index_select_v(_ptr(iq), _ptr(ik), _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, G, di,
+                                             Bs, K, dt, int(force), _ptr(sel), _ptr(block_max), _ptr(ws), ws.numel(),
+                                             _stream(stream, iq.device))
+    _check(code, "msa_index_select_v")
     return sel
 
 

@@ -493,8 +493,8 @@ constexpr int kWarpTopkPer = 32;  // candidates per lane: rows of up to 1024 blo
 // first staged in the warp's shared-memory buffer (16-byte cp.async, all in
 // flight together), then each lane takes the maxima of its blocks.
 template <int R>
-__device__ void warp_topk_row(const float* __restrict__ sm, int loc, int K, int32_t* __restrict__ out, int lane,
-                              float* buf) {
+__device__ void warp_topk_row(const float* __restrict__ sm, int loc, int K, int fs, int32_t* __restrict__ out,
+                              int lane, float* buf) {
   if (loc + 1 <= K) {
     for (int k = lane; k < K; k += 32) out[k] = k <= loc ? k : -1;
     return;
@@ -520,9 +520,15 @@ __device__ void warp_topk_row(const float* __restrict__ sm, int loc, int K, int3
     float m = -INFINITY;
 #pragma unroll
     for (int r = 0; r < R; ++r) m = fmaxf(m, buf[(t < loc ? t : 0) * R + r]);
-    v[j] = t < loc ? max(ord_f32(m), 1u) : 0u;
+    v[j] = (t < loc && t >= fs) ? max(ord_f32(m), 1u) : 0u;  // fs = 1: block 0 is kept outright
   }
-  const int need = K - 1;
+  const int need = K - 1 - fs;
+  if (fs && lane == 0) out[0] = 0;
+  out += fs;  // the ranked blocks follow block 0
+  if (need == 0) {
+    if (lane == 0) out[0] = loc;
+    return;
+  }
   const unsigned lt_mask = (1u << lane) - 1u;
   if (need <= 32) {
     // The need-th largest lane maximum T bounds v* from below (need lanes
@@ -578,7 +584,7 @@ __device__ void warp_topk_row(const float* __restrict__ sm, int loc, int K, int3
         if (take[h]) out[o + __popc(tm & lt_mask)] = tt[h];
         o += __popc(tm);
       }
-      if (lane == 0) out[K - 1] = loc;
+      if (lane == 0) out[need] = loc;
       return;
     }
   }
@@ -616,7 +622,7 @@ __device__ void warp_topk_row(const float* __restrict__ sm, int loc, int K, int3
     base += __popc(tm);
     eq_seen += __popc(eqm);
   }
-  if (lane == 0) out[K - 1] = loc;
+  if (lane == 0) out[need] = loc;
 }
 
 // ---------------------------------------------------------------------------
@@ -651,8 +657,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* buf) {
 __global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __restrict__ sub_max,
                                                                  const int32_t* __restrict__ q_offset,
                                                                  const int32_t* __restrict__ kv_len, int Lmax, int G,
-                                                                 int Bs, int K, int nsub, int32_t* __restrict__ sel,
-                                                                 uint32_t* status) {
+                                                                 int Bs, int K, int fs, int nsub,
+                                                                 int32_t* __restrict__ sel, uint32_t* status) {
   extern __shared__ uint32_t vals[];  // [loc] order-preserving block maxima
   __shared__ int wsum[2][kTkThreads / 32][3];
   __shared__ int scan_buf[kTkThreads];
@@ -674,15 +680,22 @@ __global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __
   }
   const int R = Bs / 32;  // sub-blocks per block
   const float* sm = sub_max + int64_t(row) * nsub;
+  const int need = K - 1 - fs;  // fs = 1: block 0 is kept outright, like the local block
+  if (need == 0) {
+    if (tid == 0) {
+      out[0] = 0;
+      out[1] = loc;
+    }
+    return;
+  }
   tc::griddep_wait();  // the sub-block maxima come from the index kernel
   const int per = (loc + kTkThreads - 1) / kTkThreads;  // contiguous candidates per thread
   const int t0 = min(loc, tid * per), t1 = min(loc, t0 + per);
   for (int t = t0; t < t1; ++t) {
     float m = sm[t * R];
     for (int r = 1; r < R; ++r) m = fmaxf(m, sm[t * R + r]);
-    vals[t] = ord_f32(m);
+    vals[t] = t >= fs ? max(ord_f32(m), 1u) : 0u;  // candidates >= 1; every threshold below is >= 1
   }
-  const int need = K - 1;
   uint32_t prefix = 0;
   for (int round = 0; round < 16; ++round) {
     const int sh = 30 - 2 * round;
@@ -722,13 +735,16 @@ __global__ void __launch_bounds__(kTkThreads) decode_topk_kernel(const float* __
   const int ties = need - gt_all;
   const int take_eq = max(0, min(eq, ties - eq_before));  // the lowest-t equals go first
   const int my = gt + take_eq;
-  int o = block_exclusive_scan(my, scan_buf);
+  int o = fs + block_exclusive_scan(my, scan_buf);
   int eq_seen = 0;
   for (int t = t0; t < t1; ++t) {
     const uint32_t v = vals[t];
     if (v > prefix || (v == prefix && eq_seen++ < take_eq)) out[o++] = t;
   }
-  if (tid == 0) out[K - 1] = loc;
+  if (tid == 0) {
+    if (fs) out[0] = 0;
+    out[K - 1] = loc;
+  }
 }
 
 // decode_topk for rows of at most 1024 blocks: one warp per (sequence,
@@ -738,7 +754,7 @@ constexpr int kTkwRows = 8;
 constexpr uint32_t kTkwRowBytes = kWarpTopkPer * 32 * 4 * 4;  // 1024 blocks x 4 sub-blocks
 __global__ void __launch_bounds__(kTkwRows * 32) decode_topk_warp_kernel(
     const float* __restrict__ sub_max, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
-    int Lmax, int G, int Bs, int K, int nsub, int rows, int32_t* __restrict__ sel, uint32_t* status) {
+    int Lmax, int G, int Bs, int K, int fs, int nsub, int rows, int32_t* __restrict__ sel, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t tkw_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   tc::griddep_launch_dependents();  // attention may launch now; it waits for the selection
@@ -757,11 +773,11 @@ __global__ void __launch_bounds__(kTkwRows * 32) decode_topk_warp_kernel(
   float* buf = reinterpret_cast<float*>(tkw_smem + size_t(warp) * kTkwRowBytes);
   tc::griddep_wait();  // the sub-block maxima come from the index kernel
   if (Bs == 128)
-    warp_topk_row<4>(sm, loc, K, out, lane, buf);
+    warp_topk_row<4>(sm, loc, K, fs, out, lane, buf);
   else if (Bs == 64)
-    warp_topk_row<2>(sm, loc, K, out, lane, buf);
+    warp_topk_row<2>(sm, loc, K, fs, out, lane, buf);
   else
-    warp_topk_row<1>(sm, loc, K, out, lane, buf);
+    warp_topk_row<1>(sm, loc, K, fs, out, lane, buf);
 }
 
 // Launches `kern` with programmatic stream serialization: it may begin while
@@ -878,7 +894,7 @@ static int decode_sub_stride(int Lmax) { return (((Lmax + 31) / 32) + 3) & ~3; }
 size_t decode_index_ws_bytes(int B, int G, int Nk) { return size_t(B) * G * decode_sub_stride(Nk) * sizeof(float); }
 
 cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
-                                int Lmax, int G, int Bs, int K, int32_t* sel, float* table, uint32_t* status,
+                                int Lmax, int G, int Bs, int K, int fs, int32_t* sel, float* table, uint32_t* status,
                                 cudaStream_t stream) {
   const int nsub = decode_sub_stride(Lmax);  // table row stride (>= sub-blocks per row)
   const int nblk = (Lmax + Bs - 1) / Bs;
@@ -920,7 +936,7 @@ cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q
       return e;
     if ((e = launch_after_prev(decode_topk_warp_kernel, dim3((rows + kTkwRows - 1) / kTkwRows), dim3(kTkwRows * 32),
                                tkw_smem, stream, static_cast<const float*>(table), q_offset, kv_len, Lmax, G, Bs, K,
-                               nsub, rows, sel, status)) != cudaSuccess)
+                               fs, nsub, rows, sel, status)) != cudaSuccess)
       return e;
     return cudaGetLastError();
   }
@@ -932,7 +948,8 @@ cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q
             cudaSuccess)
       return e;
     if ((e = launch_after_prev(decode_topk_kernel, dim3(B * G), dim3(kTkThreads), tk_smem, stream,
-                               static_cast<const float*>(table), q_offset, kv_len, Lmax, G, Bs, K, nsub, sel, status)) !=
+                               static_cast<const float*>(table), q_offset, kv_len, Lmax, G, Bs, K, fs, nsub, sel,
+                               status)) !=
         cudaSuccess)
       return e;
   }

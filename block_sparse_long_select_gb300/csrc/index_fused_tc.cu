@@ -3,7 +3,9 @@
 //                 fp32 accumulators in TMEM),
 //   block max     pooled straight out of TMEM in the epilogue,
 //   top-K         a running exact top-(K-1) per row over the candidate blocks
-//                 t < loc, then the local block appended,
+//                 t < loc, then the local block appended (with the sequence
+//                 start forced as well: top-(K-2) over 1 <= t < loc, plus
+//                 block 0),
 // so neither the token-score matrix nor the block-max table ever reaches HBM.
 // (hyper.ai summary of paper 2606.13392, section "方法": per GQA group, dot-
 //  product scores of the index query against every visible key, Block Max
@@ -50,7 +52,7 @@ struct Unit {
 };
 
 __device__ __forceinline__ Unit get_unit(int u, int nunits, int nrb, int NqG, int G, int Nq, int Nk, int Bs, int K,
-                                         const int32_t* q_offset, const int32_t* kv_len) {
+                                         int fs, const int32_t* q_offset, const int32_t* kv_len) {
   Unit U;
   const int gu = nunits - 1 - u;  // longest units (latest rows) first
   U.b = gu / nrb;
@@ -61,8 +63,9 @@ __device__ __forceinline__ Unit get_unit(int u, int nunits, int nrb, int NqG, in
   U.ok = sv.ok;
   U.q0 = sv.q0;
   const int maxloc = sv.ok ? (sv.q0 + (U.row0 + U.nrows - 1) / G) / Bs : 0;
-  // key tiles are needed only if some row has more visible blocks than K
-  U.nt = (sv.ok && K > 1 && maxloc + 1 > K) ? (maxloc * Bs + kTileN - 1) / kTileN : 0;
+  // key tiles are needed only if some row has more visible blocks than K and
+  // at least one block is ranked (K - 1 - fs of them)
+  U.nt = (sv.ok && K - fs > 1 && maxloc + 1 > K) ? (maxloc * Bs + kTileN - 1) / kTileN : 0;
   return U;
 }
 
@@ -90,7 +93,7 @@ template <int DI, int BS, bool REG>
 __global__ void __launch_bounds__(kThreads, 1)
     index_fused_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len, int B, int Nq,
-                          int Nk, int G, int K, int nA, int S, int32_t* __restrict__ sel, uint32_t* status) {
+                          int Nk, int G, int K, int fs, int nA, int S, int32_t* __restrict__ sel, uint32_t* status) {
   constexpr uint32_t kABytes = kUnitRows * DI * 2;   // one unit of index queries
   constexpr uint32_t kATile = 128 * DI * 2;          // one 128-row MMA tile
   constexpr uint32_t kBBytes = kTileN * DI * 2;      // one key tile
@@ -105,9 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* a_buf = smem;                                       // nA x kABytes
   uint8_t* b_buf = a_buf + size_t(nA) * kABytes;               // S x kBBytes
-  const int Kc = K - 1;
-  uint64_t* lists = reinterpret_cast<uint64_t*>(b_buf + size_t(S) * kBBytes);  // [Kc][256]
-  uint64_t* bars = lists + size_t(Kc > 0 ? Kc : 1) * kUnitRows;
+  const int Kl = K - 1;  // list slots per row (the host sizes shared memory for K - 1)
+  const int Kc = K - 1 - fs;  // blocks ranked per row: fs = 1 keeps block 0 outright, like the local block
+  uint64_t* lists = reinterpret_cast<uint64_t*>(b_buf + size_t(S) * kBBytes);  // [Kl][256]
+  uint64_t* bars = lists + size_t(Kl > 0 ? Kl : 1) * kUnitRows;
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* a_full = empty + S;
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < rounds && alive; ++r) {
         const int u = unit_at(r, cta, ncta);
         if (u >= nunits) continue;
-        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, q_offset, kv_len);
+        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
         if (U.nt == 0) continue;
         const int x = jA % nA;
         if (!tc::mbar_wait(&a_empty[x], ((jA / nA) & 1) ^ 1, abort_flag)) {
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < rounds && alive; ++r) {
         const int u = unit_at(r, cta, ncta);
         if (u >= nunits) continue;
-        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, q_offset, kv_len);
+        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
         if (U.nt == 0) continue;
         const int x = jA % nA;
         if (!tc::mbar_wait(&a_full[x], (jA / nA) & 1, abort_flag)) {
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < rounds && alive; ++r) {
       const int u = unit_at(r, cta, ncta);
       if (u >= nunits) continue;
-      const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, q_offset, kv_len);
+      const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
       const bool active = urow < U.nrows;
       const int row = U.row0 + urow;
       const int pos = U.q0 + row / G;
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < kRegList; ++k) L[k] = 0;
       auto offer_reg = [&](int t, float mx) {
-        const bool valid = cand_row && t < loc;
+        const bool valid = cand_row && unsigned(t - fs) < unsigned(loc - fs);  // fs <= t < loc
         const uint64_t x = valid ? rank_key(mx, t) : 0ull;
         ncand += valid ? 1 : 0;
         if (__any_sync(0xffffffffu, x > L[kRegList - 1])) {
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto offer = [&](int t, float mx) {  // candidate block t with maximum mx
-        if (t >= loc) return;
+        if (t >= loc || t < fs) return;
         const uint64_t key = rank_key(mx, t);
         if (cnt < Kc) {  // fill: sift up
           int i = cnt++;
@@ -395,7 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           my_list[p * kUnitRows] = x;
         }
-        for (int k = 0; k < K; ++k) out[k] = k < cnt ? int32_t(my_list[k * kUnitRows]) : (k == cnt ? loc : -1);
+        // [0 if fs], the ranked blocks ascending, the local block, -1 padding
+        if (fs) out[0] = 0;
+        for (int k = fs; k < K; ++k)
+          out[k] = k - fs < cnt ? int32_t(my_list[(k - fs) * kUnitRows]) : (k - fs == cnt ? loc : -1);
       }
     }
   }
@@ -432,7 +439,7 @@ bool index_fused_supported(int dtype, int Nq, int G, int di, int Bs, int K) {
 }
 
 cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len,
-                                  int B, int Nq, int Nk, int G, int di, int Bs, int K, int32_t* sel,
+                                  int B, int Nq, int Nk, int G, int di, int Bs, int K, int fs, int32_t* sel,
                                   uint32_t* status, cudaStream_t stream) {
   const int NqG = Nq * G;
   CUtensorMap tmA, tmB;
@@ -481,7 +488,7 @@ cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t*
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;  \
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));                    \
     if (e != cudaSuccess) return e;                                                                            \
-    kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, q_offset, kv_len, B, Nq, Nk, G, K, nA, S, sel, status); \
+    kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, q_offset, kv_len, B, Nq, Nk, G, K, fs, nA, S, sel, status); \
   } while (0)
 #define MSA_FUSED_BS(DI_, REG_) \
   do {                          \

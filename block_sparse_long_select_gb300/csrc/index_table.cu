@@ -158,13 +158,14 @@ __global__ void __launch_bounds__(kTabWarps * 32) index_blockmax_table_kernel(
 }
 
 // Warp per (b, i, g) row. Each lane keeps a descending list of its best
-// candidates (strided over blocks t < loc) in shared memory; the 32 lists are
-// then merged by K-1 rounds of a warp-wide maximum.
+// candidates (strided over blocks fs <= t < loc) in shared memory; the 32
+// lists are then merged by K-1-fs rounds of a warp-wide maximum. fs = 1 keeps
+// block 0 outright, like the local block.
 constexpr int kTopkWarps = 4;
 
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_from_table_kernel(
     const float* __restrict__ table, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len, int B,
-    int Nq, int Nk, int G, int Bs, int K, int nblk, int32_t* __restrict__ sel, uint32_t* status) {
+    int Nq, int Nk, int G, int Bs, int K, int nblk, int fs, int32_t* __restrict__ sel, uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Kc = K - 1 > 0 ? K - 1 : 1;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_from_table_kernel(
   }
   const float* M = table + row * nblk;
   int n = 0;  // entries in this lane's list
-  for (int t = lane; t < loc; t += 32) {
+  for (int t = fs + lane; t < loc; t += 32) {  // fs = 1: block 0 is kept outright
     const uint64_t key = rank_key(M[t], t);
     if (n == Kc && key <= lists[(Kc - 1) * 32 + lane]) continue;
     int p = n < Kc ? n++ : Kc - 1;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_from_table_kernel(
     lists[p * 32 + lane] = key;
   }
   int head = 0;
-  for (int k = 0; k < K - 1; ++k) {
+  for (int k = 0; k < K - 1 - fs; ++k) {
     const uint64_t mine = head < n ? lists[head * 32 + lane] : 0ull;
     uint64_t best = mine;
 #pragma unroll
@@ -214,7 +215,10 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_from_table_kernel(
     if (mine == best) ++head;  // keys are unique: exactly one lane advances
     if (lane == 0) chosen[k] = rank_key_block(best);
   }
-  if (lane == 0) chosen[K - 1] = loc;
+  if (lane == 0) {
+    chosen[K - 1 - fs] = loc;
+    if (fs) chosen[K - 1] = 0;
+  }
   __syncwarp();
   // ascending order by rank (all entries distinct)
   for (int e = lane; e < K; e += 32) {
@@ -253,7 +257,8 @@ cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* i
 }
 
 cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
-                                   int Nk, int G, int Bs, int K, int32_t* sel, uint32_t* status, cudaStream_t stream) {
+                                   int Nk, int G, int Bs, int K, int fs, int32_t* sel, uint32_t* status,
+                                   cudaStream_t stream) {
   const int nblk = (Nk + Bs - 1) / Bs;
   const int64_t rows = int64_t(B) * Nq * G;
   const int Kc = K - 1 > 0 ? K - 1 : 1;
@@ -266,7 +271,7 @@ cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, 
   const unsigned grid = unsigned((rows + kTopkWarps - 1) / kTopkWarps);
   ProfScope prof("topk_from_table", stream);
   topk_from_table_kernel<<<grid, kTopkWarps * 32, smem, stream>>>(table, q_offset, kv_len, B, Nq, Nk, G, Bs, K, nblk,
-                                                                  sel, status);
+                                                                  fs, sel, status);
   return cudaGetLastError();
 }
 

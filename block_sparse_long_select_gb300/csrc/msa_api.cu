@@ -109,30 +109,41 @@ extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int H
   }
 }
 
-extern "C" msa_status_t msa_index_select(const void* iq, const void* ik, const int32_t* q_offset,
-                                         const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs, int K,
-                                         int dtype, int32_t* sel, float* block_max, void* ws, size_t ws_bytes,
-                                         cudaStream_t stream) {
+extern "C" msa_status_t msa_index_select_v(const void* iq, const void* ik, const int32_t* q_offset,
+                                           const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs, int K,
+                                           int dtype, int force, int32_t* sel, float* block_max, void* ws,
+                                           size_t ws_bytes, cudaStream_t stream) {
   if (!iq || !ik || !sel) return MSA_ERR_INVALID_ARG;
+  if (force != MSA_FORCE_LOCAL && force != (MSA_FORCE_LOCAL | MSA_FORCE_START)) return MSA_ERR_INVALID_ARG;
+  const int fs = (force & MSA_FORCE_START) ? 1 : 0;  // block 0 kept as well
+  if (fs && K < 2) return MSA_ERR_INVALID_ARG;
   IndexPlan p = plan_index(B, Nq, Nk, G, di, Bs, K, dtype, block_max != nullptr);
   if (!p.ok) return p.err;
   msa_status_t w = check_ws(ws, ws_bytes, block_max ? kWsHeader : p.ws_bytes);
   if (w != MSA_OK) return w;
   uint32_t* status = status_word(ws);
   if (p.fused && !block_max) {
-    return cuda_status(launch_index_fused_tc(iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, K, sel, status,
+    return cuda_status(launch_index_fused_tc(iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, K, fs, sel, status,
                                              stream));
   }
   if (!block_max && decode_index_supported(dtype, B, Nq, G, di, Bs, K)) {
     float* tab = reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);
-    return cuda_status(launch_decode_index(iq, ik, q_offset, kv_len, B, Nk, G, Bs, K, sel, tab, status, stream));
+    return cuda_status(launch_decode_index(iq, ik, q_offset, kv_len, B, Nk, G, Bs, K, fs, sel, tab, status, stream));
   }
   float* table = block_max ? block_max : reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);
   cudaError_t e = launch_index_blockmax_table(dtype, iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, table, status,
                                               stream);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = launch_topk_from_table(table, q_offset, kv_len, B, Nq, Nk, G, Bs, K, sel, status, stream);
+  e = launch_topk_from_table(table, q_offset, kv_len, B, Nq, Nk, G, Bs, K, fs, sel, status, stream);
   return cuda_status(e);
+}
+
+extern "C" msa_status_t msa_index_select(const void* iq, const void* ik, const int32_t* q_offset,
+                                         const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs, int K,
+                                         int dtype, int32_t* sel, float* block_max, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream) {
+  return msa_index_select_v(iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, K, dtype, MSA_FORCE_LOCAL, sel, block_max,
+                            ws, ws_bytes, stream);
 }
 
 extern "C" msa_status_t msa_sparse_attn_prefill(const void* q, const void* k, const void* v, const int32_t* sel,

@@ -88,12 +88,14 @@ cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* i
 // Index Branch, fused tcgen05 path (bf16): scores + block max + top-K in one
 // persistent kernel; no table.
 bool index_fused_supported(int dtype, int Nq, int G, int di, int Bs, int K);
+// fs = 1 keeps block 0 as well as the local block (K - 2 blocks ranked)
 cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len,
-                                  int B, int Nq, int Nk, int G, int di, int Bs, int K, int32_t* sel,
+                                  int B, int Nq, int Nk, int G, int di, int Bs, int K, int fs, int32_t* sel,
                                   uint32_t* status, cudaStream_t stream);
 // Exact top-K over a block-max table (warp per row).
 cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
-                                   int Nk, int G, int Bs, int K, int32_t* sel, uint32_t* status, cudaStream_t stream);
+                                   int Nk, int G, int Bs, int K, int fs, int32_t* sel, uint32_t* status,
+                                   cudaStream_t stream);
 // Main Branch, prefill, KV-outer tcgen05 path (bf16).
 bool attn_kv_outer_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K);
 size_t attn_kv_outer_ws_bytes(int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K);
@@ -106,7 +108,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
 bool decode_index_supported(int dtype, int B, int Nq, int G, int di, int Bs, int K);
 size_t decode_index_ws_bytes(int B, int G, int Nk);
 cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
-                                int Lmax, int G, int Bs, int K, int32_t* sel, float* table, uint32_t* status,
+                                int Lmax, int G, int Bs, int K, int fs, int32_t* sel, float* table, uint32_t* status,
                                 cudaStream_t stream);
 // Main Branch, decode: split over selected blocks + combine (bf16).
 bool decode_attn_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K);

@@ -68,7 +68,7 @@ extern "C" msa_status_t msa_index_select_noalloc(const void* iq, const void* ik,
   if (launch_index_blockmax_table(dtype, iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, table, status, stream) !=
       cudaSuccess)
     return MSA_ERR_CUDA;
-  if (launch_topk_from_table(table, q_offset, kv_len, B, Nq, Nk, G, Bs, K, sel, status, stream) != cudaSuccess)
+  if (launch_topk_from_table(table, q_offset, kv_len, B, Nq, Nk, G, Bs, K, 0, sel, status, stream) != cudaSuccess)
     return MSA_ERR_CUDA;
   return MSA_OK;
 }

@@ -95,6 +95,22 @@ msa_status_t msa_index_select(const void* iq, const void* ik, const int32_t* q_o
                               int Nq, int Nk, int G, int di, int Bs, int K, int dtype, int32_t* sel, float* block_max,
                               void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Forced blocks of a selection (msa_index_select_v). */
+typedef enum { MSA_FORCE_LOCAL = 1, MSA_FORCE_START = 2 } msa_force_t;
+
+/* msa_index_select with a choice of forced blocks. force = MSA_FORCE_LOCAL is
+ * msa_index_select. force = MSA_FORCE_LOCAL | MSA_FORCE_START also keeps
+ * block 0 (hyper.ai summary of paper 2606.13392, section "实验": the ablation
+ * that hard-codes the sequence-start block besides the local window): a row
+ * with loc + 1 > K holds 0, loc and the K-2 blocks 1 <= t < loc with the
+ * highest block maximum (ties to the lower t), ascending; rows with
+ * loc + 1 <= K hold 0..loc as before. MSA_FORCE_START needs K >= 2. Any other
+ * force value returns MSA_ERR_INVALID_ARG before anything is enqueued. Other
+ * arguments, workspace and errors as msa_index_select. */
+msa_status_t msa_index_select_v(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len, int B,
+                                int Nq, int Nk, int G, int di, int Bs, int K, int dtype, int force, int32_t* sel,
+                                float* block_max, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* msa_index_select without a workspace argument: the same selection (and the
  * same optional block_max output) for callers that cannot allocate device
  * memory -- code that runs under another framework's allocator or inside its

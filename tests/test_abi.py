@@ -79,3 +79,7 @@ def test_host_validation_before_launch(lib):
     assert lib.msa_sparse_attn_decode(P(), P(), P(), P(), None, 1, 8, 8, 2, 64, 4, 2, 0.0, 1, P(), None, P(),
                                       1 << 20, None) == 1
     assert lib.msa_read_status(None, None) == 1
+    # forced blocks: only LOCAL or LOCAL|START; START needs K >= 2
+    assert lib.msa_index_select_v(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 2, 1, 0, P(), None, P(), 1 << 20, None) == 1
+    assert lib.msa_index_select_v(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 2, 1, 2, P(), None, P(), 1 << 20, None) == 1
+    assert lib.msa_index_select_v(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 1, 1, 3, P(), None, P(), 1 << 20, None) == 1

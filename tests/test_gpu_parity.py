@@ -166,3 +166,45 @@ def msa_index_select_dev(t, w, qo, kl):
     s = msa.msa_index_select(t["iq"], t["ik"], torch.from_numpy(qo).to(DEV), torch.from_numpy(kl).to(DEV), w.Bs, w.K)
     torch.cuda.synchronize()
     return s.cpu().numpy()
+
+
+# forced sequence-start variant (block 0 kept with the local block), one case per top-K implementation
+FORCE_START_PREFILL = {
+    "fused_registers": synth.scaled(BASE, B=1, Nq=1500, Nk=1500, Bs=64, K=8),
+    "fused_heap": synth.scaled(BASE, B=1, Nq=1200, Nk=1200, Bs=32, K=20),
+    "fused_k2_nothing_ranked": synth.scaled(BASE, B=1, Nq=800, Nk=800, Bs=32, K=2),
+    "table_fp32": synth.WORKLOADS["tiny_fp32"],
+}
+FORCE_START_DECODE = {
+    "warp_filter": dict(B=6, Nk=4096, kv_len_range=(1, 4096), Bs=128, K=16),
+    "warp_radix": dict(B=6, Nk=3000, kv_len_range=(1, 3000), Bs=32, K=40),
+    "cta_long_rows": dict(B=3, Nk=40000, kv_len_range=(33000, 40000), Bs=32, K=16),
+    "k2": dict(B=6, Nk=3000, kv_len_range=(1, 3000), Bs=64, K=2),
+}
+
+
+def _force_start_check(w, qo, kl):
+    import block_sparse_long_select_gb300 as msa
+    import oracle
+
+    t = device_inputs(w, DEV, names=("iq", "ik"))
+    sel = msa.msa_index_select_v(t["iq"], t["ik"], torch.from_numpy(qo).to(DEV), torch.from_numpy(kl).to(DEV),
+                                 w.Bs, w.K, msa.MSA_FORCE_LOCAL | msa.MSA_FORCE_START)
+    torch.cuda.synchronize()
+    iq, ik = synth.host_tensor(w, "iq"), synth.host_tensor(w, "ik")
+    rb, ri = oracle.all_rows(w.B, w.Nq)
+    osel = oracle.index_select(iq.reshape(-1, w.G, w.di), ik, rb, ri, qo, kl, w.Bs, w.K, force_start=True)
+    assert np.array_equal(sel.cpu().numpy().reshape(osel.shape), osel), w.name
+
+
+@pytest.mark.parametrize("name", sorted(FORCE_START_PREFILL))
+def test_force_start_prefill(name):
+    w = FORCE_START_PREFILL[name]
+    _force_start_check(w, synth.q_offsets(w), synth.kv_lens(w))
+
+
+@pytest.mark.parametrize("name", sorted(FORCE_START_DECODE))
+def test_force_start_decode(name):
+    w = synth.scaled(synth.WORKLOADS["decode_b64"], **FORCE_START_DECODE[name])
+    kl = synth.kv_lens(w)
+    _force_start_check(w, (kl - 1).astype(np.int32), kl)
