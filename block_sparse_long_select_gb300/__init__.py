@@ -6,8 +6,8 @@ PyTorch only provides device memory and the current stream. The functions
 carry the C names:
 
     msa_workspace_size, msa_index_select, msa_index_select_v,
-    msa_sparse_attn_prefill, msa_sparse_attn_decode, msa_read_status,
-    msa_status_string
+    msa_sparse_attn_prefill, msa_sparse_attn_decode, msa_decode_step,
+    msa_read_status, msa_status_string
 
 There is no CPU fallback: if ``libmsa.so`` is missing or was not built for
 this GPU, every call raises.
@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     MSA_FORCE_START,
     MSA_FP32,
     MSA_OP_DECODE,
+    MSA_OP_DECODE_STEP,
     MSA_OP_INDEX_SELECT,
     MSA_OP_PREFILL,
     MsaError,
@@ -28,6 +29,7 @@ from ._lib import (  # noqa: F401
     msa_index_select_v,
     msa_profile_begin,
     msa_profile_end,
+    msa_decode_step,
     msa_read_status,
     msa_sparse_attn_decode,
     msa_sparse_attn_prefill,

@@ -6,7 +6,7 @@ import os
 from functools import lru_cache
 
 MSA_BF16, MSA_FP32 = 0, 1
-MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE = 0, 1, 2
+MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE, MSA_OP_DECODE_STEP = 0, 1, 2, 3
 MSA_FORCE_LOCAL, MSA_FORCE_START = 1, 2
 STATUS_NAMES = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
                 4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_BOUNDS"}
@@ -19,6 +19,7 @@ SIGNATURES = {
     "msa_index_select_v": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 9 + [_vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_attn_prefill": (_i32, [_vp] * 6 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_attn_decode": (_i32, [_vp] * 5 + [_i32] * 7 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "msa_decode_step": (_i32, [_vp] * 9 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_read_status": (_i32, [_vp, _vp]),
     "msa_status_string": (ctypes.c_char_p, [_i32]),
     "msa_index_select_noalloc": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 8 + [_vp, _vp, _vp]),
@@ -198,3 +199,30 @@ def msa_profile_end() -> dict:
     if n < 0:
         raise RuntimeError("msa_profile_end: event query failed")
     return {buf[k].name.decode(): (buf[k].launches, buf[k].total_ms) for k in range(min(n, 64))}
+
+
+def msa_decode_step(q, k_new, v_new, iq, ik_new, k_cache, v_cache, ik_cache, kv_len, Bs, K, sel=None, out=None,
+                    lse=None, scale=0.0, ws=None, stream=None):
+    """One streaming decode step (see include/msa.h): append the new token's
+    k [B,Hkv,d], v, index key [B,di] at kv_len[b] of the caches, advance
+    kv_len, then select and attend for q [B,Hq,d], iq [B,Hkv,di].
+    Returns (sel [B,Hkv,K], out [B,Hq,d])."""
+    import torch
+
+    _need_cuda(q, k_new, v_new, iq, ik_new, k_cache, v_cache, ik_cache, kv_len, sel, out, lse)
+    B, Hq, d = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    di = ik_cache.shape[2]
+    dt = _dtype_code(q)
+    if sel is None:
+        sel = torch.empty((B, Hkv, K), dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(msa_workspace_size(MSA_OP_DECODE_STEP, B, 0, Lmax, Hkv, Hq, d, di, Bs, K, dt), q.device)
+    code = load_library().msa_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(iq), _ptr(ik_new), _ptr(k_cache),
+                                          _ptr(v_cache), _ptr(ik_cache), _ptr(kv_len), B, Lmax, Hq, Hkv, d, di, Bs, K,
+                                          float(scale), dt, _ptr(sel), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                          _stream(stream, q.device))
+    _check(code, "msa_decode_step")
+    return sel, out

@@ -799,6 +799,41 @@ cudaError_t launch_after_prev(void (*kern)(Params...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Streaming decode: append one token per sequence to its caches. Block b
+// copies the token's key and value rows (all kv heads) and its index-key row
+// to position L = kv_len[b], then advances kv_len[b] to L + 1 and records L as
+// the token's position for the selection. A sequence whose cache is full (or
+// whose length is out of range) is left unchanged; its position becomes -1,
+// so its selection row comes back -1, and the status becomes MSA_ERR_BOUNDS.
+__global__ void __launch_bounds__(256) decode_append_kernel(const uint4* __restrict__ k_new,
+                                                            const uint4* __restrict__ v_new,
+                                                            const uint4* __restrict__ ik_new, uint4* __restrict__ k_cache,
+                                                            uint4* __restrict__ v_cache, uint4* __restrict__ ik_cache,
+                                                            int32_t* __restrict__ kv_len, int32_t* __restrict__ q_pos,
+                                                            int Lmax, int kv_vec, int ik_vec, uint32_t* status) {
+  const int b = blockIdx.x;
+  const int L = kv_len[b];
+  const bool ok = L >= 0 && L < Lmax;
+  __syncthreads();  // every thread has read kv_len[b] before it advances
+  if (ok) {
+    const int64_t row = int64_t(b) * Lmax + L;
+    for (int x = threadIdx.x; x < kv_vec; x += blockDim.x) {
+      k_cache[row * kv_vec + x] = k_new[int64_t(b) * kv_vec + x];
+      v_cache[row * kv_vec + x] = v_new[int64_t(b) * kv_vec + x];
+    }
+    for (int x = threadIdx.x; x < ik_vec; x += blockDim.x) ik_cache[row * ik_vec + x] = ik_new[int64_t(b) * ik_vec + x];
+  }
+  if (threadIdx.x == 0) {
+    if (ok) {
+      kv_len[b] = L + 1;
+      q_pos[b] = L;
+    } else {
+      q_pos[b] = -1;
+      set_status(status, MSA_ERR_BOUNDS);
+    }
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -953,6 +988,19 @@ cudaError_t launch_decode_index(const void* iq, const void* ik, const int32_t* q
         cudaSuccess)
       return e;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_append(const void* k_new, const void* v_new, const void* ik_new, void* k_cache,
+                                 void* v_cache, void* ik_cache, int32_t* kv_len, int32_t* q_pos, int B, int Lmax,
+                                 int Hkv, int d, int di, int elem_bytes, uint32_t* status, cudaStream_t stream) {
+  const size_t kv_row = size_t(Hkv) * d * elem_bytes, ik_row = size_t(di) * elem_bytes;
+  if (kv_row % 16 || ik_row % 16) return cudaErrorInvalidValue;
+  ProfScope pf("decode_append", stream);
+  decode_append_kernel<<<B, 256, 0, stream>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), static_cast<const uint4*>(ik_new),
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<uint4*>(ik_cache), kv_len, q_pos, Lmax,
+      int(kv_row / 16), int(ik_row / 16), status);
   return cudaGetLastError();
 }
 

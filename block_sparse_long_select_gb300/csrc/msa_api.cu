@@ -84,6 +84,37 @@ inline msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_O
 
 inline uint32_t* status_word(void* ws) { return &static_cast<WsHeader*>(ws)->status; }
 
+// Streaming decode step: one workspace holds the status header, the new
+// tokens' positions, the index scratch and the attention scratch.
+struct StepPlan {
+  bool ok = false;
+  msa_status_t err = MSA_ERR_INVALID_ARG;
+  IndexPlan ip;
+  AttnPlan ap;
+  size_t off_pos = 0, off_index = 0, off_attn = 0, ws_bytes = 0;
+};
+
+StepPlan plan_step(int B, int Lmax, int G, int Hq, int d, int di, int Bs, int K, int dtype) {
+  StepPlan p;
+  p.ip = plan_index(B, 1, Lmax, G, di, Bs, K, dtype, false);
+  if (!p.ip.ok) {
+    p.err = p.ip.err;
+    return p;
+  }
+  p.ap = plan_attn(B, 1, Lmax, Hq, G, d, Bs, K, dtype, false);
+  if (!p.ap.ok) {
+    p.err = p.ap.err;
+    return p;
+  }
+  p.off_pos = kWsHeader;
+  p.off_index = p.off_pos + align256(size_t(B) * sizeof(int32_t));
+  p.off_attn = p.off_index + align256(p.ip.ws_bytes - kWsHeader);
+  p.ws_bytes = p.off_attn + (p.ap.ws_bytes - kWsHeader);
+  p.ok = true;
+  p.err = MSA_OK;
+  return p;
+}
+
 }  // namespace
 }  // namespace msa
 
@@ -102,6 +133,10 @@ extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int H
     }
     case MSA_OP_DECODE: {
       AttnPlan p = plan_attn(B, 1, Nk, Hq, G > 0 ? G : 1, d, Bs, K, dtype, false);
+      return p.ok ? p.ws_bytes : 0;
+    }
+    case MSA_OP_DECODE_STEP: {
+      StepPlan p = plan_step(B, Nk, G, Hq, d, di, Bs, K, dtype);
       return p.ok ? p.ws_bytes : 0;
     }
     default:
@@ -180,6 +215,46 @@ extern "C" msa_status_t msa_sparse_attn_decode(const void* q, const void* k_cach
                                           lse, static_cast<char*>(ws) + kWsHeader, status_word(ws), stream));
   cudaError_t e = launch_attn_query_outer(dtype, q, k_cache, v_cache, sel, nullptr, kv_len, true, B, 1, Lmax, Hq,
                                           Hkv, d, Bs, K, scale, out, lse, status_word(ws), stream);
+  return cuda_status(e);
+}
+
+extern "C" msa_status_t msa_decode_step(const void* q, const void* k_new, const void* v_new, const void* iq,
+                                        const void* ik_new, void* k_cache, void* v_cache, void* ik_cache,
+                                        int32_t* kv_len, int B, int Lmax, int Hq, int Hkv, int d, int di, int Bs,
+                                        int K, float scale, int dtype, int32_t* sel, void* out, float* lse, void* ws,
+                                        size_t ws_bytes, cudaStream_t stream) {
+  if (!q || !k_new || !v_new || !iq || !ik_new || !k_cache || !v_cache || !ik_cache || !kv_len || !sel || !out)
+    return MSA_ERR_INVALID_ARG;
+  if (Hkv < 1 || Hq % Hkv != 0) return MSA_ERR_INVALID_ARG;
+  StepPlan p = plan_step(B, Lmax, Hkv, Hq, d, di, Bs, K, dtype);
+  if (!p.ok) return p.err;
+  msa_status_t w = check_ws(ws, ws_bytes, p.ws_bytes);
+  if (w != MSA_OK) return w;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
+  char* base = static_cast<char*>(ws);
+  uint32_t* status = status_word(ws);
+  int32_t* pos = reinterpret_cast<int32_t*>(base + p.off_pos);
+  const int G = Hkv, esize = dtype == MSA_BF16 ? 2 : 4;
+  // 1. the new token of every sequence joins its caches
+  cudaError_t e = launch_decode_append(k_new, v_new, ik_new, k_cache, v_cache, ik_cache, kv_len, pos, B, Lmax, Hkv, d,
+                                       di, esize, status, stream);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  // 2. its selection over the grown index-key cache (position = old length)
+  float* table = reinterpret_cast<float*>(base + p.off_index);
+  if (decode_index_supported(dtype, B, 1, G, di, Bs, K)) {
+    e = launch_decode_index(iq, ik_cache, pos, kv_len, B, Lmax, G, Bs, K, 0, sel, table, status, stream);
+  } else {
+    e = launch_index_blockmax_table(dtype, iq, ik_cache, pos, kv_len, B, 1, Lmax, G, di, Bs, table, status, stream);
+    if (e == cudaSuccess) e = launch_topk_from_table(table, pos, kv_len, B, 1, Lmax, G, Bs, K, 0, sel, status, stream);
+  }
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  // 3. attention of the token over its selected blocks (pos = kv_len - 1)
+  if (p.ap.split)
+    e = launch_decode_attn(q, k_cache, v_cache, sel, kv_len, B, Lmax, Hq, Hkv, d, Bs, K, scale, out, lse,
+                           base + p.off_attn, status, stream);
+  else
+    e = launch_attn_query_outer(dtype, q, k_cache, v_cache, sel, nullptr, kv_len, true, B, 1, Lmax, Hq, Hkv, d, Bs, K,
+                                scale, out, lse, status, stream);
   return cuda_status(e);
 }
 

@@ -118,6 +118,11 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
                                float scale, void* out, float* lse, void* scratch, uint32_t* status,
                                cudaStream_t stream);
 // Main Branch, query-outer CUDA-core path (any dtype; prefill or decode).
+// Streaming decode: append one token's k, v and index-key rows per sequence
+// at kv_len[b], advance kv_len, write the token's position (or -1) to q_pos.
+cudaError_t launch_decode_append(const void* k_new, const void* v_new, const void* ik_new, void* k_cache,
+                                 void* v_cache, void* ik_cache, int32_t* kv_len, int32_t* q_pos, int B, int Lmax,
+                                 int Hkv, int d, int di, int elem_bytes, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, const void* v, const int32_t* sel,
                                     const int32_t* q_offset, const int32_t* kv_len, bool decode, int B, int Nq,
                                     int Nk, int Hq, int Hkv, int d, int Bs, int K, float scale, void* out, float* lse,

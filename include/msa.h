@@ -63,12 +63,14 @@ typedef enum {
 
 typedef enum { MSA_BF16 = 0, MSA_FP32 = 1 } msa_dtype_t;
 
-typedef enum { MSA_OP_INDEX_SELECT = 0, MSA_OP_PREFILL = 1, MSA_OP_DECODE = 2 } msa_op_t;
+typedef enum { MSA_OP_INDEX_SELECT = 0, MSA_OP_PREFILL = 1, MSA_OP_DECODE = 2, MSA_OP_DECODE_STEP = 3 } msa_op_t;
 
 /* Bytes of scratch `ws` the entry point `op` needs for these sizes (the same
  * argument meanings as the entry points; unused ones may be 0: G and di for
- * the attention ops, Hq and d for MSA_OP_INDEX_SELECT; for MSA_OP_DECODE, Nq
- * is ignored and Nk is Lmax). Returns 0 when the arguments are invalid. */
+ * the attention ops, Hq and d for MSA_OP_INDEX_SELECT; for MSA_OP_DECODE and
+ * MSA_OP_DECODE_STEP, Nq is ignored and Nk is Lmax; MSA_OP_DECODE_STEP uses
+ * every other argument, with G = Hkv). Returns 0 when the arguments are
+ * invalid. */
 size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K, int dtype);
 
 /* Index Branch: block selection for every (query row, group).
@@ -166,6 +168,30 @@ msa_status_t msa_sparse_attn_decode(const void* q, const void* k_cache, const vo
                                     const int32_t* kv_len, int B, int Lmax, int Hq, int Hkv, int d, int Bs, int K,
                                     float scale, int dtype, void* out, float* lse, void* ws, size_t ws_bytes,
                                     cudaStream_t stream);
+
+/* Streaming decode: one step of a serving loop. For every sequence b the new
+ * token's key, value and index-key rows are appended to the caches at
+ * position L = kv_len[b], kv_len[b] becomes L + 1, and the token is then
+ * selected for (msa_index_select with Nq = 1, q_offset = L) and attended
+ * (msa_sparse_attn_decode) over the grown caches. (hyper.ai summary of paper
+ * 2606.13392, "一句话总结": the decode side of the reported speedups, where each
+ * new token re-selects its blocks over the cache.)
+ *
+ *  q [B, Hq, d]; k_new, v_new [B, Hkv, d]; iq [B, Hkv, di]; ik_new [B, di]  (dtype)
+ *  k_cache, v_cache [B, Lmax, Hkv, d]; ik_cache [B, Lmax, di] (dtype): in/out
+ *  kv_len [B] int32, in/out: current lengths, advanced by one
+ *  sel [B, Hkv, K] int32, out: the token's selection (as msa_index_select)
+ *  out [B, Hq, d] (dtype), lse [B, Hq] fp32 or NULL, out (as msa_sparse_attn_decode)
+ *  ws: msa_workspace_size(MSA_OP_DECODE_STEP, B, 0, Lmax, Hkv, Hq, d, di, Bs, K, dtype)
+ * A sequence whose cache is already full (kv_len[b] == Lmax) or whose length
+ * is out of range is left unchanged: its sel row is -1, its output row zero,
+ * and the status word becomes MSA_ERR_BOUNDS. Supported sizes as for
+ * msa_index_select and msa_sparse_attn_decode; the k/v and index-key rows must
+ * be multiples of 16 bytes. */
+msa_status_t msa_decode_step(const void* q, const void* k_new, const void* v_new, const void* iq, const void* ik_new,
+                             void* k_cache, void* v_cache, void* ik_cache, int32_t* kv_len, int B, int Lmax, int Hq,
+                             int Hkv, int d, int di, int Bs, int K, float scale, int dtype, int32_t* sel, void* out,
+                             float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the sticky device status of workspace `ws`
  * (MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_BOUNDS) and clears it. Returns
