@@ -456,7 +456,37 @@ def run_msa(args, dist):
             "gpu_launches": sum(v[0] for v in dprof.values()), "clocks": dclocks,
             "ms_per_step_with_kernel_events": round(float(np.mean(dkms)), 4),
         }
-        del td, seld, outd, wsd_i, wsd_a
+        # streaming decode (msa_decode_step): each step appends one token per
+        # sequence to the caches (rows gathered before the timed region), then
+        # selects and attends for it; lengths start below the measured ones
+        # so that every append fits the cache
+        sst = dsteps + 1 + max(args.warmup, 5)
+        ks = torch.from_numpy(np.maximum(kld_np - sst, 1).astype(np.int32)).to(dev)
+        ar = torch.arange(wd.B, device=dev)
+        new_rows = [(td["k"][ar, ks.long() + j].contiguous(), td["v"][ar, ks.long() + j].contiguous(),
+                     td["ik"][ar, ks.long() + j].contiguous()) for j in range(sst)]
+        iqd = td["iq"][:, 0]
+        seld2 = torch.empty((wd.B, wd.G, wd.K), dtype=torch.int32, device=dev)
+        wsd_s = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_DECODE_STEP, wd.B, 0, wd.Nk, wd.G, wd.Hq, wd.d, wd.di,
+                                                     wd.Bs, wd.K, msa.MSA_BF16), dev)
+        cursor = [0]
+
+        def stream_step():
+            kn, vn, ikn = new_rows[cursor[0] % sst]
+            cursor[0] += 1
+            msa.msa_decode_step(qd, kn, vn, iqd, ikn, td["k"], td["v"], td["ik"], ks, wd.Bs, wd.K, sel=seld2,
+                                out=outd, ws=wsd_s)
+
+        sms, _, _, _ = time_steps(stream_step, dsteps, max(args.warmup, 5), profile=False)
+        st = msa.msa_read_status(wsd_s)
+        if st != 0:
+            raise RuntimeError(f"device status after streaming decode: {msa.msa_status_string(st)}")
+        s_tot = dist.max(sum(sms) / 1e3)
+        decode["stream"] = {"value": round(dist.sum(wd.B * dsteps) / s_tot, 1), "unit": "tokens/s",
+                            "ms_per_step": round(float(np.mean(sms)), 4), "steps": dsteps,
+                            "what": "msa_decode_step: append k/v/index-key rows at kv_len, advance kv_len, "
+                                    "select and attend over the grown caches"}
+        del td, seld, outd, wsd_i, wsd_a, wsd_s, new_rows
         torch.cuda.empty_cache()
 
     line = {
