@@ -49,6 +49,9 @@ def _load(path):
     lib.msa_oracle_sparse_attn.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32,
                                            i32, f64, vp, vp, i32]
     lib.msa_oracle_sparse_attn.restype = i32
+    lib.msa_oracle_kl_aux.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                      f64, vp, i32]
+    lib.msa_oracle_kl_aux.restype = i32
     return lib
 
 
@@ -122,6 +125,33 @@ def sparse_attn(q_rows, k, v, sel_rows, row_b, row_i, q_offset, kv_len, Bs, K, s
     if rc != 0:
         raise ValueError("oracle sparse_attn rejected its arguments")
     return out, lse
+
+
+def kl_aux(q_rows, k, iq_rows, ik, sel_rows, row_b, row_i, q_offset, kv_len, Bs, K, scale=0.0, nthreads=None,
+           lib=None):
+    """KL auxiliary forward for listed rows: KL(head-averaged main-branch
+    distribution || index softmax) over each (row, group)'s selected tokens.
+
+    q_rows [n, Hq, d]; k [B, Nk, Hkv, d]; iq_rows [n, Hkv, di]; ik [B, Nk, di];
+    sel_rows [n, Hkv, K]. Returns kl [n, Hkv] fp64.
+    """
+    q_rows, iq_rows = _c(q_rows, np.float32), _c(iq_rows, np.float32)
+    k = k if (k.dtype == np.float32 and k.flags.c_contiguous) else _c(k, np.float32)
+    ik = _c(ik, np.float32)
+    n, Hq, d = q_rows.shape
+    B, Nk, Hkv, _ = k.shape
+    di = iq_rows.shape[2]
+    sel_rows = _c(sel_rows, np.int32)
+    row_b, row_i = _c(row_b, np.int32), _c(row_i, np.int32)
+    q_offset, kv_len = _c(q_offset, np.int32), _c(kv_len, np.int32)
+    kl = np.empty((n, Hkv), dtype=np.float64)
+    rc = (lib or _lib()).msa_oracle_kl_aux(q_rows.ctypes.data, k.ctypes.data, iq_rows.ctypes.data, ik.ctypes.data,
+                                           sel_rows.ctypes.data, row_b.ctypes.data, row_i.ctypes.data, n,
+                                           q_offset.ctypes.data, kv_len.ctypes.data, B, Nk, Hq, Hkv, d, di, Bs, K,
+                                           float(scale), kl.ctypes.data, nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle kl_aux rejected its arguments")
+    return kl
 
 
 # ---------------------------------------------------------------------------

@@ -196,4 +196,80 @@ int msa_oracle_sparse_attn(const float* q_rows, const float* k, const float* v, 
   return 0;
 }
 
+// KL auxiliary (forward value only): for each (row, group), the divergence
+// KL(p || q) over the tokens T of the group's selected blocks (causally
+// visible), where p is the Main Branch's attention distribution averaged over
+// the group's query heads and q is the softmax of the Index Branch's scores
+// over the same tokens. (quant_prune_distill post 751, "Метод": the loss is the
+// KL divergence between the index branch and the head-averaged main branch,
+// main-branch probabilities under stop-gradient; hyper.ai summary, "方法":
+// the index distribution is aligned with the main branch's on the selected
+// tokens.) Index scores enter the softmax as the plain dot products.
+//   q_rows [nrows, Hq, d]; k [B, Nk, Hkv, d]; iq_rows [nrows, Hkv, di];
+//   ik [B, Nk, di]; sel_rows [nrows, Hkv, K]; kl [nrows, Hkv] (fp64, out)
+//   scale <= 0 selects 1/sqrt(d).
+int msa_oracle_kl_aux(const float* q_rows, const float* k, const float* iq_rows, const float* ik,
+                      const int32_t* sel_rows, const int32_t* row_b, const int32_t* row_i, int64_t nrows,
+                      const int32_t* q_offset, const int32_t* kv_len, int B, int Nk, int Hq, int Hkv, int d, int di,
+                      int Bs, int K, double scale, double* kl, int nthreads) {
+  if (!q_rows || !k || !iq_rows || !ik || !sel_rows || !row_b || !row_i || !q_offset || !kv_len || !kl) return 1;
+  if (B < 1 || Nk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || di < 1 || Bs < 1 || K < 1) return 1;
+  if (scale <= 0.0) scale = std::sqrt(1.0 / double(d));  // the attention's default scale
+  const int nblk = (Nk + Bs - 1) / Bs;
+  const int hpg = Hq / Hkv;
+  parallel_rows(nrows, nthreads, [&](int64_t r) {
+    const int b = row_b[r];
+    const int pos = q_offset[b] + row_i[r];
+    const int L = kv_len[b];
+    for (int g = 0; g < Hkv; ++g) {
+      std::vector<int> keys;
+      const int32_t* sl = sel_rows + (r * Hkv + g) * K;
+      for (int kk = 0; kk < K; ++kk) {
+        const int t = sl[kk];
+        if (t < 0 || t >= nblk) continue;
+        for (int j = t * Bs; j < (t + 1) * Bs && j <= pos && j < L; ++j) keys.push_back(j);  // causal, diagonal kept
+      }
+      const size_t n = keys.size();
+      if (n == 0) {
+        kl[r * Hkv + g] = 0.0;
+        continue;
+      }
+      // p: softmax of the scaled main scores per head, averaged over the group's heads
+      std::vector<double> p(n, 0.0), z(n);
+      for (int h = g * hpg; h < (g + 1) * hpg; ++h) {
+        const float* qh = q_rows + (r * Hq + h) * int64_t(d);
+        double m = -std::numeric_limits<double>::infinity();
+        for (size_t x = 0; x < n; ++x) {
+          const float* kj = k + ((int64_t(b) * Nk + keys[x]) * Hkv + g) * int64_t(d);
+          double acc = 0.0;
+          for (int c = 0; c < d; ++c) acc += double(qh[c]) * double(kj[c]);
+          z[x] = acc * scale;
+          m = std::max(m, z[x]);
+        }
+        double l = 0.0;
+        for (size_t x = 0; x < n; ++x) l += std::exp(z[x] - m);
+        for (size_t x = 0; x < n; ++x) p[x] += std::exp(z[x] - m) / l / double(hpg);
+      }
+      // q: softmax of the index scores over the same tokens
+      const float* iqg = iq_rows + (r * Hkv + g) * int64_t(di);
+      std::vector<double> s(n);
+      double ms = -std::numeric_limits<double>::infinity();
+      for (size_t x = 0; x < n; ++x) {
+        double acc = 0.0;
+        for (int c = 0; c < di; ++c) acc += double(iqg[c]) * double(ik[(int64_t(b) * Nk + keys[x]) * di + c]);
+        s[x] = acc;
+        ms = std::max(ms, s[x]);
+      }
+      double ls = 0.0;
+      for (size_t x = 0; x < n; ++x) ls += std::exp(s[x] - ms);
+      const double lse_q = ms + std::log(ls);
+      double div = 0.0;  // sum_j p_j (log p_j - log q_j)
+      for (size_t x = 0; x < n; ++x)
+        if (p[x] > 0.0) div += p[x] * (std::log(p[x]) - (s[x] - lse_q));
+      kl[r * Hkv + g] = div;
+    }
+  });
+  return 0;
+}
+
 }  // extern "C"

@@ -14,6 +14,9 @@
 * the forced sequence-start variant: structure, a second implementation, and
   its equivalences with the plain selection when block 0 is the strongest or
   the weakest block;
+* the KL auxiliary forward: non-negative, zero on matched distributions, the
+  closed form for a uniform main distribution, and invariance to shifting a
+  row's index scores;
 * planted mistakes in a copy of the oracle source fail at least one pin.
 """
 import math
@@ -331,8 +334,60 @@ def pin_force_start(lib=None):
                     assert forced[i, 0].tolist() == sorted([0] + plain[i, 0].tolist())
 
 
+def _kl_inputs(seed, B=2, Nq=40, Nk=96, Hq=4, Hkv=2, d=16, di=8, Bs=8, K=5):
+    q, k, v, iq, ik, qo, kl = rand_problem(seed, B=B, Nq=Nq, Nk=Nk, Hq=Hq, Hkv=Hkv, d=d, di=di,
+                                           q_offset=[Nk - Nq, 20], kv_len=[Nk, Nq + 20])
+    rb, ri = oracle.all_rows(B, Nq)
+    sel = oracle.index_select(iq.reshape(-1, Hkv, di), ik, rb, ri, qo, kl, Bs, K)
+    return q, k, iq, ik, qo, kl, rb, ri, sel
+
+
+def pin_kl_aux(lib=None):
+    """KL auxiliary forward: non-negative; zero when the index scores equal the
+    main scores (one head per group, scale 1); for a uniform main distribution
+    it equals the closed form -log n - mean(s) + logsumexp(s) over the selected
+    tokens (index scores from a library matmul); unchanged when every index
+    score of a row is shifted by the same constant."""
+    Bs, K = 8, 5
+    q, k, iq, ik, qo, kl_, rb, ri, sel = _kl_inputs(21)
+    n, Hq, d, Hkv, di = len(rb), 4, 16, 2, 8
+    kl = oracle.kl_aux(q.reshape(n, Hq, d), k, iq.reshape(n, Hkv, di), ik, sel, rb, ri, qo, kl_, Bs, K, lib=lib)
+    assert kl.min() > -1e-12 and kl.max() > 0
+    # matched distributions: one kv head, Hq = Hkv = 1, index = main scores at scale 1
+    rng = np.random.default_rng(5)
+    B1, N1 = 1, 48
+    q1 = rng.standard_normal((B1, N1, 1, 8)).astype(np.float32)
+    k1 = rng.standard_normal((B1, N1, 1, 8)).astype(np.float32)
+    rb1, ri1 = oracle.all_rows(B1, N1)
+    sel1 = oracle.index_select(q1.reshape(-1, 1, 8), k1[:, :, 0], rb1, ri1, [0], [N1], 4, 3)
+    kl1 = oracle.kl_aux(q1.reshape(-1, 1, 8), k1, q1.reshape(-1, 1, 8), k1[:, :, 0], sel1, rb1, ri1, [0], [N1], 4, 3,
+                        scale=1.0, lib=lib)
+    assert np.abs(kl1).max() < 1e-12
+    # uniform main distribution (query zero): closed form over the selected tokens
+    qz = np.zeros_like(q)
+    klz = oracle.kl_aux(qz.reshape(n, Hq, d), k, iq.reshape(n, Hkv, di), ik, sel, rb, ri, qo, kl_, Bs, K, lib=lib)
+    S = token_scores(iq, ik)  # [B, Nq, G, Nk]
+    for r in range(n):
+        b, i = rb[r], ri[r]
+        pos = qo[b] + i
+        for g in range(Hkv):
+            toks = [j for t in sel[r, g] if t >= 0 for j in range(t * Bs, (t + 1) * Bs) if j <= pos and j < kl_[b]]
+            sv = S[b, i, g, toks]
+            m = sv.max()
+            want = -math.log(len(toks)) - sv.mean() + m + math.log(np.exp(sv - m).sum())
+            assert abs(klz[r, g] - want) < 1e-9 * max(1.0, abs(want))
+    # a per-row constant added to every index score: an extra index dim, ik = 1, iq = c
+    c = np.random.default_rng(6).integers(-5, 6, (iq.shape[0], iq.shape[1], Hkv, 1)).astype(np.float32)
+    iq2 = np.concatenate([iq, c], axis=-1)
+    ik2 = np.concatenate([ik, np.ones(ik.shape[:2] + (1,), np.float32)], axis=-1)
+    kl2 = oracle.kl_aux(q.reshape(n, Hq, d), k, iq2.reshape(n, Hkv, di + 1), ik2, sel, rb, ri, qo, kl_, Bs, K,
+                        lib=lib)
+    assert np.abs(kl2 - kl).max() < 1e-9 * max(1.0, np.abs(kl).max())
+
+
 PINS = [pin_golden, pin_blockmax_bruteforce, pin_selection_invariants, pin_closed_forms, pin_dense_equals_sdpa,
-        pin_masked_dense_equals_sdpa, pin_attention_special_cases, pin_decode_equals_prefill_row, pin_force_start]
+        pin_masked_dense_equals_sdpa, pin_attention_special_cases, pin_decode_equals_prefill_row, pin_force_start,
+        pin_kl_aux]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -355,6 +410,12 @@ MUTATIONS = {
     "selects_lowest_maxima": ("if (M[a] != M[b]) return M[a] > M[b];", "if (M[a] != M[b]) return M[a] < M[b];"),
     "start_variant_ranks_one_too_many": ("const int ranked = K - 1 - first;", "const int ranked = K - 1;"),
     "start_variant_ranks_block_zero": ("const int first = force_start ? 1 : 0;", "const int first = 0;"),
+    "kl_causal_excludes_diagonal": ("j <= pos && j < L; ++j) keys.push_back(j);  // causal, diagonal kept",
+                                    "j < pos && j < L; ++j) keys.push_back(j);"),
+    "kl_heads_not_averaged": ("p[x] += std::exp(z[x] - m) / l / double(hpg);", "p[x] += std::exp(z[x] - m) / l;"),
+    "kl_index_scores_scaled": ("        s[x] = acc;\n", "        s[x] = acc * scale;\n"),
+    "kl_reversed_direction": ("if (p[x] > 0.0) div += p[x] * (std::log(p[x]) - (s[x] - lse_q));",
+                              "div += std::exp(s[x] - lse_q) * ((s[x] - lse_q) - std::log(p[x] + 1e-300));"),
 }
 
 
