@@ -7,7 +7,7 @@ carry the C names:
 
     msa_workspace_size, msa_index_select, msa_index_select_v,
     msa_sparse_attn_prefill, msa_sparse_attn_decode, msa_decode_step,
-    msa_read_status, msa_status_string
+    msa_kl_aux_forward, msa_read_status, msa_status_string
 
 There is no CPU fallback: if ``libmsa.so`` is missing or was not built for
 this GPU, every call raises.
@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     MSA_OP_DECODE,
     MSA_OP_DECODE_STEP,
     MSA_OP_INDEX_SELECT,
+    MSA_OP_KL_AUX,
     MSA_OP_PREFILL,
     MsaError,
     lib_path,
@@ -27,6 +28,7 @@ from ._lib import (  # noqa: F401
     msa_index_select,
     msa_index_select_noalloc,
     msa_index_select_v,
+    msa_kl_aux_forward,
     msa_profile_begin,
     msa_profile_end,
     msa_decode_step,

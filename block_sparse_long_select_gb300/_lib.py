@@ -6,7 +6,7 @@ import os
 from functools import lru_cache
 
 MSA_BF16, MSA_FP32 = 0, 1
-MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE, MSA_OP_DECODE_STEP = 0, 1, 2, 3
+MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE, MSA_OP_DECODE_STEP, MSA_OP_KL_AUX = 0, 1, 2, 3, 4
 MSA_FORCE_LOCAL, MSA_FORCE_START = 1, 2
 STATUS_NAMES = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
                 4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_BOUNDS"}
@@ -20,6 +20,7 @@ SIGNATURES = {
     "msa_sparse_attn_prefill": (_i32, [_vp] * 6 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_attn_decode": (_i32, [_vp] * 5 + [_i32] * 7 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_decode_step": (_i32, [_vp] * 9 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "msa_kl_aux_forward": (_i32, [_vp] * 8 + [_i32] * 9 + [_f32, _i32, _vp, _vp, _sz, _vp]),
     "msa_read_status": (_i32, [_vp, _vp]),
     "msa_status_string": (ctypes.c_char_p, [_i32]),
     "msa_index_select_noalloc": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 8 + [_vp, _vp, _vp]),
@@ -226,3 +227,26 @@ def msa_decode_step(q, k_new, v_new, iq, ik_new, k_cache, v_cache, ik_cache, kv_
                                           _stream(stream, q.device))
     _check(code, "msa_decode_step")
     return sel, out
+
+
+def msa_kl_aux_forward(q, k, iq, ik, sel, lse, q_offset, kv_len, Bs, K, kl=None, scale=0.0, ws=None, stream=None):
+    """KL auxiliary forward (see include/msa.h): KL(head-averaged main-branch
+    distribution || index softmax) per (row, group) -> kl [B, Nq, Hkv] fp32.
+    ``lse`` is the forward's [B, Nq, Hq] output of msa_sparse_attn_prefill."""
+    import torch
+
+    _need_cuda(q, k, iq, ik, sel, lse, q_offset, kv_len, kl)
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    di = iq.shape[3]
+    dt = _dtype_code(q)
+    if kl is None:
+        kl = torch.empty((B, Nq, Hkv), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(msa_workspace_size(MSA_OP_KL_AUX, B, Nq, Nk, Hkv, Hq, d, 0, Bs, K, dt), q.device)
+    code = load_library().msa_kl_aux_forward(_ptr(q), _ptr(k), _ptr(iq), _ptr(ik), _ptr(sel), _ptr(lse),
+                                             _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, Hq, Hkv, d, di, Bs, K,
+                                             float(scale), dt, _ptr(kl), _ptr(ws), ws.numel(),
+                                             _stream(stream, q.device))
+    _check(code, "msa_kl_aux_forward")
+    return kl

@@ -815,6 +815,266 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// KL auxiliary forward (quant_prune_distill post 751, "Метод": the index
+// branch is trained with the KL divergence to the head-averaged main-branch
+// distribution; hyper.ai summary, "方法": the two are aligned over the selected
+// tokens). Per (query, group):
+//   KL = sum_j p_j log p_j - sum_j p_j s_j + logsumexp_j s_j
+// over the selected tokens j, with p_j the main-branch attention probability
+// averaged over the group's heads (exp(scale * q_h.k_j - lse_h), lse_h from
+// the forward) and s_j the plain index score. Each selected block contributes
+// four partial values per entry (the two sums, the block's index maximum and
+// its exp-sum); kl_combine merges a row's slots.
+//
+// kl_tile: the attention's bins and tiles (one key block of one group, up to
+// 128 / hpg entries per tile), on the same cost-balanced contiguous runs. Per
+// tile: K and the index keys of the block (once per run of the bin), the
+// tile's query rows and index queries, in padded shared-memory rows; both
+// products on mma.sync with keys along M: S^T = K . Q^T (the group's heads of
+// an entry are adjacent columns, so the head average is a pair sum and one
+// shuffle) and I^T = IK . IQ^T.
+// ---------------------------------------------------------------------------
+struct KlParams {
+  const __nv_bfloat16 *q, *k, *iq, *ik;  // q [B, Nq, Hq, D]; k [B, Nk, G, D]; iq [B, Nq, G, DI]; ik [B, Nk, DI]
+  const float* lse;                      // [B, Nq, Hq] natural-log softmax normalisers of the forward
+  const int* entries;
+  const int4* tiles;
+  const int* cta_start;
+  const int32_t* q_offset;
+  const int32_t* kv_len;
+  float4* part;  // [tiles * 128 / hpg] (sum p log p, sum p s, index max, index exp-sum)
+  int b, Nq, Nk, Hq, G, nblk, c0;
+  float scale;
+};
+
+__device__ __forceinline__ void kl_ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void kl_mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int kKlThreads = 256;
+
+template <int D, int DI, int BS, int HPG>
+struct KlSmem {
+  static constexpr int E = kRows / HPG;        // entries per tile
+  static constexpr int KP = D + 8, IP = DI + 8;  // padded row lengths (bf16): 16-byte aligned, bank-conflict free
+  static constexpr size_t kK = size_t(BS) * KP * 2, kIK = size_t(BS) * IP * 2, kQ = size_t(kRows) * KP * 2,
+                          kIQ = size_t(E) * IP * 2, kLse = kRows * 4, kS = size_t(BS) * (E + 1) * 4, kEnt = E * 4,
+                          kAcc = 2 * E * 4;
+  static constexpr size_t kTotal = kK + kIK + kQ + kIQ + kLse + kS + kEnt + kAcc;
+};
+
+template <int D, int DI, int BS, int HPG>
+__global__ void __launch_bounds__(kKlThreads, 1) kl_tile_kernel(const KlParams p) {
+  using SM = KlSmem<D, DI, BS, HPG>;
+  constexpr int E = SM::E, KP = SM::KP, IP = SM::IP;
+  constexpr int MT = BS / 16;      // 16-key tiles of the block
+  constexpr int NP = 8 / MT;       // warps sharing one key tile split the columns
+  constexpr int NT = 16 / NP;      // 8-column tiles per warp (main product)
+  constexpr int NTI = (E / 8 + NP - 1) / NP;  // 8-entry tiles per warp (index product)
+  static_assert(HPG >= 2 && HPG <= 8, "head average of adjacent column pairs");
+  extern __shared__ __align__(16) uint8_t kl_smem[];
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(kl_smem);
+  __nv_bfloat16* IKs = reinterpret_cast<__nv_bfloat16*>(kl_smem + SM::kK);
+  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(kl_smem + SM::kK + SM::kIK);
+  __nv_bfloat16* IQs = reinterpret_cast<__nv_bfloat16*>(kl_smem + SM::kK + SM::kIK + SM::kQ);
+  float* lse_s = reinterpret_cast<float*>(kl_smem + SM::kK + SM::kIK + SM::kQ + SM::kIQ);
+  float* Ss = lse_s + kRows;                                   // [BS][E + 1] index scores
+  int* ents = reinterpret_cast<int*>(Ss + BS * (E + 1));        // [E]
+  float* accA = reinterpret_cast<float*>(ents + E);             // [E] sum p log p
+  float* accB = accA + E;                                       // [E] sum p s
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int mt = warp % MT, np = warp / MT;
+  const int z0 = p.cta_start[blockIdx.x], z1 = p.cta_start[blockIdx.x + 1];
+  const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
+  constexpr float kLog2eF = 1.4426950408889634f;
+  int prev_bin = -1;
+  for (int z = z0; z < z1; ++z) {
+    const int4 tl = p.tiles[z];
+    const int bin = tl.x, g = bin / p.nblk, t = bin % p.nblk;
+    if (tid < E) ents[tid] = tid < tl.z ? p.entries[tl.y + tid] : -1;
+    if (tid < E) accA[tid] = accB[tid] = 0.f;
+    if (bin != prev_bin) {  // the block's keys and index keys, rows past the sequence zero-filled
+      for (int x = tid; x < BS * (D / 8); x += kKlThreads) {
+        const int r = x / (D / 8), c = x % (D / 8), j = t * BS + r;
+        const bool in = j < p.Nk;
+        const __nv_bfloat16* src = p.k + ((int64_t(p.b) * p.Nk + (in ? j : 0)) * p.G + g) * D + c * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(Ks + r * KP + c * 8)),
+                     "l"(src), "r"(in ? 16u : 0u)
+                     : "memory");
+      }
+      for (int x = tid; x < BS * (DI / 8); x += kKlThreads) {
+        const int r = x / (DI / 8), c = x % (DI / 8), j = t * BS + r;
+        const bool in = j < p.Nk;
+        const __nv_bfloat16* src = p.ik + (int64_t(p.b) * p.Nk + (in ? j : 0)) * DI + c * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(IKs + r * IP + c * 8)),
+                     "l"(src), "r"(in ? 16u : 0u)
+                     : "memory");
+      }
+      prev_bin = bin;
+    }
+    __syncthreads();  // ents
+    for (int x = tid; x < kRows * (D / 8); x += kKlThreads) {  // query rows: row = entry * HPG + head
+      const int r = x / (D / 8), c = x % (D / 8), ent = ents[r / HPG];
+      const int il = ent >= 0 ? (ent >> 6) : 0;
+      const __nv_bfloat16* src = p.q + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * HPG + r % HPG) * D + c * 8;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(Qs + r * KP + c * 8)), "l"(src),
+                   "r"(ent >= 0 ? 16u : 0u)
+                   : "memory");
+    }
+    for (int x = tid; x < E * (DI / 8); x += kKlThreads) {
+      const int e = x / (DI / 8), c = x % (DI / 8), ent = ents[e];
+      const int il = ent >= 0 ? (ent >> 6) : 0;
+      const __nv_bfloat16* src = p.iq + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.G + g) * DI + c * 8;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(IQs + e * IP + c * 8)), "l"(src),
+                   "r"(ent >= 0 ? 16u : 0u)
+                   : "memory");
+    }
+    if (tid < kRows) {
+      const int ent = ents[tid / HPG];
+      lse_s[tid] = ent >= 0 ? p.lse[(int64_t(p.b) * p.Nq + p.c0 + (ent >> 6)) * p.Hq + g * HPG + tid % HPG] : 0.f;
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // index scores I^T: keys [16 mt, +16) x entries, to shared memory
+    {
+      const int arow = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int ni = 0; ni < NTI; ++ni) {
+        const int nt = np * NTI + ni;
+        if (nt * 8 >= E) break;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < DI / 16; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          kl_ldsm_x4(tc::smem_u32(IKs + arow * IP + ks * 16 + 8 * (lane >> 4)), a0, a1, a2, a3);
+          const __nv_bfloat16* bq = IQs + (nt * 8 + gq) * IP + ks * 16 + 2 * tq;
+          kl_mma(c, a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(bq), *reinterpret_cast<const uint32_t*>(bq + 8));
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) Ss[(mt * 16 + gq + 8 * (x >> 1)) * (E + 1) + nt * 8 + 2 * tq + (x & 1)] = c[x];
+      }
+    }
+    // main scores S^T: keys [16 mt, +16) x columns [np * 8 NT, +8 NT)
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    {
+      const int arow = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        kl_ldsm_x4(tc::smem_u32(Ks + arow * KP + ks * 16 + 8 * (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const __nv_bfloat16* bq = Qs + ((np * NT + n) * 8 + gq) * KP + ks * 16 + 2 * tq;
+          kl_mma(acc[n], a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(bq),
+                 *reinterpret_cast<const uint32_t*>(bq + 8));
+        }
+      }
+    }
+    __syncthreads();  // index scores complete
+    // p_j per (key, entry): this lane holds heads 2 tq, 2 tq + 1 (mod HPG) of the
+    // entries of its columns; the other heads sit in the lanes tq ^ 1, tq ^ 2
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int col = (np * NT + n) * 8 + 2 * tq;  // even column of this lane's pair
+      const int e = col / HPG;
+      const int ent = ents[e];
+      const int pos = sv.q0 + p.c0 + (ent >> 6);
+      float pa = 0.f, pb = 0.f;  // sums over the lane's two heads, for keys gq and gq + 8
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int key = t * BS + mt * 16 + gq + 8 * (x >> 1);
+        const bool vis = ent >= 0 && sv.ok && key <= pos && key < sv.L;
+        const float pr = vis ? ex2((acc[n][x] * p.scale - lse_s[col + (x & 1)]) * kLog2eF) : 0.f;
+        if (x >> 1) pb += pr; else pa += pr;
+      }
+      // the entry's other heads: lanes differing in the low bits of tq
+#pragma unroll
+      for (int off = 1; off < HPG / 2; off <<= 1) {
+        pa += __shfl_xor_sync(0xffffffffu, pa, off);
+        pb += __shfl_xor_sync(0xffffffffu, pb, off);
+      }
+      pa *= 1.f / HPG;
+      pb *= 1.f / HPG;
+      float A = 0.f, Bv = 0.f;
+      const int r0 = mt * 16 + gq;
+      if (pa > 0.f) {
+        A += pa * __logf(pa);
+        Bv += pa * Ss[r0 * (E + 1) + e];
+      }
+      if (pb > 0.f) {
+        A += pb * __logf(pb);
+        Bv += pb * Ss[(r0 + 8) * (E + 1) + e];
+      }
+      // sum over the 8 key rows of this lane group (lanes with equal tq)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        A += __shfl_xor_sync(0xffffffffu, A, off);
+        Bv += __shfl_xor_sync(0xffffffffu, Bv, off);
+      }
+      if (gq == 0 && (2 * tq) % HPG == 0) {  // one lane per entry
+        atomicAdd(&accA[e], A);
+        atomicAdd(&accB[e], Bv);
+      }
+    }
+    __syncthreads();
+    // the block's index log-sum-exp per entry over its visible keys
+    if (tid < E && tid < tl.z) {
+      const int ent = ents[tid];
+      const int pos = sv.q0 + p.c0 + (ent >> 6);
+      const int nk = min(BS, min(pos, sv.L - 1) - t * BS + 1);  // visible keys of the block (>= 1)
+      float m = -INFINITY;
+      for (int r = 0; r < nk; ++r) m = fmaxf(m, Ss[r * (E + 1) + tid]);
+      float l = 0.f;
+      for (int r = 0; r < nk; ++r) l += ex2((Ss[r * (E + 1) + tid] - m) * kLog2eF);
+      p.part[int64_t(z) * E + tid] = make_float4(accA[tid], accB[tid], m, l);
+    }
+    __syncthreads();  // shared rows and sums are rewritten by the next tile
+  }
+}
+
+// per (query, group): merge the slot partials of its selected blocks
+__global__ void __launch_bounds__(256) kl_combine_kernel(const int32_t* __restrict__ sel,
+                                                         const int32_t* __restrict__ q_offset,
+                                                         const int32_t* __restrict__ kv_len,
+                                                         const float4* __restrict__ part, const int* __restrict__ rev,
+                                                         int b, int Nq, int Nk, int G, int K, int Bs, int nblk, int c0,
+                                                         int cq, float* __restrict__ kl) {
+  const int64_t item = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (item >= int64_t(cq) * G) return;
+  const int il = int(item / G), g = int(item % G);
+  const int i = c0 + il;
+  const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
+  const int pos = sv.q0 + i;
+  const int32_t* srow = sel + ((int64_t(b) * Nq + i) * G + g) * K;
+  const int* rv = rev + (int64_t(il) * G + g) * K;
+  float A = 0.f, Bv = 0.f, m = -INFINITY, l = 0.f;
+  for (int k = 0; k < K; ++k) {
+    if (!sv.ok || !entry_valid(srow[k], pos, Bs, nblk)) continue;
+    const float4 v = part[rv[k]];
+    A += v.x;
+    Bv += v.y;
+    const float mn = fmaxf(m, v.z);
+    l = l * expf(m - mn) + v.w * expf(v.z - mn);
+    m = mn;
+  }
+  kl[(int64_t(b) * Nq + i) * G + g] = l > 0.f ? A - Bv + m + logf(l) : 0.f;
+}
+
 int g_sms = 0;
 int sm_count() {
   if (g_sms == 0) {
@@ -894,6 +1154,43 @@ size_t attn_smem_bytes(int d, int Bs) {
   return 1024 + kv + kRing * slot + meta + (2 + 2 * kRing + 8 + 1) * 8 + 16;
 }
 
+// selection -> per-(group, block) entry lists, tiles and the persistent
+// grid's cost split, for one query chunk [c0, c0 + cq) of sequence b
+cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int32_t* kv_len, int b, int Nq, int Nk,
+                         int G, int K, int Bs, int per_tile, int c0, int cq, int grid, char* w, const KvoLayout& L,
+                         uint32_t* status, cudaStream_t stream) {
+  const int nblk = (Nk + Bs - 1) / Bs, nbins = G * nblk, rows_per_cta = 1024;
+  const size_t hist_smem = size_t(nblk) * 4 * 2;
+  if (hist_smem > 200 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (hist_smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(attn_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem));
+    if (e != cudaSuccess) return e;
+  }
+  int* cnt = reinterpret_cast<int*>(w + L.cnt);
+  const dim3 igrid((cq + rows_per_cta - 1) / rows_per_cta, G);
+  if ((e = cudaMemsetAsync(w + L.cnt, 0, L.entry_off - L.cnt, stream)) != cudaSuccess) return e;
+  ProfScope pf("attn_invert", stream);
+  attn_count_kernel<<<igrid, 256, size_t(nblk) * 4, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0,
+                                                              cq, rows_per_cta, cnt, status);
+  attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, q_offset, b, nblk, nbins, per_tile, Bs, c0, cq, grid,
+                                           reinterpret_cast<int*>(w + L.entry_off),
+                                           reinterpret_cast<int*>(w + L.tile_off),
+                                           reinterpret_cast<int*>(w + L.cost_off), reinterpret_cast<int*>(w + L.total),
+                                           reinterpret_cast<int*>(w + L.cta_start));
+  attn_tiles_kernel<<<(nbins + 255) / 256, 256, 0, stream>>>(cnt, reinterpret_cast<int*>(w + L.entry_off),
+                                                             reinterpret_cast<int*>(w + L.tile_off), nbins, per_tile,
+                                                             reinterpret_cast<int4*>(w + L.tiles));
+  attn_fill_kernel<<<igrid, 256, hist_smem, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0, cq,
+                                                      rows_per_cta, reinterpret_cast<int*>(w + L.entry_off),
+                                                      reinterpret_cast<int*>(w + L.cursor),
+                                                      reinterpret_cast<int*>(w + L.entries),
+                                                      reinterpret_cast<int*>(w + L.rev));
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool attn_kv_outer_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K) {
@@ -914,17 +1211,10 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
                                  int Hkv, int d, int Bs, int K, float scale, void* out, float* lse, void* ws,
                                  cudaStream_t stream) {
   const int G = Hkv, hpg = Hq / Hkv, nblk = (Nk + Bs - 1) / Bs;
-  const int nbins = G * nblk;
   const int per_tile = kRows / hpg;
   const KvoLayout L = kvo_layout(Nq, Hq, G, d, Bs, K, Nk);
   char* w = static_cast<char*>(ws);
   uint32_t* status = &static_cast<WsHeader*>(ws)->status;
-  int* cnt = reinterpret_cast<int*>(w + L.cnt);
-  int* cursor = reinterpret_cast<int*>(w + L.cursor);
-  int* entry_off = reinterpret_cast<int*>(w + L.entry_off);
-  int* tile_off = reinterpret_cast<int*>(w + L.tile_off);
-  int* total = reinterpret_cast<int*>(w + L.total);
-  int* cost_off = reinterpret_cast<int*>(w + L.cost_off);
   int* cta_start = reinterpret_cast<int*>(w + L.cta_start);
   int* entries = reinterpret_cast<int*>(w + L.entries);
   int* rev = reinterpret_cast<int*>(w + L.rev);
@@ -949,8 +1239,6 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   }
 
   const size_t smem = attn_smem_bytes(d, Bs);
-  const size_t hist_smem = size_t(nblk) * 4 * 2;
-  if (hist_smem > 200 * 1024) return cudaErrorInvalidValue;
   auto set_attr = [&](auto kern) {
     // the register split re-allocates exactly the launch allocation: a build
     // that launches with another register count must not run (the increase
@@ -962,12 +1250,6 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   };
   cudaError_t e = cudaSuccess;
-  if (hist_smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(attn_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem));
-    if (e != cudaSuccess) return e;
-  }
 
   AttnParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -990,24 +1272,13 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   const int grid = sm_count() < kMaxGrid ? sm_count() : kMaxGrid;
-  const int rows_per_cta = 1024;
 
   for (int b = 0; b < B; ++b) {
     for (int c0 = 0; c0 < Nq; c0 += cq_max) {
       const int cq = Nq - c0 < cq_max ? Nq - c0 : cq_max;
-      const dim3 igrid((cq + rows_per_cta - 1) / rows_per_cta, G);
-      if ((e = cudaMemsetAsync(w + L.cnt, 0, L.entry_off - L.cnt, stream)) != cudaSuccess) return e;
-      {
-        ProfScope pf("attn_invert", stream);
-        attn_count_kernel<<<igrid, 256, size_t(nblk) * 4, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk,
-                                                                    c0, cq, rows_per_cta, cnt, status);
-        attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, q_offset, b, nblk, nbins, per_tile, Bs, c0, cq, grid,
-                                                 entry_off, tile_off, cost_off, total, cta_start);
-        attn_tiles_kernel<<<(nbins + 255) / 256, 256, 0, stream>>>(cnt, entry_off, tile_off, nbins, per_tile, tiles);
-        attn_fill_kernel<<<igrid, 256, hist_smem, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0, cq,
-                                                            rows_per_cta, entry_off, cursor, entries, rev);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-      }
+      if ((e = invert_chunk(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, per_tile, c0, cq, grid, w, L, status,
+                            stream)) != cudaSuccess)
+        return e;
       prm.b = b;
       prm.c0 = c0;
       {
@@ -1062,6 +1333,110 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
         else
           MSA_CMB(8);
 #undef MSA_CMB
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+    }
+  }
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// KL auxiliary forward (see kl_tile_kernel)
+// ---------------------------------------------------------------------------
+bool kl_aux_supported(int dtype, int Hq, int Hkv, int d, int di, int Bs, int K) {
+  if (dtype != MSA_BF16 || Hkv < 1 || Hq % Hkv != 0) return false;
+  if (!((d == 128 && di == 64) || (d == 64 && di == 32))) return false;
+  if (Bs != 32 && Bs != 64 && Bs != 128) return false;
+  if (K < 1 || K > kMaxK) return false;
+  const int hpg = Hq / Hkv;
+  return hpg == 2 || hpg == 4 || hpg == 8;
+}
+
+size_t kl_aux_ws_bytes(int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K) {
+  return kvo_layout(Nq, Hq, Hkv, d, Bs, K, Nk).end;  // the partials fit in the attention's partial area
+}
+
+cudaError_t launch_kl_aux(const void* q, const void* k, const void* iq, const void* ik, const int32_t* sel,
+                          const float* lse, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk,
+                          int Hq, int Hkv, int d, int di, int Bs, int K, float scale, float* kl, void* ws,
+                          cudaStream_t stream) {
+  const int G = Hkv, hpg = Hq / Hkv, nblk = (Nk + Bs - 1) / Bs;
+  const int per_tile = kRows / hpg;
+  const KvoLayout L = kvo_layout(Nq, Hq, G, d, Bs, K, Nk);
+  char* w = static_cast<char*>(ws);
+  uint32_t* status = &static_cast<WsHeader*>(ws)->status;
+  const int cq_max = chunk_tokens(Nq, Hq, K, d);
+  const int grid = sm_count() < kMaxGrid ? sm_count() : kMaxGrid;
+  KlParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.k = static_cast<const __nv_bfloat16*>(k);
+  prm.iq = static_cast<const __nv_bfloat16*>(iq);
+  prm.ik = static_cast<const __nv_bfloat16*>(ik);
+  prm.lse = lse;
+  prm.entries = reinterpret_cast<const int*>(w + L.entries);
+  prm.tiles = reinterpret_cast<const int4*>(w + L.tiles);
+  prm.cta_start = reinterpret_cast<const int*>(w + L.cta_start);
+  prm.q_offset = q_offset;
+  prm.kv_len = kv_len;
+  prm.part = reinterpret_cast<float4*>(w + L.part_o);
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.Hq = Hq;
+  prm.G = G;
+  prm.nblk = nblk;
+  prm.scale = scale;
+  cudaError_t e;
+  for (int b = 0; b < B; ++b) {
+    for (int c0 = 0; c0 < Nq; c0 += cq_max) {
+      const int cq = Nq - c0 < cq_max ? Nq - c0 : cq_max;
+      if ((e = invert_chunk(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, per_tile, c0, cq, grid, w, L, status,
+                            stream)) != cudaSuccess)
+        return e;
+      prm.b = b;
+      prm.c0 = c0;
+      {
+        ProfScope pf("kl_tile", stream);
+#define MSA_KL(D_, DI_, BS_, HPG_)                                                                            \
+  do {                                                                                                        \
+    auto kern = kl_tile_kernel<D_, DI_, BS_, HPG_>;                                                          \
+    const size_t smem = KlSmem<D_, DI_, BS_, HPG_>::kTotal;                                                  \
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess) \
+      return e;                                                                                               \
+    kern<<<grid, kKlThreads, smem, stream>>>(prm);                                                           \
+  } while (0)
+#define MSA_KL_HPG(D_, DI_, BS_)  \
+  do {                            \
+    if (hpg == 2)                 \
+      MSA_KL(D_, DI_, BS_, 2);    \
+    else if (hpg == 4)            \
+      MSA_KL(D_, DI_, BS_, 4);    \
+    else                          \
+      MSA_KL(D_, DI_, BS_, 8);    \
+  } while (0)
+#define MSA_KL_BS(D_, DI_)          \
+  do {                              \
+    if (Bs == 128)                  \
+      MSA_KL_HPG(D_, DI_, 128);     \
+    else if (Bs == 64)              \
+      MSA_KL_HPG(D_, DI_, 64);      \
+    else                            \
+      MSA_KL_HPG(D_, DI_, 32);      \
+  } while (0)
+        if (d == 128)
+          MSA_KL_BS(128, 64);
+        else
+          MSA_KL_BS(64, 32);
+#undef MSA_KL_BS
+#undef MSA_KL_HPG
+#undef MSA_KL
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+      {
+        ProfScope pf("kl_combine", stream);
+        const int64_t items = int64_t(cq) * G;
+        kl_combine_kernel<<<unsigned((items + 255) / 256), 256, 0, stream>>>(
+            sel, q_offset, kv_len, reinterpret_cast<const float4*>(w + L.part_o), reinterpret_cast<const int*>(w + L.rev),
+            b, Nq, Nk, G, K, Bs, nblk, c0, cq, kl);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
     }

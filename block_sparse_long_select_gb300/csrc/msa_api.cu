@@ -139,6 +139,12 @@ extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int H
       StepPlan p = plan_step(B, Nk, G, Hq, d, di, Bs, K, dtype);
       return p.ok ? p.ws_bytes : 0;
     }
+    case MSA_OP_KL_AUX: {
+      if (B < 1 || Nq < 1 || Nk < 1 || Nq > Nk || G < 1 || Hq < 1 || Hq % G != 0) return 0;
+      // the scratch does not depend on di (ignored here): check the rest with a supported pairing
+      if (!kl_aux_supported(dtype, Hq, G, d, d == 128 ? 64 : 32, Bs, K)) return 0;
+      return kl_aux_ws_bytes(Nq, Nk, Hq, G, d, Bs, K);
+    }
     default:
       return 0;
   }
@@ -256,6 +262,23 @@ extern "C" msa_status_t msa_decode_step(const void* q, const void* k_new, const 
     e = launch_attn_query_outer(dtype, q, k_cache, v_cache, sel, nullptr, kv_len, true, B, 1, Lmax, Hq, Hkv, d, Bs, K,
                                 scale, out, lse, status, stream);
   return cuda_status(e);
+}
+
+extern "C" msa_status_t msa_kl_aux_forward(const void* q, const void* k, const void* iq, const void* ik,
+                                           const int32_t* sel, const float* lse, const int32_t* q_offset,
+                                           const int32_t* kv_len, int B, int Nq, int Nk, int Hq, int Hkv, int d, int di,
+                                           int Bs, int K, float scale, int dtype, float* kl, void* ws,
+                                           size_t ws_bytes, cudaStream_t stream) {
+  if (!q || !k || !iq || !ik || !sel || !lse || !kl) return MSA_ERR_INVALID_ARG;
+  if (B < 1 || Nq < 1 || Nk < 1 || Nq > Nk || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || K < 1 || Bs < 1 ||
+      !dtype_ok(dtype))
+    return MSA_ERR_INVALID_ARG;
+  if (!kl_aux_supported(dtype, Hq, Hkv, d, di, Bs, K)) return MSA_ERR_UNSUPPORTED;
+  msa_status_t w = check_ws(ws, ws_bytes, kl_aux_ws_bytes(Nq, Nk, Hq, Hkv, d, Bs, K));
+  if (w != MSA_OK) return w;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
+  return cuda_status(launch_kl_aux(q, k, iq, ik, sel, lse, q_offset, kv_len, B, Nq, Nk, Hq, Hkv, d, di, Bs, K, scale,
+                                   kl, ws, stream));
 }
 
 extern "C" msa_status_t msa_read_status(void* ws, cudaStream_t stream) {

@@ -123,6 +123,14 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
 cudaError_t launch_decode_append(const void* k_new, const void* v_new, const void* ik_new, void* k_cache,
                                  void* v_cache, void* ik_cache, int32_t* kv_len, int32_t* q_pos, int B, int Lmax,
                                  int Hkv, int d, int di, int elem_bytes, uint32_t* status, cudaStream_t stream);
+// KL auxiliary forward: KL(head-averaged main-branch distribution || index
+// softmax) over each (row, group)'s selected tokens, on the KV-outer bins.
+bool kl_aux_supported(int dtype, int Hq, int Hkv, int d, int di, int Bs, int K);
+size_t kl_aux_ws_bytes(int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K);
+cudaError_t launch_kl_aux(const void* q, const void* k, const void* iq, const void* ik, const int32_t* sel,
+                          const float* lse, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk,
+                          int Hq, int Hkv, int d, int di, int Bs, int K, float scale, float* kl, void* ws,
+                          cudaStream_t stream);
 cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, const void* v, const int32_t* sel,
                                     const int32_t* q_offset, const int32_t* kv_len, bool decode, int B, int Nq,
                                     int Nk, int Hq, int Hkv, int d, int Bs, int K, float scale, void* out, float* lse,

@@ -63,14 +63,20 @@ typedef enum {
 
 typedef enum { MSA_BF16 = 0, MSA_FP32 = 1 } msa_dtype_t;
 
-typedef enum { MSA_OP_INDEX_SELECT = 0, MSA_OP_PREFILL = 1, MSA_OP_DECODE = 2, MSA_OP_DECODE_STEP = 3 } msa_op_t;
+typedef enum {
+  MSA_OP_INDEX_SELECT = 0,
+  MSA_OP_PREFILL = 1,
+  MSA_OP_DECODE = 2,
+  MSA_OP_DECODE_STEP = 3,
+  MSA_OP_KL_AUX = 4
+} msa_op_t;
 
 /* Bytes of scratch `ws` the entry point `op` needs for these sizes (the same
  * argument meanings as the entry points; unused ones may be 0: G and di for
  * the attention ops, Hq and d for MSA_OP_INDEX_SELECT; for MSA_OP_DECODE and
  * MSA_OP_DECODE_STEP, Nq is ignored and Nk is Lmax; MSA_OP_DECODE_STEP uses
- * every other argument, with G = Hkv). Returns 0 when the arguments are
- * invalid. */
+ * every other argument, with G = Hkv; MSA_OP_KL_AUX uses all but di, with
+ * G = Hkv). Returns 0 when the arguments are invalid or not supported. */
 size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K, int dtype);
 
 /* Index Branch: block selection for every (query row, group).
@@ -192,6 +198,31 @@ msa_status_t msa_decode_step(const void* q, const void* k_new, const void* v_new
                              void* k_cache, void* v_cache, void* ik_cache, int32_t* kv_len, int B, int Lmax, int Hq,
                              int Hkv, int d, int di, int Bs, int K, float scale, int dtype, int32_t* sel, void* out,
                              float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* KL auxiliary forward: for every (query row, group) the divergence
+ *   KL(p || q) = sum_j p_j (log p_j - log q_j)
+ * over the tokens j of the group's selected blocks (causally visible), where
+ * p is the Main Branch's attention distribution averaged over the group's
+ * query heads and q the softmax of the Index Branch's plain dot-product
+ * scores over the same tokens (quant_prune_distill post 751, "Метод": the
+ * index branch is trained with the KL divergence to the head-averaged main
+ * branch, main-branch probabilities under stop-gradient; hyper.ai summary of
+ * paper 2606.13392, "方法": the two distributions are aligned over the selected
+ * tokens). Forward value only.
+ *
+ *  q [B, Nq, Hq, d], k [B, Nk, Hkv, d], iq [B, Nq, Hkv, di], ik [B, Nk, di] (dtype)
+ *  sel [B, Nq, Hkv, K] int32: the selection (msa_index_select)
+ *  lse [B, Nq, Hq] fp32: the forward's lse (msa_sparse_attn_prefill), which
+ *       normalises p; scale must be the forward's (<= 0 selects 1/sqrt(d))
+ *  q_offset, kv_len: as for msa_index_select
+ *  kl [B, Nq, Hkv] fp32, out (0 for a row without attended tokens)
+ *  ws: msa_workspace_size(MSA_OP_KL_AUX, B, Nq, Nk, Hkv, Hq, d, 0, Bs, K, dtype)
+ *  Supported: BF16; (d, di) in {(128, 64), (64, 32)}; Bs in {32, 64, 128};
+ *  Hq / Hkv in {2, 4, 8}; other sizes return MSA_ERR_UNSUPPORTED. */
+msa_status_t msa_kl_aux_forward(const void* q, const void* k, const void* iq, const void* ik, const int32_t* sel,
+                                const float* lse, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
+                                int Nk, int Hq, int Hkv, int d, int di, int Bs, int K, float scale, int dtype,
+                                float* kl, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the sticky device status of workspace `ws`
  * (MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_BOUNDS) and clears it. Returns
