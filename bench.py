@@ -40,7 +40,8 @@ KERNEL_SOURCES = {  # kernel name -> source file (for the ncu traffic freshness 
     "attn_query_outer": "attn_query_outer.cu", "index_fused_tc": "index_fused_tc.cu",
     "attn_kv_outer_tc": "attn_kv_outer_tc.cu", "attn_invert": "attn_kv_outer_tc.cu",
     "attn_combine": "attn_kv_outer_tc.cu", "decode_index": "decode.cu", "decode_topk": "decode.cu",
-    "decode_attn": "decode.cu", "decode_combine": "decode.cu",
+    "decode_attn": "decode.cu", "decode_combine": "decode.cu", "kl_tile": "attn_kv_outer_tc.cu",
+    "kl_combine": "attn_kv_outer_tc.cu",
 }
 
 
@@ -54,6 +55,7 @@ def parse_args():
     ap.add_argument("--decode-workload", default="decode_b64")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kl", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = auto)")
     return ap.parse_args()
@@ -227,6 +229,15 @@ def decode_work(w, sel, kl):
             "attn_flops": 4.0 * w.d * (w.Hq // w.G) * float(att), "attended_keys": att}
 
 
+def kl_work(w, work):
+    """The KL auxiliary pass recomputes, for every attended key of every
+    (query, group), the Hq/G main scores (2 d flops each) and the index score
+    (2 di flops): the score half of the attention plus the index dot products
+    restricted to the selection."""
+    att = work["attended_keys"]
+    return {"kl_flops": 2.0 * w.d * (w.Hq // w.G) * float(att) + 2.0 * w.di * float(att)}
+
+
 def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="prefill"):
     """Roofline entry of one kernel. achieved = algorithmic work per launch /
     mean launch duration, both from the timed region: the per-step work of the
@@ -247,6 +258,8 @@ def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="pre
         bound, unit, per_step = "tensor", "TFLOP/s", work["index_flops"]
     elif kernel in ("attn_kv_outer_tc", "attn_query_outer"):
         bound, unit, per_step = "tensor", "TFLOP/s", work["attn_flops"]
+    elif kernel == "kl_tile":
+        bound, unit, per_step = "tensor", "TFLOP/s", work["kl_flops"]
     else:
         return None
     amount = per_step * steps / launches
@@ -341,6 +354,42 @@ def run_msa(args, dist):
     kernels = {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4),
                    "share": round(v[1] / max(sum(x[1] for x in prof.values()), 1e-9), 4)} for k, v in prof.items()}
     all_roofs = [r for r in (roofline_for(k, prof, work, peaks, peak_src, w.name, args.steps) for k in prof) if r]
+
+    # ------------------------- KL auxiliary forward ---------------------
+    # msa_kl_aux_forward over the prefill's selection and lse (one prefill
+    # with lse output before the timed region); a step is one KL pass
+    kl_leg = None
+    if not args.no_kl:
+        lse = torch.empty((w.B, w.Nq, w.Hq), dtype=torch.float32, device=dev)
+        msa.msa_index_select(t["iq"], t["ik"], qo, kl, w.Bs, w.K, sel=sel, ws=ws_i)
+        msa.msa_sparse_attn_prefill(t["q"], t["k"], t["v"], sel, qo, kl, w.Bs, w.K, out=out, lse=lse, ws=ws_a)
+        klo = torch.empty((w.B, w.Nq, w.G), dtype=torch.float32, device=dev)
+        ws_k = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_KL_AUX, w.B, w.Nq, w.Nk, w.G, w.Hq, w.d, 0, w.Bs,
+                                                    w.K, msa.MSA_BF16), dev)
+
+        def kl_step():
+            msa.msa_kl_aux_forward(t["q"], t["k"], t["iq"], t["ik"], sel, lse, qo, kl, w.Bs, w.K, kl=klo, ws=ws_k)
+
+        kms, _, kclocks, _ = time_steps(kl_step, args.steps, args.warmup, profile=False)
+        _, kprof, _, _ = time_steps(kl_step, args.steps, 0, profile=True)
+        st = msa.msa_read_status(ws_k)
+        if st != 0:
+            raise RuntimeError(f"device status after KL: {msa.msa_status_string(st)}")
+        if not bool(torch.isfinite(klo).all()):
+            raise RuntimeError("KL auxiliary output not finite")
+        kwork = kl_work(w, work)
+        k_tot = dist.max(sum(kms) / 1e3)
+        kl_leg = {"value": round(dist.sum(tokens * args.steps) / k_tot, 1), "unit": "tokens/s",
+                  "ms_per_step": round(float(np.mean(kms)), 4), "steps": args.steps,
+                  "what": "msa_kl_aux_forward: KL(head-averaged main distribution || index softmax) over the "
+                          "selected keys of every (query, group), from the forward's lse",
+                  "roofline": roofline_for("kl_tile", kprof, kwork, peaks, peak_src, w.name, args.steps)
+                  if "kl_tile" in kprof else None,
+                  "kernels": {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4)}
+                              for k, v in kprof.items()},
+                  "gpu_launches": sum(v[0] for v in kprof.values()), "clocks": kclocks,
+                  "kl_flops_per_step": kwork["kl_flops"]}
+        del lse, klo, ws_k
 
     # ---------------------------- e2e (host buffers) -------------------
     # Every step copies its inputs from pinned host memory and reads its
@@ -499,7 +548,7 @@ def run_msa(args, dist):
         "roofline": roof, "roofline_all": all_roofs, "kernels": kernels, "gpu_launches": launches,
         "kernel_times": "per-kernel CUDA events on the launching stream, in a second pass of the same steps "
                         "(the timed pass carries no events between kernels)",
-        "clocks": clocks, "e2e": e2e, "decode": decode,
+        "clocks": clocks, "e2e": e2e, "decode": decode, "kl_aux": kl_leg,
         "work": {"index_flops": work["index_flops"], "attn_flops": work["attn_flops"],
                  "attended_keys": work["attended_keys"]},
         "wall_s_timed_region": round(wall, 3),
