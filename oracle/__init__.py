@@ -1,9 +1,10 @@
-"""CPU oracle for the MSA forward path (TEST INFRASTRUCTURE ONLY).
+"""CPU oracle for the MSA path (TEST INFRASTRUCTURE ONLY).
 
 Thin ctypes wrapper over ``msa_oracle.cpp``: plain fp64 C++ that restates the
 Index Branch (dot-product index scores, block max pooling, top-K with the local
-block forced, ties to the lower block) and the Main Branch (exact causal
-softmax attention over the selected blocks). Only ``tests/``, the smoke check
+block forced, ties to the lower block), the Main Branch (exact causal softmax
+attention over the selected blocks) with its backward, and the KL auxiliary
+value. Only ``tests/``, the smoke check
 and the bench's CPU-baseline / reference leg may import this package; the
 product library never does. It shares no code with the CUDA path: inputs come
 from ``synth`` (generation only), everything else is computed here.
@@ -52,6 +53,9 @@ def _load(path):
     lib.msa_oracle_kl_aux.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                       f64, vp, i32]
     lib.msa_oracle_kl_aux.restype = i32
+    lib.msa_oracle_sparse_attn_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32,
+                                                    i32, i32, i32, f64, vp, vp, vp, i32]
+    lib.msa_oracle_sparse_attn_backward.restype = i32
     return lib
 
 
@@ -152,6 +156,36 @@ def kl_aux(q_rows, k, iq_rows, ik, sel_rows, row_b, row_i, q_offset, kv_len, Bs,
     if rc != 0:
         raise ValueError("oracle kl_aux rejected its arguments")
     return kl
+
+
+def sparse_attn_backward(q_rows, k, v, dout_rows, sel_rows, row_b, row_i, q_offset, kv_len, Bs, K, scale=0.0,
+                         nthreads=None, lib=None):
+    """Main Branch backward for listed rows (the selection carries no gradient).
+
+    q_rows, dout_rows [n, Hq, d]; k, v [B, Nk, Hkv, d]; sel_rows [n, Hkv, K].
+    Returns dq [n, Hq, d] and dk, dv [B, Nk, Hkv, d] (fp64): the listed rows'
+    contributions.
+    """
+    q_rows, dout_rows = _c(q_rows, np.float32), _c(dout_rows, np.float32)
+    k = k if (k.dtype == np.float32 and k.flags.c_contiguous) else _c(k, np.float32)
+    v = v if (v.dtype == np.float32 and v.flags.c_contiguous) else _c(v, np.float32)
+    n, Hq, d = q_rows.shape
+    B, Nk, Hkv, d2 = k.shape
+    assert d == d2 and v.shape == k.shape and dout_rows.shape == q_rows.shape
+    sel_rows = _c(sel_rows, np.int32)
+    assert sel_rows.shape == (n, Hkv, K)
+    row_b, row_i = _c(row_b, np.int32), _c(row_i, np.int32)
+    q_offset, kv_len = _c(q_offset, np.int32), _c(kv_len, np.int32)
+    dq = np.empty((n, Hq, d), dtype=np.float64)
+    dk = np.empty((B, Nk, Hkv, d), dtype=np.float64)
+    dv = np.empty((B, Nk, Hkv, d), dtype=np.float64)
+    rc = (lib or _lib()).msa_oracle_sparse_attn_backward(
+        q_rows.ctypes.data, k.ctypes.data, v.ctypes.data, dout_rows.ctypes.data, sel_rows.ctypes.data,
+        row_b.ctypes.data, row_i.ctypes.data, n, q_offset.ctypes.data, kv_len.ctypes.data, B, Nk, Hq, Hkv, d, Bs, K,
+        float(scale), dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle sparse_attn_backward rejected its arguments")
+    return dq, dk, dv
 
 
 # ---------------------------------------------------------------------------

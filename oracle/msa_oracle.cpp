@@ -1,5 +1,5 @@
-// MSA forward oracle: plain, slow, fp64 CPU restatement of what the sparse
-// attention path computes. TEST INFRASTRUCTURE ONLY: the tests, the smoke check
+// MSA oracle: plain, slow, fp64 CPU restatement of what the sparse attention
+// path computes (forward, its backward, the KL auxiliary value). TEST INFRASTRUCTURE ONLY: the tests, the smoke check
 // and the bench's CPU-baseline / reference leg call it; the product library
 // never does. It shares no code, header or helper with the CUDA path.
 //
@@ -267,6 +267,105 @@ int msa_oracle_kl_aux(const float* q_rows, const float* k, const float* iq_rows,
       for (size_t x = 0; x < n; ++x)
         if (p[x] > 0.0) div += p[x] * (std::log(p[x]) - (s[x] - lse_q));
       kl[r * Hkv + g] = div;
+    }
+  });
+  return 0;
+}
+
+// Main Branch backward for a list of query rows: the gradients of a scalar
+// loss with respect to q, k and v, given dout = dLoss/dOut. The selection is
+// a discrete choice of the Index Branch and carries no gradient; the Main
+// Branch is plain softmax attention over the selected tokens (hyper.ai
+// summary, "方法"), so its gradient is the textbook one. The forward is
+// recomputed here in fp64 from its definition, then differentiated by the
+// chain rule over the attended tokens T of each (row, head):
+//   P_j = softmax_j(scale q.k_j),  O = sum_j P_j v_j
+//   dv_j += P_j dout;  dP_j = dout.v_j;  delta = dout.O (= sum_j P_j dP_j)
+//   dS_j = P_j (dP_j - delta);  dq = scale sum_j dS_j k_j;  dk_j += scale dS_j q
+//   q_rows, dout_rows [nrows, Hq, d]; k, v [B, Nk, Hkv, d]; sel_rows [nrows, Hkv, K]
+//   dq [nrows, Hq, d] (fp64, out); dk, dv [B, Nk, Hkv, d] (fp64, out): the
+//   listed rows' contributions (zero where no listed row attends).
+//   scale <= 0 selects 1/sqrt(d).
+int msa_oracle_sparse_attn_backward(const float* q_rows, const float* k, const float* v, const float* dout_rows,
+                                    const int32_t* sel_rows, const int32_t* row_b, const int32_t* row_i,
+                                    int64_t nrows, const int32_t* q_offset, const int32_t* kv_len, int B, int Nk,
+                                    int Hq, int Hkv, int d, int Bs, int K, double scale, double* dq, double* dk,
+                                    double* dv, int nthreads) {
+  if (!q_rows || !k || !v || !dout_rows || !sel_rows || !row_b || !row_i || !q_offset || !kv_len || !dq || !dk ||
+      !dv)
+    return 1;
+  if (B < 1 || Nk < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d < 1 || Bs < 1 || K < 1) return 1;
+  if (scale <= 0.0) scale = 1.0 / std::sqrt(static_cast<double>(d));
+  const int nblk = (Nk + Bs - 1) / Bs;
+  const int hpg = Hq / Hkv;
+  const int64_t kv_elems = int64_t(B) * Nk * Hkv * d;
+  for (int64_t x = 0; x < kv_elems; ++x) dk[x] = dv[x] = 0.0;
+  // one work unit per (sequence, key/value head): it owns dk, dv of that head
+  // and dq of the group's query heads, so units never write the same element
+  parallel_rows(int64_t(B) * Hkv, nthreads, [&](int64_t u) {
+    const int b = int(u / Hkv), g = int(u % Hkv);
+    const int pos_base = q_offset[b], L = kv_len[b];
+    std::vector<int> toks;
+    std::vector<double> P, o(d);
+    for (int64_t r = 0; r < nrows; ++r) {
+      if (row_b[r] != b) continue;
+      const int pos = pos_base + row_i[r];
+      toks.clear();
+      const int32_t* blocks = sel_rows + (r * Hkv + g) * K;
+      for (int kk = 0; kk < K; ++kk) {
+        const int t = blocks[kk];
+        if (t < 0 || t >= nblk) continue;
+        for (int j = t * Bs; j < (t + 1) * Bs; ++j) {
+          if (j > pos || j >= L) break;  // the forward's mask: diagonal kept, nothing at or past kv_len
+          toks.push_back(j);
+        }
+      }
+      for (int hh = 0; hh < hpg; ++hh) {
+        const int h = g * hpg + hh;
+        const float* qh = q_rows + (r * Hq + h) * int64_t(d);
+        const float* gh = dout_rows + (r * Hq + h) * int64_t(d);
+        double* dqh = dq + (r * Hq + h) * int64_t(d);
+        for (int c = 0; c < d; ++c) dqh[c] = 0.0;
+        const size_t n = toks.size();
+        if (n == 0) continue;
+        // forward: probabilities and output
+        P.assign(n, 0.0);
+        double mx = -std::numeric_limits<double>::infinity();
+        for (size_t x = 0; x < n; ++x) {
+          const float* kj = k + ((int64_t(b) * Nk + toks[x]) * Hkv + g) * int64_t(d);
+          double dot = 0.0;
+          for (int c = 0; c < d; ++c) dot += double(qh[c]) * double(kj[c]);
+          P[x] = scale * dot;
+          if (P[x] > mx) mx = P[x];
+        }
+        double den = 0.0;
+        for (size_t x = 0; x < n; ++x) {
+          P[x] = std::exp(P[x] - mx);
+          den += P[x];
+        }
+        for (size_t x = 0; x < n; ++x) P[x] /= den;
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        for (size_t x = 0; x < n; ++x) {
+          const float* vj = v + ((int64_t(b) * Nk + toks[x]) * Hkv + g) * int64_t(d);
+          for (int c = 0; c < d; ++c) o[c] += P[x] * double(vj[c]);
+        }
+        double delta = 0.0;
+        for (int c = 0; c < d; ++c) delta += double(gh[c]) * o[c];
+        // backward
+        for (size_t x = 0; x < n; ++x) {
+          const int64_t kvrow = ((int64_t(b) * Nk + toks[x]) * Hkv + g) * int64_t(d);
+          const float* kj = k + kvrow;
+          const float* vj = v + kvrow;
+          double dP = 0.0;
+          for (int c = 0; c < d; ++c) dP += double(gh[c]) * double(vj[c]);
+          const double dS = P[x] * (dP - delta);
+          for (int c = 0; c < d; ++c) {
+            dqh[c] += scale * dS * double(kj[c]);
+            dk[kvrow + c] += scale * dS * double(qh[c]);
+            dv[kvrow + c] += P[x] * double(gh[c]);
+          }
+        }
+      }
     }
   });
   return 0;

@@ -17,6 +17,10 @@
 * the KL auxiliary forward: non-negative, zero on matched distributions, the
   closed form for a uniform main distribution, and invariance to shifting a
   row's index scores;
+* the Main Branch backward: equal to torch autograd through the masked-dense
+  restatement (fp64), to central finite differences of the forward oracle
+  (selection held fixed), and to the closed forms sum_j dk_j = 0,
+  sum_j dv_j = sum over the group's rows of dout, sum q.dq = sum k.dk;
 * planted mistakes in a copy of the oracle source fail at least one pin.
 """
 import math
@@ -385,9 +389,84 @@ def pin_kl_aux(lib=None):
     assert np.abs(kl2 - kl).max() < 1e-9 * max(1.0, np.abs(kl).max())
 
 
+def _bwd_inputs(seed, B=2, Nq=40, Nk=96, Hq=4, Hkv=2, d=16, Bs=8, K=5):
+    q, k, v, iq, ik, qo, kl = rand_problem(seed, B=B, Nq=Nq, Nk=Nk, Hq=Hq, Hkv=Hkv, d=d, di=8,
+                                           q_offset=[Nk - Nq, 20], kv_len=[Nk, Nq + 20])
+    rb, ri = oracle.all_rows(B, Nq)
+    sel = oracle.index_select(iq.reshape(-1, Hkv, 8), ik, rb, ri, qo, kl, Bs, K)
+    dout = np.random.default_rng(seed + 100).standard_normal(q.shape).astype(np.float32)
+    return q, k, v, dout, qo, kl, rb, ri, sel
+
+
+def pin_attn_backward(lib=None):
+    """Main Branch backward: torch autograd through the masked-dense
+    restatement in fp64; the closed forms of its sums; central finite
+    differences of the (separately pinned) forward oracle on a tiny case."""
+    Bs, K = 8, 5
+    B, Nq, Nk, Hq, Hkv, d = 2, 40, 96, 4, 2, 16
+    hpg = Hq // Hkv
+    q, k, v, dout, qo, kl_, rb, ri, sel = _bwd_inputs(31)
+    dq, dk, dv = oracle.sparse_attn_backward(q.reshape(-1, Hq, d), k, v, dout.reshape(-1, Hq, d), sel, rb, ri, qo,
+                                             kl_, Bs, K, lib=lib)
+    scale = 1.0 / math.sqrt(d)
+    allowed = selected_allowed(sel.reshape(B, Nq, Hkv, K), Bs, B, Nq, Nk, Hkv, qo, kl_)
+    qt = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    kt = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    vt = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    s_ = torch.einsum("bihc,bjhc->bhij", qt, kt.repeat_interleave(hpg, dim=2)) * scale
+    m = torch.from_numpy(allowed).repeat_interleave(hpg, dim=2).permute(0, 2, 1, 3)
+    p_ = torch.softmax(s_.masked_fill(~m, -math.inf), dim=-1)
+    o = torch.einsum("bhij,bjhc->bihc", p_, vt.repeat_interleave(hpg, dim=2))
+    (o * torch.from_numpy(dout.astype(np.float64))).sum().backward()
+    for got, want in ((dq.reshape(B, Nq, Hq, d), qt.grad), (dk, kt.grad), (dv, vt.grad)):
+        want = want.numpy()
+        assert np.abs(got - want).max() < 1e-10 * max(1.0, np.abs(want).max())
+    # closed forms per (sequence, kv head)
+    for b in range(B):
+        for g in range(Hkv):
+            assert np.abs(dk[b, :, g].sum(axis=0)).max() < 1e-9
+            want_v = dout[b, :, g * hpg:(g + 1) * hpg].astype(np.float64).sum(axis=(0, 1))
+            assert np.abs(dv[b, :, g].sum(axis=0) - want_v).max() < 1e-9
+            qdq = (q[b, :, g * hpg:(g + 1) * hpg].astype(np.float64) *
+                   dq.reshape(B, Nq, Hq, d)[b, :, g * hpg:(g + 1) * hpg]).sum()
+            kdk = (k[b, :, g].astype(np.float64) * dk[b, :, g]).sum()
+            assert abs(qdq - kdk) < 1e-9 * max(1.0, abs(qdq))
+    # finite differences: dyadic inputs so that x +- h is exact in fp32
+    rng = np.random.default_rng(8)
+    B1, N1, Hq1, Hkv1, d1, Bs1, K1 = 1, 24, 2, 1, 8, 4, 3
+    q1 = (rng.integers(-32, 33, (B1, N1, Hq1, d1)) / 16).astype(np.float32)
+    k1 = (rng.integers(-32, 33, (B1, N1, Hkv1, d1)) / 16).astype(np.float32)
+    v1 = (rng.integers(-32, 33, (B1, N1, Hkv1, d1)) / 16).astype(np.float32)
+    g1 = (rng.integers(-32, 33, (B1, N1, Hq1, d1)) / 16).astype(np.float32)
+    iq1 = rng.integers(-3, 4, (B1, N1, Hkv1, 4)).astype(np.float32)
+    ik1 = rng.integers(-3, 4, (B1, N1, 4)).astype(np.float32)
+    rb1, ri1 = oracle.all_rows(B1, N1)
+    qo1, kl1 = np.zeros(1, np.int32), np.full(1, N1, np.int32)
+    sel1 = oracle.index_select(iq1.reshape(-1, Hkv1, 4), ik1, rb1, ri1, qo1, kl1, Bs1, K1)
+    gq, gk, gv = oracle.sparse_attn_backward(q1.reshape(-1, Hq1, d1), k1, v1, g1.reshape(-1, Hq1, d1), sel1, rb1, ri1,
+                                             qo1, kl1, Bs1, K1, lib=lib)
+    grads = {"q": gq.reshape(q1.shape), "k": gk, "v": gv}
+
+    def loss(qq, kk, vv):
+        out, _ = oracle.sparse_attn(qq.reshape(-1, Hq1, d1), kk, vv, sel1, rb1, ri1, qo1, kl1, Bs1, K1)
+        return float((out * g1.reshape(-1, Hq1, d1).astype(np.float64)).sum())
+
+    h = 2.0 ** -10
+    for name, arr in (("q", q1), ("k", k1), ("v", v1)):
+        for _ in range(5):
+            idx = tuple(int(rng.integers(0, n)) for n in arr.shape)
+            xp, xm = arr.copy(), arr.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q1, "k": k1, "v": v1, name: xp}
+            args_m = {"q": q1, "k": k1, "v": v1, name: xm}
+            fd = (loss(args_p["q"], args_p["k"], args_p["v"]) - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * h)
+            assert abs(fd - grads[name][idx]) < 1e-5 * max(1.0, abs(fd)), (name, idx, fd, grads[name][idx])
+
+
 PINS = [pin_golden, pin_blockmax_bruteforce, pin_selection_invariants, pin_closed_forms, pin_dense_equals_sdpa,
         pin_masked_dense_equals_sdpa, pin_attention_special_cases, pin_decode_equals_prefill_row, pin_force_start,
-        pin_kl_aux]
+        pin_kl_aux, pin_attn_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -414,6 +493,11 @@ MUTATIONS = {
                                     "j < pos && j < L; ++j) keys.push_back(j);"),
     "kl_heads_not_averaged": ("p[x] += std::exp(z[x] - m) / l / double(hpg);", "p[x] += std::exp(z[x] - m) / l;"),
     "kl_index_scores_scaled": ("        s[x] = acc;\n", "        s[x] = acc * scale;\n"),
+    "bwd_drops_delta": ("const double dS = P[x] * (dP - delta);", "const double dS = P[x] * dP;"),
+    "bwd_dk_unscaled": ("dk[kvrow + c] += scale * dS * double(qh[c]);", "dk[kvrow + c] += dS * double(qh[c]);"),
+    "bwd_dv_weighted_by_ds": ("dv[kvrow + c] += P[x] * double(gh[c]);", "dv[kvrow + c] += dS * double(gh[c]);"),
+    "bwd_causal_excludes_diagonal": ("if (j > pos || j >= L) break;", "if (j >= pos || j >= L) break;"),
+    "bwd_dq_from_values": ("dqh[c] += scale * dS * double(kj[c]);", "dqh[c] += scale * dS * double(vj[c]);"),
     "kl_reversed_direction": ("if (p[x] > 0.0) div += p[x] * (std::log(p[x]) - (s[x] - lse_q));",
                               "div += std::exp(s[x] - lse_q) * ((s[x] - lse_q) - std::log(p[x] + 1e-300));"),
 }
