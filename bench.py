@@ -41,7 +41,7 @@ KERNEL_SOURCES = {  # kernel name -> source file (for the ncu traffic freshness 
     "attn_kv_outer_tc": "attn_kv_outer_tc.cu", "attn_invert": "attn_kv_outer_tc.cu",
     "attn_combine": "attn_kv_outer_tc.cu", "decode_index": "decode.cu", "decode_topk": "decode.cu",
     "decode_attn": "decode.cu", "decode_combine": "decode.cu", "kl_tile": "attn_kv_outer_tc.cu",
-    "kl_combine": "attn_kv_outer_tc.cu",
+    "kl_combine": "attn_kv_outer_tc.cu", "bwd_tile": "attn_backward.cu", "bwd_dq_combine": "attn_backward.cu",
 }
 
 
@@ -56,6 +56,7 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kl", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = auto)")
     return ap.parse_args()
@@ -238,6 +239,12 @@ def kl_work(w, work):
     return {"kl_flops": 2.0 * w.d * (w.Hq // w.G) * float(att) + 2.0 * w.di * float(att)}
 
 
+def backward_work(w, work):
+    """The backward recomputes S and forms dP, then the dV, dK and dQ products:
+    five d-long dot products per (token, head, attended key)."""
+    return {"bwd_flops": 10.0 * w.d * (w.Hq // w.G) * float(work["attended_keys"])}
+
+
 def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="prefill"):
     """Roofline entry of one kernel. achieved = algorithmic work per launch /
     mean launch duration, both from the timed region: the per-step work of the
@@ -260,6 +267,8 @@ def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="pre
         bound, unit, per_step = "tensor", "TFLOP/s", work["attn_flops"]
     elif kernel == "kl_tile":
         bound, unit, per_step = "tensor", "TFLOP/s", work["kl_flops"]
+    elif kernel == "bwd_tile":
+        bound, unit, per_step = "tensor", "TFLOP/s", work["bwd_flops"]
     else:
         return None
     amount = per_step * steps / launches
@@ -358,11 +367,12 @@ def run_msa(args, dist):
     # ------------------------- KL auxiliary forward ---------------------
     # msa_kl_aux_forward over the prefill's selection and lse (one prefill
     # with lse output before the timed region); a step is one KL pass
-    kl_leg = None
-    if not args.no_kl:
+    kl_leg = bwd_leg = None
+    if not (args.no_kl and args.no_backward):
         lse = torch.empty((w.B, w.Nq, w.Hq), dtype=torch.float32, device=dev)
         msa.msa_index_select(t["iq"], t["ik"], qo, kl, w.Bs, w.K, sel=sel, ws=ws_i)
         msa.msa_sparse_attn_prefill(t["q"], t["k"], t["v"], sel, qo, kl, w.Bs, w.K, out=out, lse=lse, ws=ws_a)
+    if not args.no_kl:
         klo = torch.empty((w.B, w.Nq, w.G), dtype=torch.float32, device=dev)
         ws_k = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_KL_AUX, w.B, w.Nq, w.Nk, w.G, w.Hq, w.d, 0, w.Bs,
                                                     w.K, msa.MSA_BF16), dev)
@@ -389,7 +399,40 @@ def run_msa(args, dist):
                               for k, v in kprof.items()},
                   "gpu_launches": sum(v[0] for v in kprof.values()), "clocks": kclocks,
                   "kl_flops_per_step": kwork["kl_flops"]}
-        del lse, klo, ws_k
+        del klo, ws_k
+    # ------------------------- Main Branch backward ---------------------
+    # msa_sparse_attn_backward over the prefill's selection, output and lse
+    # with a synthetic output gradient; a step is one backward pass
+    if not args.no_backward:
+        dout = synth.device_tensor(synth.scaled(w, seed=w.seed + 1000), "q", dev)
+        dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+        ws_b = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_BACKWARD, w.B, w.Nq, w.Nk, w.G, w.Hq, w.d, 0, w.Bs,
+                                                    w.K, msa.MSA_BF16), dev)
+
+        def bwd_step():
+            msa.msa_sparse_attn_backward(t["q"], t["k"], t["v"], out, dout, lse, sel, qo, kl, w.Bs, w.K, dq=dq,
+                                         dk=dk, dv=dv, ws=ws_b)
+
+        bms, _, bclocks, _ = time_steps(bwd_step, args.steps, args.warmup, profile=False)
+        _, bprof, _, _ = time_steps(bwd_step, args.steps, 0, profile=True)
+        st = msa.msa_read_status(ws_b)
+        if st != 0:
+            raise RuntimeError(f"device status after backward: {msa.msa_status_string(st)}")
+        bwork = backward_work(w, work)
+        b_tot = dist.max(sum(bms) / 1e3)
+        bwd_leg = {"value": round(dist.sum(tokens * args.steps) / b_tot, 1), "unit": "tokens/s",
+                   "ms_per_step": round(float(np.mean(bms)), 4), "steps": args.steps,
+                   "what": "msa_sparse_attn_backward: dq, dk, dv over the selected blocks from the forward's "
+                           "selection, output and lse, synthetic output gradient",
+                   "roofline": roofline_for("bwd_tile", bprof, bwork, peaks, peak_src, w.name, args.steps)
+                   if "bwd_tile" in bprof else None,
+                   "kernels": {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4)}
+                               for k, v in bprof.items()},
+                   "gpu_launches": sum(v[0] for v in bprof.values()), "clocks": bclocks,
+                   "bwd_flops_per_step": bwork["bwd_flops"]}
+        del dout, dq, dk, dv, ws_b
+    if not (args.no_kl and args.no_backward):
+        del lse
 
     # ---------------------------- e2e (host buffers) -------------------
     # Every step copies its inputs from pinned host memory and reads its
@@ -548,7 +591,7 @@ def run_msa(args, dist):
         "roofline": roof, "roofline_all": all_roofs, "kernels": kernels, "gpu_launches": launches,
         "kernel_times": "per-kernel CUDA events on the launching stream, in a second pass of the same steps "
                         "(the timed pass carries no events between kernels)",
-        "clocks": clocks, "e2e": e2e, "decode": decode, "kl_aux": kl_leg,
+        "clocks": clocks, "e2e": e2e, "decode": decode, "kl_aux": kl_leg, "backward": bwd_leg,
         "work": {"index_flops": work["index_flops"], "attn_flops": work["attn_flops"],
                  "attended_keys": work["attended_keys"]},
         "wall_s_timed_region": round(wall, 3),

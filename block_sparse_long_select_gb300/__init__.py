@@ -1,4 +1,4 @@
-"""MSA (MiniMax Sparse Attention) forward path on GB300: Python binding.
+"""MSA (MiniMax Sparse Attention) hot path on GB300: Python binding.
 
 Argument marshalling over the C ABI of ``libmsa.so`` (declared in
 ``include/msa.h``); every step of the path runs in the library's CUDA kernels.
@@ -7,7 +7,8 @@ carry the C names:
 
     msa_workspace_size, msa_index_select, msa_index_select_v,
     msa_sparse_attn_prefill, msa_sparse_attn_decode, msa_decode_step,
-    msa_kl_aux_forward, msa_read_status, msa_status_string
+    msa_kl_aux_forward, msa_sparse_attn_backward, msa_read_status,
+    msa_status_string
 
 There is no CPU fallback: if ``libmsa.so`` is missing or was not built for
 this GPU, every call raises.
@@ -17,6 +18,7 @@ from ._lib import (  # noqa: F401
     MSA_FORCE_LOCAL,
     MSA_FORCE_START,
     MSA_FP32,
+    MSA_OP_BACKWARD,
     MSA_OP_DECODE,
     MSA_OP_DECODE_STEP,
     MSA_OP_INDEX_SELECT,
@@ -33,6 +35,7 @@ from ._lib import (  # noqa: F401
     msa_profile_end,
     msa_decode_step,
     msa_read_status,
+    msa_sparse_attn_backward,
     msa_sparse_attn_decode,
     msa_sparse_attn_prefill,
     msa_status_string,

@@ -6,7 +6,7 @@ import os
 from functools import lru_cache
 
 MSA_BF16, MSA_FP32 = 0, 1
-MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE, MSA_OP_DECODE_STEP, MSA_OP_KL_AUX = 0, 1, 2, 3, 4
+MSA_OP_INDEX_SELECT, MSA_OP_PREFILL, MSA_OP_DECODE, MSA_OP_DECODE_STEP, MSA_OP_KL_AUX, MSA_OP_BACKWARD = 0, 1, 2, 3, 4, 5
 MSA_FORCE_LOCAL, MSA_FORCE_START = 1, 2
 STATUS_NAMES = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
                 4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_BOUNDS"}
@@ -21,6 +21,7 @@ SIGNATURES = {
     "msa_sparse_attn_decode": (_i32, [_vp] * 5 + [_i32] * 7 + [_f32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "msa_decode_step": (_i32, [_vp] * 9 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_kl_aux_forward": (_i32, [_vp] * 8 + [_i32] * 9 + [_f32, _i32, _vp, _vp, _sz, _vp]),
+    "msa_sparse_attn_backward": (_i32, [_vp] * 9 + [_i32] * 8 + [_f32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_read_status": (_i32, [_vp, _vp]),
     "msa_status_string": (ctypes.c_char_p, [_i32]),
     "msa_index_select_noalloc": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 8 + [_vp, _vp, _vp]),
@@ -250,3 +251,28 @@ def msa_kl_aux_forward(q, k, iq, ik, sel, lse, q_offset, kv_len, Bs, K, kl=None,
                                              _stream(stream, q.device))
     _check(code, "msa_kl_aux_forward")
     return kl
+
+
+def msa_sparse_attn_backward(q, k, v, out, dout, lse, sel, q_offset, kv_len, Bs, K, dq=None, dk=None, dv=None,
+                             scale=0.0, ws=None, stream=None):
+    """Main Branch backward (see include/msa.h): gradients of q [B,Nq,Hq,d],
+    k and v [B,Nk,Hkv,d] through msa_sparse_attn_prefill, given its output
+    ``out``, lse [B,Nq,Hq] and selection ``sel`` and the output gradient
+    ``dout``. Returns (dq, dk, dv) in q's dtype."""
+    import torch
+
+    _need_cuda(q, k, v, out, dout, lse, sel, q_offset, kv_len, dq, dk, dv)
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    dt = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if ws is None:
+        ws = workspace(msa_workspace_size(MSA_OP_BACKWARD, B, Nq, Nk, Hkv, Hq, d, 0, Bs, K, dt), q.device)
+    code = load_library().msa_sparse_attn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                                   _ptr(sel), _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, Hq, Hkv, d,
+                                                   Bs, K, float(scale), dt, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                                   ws.numel(), _stream(stream, q.device))
+    _check(code, "msa_sparse_attn_backward")
+    return dq, dk, dv

@@ -95,7 +95,7 @@ __global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t
 // counts: a tile, the first tile of a bin (its K/V load and the pipeline
 // bubble around it), a tile holding rows whose local block this is (masked).
 constexpr int kCostTile = 32, kCostBin = 17, kCostMasked = 8;
-constexpr int kMaxGrid = 1024;  // persistent grid: one CTA per SM
+constexpr int kMaxGrid = kKvoMaxGrid;  // persistent grid: one CTA per SM
 
 // single CTA of 1024 threads: tile offsets, entry offsets (= tile offset x
 // entries per tile: every tile owns a full slot range), tile total, and the
@@ -1075,7 +1075,12 @@ __global__ void __launch_bounds__(256) kl_combine_kernel(const int32_t* __restri
   kl[(int64_t(b) * Nq + i) * G + g] = l > 0.f ? A - Bv + m + logf(l) : 0.f;
 }
 
-int g_sms = 0;
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side of the inversion (shared with the backward's translation unit)
+// ---------------------------------------------------------------------------
+static int g_sms = 0;
 int sm_count() {
   if (g_sms == 0) {
     int dev = 0, n = 0;
@@ -1086,7 +1091,7 @@ int sm_count() {
   return g_sms;
 }
 
-inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+static inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int chunk_tokens(int Nq, int Hq, int K, int d) {
   static int env = -1;
@@ -1102,11 +1107,6 @@ int chunk_tokens(int Nq, int Hq, int K, int d) {
   const size_t nchunks = (size_t(Nq) + cap - 1) / cap;
   return int((size_t(Nq) + nchunks - 1) / nchunks);
 }
-
-struct KvoLayout {
-  size_t cnt, cursor, entry_off, tile_off, cost_off, total, cta_start, entries, rev, tiles, part_o, part_lse, end;
-  size_t max_tiles;
-};
 
 KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   const int nblk = (Nk + Bs - 1) / Bs;
@@ -1147,7 +1147,7 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   return L;
 }
 
-size_t attn_smem_bytes(int d, int Bs) {
+static size_t attn_smem_bytes(int d, int Bs) {
   const size_t kv = size_t(Bs) * d * 2 * 2;
   const size_t slot = size_t(kRows) * d * 2;
   const size_t meta = size_t(kRing + 1) * kRows * 4 + 16;
@@ -1190,8 +1190,6 @@ cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int3
                                                       reinterpret_cast<int*>(w + L.rev));
   return cudaGetLastError();
 }
-
-}  // namespace
 
 bool attn_kv_outer_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K) {
   if (dtype != MSA_BF16 || (d != 64 && d != 128)) return false;

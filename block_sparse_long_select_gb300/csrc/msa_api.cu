@@ -145,6 +145,11 @@ extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int H
       if (!kl_aux_supported(dtype, Hq, G, d, d == 128 ? 64 : 32, Bs, K)) return 0;
       return kl_aux_ws_bytes(Nq, Nk, Hq, G, d, Bs, K);
     }
+    case MSA_OP_BACKWARD: {
+      if (B < 1 || Nq < 1 || Nk < 1 || Nq > Nk || G < 1 || Hq < 1 || Hq % G != 0) return 0;
+      if (!attn_backward_supported(dtype, Hq, G, d, Bs, K)) return 0;
+      return attn_backward_ws_bytes(B, Nq, Nk, Hq, G, d, Bs, K);
+    }
     default:
       return 0;
   }
@@ -279,6 +284,24 @@ extern "C" msa_status_t msa_kl_aux_forward(const void* q, const void* k, const v
   if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
   return cuda_status(launch_kl_aux(q, k, iq, ik, sel, lse, q_offset, kv_len, B, Nq, Nk, Hq, Hkv, d, di, Bs, K, scale,
                                    kl, ws, stream));
+}
+
+extern "C" msa_status_t msa_sparse_attn_backward(const void* q, const void* k, const void* v, const void* out,
+                                                 const void* dout, const float* lse, const int32_t* sel,
+                                                 const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
+                                                 int Nk, int Hq, int Hkv, int d, int Bs, int K, float scale,
+                                                 int dtype, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                                                 cudaStream_t stream) {
+  if (!q || !k || !v || !out || !dout || !lse || !sel || !dq || !dk || !dv) return MSA_ERR_INVALID_ARG;
+  if (B < 1 || Nq < 1 || Nk < 1 || Nq > Nk || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || K < 1 || Bs < 1 ||
+      !dtype_ok(dtype))
+    return MSA_ERR_INVALID_ARG;
+  if (!attn_backward_supported(dtype, Hq, Hkv, d, Bs, K)) return MSA_ERR_UNSUPPORTED;
+  msa_status_t w = check_ws(ws, ws_bytes, attn_backward_ws_bytes(B, Nq, Nk, Hq, Hkv, d, Bs, K));
+  if (w != MSA_OK) return w;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf(float(d));
+  return cuda_status(launch_attn_backward(q, k, v, out, dout, lse, sel, q_offset, kv_len, B, Nq, Nk, Hq, Hkv, d, Bs,
+                                          K, scale, dq, dk, dv, ws, stream));
 }
 
 extern "C" msa_status_t msa_read_status(void* ws, cudaStream_t stream) {

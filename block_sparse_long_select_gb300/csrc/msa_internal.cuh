@@ -80,6 +80,27 @@ class ProfScope {
   cudaEvent_t start_ = nullptr;
 };
 
+// ---- KV-outer inversion (host side; kernels in attn_kv_outer_tc.cu) --------
+// Per query chunk of one sequence: the selection inverted into per-(group,
+// key block) bins of (query, slot) entries, padded to 128-row tiles (128 / hpg
+// entries per tile), the tile list, the reverse map (query, group, slot) ->
+// entry position, and a cost-balanced split of the tiles over a persistent
+// grid. Used by the prefill attention, the KL pass and the backward.
+constexpr int kKvoRows = 128;       // rows (entry x head) per tile
+constexpr int kKvoMaxGrid = 1024;   // cta_start capacity
+struct KvoLayout {
+  size_t cnt, cursor, entry_off, tile_off, cost_off, total, cta_start, entries, rev, tiles, part_o, part_lse, end;
+  size_t max_tiles;
+};
+// query tokens per chunk (equal chunks; the forward's bf16 partials stay under ~4 GiB)
+int chunk_tokens(int Nq, int Hq, int K, int d);
+KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk);
+int sm_count();
+// Fills the layout's inversion regions for queries [c0, c0 + cq) of sequence b.
+cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int32_t* kv_len, int b, int Nq, int Nk,
+                         int G, int K, int Bs, int per_tile, int c0, int cq, int grid, char* w, const KvoLayout& L,
+                         uint32_t* status, cudaStream_t stream);
+
 // ---- launchers (host) ------------------------------------------------------
 // Index Branch, CUDA-core table path: block maxima for every visible block.
 cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* ik, const int32_t* q_offset,
@@ -131,6 +152,14 @@ cudaError_t launch_kl_aux(const void* q, const void* k, const void* iq, const vo
                           const float* lse, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk,
                           int Hq, int Hkv, int d, int di, int Bs, int K, float scale, float* kl, void* ws,
                           cudaStream_t stream);
+// Main Branch backward (bf16): dq, dk, dv over the selected blocks on the
+// KV-outer bins, from the forward's out and lse.
+bool attn_backward_supported(int dtype, int Hq, int Hkv, int d, int Bs, int K);
+size_t attn_backward_ws_bytes(int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K);
+cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                 const float* lse, const int32_t* sel, const int32_t* q_offset,
+                                 const int32_t* kv_len, int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K,
+                                 float scale, void* dq, void* dk, void* dv, void* ws, cudaStream_t stream);
 cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, const void* v, const int32_t* sel,
                                     const int32_t* q_offset, const int32_t* kv_len, bool decode, int B, int Nq,
                                     int Nk, int Hq, int Hkv, int d, int Bs, int K, float scale, void* out, float* lse,

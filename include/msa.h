@@ -68,15 +68,17 @@ typedef enum {
   MSA_OP_PREFILL = 1,
   MSA_OP_DECODE = 2,
   MSA_OP_DECODE_STEP = 3,
-  MSA_OP_KL_AUX = 4
+  MSA_OP_KL_AUX = 4,
+  MSA_OP_BACKWARD = 5
 } msa_op_t;
 
 /* Bytes of scratch `ws` the entry point `op` needs for these sizes (the same
  * argument meanings as the entry points; unused ones may be 0: G and di for
  * the attention ops, Hq and d for MSA_OP_INDEX_SELECT; for MSA_OP_DECODE and
  * MSA_OP_DECODE_STEP, Nq is ignored and Nk is Lmax; MSA_OP_DECODE_STEP uses
- * every other argument, with G = Hkv; MSA_OP_KL_AUX uses all but di, with
- * G = Hkv). Returns 0 when the arguments are invalid or not supported. */
+ * every other argument, with G = Hkv; MSA_OP_KL_AUX and MSA_OP_BACKWARD use
+ * all but di, with G = Hkv). Returns 0 when the arguments are invalid or not
+ * supported. */
 size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K, int dtype);
 
 /* Index Branch: block selection for every (query row, group).
@@ -223,6 +225,33 @@ msa_status_t msa_kl_aux_forward(const void* q, const void* k, const void* iq, co
                                 const float* lse, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
                                 int Nk, int Hq, int Hkv, int d, int di, int Bs, int K, float scale, int dtype,
                                 float* kl, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Main Branch backward: the gradients of a loss with respect to q, k and v
+ * through the sparse attention of msa_sparse_attn_prefill, given the
+ * gradient dout of its output. The selection is held fixed (the Index Branch's
+ * choice carries no gradient).
+ * (hyper.ai summary, "方法": the Main Branch is standard scaled-dot-product
+ *  softmax attention over the selected blocks; "一句话总结"/"实验": the model
+ *  is trained through it. Per (row, head), over the attended keys j:
+ *  P_j = exp(scale q.k_j - lse), delta = dout . out, dS_j = P_j (dout.v_j - delta),
+ *  dq = scale sum_j dS_j k_j, dk_j = scale sum dS_j q, dv_j = sum P_j dout.)
+ *
+ *  q, out, dout [B, Nq, Hq, d]; k, v [B, Nk, Hkv, d] (dtype), as in the forward
+ *  lse       [B, Nq, Hq] fp32: the forward's log-sum-exp output
+ *  sel       [B, Nq, Hkv, K] int32: the forward's selection
+ *  q_offset, kv_len, scale: as for msa_sparse_attn_prefill
+ *  dq [B, Nq, Hq, d], dk, dv [B, Nk, Hkv, d] (dtype), out: fp32 accumulation,
+ *            rounded once; keys no row attends get 0
+ *  ws: msa_workspace_size(MSA_OP_BACKWARD, B, Nq, Nk, Hkv, Hq, d, 0, Bs, K, dtype)
+ *  Supported: BF16; d in {64, 128}; Bs in {32, 64, 128}; Hq / Hkv in
+ *  {1, 2, 4, 8}; 1 <= K <= 64. Other sizes return MSA_ERR_UNSUPPORTED.
+ *  Out-of-range sel entries set MSA_ERR_BOUNDS in the workspace status and
+ *  are skipped. */
+msa_status_t msa_sparse_attn_backward(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                                      const float* lse, const int32_t* sel, const int32_t* q_offset,
+                                      const int32_t* kv_len, int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs,
+                                      int K, float scale, int dtype, void* dq, void* dk, void* dv, void* ws,
+                                      size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the sticky device status of workspace `ws`
  * (MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_BOUNDS) and clears it. Returns
