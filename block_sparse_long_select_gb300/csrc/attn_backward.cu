@@ -67,6 +67,9 @@ __device__ __forceinline__ void cp16(void* dst, const void* src, bool in) {
                "r"(in ? 16u : 0u)
                : "memory");
 }
+__device__ __forceinline__ void cp16_addr(uint32_t dst, const void* src, bool in) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(in ? 16u : 0u) : "memory");
+}
 __device__ __forceinline__ void cp4(void* dst, const void* src, bool in) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(dst)), "l"(src), "r"(in ? 4u : 0u)
                : "memory");
@@ -121,7 +124,7 @@ struct BwdParams {
   const int* cta_start;                   // [grid + 1]
   const int32_t* q_offset;
   const int32_t* kv_len;
-  float* part_dq;  // [entry position * hpg + head][D] fp32, unscaled
+  float4* part_dq;  // per tile, chunk-major: float4 c of tile row r at (z * D/4 + c) * 128 + r; unscaled
   float* dk_acc;   // [Nk, G, D] fp32 of sequence b, unscaled
   float* dv_acc;   // [Nk, G, D] fp32 of sequence b
   int b, Nq, Nk, Hq, G, hpg, hpg_log2, nblk, c0;
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
   constexpr int DW = D / WS;             // phase 2: d columns per warp
   constexpr int NTD = DW / 8;            // phase 2: 8-column tiles per warp
   constexpr int QC = D < 64 ? D : 64;    // phase 3: dq columns per pass
-  static_assert(MT >= 1 && MT <= 8 && NTD % 2 == 0 && RW % 32 == 0, "tile split");
+  static_assert(MT >= 1 && MT <= 4 && NTD % 2 == 0 && RW % 32 == 0, "tile split (blocks of 32 or 64 keys)");
   extern __shared__ __align__(16) uint8_t bwd_smem[];
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(bwd_smem);
   __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(bwd_smem + SM::kKV);
@@ -332,12 +335,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = m0 + gq + 8 * hr;
-          const int e = r >> p.hpg_log2;
-          if (e < tl.z) {
-            float* dst = p.part_dq + (int64_t(tl.y + e) * p.hpg + (r & hmask)) * D + cq + 2 * tq;
+          if ((r >> p.hpg_log2) < tl.z) {
+            // columns cq + n * 8 + 2 tq (+1): half (tq & 1) of float4 chunk (cq + n * 8) / 4 + (tq >> 1)
+            float* dst = reinterpret_cast<float*>(p.part_dq + (int64_t(z) * (D / 4) + (cq >> 2) + (tq >> 1)) * kBwdRows +
+                                                  r) + 2 * (tq & 1);
 #pragma unroll
             for (int n = 0; n < QC / 8; ++n)
-              *reinterpret_cast<float2*>(dst + n * 8) = make_float2(acc[n][2 * hr], acc[n][2 * hr + 1]);
+              *reinterpret_cast<float2*>(dst + n * 2 * kBwdRows * 4) = make_float2(acc[n][2 * hr], acc[n][2 * hr + 1]);
           }
         }
       }
@@ -387,6 +391,420 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// tcgen05 tile kernel for blocks of 128 keys (keys along M = 128 TMEM lanes).
+// Per tile: S^T = K Q^T and dP^T = V dO^T into TMEM; the epilogue warpgroup
+// (one thread per key) forms P^T and dS^T, writes them back over S^T and dP^T
+// as bf16 pairs and dS^T to shared memory (MN-major, 128B-swizzled); then
+// dV += P^T dO and dK += dS^T Q take their A operand from TMEM (dO and Q are
+// read MN-major from the gathered tile) and dQ = dS K takes dS from shared
+// memory into the TMEM columns that P^T and dS^T left free. dV and dK stay
+// in TMEM for the run of the bin's tiles.
+// TMEM columns: S^T [0, 128) (P^T packed into [0, 64), dQ half 0 at [64, 128)),
+// dP^T [128, 256) (dS^T packed into [128, 192), dQ half 1 at [192, 256)),
+// dV [256, 256 + D), dK [256 + D, 256 + 2 D).
+// Warps 0-3 gather the tile's q and dout rows (cp.async, 128B-swizzled K-major,
+// two ring slots) and its row data (lse, delta, last visible key); warps 4-7
+// are the epilogue; warp 8 loads K and V by TMA; warp 9 owns TMEM and issues
+// the MMAs. Every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr int kTcThreads = 320;
+constexpr int kTcBs = 128;
+
+__host__ __device__ constexpr uint32_t bwd_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                      // D format: f32
+         | (1u << 7)                    // A format: bf16
+         | (1u << 10)                   // B format: bf16
+         | (uint32_t(a_mn) << 15)       // A major-ness (1 = MN-major)
+         | (uint32_t(b_mn) << 16)       // B major-ness (1 = MN-major)
+         | (uint32_t(N >> 3) << 17)     // N / 8
+         | (uint32_t(M >> 4) << 24);    // M / 16
+}
+
+template <int D>
+struct TcSmem {
+  static constexpr uint32_t kHalf = kTcBs * 128;           // one 64-wide half of a 128-row operand
+  static constexpr uint32_t kKV = D * kTcBs * 2;           // K or V block
+  static constexpr uint32_t kRowsT = kBwdRows * D * 2;     // q or dout tile
+  static constexpr uint32_t kSlot = 2 * kRowsT;            // q + dout
+  static constexpr uint32_t kDs = kBwdRows * kTcBs * 2;    // dS (MN-major)
+  static constexpr uint32_t oK = 0, oV = kKV, oRing = 2 * kKV, oDs = oRing + 2 * kSlot;
+  static constexpr uint32_t oRowF = oDs + kDs;             // [2][128] float2 (lse * log2e, delta)
+  static constexpr uint32_t oLim = oRowF + 2 * kBwdRows * 8;  // [2][128] int8: last visible key of the row - t*128
+  static constexpr uint32_t oBar = oLim + 2 * kBwdRows;     // 8-byte aligned
+  static constexpr uint32_t kBars = 13;
+  static constexpr uint32_t kTotal = oBar + kBars * 8 + 16;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdParams p,
+                  uint32_t* status) {
+  using SM = TcSmem<D>;
+  constexpr int NH = D / 64;
+  constexpr uint32_t kIdS = bwd_idesc(128, 128, false, false);  // S^T, dP^T: K and V x q / dout rows
+  constexpr uint32_t kIdKV = bwd_idesc(128, D, false, true);    // dV, dK: A from TMEM, B = dout / q MN-major
+  constexpr uint32_t kIdQ = bwd_idesc(128, 64, true, true);     // dQ half: A = dS MN-major, B = K half MN-major
+  constexpr uint32_t kColDv = 256, kColDk = 256 + D;
+  extern __shared__ __align__(1024) uint8_t tc_smem[];
+  if (tc::smem_u32(tc_smem) & 1023u) {  // the swizzled operands need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(status, MSA_ERR_CUDA);
+    return;
+  }
+  uint8_t* k_buf = tc_smem + SM::oK;
+  uint8_t* v_buf = tc_smem + SM::oV;
+  uint8_t* ring = tc_smem + SM::oRing;
+  uint8_t* ds_buf = tc_smem + SM::oDs;
+  float2* rowf = reinterpret_cast<float2*>(tc_smem + SM::oRowF);
+  int8_t* lim_s = reinterpret_cast<int8_t*>(tc_smem + SM::oLim);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tc_smem + SM::oBar);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;   // [2]
+  uint64_t* q_empty = bars + 4;  // [2]
+  uint64_t* s_full = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* dq_full = bars + 8;
+  uint64_t* tm_empty = bars + 9;
+  uint64_t* acc_full = bars + 10;
+  uint64_t* acc_empty = bars + 11;
+  uint64_t* done_bar = bars + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + SM::kBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kGather0 = 0, kEpi0 = 4, kTmaWarp = 8, kMmaWarp = 9;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(kv_full, 1);
+    tc::mbar_init(kv_empty, 1);
+    for (int r = 0; r < 2; ++r) {
+      tc::mbar_init(&q_full[r], 4);
+      tc::mbar_init(&q_empty[r], 1);
+    }
+    tc::mbar_init(s_full, 1);
+    tc::mbar_init(p_full, 4);
+    tc::mbar_init(dq_full, 1);
+    tc::mbar_init(tm_empty, 4);
+    tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_empty, 4);
+    tc::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tc::tma_prefetch(&tmK);
+    tc::tma_prefetch(&tmV);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const int z0 = p.cta_start[blockIdx.x], z1 = p.cta_start[blockIdx.x + 1];
+  const int n = z1 - z0;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(status, MSA_ERR_TIMEOUT);
+  };
+  const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
+
+  if (warp < kEpi0) {
+    // ------------------- q / dout row gather + row data -------------------
+    // Warp gw fills rows [32 gw, 32 gw + 32) of every tile; a warp
+    // instruction covers two whole 256-byte rows (16-byte chunks, swizzled).
+    const int gw = warp - kGather0;
+    constexpr int kCpr = D / 8, kRpi = 32 / kCpr;
+    const int chunk = lane % kCpr, sub = lane / kCpr;
+    const uint32_t hf = uint32_t(chunk) >> 3, cc = uint32_t(chunk) & 7u;
+    const int hmask = p.hpg - 1;
+    for (int z = 0; z < n; ++z) {
+      const int slot = z & 1;
+      if (!tc::mbar_wait(&q_empty[slot], ((z >> 1) & 1) ^ 1, abort_flag)) {
+        fail();
+        break;
+      }
+      const int4 tl = p.tiles[z0 + z];
+      const int g = tl.x / p.nblk, t = tl.x % p.nblk;
+      const int r = gw * 32 + lane;  // this lane's row (row data)
+      const int e = r >> p.hpg_log2;
+      const int ent = e < tl.z ? p.entries[tl.y + e] : -1;
+      const int il = ent >= 0 ? (ent >> 6) : 0;
+      const int64_t qrow = (int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + (r & hmask);
+      const uint32_t qs = tc::smem_u32(ring + slot * SM::kSlot), os = qs + SM::kRowsT;
+#pragma unroll 4
+      for (int it = 0; it < 32 / kRpi; ++it) {
+        const int rr = it * kRpi + sub;  // row within this warp's 32
+        const int row = gw * 32 + rr;
+        const int ent_r = __shfl_sync(0xffffffffu, ent, rr);
+        const int64_t qr = __shfl_sync(0xffffffffu, qrow, rr);
+        const uint32_t dst = hf * (kBwdRows * 128) + row * 128 + ((cc ^ uint32_t(row & 7)) << 4);
+        cp16_addr(qs + dst, p.q + qr * D + chunk * 8, ent_r >= 0);
+        cp16_addr(os + dst, p.dout + qr * D + chunk * 8, ent_r >= 0);
+      }
+      cp_commit();
+      float2 rf = make_float2(0.f, 0.f);
+      int lim = -1;
+      if (ent >= 0 && sv.ok) {
+        rf = make_float2(p.lse[qrow] * kLog2eBwd, p.delta[qrow]);
+        const int pos = sv.q0 + p.c0 + il;
+        lim = min(min(pos, sv.L - 1) - t * kTcBs, kTcBs - 1);
+      }
+      rowf[slot * kBwdRows + r] = rf;
+      lim_s[slot * kBwdRows + r] = int8_t(lim);
+      cp_wait_all();
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&q_full[slot]);
+    }
+    cp_wait_all();
+  } else if (warp < kTmaWarp) {
+    // ------------------------------ epilogue ------------------------------
+    const int quarter = warp & 3;
+    const int key = quarter * 32 + lane;  // TMEM lane: key of S^T, dP^T, dV, dK; row of dQ
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    int bin_first = 0, nbins = 0;
+    for (int z = 0; z < n; ++z) {
+      const int slot = z & 1;
+      const int4 tl = p.tiles[z0 + z];
+      const int bin = tl.x;
+      if (z > 0 && p.tiles[z0 + z - 1].x != bin) bin_first = z;
+      const bool last_of_bin = z + 1 == n || p.tiles[z0 + z + 1].x != bin;
+      // the slot's row data come from the gather warps: observe their phase
+      // directly (it has completed: the MMA read the slot before s_full)
+      if (!tc::mbar_wait(s_full, z & 1, abort_flag) || !tc::mbar_wait(&q_full[slot], (z >> 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const float2* rf = rowf + slot * kBwdRows;
+      const int8_t* lm = lim_s + slot * kBwdRows;
+      const uint32_t ds_row = tc::smem_u32(ds_buf) + uint32_t(key) * 128u;
+#pragma unroll 1
+      for (int c = 0; c < kBwdRows / 32; ++c) {  // 32 tile rows at a time
+        uint32_t sv32[32], dv32[32];
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + uint32_t(c * 32), sv32);
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + 128u + uint32_t(c * 32), dv32);
+        tc::tmem_ld_wait();
+        uint32_t pk[16], dk2[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int r = c * 32 + j + e2;
+            const float2 f = rf[r];
+            const bool vis = key <= int(lm[r]);
+            const float pr = vis ? bwd_ex2(fmaf(__uint_as_float(sv32[j + e2]), p.scale * kLog2eBwd, -f.x)) : 0.f;
+            pp[e2] = pr;
+            dd[e2] = pr * (__uint_as_float(dv32[j + e2]) - f.y);
+          }
+          pk[j >> 1] = bwd_pack(pp[0], pp[1]);
+          dk2[j >> 1] = bwd_pack(dd[0], dd[1]);
+        }
+        tc::tmem_st_32x32b_x16(tmem + lane_base + uint32_t(c * 16), pk);
+        tc::tmem_st_32x32b_x16(tmem + lane_base + 128u + uint32_t(c * 16), dk2);
+        // dS^T row of this key: rows [32 c, 32 c + 32) = four 16-byte chunks of half (32 c) / 64
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t half = uint32_t(c >> 1), ch = uint32_t((c & 1) * 4 + q4);
+          const uint32_t addr = ds_row + half * SM::kHalf + ((ch ^ uint32_t(key & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dk2[q4 * 4]), "r"(dk2[q4 * 4 + 1]),
+                       "r"(dk2[q4 * 4 + 2]), "r"(dk2[q4 * 4 + 3])
+                       : "memory");
+        }
+      }
+      tc::tmem_st_wait();
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(p_full);
+      // dQ rows of this tile (lane = row) out of TMEM, then the fp32 partial
+      if (!tc::mbar_wait(dq_full, z & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t qv[D];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + (h == 0 ? 64u : 192u), qv + h * 64);
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + (h == 0 ? 64u : 192u) + 32u, qv + h * 64 + 32);
+      }
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tm_empty);
+      if ((key >> p.hpg_log2) < tl.z) {
+        float4* dst = p.part_dq + int64_t(z0 + z) * (D / 4) * kBwdRows + key;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4)
+          dst[c4 * kBwdRows] = make_float4(__uint_as_float(qv[4 * c4]), __uint_as_float(qv[4 * c4 + 1]),
+                                           __uint_as_float(qv[4 * c4 + 2]), __uint_as_float(qv[4 * c4 + 3]));
+      }
+      if (last_of_bin) {
+        // dV and dK of the bin's run (lane = key) into the sequence's accumulators
+        if (!tc::mbar_wait(acc_full, nbins & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const int g = bin / p.nblk, t = bin % p.nblk;
+        const int j = t * kTcBs + key;
+        const bool whole = z0 + bin_first == p.tile_off[bin] && z0 + z + 1 == p.tile_off[bin + 1];
+        float* dkr = p.dk_acc + (int64_t(j) * p.G + g) * D;
+        float* dvr = p.dv_acc + (int64_t(j) * p.G + g) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t a[32], b2[32];
+          tc::tmem_ld_32x32b_x32(tmem + lane_base + kColDv + uint32_t(c * 32), a);
+          tc::tmem_ld_32x32b_x32(tmem + lane_base + kColDk + uint32_t(c * 32), b2);
+          tc::tmem_ld_wait();
+          if (j < p.Nk) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4) {
+              float4* pv = reinterpret_cast<float4*>(dvr + c * 32 + x);
+              float4* pk4 = reinterpret_cast<float4*>(dkr + c * 32 + x);
+              const float4 av = make_float4(__uint_as_float(a[x]), __uint_as_float(a[x + 1]), __uint_as_float(a[x + 2]),
+                                            __uint_as_float(a[x + 3]));
+              const float4 bk = make_float4(__uint_as_float(b2[x]), __uint_as_float(b2[x + 1]),
+                                            __uint_as_float(b2[x + 2]), __uint_as_float(b2[x + 3]));
+              if (whole) {
+                float4 ov = *pv, ok = *pk4;
+                ov.x += av.x; ov.y += av.y; ov.z += av.z; ov.w += av.w;
+                ok.x += bk.x; ok.y += bk.y; ok.z += bk.z; ok.w += bk.w;
+                *pv = ov;
+                *pk4 = ok;
+              } else {
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(pv), "f"(av.x), "f"(av.y),
+                             "f"(av.z), "f"(av.w)
+                             : "memory");
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(pk4), "f"(bk.x), "f"(bk.y),
+                             "f"(bk.z), "f"(bk.w)
+                             : "memory");
+              }
+            }
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(acc_empty);
+        ++nbins;
+      }
+    }
+  } else if (warp == kTmaWarp) {
+    // ------------------------------ K/V producer ------------------------------
+    if (lane == 0) {
+      int prev_bin = -1, loads = 0;
+      for (int z = 0; z < n; ++z) {
+        const int bin = p.tiles[z0 + z].x;
+        if (bin == prev_bin) continue;
+        prev_bin = bin;
+        if (!tc::mbar_wait(kv_empty, (loads & 1) ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        const int g = bin / p.nblk, t = bin % p.nblk;
+        tc::mbar_arrive_expect_tx(kv_full, 2 * SM::kKV);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          tc::tma_load_4d(k_buf + h * SM::kHalf, &tmK, kv_full, h * 64, g, t * kTcBs, p.b);
+          tc::tma_load_4d(v_buf + h * SM::kHalf, &tmV, kv_full, h * 64, g, t * kTcBs, p.b);
+        }
+        ++loads;
+      }
+      int zero = 0;
+      if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // drain the last copy
+    }
+  } else {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      int kv_uses = 0, nbins = 0;
+      const uint32_t ka = tc::smem_u32(k_buf), va = tc::smem_u32(v_buf), dsa = tc::smem_u32(ds_buf);
+      for (int z = 0; z < n; ++z) {
+        const int slot = z & 1;
+        const int bin = p.tiles[z0 + z].x;
+        const bool first = z == 0 || p.tiles[z0 + z - 1].x != bin;
+        const bool last = z + 1 == n || p.tiles[z0 + z + 1].x != bin;
+        if (first) {
+          if (!tc::mbar_wait(kv_full, kv_uses & 1, abort_flag)) {
+            fail();
+            break;
+          }
+          ++kv_uses;
+        }
+        if (!tc::mbar_wait(&q_full[slot], (z >> 1) & 1, abort_flag) ||
+            (z > 0 && !tc::mbar_wait(tm_empty, (z - 1) & 1, abort_flag))) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t qa = tc::smem_u32(ring + slot * SM::kSlot), oa = qa + SM::kRowsT;
+        // S^T = K Q^T, dP^T = V dO^T (both operands K-major along d)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t kd = tc::smem_desc(ka + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
+          const uint64_t qd = tc::smem_desc(qa + (kk >> 2) * (kBwdRows * 128) + off, 16, 1024, 2);
+          tc::mma_f16_ss(tmem, kd, qd, kIdS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t vd = tc::smem_desc(va + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
+          const uint64_t od = tc::smem_desc(oa + (kk >> 2) * (kBwdRows * 128) + off, 16, 1024, 2);
+          tc::mma_f16_ss(tmem + 128u, vd, od, kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(s_full);
+        if (!tc::mbar_wait(p_full, z & 1, abort_flag) ||
+            (first && nbins > 0 && !tc::mbar_wait(acc_empty, (nbins - 1) & 1, abort_flag))) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        // dV += P^T dO, dK += dS^T Q: A from TMEM (16 rows = 8 packed columns per step), B MN-major
+#pragma unroll
+        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
+          const uint64_t od = tc::smem_desc(oa + kk * 16 * 128, kBwdRows * 128, 1024, 2);
+          tc::mma_f16_ts(tmem + kColDv, tmem + uint32_t(kk) * 8u, od, kIdKV, (first && kk == 0) ? 0u : 1u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
+          const uint64_t qd = tc::smem_desc(qa + kk * 16 * 128, kBwdRows * 128, 1024, 2);
+          tc::mma_f16_ts(tmem + kColDk, tmem + 128u + uint32_t(kk) * 8u, qd, kIdKV, (first && kk == 0) ? 0u : 1u);
+        }
+        // dQ = dS K, one 64-column half of d at a time (A = dS MN-major over the tile rows)
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < kTcBs / 16; ++kk) {
+            const uint64_t sd = tc::smem_desc(dsa + kk * 16 * 128, SM::kHalf, 1024, 2);
+            const uint64_t kd = tc::smem_desc(ka + h * SM::kHalf + kk * 16 * 128, SM::kHalf, 1024, 2);
+            tc::mma_f16_ss(tmem + (h == 0 ? 64u : 192u), sd, kd, kIdQ, kk > 0 ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(dq_full);
+        tc::mma_commit(&q_empty[slot]);
+        if (last) {
+          tc::mma_commit(acc_full);
+          tc::mma_commit(kv_empty);
+          ++nbins;
+        }
+      }
+      int zero = 0;
+      tc::mma_commit(done_bar);
+      tc::mbar_wait(done_bar, 0, &zero);
+    }
+  }
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dq: one warp per (query, group) sums its valid slots' partial rows in slot
 // order; NU float4 of the group's hpg x D row block per lane
@@ -396,12 +814,21 @@ __global__ void __launch_bounds__(256) bwd_dq_combine_kernel(
     const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
     const float4* __restrict__ part_dq, const int* __restrict__ rev, int b, int Nq, int Nk, int Hq, int G, int K,
     int Bs, int nblk, int D, int c0, int cq, float scale, __nv_bfloat16* __restrict__ dq) {
+  // partial rows of an entry at position e: tile e / per_tile, rows (e % per_tile) * hpg + head,
+  // float4 chunk c of row r of tile z at (z * D/4 + c) * 128 + r; lane vector vi = chunk * hpg + head
   constexpr int kWarps = 256 / 32;
   constexpr int kBatch = NU <= 2 ? 8 : (NU == 4 ? 4 : 2);  // slots whose loads are in flight together
   __shared__ int slot_e[kWarps][kMaxK];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int hpg = Hq / G;
   const int nvec = hpg * D / 4;  // float4 per slot
+  const int per_tile = kBwdRows / hpg;
+  int voff[NU];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const int vi = lane + 32 * u;
+    voff[u] = vi < nvec ? (vi / hpg) * kBwdRows + vi % hpg : 0;
+  }
   const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
   const int64_t nitems = int64_t(cq) * G;
   for (int64_t item = int64_t(blockIdx.x) * kWarps + wl; item < nitems; item += int64_t(gridDim.x) * kWarps) {
@@ -426,11 +853,12 @@ __global__ void __launch_bounds__(256) bwd_dq_combine_kernel(
 #pragma unroll
       for (int jj = 0; jj < kBatch; ++jj) {
         const bool in = j0 + jj < nv;
-        const int64_t base = in ? int64_t(slot_e[wl][j0 + jj]) * nvec : 0;
+        const int e = in ? slot_e[wl][j0 + jj] : 0;
+        const int64_t base = int64_t(e / per_tile) * (D / 4) * kBwdRows + (e % per_tile) * hpg;
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
           const int vi = lane + 32 * u;
-          x[jj][u] = (in && vi < nvec) ? part_dq[base + vi] : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[jj][u] = (in && vi < nvec) ? part_dq[base + voff[u]] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
 #pragma unroll
@@ -451,7 +879,7 @@ __global__ void __launch_bounds__(256) bwd_dq_combine_kernel(
         uint2 o;
         o.x = bwd_pack(acc[u].x * scale, acc[u].y * scale);
         o.y = bwd_pack(acc[u].z * scale, acc[u].w * scale);
-        *reinterpret_cast<uint2*>(drow + vi * 4) = o;
+        *reinterpret_cast<uint2*>(drow + (vi % hpg) * D + (vi / hpg) * 4) = o;
       }
     }
     __syncwarp();
@@ -545,7 +973,7 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
   prm.cta_start = reinterpret_cast<const int*>(w + L.cta_start);
   prm.q_offset = q_offset;
   prm.kv_len = kv_len;
-  prm.part_dq = reinterpret_cast<float*>(w + L.part_o);
+  prm.part_dq = reinterpret_cast<float4*>(w + L.part_o);
   prm.dk_acc = reinterpret_cast<float*>(w + W.dk_acc);
   prm.dv_acc = reinterpret_cast<float*>(w + W.dv_acc);
   prm.Nq = Nq;
@@ -558,6 +986,15 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
   prm.scale = scale;
   const int* rev = reinterpret_cast<const int*>(w + L.rev);
   const int64_t kv_elems = int64_t(Nk) * G * d;
+  CUtensorMap tmK, tmV;  // blocks of 128 keys, 64-column halves, 128B swizzle (the tcgen05 path)
+  if (Bs == kTcBs) {
+    const uint64_t dims[4] = {uint64_t(d), uint64_t(Hkv), uint64_t(Nk), uint64_t(B)};
+    const uint64_t strides[3] = {uint64_t(d) * 2, uint64_t(Hkv) * d * 2, uint64_t(Nk) * Hkv * d * 2};
+    const uint32_t box[4] = {64, 1, uint32_t(kTcBs), 1};
+    if (!make_tmap_bf16(&tmK, k, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_bf16(&tmV, v, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
 
   for (int b = 0; b < B; ++b) {
     if ((e = cudaMemsetAsync(w + W.dk_acc, 0, W.end - W.dk_acc, stream)) != cudaSuccess) return e;
@@ -568,7 +1005,23 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
         return e;
       prm.b = b;
       prm.c0 = c0;
-      {
+      if (Bs == kTcBs) {
+        ProfScope pf("bwd_tile_tc", stream);
+        if (d == 128) {
+          auto kern = bwd_tc_kernel<128>;
+          if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        int(TcSmem<128>::kTotal))) != cudaSuccess)
+            return e;
+          kern<<<grid, kTcThreads, TcSmem<128>::kTotal, stream>>>(tmK, tmV, prm, status);
+        } else {
+          auto kern = bwd_tc_kernel<64>;
+          if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        int(TcSmem<64>::kTotal))) != cudaSuccess)
+            return e;
+          kern<<<grid, kTcThreads, TcSmem<64>::kTotal, stream>>>(tmK, tmV, prm, status);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      } else {
         ProfScope pf("bwd_tile", stream);
 #define MSA_BWD(D_, BS_)                                                                              \
   do {                                                                                                \
@@ -579,17 +1032,13 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
       return e;                                                                                       \
     kern<<<grid, kBwdThreads, smem, stream>>>(prm);                                                   \
   } while (0)
-        if (d == 128) {
-          if (Bs == 128)
-            MSA_BWD(128, 128);
-          else if (Bs == 64)
+        if (d == 128) {  // blocks of 32 or 64 keys (128 takes the tcgen05 kernel)
+          if (Bs == 64)
             MSA_BWD(128, 64);
           else
             MSA_BWD(128, 32);
         } else {
-          if (Bs == 128)
-            MSA_BWD(64, 128);
-          else if (Bs == 64)
+          if (Bs == 64)
             MSA_BWD(64, 64);
           else
             MSA_BWD(64, 32);
