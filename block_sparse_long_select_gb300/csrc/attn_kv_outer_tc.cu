@@ -1392,7 +1392,29 @@ cudaError_t launch_kl_aux(const void* q, const void* k, const void* iq, const vo
         return e;
       prm.b = b;
       prm.c0 = c0;
-      {
+      if (kl_tc_supported(d, di, Bs, hpg)) {
+        ProfScope pf("kl_tile_tc", stream);
+        KlTcArgs ka;
+        ka.q = prm.q;
+        ka.iq = prm.iq;
+        ka.lse = lse;
+        ka.entries = prm.entries;
+        ka.tiles = prm.tiles;
+        ka.cta_start = prm.cta_start;
+        ka.q_offset = q_offset;
+        ka.kv_len = kv_len;
+        ka.part = prm.part;
+        ka.status = status;
+        ka.b = b;
+        ka.Nq = Nq;
+        ka.Nk = Nk;
+        ka.Hq = Hq;
+        ka.G = G;
+        ka.nblk = nblk;
+        ka.c0 = c0;
+        ka.scale = scale;
+        if ((e = launch_kl_tile_tc(ka, k, ik, B, Nk, Hkv, hpg, grid, stream)) != cudaSuccess) return e;
+      } else {
         ProfScope pf("kl_tile", stream);
 #define MSA_KL(D_, DI_, BS_, HPG_)                                                                            \
   do {                                                                                                        \

@@ -1,0 +1,476 @@
+// KL auxiliary forward, tile pass on tcgen05 (bf16, d = 128, di = 64, blocks of
+// 128 keys). (quant_prune_distill post 751, "Метод": the index branch is
+// trained with the KL divergence to the head-averaged main-branch
+// distribution; hyper.ai summary, "方法": the two are aligned over the selected
+// tokens.) For each (group, key block) tile of the KV-outer inversion
+// (128 / hpg entries x hpg heads), per entry e over the block's visible keys j:
+//   pbar_j = (1 / hpg) sum_h exp(scale q_h.k_j - lse_h)     (main branch, head mean)
+//   s_j    = iq_e . ik_j                                     (index score)
+//   partial = (sum_j pbar_j log pbar_j, sum_j pbar_j s_j, max_j s_j, sum_j exp(s_j - max))
+// which the combine merges over the entry's selected blocks into
+//   KL = sum pbar log pbar - sum pbar s + logsumexp s.
+//
+// Keys lie along M (the 128 TMEM lanes): S^T = K q^T (128 x 128 rows) and
+// I^T = IK iq^T (128 x entries) land in TMEM, so the epilogue thread of key j
+// holds all heads of every entry in neighbouring columns (the head mean is
+// in-thread). The sums over keys are a reduce-scatter across the warp's lanes
+// (lane l ends with entry l of a group of 32) and a four-warp combine in
+// shared memory. Two TMEM sets let the MMA of tile z + 1 run under the
+// epilogue of tile z.
+// Warps 0-3 epilogue, 4-5 gather q rows, index-query rows and row data
+// (cp.async, 128B-swizzled K-major, two ring slots), 6 TMA of K and IK per
+// bin, 7 TMEM owner and MMA issuer. Every wait is bounded.
+#include <cmath>
+
+#include "msa_internal.cuh"
+#include "tc_utils.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kKtThreads = 256;
+constexpr int kKtD = 128, kKtDI = 64, kKtBs = 128, kKtRows = kKvoRows;
+constexpr float kKtLog2e = 1.4426950408889634f;
+constexpr float kKtLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float kt_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float kt_lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void kt_cp16(uint32_t dst, const void* src, bool in) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(in ? 16u : 0u) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit_kt() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_kt() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__host__ __device__ constexpr uint32_t kt_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// reduce-scatter of 32 per-lane values: afterwards v[0] of lane l is the sum
+// over the warp's lanes of the original v[l]
+__device__ __forceinline__ void kt_rs_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+// (max, exp-sum) pairs merged the same way (natural-log units; -inf = empty)
+__device__ __forceinline__ void kt_lse_merge(float& m, float& l, float m2, float l2) {
+  const float M = fmaxf(m, m2);
+  const float a = m == -INFINITY ? 0.f : l * kt_ex2((m - M) * kKtLog2e);
+  const float b = m2 == -INFINITY ? 0.f : l2 * kt_ex2((m2 - M) * kKtLog2e);
+  m = M;
+  l = a + b;
+}
+__device__ __forceinline__ void kt_rs_lse(float (&m)[32], float (&l)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float sm = up ? m[i] : m[i + o], sl = up ? l[i] : l[i + o];
+      float km = up ? m[i + o] : m[i], kl = up ? l[i + o] : l[i];
+      const float rm = __shfl_xor_sync(0xffffffffu, sm, o), rl = __shfl_xor_sync(0xffffffffu, sl, o);
+      kt_lse_merge(km, kl, rm, rl);
+      m[i] = km;
+      l[i] = kl;
+    }
+  }
+}
+
+template <int HPG>
+struct KtSmem {
+  static constexpr int E = kKtRows / HPG;                  // entries per tile
+  static constexpr uint32_t kHalf = kKtRows * 128;         // one 64-wide half of a 128-row operand
+  static constexpr uint32_t kK = kKtBs * kKtD * 2;         // K block (two halves)
+  static constexpr uint32_t kIK = kKtBs * kKtDI * 2;       // IK block (one half)
+  static constexpr uint32_t kQ = kKtRows * kKtD * 2;       // gathered q rows
+  static constexpr uint32_t kIQ = E * kKtDI * 2;           // gathered index-query rows (E x 128 B)
+  static constexpr uint32_t kSlot = kQ + kIQ;              // multiple of 1024
+  static constexpr uint32_t oK = 0, oIK = kK, oRing = kK + kIK;
+  static constexpr uint32_t oLse = oRing + 2 * kSlot;      // [2][128] lse * log2(e)
+  static constexpr uint32_t oLim = oLse + 2 * kKtRows * 4;  // [2][E] last visible key - t * 128 (-1: none)
+  static constexpr uint32_t oRed = oLim + 2 * E * 4;        // [2][4][32] float4 per-warp sums
+  static constexpr uint32_t oBar = oRed + 2 * 4 * 32 * 16;
+  static constexpr uint32_t kBars = 16;
+  static constexpr uint32_t kTotal = oBar + kBars * 8 + 16;
+};
+
+template <int HPG>
+__global__ void __launch_bounds__(kKtThreads, 1)
+    kl_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmIK,
+                 const KlTcArgs p) {
+  using SM = KtSmem<HPG>;
+  constexpr int E = SM::E;
+  constexpr int EG = E < 32 ? E : 32;  // entries per reduce-scatter group
+  constexpr int NG = E / EG;
+  constexpr int RG = EG * HPG;         // tile rows (S^T columns) per group
+  static_assert(RG % 32 == 0 && E % 16 == 0, "entry groups");
+  constexpr uint32_t kIdS = kt_idesc(128, 128), kIdI = kt_idesc(128, E);
+  extern __shared__ __align__(1024) uint8_t kt_smem[];
+  if (tc::smem_u32(kt_smem) & 1023u) {  // the swizzled operands need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, MSA_ERR_CUDA);
+    return;
+  }
+  uint8_t* k_buf = kt_smem + SM::oK;
+  uint8_t* ik_buf = kt_smem + SM::oIK;
+  uint8_t* ring = kt_smem + SM::oRing;
+  float* lse_s = reinterpret_cast<float*>(kt_smem + SM::oLse);
+  int* lim_s = reinterpret_cast<int*>(kt_smem + SM::oLim);
+  float4* red = reinterpret_cast<float4*>(kt_smem + SM::oRed);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kt_smem + SM::oBar);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;    // [2] ring slots
+  uint64_t* q_empty = bars + 4;   // [2]
+  uint64_t* s_full = bars + 6;    // [2] TMEM sets
+  uint64_t* tm_empty = bars + 8;  // [2]
+  uint64_t* done_bar = bars + 10;
+  uint64_t* red_full = bars + 11;   // [2] the four warps' sums of a group are in red[buf]
+  uint64_t* red_empty = bars + 13;  // [2] warp 0 has merged red[buf]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + SM::kBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kGather0 = 4, kTmaWarp = 6, kMmaWarp = 7;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(kv_full, 1);
+    tc::mbar_init(kv_empty, 1);
+    for (int r = 0; r < 2; ++r) {
+      tc::mbar_init(&q_full[r], 2);
+      tc::mbar_init(&q_empty[r], 1);
+      tc::mbar_init(&s_full[r], 1);
+      tc::mbar_init(&tm_empty[r], 4);
+      tc::mbar_init(&red_full[r], 4);
+      tc::mbar_init(&red_empty[r], 1);
+    }
+    tc::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tc::tma_prefetch(&tmK);
+    tc::tma_prefetch(&tmIK);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const int z0 = p.cta_start[blockIdx.x], z1 = p.cta_start[blockIdx.x + 1];
+  const int n = z1 - z0;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, MSA_ERR_TIMEOUT);
+  };
+  const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
+
+  if (warp < kGather0) {
+    // ------------------------------ epilogue ------------------------------
+    const int quarter = warp & 3;
+    const int key = quarter * 32 + lane;  // TMEM lane = key of the block
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const float sl2 = p.scale * kKtLog2e;
+    int gc = 0;  // groups merged so far (red buffer gc & 1)
+    bool alive = true;
+    for (int z = 0; z < n && alive; ++z) {
+      const int set = z & 1;
+      if (!tc::mbar_wait(&s_full[set], (z >> 1) & 1, abort_flag) ||
+          !tc::mbar_wait(&q_full[set], (z >> 1) & 1, abort_flag)) {  // row data of the slot (already complete)
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const int4 tl = p.tiles[z0 + z];
+      const float* lse2 = lse_s + set * kKtRows;
+      const int* lim = lim_s + set * E;
+      const uint32_t s_col = tmem + lane_base + uint32_t(set) * 256u;
+#pragma unroll 1
+      for (int eg = 0; eg < NG; ++eg) {
+        float va[32], vb[32], vm[32], vl[32];
+        // index scores of the group's entries
+        uint32_t sc[32];
+        if (EG == 32)
+          tc::tmem_ld_32x32b_x32(s_col + 128u + uint32_t(eg * EG), sc);
+        else
+          tc::tmem_ld_32x32b_x16(s_col + 128u + uint32_t(eg * EG), sc);
+#pragma unroll
+        for (int x = EG; x < 32; ++x) sc[x] = 0u;
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          va[x] = vb[x] = 0.f;
+          vm[x] = -INFINITY;
+          vl[x] = 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < RG / 32; ++c) {
+          uint32_t sv32[32];
+          tc::tmem_ld_32x32b_x32(s_col + uint32_t(eg * RG + c * 32), sv32);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int ee = 0; ee < 32 / HPG; ++ee) {
+            const int el = c * (32 / HPG) + ee;  // entry within the group
+            const int e = eg * EG + el;
+            const bool vis = key <= lim[e];
+            float ps = 0.f;
+#pragma unroll
+            for (int h = 0; h < HPG; ++h) {
+              const int col = ee * HPG + h;
+              ps += kt_ex2(fmaf(__uint_as_float(sv32[col]), sl2, -lse2[e * HPG + h]));
+            }
+            const float pb = vis ? ps * (1.f / HPG) : 0.f;
+            const float s = __uint_as_float(sc[el]);
+            va[el] = pb > 0.f ? pb * (kt_lg2(pb) * kKtLn2) : 0.f;
+            vb[el] = pb * s;
+            vm[el] = vis ? s : -INFINITY;
+            vl[el] = vis ? 1.f : 0.f;
+          }
+        }
+        if (eg + 1 == NG) {  // every TMEM column of this tile is in registers
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tm_empty[set]);
+        }
+        kt_rs_sum(va, lane);
+        kt_rs_sum(vb, lane);
+        kt_rs_lse(vm, vl, lane);
+        // the four warps' sums meet in red[buf]; warp 0 merges them (bounded waits, no bar.sync)
+        const int buf = gc & 1;
+        if (!tc::mbar_wait(&red_empty[buf], ((gc >> 1) & 1) ^ 1, abort_flag)) {
+          fail();
+          alive = false;
+          break;
+        }
+        red[(buf * 4 + quarter) * 32 + lane] = make_float4(va[0], vb[0], vm[0], vl[0]);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&red_full[buf]);
+        if (quarter == 0) {
+          if (!tc::mbar_wait(&red_full[buf], (gc >> 1) & 1, abort_flag)) {
+            fail();
+            alive = false;
+            break;
+          }
+          if (lane < EG) {
+            float4 a = red[(buf * 4) * 32 + lane];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) {
+              const float4 o = red[(buf * 4 + w) * 32 + lane];
+              a.x += o.x;
+              a.y += o.y;
+              kt_lse_merge(a.z, a.w, o.z, o.w);
+            }
+            const int e = eg * EG + lane;
+            if (e < tl.z) p.part[int64_t(z0 + z) * E + e] = a;
+          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&red_empty[buf]);
+        }
+        ++gc;
+      }
+    }
+  } else if (warp < kTmaWarp) {
+    // -------------- q rows, index-query rows and row data (gather) --------------
+    const int gw = warp - kGather0;  // rows [64 gw, 64 gw + 64), entries [E/2 gw, E/2 (gw + 1))
+    constexpr int kCpr = kKtD / 8, kRpi = 32 / kCpr;         // q: 16 chunks per row, 2 rows per instruction
+    constexpr int kCprI = kKtDI / 8, kRpiI = 32 / kCprI;    // iq: 8 chunks per row, 4 rows per instruction
+    const int chunk = lane % kCpr, sub = lane / kCpr;
+    const int chunkI = lane % kCprI, subI = lane / kCprI;
+    for (int z = 0; z < n; ++z) {
+      const int slot = z & 1;
+      // the slot is free once the MMA has read its rows and the epilogue of
+      // tile z - 2 (same slot and TMEM set) has read its row data
+      if (!tc::mbar_wait(&q_empty[slot], ((z >> 1) & 1) ^ 1, abort_flag) ||
+          !tc::mbar_wait(&tm_empty[slot], ((z >> 1) & 1) ^ 1, abort_flag)) {
+        fail();
+        break;
+      }
+      const int4 tl = p.tiles[z0 + z];
+      const int g = tl.x / p.nblk, t = tl.x % p.nblk;
+      const uint32_t qs = tc::smem_u32(ring + slot * SM::kSlot), iqs = qs + SM::kQ;
+      // this lane's two rows of the warp's 64 (row data) and their entries
+      int ent2[2];
+      int64_t qrow2[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int r = gw * 64 + x * 32 + lane;
+        const int e = r / HPG;
+        ent2[x] = e < tl.z ? p.entries[tl.y + e] : -1;
+        const int il = ent2[x] >= 0 ? (ent2[x] >> 6) : 0;
+        qrow2[x] = (int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * HPG + (r % HPG);
+      }
+#pragma unroll 4
+      for (int it = 0; it < 64 / kRpi; ++it) {
+        const int rr = it * kRpi + sub;  // row within this warp's 64
+        const int row = gw * 64 + rr;
+        const int src_lane = rr & 31, x = rr >> 5;
+        const int ent_r = __shfl_sync(0xffffffffu, x ? ent2[1] : ent2[0], src_lane);
+        const int64_t qr = __shfl_sync(0xffffffffu, x ? qrow2[1] : qrow2[0], src_lane);
+        const uint32_t hf = uint32_t(chunk) >> 3, cc = uint32_t(chunk) & 7u;
+        kt_cp16(qs + hf * SM::kHalf + row * 128 + ((cc ^ uint32_t(row & 7)) << 4), p.q + qr * kKtD + chunk * 8,
+                ent_r >= 0);
+      }
+      // index-query rows of entries [E/2 gw, E/2 gw + E/2)
+      for (int it = 0; it < (E / 2) / kRpiI; ++it) {
+        const int e = gw * (E / 2) + it * kRpiI + subI;
+        const int ent = e < tl.z ? p.entries[tl.y + e] : -1;
+        const int il = ent >= 0 ? (ent >> 6) : 0;
+        const __nv_bfloat16* src = p.iq + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.G + g) * kKtDI + chunkI * 8;
+        kt_cp16(iqs + e * 128 + ((uint32_t(chunkI) ^ uint32_t(e & 7)) << 4), src, ent >= 0);
+      }
+      cp_async_commit_kt();
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int r = gw * 64 + x * 32 + lane;
+        lse_s[slot * kKtRows + r] = ent2[x] >= 0 ? p.lse[qrow2[x]] * kKtLog2e : 0.f;
+      }
+      for (int e = gw * (E / 2) + lane; e < (gw + 1) * (E / 2); e += 32) {
+        const int ent = e < tl.z ? p.entries[tl.y + e] : -1;
+        int lm = -1;
+        if (ent >= 0 && sv.ok) {
+          const int pos = sv.q0 + p.c0 + (ent >> 6);
+          lm = min(min(pos, sv.L - 1) - t * kKtBs, kKtBs - 1);
+        }
+        lim_s[slot * E + e] = lm;
+      }
+      cp_async_wait_all_kt();
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&q_full[slot]);
+    }
+    cp_async_wait_all_kt();
+  } else if (warp == kTmaWarp) {
+    // ------------------------------ K / IK producer ------------------------------
+    if (lane == 0) {
+      int prev_bin = -1, loads = 0;
+      for (int z = 0; z < n; ++z) {
+        const int bin = p.tiles[z0 + z].x;
+        if (bin == prev_bin) continue;
+        prev_bin = bin;
+        if (!tc::mbar_wait(kv_empty, (loads & 1) ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        const int g = bin / p.nblk, t = bin % p.nblk;
+        tc::mbar_arrive_expect_tx(kv_full, SM::kK + SM::kIK);
+#pragma unroll
+        for (int h = 0; h < kKtD / 64; ++h)
+          tc::tma_load_4d(k_buf + h * SM::kHalf, &tmK, kv_full, h * 64, g, t * kKtBs, p.b);
+        tc::tma_load_3d(ik_buf, &tmIK, kv_full, 0, t * kKtBs, p.b);
+        ++loads;
+      }
+      int zero = 0;
+      if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // drain the last copy
+    }
+  } else {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      int kv_uses = 0;
+      const uint32_t ka = tc::smem_u32(k_buf), ika = tc::smem_u32(ik_buf);
+      for (int z = 0; z < n; ++z) {
+        const int set = z & 1, slot = z & 1;
+        const int bin = p.tiles[z0 + z].x;
+        const bool first = z == 0 || p.tiles[z0 + z - 1].x != bin;
+        const bool last = z + 1 == n || p.tiles[z0 + z + 1].x != bin;
+        if (first) {
+          if (!tc::mbar_wait(kv_full, kv_uses & 1, abort_flag)) {
+            fail();
+            break;
+          }
+          ++kv_uses;
+        }
+        if (!tc::mbar_wait(&q_full[slot], (z >> 1) & 1, abort_flag) ||
+            !tc::mbar_wait(&tm_empty[set], ((z >> 1) & 1) ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t qa = tc::smem_u32(ring + slot * SM::kSlot), iqa = qa + SM::kQ;
+        const uint32_t d_s = tmem + uint32_t(set) * 256u;
+#pragma unroll
+        for (int kk = 0; kk < kKtD / 16; ++kk) {  // S^T = K q^T
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t kd = tc::smem_desc(ka + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
+          const uint64_t qd = tc::smem_desc(qa + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
+          tc::mma_f16_ss(d_s, kd, qd, kIdS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kKtDI / 16; ++kk) {  // I^T = IK iq^T
+          const uint32_t off = kk * 32;
+          const uint64_t kd = tc::smem_desc(ika + off, 16, 1024, 2);
+          const uint64_t qd = tc::smem_desc(iqa + off, 16, 1024, 2);
+          tc::mma_f16_ss(d_s + 128u, kd, qd, kIdI, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&s_full[set]);
+        tc::mma_commit(&q_empty[slot]);
+        if (last) tc::mma_commit(kv_empty);
+      }
+      int zero = 0;
+      tc::mma_commit(done_bar);
+      tc::mbar_wait(done_bar, 0, &zero);
+    }
+  }
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool kl_tc_supported(int d, int di, int Bs, int hpg) {
+  return d == kKtD && di == kKtDI && Bs == kKtBs && (hpg == 2 || hpg == 4 || hpg == 8);
+}
+
+cudaError_t launch_kl_tile_tc(const KlTcArgs& a, const void* k, const void* ik, int B, int Nk, int Hkv, int hpg,
+                              int grid, cudaStream_t stream) {
+  CUtensorMap tmK, tmIK;
+  {
+    const uint64_t dims[4] = {uint64_t(kKtD), uint64_t(Hkv), uint64_t(Nk), uint64_t(B)};
+    const uint64_t strides[3] = {uint64_t(kKtD) * 2, uint64_t(Hkv) * kKtD * 2, uint64_t(Nk) * Hkv * kKtD * 2};
+    const uint32_t box[4] = {64, 1, uint32_t(kKtBs), 1};
+    if (!make_tmap_bf16(&tmK, k, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {uint64_t(kKtDI), uint64_t(Nk), uint64_t(B)};
+    const uint64_t strides[2] = {uint64_t(kKtDI) * 2, uint64_t(Nk) * kKtDI * 2};
+    const uint32_t box[3] = {64, uint32_t(kKtBs), 1};
+    if (!make_tmap_bf16(&tmIK, ik, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
+  cudaError_t e;
+#define MSA_KT(H_)                                                                                               \
+  do {                                                                                                           \
+    auto kern = kl_tc_kernel<H_>;                                                                                \
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(KtSmem<H_>::kTotal))) != \
+        cudaSuccess)                                                                                             \
+      return e;                                                                                                  \
+    kern<<<grid, kKtThreads, KtSmem<H_>::kTotal, stream>>>(tmK, tmIK, a);                                        \
+  } while (0)
+  if (hpg == 2)
+    MSA_KT(2);
+  else if (hpg == 4)
+    MSA_KT(4);
+  else
+    MSA_KT(8);
+#undef MSA_KT
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -160,6 +160,24 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
                                  const float* lse, const int32_t* sel, const int32_t* q_offset,
                                  const int32_t* kv_len, int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs, int K,
                                  float scale, void* dq, void* dk, void* dv, void* ws, cudaStream_t stream);
+// KL auxiliary tile pass on tcgen05 (d 128, di 64, blocks of 128 keys): one
+// launch over a chunk's tiles, writing the per-entry partials the combine reads.
+struct KlTcArgs {
+  const __nv_bfloat16 *q, *iq;  // q [B, Nq, Hq, 128]; iq [B, Nq, G, 64]
+  const float* lse;             // [B, Nq, Hq]
+  const int* entries;
+  const int4* tiles;
+  const int* cta_start;
+  const int32_t* q_offset;
+  const int32_t* kv_len;
+  float4* part;  // [entry position] (sum p log p, sum p s, index max, index exp-sum)
+  uint32_t* status;
+  int b, Nq, Nk, Hq, G, nblk, c0;
+  float scale;
+};
+bool kl_tc_supported(int d, int di, int Bs, int hpg);
+cudaError_t launch_kl_tile_tc(const KlTcArgs& a, const void* k, const void* ik, int B, int Nk, int Hkv, int hpg,
+                              int grid, cudaStream_t stream);
 cudaError_t launch_attn_query_outer(int dtype, const void* q, const void* k, const void* v, const int32_t* sel,
                                     const int32_t* q_offset, const int32_t* kv_len, bool decode, int B, int Nq,
                                     int Nk, int Hq, int Hkv, int d, int Bs, int K, float scale, void* out, float* lse,

@@ -42,6 +42,9 @@ CASES = {
     "bs32_hpg4_hot": synth.scaled(BASE, B=1, Nq=900, Nk=900, Bs=32, K=12, hot="first4"),
     "d64_di32_hpg2": synth.scaled(BASE, B=2, Nq=700, Nk=700, Hq=8, Hkv=4, d=64, di=32, Bs=64, K=5),
     "d64_di32_hpg8": synth.scaled(BASE, B=1, Nq=800, Nk=800, Hq=16, Hkv=2, d=64, di=32, Bs=32, K=9),
+    # blocks of 128 keys with d 128 / di 64 take the tcgen05 tile pass: head ratios 2 and 8, hot blocks
+    "bs128_hpg2": synth.scaled(BASE, B=1, Nq=1200, Nk=1200, Hq=16, Hkv=8, Bs=128, K=5),
+    "bs128_hpg8_hot": synth.scaled(BASE, B=1, Nq=1300, Nk=1300, Hq=32, Hkv=4, Bs=128, K=6, hot="first4"),
 }
 
 
