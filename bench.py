@@ -42,6 +42,7 @@ KERNEL_SOURCES = {  # kernel name -> source file (for the ncu traffic freshness 
     "attn_combine": "attn_kv_outer_tc.cu", "decode_index": "decode.cu", "decode_topk": "decode.cu",
     "decode_attn": "decode.cu", "decode_combine": "decode.cu", "kl_tile": "attn_kv_outer_tc.cu",
     "kl_combine": "attn_kv_outer_tc.cu", "bwd_tile": "attn_backward.cu", "bwd_dq_combine": "attn_backward.cu",
+    "kl_tile_tc": "kl_tc.cu", "bwd_tile_tc": "attn_backward.cu",
 }
 
 
@@ -265,9 +266,9 @@ def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="pre
         bound, unit, per_step = "tensor", "TFLOP/s", work["index_flops"]
     elif kernel in ("attn_kv_outer_tc", "attn_query_outer"):
         bound, unit, per_step = "tensor", "TFLOP/s", work["attn_flops"]
-    elif kernel == "kl_tile":
+    elif kernel in ("kl_tile", "kl_tile_tc"):
         bound, unit, per_step = "tensor", "TFLOP/s", work["kl_flops"]
-    elif kernel == "bwd_tile":
+    elif kernel in ("bwd_tile", "bwd_tile_tc"):
         bound, unit, per_step = "tensor", "TFLOP/s", work["bwd_flops"]
     else:
         return None
@@ -393,8 +394,8 @@ def run_msa(args, dist):
                   "ms_per_step": round(float(np.mean(kms)), 4), "steps": args.steps,
                   "what": "msa_kl_aux_forward: KL(head-averaged main distribution || index softmax) over the "
                           "selected keys of every (query, group), from the forward's lse",
-                  "roofline": roofline_for("kl_tile", kprof, kwork, peaks, peak_src, w.name, args.steps)
-                  if "kl_tile" in kprof else None,
+                  "roofline": next((roofline_for(k_, kprof, kwork, peaks, peak_src, w.name, args.steps)
+                                    for k_ in ("kl_tile_tc", "kl_tile") if k_ in kprof), None),
                   "kernels": {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4)}
                               for k, v in kprof.items()},
                   "gpu_launches": sum(v[0] for v in kprof.values()), "clocks": kclocks,
@@ -424,8 +425,8 @@ def run_msa(args, dist):
                    "ms_per_step": round(float(np.mean(bms)), 4), "steps": args.steps,
                    "what": "msa_sparse_attn_backward: dq, dk, dv over the selected blocks from the forward's "
                            "selection, output and lse, synthetic output gradient",
-                   "roofline": roofline_for("bwd_tile", bprof, bwork, peaks, peak_src, w.name, args.steps)
-                   if "bwd_tile" in bprof else None,
+                   "roofline": next((roofline_for(k_, bprof, bwork, peaks, peak_src, w.name, args.steps)
+                                     for k_ in ("bwd_tile_tc", "bwd_tile") if k_ in bprof), None),
                    "kernels": {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4)}
                                for k, v in bprof.items()},
                    "gpu_launches": sum(v[0] for v in bprof.values()), "clocks": bclocks,

@@ -17,7 +17,7 @@
 //      are formed in registers and written to shared memory as bf16;
 //   2. dV += P^T dO and dK += dS^T Q, accumulated in registers over the run's
 //      tiles of one bin (each warp a 16-key strip x a slice of d);
-//   3. dQ = dS K for the tile's rows, stored as an fp32 partial per (entry,
+//   3. dQ = dS K for the tile's rows, stored as a bf16 partial per (entry,
 //      head) row, while the next tile's rows are already being gathered.
 // When a bin's run ends, dK and dV are added into per-sequence fp32
 // accumulators: plainly when this CTA holds every tile of the bin, atomically
@@ -124,7 +124,7 @@ struct BwdParams {
   const int* cta_start;                   // [grid + 1]
   const int32_t* q_offset;
   const int32_t* kv_len;
-  float4* part_dq;  // per tile, chunk-major: float4 c of tile row r at (z * D/4 + c) * 128 + r; unscaled
+  uint4* part_dq;  // per tile, chunk-major bf16: 8-column chunk c of tile row r at (z * D/8 + c) * 128 + r; unscaled
   float* dk_acc;   // [Nk, G, D] fp32 of sequence b, unscaled
   float* dv_acc;   // [Nk, G, D] fp32 of sequence b
   int b, Nq, Nk, Hq, G, hpg, hpg_log2, nblk, c0;
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
     __syncthreads();  // Q and dO are free: gather the next tile's rows under phase 3
     const bool more = z + 1 < z1;
     if (more) load_rows(z + 1, nb ^ 1);
-    // ---- 3. dQ rows [16 warp, +16) = dS K, keys reduced; fp32 partial rows
+    // ---- 3. dQ rows [16 warp, +16) = dS K, keys reduced; bf16 partial rows
     {
       const int m0 = warp * 16;
       const int arow = (lane & 7) + 8 * (lane >> 4), acol = m0 + 8 * ((lane >> 3) & 1);
@@ -336,12 +336,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
         for (int hr = 0; hr < 2; ++hr) {
           const int r = m0 + gq + 8 * hr;
           if ((r >> p.hpg_log2) < tl.z) {
-            // columns cq + n * 8 + 2 tq (+1): half (tq & 1) of float4 chunk (cq + n * 8) / 4 + (tq >> 1)
-            float* dst = reinterpret_cast<float*>(p.part_dq + (int64_t(z) * (D / 4) + (cq >> 2) + (tq >> 1)) * kBwdRows +
-                                                  r) + 2 * (tq & 1);
+            // columns cq + n * 8 + 2 tq (+1): bf16 pair tq of 8-column chunk (cq + n * 8) / 8
+            uint32_t* dst = reinterpret_cast<uint32_t*>(p.part_dq + (int64_t(z) * (D / 8) + (cq >> 3)) * kBwdRows + r) + tq;
 #pragma unroll
-            for (int n = 0; n < QC / 8; ++n)
-              *reinterpret_cast<float2*>(dst + n * 2 * kBwdRows * 4) = make_float2(acc[n][2 * hr], acc[n][2 * hr + 1]);
+            for (int n = 0; n < QC / 8; ++n) dst[n * kBwdRows * 4] = bwd_pack(acc[n][2 * hr], acc[n][2 * hr + 1]);
           }
         }
       }
@@ -399,7 +397,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
 // as bf16 pairs and dS^T to shared memory (MN-major, 128B-swizzled); then
 // dV += P^T dO and dK += dS^T Q take their A operand from TMEM (dO and Q are
 // read MN-major from the gathered tile) and dQ = dS K takes dS from shared
-// memory into the TMEM columns that P^T and dS^T left free. dV and dK stay
+// memory into the TMEM columns that P^T and dS^T left free (bf16 partials,
+// summed in fp32 by the combine). dV and dK stay
 // in TMEM for the run of the bin's tiles.
 // TMEM columns: S^T [0, 128) (P^T packed into [0, 64), dQ half 0 at [64, 128)),
 // dP^T [128, 256) (dS^T packed into [128, 192), dQ half 1 at [192, 256)),
@@ -430,7 +429,7 @@ struct TcSmem {
   static constexpr uint32_t kSlot = 2 * kRowsT;            // q + dout
   static constexpr uint32_t kDs = kBwdRows * kTcBs * 2;    // dS (MN-major)
   static constexpr uint32_t oK = 0, oV = kKV, oRing = 2 * kKV, oDs = oRing + 2 * kSlot;
-  static constexpr uint32_t oRowF = oDs + kDs;             // [2][128] float2 (lse * log2e, delta)
+  static constexpr uint32_t oRowF = oDs + kDs;             // [2][2][128] float: lse (natural log), delta
   static constexpr uint32_t oLim = oRowF + 2 * kBwdRows * 8;  // [2][128] int8: last visible key of the row - t*128
   static constexpr uint32_t oBar = oLim + 2 * kBwdRows;     // 8-byte aligned
   static constexpr uint32_t kBars = 13;
@@ -456,7 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* v_buf = tc_smem + SM::oV;
   uint8_t* ring = tc_smem + SM::oRing;
   uint8_t* ds_buf = tc_smem + SM::oDs;
-  float2* rowf = reinterpret_cast<float2*>(tc_smem + SM::oRowF);
+  float* rowf = reinterpret_cast<float*>(tc_smem + SM::oRowF);  // slot s: lse at [2 s][r], delta at [2 s + 1][r]
   int8_t* lim_s = reinterpret_cast<int8_t*>(tc_smem + SM::oLim);
   uint64_t* bars = reinterpret_cast<uint64_t*>(tc_smem + SM::oBar);
   uint64_t* kv_full = bars + 0;
@@ -520,17 +519,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int chunk = lane % kCpr, sub = lane / kCpr;
     const uint32_t hf = uint32_t(chunk) >> 3, cc = uint32_t(chunk) & 7u;
     const int hmask = p.hpg - 1;
+    const int r = gw * 32 + lane;  // this lane's row (row data)
+    const int e = r >> p.hpg_log2;
+    // tile records and entries are fetched one tile ahead, off the critical path
+    int4 tl_n = make_int4(0, 0, 0, 0);
+    int ent_n = -1;
+    auto fetch = [&](int z) {
+      tl_n = p.tiles[z0 + z];
+      ent_n = e < tl_n.z ? p.entries[tl_n.y + e] : -1;
+    };
+    if (n > 0) fetch(0);
     for (int z = 0; z < n; ++z) {
       const int slot = z & 1;
+      const int4 tl = tl_n;
+      const int ent = ent_n;
+      if (z + 1 < n) fetch(z + 1);
       if (!tc::mbar_wait(&q_empty[slot], ((z >> 1) & 1) ^ 1, abort_flag)) {
         fail();
         break;
       }
-      const int4 tl = p.tiles[z0 + z];
       const int g = tl.x / p.nblk, t = tl.x % p.nblk;
-      const int r = gw * 32 + lane;  // this lane's row (row data)
-      const int e = r >> p.hpg_log2;
-      const int ent = e < tl.z ? p.entries[tl.y + e] : -1;
       const int il = ent >= 0 ? (ent >> 6) : 0;
       const int64_t qrow = (int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + (r & hmask);
       const uint32_t qs = tc::smem_u32(ring + slot * SM::kSlot), os = qs + SM::kRowsT;
@@ -544,15 +552,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cp16_addr(qs + dst, p.q + qr * D + chunk * 8, ent_r >= 0);
         cp16_addr(os + dst, p.dout + qr * D + chunk * 8, ent_r >= 0);
       }
+      // the row's lse and delta by 4-byte copies (zero for padding rows)
+      cp4(rowf + (2 * slot) * kBwdRows + r, p.lse + qrow, ent >= 0);
+      cp4(rowf + (2 * slot + 1) * kBwdRows + r, p.delta + qrow, ent >= 0);
       cp_commit();
-      float2 rf = make_float2(0.f, 0.f);
       int lim = -1;
-      if (ent >= 0 && sv.ok) {
-        rf = make_float2(p.lse[qrow] * kLog2eBwd, p.delta[qrow]);
-        const int pos = sv.q0 + p.c0 + il;
-        lim = min(min(pos, sv.L - 1) - t * kTcBs, kTcBs - 1);
-      }
-      rowf[slot * kBwdRows + r] = rf;
+      if (ent >= 0 && sv.ok) lim = min(min(sv.q0 + p.c0 + il, sv.L - 1) - t * kTcBs, kTcBs - 1);
       lim_s[slot * kBwdRows + r] = int8_t(lim);
       cp_wait_all();
       tc::fence_proxy_async_smem();
@@ -565,13 +570,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int quarter = warp & 3;
     const int key = quarter * 32 + lane;  // TMEM lane: key of S^T, dP^T, dV, dK; row of dQ
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    int bin_first = 0, nbins = 0;
+    int bin_first = 0, nbins = 0, prev_bin = -1;
+    int4 tl_n = n > 0 ? p.tiles[z0] : make_int4(0, 0, 0, 0);
     for (int z = 0; z < n; ++z) {
       const int slot = z & 1;
-      const int4 tl = p.tiles[z0 + z];
+      const int4 tl = tl_n;
+      if (z + 1 < n) tl_n = p.tiles[z0 + z + 1];  // in flight while this tile is processed
       const int bin = tl.x;
-      if (z > 0 && p.tiles[z0 + z - 1].x != bin) bin_first = z;
-      const bool last_of_bin = z + 1 == n || p.tiles[z0 + z + 1].x != bin;
+      if (z > 0 && prev_bin != bin) bin_first = z;
+      prev_bin = bin;
       // the slot's row data come from the gather warps: observe their phase
       // directly (it has completed: the MMA read the slot before s_full)
       if (!tc::mbar_wait(s_full, z & 1, abort_flag) || !tc::mbar_wait(&q_full[slot], (z >> 1) & 1, abort_flag)) {
@@ -579,9 +586,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const float2* rf = rowf + slot * kBwdRows;
+      const float* lse_r = rowf + (2 * slot) * kBwdRows;
+      const float* dlt_r = rowf + (2 * slot + 1) * kBwdRows;
       const int8_t* lm = lim_s + slot * kBwdRows;
       const uint32_t ds_row = tc::smem_u32(ds_buf) + uint32_t(key) * 128u;
+      const float sl2 = p.scale * kLog2eBwd;
 #pragma unroll 1
       for (int c = 0; c < kBwdRows / 32; ++c) {  // 32 tile rows at a time
         uint32_t sv32[32], dv32[32];
@@ -595,11 +604,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int r = c * 32 + j + e2;
-            const float2 f = rf[r];
             const bool vis = key <= int(lm[r]);
-            const float pr = vis ? bwd_ex2(fmaf(__uint_as_float(sv32[j + e2]), p.scale * kLog2eBwd, -f.x)) : 0.f;
+            const float pr =
+                vis ? bwd_ex2(fmaf(__uint_as_float(sv32[j + e2]), sl2, -lse_r[r] * kLog2eBwd)) : 0.f;
             pp[e2] = pr;
-            dd[e2] = pr * (__uint_as_float(dv32[j + e2]) - f.y);
+            dd[e2] = pr * (__uint_as_float(dv32[j + e2]) - dlt_r[r]);
           }
           pk[j >> 1] = bwd_pack(pp[0], pp[1]);
           dk2[j >> 1] = bwd_pack(dd[0], dd[1]);
@@ -621,7 +630,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(p_full);
-      // dQ rows of this tile (lane = row) out of TMEM, then the fp32 partial
+      // dQ rows of this tile (lane = row) out of TMEM, then the bf16 partial
       if (!tc::mbar_wait(dq_full, z & 1, abort_flag)) {
         fail();
         break;
@@ -637,14 +646,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tm_empty);
-      if ((key >> p.hpg_log2) < tl.z) {
-        float4* dst = p.part_dq + int64_t(z0 + z) * (D / 4) * kBwdRows + key;
+      if ((key >> p.hpg_log2) < tl.z) {  // bf16 partial, chunk-major: a warp store covers 512 contiguous bytes
+        uint4* dst = p.part_dq + int64_t(z0 + z) * (D / 8) * kBwdRows + key;
 #pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4)
-          dst[c4 * kBwdRows] = make_float4(__uint_as_float(qv[4 * c4]), __uint_as_float(qv[4 * c4 + 1]),
-                                           __uint_as_float(qv[4 * c4 + 2]), __uint_as_float(qv[4 * c4 + 3]));
+        for (int c8 = 0; c8 < D / 8; ++c8)
+          dst[c8 * kBwdRows] =
+              make_uint4(bwd_pack(__uint_as_float(qv[8 * c8]), __uint_as_float(qv[8 * c8 + 1])),
+                         bwd_pack(__uint_as_float(qv[8 * c8 + 2]), __uint_as_float(qv[8 * c8 + 3])),
+                         bwd_pack(__uint_as_float(qv[8 * c8 + 4]), __uint_as_float(qv[8 * c8 + 5])),
+                         bwd_pack(__uint_as_float(qv[8 * c8 + 6]), __uint_as_float(qv[8 * c8 + 7])));
       }
-      if (last_of_bin) {
+      if (z + 1 == n || tl_n.x != bin) {  // last tile of the bin's run
         // dV and dK of the bin's run (lane = key) into the sequence's accumulators
         if (!tc::mbar_wait(acc_full, nbins & 1, abort_flag)) {
           fail();
@@ -721,13 +733,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0) {
-      int kv_uses = 0, nbins = 0;
+      int kv_uses = 0, nbins = 0, prev_bin = -1;
       const uint32_t ka = tc::smem_u32(k_buf), va = tc::smem_u32(v_buf), dsa = tc::smem_u32(ds_buf);
+      int bin_n = n > 0 ? p.tiles[z0].x : -1;
       for (int z = 0; z < n; ++z) {
         const int slot = z & 1;
-        const int bin = p.tiles[z0 + z].x;
-        const bool first = z == 0 || p.tiles[z0 + z - 1].x != bin;
-        const bool last = z + 1 == n || p.tiles[z0 + z + 1].x != bin;
+        const int bin = bin_n;
+        bin_n = z + 1 < n ? p.tiles[z0 + z + 1].x : -1;  // one tile ahead
+        const bool first = bin != prev_bin;
+        prev_bin = bin;
         if (first) {
           if (!tc::mbar_wait(kv_full, kv_uses & 1, abort_flag)) {
             fail();
@@ -787,7 +801,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::mma_commit(dq_full);
         tc::mma_commit(&q_empty[slot]);
-        if (last) {
+        if (bin_n != bin) {  // last tile of the bin's run
           tc::mma_commit(acc_full);
           tc::mma_commit(kv_empty);
           ++nbins;
@@ -807,21 +821,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---------------------------------------------------------------------------
 // dq: one warp per (query, group) sums its valid slots' partial rows in slot
-// order; NU float4 of the group's hpg x D row block per lane
+// order; NU 8-column bf16 chunks of the group's hpg x D row block per lane
 // ---------------------------------------------------------------------------
 template <int NU>
 __global__ void __launch_bounds__(256) bwd_dq_combine_kernel(
     const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
-    const float4* __restrict__ part_dq, const int* __restrict__ rev, int b, int Nq, int Nk, int Hq, int G, int K,
+    const uint4* __restrict__ part_dq, const int* __restrict__ rev, int b, int Nq, int Nk, int Hq, int G, int K,
     int Bs, int nblk, int D, int c0, int cq, float scale, __nv_bfloat16* __restrict__ dq) {
   // partial rows of an entry at position e: tile e / per_tile, rows (e % per_tile) * hpg + head,
-  // float4 chunk c of row r of tile z at (z * D/4 + c) * 128 + r; lane vector vi = chunk * hpg + head
+  // 8-column chunk c of row r of tile z at (z * D/8 + c) * 128 + r; lane vector vi = chunk * hpg + head
   constexpr int kWarps = 256 / 32;
-  constexpr int kBatch = NU <= 2 ? 8 : (NU == 4 ? 4 : 2);  // slots whose loads are in flight together
+  constexpr int kBatch = NU <= 2 ? 8 : 4;  // slots whose loads are in flight together
   __shared__ int slot_e[kWarps][kMaxK];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int hpg = Hq / G;
-  const int nvec = hpg * D / 4;  // float4 per slot
+  const int nvec = hpg * D / 8;  // 16-byte chunks per slot
   const int per_tile = kBwdRows / hpg;
   int voff[NU];
 #pragma unroll
@@ -845,42 +859,44 @@ __global__ void __launch_bounds__(256) bwd_dq_combine_kernel(
       nv += __popc(bal);
     }
     __syncwarp();
-    float4 acc[NU];
+    float acc[NU][8];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < NU; ++u)
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[u][x] = 0.f;
     for (int j0 = 0; j0 < nv; j0 += kBatch) {
-      float4 x[kBatch][NU];
+      uint4 x[kBatch][NU];
 #pragma unroll
       for (int jj = 0; jj < kBatch; ++jj) {
         const bool in = j0 + jj < nv;
         const int e = in ? slot_e[wl][j0 + jj] : 0;
-        const int64_t base = int64_t(e / per_tile) * (D / 4) * kBwdRows + (e % per_tile) * hpg;
+        const int64_t base = int64_t(e / per_tile) * (D / 8) * kBwdRows + (e % per_tile) * hpg;
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
           const int vi = lane + 32 * u;
-          x[jj][u] = (in && vi < nvec) ? part_dq[base + voff[u]] : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[jj][u] = (in && vi < nvec) ? part_dq[base + voff[u]] : make_uint4(0u, 0u, 0u, 0u);
         }
       }
 #pragma unroll
       for (int jj = 0; jj < kBatch; ++jj)
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
-          acc[u].x += x[jj][u].x;
-          acc[u].y += x[jj][u].y;
-          acc[u].z += x[jj][u].z;
-          acc[u].w += x[jj][u].w;
+          const uint32_t w4[4] = {x[jj][u].x, x[jj][u].y, x[jj][u].z, x[jj][u].w};
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) {  // bf16 -> fp32 is a 16-bit shift (low half = even column)
+            acc[u][2 * q2] += __uint_as_float(w4[q2] << 16);
+            acc[u][2 * q2 + 1] += __uint_as_float(w4[q2] & 0xffff0000u);
+          }
         }
     }
     __nv_bfloat16* drow = dq + ((int64_t(b) * Nq + i) * Hq + int64_t(g) * hpg) * D;
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
       const int vi = lane + 32 * u;
-      if (vi < nvec) {
-        uint2 o;
-        o.x = bwd_pack(acc[u].x * scale, acc[u].y * scale);
-        o.y = bwd_pack(acc[u].z * scale, acc[u].w * scale);
-        *reinterpret_cast<uint2*>(drow + (vi % hpg) * D + (vi / hpg) * 4) = o;
-      }
+      if (vi < nvec)
+        *reinterpret_cast<uint4*>(drow + (vi % hpg) * D + (vi / hpg) * 8) =
+            make_uint4(bwd_pack(acc[u][0] * scale, acc[u][1] * scale), bwd_pack(acc[u][2] * scale, acc[u][3] * scale),
+                       bwd_pack(acc[u][4] * scale, acc[u][5] * scale), bwd_pack(acc[u][6] * scale, acc[u][7] * scale));
     }
     __syncwarp();
   }
@@ -900,13 +916,13 @@ __global__ void __launch_bounds__(256) bwd_kv_store_kernel(const float4* __restr
 inline size_t a256b(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct BwdLayout {
-  KvoLayout L;  // inversion; its partial area (sized for 2d bf16 = d fp32 per row) holds the dq partials
+  KvoLayout L;  // inversion; its partial area (bf16 rows of d) holds the dq partials
   size_t delta, dk_acc, dv_acc, end;
 };
 
 BwdLayout bwd_layout(int B, int Nq, int Nk, int Hq, int G, int d, int Bs, int K) {
   BwdLayout W;
-  W.L = kvo_layout(Nq, Hq, G, 2 * d, Bs, K, Nk);
+  W.L = kvo_layout(Nq, Hq, G, d, Bs, K, Nk);
   size_t o = W.L.end;
   W.delta = o;
   o += a256b(size_t(B) * Nq * Hq * 4);
@@ -945,7 +961,7 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
   uint32_t* status = &static_cast<WsHeader*>(ws)->status;
   float* delta = reinterpret_cast<float*>(w + W.delta);
   const int grid = sm_count() < kKvoMaxGrid ? sm_count() : kKvoMaxGrid;
-  const int cq_max = chunk_tokens(Nq, Hq, K, 2 * d);
+  const int cq_max = chunk_tokens(Nq, Hq, K, d);
   cudaError_t e;
   {
     ProfScope pf("bwd_delta", stream);
@@ -973,7 +989,7 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
   prm.cta_start = reinterpret_cast<const int*>(w + L.cta_start);
   prm.q_offset = q_offset;
   prm.kv_len = kv_len;
-  prm.part_dq = reinterpret_cast<float4*>(w + L.part_o);
+  prm.part_dq = reinterpret_cast<uint4*>(w + L.part_o);
   prm.dk_acc = reinterpret_cast<float*>(w + W.dk_acc);
   prm.dv_acc = reinterpret_cast<float*>(w + W.dv_acc);
   prm.Nq = Nq;
@@ -1049,10 +1065,10 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
       {
         ProfScope pf("bwd_dq_combine", stream);
         const int64_t items = int64_t(cq) * G;
-        const int nvec = hpg * d / 4;
+        const int nvec = hpg * d / 8;
         const int64_t need = (items + 7) / 8;
         const int cgrid = int(need < int64_t(grid) * 8 ? need : int64_t(grid) * 8);
-        const float4* pd = reinterpret_cast<const float4*>(w + L.part_o);
+        const uint4* pd = reinterpret_cast<const uint4*>(w + L.part_o);
         __nv_bfloat16* dq16 = static_cast<__nv_bfloat16*>(dq);
 #define MSA_DQC(NU_)                                                                                             \
   bwd_dq_combine_kernel<NU_><<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, pd, rev, b, Nq, Nk, Hq, G, K, Bs, \
@@ -1061,10 +1077,8 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
           MSA_DQC(1);
         else if (nvec <= 64)
           MSA_DQC(2);
-        else if (nvec <= 128)
-          MSA_DQC(4);
         else
-          MSA_DQC(8);
+          MSA_DQC(4);
 #undef MSA_DQC
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }

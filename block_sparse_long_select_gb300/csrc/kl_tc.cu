@@ -15,11 +15,12 @@
 // holds all heads of every entry in neighbouring columns (the head mean is
 // in-thread). The sums over keys are a reduce-scatter across the warp's lanes
 // (lane l ends with entry l of a group of 32) and a four-warp combine in
-// shared memory. Two TMEM sets let the MMA of tile z + 1 run under the
-// epilogue of tile z.
-// Warps 0-3 epilogue, 4-5 gather q rows, index-query rows and row data
-// (cp.async, 128B-swizzled K-major, two ring slots), 6 TMA of K and IK per
-// bin, 7 TMEM owner and MMA issuer. Every wait is bounded.
+// shared memory. Two epilogue warpgroups take alternate tiles, each with its
+// own TMEM set, so the MMA of one tile runs under the epilogue of the other.
+// Warps 0-7 epilogue (warpgroup z & 1 takes tile z), 8-9 gather q rows,
+// index-query rows and row data (cp.async, 128B-swizzled K-major, two ring
+// slots; tile records and entries fetched a tile ahead), 10 TMA of K and IK
+// per bin, 11 TMEM owner and MMA issuer. Every wait is bounded.
 #include <cmath>
 
 #include "msa_internal.cuh"
@@ -28,7 +29,8 @@
 namespace msa {
 namespace {
 
-constexpr int kKtThreads = 256;
+constexpr int kKtThreads = 384;
+constexpr int kKtEG = 16;  // entries per reduce-scatter group
 constexpr int kKtD = 128, kKtDI = 64, kKtBs = 128, kKtRows = kKvoRows;
 constexpr float kKtLog2e = 1.4426950408889634f;
 constexpr float kKtLn2 = 0.6931471805599453f;
@@ -54,11 +56,12 @@ __host__ __device__ constexpr uint32_t kt_idesc(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-// reduce-scatter of 32 per-lane values: afterwards v[0] of lane l is the sum
-// over the warp's lanes of the original v[l]
-__device__ __forceinline__ void kt_rs_sum(float (&v)[32], int lane) {
+// reduce-scatter of 16 per-lane values: four levels within each 16-lane half,
+// then one exchange across the halves; afterwards v[0] of lane l is the sum
+// over all 32 lanes of the original v[l & 15]
+__device__ __forceinline__ void kt_rs_sum(float (&v)[kKtEG], int lane) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = kKtEG / 2; o >= 1; o >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < o; ++i) {
@@ -67,6 +70,7 @@ __device__ __forceinline__ void kt_rs_sum(float (&v)[32], int lane) {
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 // (max, exp-sum) pairs merged the same way (natural-log units; -inf = empty)
 __device__ __forceinline__ void kt_lse_merge(float& m, float& l, float m2, float l2) {
@@ -76,9 +80,9 @@ __device__ __forceinline__ void kt_lse_merge(float& m, float& l, float m2, float
   m = M;
   l = a + b;
 }
-__device__ __forceinline__ void kt_rs_lse(float (&m)[32], float (&l)[32], int lane) {
+__device__ __forceinline__ void kt_rs_lse(float (&m)[kKtEG], float (&l)[kKtEG], int lane) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = kKtEG / 2; o >= 1; o >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < o; ++i) {
@@ -90,6 +94,8 @@ __device__ __forceinline__ void kt_rs_lse(float (&m)[32], float (&l)[32], int la
       l[i] = kl;
     }
   }
+  const float rm = __shfl_xor_sync(0xffffffffu, m[0], 16), rl = __shfl_xor_sync(0xffffffffu, l[0], 16);
+  kt_lse_merge(m[0], l[0], rm, rl);
 }
 
 template <int HPG>
@@ -102,11 +108,11 @@ struct KtSmem {
   static constexpr uint32_t kIQ = E * kKtDI * 2;           // gathered index-query rows (E x 128 B)
   static constexpr uint32_t kSlot = kQ + kIQ;              // multiple of 1024
   static constexpr uint32_t oK = 0, oIK = kK, oRing = kK + kIK;
-  static constexpr uint32_t oLse = oRing + 2 * kSlot;      // [2][128] lse * log2(e)
+  static constexpr uint32_t oLse = oRing + 2 * kSlot;      // [2][128] lse (natural log)
   static constexpr uint32_t oLim = oLse + 2 * kKtRows * 4;  // [2][E] last visible key - t * 128 (-1: none)
-  static constexpr uint32_t oRed = oLim + 2 * E * 4;        // [2][4][32] float4 per-warp sums
-  static constexpr uint32_t oBar = oRed + 2 * 4 * 32 * 16;
-  static constexpr uint32_t kBars = 16;
+  static constexpr uint32_t oRed = oLim + 2 * E * 4;        // [2 warpgroups][2][4 warps][16] float4 per-warp sums
+  static constexpr uint32_t oBar = oRed + 2 * 2 * 4 * kKtEG * 16;
+  static constexpr uint32_t kBars = 20;
   static constexpr uint32_t kTotal = oBar + kBars * 8 + 16;
 };
 
@@ -116,10 +122,10 @@ __global__ void __launch_bounds__(kKtThreads, 1)
                  const KlTcArgs p) {
   using SM = KtSmem<HPG>;
   constexpr int E = SM::E;
-  constexpr int EG = E < 32 ? E : 32;  // entries per reduce-scatter group
+  constexpr int EG = kKtEG;    // entries per reduce-scatter group
   constexpr int NG = E / EG;
-  constexpr int RG = EG * HPG;         // tile rows (S^T columns) per group
-  static_assert(RG % 32 == 0 && E % 16 == 0, "entry groups");
+  constexpr int RG = EG * HPG;  // tile rows (S^T columns) per group
+  static_assert(RG % 32 == 0 && E % EG == 0, "entry groups");
   constexpr uint32_t kIdS = kt_idesc(128, 128), kIdI = kt_idesc(128, E);
   extern __shared__ __align__(1024) uint8_t kt_smem[];
   if (tc::smem_u32(kt_smem) & 1023u) {  // the swizzled operands need 1024-byte alignment
@@ -140,13 +146,13 @@ __global__ void __launch_bounds__(kKtThreads, 1)
   uint64_t* s_full = bars + 6;    // [2] TMEM sets
   uint64_t* tm_empty = bars + 8;  // [2]
   uint64_t* done_bar = bars + 10;
-  uint64_t* red_full = bars + 11;   // [2] the four warps' sums of a group are in red[buf]
-  uint64_t* red_empty = bars + 13;  // [2] warp 0 has merged red[buf]
+  uint64_t* red_full = bars + 11;   // [warpgroup][2]: the four warps' sums of a group are in red
+  uint64_t* red_empty = bars + 15;  // [warpgroup][2]: its warp 0 has merged them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + SM::kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kGather0 = 4, kTmaWarp = 6, kMmaWarp = 7;
+  constexpr int kGather0 = 8, kTmaWarp = 10, kMmaWarp = 11;
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
@@ -155,6 +161,8 @@ __global__ void __launch_bounds__(kKtThreads, 1)
       tc::mbar_init(&q_empty[r], 1);
       tc::mbar_init(&s_full[r], 1);
       tc::mbar_init(&tm_empty[r], 4);
+    }
+    for (int r = 0; r < 4; ++r) {
       tc::mbar_init(&red_full[r], 4);
       tc::mbar_init(&red_empty[r], 1);
     }
@@ -183,38 +191,36 @@ __global__ void __launch_bounds__(kKtThreads, 1)
 
   if (warp < kGather0) {
     // ------------------------------ epilogue ------------------------------
+    const int wg = warp >> 2;  // takes tiles z with z & 1 == wg (TMEM set and ring slot wg)
     const int quarter = warp & 3;
     const int key = quarter * 32 + lane;  // TMEM lane = key of the block
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale * kKtLog2e;
-    int gc = 0;  // groups merged so far (red buffer gc & 1)
+    int gc = 0;  // this warpgroup's groups merged so far (red buffer gc & 1)
     bool alive = true;
-    for (int z = 0; z < n && alive; ++z) {
+    int4 tl_n = wg < n ? p.tiles[z0 + wg] : make_int4(0, 0, 0, 0);
+    for (int z = wg; z < n && alive; z += 2) {
       const int set = z & 1;
+      const int4 tl = tl_n;
+      if (z + 2 < n) tl_n = p.tiles[z0 + z + 2];  // in flight during this tile
       if (!tc::mbar_wait(&s_full[set], (z >> 1) & 1, abort_flag) ||
           !tc::mbar_wait(&q_full[set], (z >> 1) & 1, abort_flag)) {  // row data of the slot (already complete)
         fail();
         break;
       }
       tc::fence_after_sync();
-      const int4 tl = p.tiles[z0 + z];
-      const float* lse2 = lse_s + set * kKtRows;
+      const float* lse_r = lse_s + set * kKtRows;
       const int* lim = lim_s + set * E;
       const uint32_t s_col = tmem + lane_base + uint32_t(set) * 256u;
 #pragma unroll 1
       for (int eg = 0; eg < NG; ++eg) {
-        float va[32], vb[32], vm[32], vl[32];
+        float va[EG], vb[EG], vm[EG], vl[EG];
         // index scores of the group's entries
-        uint32_t sc[32];
-        if (EG == 32)
-          tc::tmem_ld_32x32b_x32(s_col + 128u + uint32_t(eg * EG), sc);
-        else
-          tc::tmem_ld_32x32b_x16(s_col + 128u + uint32_t(eg * EG), sc);
-#pragma unroll
-        for (int x = EG; x < 32; ++x) sc[x] = 0u;
+        uint32_t sc[EG];
+        tc::tmem_ld_32x32b_x16(s_col + 128u + uint32_t(eg * EG), sc);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
+        for (int x = 0; x < EG; ++x) {
           va[x] = vb[x] = 0.f;
           vm[x] = -INFINITY;
           vl[x] = 0.f;
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(kKtThreads, 1)
 #pragma unroll
             for (int h = 0; h < HPG; ++h) {
               const int col = ee * HPG + h;
-              ps += kt_ex2(fmaf(__uint_as_float(sv32[col]), sl2, -lse2[e * HPG + h]));
+              ps += kt_ex2(fmaf(__uint_as_float(sv32[col]), sl2, -lse_r[e * HPG + h] * kKtLog2e));
             }
             const float pb = vis ? ps * (1.f / HPG) : 0.f;
             const float s = __uint_as_float(sc[el]);
@@ -252,26 +258,26 @@ __global__ void __launch_bounds__(kKtThreads, 1)
         kt_rs_sum(vb, lane);
         kt_rs_lse(vm, vl, lane);
         // the four warps' sums meet in red[buf]; warp 0 merges them (bounded waits, no bar.sync)
-        const int buf = gc & 1;
-        if (!tc::mbar_wait(&red_empty[buf], ((gc >> 1) & 1) ^ 1, abort_flag)) {
+        const int buf = gc & 1, rb = wg * 2 + buf;
+        if (!tc::mbar_wait(&red_empty[rb], ((gc >> 1) & 1) ^ 1, abort_flag)) {
           fail();
           alive = false;
           break;
         }
-        red[(buf * 4 + quarter) * 32 + lane] = make_float4(va[0], vb[0], vm[0], vl[0]);
+        if (lane < EG) red[(rb * 4 + quarter) * EG + lane] = make_float4(va[0], vb[0], vm[0], vl[0]);
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&red_full[buf]);
+        if (lane == 0) tc::mbar_arrive(&red_full[rb]);
         if (quarter == 0) {
-          if (!tc::mbar_wait(&red_full[buf], (gc >> 1) & 1, abort_flag)) {
+          if (!tc::mbar_wait(&red_full[rb], (gc >> 1) & 1, abort_flag)) {
             fail();
             alive = false;
             break;
           }
           if (lane < EG) {
-            float4 a = red[(buf * 4) * 32 + lane];
+            float4 a = red[(rb * 4) * EG + lane];
 #pragma unroll
             for (int w = 1; w < 4; ++w) {
-              const float4 o = red[(buf * 4 + w) * 32 + lane];
+              const float4 o = red[(rb * 4 + w) * EG + lane];
               a.x += o.x;
               a.y += o.y;
               kt_lse_merge(a.z, a.w, o.z, o.w);
@@ -280,7 +286,7 @@ __global__ void __launch_bounds__(kKtThreads, 1)
             if (e < tl.z) p.part[int64_t(z0 + z) * E + e] = a;
           }
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&red_empty[buf]);
+          if (lane == 0) tc::mbar_arrive(&red_empty[rb]);
         }
         ++gc;
       }
@@ -292,8 +298,36 @@ __global__ void __launch_bounds__(kKtThreads, 1)
     constexpr int kCprI = kKtDI / 8, kRpiI = 32 / kCprI;    // iq: 8 chunks per row, 4 rows per instruction
     const int chunk = lane % kCpr, sub = lane / kCpr;
     const int chunkI = lane % kCprI, subI = lane / kCprI;
+    constexpr int kItI = (E / 2) / kRpiI;  // index-query copy rounds per tile
+    // tile records and the entries this lane needs, fetched one tile ahead
+    int4 tl_n = make_int4(0, 0, 0, 0);
+    int ent2_n[2], entI_n[kItI], entL_n;
+    auto fetch = [&](int z) {
+      tl_n = p.tiles[z0 + z];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int e = (gw * 64 + x * 32 + lane) / HPG;
+        ent2_n[x] = e < tl_n.z ? p.entries[tl_n.y + e] : -1;
+      }
+#pragma unroll
+      for (int it = 0; it < kItI; ++it) {
+        const int e = gw * (E / 2) + it * kRpiI + subI;
+        entI_n[it] = e < tl_n.z ? p.entries[tl_n.y + e] : -1;
+      }
+      const int eL = gw * (E / 2) + lane;
+      entL_n = (lane < E / 2 && eL < tl_n.z) ? p.entries[tl_n.y + eL] : -1;
+    };
+    if (n > 0) fetch(0);
     for (int z = 0; z < n; ++z) {
       const int slot = z & 1;
+      const int4 tl = tl_n;
+      int ent2[2], entI[kItI];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) ent2[x] = ent2_n[x];
+#pragma unroll
+      for (int it = 0; it < kItI; ++it) entI[it] = entI_n[it];
+      const int entL = entL_n;
+      if (z + 1 < n) fetch(z + 1);
       // the slot is free once the MMA has read its rows and the epilogue of
       // tile z - 2 (same slot and TMEM set) has read its row data
       if (!tc::mbar_wait(&q_empty[slot], ((z >> 1) & 1) ^ 1, abort_flag) ||
@@ -301,17 +335,13 @@ __global__ void __launch_bounds__(kKtThreads, 1)
         fail();
         break;
       }
-      const int4 tl = p.tiles[z0 + z];
       const int g = tl.x / p.nblk, t = tl.x % p.nblk;
       const uint32_t qs = tc::smem_u32(ring + slot * SM::kSlot), iqs = qs + SM::kQ;
-      // this lane's two rows of the warp's 64 (row data) and their entries
-      int ent2[2];
+      // this lane's two rows of the warp's 64 (row data)
       int64_t qrow2[2];
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const int r = gw * 64 + x * 32 + lane;
-        const int e = r / HPG;
-        ent2[x] = e < tl.z ? p.entries[tl.y + e] : -1;
         const int il = ent2[x] >= 0 ? (ent2[x] >> 6) : 0;
         qrow2[x] = (int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * HPG + (r % HPG);
       }
@@ -327,27 +357,27 @@ __global__ void __launch_bounds__(kKtThreads, 1)
                 ent_r >= 0);
       }
       // index-query rows of entries [E/2 gw, E/2 gw + E/2)
-      for (int it = 0; it < (E / 2) / kRpiI; ++it) {
+#pragma unroll
+      for (int it = 0; it < kItI; ++it) {
         const int e = gw * (E / 2) + it * kRpiI + subI;
-        const int ent = e < tl.z ? p.entries[tl.y + e] : -1;
+        const int ent = entI[it];
         const int il = ent >= 0 ? (ent >> 6) : 0;
         const __nv_bfloat16* src = p.iq + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.G + g) * kKtDI + chunkI * 8;
         kt_cp16(iqs + e * 128 + ((uint32_t(chunkI) ^ uint32_t(e & 7)) << 4), src, ent >= 0);
       }
-      cp_async_commit_kt();
+      // lse of the two rows by 4-byte copies (zero for padding rows)
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const int r = gw * 64 + x * 32 + lane;
-        lse_s[slot * kKtRows + r] = ent2[x] >= 0 ? p.lse[qrow2[x]] * kKtLog2e : 0.f;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(lse_s + slot * kKtRows + r)),
+                     "l"(p.lse + qrow2[x]), "r"(ent2[x] >= 0 ? 4u : 0u)
+                     : "memory");
       }
-      for (int e = gw * (E / 2) + lane; e < (gw + 1) * (E / 2); e += 32) {
-        const int ent = e < tl.z ? p.entries[tl.y + e] : -1;
+      cp_async_commit_kt();
+      if (lane < E / 2) {
         int lm = -1;
-        if (ent >= 0 && sv.ok) {
-          const int pos = sv.q0 + p.c0 + (ent >> 6);
-          lm = min(min(pos, sv.L - 1) - t * kKtBs, kKtBs - 1);
-        }
-        lim_s[slot * E + e] = lm;
+        if (entL >= 0 && sv.ok) lm = min(min(sv.q0 + p.c0 + (entL >> 6), sv.L - 1) - t * kKtBs, kKtBs - 1);
+        lim_s[slot * E + gw * (E / 2) + lane] = lm;
       }
       cp_async_wait_all_kt();
       tc::fence_proxy_async_smem();
@@ -381,13 +411,16 @@ __global__ void __launch_bounds__(kKtThreads, 1)
   } else {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0) {
-      int kv_uses = 0;
+      int kv_uses = 0, prev_bin = -1;
       const uint32_t ka = tc::smem_u32(k_buf), ika = tc::smem_u32(ik_buf);
+      int bin_n = n > 0 ? p.tiles[z0].x : -1;
       for (int z = 0; z < n; ++z) {
         const int set = z & 1, slot = z & 1;
-        const int bin = p.tiles[z0 + z].x;
-        const bool first = z == 0 || p.tiles[z0 + z - 1].x != bin;
-        const bool last = z + 1 == n || p.tiles[z0 + z + 1].x != bin;
+        const int bin = bin_n;
+        bin_n = z + 1 < n ? p.tiles[z0 + z + 1].x : -1;  // one tile ahead
+        const bool first = bin != prev_bin;
+        const bool last = bin_n != bin;
+        prev_bin = bin;
         if (first) {
           if (!tc::mbar_wait(kv_full, kv_uses & 1, abort_flag)) {
             fail();

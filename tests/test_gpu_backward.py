@@ -7,7 +7,8 @@ recomputes the forward in fp64 from the definition.
 Tolerance per gradient tensor (the pages give none; derived): the kernels
 round P and dS to bf16 before the dV, dK and dQ products (relative 2^-9
 each), take delta = dout . out from the bf16 forward output, accumulate in
-fp32 and round each result to bf16 once (2^-9). The gradients are sums of
+fp32 and round each result to bf16 once (2^-9); dq is also rounded to bf16
+once per selected block (its slot partials) before the fp32 sum. The gradients are sums of
 terms of both signs, so the error is bounded relative to the magnitudes
 summed, not to the (possibly cancelling) result: max |err| <= 2e-2 max |ref|
 and mean |err| <= 1e-2 mean |ref| over each of dq, dk, dv.
