@@ -365,6 +365,74 @@ def run_msa(args, dist):
                    "share": round(v[1] / max(sum(x[1] for x in prof.values()), 1e-9), 4)} for k, v in prof.items()}
     all_roofs = [r for r in (roofline_for(k, prof, work, peaks, peak_src, w.name, args.steps) for k in prof) if r]
 
+    # ---------------------------- e2e (host buffers) -------------------
+    # Every step copies its inputs from pinned host memory and reads its
+    # output back, inside the timed region. The copies run on a second
+    # stream, pipelined the way a serving loop runs them: the inputs of step
+    # s+1 land in the other of two device input sets while step s computes,
+    # and the output of step s is read back as soon as step s is done.
+    e2e = None
+    if not args.no_e2e:
+        host = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in t}
+        for n in t:
+            host[n].copy_(t[n])
+        qo_h, kl_h = qo.cpu().pin_memory(), kl.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(x.numel() * x.element_size() for x in host.values()) + 2 * qo.numel() * 4
+        d2h = out_h.numel() * out_h.element_size()
+        sets = [dict(t, qo=qo, kl=kl, out=out),
+                dict({n: torch.empty_like(t[n]) for n in t}, qo=torch.empty_like(qo), kl=torch.empty_like(kl),
+                     out=torch.empty_like(out))]
+        cstream = torch.cuda.Stream(dev)
+
+        def copy_in(k):
+            for n in t:
+                sets[k][n].copy_(host[n], non_blocking=True)
+            sets[k]["qo"].copy_(qo_h, non_blocking=True)
+            sets[k]["kl"].copy_(kl_h, non_blocking=True)
+
+        def pipeline(nsteps):
+            ready = [torch.cuda.Event() for _ in range(2)]  # a set's inputs have landed
+            done = [torch.cuda.Event() for _ in range(2)]   # a set's step has finished
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            t0.record(cstream)
+            with torch.cuda.stream(cstream):
+                copy_in(0)
+                ready[0].record(cstream)
+            for s_ in range(nsteps):
+                k = s_ % 2
+                S = sets[k]
+                stream.wait_event(ready[k])
+                msa.msa_index_select(S["iq"], S["ik"], S["qo"], S["kl"], w.Bs, w.K, sel=sel, ws=ws_i)
+                msa.msa_sparse_attn_prefill(S["q"], S["k"], S["v"], sel, S["qo"], S["kl"], w.Bs, w.K, out=S["out"],
+                                            ws=ws_a)
+                done[k].record(stream)
+                with torch.cuda.stream(cstream):
+                    if s_ + 1 < nsteps:
+                        if s_ >= 1:
+                            cstream.wait_event(done[1 - k])  # step s-1 no longer reads the other set
+                        copy_in(1 - k)
+                        ready[1 - k].record(cstream)
+                    cstream.wait_event(done[k])
+                    out_h.copy_(S["out"], non_blocking=True)
+            t1.record(cstream)
+            torch.cuda.synchronize(dev)
+            return t0.elapsed_time(t1)
+
+        pipeline(2)  # warm-up
+        n_e = max(6, args.steps // 2)
+        dist.barrier()
+        e_ms = pipeline(n_e)
+        e_tot = dist.max(e_ms / 1e3)
+        e2e = {"value": round(dist.sum(tokens * n_e) / e_tot, 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms / n_e, 4), "steps": n_e,
+               "copies": "pinned host buffers, a copy stream overlapping step s+1's inputs with step s"}
+        del host, out_h, sets
+
+    torch.cuda.empty_cache()
+
     # ------------------------- KL auxiliary forward ---------------------
     # msa_kl_aux_forward over the prefill's selection and lse (one prefill
     # with lse output before the timed region); a step is one KL pass
@@ -434,72 +502,6 @@ def run_msa(args, dist):
         del dout, dq, dk, dv, ws_b
     if not (args.no_kl and args.no_backward):
         del lse
-
-    # ---------------------------- e2e (host buffers) -------------------
-    # Every step copies its inputs from pinned host memory and reads its
-    # output back, inside the timed region. The copies run on a second
-    # stream, pipelined the way a serving loop runs them: the inputs of step
-    # s+1 land in the other of two device input sets while step s computes,
-    # and the output of step s is read back as soon as step s is done.
-    e2e = None
-    if not args.no_e2e:
-        host = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in t}
-        for n in t:
-            host[n].copy_(t[n])
-        qo_h, kl_h = qo.cpu().pin_memory(), kl.cpu().pin_memory()
-        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h2d = sum(x.numel() * x.element_size() for x in host.values()) + 2 * qo.numel() * 4
-        d2h = out_h.numel() * out_h.element_size()
-        sets = [dict(t, qo=qo, kl=kl, out=out),
-                dict({n: torch.empty_like(t[n]) for n in t}, qo=torch.empty_like(qo), kl=torch.empty_like(kl),
-                     out=torch.empty_like(out))]
-        cstream = torch.cuda.Stream(dev)
-
-        def copy_in(k):
-            for n in t:
-                sets[k][n].copy_(host[n], non_blocking=True)
-            sets[k]["qo"].copy_(qo_h, non_blocking=True)
-            sets[k]["kl"].copy_(kl_h, non_blocking=True)
-
-        def pipeline(nsteps):
-            ready = [torch.cuda.Event() for _ in range(2)]  # a set's inputs have landed
-            done = [torch.cuda.Event() for _ in range(2)]   # a set's step has finished
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(dev)
-            t0.record(cstream)
-            with torch.cuda.stream(cstream):
-                copy_in(0)
-                ready[0].record(cstream)
-            for s_ in range(nsteps):
-                k = s_ % 2
-                S = sets[k]
-                stream.wait_event(ready[k])
-                msa.msa_index_select(S["iq"], S["ik"], S["qo"], S["kl"], w.Bs, w.K, sel=sel, ws=ws_i)
-                msa.msa_sparse_attn_prefill(S["q"], S["k"], S["v"], sel, S["qo"], S["kl"], w.Bs, w.K, out=S["out"],
-                                            ws=ws_a)
-                done[k].record(stream)
-                with torch.cuda.stream(cstream):
-                    if s_ + 1 < nsteps:
-                        if s_ >= 1:
-                            cstream.wait_event(done[1 - k])  # step s-1 no longer reads the other set
-                        copy_in(1 - k)
-                        ready[1 - k].record(cstream)
-                    cstream.wait_event(done[k])
-                    out_h.copy_(S["out"], non_blocking=True)
-            t1.record(cstream)
-            torch.cuda.synchronize(dev)
-            return t0.elapsed_time(t1)
-
-        pipeline(2)  # warm-up
-        n_e = max(6, args.steps // 2)
-        dist.barrier()
-        e_ms = pipeline(n_e)
-        e_tot = dist.max(e_ms / 1e3)
-        e2e = {"value": round(dist.sum(tokens * n_e) / e_tot, 1), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e_ms / n_e, 4), "steps": n_e,
-               "copies": "pinned host buffers, a copy stream overlapping step s+1's inputs with step s"}
-        del host, out_h, sets
 
     del t, out, sel, ws_i, ws_a
     torch.cuda.empty_cache()
