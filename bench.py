@@ -421,7 +421,7 @@ def run_msa(args, dist):
             return t0.elapsed_time(t1)
 
         pipeline(2)  # warm-up
-        n_e = max(6, args.steps // 2)
+        n_e = max(8, args.steps)  # the pipeline fill (first inputs) and drain (last output) spread over the steps
         dist.barrier()
         e_ms = pipeline(n_e)
         e_tot = dist.max(e_ms / 1e3)
