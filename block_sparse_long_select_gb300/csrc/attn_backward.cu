@@ -20,8 +20,8 @@
 //   3. dQ = dS K for the tile's rows, stored as a bf16 partial per (entry,
 //      head) row, while the next tile's rows are already being gathered.
 // When a bin's run ends, dK and dV are added into per-sequence fp32
-// accumulators: plainly when this CTA holds every tile of the bin, atomically
-// when the bin is split over CTAs. bwd_dq_combine then sums each row's slot
+// accumulators with fire-and-forget vector atomics (a bin held whole by one
+// CTA gets one add per query chunk; a bin split over CTAs gets one per CTA). bwd_dq_combine then sums each row's slot
 // partials in slot order (deterministic) and bwd_kv_store rounds dk and dv.
 #include <cmath>
 
@@ -120,7 +120,6 @@ struct BwdParams {
   const float *lse, *delta;               // [B, Nq, Hq]: forward log-sum-exp (natural log), dout . out
   const int* entries;                     // chunk entries (local query * 64 + slot), bins padded to tiles
   const int4* tiles;                      // (bin, first entry position, entries)
-  const int* tile_off;                    // [nbins + 1] first tile of each bin
   const int* cta_start;                   // [grid + 1]
   const int32_t* q_offset;
   const int32_t* kv_len;
@@ -214,7 +213,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
   };
 
   int bin = p.tiles[z0].x;
-  int bin_first = z0;
   load_kv(bin);
   load_rows(z0, 0);
   float dk[NTD][4], dv[NTD][4];
@@ -346,8 +344,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
     }
     // ---- end of the bin's run: add dK, dV into the sequence's accumulators
     const int next_bin = more ? p.tiles[z + 1].x : -1;
-    if (next_bin != bin) {
-      const bool whole = bin_first == p.tile_off[bin] && z + 1 == p.tile_off[bin + 1];
+    if (next_bin != bin) {  // fire-and-forget vector adds (see the tcgen05 kernel's flush)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int j = t * BS + mt * 16 + gq + 8 * hr;
@@ -357,20 +354,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
           for (int n = 0; n < NTD; ++n) {
             float* pk = p.dk_acc + base + n * 8;
             float* pv = p.dv_acc + base + n * 8;
-            if (whole) {
-              float2 a = *reinterpret_cast<float2*>(pk), c = *reinterpret_cast<float2*>(pv);
-              a.x += dk[n][2 * hr];
-              a.y += dk[n][2 * hr + 1];
-              c.x += dv[n][2 * hr];
-              c.y += dv[n][2 * hr + 1];
-              *reinterpret_cast<float2*>(pk) = a;
-              *reinterpret_cast<float2*>(pv) = c;
-            } else {
-              atomicAdd(pk, dk[n][2 * hr]);
-              atomicAdd(pk + 1, dk[n][2 * hr + 1]);
-              atomicAdd(pv, dv[n][2 * hr]);
-              atomicAdd(pv + 1, dv[n][2 * hr + 1]);
-            }
+            asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(pk), "f"(dk[n][2 * hr]), "f"(dk[n][2 * hr + 1])
+                         : "memory");
+            asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(pv), "f"(dv[n][2 * hr]), "f"(dv[n][2 * hr + 1])
+                         : "memory");
           }
         }
       }
@@ -381,7 +368,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_tile_kernel(const BwdParam
       if (more) {
         __syncthreads();  // every warp is done with this block's K
         bin = next_bin;
-        bin_first = z + 1;
         load_kv(bin);
       }
     }
@@ -570,15 +556,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int quarter = warp & 3;
     const int key = quarter * 32 + lane;  // TMEM lane: key of S^T, dP^T, dV, dK; row of dQ
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    int bin_first = 0, nbins = 0, prev_bin = -1;
+    int nbins = 0;
     int4 tl_n = n > 0 ? p.tiles[z0] : make_int4(0, 0, 0, 0);
     for (int z = 0; z < n; ++z) {
       const int slot = z & 1;
       const int4 tl = tl_n;
       if (z + 1 < n) tl_n = p.tiles[z0 + z + 1];  // in flight while this tile is processed
       const int bin = tl.x;
-      if (z > 0 && prev_bin != bin) bin_first = z;
-      prev_bin = bin;
       // the slot's row data come from the gather warps: observe their phase
       // directly (it has completed: the MMA read the slot before s_full)
       if (!tc::mbar_wait(s_full, z & 1, abort_flag) || !tc::mbar_wait(&q_full[slot], (z >> 1) & 1, abort_flag)) {
@@ -663,9 +647,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc::fence_after_sync();
+        // fire-and-forget vector adds (no load on the epilogue's path): a bin
+        // that this CTA holds whole has this one flush per query chunk, so its
+        // sum is deterministic; a split bin's CTAs add in any order
         const int g = bin / p.nblk, t = bin % p.nblk;
         const int j = t * kTcBs + key;
-        const bool whole = z0 + bin_first == p.tile_off[bin] && z0 + z + 1 == p.tile_off[bin + 1];
         float* dkr = p.dk_acc + (int64_t(j) * p.G + g) * D;
         float* dvr = p.dv_acc + (int64_t(j) * p.G + g) * D;
 #pragma unroll 1
@@ -683,20 +669,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                             __uint_as_float(a[x + 3]));
               const float4 bk = make_float4(__uint_as_float(b2[x]), __uint_as_float(b2[x + 1]),
                                             __uint_as_float(b2[x + 2]), __uint_as_float(b2[x + 3]));
-              if (whole) {
-                float4 ov = *pv, ok = *pk4;
-                ov.x += av.x; ov.y += av.y; ov.z += av.z; ov.w += av.w;
-                ok.x += bk.x; ok.y += bk.y; ok.z += bk.z; ok.w += bk.w;
-                *pv = ov;
-                *pk4 = ok;
-              } else {
-                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(pv), "f"(av.x), "f"(av.y),
-                             "f"(av.z), "f"(av.w)
-                             : "memory");
-                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(pk4), "f"(bk.x), "f"(bk.y),
-                             "f"(bk.z), "f"(bk.w)
-                             : "memory");
-              }
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(pv), "f"(av.x), "f"(av.y), "f"(av.z),
+                           "f"(av.w)
+                           : "memory");
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(pk4), "f"(bk.x), "f"(bk.y), "f"(bk.z),
+                           "f"(bk.w)
+                           : "memory");
             }
           }
         }
@@ -985,7 +963,6 @@ cudaError_t launch_attn_backward(const void* q, const void* k, const void* v, co
   prm.delta = delta;
   prm.entries = reinterpret_cast<const int*>(w + L.entries);
   prm.tiles = reinterpret_cast<const int4*>(w + L.tiles);
-  prm.tile_off = reinterpret_cast<const int*>(w + L.tile_off);
   prm.cta_start = reinterpret_cast<const int*>(w + L.cta_start);
   prm.q_offset = q_offset;
   prm.kv_len = kv_len;
