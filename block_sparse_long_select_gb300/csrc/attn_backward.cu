@@ -77,6 +77,13 @@ __device__ __forceinline__ void cp4(void* dst, const void* src, bool in) {
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// 8 registers -> 32 TMEM lanes x 8 columns
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ bool bwd_entry_valid(int t, int pos, int Bs, int nblk) {
   return t >= 0 && t < nblk && t * Bs <= pos;
 }
@@ -415,7 +422,7 @@ struct TcSmem {
   static constexpr uint32_t kSlot = 2 * kRowsT;            // q + dout
   static constexpr uint32_t kDs = kBwdRows * kTcBs * 2;    // dS (MN-major)
   static constexpr uint32_t oK = 0, oV = kKV, oRing = 2 * kKV, oDs = oRing + 2 * kSlot;
-  static constexpr uint32_t oRowF = oDs + kDs;             // [2][2][128] float: lse (natural log), delta
+  static constexpr uint32_t oRowF = oDs + kDs;             // [2][2][128] float: lse * log2(e), delta
   static constexpr uint32_t oLim = oRowF + 2 * kBwdRows * 8;  // [2][128] int8: last visible key of the row - t*128
   static constexpr uint32_t oBar = oLim + 2 * kBwdRows;     // 8-byte aligned
   static constexpr uint32_t kBars = 13;
@@ -546,6 +553,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (ent >= 0 && sv.ok) lim = min(min(sv.q0 + p.c0 + il, sv.L - 1) - t * kTcBs, kTcBs - 1);
       lim_s[slot * kBwdRows + r] = int8_t(lim);
       cp_wait_all();
+      rowf[(2 * slot) * kBwdRows + r] *= kLog2eBwd;  // the epilogue wants lse in log2 units
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&q_full[slot]);
@@ -558,6 +566,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     int nbins = 0;
     int4 tl_n = n > 0 ? p.tiles[z0] : make_int4(0, 0, 0, 0);
+    // tile z's dQ row (bf16 pairs) waits in registers and is stored while the
+    // MMAs of tile z + 1 run (the epilogue would otherwise idle there)
+    uint32_t dq_pk[D / 2];
+    uint4* dq_dst = nullptr;
+    auto store_dq = [&]() {
+      if (dq_dst != nullptr) {
+#pragma unroll
+        for (int c8 = 0; c8 < D / 8; ++c8)
+          dq_dst[c8 * kBwdRows] = make_uint4(dq_pk[4 * c8], dq_pk[4 * c8 + 1], dq_pk[4 * c8 + 2], dq_pk[4 * c8 + 3]);
+        dq_dst = nullptr;
+      }
+    };
     for (int z = 0; z < n; ++z) {
       const int slot = z & 1;
       const int4 tl = tl_n;
@@ -570,42 +590,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const float* lse_r = rowf + (2 * slot) * kBwdRows;
+      const float* lse_r = rowf + (2 * slot) * kBwdRows;  // lse * log2(e)
       const float* dlt_r = rowf + (2 * slot + 1) * kBwdRows;
       const int8_t* lm = lim_s + slot * kBwdRows;
       const uint32_t ds_row = tc::smem_u32(ds_buf) + uint32_t(key) * 128u;
       const float sl2 = p.scale * kLog2eBwd;
 #pragma unroll 1
-      for (int c = 0; c < kBwdRows / 32; ++c) {  // 32 tile rows at a time
-        uint32_t sv32[32], dv32[32];
-        tc::tmem_ld_32x32b_x32(tmem + lane_base + uint32_t(c * 32), sv32);
-        tc::tmem_ld_32x32b_x32(tmem + lane_base + 128u + uint32_t(c * 32), dv32);
-        tc::tmem_ld_wait();
-        uint32_t pk[16], dk2[16];
+      for (int c = 0; c < kBwdRows / 16; ++c) {  // 16 tile rows at a time
+        uint32_t sv16[16], dv16[16];
+        tc::tmem_ld_32x32b_x16(tmem + lane_base + uint32_t(c * 16), sv16);
+        tc::tmem_ld_32x32b_x16(tmem + lane_base + 128u + uint32_t(c * 16), dv16);
+        // the 16 rows' data in four vector loads (all threads read the same words: broadcast)
+        float lse16[16], dlt16[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 a4 = reinterpret_cast<const float4*>(lse_r + c * 16)[q4];
+          const float4 b4 = reinterpret_cast<const float4*>(dlt_r + c * 16)[q4];
+          lse16[4 * q4] = a4.x; lse16[4 * q4 + 1] = a4.y; lse16[4 * q4 + 2] = a4.z; lse16[4 * q4 + 3] = a4.w;
+          dlt16[4 * q4] = b4.x; dlt16[4 * q4 + 1] = b4.y; dlt16[4 * q4 + 2] = b4.z; dlt16[4 * q4 + 3] = b4.w;
+        }
+        const uint4 lim16 = reinterpret_cast<const uint4*>(lm)[c];
+        const uint32_t limw[4] = {lim16.x, lim16.y, lim16.z, lim16.w};
+        tc::tmem_ld_wait();
+        uint32_t pk[8], dk2[8];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
           float pp[2], dd[2];
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int r = c * 32 + j + e2;
-            const bool vis = key <= int(lm[r]);
-            const float pr =
-                vis ? bwd_ex2(fmaf(__uint_as_float(sv32[j + e2]), sl2, -lse_r[r] * kLog2eBwd)) : 0.f;
+            const int jr = j + e2;
+            const int lim_r = int(int8_t((limw[jr >> 2] >> (8 * (jr & 3))) & 0xffu));
+            const float pr = key <= lim_r ? bwd_ex2(fmaf(__uint_as_float(sv16[jr]), sl2, -lse16[jr])) : 0.f;
             pp[e2] = pr;
-            dd[e2] = pr * (__uint_as_float(dv32[j + e2]) - dlt_r[r]);
+            dd[e2] = pr * (__uint_as_float(dv16[jr]) - dlt16[jr]);
           }
           pk[j >> 1] = bwd_pack(pp[0], pp[1]);
           dk2[j >> 1] = bwd_pack(dd[0], dd[1]);
         }
-        tc::tmem_st_32x32b_x16(tmem + lane_base + uint32_t(c * 16), pk);
-        tc::tmem_st_32x32b_x16(tmem + lane_base + 128u + uint32_t(c * 16), dk2);
-        // dS^T row of this key: rows [32 c, 32 c + 32) = four 16-byte chunks of half (32 c) / 64
+        tmem_st_x8(tmem + lane_base + uint32_t(c * 8), pk);  // P^T rows 16 c.. packed over S^T already read
+        tmem_st_x8(tmem + lane_base + 128u + uint32_t(c * 8), dk2);
+        // dS^T row of this key: rows [16 c, 16 c + 16) = two 16-byte chunks of half (16 c) / 64
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t half = uint32_t(c >> 1), ch = uint32_t((c & 1) * 4 + q4);
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const uint32_t half = uint32_t(c >> 2), ch = uint32_t((c & 3) * 2 + q2);
           const uint32_t addr = ds_row + half * SM::kHalf + ((ch ^ uint32_t(key & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dk2[q4 * 4]), "r"(dk2[q4 * 4 + 1]),
-                       "r"(dk2[q4 * 4 + 2]), "r"(dk2[q4 * 4 + 3])
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dk2[q2 * 4]), "r"(dk2[q2 * 4 + 1]),
+                       "r"(dk2[q2 * 4 + 2]), "r"(dk2[q2 * 4 + 3])
                        : "memory");
         }
       }
@@ -614,7 +644,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(p_full);
-      // dQ rows of this tile (lane = row) out of TMEM, then the bf16 partial
+      store_dq();  // the previous tile's dQ, under this tile's dV/dK/dQ MMAs
+      // dQ rows of this tile (lane = row) out of TMEM, packed to the bf16 partial
       if (!tc::mbar_wait(dq_full, z & 1, abort_flag)) {
         fail();
         break;
@@ -630,16 +661,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tm_empty);
-      if ((key >> p.hpg_log2) < tl.z) {  // bf16 partial, chunk-major: a warp store covers 512 contiguous bytes
-        uint4* dst = p.part_dq + int64_t(z0 + z) * (D / 8) * kBwdRows + key;
 #pragma unroll
-        for (int c8 = 0; c8 < D / 8; ++c8)
-          dst[c8 * kBwdRows] =
-              make_uint4(bwd_pack(__uint_as_float(qv[8 * c8]), __uint_as_float(qv[8 * c8 + 1])),
-                         bwd_pack(__uint_as_float(qv[8 * c8 + 2]), __uint_as_float(qv[8 * c8 + 3])),
-                         bwd_pack(__uint_as_float(qv[8 * c8 + 4]), __uint_as_float(qv[8 * c8 + 5])),
-                         bwd_pack(__uint_as_float(qv[8 * c8 + 6]), __uint_as_float(qv[8 * c8 + 7])));
-      }
+      for (int x = 0; x < D / 2; ++x) dq_pk[x] = bwd_pack(__uint_as_float(qv[2 * x]), __uint_as_float(qv[2 * x + 1]));
+      // bf16 partial, chunk-major: a warp store covers 512 contiguous bytes
+      if ((key >> p.hpg_log2) < tl.z) dq_dst = p.part_dq + int64_t(z0 + z) * (D / 8) * kBwdRows + key;
       if (z + 1 == n || tl_n.x != bin) {  // last tile of the bin's run
         // dV and dK of the bin's run (lane = key) into the sequence's accumulators
         if (!tc::mbar_wait(acc_full, nbins & 1, abort_flag)) {
@@ -684,6 +709,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ++nbins;
       }
     }
+    store_dq();  // the last tile's dQ
   } else if (warp == kTmaWarp) {
     // ------------------------------ K/V producer ------------------------------
     if (lane == 0) {
