@@ -15,12 +15,13 @@
 // holds all heads of every entry in neighbouring columns (the head mean is
 // in-thread). The sums over keys are a reduce-scatter across the warp's lanes
 // (lane l ends with entry l of a group of 32) and a four-warp combine in
-// shared memory. Two epilogue warpgroups take alternate tiles, each with its
-// own TMEM set, so the MMA of one tile runs under the epilogue of the other.
-// Warps 0-7 epilogue (warpgroup z & 1 takes tile z), 8-9 gather q rows,
-// index-query rows and row data (cp.async, 128B-swizzled K-major, two ring
-// slots; tile records and entries fetched a tile ahead), 10 TMA of K and IK
-// per bin, 11 TMEM owner and MMA issuer. Every wait is bounded.
+// shared memory. NS epilogue warpgroups (NS = 3 when three TMEM sets of
+// 128 + E columns fit, else 2) take tiles in turn, each with its own TMEM set
+// and gather ring slot, so the MMAs of the next tiles run under the epilogues.
+// Warps 0..4 NS - 1 epilogue (warpgroup z % NS takes tile z), then two warps
+// gathering q rows, index-query rows and row data (cp.async, 128B-swizzled
+// K-major; tile records and entries fetched a tile ahead), one TMA warp for K
+// and IK per bin, one TMEM owner and MMA issuer. Every wait is bounded.
 #include <cmath>
 
 #include "msa_internal.cuh"
@@ -29,7 +30,6 @@
 namespace msa {
 namespace {
 
-constexpr int kKtThreads = 384;
 constexpr int kKtEG = 16;  // entries per reduce-scatter group
 constexpr int kKtD = 128, kKtDI = 64, kKtBs = 128, kKtRows = kKvoRows;
 constexpr float kKtLog2e = 1.4426950408889634f;
@@ -101,6 +101,8 @@ __device__ __forceinline__ void kt_rs_lse(float (&m)[kKtEG], float (&l)[kKtEG], 
 template <int HPG>
 struct KtSmem {
   static constexpr int E = kKtRows / HPG;                  // entries per tile
+  static constexpr int NS = 512 / (128 + E) >= 3 ? 3 : 2;  // TMEM sets = epilogue warpgroups = ring slots
+  static constexpr int kThreads = (4 * NS + 4) * 32;
   static constexpr uint32_t kHalf = kKtRows * 128;         // one 64-wide half of a 128-row operand
   static constexpr uint32_t kK = kKtBs * kKtD * 2;         // K block (two halves)
   static constexpr uint32_t kIK = kKtBs * kKtDI * 2;       // IK block (one half)
@@ -108,20 +110,21 @@ struct KtSmem {
   static constexpr uint32_t kIQ = E * kKtDI * 2;           // gathered index-query rows (E x 128 B)
   static constexpr uint32_t kSlot = kQ + kIQ;              // multiple of 1024
   static constexpr uint32_t oK = 0, oIK = kK, oRing = kK + kIK;
-  static constexpr uint32_t oLse = oRing + 2 * kSlot;      // [2][128] lse (natural log)
-  static constexpr uint32_t oLim = oLse + 2 * kKtRows * 4;  // [2][E] last visible key - t * 128 (-1: none)
-  static constexpr uint32_t oRed = oLim + 2 * E * 4;        // [2 warpgroups][2][4 warps][16] float4 per-warp sums
-  static constexpr uint32_t oBar = oRed + 2 * 2 * 4 * kKtEG * 16;
-  static constexpr uint32_t kBars = 20;
+  static constexpr uint32_t oLse = oRing + NS * kSlot;     // [NS][128] lse * log2(e)
+  static constexpr uint32_t oLim = oLse + NS * kKtRows * 4;  // [NS][E] last visible key - t * 128 (-1: none)
+  static constexpr uint32_t oRed = oLim + NS * E * 4;       // [NS warpgroups][2][4 warps][16] float4 per-warp sums
+  static constexpr uint32_t oBar = oRed + NS * 2 * 4 * kKtEG * 16;
+  static constexpr uint32_t kBars = 3 + 8 * NS;
   static constexpr uint32_t kTotal = oBar + kBars * 8 + 16;
 };
 
 template <int HPG>
-__global__ void __launch_bounds__(kKtThreads, 1)
+__global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
     kl_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmIK,
                  const KlTcArgs p) {
   using SM = KtSmem<HPG>;
-  constexpr int E = SM::E;
+  constexpr int E = SM::E, NS = SM::NS;
+  constexpr uint32_t kSet = 128 + E;  // TMEM columns per set: S^T, then I^T
   constexpr int EG = kKtEG;    // entries per reduce-scatter group
   constexpr int NG = E / EG;
   constexpr int RG = EG * HPG;  // tile rows (S^T columns) per group
@@ -141,28 +144,28 @@ __global__ void __launch_bounds__(kKtThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(kt_smem + SM::oBar);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;    // [2] ring slots
-  uint64_t* q_empty = bars + 4;   // [2]
-  uint64_t* s_full = bars + 6;    // [2] TMEM sets
-  uint64_t* tm_empty = bars + 8;  // [2]
-  uint64_t* done_bar = bars + 10;
-  uint64_t* red_full = bars + 11;   // [warpgroup][2]: the four warps' sums of a group are in red
-  uint64_t* red_empty = bars + 15;  // [warpgroup][2]: its warp 0 has merged them
+  uint64_t* done_bar = bars + 2;
+  uint64_t* q_full = bars + 3;               // [NS] ring slots
+  uint64_t* q_empty = q_full + NS;           // [NS]
+  uint64_t* s_full = q_empty + NS;           // [NS] TMEM sets
+  uint64_t* tm_empty = s_full + NS;          // [NS]
+  uint64_t* red_full = tm_empty + NS;        // [NS][2]: a warpgroup's four warps' sums of a group are in red
+  uint64_t* red_empty = red_full + 2 * NS;   // [NS][2]: its warp 0 has merged them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + SM::kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kGather0 = 8, kTmaWarp = 10, kMmaWarp = 11;
+  constexpr int kGather0 = 4 * NS, kTmaWarp = 4 * NS + 2, kMmaWarp = 4 * NS + 3;
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < NS; ++r) {
       tc::mbar_init(&q_full[r], 2);
       tc::mbar_init(&q_empty[r], 1);
       tc::mbar_init(&s_full[r], 1);
       tc::mbar_init(&tm_empty[r], 4);
     }
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < 2 * NS; ++r) {
       tc::mbar_init(&red_full[r], 4);
       tc::mbar_init(&red_empty[r], 1);
     }
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kKtThreads, 1)
 
   if (warp < kGather0) {
     // ------------------------------ epilogue ------------------------------
-    const int wg = warp >> 2;  // takes tiles z with z & 1 == wg (TMEM set and ring slot wg)
+    const int wg = warp >> 2;  // takes tiles z with z % NS == wg (TMEM set and ring slot wg)
     const int quarter = warp & 3;
     const int key = quarter * 32 + lane;  // TMEM lane = key of the block
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
@@ -199,19 +202,19 @@ __global__ void __launch_bounds__(kKtThreads, 1)
     int gc = 0;  // this warpgroup's groups merged so far (red buffer gc & 1)
     bool alive = true;
     int4 tl_n = wg < n ? p.tiles[z0 + wg] : make_int4(0, 0, 0, 0);
-    for (int z = wg; z < n && alive; z += 2) {
-      const int set = z & 1;
+    for (int z = wg; z < n && alive; z += NS) {
+      const int set = wg, ph = (z / NS) & 1;
       const int4 tl = tl_n;
-      if (z + 2 < n) tl_n = p.tiles[z0 + z + 2];  // in flight during this tile
-      if (!tc::mbar_wait(&s_full[set], (z >> 1) & 1, abort_flag) ||
-          !tc::mbar_wait(&q_full[set], (z >> 1) & 1, abort_flag)) {  // row data of the slot (already complete)
+      if (z + NS < n) tl_n = p.tiles[z0 + z + NS];  // in flight during this tile
+      if (!tc::mbar_wait(&s_full[set], ph, abort_flag) ||
+          !tc::mbar_wait(&q_full[set], ph, abort_flag)) {  // row data of the slot (already complete)
         fail();
         break;
       }
       tc::fence_after_sync();
       const float* lse_r = lse_s + set * kKtRows;
       const int* lim = lim_s + set * E;
-      const uint32_t s_col = tmem + lane_base + uint32_t(set) * 256u;
+      const uint32_t s_col = tmem + lane_base + uint32_t(set) * kSet;
 #pragma unroll 1
       for (int eg = 0; eg < NG; ++eg) {
         float va[EG], vb[EG], vm[EG], vl[EG];
@@ -229,17 +232,31 @@ __global__ void __launch_bounds__(kKtThreads, 1)
         for (int c = 0; c < RG / 32; ++c) {
           uint32_t sv32[32];
           tc::tmem_ld_32x32b_x32(s_col + uint32_t(eg * RG + c * 32), sv32);
+          // the chunk's 32 rows of lse * log2(e) and its 32 / HPG entries' visibility
+          // limits in vector loads (the same words for every thread: broadcast)
+          constexpr int EC = 32 / HPG;
+          float l32[32];
+          int lm[EC];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 v = reinterpret_cast<const float4*>(lse_r + eg * RG + c * 32)[q4];
+            l32[4 * q4] = v.x; l32[4 * q4 + 1] = v.y; l32[4 * q4 + 2] = v.z; l32[4 * q4 + 3] = v.w;
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < EC / 4; ++q4) {
+            const int4 v = reinterpret_cast<const int4*>(lim + eg * EG + c * EC)[q4];
+            lm[4 * q4] = v.x; lm[4 * q4 + 1] = v.y; lm[4 * q4 + 2] = v.z; lm[4 * q4 + 3] = v.w;
+          }
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int ee = 0; ee < 32 / HPG; ++ee) {
-            const int el = c * (32 / HPG) + ee;  // entry within the group
-            const int e = eg * EG + el;
-            const bool vis = key <= lim[e];
+          for (int ee = 0; ee < EC; ++ee) {
+            const int el = c * EC + ee;  // entry within the group
+            const bool vis = key <= lm[ee];
             float ps = 0.f;
 #pragma unroll
             for (int h = 0; h < HPG; ++h) {
               const int col = ee * HPG + h;
-              ps += kt_ex2(fmaf(__uint_as_float(sv32[col]), sl2, -lse_r[e * HPG + h] * kKtLog2e));
+              ps += kt_ex2(fmaf(__uint_as_float(sv32[col]), sl2, -l32[col]));
             }
             const float pb = vis ? ps * (1.f / HPG) : 0.f;
             const float s = __uint_as_float(sc[el]);
@@ -319,7 +336,7 @@ __global__ void __launch_bounds__(kKtThreads, 1)
     };
     if (n > 0) fetch(0);
     for (int z = 0; z < n; ++z) {
-      const int slot = z & 1;
+      const int slot = z % NS, ph = (z / NS) & 1;
       const int4 tl = tl_n;
       int ent2[2], entI[kItI];
 #pragma unroll
@@ -329,9 +346,9 @@ __global__ void __launch_bounds__(kKtThreads, 1)
       const int entL = entL_n;
       if (z + 1 < n) fetch(z + 1);
       // the slot is free once the MMA has read its rows and the epilogue of
-      // tile z - 2 (same slot and TMEM set) has read its row data
-      if (!tc::mbar_wait(&q_empty[slot], ((z >> 1) & 1) ^ 1, abort_flag) ||
-          !tc::mbar_wait(&tm_empty[slot], ((z >> 1) & 1) ^ 1, abort_flag)) {
+      // tile z - NS (same slot and TMEM set) has read its row data
+      if (!tc::mbar_wait(&q_empty[slot], ph ^ 1, abort_flag) ||
+          !tc::mbar_wait(&tm_empty[slot], ph ^ 1, abort_flag)) {
         fail();
         break;
       }
@@ -380,6 +397,8 @@ __global__ void __launch_bounds__(kKtThreads, 1)
         lim_s[slot * E + gw * (E / 2) + lane] = lm;
       }
       cp_async_wait_all_kt();
+#pragma unroll
+      for (int x = 0; x < 2; ++x) lse_s[slot * kKtRows + gw * 64 + x * 32 + lane] *= kKtLog2e;  // log2 units
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&q_full[slot]);
@@ -415,7 +434,7 @@ __global__ void __launch_bounds__(kKtThreads, 1)
       const uint32_t ka = tc::smem_u32(k_buf), ika = tc::smem_u32(ik_buf);
       int bin_n = n > 0 ? p.tiles[z0].x : -1;
       for (int z = 0; z < n; ++z) {
-        const int set = z & 1, slot = z & 1;
+        const int set = z % NS, slot = set, ph = (z / NS) & 1;
         const int bin = bin_n;
         bin_n = z + 1 < n ? p.tiles[z0 + z + 1].x : -1;  // one tile ahead
         const bool first = bin != prev_bin;
@@ -428,14 +447,13 @@ __global__ void __launch_bounds__(kKtThreads, 1)
           }
           ++kv_uses;
         }
-        if (!tc::mbar_wait(&q_full[slot], (z >> 1) & 1, abort_flag) ||
-            !tc::mbar_wait(&tm_empty[set], ((z >> 1) & 1) ^ 1, abort_flag)) {
+        if (!tc::mbar_wait(&q_full[slot], ph, abort_flag) || !tc::mbar_wait(&tm_empty[set], ph ^ 1, abort_flag)) {
           fail();
           break;
         }
         tc::fence_after_sync();
         const uint32_t qa = tc::smem_u32(ring + slot * SM::kSlot), iqa = qa + SM::kQ;
-        const uint32_t d_s = tmem + uint32_t(set) * 256u;
+        const uint32_t d_s = tmem + uint32_t(set) * kSet;
 #pragma unroll
         for (int kk = 0; kk < kKtD / 16; ++kk) {  // S^T = K q^T
           const uint32_t off = (kk & 3) * 32;
@@ -494,7 +512,7 @@ cudaError_t launch_kl_tile_tc(const KlTcArgs& a, const void* k, const void* ik, 
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(KtSmem<H_>::kTotal))) != \
         cudaSuccess)                                                                                             \
       return e;                                                                                                  \
-    kern<<<grid, kKtThreads, KtSmem<H_>::kTotal, stream>>>(tmK, tmIK, a);                                        \
+    kern<<<grid, KtSmem<H_>::kThreads, KtSmem<H_>::kTotal, stream>>>(tmK, tmIK, a);                              \
   } while (0)
   if (hpg == 2)
     MSA_KT(2);
