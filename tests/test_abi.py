@@ -83,3 +83,34 @@ def test_host_validation_before_launch(lib):
     assert lib.msa_index_select_v(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 2, 1, 0, P(), None, P(), 1 << 20, None) == 1
     assert lib.msa_index_select_v(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 2, 1, 2, P(), None, P(), 1 << 20, None) == 1
     assert lib.msa_index_select_v(P(), P(), None, None, 1, 8, 8, 1, 32, 4, 1, 1, 3, P(), None, P(), 1 << 20, None) == 1
+
+
+def test_kl_and_backward_host_validation(lib):
+    P = lambda: FAKE  # noqa: E731
+    bf16 = msa.MSA_BF16
+    # workspace sizes: supported shapes get one, unsupported ones 0
+    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 128, 0, 128, 16, bf16) >= 256
+    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 96, 0, 128, 16, bf16) == 0
+    assert msa.msa_workspace_size(msa.MSA_OP_BACKWARD, 1, 8192, 8192, 8, 32, 128, 0, 128, 16, bf16) >= 256
+    assert msa.msa_workspace_size(msa.MSA_OP_BACKWARD, 1, 8192, 8192, 2, 32, 128, 0, 128, 16, bf16) == 0  # hpg 16
+    assert msa.msa_workspace_size(msa.MSA_OP_BACKWARD, 1, 8192, 8192, 8, 32, 128, 0, 16, 16, bf16) == 0  # Bs 16
+
+    def kl(lse=True, Hq=8, Hkv=2, d=128, di=64, Bs=128, ws_bytes=1 << 30):
+        return lib.msa_kl_aux_forward(P(), P(), P(), P(), P(), P() if lse else None, None, None, 1, 8, 8, Hq, Hkv, d,
+                                      di, Bs, 2, 0.0, bf16, P(), P(), ws_bytes, None)
+    assert kl(lse=False) == 1          # the forward's lse is required
+    assert kl(Hq=6, Hkv=4) == 1        # Hq not a multiple of Hkv
+    assert kl(d=96) == 2               # head dimension not built
+    assert kl(d=128, di=32) == 2       # (d, di) pairing not built
+    assert kl(ws_bytes=16) == 3        # workspace too small
+
+    def bwd(dout=True, Hq=8, Hkv=2, d=128, Bs=128, dtype=bf16, ws_bytes=1 << 30):
+        return lib.msa_sparse_attn_backward(P(), P(), P(), P(), P() if dout else None, P(), P(), None, None, 1, 8, 8,
+                                            Hq, Hkv, d, Bs, 2, 0.0, dtype, P(), P(), P(), P(), ws_bytes, None)
+    assert bwd(dout=False) == 1        # the output gradient is required
+    assert bwd(Hq=6, Hkv=4) == 1       # Hq not a multiple of Hkv
+    assert bwd(d=96) == 2              # head dimension not built
+    assert bwd(Bs=16) == 2             # block size not built
+    assert bwd(Hq=32, Hkv=2) == 2      # 16 heads per group: beyond the built ratios
+    assert bwd(dtype=msa.MSA_FP32) == 2  # bf16 only
+    assert bwd(ws_bytes=16) == 3       # workspace too small
