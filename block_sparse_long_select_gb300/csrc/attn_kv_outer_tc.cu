@@ -1100,9 +1100,11 @@ int chunk_tokens(int Nq, int Hq, int K, int d) {
     env = s ? atoi(s) : 0;
   }
   if (env > 0) return env < Nq ? env : Nq;
-  // bound the partial buffers to ~4 GiB, in equal chunks (no short tail chunk)
+  // bound the partial buffers to ~6 GiB, in equal chunks (no short tail chunk);
+  // at 128K tokens this gives three chunks, measured faster than five (the
+  // per-chunk inversion and grid tails) and than one or two (attention's working set)
   const size_t per_tok = size_t(Hq) * K * (size_t(d) * 2 + 4);
-  size_t cap = (size_t(4) << 30) / per_tok;
+  size_t cap = (size_t(6) << 30) / per_tok;
   if (cap < 1024) cap = 1024;
   const size_t nchunks = (size_t(Nq) + cap - 1) / cap;
   return int((size_t(Nq) + nchunks - 1) / nchunks);

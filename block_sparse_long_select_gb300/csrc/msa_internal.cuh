@@ -92,7 +92,7 @@ struct KvoLayout {
   size_t cnt, cursor, entry_off, tile_off, cost_off, total, cta_start, entries, rev, tiles, part_o, part_lse, end;
   size_t max_tiles;
 };
-// query tokens per chunk (equal chunks; the forward's bf16 partials stay under ~4 GiB)
+// query tokens per chunk (equal chunks; the forward's bf16 partials stay under ~6 GiB)
 int chunk_tokens(int Nq, int Hq, int K, int d);
 KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk);
 int sm_count();
