@@ -11,18 +11,25 @@
 //
 // The work follows the forward's inversion: per-(group, key block) bins of
 // (query, slot) entries in 128-row tiles (128 / hpg entries x hpg heads), on
-// the same cost-balanced contiguous runs of a persistent grid. Per tile, with
-// the block's K and V resident in shared memory for the run of its bin:
-//   1. S^T = K Q^T and dP^T = V dO^T on mma.sync (keys along M); P^T and dS^T
-//      are formed in registers and written to shared memory as bf16;
-//   2. dV += P^T dO and dK += dS^T Q, accumulated in registers over the run's
-//      tiles of one bin (each warp a 16-key strip x a slice of d);
-//   3. dQ = dS K for the tile's rows, stored as a bf16 partial per (entry,
-//      head) row, while the next tile's rows are already being gathered.
-// When a bin's run ends, dK and dV are added into per-sequence fp32
-// accumulators with fire-and-forget vector atomics (a bin held whole by one
-// CTA gets one add per query chunk; a bin split over CTAs gets one per CTA). bwd_dq_combine then sums each row's slot
-// partials in slot order (deterministic) and bwd_kv_store rounds dk and dv.
+// the same cost-balanced contiguous runs of a persistent grid, with the
+// block's K and V resident in shared memory for the run of its bin. Two tile
+// kernels:
+//   bwd_tc_kernel (blocks of 128 keys, tcgen05): keys along M; S^T, dP^T in
+//     TMEM; P^T, dS^T written back over them (A operands of dV, dK); dQ from
+//     dS in shared memory; dV, dK accumulated in TMEM over the bin's run (see
+//     the kernel's own notes below).
+//   bwd_tile_kernel (blocks of 32 or 64 keys, mma.sync): per tile
+//     1. S^T = K Q^T and dP^T = V dO^T (keys along M); P^T and dS^T formed in
+//        registers and written to shared memory as bf16;
+//     2. dV += P^T dO and dK += dS^T Q, accumulated in registers over the run's
+//        tiles of one bin (each warp a 16-key strip x a slice of d);
+//     3. dQ = dS K for the tile's rows while the next tile's rows are gathered.
+// dQ leaves both kernels as a bf16 partial per (entry, head) row. When a bin's
+// run ends, dK and dV are added into per-sequence fp32 accumulators with
+// fire-and-forget vector atomics (a bin held whole by one CTA gets one add per
+// query chunk; a bin split over CTAs gets one per CTA). bwd_dq_combine then
+// sums each row's slot partials in slot order (deterministic) and
+// bwd_kv_store rounds dk and dv.
 #include <cmath>
 
 #include "msa_internal.cuh"

@@ -14,8 +14,8 @@
 // I^T = IK iq^T (128 x entries) land in TMEM, so the epilogue thread of key j
 // holds all heads of every entry in neighbouring columns (the head mean is
 // in-thread). The sums over keys are a reduce-scatter across the warp's lanes
-// (lane l ends with entry l of a group of 32) and a four-warp combine in
-// shared memory. NS epilogue warpgroups (NS = 3 when three TMEM sets of
+// (lanes l and l + 16 end with entry l of a group of 16) and a four-warp
+// merge in shared memory. NS epilogue warpgroups (NS = 3 when three TMEM sets of
 // 128 + E columns fit, else 2) take tiles in turn, each with its own TMEM set
 // and gather ring slot, so the MMAs of the next tiles run under the epilogues.
 // Warps 0..4 NS - 1 epilogue (warpgroup z % NS takes tile z), then two warps
