@@ -421,7 +421,7 @@ def run_msa(args, dist):
             return t0.elapsed_time(t1)
 
         pipeline(2)  # warm-up
-        n_e = max(8, args.steps)  # the pipeline fill (first inputs) and drain (last output) spread over the steps
+        n_e = max(8, 2 * args.steps)  # the pipeline fill (first inputs) and drain (last output) spread over the steps
         # three timed runs of the pipelined loop, the median reported (host
         # copies vary from run to run); each run is n_e full steps
         trials = []
