@@ -160,3 +160,12 @@ def test_backward_128k_properties_and_sampled_rows():
         odq, _, _ = oracle.sparse_attn_backward(q, k, v, g, srow[None], np.zeros(1, np.int32), np.array([r], np.int32),
                                                 qo, kl_, w.Bs, w.K)
         _assert_grad(dq_h[0, r][None], odq, f"dq row {r}", scale_floor=dq_scale)
+
+
+@pytest.mark.parametrize("Bs", [128, 32])
+def test_backward_few_queries(Bs):
+    """Three queries at the end of ragged sequences: a handful of tiles, most
+    CTAs of the persistent grid without work."""
+    w = synth.scaled(BASE, B=2, Nq=3, Nk=260, Bs=Bs, K=4)
+    kl = np.array([260, 200], np.int32)
+    check_case(w, (kl - 3).astype(np.int32), kl)

@@ -106,3 +106,22 @@ def test_kl_aux_128k_sampled_rows():
         want = oracle.kl_aux(q, k, iq, ik, srow[None], np.zeros(1, np.int32), np.array([r], np.int32), qo, kl_, w.Bs,
                              w.K)
         _assert_kl(got[0, r][None], want, f"row {r}")
+
+
+@pytest.mark.parametrize("Bs", [128, 32])
+def test_kl_aux_few_queries(Bs):
+    """Three queries at the end of ragged sequences (most CTAs without tiles)."""
+    torch.cuda.set_device(DEV)
+    w = synth.scaled(BASE, B=2, Nq=3, Nk=260, Bs=Bs, K=4)
+    kl_ = np.array([260, 200], np.int32)
+    qo = (kl_ - 3).astype(np.int32)
+    t = device_inputs(w, DEV)
+    sel, out, lse = gpu_prefill(w, t, DEV, qo, kl_)
+    got = _gpu_kl(w, t, sel, lse, qo, kl_)
+    h = {n: synth.host_tensor(w, n) for n in ("q", "k", "iq", "ik")}
+    rb, ri = oracle.all_rows(w.B, w.Nq)
+    osel = oracle.index_select(h["iq"].reshape(-1, w.G, w.di), h["ik"], rb, ri, qo, kl_, w.Bs, w.K)
+    assert np.array_equal(sel.cpu().numpy().reshape(osel.shape), osel)
+    want = oracle.kl_aux(h["q"].reshape(-1, w.Hq, w.d), h["k"], h["iq"].reshape(-1, w.G, w.di), h["ik"], osel, rb, ri,
+                         qo, kl_, w.Bs, w.K)
+    _assert_kl(got.reshape(want.shape), want, f"few queries Bs {Bs}")
