@@ -72,7 +72,7 @@ __device__ __forceinline__ void kt_rs_sum(float (&v)[kKtEG], int lane) {
   }
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
-// (max, exp-sum) pairs merged the same way (natural-log units; -inf = empty)
+// merge of two (max, exp-sum) pairs (natural-log units; -inf = empty)
 __device__ __forceinline__ void kt_lse_merge(float& m, float& l, float m2, float l2) {
   const float M = fmaxf(m, m2);
   const float a = m == -INFINITY ? 0.f : l * kt_ex2((m - M) * kKtLog2e);
@@ -80,24 +80,6 @@ __device__ __forceinline__ void kt_lse_merge(float& m, float& l, float m2, float
   m = M;
   l = a + b;
 }
-__device__ __forceinline__ void kt_rs_lse(float (&m)[kKtEG], float (&l)[kKtEG], int lane) {
-#pragma unroll
-  for (int o = kKtEG / 2; o >= 1; o >>= 1) {
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float sm = up ? m[i] : m[i + o], sl = up ? l[i] : l[i + o];
-      float km = up ? m[i + o] : m[i], kl = up ? l[i + o] : l[i];
-      const float rm = __shfl_xor_sync(0xffffffffu, sm, o), rl = __shfl_xor_sync(0xffffffffu, sl, o);
-      kt_lse_merge(km, kl, rm, rl);
-      m[i] = km;
-      l[i] = kl;
-    }
-  }
-  const float rm = __shfl_xor_sync(0xffffffffu, m[0], 16), rl = __shfl_xor_sync(0xffffffffu, l[0], 16);
-  kt_lse_merge(m[0], l[0], rm, rl);
-}
-
 template <int HPG>
 struct KtSmem {
   static constexpr int E = kKtRows / HPG;                  // entries per tile
@@ -273,7 +255,18 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
         }
         kt_rs_sum(va, lane);
         kt_rs_sum(vb, lane);
-        kt_rs_lse(vm, vl, lane);
+        // the index scores' log-sum-exp over this warp's 32 keys: the warp
+        // maximum per entry (one redux each, the same value in every lane),
+        // then a plain sum of exp(s - max); warp 0 merges the warps' pairs
+        float mw = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < EG; ++x) {
+          const float m = tc::warp_max_f32(vm[x]);
+          vl[x] = vl[x] > 0.f ? kt_ex2((vm[x] - m) * kKtLog2e) : 0.f;
+          if ((lane & (EG - 1)) == x) mw = m;  // lane l ends with entry l mod 16
+        }
+        kt_rs_sum(vl, lane);
+        vm[0] = mw;
         // the four warps' sums meet in red[buf]; warp 0 merges them (bounded waits, no bar.sync)
         const int buf = gc & 1, rb = wg * 2 + buf;
         if (!tc::mbar_wait(&red_empty[rb], ((gc >> 1) & 1) ^ 1, abort_flag)) {
