@@ -383,7 +383,8 @@ def run_msa(args, dist):
         sets = [dict(t, qo=qo, kl=kl, out=out),
                 dict({n: torch.empty_like(t[n]) for n in t}, qo=torch.empty_like(qo), kl=torch.empty_like(kl),
                      out=torch.empty_like(out))]
-        cstream = torch.cuda.Stream(dev)
+        up = torch.cuda.Stream(dev)    # host -> device: the next step's inputs
+        down = torch.cuda.Stream(dev)  # device -> host: the finished step's output (both directions at once)
 
         def copy_in(k):
             for n in t:
@@ -392,31 +393,39 @@ def run_msa(args, dist):
             sets[k]["kl"].copy_(kl_h, non_blocking=True)
 
         def pipeline(nsteps):
-            ready = [torch.cuda.Event() for _ in range(2)]  # a set's inputs have landed
-            done = [torch.cuda.Event() for _ in range(2)]   # a set's step has finished
+            ready = [torch.cuda.Event() for _ in range(2)]    # a set's inputs have landed
+            done = [torch.cuda.Event() for _ in range(2)]     # a set's step has finished (its inputs are free)
+            drained = [torch.cuda.Event() for _ in range(2)]  # a set's output has been read back
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize(dev)
-            t0.record(cstream)
-            with torch.cuda.stream(cstream):
+            t0.record(stream)
+            up.wait_event(t0)
+            with torch.cuda.stream(up):
                 copy_in(0)
-                ready[0].record(cstream)
+                ready[0].record(up)
             for s_ in range(nsteps):
                 k = s_ % 2
                 S = sets[k]
                 stream.wait_event(ready[k])
+                if s_ >= 2:
+                    stream.wait_event(drained[k])  # step s-2's output in this set has been read back
                 msa.msa_index_select(S["iq"], S["ik"], S["qo"], S["kl"], w.Bs, w.K, sel=sel, ws=ws_i)
                 msa.msa_sparse_attn_prefill(S["q"], S["k"], S["v"], sel, S["qo"], S["kl"], w.Bs, w.K, out=S["out"],
                                             ws=ws_a)
                 done[k].record(stream)
-                with torch.cuda.stream(cstream):
-                    if s_ + 1 < nsteps:
+                if s_ + 1 < nsteps:
+                    with torch.cuda.stream(up):
                         if s_ >= 1:
-                            cstream.wait_event(done[1 - k])  # step s-1 no longer reads the other set
+                            up.wait_event(done[1 - k])  # step s-1 no longer reads the other set
                         copy_in(1 - k)
-                        ready[1 - k].record(cstream)
-                    cstream.wait_event(done[k])
+                        ready[1 - k].record(up)
+                with torch.cuda.stream(down):
+                    down.wait_event(done[k])
                     out_h.copy_(S["out"], non_blocking=True)
-            t1.record(cstream)
+                    drained[k].record(down)
+            stream.wait_stream(up)
+            stream.wait_stream(down)
+            t1.record(stream)
             torch.cuda.synchronize(dev)
             return t0.elapsed_time(t1)
 
@@ -433,7 +442,8 @@ def run_msa(args, dist):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_tot * 1e3 / n_e, 4), "steps": n_e,
                "trials_ms_per_step": [round(x * 1e3 / n_e, 4) for x in trials], "statistic": "median of 3 runs",
-               "copies": "pinned host buffers, a copy stream overlapping step s+1's inputs with step s"}
+               "copies": "pinned host buffers; an upload stream copies step s+1's inputs and a download stream reads "
+                         "step s-1's output back while step s computes"}
         del host, out_h, sets
 
     torch.cuda.empty_cache()
