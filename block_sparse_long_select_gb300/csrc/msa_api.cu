@@ -84,6 +84,12 @@ inline msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_O
 
 inline uint32_t* status_word(void* ws) { return &static_cast<WsHeader*>(ws)->status; }
 
+// An empty batch: B == 0, or Nq == 0 for an entry point with query rows.
+// Nothing is read or computed; the other arguments are still checked as for a
+// batch of one row, so an unsupported configuration fails the same way.
+inline bool empty_batch(int B, int Nq) { return B >= 0 && Nq >= 0 && (B == 0 || Nq == 0); }
+inline int one_key_min(int Nk) { return Nk < 0 ? Nk : std::max(Nk, 1); }
+
 // Streaming decode step: one workspace holds the status header, the new
 // tokens' positions, the index scratch and the attention scratch.
 struct StepPlan {
@@ -122,6 +128,12 @@ using namespace msa;
 
 extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K,
                                      int dtype) {
+  const bool rowless = op == MSA_OP_DECODE || op == MSA_OP_DECODE_STEP;  // Nq is ignored
+  if (empty_batch(B, rowless ? 1 : Nq)) {
+    // only the status header, if the call is valid for one row
+    const size_t one = msa_workspace_size(op, 1, 1, one_key_min(Nk), G, Hq, d, di, Bs, K, dtype);
+    return one ? kWsHeader : 0;
+  }
   switch (op) {
     case MSA_OP_INDEX_SELECT: {
       IndexPlan p = plan_index(B, Nq, Nk, G, di, Bs, K, dtype, false);
@@ -159,10 +171,14 @@ extern "C" msa_status_t msa_index_select_v(const void* iq, const void* ik, const
                                            const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs, int K,
                                            int dtype, int force, int32_t* sel, float* block_max, void* ws,
                                            size_t ws_bytes, cudaStream_t stream) {
-  if (!iq || !ik || !sel) return MSA_ERR_INVALID_ARG;
   if (force != MSA_FORCE_LOCAL && force != (MSA_FORCE_LOCAL | MSA_FORCE_START)) return MSA_ERR_INVALID_ARG;
   const int fs = (force & MSA_FORCE_START) ? 1 : 0;  // block 0 kept as well
   if (fs && K < 2) return MSA_ERR_INVALID_ARG;
+  if (empty_batch(B, Nq)) {
+    const IndexPlan one = plan_index(1, 1, one_key_min(Nk), G, di, Bs, K, dtype, false);
+    return one.ok ? MSA_OK : one.err;
+  }
+  if (!iq || !ik || !sel) return MSA_ERR_INVALID_ARG;
   IndexPlan p = plan_index(B, Nq, Nk, G, di, Bs, K, dtype, block_max != nullptr);
   if (!p.ok) return p.err;
   msa_status_t w = check_ws(ws, ws_bytes, block_max ? kWsHeader : p.ws_bytes);
@@ -197,6 +213,10 @@ extern "C" msa_status_t msa_sparse_attn_prefill(const void* q, const void* k, co
                                                 int Hq, int Hkv, int d, int Bs, int K, float scale, int dtype,
                                                 void* out, float* lse, void* ws, size_t ws_bytes,
                                                 cudaStream_t stream) {
+  if (empty_batch(B, Nq)) {
+    const AttnPlan one = plan_attn(1, 1, one_key_min(Nk), Hq, Hkv, d, Bs, K, dtype, true);
+    return one.ok ? MSA_OK : one.err;
+  }
   if (!q || !k || !v || !sel || !out) return MSA_ERR_INVALID_ARG;
   AttnPlan p = plan_attn(B, Nq, Nk, Hq, Hkv, d, Bs, K, dtype, true);
   if (!p.ok) return p.err;
@@ -215,6 +235,10 @@ extern "C" msa_status_t msa_sparse_attn_decode(const void* q, const void* k_cach
                                                const int32_t* sel, const int32_t* kv_len, int B, int Lmax, int Hq,
                                                int Hkv, int d, int Bs, int K, float scale, int dtype, void* out,
                                                float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (empty_batch(B, 1)) {
+    const AttnPlan one = plan_attn(1, 1, Lmax, Hq, Hkv, d, Bs, K, dtype, false);
+    return one.ok ? MSA_OK : one.err;
+  }
   if (!q || !k_cache || !v_cache || !sel || !kv_len || !out) return MSA_ERR_INVALID_ARG;
   AttnPlan p = plan_attn(B, 1, Lmax, Hq, Hkv, d, Bs, K, dtype, false);
   if (!p.ok) return p.err;
@@ -234,9 +258,13 @@ extern "C" msa_status_t msa_decode_step(const void* q, const void* k_new, const 
                                         int32_t* kv_len, int B, int Lmax, int Hq, int Hkv, int d, int di, int Bs,
                                         int K, float scale, int dtype, int32_t* sel, void* out, float* lse, void* ws,
                                         size_t ws_bytes, cudaStream_t stream) {
+  if (Hkv < 1 || Hq % Hkv != 0) return MSA_ERR_INVALID_ARG;
+  if (empty_batch(B, 1)) {
+    const StepPlan one = plan_step(1, Lmax, Hkv, Hq, d, di, Bs, K, dtype);
+    return one.ok ? MSA_OK : one.err;
+  }
   if (!q || !k_new || !v_new || !iq || !ik_new || !k_cache || !v_cache || !ik_cache || !kv_len || !sel || !out)
     return MSA_ERR_INVALID_ARG;
-  if (Hkv < 1 || Hq % Hkv != 0) return MSA_ERR_INVALID_ARG;
   StepPlan p = plan_step(B, Lmax, Hkv, Hq, d, di, Bs, K, dtype);
   if (!p.ok) return p.err;
   msa_status_t w = check_ws(ws, ws_bytes, p.ws_bytes);
@@ -274,6 +302,11 @@ extern "C" msa_status_t msa_kl_aux_forward(const void* q, const void* k, const v
                                            const int32_t* kv_len, int B, int Nq, int Nk, int Hq, int Hkv, int d, int di,
                                            int Bs, int K, float scale, int dtype, float* kl, void* ws,
                                            size_t ws_bytes, cudaStream_t stream) {
+  if (empty_batch(B, Nq)) {
+    if (Nk < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || K < 1 || Bs < 1 || !dtype_ok(dtype))
+      return MSA_ERR_INVALID_ARG;
+    return kl_aux_supported(dtype, Hq, Hkv, d, di, Bs, K) ? MSA_OK : MSA_ERR_UNSUPPORTED;
+  }
   if (!q || !k || !iq || !ik || !sel || !lse || !kl) return MSA_ERR_INVALID_ARG;
   if (B < 1 || Nq < 1 || Nk < 1 || Nq > Nk || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || K < 1 || Bs < 1 ||
       !dtype_ok(dtype))
@@ -292,6 +325,17 @@ extern "C" msa_status_t msa_sparse_attn_backward(const void* q, const void* k, c
                                                  int Nk, int Hq, int Hkv, int d, int Bs, int K, float scale,
                                                  int dtype, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                                                  cudaStream_t stream) {
+  if (empty_batch(B, Nq)) {
+    if (Nk < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || K < 1 || Bs < 1 || !dtype_ok(dtype))
+      return MSA_ERR_INVALID_ARG;
+    if (!attn_backward_supported(dtype, Hq, Hkv, d, Bs, K)) return MSA_ERR_UNSUPPORTED;
+    const size_t kv_bytes = size_t(B) * Nk * Hkv * d * 2;  // bf16
+    if (kv_bytes == 0) return MSA_OK;
+    // keys that no query reaches: dk = dv = 0
+    if (!dk || !dv) return MSA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(dk, 0, kv_bytes, stream) != cudaSuccess) return MSA_ERR_CUDA;
+    return cuda_status(cudaMemsetAsync(dv, 0, kv_bytes, stream));
+  }
   if (!q || !k || !v || !out || !dout || !lse || !sel || !dq || !dk || !dv) return MSA_ERR_INVALID_ARG;
   if (B < 1 || Nq < 1 || Nk < 1 || Nq > Nk || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || K < 1 || Bs < 1 ||
       !dtype_ok(dtype))

@@ -39,6 +39,13 @@
  *    Per-sequence values (q_offset, kv_len, sel entries) live on the device
  *    and are checked there: an offending row is skipped (its sel row is -1,
  *    its output row zero) and the status becomes MSA_ERR_BOUNDS.
+ *  - An empty batch (B == 0, or Nq == 0 for an entry point with query rows)
+ *    is valid. The other arguments are checked as for a batch of one row,
+ *    pointers (ws included) may be NULL and are not read, nothing is
+ *    enqueued, and the call returns MSA_OK. The one exception:
+ *    msa_sparse_attn_backward with B * Nk > 0 and Nq == 0 zero-fills dk and
+ *    dv (no query reaches any key), so those two must be given.
+ *    msa_workspace_size returns 256 for an empty batch.
  */
 #ifndef MSA_H_
 #define MSA_H_
@@ -78,7 +85,7 @@ typedef enum {
  * MSA_OP_DECODE_STEP, Nq is ignored and Nk is Lmax; MSA_OP_DECODE_STEP uses
  * every other argument, with G = Hkv; MSA_OP_KL_AUX and MSA_OP_BACKWARD use
  * all but di, with G = Hkv). Returns 0 when the arguments are invalid or not
- * supported. */
+ * supported, and 256 for a valid empty batch. */
 size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K, int dtype);
 
 /* Index Branch: block selection for every (query row, group).

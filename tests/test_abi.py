@@ -48,8 +48,9 @@ def test_workspace_size(lib):
     assert ws >= 256 and ws % 256 == 0
     assert msa.msa_workspace_size(msa.MSA_OP_PREFILL, 1, 8192, 8192, 8, 32, 128, 0, 128, 16, msa.MSA_BF16) >= 256
     assert msa.msa_workspace_size(msa.MSA_OP_DECODE, 64, 1, 131072, 8, 32, 128, 0, 128, 16, msa.MSA_BF16) >= 256
-    # invalid: zero batch, Hq not a multiple of Hkv, unknown op
-    assert msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, 0, 512, 512, 2, 0, 0, 32, 32, 4, 1) == 0
+    # invalid: negative batch, Hq not a multiple of Hkv, unknown op (an empty batch is valid: 256)
+    assert msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, -1, 512, 512, 2, 0, 0, 32, 32, 4, 1) == 0
+    assert msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, 0, 512, 512, 2, 0, 0, 32, 32, 4, 1) == 256
     assert msa.msa_workspace_size(msa.MSA_OP_PREFILL, 1, 64, 64, 3, 8, 64, 0, 32, 4, 1) == 0
     assert msa.msa_workspace_size(7, 1, 64, 64, 2, 8, 64, 32, 32, 4, 1) == 0
 
@@ -114,3 +115,48 @@ def test_kl_and_backward_host_validation(lib):
     assert bwd(Hq=32, Hkv=2) == 2      # 16 heads per group: beyond the built ratios
     assert bwd(dtype=msa.MSA_FP32) == 2  # bf16 only
     assert bwd(ws_bytes=16) == 3       # workspace too small
+
+
+def test_empty_batches_on_the_host(lib):
+    """B == 0 or Nq == 0: valid, nothing read (NULL pointers), nothing enqueued;
+    the other arguments are still checked. Runs without a GPU: no CUDA call is
+    made on these paths."""
+    bf16 = msa.MSA_BF16
+    for op in (msa.MSA_OP_INDEX_SELECT, msa.MSA_OP_PREFILL, msa.MSA_OP_KL_AUX, msa.MSA_OP_BACKWARD):
+        assert msa.msa_workspace_size(op, 0, 64, 64, 2, 8, 128, 64, 128, 4, bf16) == 256
+        assert msa.msa_workspace_size(op, 2, 0, 64, 2, 8, 128, 64, 128, 4, bf16) == 256
+        assert msa.msa_workspace_size(op, -1, 64, 64, 2, 8, 128, 64, 128, 4, bf16) == 0
+        assert msa.msa_workspace_size(op, 0, 64, 64, 2, 8, 96, 48, 128, 4, bf16) == 0  # d 96 / di 48 not built
+    for op in (msa.MSA_OP_DECODE, msa.MSA_OP_DECODE_STEP):
+        assert msa.msa_workspace_size(op, 0, 0, 64, 2, 8, 128, 64, 128, 4, bf16) == 256
+    N = None
+    # index selection: empty batch, empty rows; unsupported di and bad force still fail
+    assert lib.msa_index_select(N, N, N, N, 0, 8, 8, 1, 32, 4, 2, 1, N, N, N, 0, N) == 0
+    assert lib.msa_index_select(N, N, N, N, 3, 0, 8, 1, 32, 4, 2, 1, N, N, N, 0, N) == 0
+    assert lib.msa_index_select(N, N, N, N, 0, 8, 8, 1, 48, 4, 2, 1, N, N, N, 0, N) == 2
+    assert lib.msa_index_select(N, N, N, N, -1, 8, 8, 1, 32, 4, 2, 1, N, N, N, 0, N) == 1
+    assert lib.msa_index_select_v(N, N, N, N, 0, 8, 8, 1, 32, 4, 1, 1, 3, N, N, N, 0, N) == 1  # START needs K >= 2
+    assert lib.msa_index_select_noalloc(N, N, N, N, 0, 8, 8, 1, 32, 4, 2, 1, N, N, N) == 0
+    assert lib.msa_index_select_noalloc(N, N, N, N, 0, 8, 8, 1, 48, 4, 2, 1, N, N, N) == 2
+    # attention
+    assert lib.msa_sparse_attn_prefill(N, N, N, N, N, N, 0, 8, 8, 8, 2, 64, 4, 2, 0.0, 1, N, N, N, 0, N) == 0
+    assert lib.msa_sparse_attn_prefill(N, N, N, N, N, N, 2, 0, 8, 8, 2, 64, 4, 2, 0.0, 1, N, N, N, 0, N) == 0
+    assert lib.msa_sparse_attn_prefill(N, N, N, N, N, N, 0, 8, 8, 6, 4, 64, 4, 2, 0.0, 1, N, N, N, 0, N) == 1
+    assert lib.msa_sparse_attn_prefill(N, N, N, N, N, N, 0, 8, 8, 8, 2, 96, 4, 2, 0.0, 1, N, N, N, 0, N) == 2
+    assert lib.msa_sparse_attn_decode(N, N, N, N, N, 0, 8, 8, 2, 64, 4, 2, 0.0, 1, N, N, N, 0, N) == 0
+    assert lib.msa_decode_step(N, N, N, N, N, N, N, N, N, 0, 64, 8, 2, 64, 32, 16, 2, 0.0, 1, N, N, N, N, 0,
+                               N) == 0
+    # KL and backward (B == 0: nothing at all to write)
+    assert lib.msa_kl_aux_forward(N, N, N, N, N, N, N, N, 0, 8, 8, 8, 2, 128, 64, 128, 2, 0.0, bf16, N, N, 0,
+                                  N) == 0
+    assert lib.msa_kl_aux_forward(N, N, N, N, N, N, N, N, 2, 0, 8, 8, 2, 128, 64, 128, 2, 0.0, bf16, N, N, 0,
+                                  N) == 0
+    assert lib.msa_kl_aux_forward(N, N, N, N, N, N, N, N, 0, 8, 8, 8, 2, 96, 64, 128, 2, 0.0, bf16, N, N, 0,
+                                  N) == 2
+    bwd = lambda B, Nq, Nk, d=128, dtype=bf16: lib.msa_sparse_attn_backward(  # noqa: E731
+        N, N, N, N, N, N, N, N, N, B, Nq, Nk, 8, 2, d, 128, 2, 0.0, dtype, N, N, N, N, 0, N)
+    assert bwd(0, 8, 8) == 0
+    assert bwd(2, 0, 0) == 0
+    assert bwd(2, 0, 8) == 1            # keys but no queries: dk and dv are zero-filled, so they must be given
+    assert bwd(0, 8, 8, d=96) == 2
+    assert bwd(0, 8, 8, dtype=msa.MSA_FP32) == 2

@@ -208,3 +208,51 @@ def test_force_start_decode(name):
     w = synth.scaled(synth.WORKLOADS["decode_b64"], **FORCE_START_DECODE[name])
     kl = synth.kv_lens(w)
     _force_start_check(w, (kl - 1).astype(np.int32), kl)
+
+
+def test_empty_batches():
+    """An empty batch through every entry point: zero-size outputs, no device
+    error; the backward with keys but no queries gives dk = dv = 0 (the
+    oracle's gradients of zero listed rows)."""
+    import block_sparse_long_select_gb300 as msa
+    import oracle
+
+    bf, i32 = torch.bfloat16, torch.int32
+    e = lambda *s, dt=bf: torch.empty(s, dtype=dt, device=DEV)  # noqa: E731
+    B, Nk, Hq, Hkv, d, di, Bs, K = 2, 300, 8, 2, 128, 64, 128, 2
+    kl = torch.full((B,), Nk, dtype=i32, device=DEV)
+    qo0 = torch.zeros(B, dtype=i32, device=DEV)
+    for b, nq in ((0, 16), (B, 0)):
+        sel = msa.msa_index_select(e(b, nq, Hkv, di), e(b, Nk, di), qo0[:b], kl[:b], Bs, K)
+        assert tuple(sel.shape) == (b, nq, Hkv, K)
+        sel_v = msa.msa_index_select_v(e(b, nq, Hkv, di), e(b, Nk, di), qo0[:b], kl[:b], Bs, K,
+                                       msa.MSA_FORCE_LOCAL | msa.MSA_FORCE_START)
+        assert sel_v.numel() == 0
+        lse = e(b, nq, Hq, dt=torch.float32)
+        out = msa.msa_sparse_attn_prefill(e(b, nq, Hq, d), e(b, Nk, Hkv, d), e(b, Nk, Hkv, d), sel, qo0[:b], kl[:b],
+                                          Bs, K, lse=lse)
+        assert tuple(out.shape) == (b, nq, Hq, d)
+        klv = msa.msa_kl_aux_forward(e(b, nq, Hq, d), e(b, Nk, Hkv, d), e(b, nq, Hkv, di), e(b, Nk, di), sel, lse,
+                                     qo0[:b], kl[:b], Bs, K)
+        assert tuple(klv.shape) == (b, nq, Hkv)
+    out = msa.msa_sparse_attn_decode(e(0, Hq, d), e(0, Nk, Hkv, d), e(0, Nk, Hkv, d), e(0, Hkv, K, dt=i32),
+                                     kl[:0], Bs, K)
+    assert out.numel() == 0
+    sel, out = msa.msa_decode_step(e(0, Hq, d), e(0, Hkv, d), e(0, Hkv, d), e(0, Hkv, di), e(0, di),
+                                   e(0, Nk, Hkv, d), e(0, Nk, Hkv, d), e(0, Nk, di), kl[:0], Bs, K)
+    assert sel.numel() == 0 and out.numel() == 0
+    # backward of a batch with keys but no query rows
+    k = synth.device_tensor(synth.scaled(BASE, B=B, Nq=1, Nk=Nk, Hq=Hq, Hkv=Hkv, Bs=Bs, K=K), "k", DEV)
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(k, float("nan"))
+    dq, dk, dv = msa.msa_sparse_attn_backward(e(B, 0, Hq, d), k, k, e(B, 0, Hq, d), e(B, 0, Hq, d),
+                                              e(B, 0, Hq, dt=torch.float32), e(B, 0, Hkv, K, dt=i32), qo0, kl, Bs, K,
+                                              dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    z = np.zeros((0, Hq, d), np.float32)
+    kh = k.float().cpu().numpy()
+    _, odk, odv = oracle.sparse_attn_backward(z, kh, kh, z, np.zeros((0, Hkv, K), np.int32), np.zeros(0, np.int32),
+                                              np.zeros(0, np.int32), np.zeros(B, np.int32), np.full(B, Nk, np.int32),
+                                              Bs, K)
+    assert dq.numel() == 0
+    assert np.array_equal(dk.float().cpu().numpy(), odk) and np.array_equal(dv.float().cpu().numpy(), odv)
