@@ -24,6 +24,13 @@ SMALL = {
     "bf16_d64_di32": synth.scaled(BASE, B=2, Nq=640, Nk=640, Hq=8, Hkv=2, d=64, di=32, Bs=64, K=5),
     "bf16_hot_blocks": synth.scaled(BASE, B=1, Nq=2048, Nk=2048, Bs=32, K=16, hot="first4"),
     "bf16_single_row": synth.scaled(BASE, B=1, Nq=1, Nk=1, Bs=128, K=16),
+    # head ratios beyond 8 (tensor-core attention takes up to hpg * d = 2048)
+    "bf16_hpg16": synth.scaled(BASE, B=1, Nq=600, Nk=600, Hq=32, Hkv=2, Bs=64, K=4),
+    "bf16_hpg32_d64": synth.scaled(BASE, B=1, Nq=1100, Nk=1100, Hq=32, Hkv=1, d=64, di=32, Bs=128, K=3),
+    # block sizes outside the tensor-core builds: the table index path and the CUDA-core attention
+    "bf16_bs100_generic": synth.scaled(BASE, B=2, Nq=900, Nk=900, Hq=8, Hkv=2, Bs=100, K=5),
+    "bf16_bs1_k64_tokens": synth.scaled(BASE, B=1, Nq=300, Nk=300, Hq=8, Hkv=2, Bs=1, K=64),
+    "bf16_bs1024_k2": synth.scaled(BASE, B=1, Nq=2500, Nk=2500, Hq=8, Hkv=2, Bs=1024, K=2),
 }
 
 
@@ -117,6 +124,8 @@ DECODE_VARIANTS = {
     "bs128_hpg2_d64_di32": dict(Bs=128, K=6, Hq=8, Hkv=4, d=64, di=32),
     # K - 1 > 32: the warp top-K takes its exact radix path instead of the lane-maximum filter
     "bs32_k40_radix": dict(Bs=32, K=40),
+    # a block size outside the decode kernels' builds: table index path, CUDA-core attention
+    "bs100_generic": dict(Bs=100, K=5),
 }
 
 
@@ -131,6 +140,20 @@ def test_decode_variants(name):
     assert np.array_equal(sel.cpu().numpy(), osel), name
     assert_close(out.float().cpu().numpy(), oout[:, 0], "bf16", name)
     assert_close(lse.cpu().numpy(), olse[:, 0], "bf16", name, lse=True)
+
+
+def test_decode_batch_beyond_index_kernel():
+    """1025 sequences: one more than the decode index kernel's per-CTA sequence table, so the
+    selection takes the table path; the split attention kernel serves any batch."""
+    w = synth.scaled(synth.WORKLOADS["decode_b64"], B=1025, Nk=160, kv_len_range=(1, 160), Hq=8, Hkv=2, d=64,
+                     Bs=32, K=4)
+    t = device_inputs(w, DEV)
+    sel, out, lse = gpu_decode(w, t, DEV)
+    h = host_inputs(w)
+    osel, oout, olse = oracle_full(w, h)
+    assert np.array_equal(sel.cpu().numpy(), osel)
+    assert_close(out.float().cpu().numpy(), oout[:, 0], "bf16", w.name)
+    assert_close(lse.cpu().numpy(), olse[:, 0], "bf16", w.name, lse=True)
 
 
 def test_decode_long_rows_cta_topk():
