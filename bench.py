@@ -40,7 +40,7 @@ KERNEL_SOURCES = {  # kernel name -> source file (for the ncu traffic freshness 
     "attn_query_outer": "attn_query_outer.cu", "index_fused_tc": "index_fused_tc.cu",
     "attn_kv_outer_tc": "attn_kv_outer_tc.cu", "attn_invert": "attn_kv_outer_tc.cu",
     "attn_combine": "attn_kv_outer_tc.cu", "decode_index": "decode.cu", "decode_topk": "decode.cu",
-    "decode_attn": "decode.cu", "decode_combine": "decode.cu", "kl_tile": "attn_kv_outer_tc.cu",
+    "decode_attn": "decode.cu", "kl_tile": "attn_kv_outer_tc.cu",
     "kl_combine": "attn_kv_outer_tc.cu", "bwd_tile": "attn_backward.cu", "bwd_dq_combine": "attn_backward.cu",
     "kl_tile_tc": "kl_tc.cu", "bwd_tile_tc": "attn_backward.cu",
 }
