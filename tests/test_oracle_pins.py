@@ -389,6 +389,33 @@ def pin_kl_aux(lib=None):
     assert np.abs(kl2 - kl).max() < 1e-9 * max(1.0, np.abs(kl).max())
 
 
+GOLDEN_KL = os.path.join(os.path.dirname(__file__), "golden", "handworked_kl.txt")
+
+
+def pin_kl_golden(lib=None):
+    """The hand-worked KL values of tests/golden/handworked_kl.txt: two heads
+    with different distributions (their probabilities averaged), unequal index
+    scores, and a row with a single visible token."""
+    k = np.array([0.0, math.log(3.0)], np.float32).reshape(1, 2, 1, 1)
+    ik = np.array([0.0, 1.0], np.float32).reshape(1, 2, 1)
+    n = 0
+    with open(GOLDEN_KL) as f:
+        for ln in f:
+            ln = ln.split("#")[0].strip()
+            if not ln:
+                continue
+            head, _, tail = ln.partition(":")
+            parts = head.split()
+            assert parts[0] == "kl", ln
+            pos, q0, q1, iqv = int(parts[1]), float(parts[2]), float(parts[3]), float(parts[4])
+            want = float(tail)
+            got = oracle.kl_aux(np.array([[[q0], [q1]]], np.float32), k, np.array([[[iqv]]], np.float32), ik,
+                                np.array([[[0]]], np.int32), [0], [pos], [0], [2], 2, 1, scale=1.0, lib=lib)
+            assert abs(got[0, 0] - want) < 1e-7, (ln, got[0, 0])
+            n += 1
+    assert n == 3
+
+
 def _bwd_inputs(seed, B=2, Nq=40, Nk=96, Hq=4, Hkv=2, d=16, Bs=8, K=5):
     q, k, v, iq, ik, qo, kl = rand_problem(seed, B=B, Nq=Nq, Nk=Nk, Hq=Hq, Hkv=Hkv, d=d, di=8,
                                            q_offset=[Nk - Nq, 20], kv_len=[Nk, Nq + 20])
@@ -466,7 +493,7 @@ def pin_attn_backward(lib=None):
 
 PINS = [pin_golden, pin_blockmax_bruteforce, pin_selection_invariants, pin_closed_forms, pin_dense_equals_sdpa,
         pin_masked_dense_equals_sdpa, pin_attention_special_cases, pin_decode_equals_prefill_row, pin_force_start,
-        pin_kl_aux, pin_attn_backward]
+        pin_kl_aux, pin_kl_golden, pin_attn_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
