@@ -546,3 +546,22 @@ def test_planted_mistake_is_caught(name, tmp_path):
         except (AssertionError, ValueError, IndexError):
             failed.append(pin.__name__)
     assert failed, f"mutation {name} passed every pin"
+
+
+def test_oracle_independent_of_thread_count():
+    """Every oracle function gives bit-identical results on 1 and 4 threads
+    (rows are independent; the backward's dk / dv sums keep a fixed order), so
+    the timed CPU baseline and the parity references are the same computation."""
+    q, k, v, iq, ik, qo, kl = rand_problem(7, B=2, Nq=40, Nk=96, q_offset=[56, 20], kv_len=[96, 60])
+    rb, ri = oracle.all_rows(2, 40)
+    g = np.random.default_rng(1).standard_normal(q.shape).astype(np.float32)
+    res = []
+    for nt in (1, 4):
+        sel = oracle.index_select(iq.reshape(-1, 2, 8), ik, rb, ri, qo, kl, 8, 5, nthreads=nt)
+        out, lse = oracle.sparse_attn(q.reshape(-1, 4, 16), k, v, sel, rb, ri, qo, kl, 8, 5, nthreads=nt)
+        klv = oracle.kl_aux(q.reshape(-1, 4, 16), k, iq.reshape(-1, 2, 8), ik, sel, rb, ri, qo, kl, 8, 5, nthreads=nt)
+        grads = oracle.sparse_attn_backward(q.reshape(-1, 4, 16), k, v, g.reshape(-1, 4, 16), sel, rb, ri, qo, kl, 8,
+                                            5, nthreads=nt)
+        res.append((sel, out, lse, klv) + tuple(grads))
+    for a, b in zip(*res):
+        assert np.array_equal(a, b)
