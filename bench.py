@@ -620,6 +620,9 @@ def run_msa(args, dist):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # ---------------------------------------------------------------------------
+_KV_HOST = {}  # (Nk, Hkv, d) -> zero-filled host K / V of one sequence, reused across calls
+
+
 def oracle_prefill_rows(w, rows, ik_host):
     """Oracle index select + attention for the listed rows of sequence 0.
     Returns seconds spent inside the oracle (input generation excluded)."""
@@ -633,16 +636,21 @@ def oracle_prefill_rows(w, rows, ik_host):
     t0 = time.perf_counter()
     sel = oracle.index_select(iq, ik_host, rb, rows, qo, kl, w.Bs, w.K)
     t1 = time.perf_counter()
-    k = np.zeros((1, w.Nk, w.Hkv, w.d), np.float32)
-    v = np.zeros((1, w.Nk, w.Hkv, w.d), np.float32)
+    key = (w.Nk, w.Hkv, w.d)
+    if key not in _KV_HOST:
+        _KV_HOST[key] = (np.zeros((1, w.Nk, w.Hkv, w.d), np.float32), np.zeros((1, w.Nk, w.Hkv, w.d), np.float32))
+    k, v = _KV_HOST[key]
     row = w.Hkv * w.d
-    for tb in sorted(set(int(x) for x in sel.reshape(-1) if x >= 0)):
-        j0, j1 = tb * w.Bs, min((tb + 1) * w.Bs, w.Nk)
+    spans = [(tb * w.Bs, min((tb + 1) * w.Bs, w.Nk)) for tb in sorted(set(int(x) for x in sel.reshape(-1) if x >= 0))]
+    for j0, j1 in spans:  # only the selected blocks are filled (the oracle reads no others)
         k[0, j0:j1] = synth.host_range(w, "k", j0 * row, (j1 - j0) * row).reshape(j1 - j0, w.Hkv, w.d)
         v[0, j0:j1] = synth.host_range(w, "v", j0 * row, (j1 - j0) * row).reshape(j1 - j0, w.Hkv, w.d)
     t2 = time.perf_counter()
     oracle.sparse_attn(q, k, v, sel, rb, rows, qo, kl, w.Bs, w.K)
     t3 = time.perf_counter()
+    for j0, j1 in spans:  # back to zeros for the next call
+        k[0, j0:j1] = 0.0
+        v[0, j0:j1] = 0.0
     return (t1 - t0) + (t3 - t2)
 
 
