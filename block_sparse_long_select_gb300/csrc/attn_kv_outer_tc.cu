@@ -27,10 +27,9 @@
 //                   atomics on any output.
 //
 // attn_kv_outer warp roles (512 threads): warp 0 K/V TMA producer, warps 1-4
-// query-row gather by cp.async (one ring slot each, rows 0-79), warp 6
-// query-row gather by four-row TMA gathers (rows 80-127 of every slot; the
-// next tile's entries are fetched while the current one is issued), warp 5
-// TMEM owner + MMA issuer, warp 7 idle; warps 8-15 two epilogue warpgroups that
+// query-row gather (one ring slot each; per tile, four-row TMA gathers for
+// rows 80-127 and cp.async for rows 0-79, entries fetched a ring ahead), warp 5
+// TMEM owner + MMA issuer, warps 6-7 idle; warps 8-15 two epilogue warpgroups that
 // alternate tiles (ping-pong), each owning S (Bs columns) and O (D columns) in
 // TMEM. Warpgroups 0-1 hand registers to the epilogue (88 -> 168 per thread)
 // so that a whole S row and a whole O row are read from TMEM at once. All
@@ -52,7 +51,6 @@ constexpr int kProdRegs = 88, kEpiRegs = 168;
 static_assert(256 * kProdRegs + 256 * kEpiRegs <= kAttnThreads * kLaunchRegs, "register split");
 constexpr int kKvWarp = 0;
 constexpr int kGatherWarp0 = 1;  // warps 1..4: cp.async gathers
-constexpr int kTmaGatherWarp = 6;  // TMA gathers
 constexpr int kMmaWarpA = 5;
 constexpr int kEpiWarp0 = 8;  // warps 8..15 (warpgroups 2 and 3)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -97,15 +95,38 @@ __global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t
 constexpr int kCostTile = 32, kCostBin = 17, kCostMasked = 8;
 constexpr int kMaxGrid = kKvoMaxGrid;  // persistent grid: one CTA per SM
 
+// The tile where a cost prefix reaches X, searching bins [blo, bhi] (the last
+// bin whose cost offset is <= X, then a proportional share of its tiles).
+__device__ int split_tile(const int* __restrict__ cost_off, const int* __restrict__ tile_off, int blo, int bhi,
+                          int64_t X) {
+  while (blo < bhi) {
+    const int mid = (blo + bhi + 1) >> 1;
+    if (cost_off[mid] <= X)
+      blo = mid;
+    else
+      bhi = mid - 1;
+  }
+  const int nt = tile_off[blo + 1] - tile_off[blo];
+  const int64_t c = int64_t(cost_off[blo + 1]) - cost_off[blo];
+  const int64_t kq = c > 0 ? (X - cost_off[blo]) * nt / c : 0;
+  return tile_off[blo] + (kq < nt ? int(kq) : nt);
+}
+
 // single CTA of 1024 threads: tile offsets, entry offsets (= tile offset x
 // entries per tile: every tile owns a full slot range), tile total, and the
-// persistent grid's split: CTA j takes tiles [cta_start[j], cta_start[j+1]),
-// contiguous runs of equal estimated cost.
+// persistent grid's splits:
+//  - cta_start: CTA j takes tiles [cta_start[j], cta_start[j+1]), contiguous
+//    runs of equal estimated cost (the KL and backward passes);
+//  - cta_seg [nph][grid + 1]: phase p (the bins of groups
+//    [p G / nph, (p+1) G / nph)) split the same way on its own, so that CTA j
+//    takes a 1/grid share of every phase, phase after phase (the forward
+//    attention: all CTAs gather the query rows of the same groups at a time).
 __global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__ cnt, const int32_t* __restrict__ q_offset,
                                                          int b, int nblk, int nbins, int per_tile, int Bs, int c0,
-                                                         int cq, int grid, int* __restrict__ entry_off,
+                                                         int cq, int grid, int G, int nph, int* __restrict__ entry_off,
                                                          int* __restrict__ tile_off, int* __restrict__ cost_off,
-                                                         int* __restrict__ total_tiles, int* __restrict__ cta_start) {
+                                                         int* __restrict__ total_tiles, int* __restrict__ cta_start,
+                                                         int* __restrict__ cta_seg) {
   __shared__ int s_e[1024], s_t[1024], s_c[1024];
   const int tid = threadIdx.x;
   const int per = (nbins + 1023) / 1024;
@@ -158,25 +179,13 @@ __global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__
   // CTA j starts at the tile where the cost prefix reaches total * j / grid
   const int64_t ctot = s_c[1023];
   const int ttot = s_t[1023];
-  for (int j = tid; j <= grid; j += 1024) {
-    if (j == grid) {
-      cta_start[j] = ttot;
-      continue;
-    }
-    const int64_t X = ctot * j / grid;
-    int lo_b = 0, hi_b = nbins - 1;  // the last bin with cost_off <= X
-    while (lo_b < hi_b) {
-      const int mid = (lo_b + hi_b + 1) >> 1;
-      if (cost_off[mid] <= X)
-        lo_b = mid;
-      else
-        hi_b = mid - 1;
-    }
-    const int nt = tile_off[lo_b + 1] - tile_off[lo_b];
-    const int64_t c = int64_t(cost_off[lo_b + 1]) - cost_off[lo_b];
-    const int64_t kq = c > 0 ? (X - cost_off[lo_b]) * nt / c : 0;
-    const int k = kq < nt ? int(kq) : nt;
-    cta_start[j] = tile_off[lo_b] + k;
+  for (int j = tid; j <= grid; j += 1024)
+    cta_start[j] = j == grid ? ttot : split_tile(cost_off, tile_off, 0, nbins - 1, ctot * j / grid);
+  for (int x = tid; x < nph * (grid + 1); x += 1024) {
+    const int ph = x / (grid + 1), j = x % (grid + 1);
+    const int blo = (ph * G / nph) * nblk, bhi = ((ph + 1) * G / nph) * nblk;  // bins [blo, bhi)
+    const int64_t c0p = cost_off[blo], c1p = cost_off[bhi];
+    cta_seg[x] = j == grid ? tile_off[bhi] : split_tile(cost_off, tile_off, blo, bhi - 1, c0p + (c1p - c0p) * j / grid);
   }
 }
 
@@ -247,6 +256,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -258,14 +272,28 @@ struct AttnParams {
   uint4* part_o;           // [tiles][D / 8 chunks][128 rows] x 16 bytes (8 bf16)
   const int* entries;      // chunk entries
   const int4* tiles;       // chunk tiles
-  const int* cta_start;    // [grid + 1]: this CTA's tiles are [cta_start[j], cta_start[j + 1])
+  const int* cta_seg;      // [nph][grid + 1]: CTA j's tiles of phase p are [cta_seg[p][j], cta_seg[p][j + 1])
   const int32_t* q_offset;
   const int32_t* kv_len;
   float* part_lse;        // [entries, hpg]: row (entry * hpg + head in group)
   uint32_t* status;
-  int b, Nq, Nk, Hq, G, Bs, K, nblk, c0, hpg;
+  int b, Nq, Nk, Hq, G, Bs, K, nblk, c0, hpg, nph, grid;
+  int inject_timeout;  // test hook: the MMA warp first waits on a barrier nothing completes
   float scale_log2;  // softmax scale * log2(e)
   float scale;
+};
+
+// A CTA's tiles: run r (one phase) holds its local tiles [pref[r], pref[r+1]),
+// which are the chunk's tiles lo[r] + (z - pref[r]). Each warp role walks its
+// local tile numbers in increasing order, so the lookup keeps its run.
+struct TileRuns {
+  const int* lo;
+  const int* pref;
+  int r = 0;
+  __device__ __forceinline__ int at(int z) {
+    while (z >= pref[r + 1]) ++r;
+    return lo[r] + (z - pref[r]);
+  }
 };
 
 constexpr int kRing = 4;  // gathered-query tile ring depth (one cp.async gather warp per slot)
@@ -297,9 +325,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* v_buf = k_buf + kKBytes;         // [NH][BS][128 B]
   uint8_t* ring = v_buf + kKBytes;          // kRing x kSlot: gathered Q tiles
   int* meta = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kRing + 1][128] gathered tiles' entries (query*64+slot) or -1
+  int* run_lo = meta + (kRing + 1) * kRows;                 // [kKvoMaxPhases]
+  int* run_pref = run_lo + kKvoMaxPhases;                   // [kKvoMaxPhases + 1]
   // mbarriers need 8-byte alignment: round the barrier area up to 16 bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(meta + (kRing + 1) * kRows) + 15) & ~uintptr_t(15));
+      (reinterpret_cast<uintptr_t>(run_pref + kKvoMaxPhases + 1) + 15) & ~uintptr_t(15));
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* q_full = bars + 2;                // [kRing]
@@ -309,7 +339,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* o_full = p_full + 2;              // [2]
   uint64_t* o_empty = o_full + 2;             // [2]
   uint64_t* done_bar = o_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* never_bar = done_bar + 1;  // no thread arrives on it (timeout injection)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -317,7 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
     for (int r = 0; r < kRing; ++r) {
-      tc::mbar_init(&q_full[r], 2);  // the slot's cp.async warp + the TMA gather warp
+      tc::mbar_init(&q_full[r], kRowsLsu < kRows ? 2 : 1);  // the gather warp: TMA bytes + its own copies
       tc::mbar_init(&q_empty[r], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -327,8 +358,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::mbar_init(&o_empty[s], 4);
     }
     tc::mbar_init(done_bar, 1);
+    tc::mbar_init(never_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
+    // this CTA's share of every phase, phase after phase
+    int acc = 0;
+    run_pref[0] = 0;
+    for (int ph = 0; ph < p.nph; ++ph) {
+      const int* seg = p.cta_seg + ph * (p.grid + 1);
+      const int lo = seg[blockIdx.x], hi = seg[blockIdx.x + 1];
+      run_lo[ph] = lo;
+      acc += hi - lo;
+      run_pref[ph + 1] = acc;
+    }
   }
   if (warp == kMmaWarpA) {
     tc::tmem_alloc(tmem_slot, 512);
@@ -343,10 +385,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // this CTA's contiguous run of tiles
-  const int z0 = p.cta_start[blockIdx.x];
-  const int z1 = p.cta_start[blockIdx.x + 1];
-  const int n = z1 - z0;
+  // this CTA's tiles: local numbers z in [0, n), mapped to the chunk's tiles by TileRuns
+  const int n = run_pref[p.nph];
   auto fail = [&]() {
     *abort_flag = 1;
     set_status(p.status, MSA_ERR_TIMEOUT);
@@ -360,9 +400,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == kKvWarp) {
     // ----------------------------- K/V producer -----------------------------
     if (lane == 0) {
+      const uint64_t pol_kv = tc::policy_evict_first();  // each block's K/V is read by one or two CTAs
+      TileRuns runs{run_lo, run_pref};
       int prev_bin = -1, loads = 0;
       for (int z = 0; z < n; ++z) {
-        const int bin = p.tiles[z0 + z].x;
+        const int bin = p.tiles[runs.at(z)].x;
         if (bin == prev_bin) continue;
         prev_bin = bin;
         if (!tc::mbar_wait(kv_empty, (loads & 1) ^ 1, abort_flag)) {
@@ -373,8 +415,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc::mbar_arrive_expect_tx(kv_full, 2 * kKBytes);
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          tc::tma_load_4d(k_buf + h * kKVHalf, &tmK, kv_full, h * 64, g, t * BS, p.b);
-          tc::tma_load_4d(v_buf + h * kKVHalf, &tmV, kv_full, h * 64, g, t * BS, p.b);
+          tc::tma_load_4d_hint(k_buf + h * kKVHalf, &tmK, kv_full, h * 64, g, t * BS, p.b, pol_kv);
+          tc::tma_load_4d_hint(v_buf + h * kKVHalf, &tmV, kv_full, h * 64, g, t * BS, p.b, pol_kv);
         }
         ++loads;
       }
@@ -382,28 +424,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // drain the last copy
     }
   } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kRing) {
-    // ------------------------ query-row gather, cp.async ------------------------
-    // Gather warp gw owns ring slot gw (tiles z = gw, gw + kRing, ...) and
-    // copies rows [0, kRowsLsu) of its tiles in 16-byte chunks (a warp
-    // instruction covers whole 256-byte rows) into the 128B-swizzled K-major
-    // layout; its arrival on the slot's barrier follows its own copies.
+    // ------------------------------ query-row gather ------------------------------
+    // Gather warp gw owns ring slot gw (tiles z = gw, gw + kRing, ...). Its
+    // tiles' entries are fetched kRing tiles ahead. Per tile it first issues
+    // four-row TMA gathers for rows [kRowsLsu, 128) (lane l < kTmaLanes: one
+    // gather per 64-column half; the bytes are counted on the slot's barrier
+    // with the warp's first arrival), then copies rows [0, kRowsLsu) in
+    // 16-byte cp.async chunks (a warp instruction covers whole 256-byte rows);
+    // its second arrival follows its own copies. Both paths write the
+    // 128B-swizzled K-major layout (the swizzle is address-based); they have
+    // separate in-flight limits, so they run side by side. Rows of padding
+    // entries read the chunk's first query (finite values; their outputs are
+    // never read).
     const int gw = warp - kGatherWarp0;
     constexpr int kCpr = D / 8;            // 16-byte chunks per row
     constexpr int kRowsPerIt = 32 / kCpr;  // rows per warp instruction
     constexpr int kEntPerLane = kRows / 32;
+    constexpr int kTmaLanes = (kRows - kRowsLsu) / 4;
     const int per_tile = kRows / p.hpg;
     int* my_meta = meta + gw * kRows;
     int4 tl = make_int4(0, 0, 0, 0);
     int ev[kEntPerLane];
-    auto fetch = [&](int z) {  // independent loads: tile z's entries start at (z0 + z) * per_tile
-      tl = p.tiles[z0 + z];
+    TileRuns runs{run_lo, run_pref};
+    const uint64_t pol_q = tc::policy_evict_last();  // the phase's query rows are reused by every CTA
+    auto fetch = [&](int z) {  // independent loads: tile zt's entries start at zt * per_tile
+      const int zt = runs.at(z);
+      tl = p.tiles[zt];
 #pragma unroll
       for (int x = 0; x < kEntPerLane; ++x) {
         const int e = lane + 32 * x;
-        ev[x] = e < per_tile ? p.entries[int64_t(z0 + z) * per_tile + e] : -1;
+        ev[x] = e < per_tile ? p.entries[int64_t(zt) * per_tile + e] : -1;
       }
     };
     if (gw < n) fetch(gw);
+    int last = -1;  // the last tile this warp issued
     for (int z = gw; z < n; z += kRing) {
       if (!tc::mbar_wait(&q_empty[gw], ((z / kRing) & 1) ^ 1, abort_flag)) {
         fail();
@@ -414,6 +468,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = lane + 32 * x < tl.z ? ev[x] : -1;
       __syncwarp();
       const int g = tl.x / p.nblk;
+      if constexpr (kTmaLanes > 0) {
+        int rows[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int row = kRowsLsu + (lane % kTmaLanes) * 4 + j;
+          const int ent = my_meta[row / p.hpg];
+          const int il = ent >= 0 ? (ent >> 6) : 0;
+          rows[j] = (p.b * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg;
+        }
+        if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[gw], uint32_t(kRows - kRowsLsu) * D * 2);
+        __syncwarp();
+        if (lane < kTmaLanes) {
+          uint8_t* dst = ring + gw * kSlot + (kRowsLsu + lane * 4) * 128;
+#pragma unroll
+          for (int hf = 0; hf < NH; ++hf)
+            tc::tma_gather4_hint(dst + hf * (kRows * 128), &tmQ, &q_full[gw], hf * 64, rows[0], rows[1], rows[2],
+                                 rows[3], pol_q);
+        }
+      }
+      last = z;
       const uint32_t slot = tc::smem_u32(ring + gw * kSlot);
       const int chunk = lane % kCpr, sub = lane / kCpr;
       const uint32_t hf = chunk >> 3, cc = chunk & 7;
@@ -424,7 +498,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int il = ent >= 0 ? (ent >> 6) : 0;
         const __nv_bfloat16* src =
             p.q + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg) * D + chunk * 8;
-        cp_async16(slot + hf * (kRows * 128) + row * 128 + ((cc ^ uint32_t(row & 7)) << 4), src, ent >= 0 ? 16u : 0u);
+        cp_async16_hint(slot + hf * (kRows * 128) + row * 128 + ((cc ^ uint32_t(row & 7)) << 4), src,
+                        ent >= 0 ? 16u : 0u, pol_q);
       }
       cp_async_commit();
       if (z + kRing < n) fetch(z + kRing);
@@ -434,65 +509,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) tc::mbar_arrive(&q_full[gw]);
     }
     cp_async_wait<0>();
-  } else if (warp == kTmaGatherWarp) {
-    // ------------------------ query-row gather, TMA ------------------------
-    // Rows [kRowsLsu, 128) of every tile, in ring order: lane l < kTmaLanes
-    // loads four rows with one four-row gather per 64-column half (same
-    // swizzled layout); the bytes are counted on the slot's barrier. Rows of
-    // padding entries read the chunk's first query (finite values; their
-    // outputs are never read).
-    constexpr int kTmaLanes = (kRows - kRowsLsu) / 4;
-    constexpr int kEntPerLane = kRows / 32;
-    const int per_tile = kRows / p.hpg;
-    int* my_meta = meta + kRing * kRows;
-    int4 tl_n = make_int4(0, 0, 0, 0);
-    int ev_n[kEntPerLane];
-    auto fetch = [&](int z) {
-      tl_n = p.tiles[z0 + z];
-#pragma unroll
-      for (int x = 0; x < kEntPerLane; ++x) {
-        const int e = lane + 32 * x;
-        ev_n[x] = e < per_tile ? p.entries[int64_t(z0 + z) * per_tile + e] : -1;
-      }
-    };
-    if (n > 0) fetch(0);
-    int issued = 0;
-    for (int z = 0; z < n; ++z) {
-      const int rs = z % kRing;
-      const int4 tl = tl_n;
-#pragma unroll
-      for (int x = 0; x < kEntPerLane; ++x)
-        if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = lane + 32 * x < tl.z ? ev_n[x] : -1;
-      if (z + 1 < n) fetch(z + 1);
-      __syncwarp();
-      const int g = tl.x / p.nblk;
-      int rows[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = kRowsLsu + (lane % kTmaLanes) * 4 + j;
-        const int ent = my_meta[row / p.hpg];
-        const int il = ent >= 0 ? (ent >> 6) : 0;
-        rows[j] = (p.b * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg;
-      }
-      if (!tc::mbar_wait(&q_empty[rs], ((z / kRing) & 1) ^ 1, abort_flag)) {
-        fail();
-        break;
-      }
-      if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[rs], uint32_t(kRows - kRowsLsu) * D * 2);
-      __syncwarp();
-      if (lane < kTmaLanes) {
-        uint8_t* dst = ring + rs * kSlot + (kRowsLsu + lane * 4) * 128;
-#pragma unroll
-        for (int hf = 0; hf < NH; ++hf)
-          tc::tma_gather4(dst + hf * (kRows * 128), &tmQ, &q_full[rs], hf * 64, rows[0], rows[1], rows[2], rows[3]);
-      }
-      ++issued;
-      __syncwarp();  // every lane has read my_meta before it is rewritten
-    }
-    // drain: no copy may still be landing in shared memory when the CTA exits
+    // drain: no gather may still be landing in shared memory when the CTA exits
     int zero = 0;
-    for (int z = issued > kRing ? issued - kRing : 0; z < issued; ++z)
-      tc::mbar_wait(&q_full[z % kRing], (z / kRing) & 1, &zero);
+    if (kTmaLanes > 0 && last >= 0 && lane == 0) tc::mbar_wait(&q_full[gw], (last / kRing) & 1, &zero);
   } else if (warp == kMmaWarpA) {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0) {
@@ -516,11 +535,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (last_of_bin) tc::mma_commit(kv_empty);
         return true;
       };
-      int bin_next = n > 0 ? p.tiles[z0].x : -1;
+      if (p.inject_timeout && !tc::mbar_wait_for(never_bar, 0, abort_flag, tc::kInjectedWaitCycles)) {
+        fail();
+        alive = false;
+      }
+      TileRuns runs{run_lo, run_pref};
+      int bin_next = n > 0 ? p.tiles[runs.at(0)].x : -1;
       for (int z = 0; z < n && alive; ++z) {
         const int s = z & 1, rs = z % kRing;
         const int bin = bin_next;
-        if (z + 1 < n) bin_next = p.tiles[z0 + z + 1].x;
+        if (z + 1 < n) bin_next = p.tiles[runs.at(z + 1)].x;
         if (bin != prev_bin) {
           if (z > 0 && !issue_pv(z - 1, true)) {
             fail();
@@ -573,13 +597,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int r = quarter * 32 + lane;             // tile row
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
+    TileRuns runs{run_lo, run_pref};
+    const uint64_t pol_part = tc::policy_evict_first();  // partials are read back once, by the combine
     for (int z = w; z < n; z += 2) {
       const int s = z & 1;  // == w
       // this tile's metadata straight from global memory (the Q ring slot and
       // its staged metadata are recycled as soon as QK^T has consumed them);
       // the loads are in flight while S is being computed
-      const int4 tl = p.tiles[z0 + z];
-      const int e_raw = p.entries[int64_t(z0 + z) * (kRows / p.hpg) + r / p.hpg];
+      const int zg = runs.at(z);  // the chunk's tile index = its partial row block
+      const int4 tl = p.tiles[zg];
+      const int e_raw = p.entries[int64_t(zg) * (kRows / p.hpg) + r / p.hpg];
       const int ent = r / p.hpg < tl.z ? e_raw : -1;
       if (!tc::mbar_wait(&s_full[s], (z >> 1) & 1, abort_flag)) {
         fail();
@@ -641,7 +668,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::fence_after_sync();
       const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int zg = z0 + z;  // tile index in the chunk = its partial row block
       uint4* dst = p.part_o + int64_t(zg) * (D / 8) * kRows + r;
       constexpr int kOH = D > 64 ? 64 : D;  // O columns per TMEM round trip
 #pragma unroll
@@ -662,10 +688,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           o.y = pack_bf16(__uint_as_float(ov[c * 8 + 2]) * inv, __uint_as_float(ov[c * 8 + 3]) * inv);
           o.z = pack_bf16(__uint_as_float(ov[c * 8 + 4]) * inv, __uint_as_float(ov[c * 8 + 5]) * inv);
           o.w = pack_bf16(__uint_as_float(ov[c * 8 + 6]) * inv, __uint_as_float(ov[c * 8 + 7]) * inv);
-          dst[(h0 / 8 + c) * kRows] = o;
+          tc::st_v4_hint(dst + (h0 / 8 + c) * kRows, o, pol_part);
         }
       }
-      p.part_lse[int64_t(zg) * kRows + r] = valid ? mx * p.scale + logf(l) : 0.f;
+      tc::st_f32_hint(p.part_lse + int64_t(zg) * kRows + r, valid ? mx * p.scale + logf(l) : 0.f, pol_part);
     }
   }
 
@@ -1134,6 +1160,8 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   o += 256;
   L.cta_start = o;
   o += a256(size_t(kMaxGrid + 1) * 4);
+  L.cta_seg = o;
+  o += a256(size_t(kKvoMaxPhases) * (kMaxGrid + 1) * 4);
   L.max_tiles = max_tiles;
   L.entries = o;
   o += a256(max_tiles * per_tile * 4);  // bins padded to whole tiles
@@ -1152,8 +1180,8 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
 static size_t attn_smem_bytes(int d, int Bs) {
   const size_t kv = size_t(Bs) * d * 2 * 2;
   const size_t slot = size_t(kRows) * d * 2;
-  const size_t meta = size_t(kRing + 1) * kRows * 4 + 16;
-  return 1024 + kv + kRing * slot + meta + (2 + 2 * kRing + 8 + 1) * 8 + 16;
+  const size_t meta = size_t(kRing + 1) * kRows * 4 + size_t(2 * kKvoMaxPhases + 1) * 4 + 16;
+  return 1024 + kv + kRing * slot + meta + (2 + 2 * kRing + 8 + 2) * 8 + 16;
 }
 
 // selection -> per-(group, block) entry lists, tiles and the persistent
@@ -1177,11 +1205,12 @@ cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int3
   ProfScope pf("attn_invert", stream);
   attn_count_kernel<<<igrid, 256, size_t(nblk) * 4, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0,
                                                               cq, rows_per_cta, cnt, status);
-  attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, q_offset, b, nblk, nbins, per_tile, Bs, c0, cq, grid,
-                                           reinterpret_cast<int*>(w + L.entry_off),
+  attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, q_offset, b, nblk, nbins, per_tile, Bs, c0, cq, grid, G,
+                                           kvo_phases(G), reinterpret_cast<int*>(w + L.entry_off),
                                            reinterpret_cast<int*>(w + L.tile_off),
                                            reinterpret_cast<int*>(w + L.cost_off), reinterpret_cast<int*>(w + L.total),
-                                           reinterpret_cast<int*>(w + L.cta_start));
+                                           reinterpret_cast<int*>(w + L.cta_start),
+                                           reinterpret_cast<int*>(w + L.cta_seg));
   attn_tiles_kernel<<<(nbins + 255) / 256, 256, 0, stream>>>(cnt, reinterpret_cast<int*>(w + L.entry_off),
                                                              reinterpret_cast<int*>(w + L.tile_off), nbins, per_tile,
                                                              reinterpret_cast<int4*>(w + L.tiles));
@@ -1215,7 +1244,6 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   const KvoLayout L = kvo_layout(Nq, Hq, G, d, Bs, K, Nk);
   char* w = static_cast<char*>(ws);
   uint32_t* status = &static_cast<WsHeader*>(ws)->status;
-  int* cta_start = reinterpret_cast<int*>(w + L.cta_start);
   int* entries = reinterpret_cast<int*>(w + L.entries);
   int* rev = reinterpret_cast<int*>(w + L.rev);
   int4* tiles = reinterpret_cast<int4*>(w + L.tiles);
@@ -1256,7 +1284,7 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   prm.part_o = part_o;
   prm.entries = entries;
   prm.tiles = tiles;
-  prm.cta_start = cta_start;
+  prm.cta_seg = reinterpret_cast<const int*>(w + L.cta_seg);
   prm.q_offset = q_offset;
   prm.kv_len = kv_len;
   prm.part_lse = part_lse;
@@ -1272,6 +1300,9 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   const int grid = sm_count() < kMaxGrid ? sm_count() : kMaxGrid;
+  prm.nph = kvo_phases(G);
+  prm.grid = grid;
+  prm.inject_timeout = debug_inject_timeout() ? 1 : 0;
 
   for (int b = 0; b < B; ++b) {
     for (int c0 = 0; c0 < Nq; c0 += cq_max) {

@@ -65,6 +65,10 @@ __device__ __forceinline__ SeqView seq_view(const int32_t* q_offset, const int32
   return s;
 }
 
+// Test hook (msa_debug_inject_timeout): attention kernels first make one
+// bounded wait that runs out.
+bool debug_inject_timeout();
+
 // RAII bracket of one kernel launch with a CUDA event pair while profiling is
 // on (msa_profile_begin / msa_profile_end); a no-op otherwise.
 class ProfScope {
@@ -88,8 +92,11 @@ class ProfScope {
 // grid. Used by the prefill attention, the KL pass and the backward.
 constexpr int kKvoRows = 128;       // rows (entry x head) per tile
 constexpr int kKvoMaxGrid = 1024;   // cta_start capacity
+constexpr int kKvoMaxPhases = 16;   // forward attention: group ranges processed one after another
+inline int kvo_phases(int G) { return G < kKvoMaxPhases ? G : kKvoMaxPhases; }
 struct KvoLayout {
-  size_t cnt, cursor, entry_off, tile_off, cost_off, total, cta_start, entries, rev, tiles, part_o, part_lse, end;
+  size_t cnt, cursor, entry_off, tile_off, cost_off, total, cta_start, cta_seg, entries, rev, tiles, part_o, part_lse,
+      end;
   size_t max_tiles;
 };
 // query tokens per chunk (equal chunks; the forward's bf16 partials stay under ~6 GiB)
@@ -100,6 +107,10 @@ int sm_count();
 cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int32_t* kv_len, int b, int Nq, int Nk,
                          int G, int K, int Bs, int per_tile, int c0, int cq, int grid, char* w, const KvoLayout& L,
                          uint32_t* status, cudaStream_t stream);
+
+// Status of an empty index selection (B == 0 or Nq == 0), shared by the entry
+// points that select: the other arguments are checked as for one row.
+msa_status_t index_select_empty_status(int Nk, int G, int di, int Bs, int K, int dtype);
 
 // ---- launchers (host) ------------------------------------------------------
 // Index Branch, CUDA-core table path: block maxima for every visible block.

@@ -47,16 +47,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase of parity `parity` to complete. Returns false if the
-// wait ran past kWaitLimitCycles or *abort became non-zero.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// wait ran past `limit` cycles or *abort became non-zero.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_for(bar, parity, abort, kWaitLimitCycles);
+}
+
+// Test hook: with timeout injection on (msa_debug_inject_timeout), a kernel
+// waits once on a barrier that nothing completes, with this short limit
+// (~1 ms), and then takes its ordinary timeout path.
+constexpr long long kInjectedWaitCycles = 2000000LL;
 
 // ---- programmatic dependent launch --------------------------------------------
 // Waits until the grids this one depends on have completed and their writes
@@ -103,6 +111,60 @@ __device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* m
       "%5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
+}
+
+// ---- L2 cache policies --------------------------------------------------------
+// A 64-bit policy for the .L2::cache_hint forms below: evict_first marks lines
+// that are read or written once (streamed), so they leave L2 before data that
+// is reused; evict_last marks lines that should stay.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_4d_hint(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                                 int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_gather4_hint(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                                 int r0, int r1, int r2, int r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "l"(policy)
+      : "memory");
+}
+// 16-byte global store / load that bypass L1 and carry an L2 policy.
+__device__ __forceinline__ void st_v4_hint(void* gptr, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(gptr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void st_f32_hint(float* gptr, float v, uint64_t policy) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(gptr), "f"(v), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_v4_hint(const void* gptr, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(gptr), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ float ld_f32_hint(const float* gptr, uint64_t policy) {
+  float v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(gptr), "l"(policy));
+  return v;
 }
 
 // 2-D tiled store of the box at (c0, c1) from shared memory (bulk-group completion).
