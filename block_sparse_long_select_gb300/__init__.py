@@ -27,6 +27,7 @@ from ._lib import (  # noqa: F401
     MsaError,
     lib_path,
     load_library,
+    msa_debug_inject_timeout,
     msa_index_select,
     msa_index_select_noalloc,
     msa_index_select_v,

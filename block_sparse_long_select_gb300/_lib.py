@@ -27,6 +27,7 @@ SIGNATURES = {
     "msa_index_select_noalloc": (_i32, [_vp, _vp, _vp, _vp] + [_i32] * 8 + [_vp, _vp, _vp]),
     "msa_profile_begin": (_i32, []),
     "msa_profile_end": (_i32, [_vp, _i32]),
+    "msa_debug_inject_timeout": (_i32, [_i32]),
 }
 
 
@@ -90,6 +91,28 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _check_select_args(iq, ik, q_offset, kv_len, Bs, K, sel, block_max):
+    """Shapes, dtypes and devices of an index selection's tensors (the library
+    writes sel and block_max through raw pointers: a short or mistyped buffer
+    would be overrun on the device)."""
+    import torch
+
+    if iq.dim() != 4 or ik.dim() != 3:
+        raise ValueError("iq must be [B, Nq, G, di] and ik [B, Nk, di]")
+    B, Nq, G, di = iq.shape
+    if ik.shape[0] != B or ik.shape[2] != di or ik.dtype != iq.dtype or ik.device != iq.device:
+        raise ValueError("ik must be [B, Nk, di] with iq's dtype and device")
+    for name, t in (("q_offset", q_offset), ("kv_len", kv_len)):
+        if t is not None and (t.dtype != torch.int32 or t.numel() != B or t.device != iq.device):
+            raise ValueError(f"{name} must be int32 of length B on iq's device")
+    if sel is not None and (sel.dtype != torch.int32 or sel.numel() != B * Nq * G * K or sel.device != iq.device):
+        raise ValueError("sel must be int32 with B * Nq * G * K elements on iq's device")
+    nblk = (ik.shape[1] + Bs - 1) // Bs if Bs > 0 else 0
+    if block_max is not None and (block_max.dtype != torch.float32 or block_max.numel() != B * Nq * G * nblk or
+                                  block_max.device != iq.device):
+        raise ValueError("block_max must be float32 with B * Nq * G * ceil(Nk / Bs) elements on iq's device")
+
+
 def msa_workspace_size(op, B, Nq, Nk, G, Hq, d, di, Bs, K, dtype) -> int:
     return int(load_library().msa_workspace_size(op, B, Nq, Nk, G, Hq, d, di, Bs, K, dtype))
 
@@ -114,6 +137,7 @@ def msa_index_select_v(iq, ik, q_offset, kv_len, Bs, K, force, sel=None, block_m
     import torch
 
     _need_cuda(iq, ik, q_offset, kv_len, sel, block_max)
+    _check_select_args(iq, ik, q_offset, kv_len, Bs, K, sel, block_max)
     B, Nq, G, di = iq.shape
     Nk = ik.shape[1]
     dt = _dtype_code(iq)
@@ -132,6 +156,9 @@ def msa_index_select_noalloc(iq, ik, q_offset, kv_len, Bs, K, sel, block_max=Non
     """msa_index_select on the library's static scratch (no workspace; see include/msa.h).
     ``sel`` must be given: this wrapper allocates nothing either."""
     _need_cuda(iq, ik, q_offset, kv_len, sel, block_max)
+    if sel is None:
+        raise ValueError("msa_index_select_noalloc needs a caller-owned sel")
+    _check_select_args(iq, ik, q_offset, kv_len, Bs, K, sel, block_max)
     B, Nq, G, di = iq.shape
     Nk = ik.shape[1]
     code = load_library().msa_index_select_noalloc(_ptr(iq), _ptr(ik), _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, G,
@@ -203,6 +230,13 @@ def msa_profile_end() -> dict:
     return {buf[k].name.decode(): (buf[k].launches, buf[k].total_ms) for k in range(min(n, 64))}
 
 
+def msa_debug_inject_timeout(enable: bool) -> bool:
+    """Test hook (see include/msa_profile.h): while on, the attention kernels
+    make one bounded wait that runs out and report MSA_ERR_TIMEOUT. Returns the
+    previous setting."""
+    return bool(load_library().msa_debug_inject_timeout(1 if enable else 0))
+
+
 def msa_decode_step(q, k_new, v_new, iq, ik_new, k_cache, v_cache, ik_cache, kv_len, Bs, K, sel=None, out=None,
                     lse=None, scale=0.0, ws=None, stream=None):
     """One streaming decode step (see include/msa.h): append the new token's
@@ -244,7 +278,7 @@ def msa_kl_aux_forward(q, k, iq, ik, sel, lse, q_offset, kv_len, Bs, K, kl=None,
     if kl is None:
         kl = torch.empty((B, Nq, Hkv), dtype=torch.float32, device=q.device)
     if ws is None:
-        ws = workspace(msa_workspace_size(MSA_OP_KL_AUX, B, Nq, Nk, Hkv, Hq, d, 0, Bs, K, dt), q.device)
+        ws = workspace(msa_workspace_size(MSA_OP_KL_AUX, B, Nq, Nk, Hkv, Hq, d, di, Bs, K, dt), q.device)
     code = load_library().msa_kl_aux_forward(_ptr(q), _ptr(k), _ptr(iq), _ptr(ik), _ptr(sel), _ptr(lse),
                                              _ptr(q_offset), _ptr(kv_len), B, Nq, Nk, Hq, Hkv, d, di, Bs, K,
                                              float(scale), dt, _ptr(kl), _ptr(ws), ws.numel(),

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const __nv_bfloat16* __restrict__ q,
     const int32_t* __restrict__ sel, const int32_t* __restrict__ kv_len, int Lmax, int Hq, int G, int K, int nblk,
     float scale_log2, float* __restrict__ part_o, float* __restrict__ part_ml, int* __restrict__ arrivals,
-    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* status) {
+    __nv_bfloat16* __restrict__ out, float* __restrict__ lse, uint32_t* status, int inject_timeout) {
   constexpr int NH = D / 64;
   constexpr uint32_t kHalf = BS * 128;
   constexpr uint32_t kTile = BS * D * 2;
@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
       abort_s = 0;
       tc::mbar_init(&bars[0], 1);
       tc::mbar_init(&bars[1], 1);
+      tc::mbar_init(&bars[2], 1);  // nothing arrives on it (timeout injection)
       tc::fence_barrier_init();
     }
     __syncthreads();
@@ -147,7 +148,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
       }
     }
     const int nvalid = min(BS, pos - t * BS + 1);  // keys j <= pos in this block
-    bool ok = tc::mbar_wait(&bars[0], 0, &abort_s);
+    if (inject_timeout && tid == 0 && !tc::mbar_wait_for(&bars[2], 0, &abort_s, tc::kInjectedWaitCycles))
+      abort_s = 1;
+    __syncthreads();
+    // every thread of the CTA takes the same branch below (the MMAs are warp-wide)
+    bool ok = __syncthreads_and(!abort_s && tc::mbar_wait(&bars[0], 0, &abort_s));
     if (ok && warp < BS / 16) {
       // S^T tile: keys [16 warp, 16 warp + 16) x heads
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
       }
     }
     __syncthreads();
-    if (ok) ok = tc::mbar_wait(&bars[1], 0, &abort_s);
+    ok = __syncthreads_and(ok && tc::mbar_wait(&bars[1], 0, &abort_s));
     if (ok) {
       // O^T tile: head dims [16 warp, 16 warp + 16) x heads, over all keys
       if (warp < D / 16) {
@@ -221,10 +226,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
         out_ml[2 * tid + 1] = ml[2 * tid + 1];
       }
     } else {
+      // gave up: record it, let the copies land (bounded) before the CTA
+      // releases its shared memory, and leave an empty slot for the merge. The
+      // CTA still counts its arrival below, so the (sequence, group) counter
+      // returns to zero and the workspace stays usable.
       if (tid == 0) set_status(status, MSA_ERR_TIMEOUT);
-      int zero = 0;  // copies may still land: wait (bounded) before the CTA gives up its smem
+      int zero = 0;
       tc::mbar_wait(&bars[0], 0, &zero);
       tc::mbar_wait(&bars[1], 0, &zero);
+      for (int x = tid; x < kOut; x += kDecThreads) out_o[x] = 0.f;
+      if (tid < HPG) {
+        out_ml[2 * tid] = -INFINITY;
+        out_ml[2 * tid + 1] = 0.f;
+      }
     }
   } else {  // empty slot: contributes nothing to the merge
     for (int x = tid; x < kOut; x += kDecThreads) out_o[x] = 0.f;
@@ -872,6 +886,7 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
     return cudaErrorInvalidValue;
   const size_t smem = dec_smem_bytes(d, Bs, hpg);
   const float scale_log2 = scale * kLog2eD;
+  const int inject = debug_inject_timeout() ? 1 : 0;
   cudaError_t e;
   ProfScope pf("decode_attn", stream);
 #define MSA_DEC(D_, BS_, HPG_)                                                                                   \
@@ -881,8 +896,8 @@ cudaError_t launch_decode_attn(const void* q, const void* k_cache, const void* v
       return e;                                                                                                  \
     if ((e = launch_after_prev(kern, dim3(unsigned(items)), dim3(kDecThreads), smem, stream, tmK, tmV,              \
                                static_cast<const __nv_bfloat16*>(q), sel, kv_len, Lmax, Hq, G, K, nblk, scale_log2,   \
-                               part_o, part_ml, arrivals, static_cast<__nv_bfloat16*>(out), lse, status)) !=         \
-        cudaSuccess)                                                                                             \
+                               part_o, part_ml, arrivals, static_cast<__nv_bfloat16*>(out), lse, status,            \
+                               inject)) != cudaSuccess)                                                          \
       return e;                                                                                                  \
   } while (0)
 #define MSA_DEC_BS(D_, HPG_)  \

@@ -1,4 +1,5 @@
 // Per-kernel CUDA-event timing of the library's launches (see msa_profile.h).
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -16,6 +17,7 @@ struct Record {
 
 std::mutex g_mu;
 bool g_on = false;
+std::atomic<int> g_inject_timeout{0};
 std::vector<Record> g_records;
 std::vector<cudaEvent_t> g_pool;
 
@@ -31,6 +33,8 @@ cudaEvent_t take_event() {
 }
 
 }  // namespace
+
+bool debug_inject_timeout() { return g_inject_timeout.load() != 0; }
 
 ProfScope::ProfScope(const char* name, cudaStream_t stream) : name_(name), stream_(stream) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -89,3 +93,5 @@ extern "C" int msa_profile_end(msa_kernel_time_t* out, int max_entries) {
   for (size_t k = 0; k < agg.size() && int(k) < max_entries; ++k) out[k] = agg[k];
   return int(agg.size());
 }
+
+extern "C" int msa_debug_inject_timeout(int enable) { return msa::g_inject_timeout.exchange(enable ? 1 : 0); }
