@@ -122,6 +122,14 @@ StepPlan plan_step(int B, int Lmax, int G, int Hq, int d, int di, int Bs, int K,
 }
 
 }  // namespace
+
+// Status of an empty index selection (B == 0 or Nq == 0): the other arguments
+// are checked as for one row of one sequence.
+msa_status_t index_select_empty_status(int Nk, int G, int di, int Bs, int K, int dtype) {
+  const IndexPlan one = plan_index(1, 1, one_key_min(Nk), G, di, Bs, K, dtype, false);
+  return one.ok ? MSA_OK : one.err;
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -153,8 +161,8 @@ extern "C" size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int H
     }
     case MSA_OP_KL_AUX: {
       if (B < 1 || Nq < 1 || Nk < 1 || Nq > Nk || G < 1 || Hq < 1 || Hq % G != 0) return 0;
-      // the scratch does not depend on di (ignored here): check the rest with a supported pairing
-      if (!kl_aux_supported(dtype, Hq, G, d, d == 128 ? 64 : 32, Bs, K)) return 0;
+      // the scratch does not depend on di, but a pairing the entry point rejects gets no size
+      if (!kl_aux_supported(dtype, Hq, G, d, di, Bs, K)) return 0;
       return kl_aux_ws_bytes(Nq, Nk, Hq, G, d, Bs, K);
     }
     case MSA_OP_BACKWARD: {
@@ -174,10 +182,7 @@ extern "C" msa_status_t msa_index_select_v(const void* iq, const void* ik, const
   if (force != MSA_FORCE_LOCAL && force != (MSA_FORCE_LOCAL | MSA_FORCE_START)) return MSA_ERR_INVALID_ARG;
   const int fs = (force & MSA_FORCE_START) ? 1 : 0;  // block 0 kept as well
   if (fs && K < 2) return MSA_ERR_INVALID_ARG;
-  if (empty_batch(B, Nq)) {
-    const IndexPlan one = plan_index(1, 1, one_key_min(Nk), G, di, Bs, K, dtype, false);
-    return one.ok ? MSA_OK : one.err;
-  }
+  if (empty_batch(B, Nq)) return index_select_empty_status(Nk, G, di, Bs, K, dtype);
   if (!iq || !ik || !sel) return MSA_ERR_INVALID_ARG;
   IndexPlan p = plan_index(B, Nq, Nk, G, di, Bs, K, dtype, block_max != nullptr);
   if (!p.ok) return p.err;

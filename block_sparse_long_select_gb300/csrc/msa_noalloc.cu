@@ -25,7 +25,9 @@ void* g_noalloc_addr[kMaxDevices] = {nullptr};
 
 // Device address of the static scratch on the current device. The host-side
 // symbol is only a stand-in, so the address is looked up once per device
-// (with that device current) and cached.
+// (with that device current) and cached for the life of the process; a
+// cudaDeviceReset after the first call would leave the cached address stale,
+// so the entry point does not support one.
 cudaError_t noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -51,11 +53,8 @@ extern "C" msa_status_t msa_index_select_noalloc(const void* iq, const void* ik,
                                                  const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs,
                                                  int K, int dtype, int32_t* sel, float* block_max,
                                                  cudaStream_t stream) {
-  if (B >= 0 && Nq >= 0 && (B == 0 || Nq == 0)) {  // an empty batch: nothing to read or compute
-    if (Nk < 0 || G < 1 || di < 1 || Bs < 1 || K < 1 || (dtype != MSA_BF16 && dtype != MSA_FP32))
-      return MSA_ERR_INVALID_ARG;
-    return ((di != 32 && di != 64) || Bs > kMaxBs || K > kMaxK) ? MSA_ERR_UNSUPPORTED : MSA_OK;
-  }
+  // an empty batch: nothing to read or compute, the same checks as msa_index_select
+  if (B >= 0 && Nq >= 0 && (B == 0 || Nq == 0)) return index_select_empty_status(Nk, G, di, Bs, K, dtype);
   if (!iq || !ik || !sel) return MSA_ERR_INVALID_ARG;
   if (B < 1 || Nq < 1 || Nk < 1 || G < 1 || di < 1 || Bs < 1 || K < 1 || Nq > Nk) return MSA_ERR_INVALID_ARG;
   if (dtype != MSA_BF16 && dtype != MSA_FP32) return MSA_ERR_INVALID_ARG;

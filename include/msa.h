@@ -35,6 +35,11 @@
  *    first word is a sticky device status that kernels set when they detect a
  *    bad index or a wait that ran out; msa_read_status() reads and clears it.
  *    Calls that share one workspace must be ordered on one stream.
+ *  - Every device wait is bounded (about a second). A kernel whose wait runs
+ *    out records MSA_ERR_TIMEOUT, lets its copies and matrix products finish
+ *    and returns; the outputs of that call are unspecified. Nothing the next
+ *    call depends on is left behind in the workspace: once msa_read_status()
+ *    has cleared the status, the same workspace can be used again.
  *  - Argument errors found on the host return before anything is enqueued.
  *    Per-sequence values (q_offset, kv_len, sel entries) live on the device
  *    and are checked there: an offending row is skipped (its sel row is -1,
@@ -82,8 +87,8 @@ typedef enum {
 /* Bytes of scratch `ws` the entry point `op` needs for these sizes (the same
  * argument meanings as the entry points; unused ones may be 0: G and di for
  * the attention ops, Hq and d for MSA_OP_INDEX_SELECT; for MSA_OP_DECODE and
- * MSA_OP_DECODE_STEP, Nq is ignored and Nk is Lmax; MSA_OP_DECODE_STEP uses
- * every other argument, with G = Hkv; MSA_OP_KL_AUX and MSA_OP_BACKWARD use
+ * MSA_OP_DECODE_STEP, Nq is ignored and Nk is Lmax; MSA_OP_DECODE_STEP and
+ * MSA_OP_KL_AUX use every other argument, with G = Hkv; MSA_OP_BACKWARD uses
  * all but di, with G = Hkv). Returns 0 when the arguments are invalid or not
  * supported, and 256 for a valid empty batch. */
 size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, int di, int Bs, int K, int dtype);
@@ -141,7 +146,9 @@ msa_status_t msa_index_select_v(const void* iq, const void* ik, const int32_t* q
  * B*Nq*G*ceil(Nk/Bs)*4 bytes (0 when block_max is given); a call needing more
  * than 32 MiB - 256 B returns MSA_ERR_WORKSPACE before anything is enqueued.
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture. Every call
+ * device current and keeps it for the life of the process; make that first call
+ * before any stream capture, and do not reset the device (cudaDeviceReset)
+ * after it while this library stays loaded. Every call
  * shares the one array and clears its status word first: calls whose work
  * overlaps on the GPU (other streams, or other host threads) race on it. Rows
  * that fail the device-side range checks come back as -1 rows; the status
@@ -161,7 +168,9 @@ msa_status_t msa_index_select_noalloc(const void* iq, const void* ik, const int3
  *  q_offset, kv_len: as for msa_index_select
  *  scale  softmax scale; <= 0 selects 1/sqrt(d)
  *  out  [B, Nq, Hq, d] (dtype), out; lse [B, Nq, Hq] fp32 or NULL, out:
- *       natural-log sum of exp of the scaled scores over the attended keys
+ *       natural-log sum of exp of the scaled scores over the attended keys.
+ *       Both are deterministic: each row merges its per-block partials in slot
+ *       order, with no atomic update of any output.
  *  Supported: d in {64, 128}; BF16 or FP32; Bs and K as for msa_index_select. */
 msa_status_t msa_sparse_attn_prefill(const void* q, const void* k, const void* v, const int32_t* sel,
                                      const int32_t* q_offset, const int32_t* kv_len, int B, int Nq, int Nk, int Hq,
@@ -225,9 +234,13 @@ msa_status_t msa_decode_step(const void* q, const void* k_new, const void* v_new
  *       normalises p; scale must be the forward's (<= 0 selects 1/sqrt(d))
  *  q_offset, kv_len: as for msa_index_select
  *  kl [B, Nq, Hkv] fp32, out (0 for a row without attended tokens)
- *  ws: msa_workspace_size(MSA_OP_KL_AUX, B, Nq, Nk, Hkv, Hq, d, 0, Bs, K, dtype)
+ *  ws: msa_workspace_size(MSA_OP_KL_AUX, B, Nq, Nk, Hkv, Hq, d, di, Bs, K, dtype)
  *  Supported: BF16; (d, di) in {(128, 64), (64, 32)}; Bs in {32, 64, 128};
- *  Hq / Hkv in {2, 4, 8}; other sizes return MSA_ERR_UNSUPPORTED. */
+ *  Hq / Hkv in {2, 4, 8}; other sizes return MSA_ERR_UNSUPPORTED.
+ *  Determinism: for d 128, di 64 and Bs 128 (tensor-core pass) every sum is
+ *  taken in a fixed order and repeated calls give identical bits; the other
+ *  built shapes add the per-entry sums of a tile with shared-memory atomics,
+ *  so their values can differ in the last bits from run to run. */
 msa_status_t msa_kl_aux_forward(const void* q, const void* k, const void* iq, const void* ik, const int32_t* sel,
                                 const float* lse, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
                                 int Nk, int Hq, int Hkv, int d, int di, int Bs, int K, float scale, int dtype,
@@ -253,7 +266,12 @@ msa_status_t msa_kl_aux_forward(const void* q, const void* k, const void* iq, co
  *  Supported: BF16; d in {64, 128}; Bs in {32, 64, 128}; Hq / Hkv in
  *  {1, 2, 4, 8}; 1 <= K <= 64. Other sizes return MSA_ERR_UNSUPPORTED.
  *  Out-of-range sel entries set MSA_ERR_BOUNDS in the workspace status and
- *  are skipped. */
+ *  are skipped.
+ *  Determinism: dq is a fixed-order sum (per-slot partials merged in slot
+ *  order) and repeats bit for bit. dk and dv sum contributions of every query
+ *  row that attends a key; they are accumulated in fp32 with atomic adds whose
+ *  order varies from run to run, so they can differ in the last bits between
+ *  runs (the forward's outputs, sel, out and lse, are deterministic). */
 msa_status_t msa_sparse_attn_backward(const void* q, const void* k, const void* v, const void* out, const void* dout,
                                       const float* lse, const int32_t* sel, const int32_t* q_offset,
                                       const int32_t* kv_len, int B, int Nq, int Nk, int Hq, int Hkv, int d, int Bs,

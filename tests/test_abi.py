@@ -90,8 +90,11 @@ def test_kl_and_backward_host_validation(lib):
     P = lambda: FAKE  # noqa: E731
     bf16 = msa.MSA_BF16
     # workspace sizes: supported shapes get one, unsupported ones 0
-    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 128, 0, 128, 16, bf16) >= 256
-    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 96, 0, 128, 16, bf16) == 0
+    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 128, 64, 128, 16, bf16) >= 256
+    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 96, 64, 128, 16, bf16) == 0
+    # di is checked as the entry point checks it: (128, 32) is not a built pairing, 0 is no di
+    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 128, 32, 128, 16, bf16) == 0
+    assert msa.msa_workspace_size(msa.MSA_OP_KL_AUX, 1, 8192, 8192, 8, 32, 128, 0, 128, 16, bf16) == 0
     assert msa.msa_workspace_size(msa.MSA_OP_BACKWARD, 1, 8192, 8192, 8, 32, 128, 0, 128, 16, bf16) >= 256
     assert msa.msa_workspace_size(msa.MSA_OP_BACKWARD, 1, 8192, 8192, 2, 32, 128, 0, 128, 16, bf16) == 0  # hpg 16
     assert msa.msa_workspace_size(msa.MSA_OP_BACKWARD, 1, 8192, 8192, 8, 32, 128, 0, 16, 16, bf16) == 0  # Bs 16

@@ -68,26 +68,58 @@ def test_chunked_prefill_offsets():
 
 
 def test_prefill_8k_bf16():
-    """Prefill bf16 config (seq 8192, block 128, K 16): every selection bit-exact,
-    attention on a stratified sample of rows (dense head rows, tail, spread)."""
+    """Prefill bf16 config (seq 8192, block 128, K 16), in the bench's launch
+    configuration: every selection bit-exact and every output row (all 8192
+    rows x 32 heads x 128 dims) and lse within the bf16 tolerances."""
     w = synth.WORKLOADS["prefill_8k"]
     t = device_inputs(w, DEV)
     sel, out, lse = gpu_prefill(w, t, DEV)
     sel = sel.cpu().numpy()
     h = host_inputs(w)
+    osel, oout, olse = oracle_full(w, h)
+    assert np.array_equal(sel, osel)
+    assert_close(out.float().cpu().numpy(), oout, "bf16", w.name)
+    assert_close(lse.cpu().numpy(), olse, "bf16", w.name, lse=True)
+
+
+# the optional block_max output of msa_index_select (it takes the table path):
+# block maxima of the visible keys, NaN past the local block
+BLOCK_MAX_CASES = {
+    "bf16_bs64": (synth.scaled(BASE, B=2, Nq=700, Nk=700, Bs=64, K=4), None),
+    "bf16_bs100_chunked": (synth.scaled(BASE, B=3, Nq=300, Nk=1100, Hq=8, Hkv=2, Bs=100, K=5),
+                           np.array([1100, 900, 301], np.int32)),
+    "bf16_bs128_hot": (synth.scaled(BASE, B=1, Nq=1000, Nk=1000, Bs=128, K=3, hot="first4"), None),
+    "fp32_tiny": (synth.WORKLOADS["tiny_fp32"], None),
+    "bf16_one_query_rows": (synth.scaled(synth.WORKLOADS["decode_b64"], B=6, Nk=3000, kv_len_range=(1, 3000),
+                                         Bs=64, K=8), None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BLOCK_MAX_CASES))
+def test_block_max_output(name):
+    """block_max element by element against the oracle's block maxima: exact
+    (integer-valued index inputs make every score exact in fp32), NaN at
+    exactly the blocks the oracle leaves out (t > loc); the selection too."""
+    import block_sparse_long_select_gb300 as msa
     import oracle
 
-    rb, ri = oracle.all_rows(1, w.Nq)
-    osel = oracle.index_select(h["iq"].reshape(-1, w.G, w.di), h["ik"], rb, ri, synth.q_offsets(w),
-                               synth.kv_lens(w), w.Bs, w.K).reshape(sel.shape)
-    assert np.array_equal(sel, osel)
-    rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([np.arange(0, 256), np.arange(w.Nq - 128, w.Nq),
-                                     rng.choice(w.Nq, 640, replace=False)]))
-    oout, olse = oracle.sparse_attn(h["q"][0, rows], h["k"], h["v"], osel[0, rows], np.zeros(len(rows), np.int32),
-                                    rows.astype(np.int32), synth.q_offsets(w), synth.kv_lens(w), w.Bs, w.K)
-    assert_close(out[0, rows].float().cpu().numpy(), oout, "bf16", w.name)
-    assert_close(lse[0, rows].cpu().numpy(), olse, "bf16", w.name, lse=True)
+    w, kv_len = BLOCK_MAX_CASES[name]
+    kl = synth.kv_lens(w) if kv_len is None else kv_len
+    qo = synth.q_offsets(w) if kv_len is None else (kl - w.Nq).astype(np.int32)
+    t = device_inputs(w, DEV, names=("iq", "ik"))
+    nblk = (w.Nk + w.Bs - 1) // w.Bs
+    bm = torch.full((w.B, w.Nq, w.G, nblk), 12345.0, dtype=torch.float32, device=DEV)
+    sel = msa.msa_index_select(t["iq"], t["ik"], torch.from_numpy(qo).to(DEV), torch.from_numpy(kl).to(DEV), w.Bs,
+                               w.K, block_max=bm)
+    torch.cuda.synchronize()
+    iq, ik = synth.host_tensor(w, "iq"), synth.host_tensor(w, "ik")
+    rb, ri = oracle.all_rows(w.B, w.Nq)
+    osel, obm = oracle.index_select(iq.reshape(-1, w.G, w.di), ik, rb, ri, qo, kl, w.Bs, w.K, want_block_max=True)
+    got = bm.cpu().numpy().reshape(obm.shape).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(obm)), f"{name}: visible blocks differ"
+    vis = ~np.isnan(obm)
+    assert np.array_equal(got[vis], obm[vis]), f"{name}: block maxima differ"
+    assert np.array_equal(sel.cpu().numpy().reshape(osel.shape), osel), name
 
 
 def test_decode_small():
