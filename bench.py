@@ -58,6 +58,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kl", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the Bs 64/32 and 1M prefill legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0 = auto)")
     return ap.parse_args()
@@ -274,8 +275,10 @@ def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="pre
         return None
     amount = per_step * steps / launches
     if bound == "tensor":
+        # the burst figure: these kernels run inside steps of milliseconds to a
+        # fraction of a second, not seconds-long loops under the power cap
         achieved = amount / per_launch_s / 1e12
-        peak, peak_name = peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
+        peak, peak_name = peaks["bf16_tflops"], "bf16_tflops (burst)"
     else:
         achieved = amount / per_launch_s / 1e9
         peak, peak_name = peaks["hbm_gbs"], "hbm_gbs"
@@ -458,7 +461,7 @@ def run_msa(args, dist):
         msa.msa_sparse_attn_prefill(t["q"], t["k"], t["v"], sel, qo, kl, w.Bs, w.K, out=out, lse=lse, ws=ws_a)
     if not args.no_kl:
         klo = torch.empty((w.B, w.Nq, w.G), dtype=torch.float32, device=dev)
-        ws_k = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_KL_AUX, w.B, w.Nq, w.Nk, w.G, w.Hq, w.d, 0, w.Bs,
+        ws_k = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_KL_AUX, w.B, w.Nq, w.Nk, w.G, w.Hq, w.d, w.di, w.Bs,
                                                     w.K, msa.MSA_BF16), dev)
 
         def kl_step():
@@ -520,6 +523,56 @@ def run_msa(args, dist):
 
     del t, out, sel, ws_i, ws_a
     torch.cuda.empty_cache()
+
+    # ---------------- other prefill configurations (one leg each) ----------------
+    # the block-size sweep at 128K (Bs 64 with K 32, Bs 32 with K 64) and the
+    # 1M-token prefill: the same two calls per step, timed the same way, with
+    # the index and attention rooflines of each
+    def prefill_leg(name, steps, warmup):
+        wl = synth.WORKLOADS[name]
+        qo_l, kl_l = synth.q_offsets(wl), synth.kv_lens(wl)
+        tl = {n: synth.device_tensor(wl, n, dev) for n in ("q", "k", "v", "iq", "ik")}
+        qo_t, kl_t = torch.from_numpy(qo_l).to(dev), torch.from_numpy(kl_l).to(dev)
+        sel_l = torch.empty((wl.B, wl.Nq, wl.G, wl.K), dtype=torch.int32, device=dev)
+        out_l = torch.empty_like(tl["q"])
+        wsi = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_INDEX_SELECT, wl.B, wl.Nq, wl.Nk, wl.G, 0, 0, wl.di,
+                                                   wl.Bs, wl.K, msa.MSA_BF16), dev)
+        wsa = msa.workspace(msa.msa_workspace_size(msa.MSA_OP_PREFILL, wl.B, wl.Nq, wl.Nk, wl.G, wl.Hq, wl.d, 0,
+                                                   wl.Bs, wl.K, msa.MSA_BF16), dev)
+
+        def step_l():
+            msa.msa_index_select(tl["iq"], tl["ik"], qo_t, kl_t, wl.Bs, wl.K, sel=sel_l, ws=wsi)
+            msa.msa_sparse_attn_prefill(tl["q"], tl["k"], tl["v"], sel_l, qo_t, kl_t, wl.Bs, wl.K, out=out_l,
+                                        ws=wsa)
+
+        lms, _, lclocks, _ = time_steps(step_l, steps, warmup, profile=False)
+        _, lprof, _, _ = time_steps(step_l, steps, 0, profile=True)
+        for ws_ in (wsi, wsa):
+            st_ = msa.msa_read_status(ws_)
+            if st_ != 0:
+                raise RuntimeError(f"device status after {name}: {msa.msa_status_string(st_)}")
+        lwork = prefill_work(wl, sel_l, qo_l, kl_l)
+        l_tot = dist.max(sum(lms) / 1e3)
+        res = {"value": round(dist.sum(wl.B * wl.Nq * steps) / l_tot, 1), "unit": "tokens/s",
+               "ms_per_step": round(float(np.mean(lms)), 4), "steps": steps, "warmup": warmup,
+               "config": {"workload": wl.name, "batch": wl.B, "seq_len": wl.Nq, "Bs": wl.Bs, "K": wl.K,
+                          "hot_blocks": wl.hot},
+               "roofline_all": [r for r in (roofline_for(k_, lprof, lwork, peaks, peak_src, wl.name, steps)
+                                            for k_ in lprof) if r],
+               "kernels": {k_: {"launches": v_[0], "ms_per_step": round(v_[1] / steps, 4)} for k_, v_ in lprof.items()},
+               "gpu_launches": sum(v_[0] for v_ in lprof.values()), "clocks": lclocks,
+               "work": {"index_flops": lwork["index_flops"], "attn_flops": lwork["attn_flops"],
+                        "attended_keys": lwork["attended_keys"]}}
+        del tl, sel_l, out_l, wsi, wsa
+        torch.cuda.empty_cache()
+        return res
+
+    sweep = None
+    if not args.no_sweep:
+        sweep = {}
+        for name, nsteps in (("prefill_128k_bs64", min(args.steps, 10)), ("prefill_128k_bs32", min(args.steps, 10)),
+                             ("prefill_1m", 3)):
+            sweep[name] = prefill_leg(name, nsteps, args.warmup)
 
     # ------------------------------ decode -----------------------------
     decode = None
@@ -609,7 +662,7 @@ def run_msa(args, dist):
         "roofline": roof, "roofline_all": all_roofs, "kernels": kernels, "gpu_launches": launches,
         "kernel_times": "per-kernel CUDA events on the launching stream, in a second pass of the same steps "
                         "(the timed pass carries no events between kernels)",
-        "clocks": clocks, "e2e": e2e, "decode": decode, "kl_aux": kl_leg, "backward": bwd_leg,
+        "clocks": clocks, "e2e": e2e, "decode": decode, "kl_aux": kl_leg, "backward": bwd_leg, "prefill_sweep": sweep,
         "work": {"index_flops": work["index_flops"], "attn_flops": work["attn_flops"],
                  "attended_keys": work["attended_keys"]},
         "wall_s_timed_region": round(wall, 3),
@@ -654,6 +707,26 @@ def oracle_prefill_rows(w, rows, ik_host):
     return (t1 - t0) + (t3 - t2)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else the machine type)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+
+    return platform.machine() or "unknown"
+
+
 def sample_rows(w, n, offset=0):
     """n query rows evenly spaced over the sequence (their mean cost equals the
     mean cost per token, which grows with position)."""
@@ -661,16 +734,80 @@ def sample_rows(w, n, offset=0):
     return np.array([int((k + 0.5) * step) + offset for k in range(n)], np.int32) % w.Nq
 
 
-def cpu_baseline(w, rows_n):
+def oracle_full_prefill(w):
+    """The oracle over every row of a prefill workload (dense host inputs).
+    Returns seconds inside the oracle (input generation excluded)."""
+    import oracle
+
+    h = {n: synth.host_tensor(w, n) for n in ("q", "k", "v", "iq", "ik")}
+    t0 = time.perf_counter()
+    oracle.msa_forward(h["q"], h["k"], h["v"], h["iq"], h["ik"], w.Bs, w.K, q_offset=synth.q_offsets(w),
+                       kv_len=synth.kv_lens(w))
+    return time.perf_counter() - t0
+
+
+def oracle_full_decode(w):
+    """The oracle over every sequence of a decode workload: one batched index
+    selection over the whole index-key cache, then attention per sequence on a
+    host K/V holding that sequence's selected blocks. Returns oracle seconds."""
+    import oracle
+
+    kl = synth.kv_lens(w)
+    qo = (kl - 1).astype(np.int32)
+    ik = synth.host_tensor(w, "ik")
+    iq = synth.host_tensor(w, "iq").reshape(w.B, w.G, w.di)
+    q = synth.host_tensor(w, "q").reshape(w.B, w.Hq, w.d)
+    rb, ri = np.arange(w.B, dtype=np.int32), np.zeros(w.B, np.int32)
+    t0 = time.perf_counter()
+    sel = oracle.index_select(iq, ik, rb, ri, qo, kl, w.Bs, w.K)
+    secs = time.perf_counter() - t0
+    del ik
+    row = w.Hkv * w.d
+    k = np.zeros((1, w.Nk, w.Hkv, w.d), np.float32)
+    v = np.zeros((1, w.Nk, w.Hkv, w.d), np.float32)
+    for b in range(w.B):
+        spans = [(t * w.Bs, min((t + 1) * w.Bs, w.Nk)) for t in sorted(set(int(x) for x in sel[b].reshape(-1) if x >= 0))]
+        for j0, j1 in spans:
+            k[0, j0:j1] = synth.host_range(w, "k", (b * w.Nk + j0) * row, (j1 - j0) * row).reshape(j1 - j0, w.Hkv, w.d)
+            v[0, j0:j1] = synth.host_range(w, "v", (b * w.Nk + j0) * row, (j1 - j0) * row).reshape(j1 - j0, w.Hkv, w.d)
+        t0 = time.perf_counter()
+        oracle.sparse_attn(q[b:b + 1], k, v, sel[b:b + 1], np.zeros(1, np.int32), np.zeros(1, np.int32), qo[b:b + 1],
+                           kl[b:b + 1], w.Bs, w.K)
+        secs += time.perf_counter() - t0
+        for j0, j1 in spans:
+            k[0, j0:j1] = 0.0
+            v[0, j0:j1] = 0.0
+    return secs
+
+
+def cpu_baseline(w, rows_n, full_legs=True):
+    """The oracle timed on this host's cores: a row sample of the bench
+    workload (the headline CPU figure), and full runs of the tiny fp32, 8K
+    prefill and decode workloads."""
     import oracle
 
     ik = synth.host_tensor(w, "ik")
     rows = sample_rows(w, rows_n)
     secs = oracle_prefill_rows(w, rows, ik)
-    return {"value": round(len(rows) / secs, 2), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{len(rows)} query rows evenly spaced over the {w.Nq}-token sequence, all {w.G} groups / "
-                      f"{w.Hq} heads; index select + attention in fp64; tokens/s = rows / oracle seconds",
-            "seconds": round(secs, 2)}
+    del ik
+    res = {"value": round(len(rows) / secs, 2), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+           "cpu_model": cpu_model(),
+           "sample": f"{len(rows)} query rows evenly spaced over the {w.Nq}-token sequence, all {w.G} groups / "
+                     f"{w.Hq} heads; index select + attention in fp64; tokens/s = rows / oracle seconds",
+           "seconds": round(secs, 2)}
+    if full_legs:
+        full = {}
+        for name in ("tiny_fp32", "prefill_8k"):
+            wl = synth.WORKLOADS[name]
+            sec = oracle_full_prefill(wl)
+            full[name] = {"value": round(wl.B * wl.Nq / sec, 2), "unit": "tokens/s", "seconds": round(sec, 3),
+                          "rows": wl.B * wl.Nq, "what": "every query row, index select + attention"}
+        wd = synth.WORKLOADS["decode_b64"]
+        sec = oracle_full_decode(wd)
+        full[wd.name] = {"value": round(wd.B / sec, 2), "unit": "tokens/s", "seconds": round(sec, 3), "rows": wd.B,
+                         "what": "every sequence's new token, index select over its cache + attention"}
+        res["full"] = full
+    return res
 
 
 def run_reference(args, dist):
@@ -679,7 +816,8 @@ def run_reference(args, dist):
 
     w = synth.WORKLOADS[args.workload]
     ik = synth.host_tensor(w, "ik")
-    rows_per_step = 8
+    # enough rows per step that the oracle's row-parallel threads all work
+    rows_per_step = 16 * oracle.threads()
     for s in range(args.warmup):
         oracle_prefill_rows(w, sample_rows(w, rows_per_step, offset=s), ik)
     secs = 0.0
@@ -691,9 +829,13 @@ def run_reference(args, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "batch": w.B, "seq_len": w.Nq, "Bs": w.Bs, "K": w.K},
+        "config": {"workload": w.name, "batch": w.B, "seq_len": w.Nq, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "di": w.di, "Bs": w.Bs, "K": w.K, "hot_blocks": w.hot, "parallelism": f"replicas x{dist.world}",
+                   "l2": "n/a (host)"},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-                         "sample": f"{rows_per_step} evenly spaced query rows per step (all groups/heads)"},
+                         "cpu_model": cpu_model(),
+                         "sample": f"{rows_per_step} evenly spaced query rows per step (all groups/heads), "
+                                   f"index select + attention in fp64"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
