@@ -47,12 +47,14 @@ namespace {
 constexpr int kRows = 128;  // query rows per tile (M of both MMAs)
 constexpr int kAttnThreads = 512;
 constexpr int kLaunchRegs = 128;  // registers per thread at launch (checked on the host)
-constexpr int kProdRegs = 88, kEpiRegs = 168;
-static_assert(256 * kProdRegs + 256 * kEpiRegs <= kAttnThreads * kLaunchRegs, "register split");
-constexpr int kKvWarp = 0;
-constexpr int kGatherWarp0 = 1;  // warps 1..4: cp.async gathers
-constexpr int kMmaWarpA = 5;
-constexpr int kEpiWarp0 = 8;  // warps 8..15 (warpgroups 2 and 3)
+// warpgroup 0: producers (K/V, gathers, MMA); 1: partial stores; 2-3: softmax
+constexpr int kProdRegs = 80, kStoreRegs = 96, kSoftRegs = 168;
+static_assert(128 * (kProdRegs + kStoreRegs + 2 * kSoftRegs) <= kAttnThreads * kLaunchRegs, "register split");
+constexpr int kTmaWarp0 = 0;  // warps 0..2: query-row gathers (four-row TMA gathers)
+constexpr int kTmaWarps = 3;
+constexpr int kMmaWarpA = 3;  // MMA issuer, TMEM owner and K/V loads
+constexpr int kStoreWarp0 = 4;  // warps 4..7 (warpgroup 1)
+constexpr int kEpiWarp0 = 8;    // warps 8..15 (warpgroups 2 and 3)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -253,14 +255,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
-               "r"(src_bytes), "l"(policy)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -296,12 +290,12 @@ struct TileRuns {
   }
 };
 
-constexpr int kRing = 4;  // gathered-query tile ring depth (one cp.async gather warp per slot)
-static_assert(kRing <= 4, "cp.async gather warps are warps 1..4");
-// Rows of a tile gathered by cp.async (the rest by four-row TMA gathers):
-// the two paths have separate in-flight limits, so they run side by side.
-constexpr int kRowsLsu = 80;
-static_assert(kRowsLsu % 8 == 0 && (kRows - kRowsLsu) % 4 == 0 && kRows - kRowsLsu <= 128, "row split");
+constexpr int kRing = 4;  // gathered-query tile ring depth (tile z in slot z % kRing)
+static_assert(kMmaWarpA == kTmaWarp0 + kTmaWarps && kMmaWarpA < 4, "warpgroup 0: gather warps, then the MMA warp");
+// Query rows reach the ring by four-row TMA gathers (512 bytes each, 64 per
+// tile). Issuing one takes a warp about 100 cycles, so the gather rate grows
+// with the number of warps that issue them; measured alternatives were
+// slower: a cp.async warp issues about a third of that rate.
 
 
 template <int D, int BS>
@@ -324,8 +318,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* k_buf = smem;                    // [NH][BS][128 B]
   uint8_t* v_buf = k_buf + kKBytes;         // [NH][BS][128 B]
   uint8_t* ring = v_buf + kKBytes;          // kRing x kSlot: gathered Q tiles
-  int* meta = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kRing + 1][128] gathered tiles' entries (query*64+slot) or -1
-  int* run_lo = meta + (kRing + 1) * kRows;                 // [kKvoMaxPhases]
+  int* meta = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kRing][128] tiles' entries (query*64+slot) or -1
+  int* run_lo = meta + kRing * kRows;                       // [kKvoMaxPhases]
   int* run_pref = run_lo + kKvoMaxPhases;                   // [kKvoMaxPhases + 1]
   // mbarriers need 8-byte alignment: round the barrier area up to 16 bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(
@@ -348,14 +342,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
     for (int r = 0; r < kRing; ++r) {
-      tc::mbar_init(&q_full[r], kRowsLsu < kRows ? 2 : 1);  // the gather warp: TMA bytes + its own copies
+      tc::mbar_init(&q_full[r], 1);  // the tile's gather warp (arrival with the expected bytes)
       tc::mbar_init(&q_empty[r], 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&s_full[s], 1);
       tc::mbar_init(&p_full[s], 4);
       tc::mbar_init(&o_full[s], 1);
-      tc::mbar_init(&o_empty[s], 4);
+      tc::mbar_init(&o_empty[s], 4);  // the four store warps
     }
     tc::mbar_init(done_bar, 1);
     tc::mbar_init(never_bar, 1);
@@ -376,7 +370,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::tmem_alloc(tmem_slot, 512);
     tc::tmem_relinquish();
   }
-  if (warp == kKvWarp && lane == 0) {
+  if (warp == kMmaWarpA && lane == 0) {
     tc::tma_prefetch(&tmK);
     tc::tma_prefetch(&tmV);
     tc::tma_prefetch(&tmQ);
@@ -395,54 +389,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // Each register re-allocation sits at the top of its warpgroups' branch
   // (one instruction for all warps of a warpgroup) so that the compiler
   // budgets each branch with its own register count.
-  if (warp < kEpiWarp0) {
+  if (warp < kStoreWarp0) {
   tc::regs_dec<kProdRegs>();
-  if (warp == kKvWarp) {
-    // ----------------------------- K/V producer -----------------------------
-    if (lane == 0) {
-      const uint64_t pol_kv = tc::policy_evict_first();  // each block's K/V is read by one or two CTAs
-      TileRuns runs{run_lo, run_pref};
-      int prev_bin = -1, loads = 0;
-      for (int z = 0; z < n; ++z) {
-        const int bin = p.tiles[runs.at(z)].x;
-        if (bin == prev_bin) continue;
-        prev_bin = bin;
-        if (!tc::mbar_wait(kv_empty, (loads & 1) ^ 1, abort_flag)) {
-          fail();
-          break;
-        }
-        const int g = bin / p.nblk, t = bin % p.nblk;
-        tc::mbar_arrive_expect_tx(kv_full, 2 * kKBytes);
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          tc::tma_load_4d_hint(k_buf + h * kKVHalf, &tmK, kv_full, h * 64, g, t * BS, p.b, pol_kv);
-          tc::tma_load_4d_hint(v_buf + h * kKVHalf, &tmV, kv_full, h * 64, g, t * BS, p.b, pol_kv);
-        }
-        ++loads;
-      }
-      int zero = 0;
-      if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // drain the last copy
-    }
-  } else if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kRing) {
+  if (warp >= kTmaWarp0 && warp < kTmaWarp0 + kTmaWarps) {
     // ------------------------------ query-row gather ------------------------------
-    // Gather warp gw owns ring slot gw (tiles z = gw, gw + kRing, ...). Its
-    // tiles' entries are fetched kRing tiles ahead. Per tile it first issues
-    // four-row TMA gathers for rows [kRowsLsu, 128) (lane l < kTmaLanes: one
-    // gather per 64-column half; the bytes are counted on the slot's barrier
-    // with the warp's first arrival), then copies rows [0, kRowsLsu) in
-    // 16-byte cp.async chunks (a warp instruction covers whole 256-byte rows);
-    // its second arrival follows its own copies. Both paths write the
-    // 128B-swizzled K-major layout (the swizzle is address-based); they have
-    // separate in-flight limits, so they run side by side. Rows of padding
-    // entries read the chunk's first query (finite values; their outputs are
-    // never read).
-    const int gw = warp - kGatherWarp0;
-    constexpr int kCpr = D / 8;            // 16-byte chunks per row
-    constexpr int kRowsPerIt = 32 / kCpr;  // rows per warp instruction
+    // Gather warp gi takes tiles z = gi, gi + kTmaWarps, ... (ring slot z %
+    // kRing); each tile's entries are fetched one of its tiles ahead. Lane l
+    // gathers rows [4 l, 4 l + 4) with one four-row TMA gather per 64-column
+    // half into the 128B-swizzled K-major layout (the swizzle is
+    // address-based); the bytes are counted on the slot's barrier with the
+    // warp's arrival. Rows of padding entries read the chunk's first query
+    // (finite values; their outputs are never read).
+    const int gi = warp - kTmaWarp0;
     constexpr int kEntPerLane = kRows / 32;
-    constexpr int kTmaLanes = (kRows - kRowsLsu) / 4;
+    static_assert(kRows == 32 * 4, "one lane per four rows");
     const int per_tile = kRows / p.hpg;
-    int* my_meta = meta + gw * kRows;
     int4 tl = make_int4(0, 0, 0, 0);
     int ev[kEntPerLane];
     TileRuns runs{run_lo, run_pref};
@@ -456,66 +417,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ev[x] = e < per_tile ? p.entries[int64_t(zt) * per_tile + e] : -1;
       }
     };
-    if (gw < n) fetch(gw);
-    int last = -1;  // the last tile this warp issued
-    for (int z = gw; z < n; z += kRing) {
-      if (!tc::mbar_wait(&q_empty[gw], ((z / kRing) & 1) ^ 1, abort_flag)) {
+    if (gi < n) fetch(gi);
+    int issued = 0, last = -1;  // tiles issued by this warp, the last of them
+    for (int z = gi; z < n; z += kTmaWarps) {
+      const int rs = z % kRing;
+      if (!tc::mbar_wait(&q_empty[rs], ((z / kRing) & 1) ^ 1, abort_flag)) {
         fail();
         break;
       }
+      int* my_meta = meta + rs * kRows;
 #pragma unroll
       for (int x = 0; x < kEntPerLane; ++x)
         if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = lane + 32 * x < tl.z ? ev[x] : -1;
       __syncwarp();
       const int g = tl.x / p.nblk;
-      if constexpr (kTmaLanes > 0) {
-        int rows[4];
+      int rows[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int row = kRowsLsu + (lane % kTmaLanes) * 4 + j;
-          const int ent = my_meta[row / p.hpg];
-          const int il = ent >= 0 ? (ent >> 6) : 0;
-          rows[j] = (p.b * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg;
-        }
-        if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[gw], uint32_t(kRows - kRowsLsu) * D * 2);
-        __syncwarp();
-        if (lane < kTmaLanes) {
-          uint8_t* dst = ring + gw * kSlot + (kRowsLsu + lane * 4) * 128;
-#pragma unroll
-          for (int hf = 0; hf < NH; ++hf)
-            tc::tma_gather4_hint(dst + hf * (kRows * 128), &tmQ, &q_full[gw], hf * 64, rows[0], rows[1], rows[2],
-                                 rows[3], pol_q);
-        }
-      }
-      last = z;
-      const uint32_t slot = tc::smem_u32(ring + gw * kSlot);
-      const int chunk = lane % kCpr, sub = lane / kCpr;
-      const uint32_t hf = chunk >> 3, cc = chunk & 7;
-#pragma unroll 4
-      for (int it = 0; it < kRowsLsu / kRowsPerIt; ++it) {
-        const int row = it * kRowsPerIt + sub;
+      for (int j = 0; j < 4; ++j) {
+        const int row = lane * 4 + j;
         const int ent = my_meta[row / p.hpg];
         const int il = ent >= 0 ? (ent >> 6) : 0;
-        const __nv_bfloat16* src =
-            p.q + ((int64_t(p.b) * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg) * D + chunk * 8;
-        cp_async16_hint(slot + hf * (kRows * 128) + row * 128 + ((cc ^ uint32_t(row & 7)) << 4), src,
-                        ent >= 0 ? 16u : 0u, pol_q);
+        rows[j] = (p.b * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg;
       }
-      cp_async_commit();
-      if (z + kRing < n) fetch(z + kRing);
-      cp_async_wait<0>();
-      tc::fence_proxy_async_smem();
+      if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[rs], uint32_t(kRows) * D * 2);
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&q_full[gw]);
+      {
+        uint8_t* dst = ring + rs * kSlot + lane * 4 * 128;
+#pragma unroll
+        for (int hf = 0; hf < NH; ++hf)
+          tc::tma_gather4_hint(dst + hf * (kRows * 128), &tmQ, &q_full[rs], hf * 64, rows[0], rows[1], rows[2],
+                               rows[3], pol_q);
+      }
+      ++issued;
+      last = z;
+      if (z + kTmaWarps < n) fetch(z + kTmaWarps);
+      __syncwarp();  // every lane has read my_meta before the slot comes round again
     }
-    cp_async_wait<0>();
-    // drain: no gather may still be landing in shared memory when the CTA exits
+    // drain after an abort: no gather may still be landing in shared memory
+    // when the CTA exits. (In a full run the MMA warp has waited for every
+    // tile before the final barrier.) Waits for the last tile this warp issued
+    // into each ring slot; one that another warp's later tile has already
+    // overtaken ran its course long ago, and its wait ends at the bound.
     int zero = 0;
-    if (kTmaLanes > 0 && last >= 0 && lane == 0) tc::mbar_wait(&q_full[gw], (last / kRing) & 1, &zero);
+    if (*abort_flag && lane == 0)
+      for (int k = 0; k * kTmaWarps < kRing && k < issued; ++k) {
+        const int z = last - k * kTmaWarps;
+        tc::mbar_wait(&q_full[z % kRing], (z / kRing) & 1, &zero);
+      }
   } else if (warp == kMmaWarpA) {
     // ------------------------------- MMA issuer -------------------------------
     if (lane == 0) {
-      int prev_bin = -1, kv_uses = 0;
+      const uint64_t pol_kv = tc::policy_evict_first();  // each block's K/V is read by one or two CTAs
+      int prev_bin = -1, loads = 0;
       bool alive = true;
       auto issue_pv = [&](int z, bool last_of_bin) -> bool {
         const int s = z & 1;
@@ -546,15 +499,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int bin = bin_next;
         if (z + 1 < n) bin_next = p.tiles[runs.at(z + 1)].x;
         if (bin != prev_bin) {
+          // a new key block: the previous block's last PV, then this block's
+          // K and V over the same buffers once that PV has read V
           if (z > 0 && !issue_pv(z - 1, true)) {
             fail();
             break;
           }
-          if (!tc::mbar_wait(kv_full, kv_uses & 1, abort_flag)) {
+          if (loads > 0 && !tc::mbar_wait(kv_empty, (loads - 1) & 1, abort_flag)) {
             fail();
             break;
           }
-          ++kv_uses;
+          const int g = bin / p.nblk, t = bin % p.nblk;
+          tc::mbar_arrive_expect_tx(kv_full, 2 * kKBytes);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            tc::tma_load_4d_hint(k_buf + h * kKVHalf, &tmK, kv_full, h * 64, g, t * BS, p.b, pol_kv);
+            tc::tma_load_4d_hint(v_buf + h * kKVHalf, &tmV, kv_full, h * 64, g, t * BS, p.b, pol_kv);
+          }
+          ++loads;
+          if (!tc::mbar_wait(kv_full, (loads - 1) & 1, abort_flag)) {
+            fail();
+            break;
+          }
         }
         if (!tc::mbar_wait(&q_full[rs], (z / kRing) & 1, abort_flag)) {
           fail();
@@ -585,26 +551,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!issue_pv(n - 1, true)) fail();
       }
       int zero = 0;
+      if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // no K/V copy still landing
       tc::mma_commit(done_bar);
       tc::mbar_wait(done_bar, 0, &zero);
     }
-  }  // warps 6-7: idle
+  }  // other warps of warpgroup 0: none
+  } else if (warp < kEpiWarp0) {
+    tc::regs_dec<kStoreRegs>();
+    // --------------------------- partial stores ---------------------------
+    // Warpgroup 1 reads every tile's O (TMEM lanes of its warp's quarter)
+    // and stores it as the tile's bf16 partial rows: 16-byte chunk c of row
+    // r of tile zg at part_o[(zg * D/8 + c) * 128 + r], so each warp store
+    // instruction writes 32 consecutive rows' chunk (512 contiguous bytes).
+    // P was normalised by the row sum before PV, so O is the partial itself.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    TileRuns runs{run_lo, run_pref};
+    const uint64_t pol_part = tc::policy_evict_first();  // partials are read back once, by the combine
+    for (int z = 0; z < n; ++z) {
+      const int s = z & 1;
+      const int zg = runs.at(z);  // the chunk's tile index = its partial row block
+      if (!tc::mbar_wait(&o_full[s], (z >> 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
+      uint4* dst = p.part_o + int64_t(zg) * (D / 8) * kRows + r;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        tc::tmem_ld_32x32b_x32(o_addr + c0, ov);
+        tc::tmem_ld_wait();
+        if (c0 + 32 >= D) {  // O is in registers: the next PV may overwrite it
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&o_empty[s]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 o;
+          o.x = pack_bf16(__uint_as_float(ov[c * 8 + 0]), __uint_as_float(ov[c * 8 + 1]));
+          o.y = pack_bf16(__uint_as_float(ov[c * 8 + 2]), __uint_as_float(ov[c * 8 + 3]));
+          o.z = pack_bf16(__uint_as_float(ov[c * 8 + 4]), __uint_as_float(ov[c * 8 + 5]));
+          o.w = pack_bf16(__uint_as_float(ov[c * 8 + 6]), __uint_as_float(ov[c * 8 + 7]));
+          tc::st_v4_hint(dst + (c0 / 8 + c) * kRows, o, pol_part);
+        }
+      }
+    }
   } else {
-    tc::regs_inc<kEpiRegs>();
-    // -------------------------------- epilogue --------------------------------
+    tc::regs_inc<kSoftRegs>();
+    // -------------------------------- softmax --------------------------------
+    // Warpgroups 2 and 3 take alternate tiles (TMEM set s = z & 1): the whole
+    // S row of a thread's TMEM lane in registers, causal mask in the local
+    // block, exact softmax with the row sum folded into P (bf16 pairs written
+    // back over S for the PV MMA), and the row's log-sum-exp stored for the
+    // combine.
     const int w = (warp - kEpiWarp0) >> 2;         // warpgroup: tiles z with z % 2 == w
     const int quarter = warp & 3;                  // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;             // tile row
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
     TileRuns runs{run_lo, run_pref};
-    const uint64_t pol_part = tc::policy_evict_first();  // partials are read back once, by the combine
+    const uint64_t pol_part = tc::policy_evict_first();
     for (int z = w; z < n; z += 2) {
       const int s = z & 1;  // == w
       // this tile's metadata straight from global memory (the Q ring slot and
       // its staged metadata are recycled as soon as QK^T has consumed them);
       // the loads are in flight while S is being computed
-      const int zg = runs.at(z);  // the chunk's tile index = its partial row block
+      const int zg = runs.at(z);
       const int4 tl = p.tiles[zg];
       const int e_raw = p.entries[int64_t(zg) * (kRows / p.hpg) + r / p.hpg];
       const int ent = r / p.hpg < tl.z ? e_raw : -1;
@@ -637,60 +653,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j < BS; j += 2)
         m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
       const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      // probabilities as bf16 pairs written back over S in TMEM (the PV MMA
-      // reads its A operand from there), row sum in fp32
+      // probabilities (in place) and their sum in fp32
       const float mneg = -mx * p.scale_log2;
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < BS; ++j) {
+        const float pj = ex2(fmaf(__uint_as_float(v[j]), p.scale_log2, mneg));
+        l4[j & 3] += pj;
+        v[j] = __float_as_uint(pj);
+      }
+      const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // P / l as bf16 pairs written back over S in TMEM (the PV MMA reads its
+      // A operand from there): keys 2c (low half) and 2c+1 (high half) in column c
 #pragma unroll
       for (int c0 = 0; c0 < BS / 32; ++c0) {
         uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j]), p.scale_log2, mneg));
-          const float p1 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j + 1]), p.scale_log2, mneg));
-          l4[(j >> 1) & 3] += p0 + p1;
-          pk[j >> 1] = pack_bf16(p0, p1);  // keys 2c (low half) and 2c+1 (high half) in column c
-        }
+        for (int j = 0; j < 32; j += 2)
+          pk[j >> 1] = pack_bf16(__uint_as_float(v[c0 * 32 + j]) * inv, __uint_as_float(v[c0 * 32 + j + 1]) * inv);
         tc::tmem_st_32x32b_x16(s_addr + c0 * 16, pk);
       }
-      const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
       tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&p_full[s]);
-      // output: O / l in bf16, stored from registers. Partial row r of tile zg
-      // keeps its 16-byte chunk c at part_o[(zg * D/8 + c) * 128 + r], so each
-      // warp store instruction writes 32 consecutive rows' chunk: 512 bytes.
-      if (!tc::mbar_wait(&o_full[s], (z >> 1) & 1, abort_flag)) {
-        fail();
-        break;
-      }
-      tc::fence_after_sync();
-      const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = p.part_o + int64_t(zg) * (D / 8) * kRows + r;
-      constexpr int kOH = D > 64 ? 64 : D;  // O columns per TMEM round trip
-#pragma unroll
-      for (int h0 = 0; h0 < D; h0 += kOH) {
-        uint32_t ov[kOH];
-#pragma unroll
-        for (int c = 0; c < kOH / 32; ++c) tc::tmem_ld_32x32b_x32(o_addr + h0 + c * 32, ov + c * 32);
-        tc::tmem_ld_wait();
-        if (h0 + kOH >= D) {  // O is in registers: the next PV may overwrite it
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&o_empty[s]);
-        }
-#pragma unroll
-        for (int c = 0; c < kOH / 8; ++c) {
-          uint4 o;
-          o.x = pack_bf16(__uint_as_float(ov[c * 8 + 0]) * inv, __uint_as_float(ov[c * 8 + 1]) * inv);
-          o.y = pack_bf16(__uint_as_float(ov[c * 8 + 2]) * inv, __uint_as_float(ov[c * 8 + 3]) * inv);
-          o.z = pack_bf16(__uint_as_float(ov[c * 8 + 4]) * inv, __uint_as_float(ov[c * 8 + 5]) * inv);
-          o.w = pack_bf16(__uint_as_float(ov[c * 8 + 6]) * inv, __uint_as_float(ov[c * 8 + 7]) * inv);
-          tc::st_v4_hint(dst + (h0 / 8 + c) * kRows, o, pol_part);
-        }
-      }
       tc::st_f32_hint(p.part_lse + int64_t(zg) * kRows + r, valid ? mx * p.scale + logf(l) : 0.f, pol_part);
     }
   }
@@ -708,31 +695,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // rows (found through the reverse map), stored chunk-major: 16-byte chunk c
 // of row r in tile zg at ((zg * D/8 + c) * 128 + r). Lane vector vi takes
 // head vi % hpg and chunk vi / hpg, so neighbouring lanes read neighbouring
-// rows of one chunk. Each lane owns NU vectors. Slots are merged in slot
-// order with log-sum-exp weights. The next item's selection row and reverse
-// map row are loaded while the current item's partials are in flight.
+// rows of one chunk; hpg divides 32, so every vector of a lane has the head
+// h = lane % hpg. Each lane owns NU vectors.
+// Per item: the valid slots (slot order) and their lse values go to the
+// warp's shared-memory area; each lane forms its head's merge weights
+// w_s = exp(lse_s - max) / sum_s exp(lse_s - max), then accumulates
+// sum_s w_s * partial_s in slot order with a batch of slots' loads in flight.
+// Weights known up front need no running rescale, which keeps the register
+// count low enough for several CTAs per SM (more loads in flight). The next
+// item's selection and reverse-map rows are loaded while the current item's
+// partials are in flight. Deterministic; no atomics on any output.
 // ---------------------------------------------------------------------------
+constexpr int kCmbWarps = 8;
+inline size_t combine_smem_bytes(int K, int hpg) { return size_t(kCmbWarps) * (2 * K + K * hpg) * 4; }
+
 template <int NU>
-__global__ void __launch_bounds__(256) attn_combine_kernel(
+__global__ void __launch_bounds__(256, NU <= 2 ? 2 : 1) attn_combine_kernel(
     const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
     const uint4* __restrict__ part_o, const float* __restrict__ part_lse, const int* __restrict__ rev, int b,
     int Nq, int Nk, int Hq, int G, int K, int Bs, int nblk, int D, int c0, int cq, __nv_bfloat16* __restrict__ out,
     float* __restrict__ lse_out) {
   constexpr int kBatch = NU <= 2 ? 8 : (NU == 4 ? 4 : 2);  // slots whose loads are in flight together
-  constexpr int kWarps = 256 / 32;
-  __shared__ int slot_e[kWarps][2][kMaxK];
+  extern __shared__ int cmb_smem[];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  const int64_t nitems = int64_t(cq) * G;
-  const int64_t stride = int64_t(gridDim.x) * kWarps;
   const int hpg = Hq / G;
-  const int nvec = hpg * D / 8;  // 16-byte vectors per slot
+  int* slot_e = cmb_smem + wl * (2 * K + K * hpg);                     // [2][K] valid slots' entries
+  float* lse_s = reinterpret_cast<float*>(slot_e + 2 * K);             // [K][hpg] their lse values
+  const int64_t nitems = int64_t(cq) * G;
+  const int64_t stride = int64_t(gridDim.x) * kCmbWarps;
+  const int nvec = hpg * D / 8;
+  const int h = lane % hpg;  // the head of every vector of this lane
   const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
-  int head[NU], voff[NU];
+  int voff[NU];
 #pragma unroll
   for (int u = 0; u < NU; ++u) {
     const int vi = lane + 32 * u;
-    head[u] = vi < nvec ? vi % hpg : 0;
-    voff[u] = vi < nvec ? (vi / hpg) * 128 + head[u] : 0;  // chunk-major offset from the slot's first row
+    voff[u] = vi < nvec ? (vi / hpg) * 128 + h : 0;  // chunk-major offset from the slot's first row
   }
   // an item's selection and reverse-map entries for slots lane and lane + 32
   int s_t[2], s_e[2];
@@ -741,28 +739,28 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
     const int32_t* srow = sel + ((int64_t(b) * Nq + c0 + il) * G + g) * K;
     const int* rv = rev + (int64_t(il) * G + g) * K;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int k = lane + 32 * h;
-      s_t[h] = k < K ? srow[k] : -1;
-      s_e[h] = k < K ? rv[k] : 0;
+    for (int x = 0; x < 2; ++x) {
+      const int k = lane + 32 * x;
+      s_t[x] = k < K ? srow[k] : -1;
+      s_e[x] = k < K ? rv[k] : 0;
     }
   };
-  // valid slots in slot order, as partial-row entries, into slot_e[wl][buf]
+  // valid slots in slot order, as partial-row entries, into slot_e[buf]
   auto meta_finish = [&](int64_t it, int buf) {
     const int pos = sv.q0 + c0 + int(it / G);
     int nv = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int k = lane + 32 * h;
-      const bool ok = k < K && sv.ok && entry_valid(s_t[h], pos, Bs, nblk);
+    for (int x = 0; x < 2; ++x) {
+      const int k = lane + 32 * x;
+      const bool ok = k < K && sv.ok && entry_valid(s_t[x], pos, Bs, nblk);
       const unsigned bal = __ballot_sync(0xffffffffu, ok);
-      if (ok) slot_e[wl][buf][nv + __popc(bal & ((1u << lane) - 1u))] = s_e[h];
+      if (ok) slot_e[buf * K + nv + __popc(bal & ((1u << lane) - 1u))] = s_e[x];
       nv += __popc(bal);
     }
     __syncwarp();
     return nv;
   };
-  int64_t item = int64_t(blockIdx.x) * kWarps + wl;
+  int64_t item = int64_t(blockIdx.x) * kCmbWarps + wl;
   int buf = 0, nvalid = 0;
   if (item < nitems) {
     meta_load(item);
@@ -773,53 +771,44 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
     if (next < nitems) meta_load(next);
     const int il = int(item / G), g = int(item % G);
     const int i = c0 + il;
-    float m[NU], wsum[NU], acc[NU][8];
+    const int* se = slot_e + buf * K;
+    // the slots' lse values of every head of the group
+    for (int x = lane; x < nvalid * hpg; x += 32) lse_s[x] = part_lse[int64_t(se[x / hpg]) * hpg + x % hpg];
+    __syncwarp();
+    // this lane's head: maximum, then the sum of the weights (slot order)
+    float mx = -INFINITY;
+    for (int j = 0; j < nvalid; ++j) mx = fmaxf(mx, lse_s[j * hpg + h]);
+    float den = 0.f;
+    for (int j = 0; j < nvalid; ++j) den += expf(lse_s[j * hpg + h] - mx);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    float acc[NU][8];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-      m[u] = -INFINITY;
-      wsum[u] = 0.f;
+    for (int u = 0; u < NU; ++u)
 #pragma unroll
       for (int x = 0; x < 8; ++x) acc[u][x] = 0.f;
-    }
-    // kBatch slots at a time: all their loads first, then a running
-    // log-sum-exp rescale (slot order is fixed: the result is deterministic)
     for (int j0 = 0; j0 < nvalid; j0 += kBatch) {
-      float l[kBatch][NU];
       uint4 raw[kBatch][NU];
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const bool have = j0 + j < nvalid;
-        const int64_t R = have ? int64_t(slot_e[wl][buf][j0 + j]) * hpg : 0;  // the slot's first partial row
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const bool have = j0 + jj < nvalid;
+        const int64_t R = have ? int64_t(se[j0 + jj]) * hpg : 0;  // the slot's first partial row
         const uint4* base = part_o + (R >> 7) * (D / 8) * 128 + (R & 127);
 #pragma unroll
-        for (int u = 0; u < NU; ++u) {
-          const int vi = lane + 32 * u;
-          l[j][u] = have ? part_lse[R + head[u]] : -INFINITY;
-          raw[j][u] = (have && vi < nvec) ? base[voff[u]] : make_uint4(0, 0, 0, 0);
-        }
+        for (int u = 0; u < NU; ++u)
+          raw[jj][u] = (have && lane + 32 * u < nvec) ? base[voff[u]] : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        float mb = m[u];
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const float w = j0 + jj < nvalid ? expf(lse_s[(j0 + jj) * hpg + h] - mx) * inv : 0.f;
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, l[j][u]);
-        const float rescale = m[u] > -INFINITY ? expf(m[u] - mb) : 0.f;
-        wsum[u] *= rescale;
+        for (int u = 0; u < NU; ++u) {
+          const uint32_t w4[4] = {raw[jj][u].x, raw[jj][u].y, raw[jj][u].z, raw[jj][u].w};
 #pragma unroll
-        for (int x = 0; x < 8; ++x) acc[u][x] *= rescale;
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-          const float wk = l[j][u] > -INFINITY ? expf(l[j][u] - mb) : 0.f;
-          wsum[u] += wk;
-          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[j][u]);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const float2 f = __bfloat1622float2(h2[x]);
-            acc[u][2 * x] = fmaf(wk, f.x, acc[u][2 * x]);
-            acc[u][2 * x + 1] = fmaf(wk, f.y, acc[u][2 * x + 1]);
+          for (int q2 = 0; q2 < 4; ++q2) {  // bf16 -> fp32 is a 16-bit shift (low half = even column)
+            acc[u][2 * q2] = fmaf(w, __uint_as_float(w4[q2] << 16), acc[u][2 * q2]);
+            acc[u][2 * q2 + 1] = fmaf(w, __uint_as_float(w4[q2] & 0xffff0000u), acc[u][2 * q2 + 1]);
           }
         }
-        m[u] = mb;
       }
     }
     __nv_bfloat16* dst = out + ((int64_t(b) * Nq + i) * Hq + g * hpg) * D;
@@ -827,16 +816,16 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
     for (int u = 0; u < NU; ++u) {
       const int vi = lane + 32 * u;
       if (vi >= nvec) continue;
-      const float inv = wsum[u] > 0.f ? 1.f / wsum[u] : 0.f;
       uint4 o;
-      o.x = pack_bf16(acc[u][0] * inv, acc[u][1] * inv);
-      o.y = pack_bf16(acc[u][2] * inv, acc[u][3] * inv);
-      o.z = pack_bf16(acc[u][4] * inv, acc[u][5] * inv);
-      o.w = pack_bf16(acc[u][6] * inv, acc[u][7] * inv);
-      *reinterpret_cast<uint4*>(dst + head[u] * D + (vi / hpg) * 8) = o;
-      if (lse_out && vi < hpg)
-        lse_out[(int64_t(b) * Nq + i) * Hq + g * hpg + head[u]] = wsum[u] > 0.f ? m[u] + logf(wsum[u]) : -INFINITY;
+      o.x = pack_bf16(acc[u][0], acc[u][1]);
+      o.y = pack_bf16(acc[u][2], acc[u][3]);
+      o.z = pack_bf16(acc[u][4], acc[u][5]);
+      o.w = pack_bf16(acc[u][6], acc[u][7]);
+      *reinterpret_cast<uint4*>(dst + h * D + (vi / hpg) * 8) = o;
     }
+    if (lse_out && lane < hpg)
+      lse_out[(int64_t(b) * Nq + i) * Hq + g * hpg + lane] = den > 0.f ? mx + logf(den) : -INFINITY;
+    __syncwarp();  // every lane is done with lse_s and slot_e[buf] before they are rewritten
     if (next < nitems) nvalid = meta_finish(next, buf ^ 1);
   }
 }
@@ -1180,7 +1169,7 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
 static size_t attn_smem_bytes(int d, int Bs) {
   const size_t kv = size_t(Bs) * d * 2 * 2;
   const size_t slot = size_t(kRows) * d * 2;
-  const size_t meta = size_t(kRing + 1) * kRows * 4 + size_t(2 * kKvoMaxPhases + 1) * 4 + 16;
+  const size_t meta = size_t(kRing) * kRows * 4 + size_t(2 * kKvoMaxPhases + 1) * 4 + 16;
   return 1024 + kv + kRing * slot + meta + (2 + 2 * kRing + 8 + 2) * 8 + 16;
 }
 
@@ -1347,13 +1336,17 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
 #define MSA_CMB(NU_)                                                                                           \
   do {                                                                                                         \
     auto kern = attn_combine_kernel<NU_>;                                                                      \
+    const size_t csm = combine_smem_bytes(K, hpg);                                                             \
+    if (csm > 48 * 1024 &&                                                                                     \
+        (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(csm))) != cudaSuccess)  \
+      return e;                                                                                                \
     int per_sm = 0;                                                                                            \
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)     \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, csm) != cudaSuccess || per_sm < 1)   \
       per_sm = 1;                                                                                              \
-    const int64_t need = (items + 7) / 8;                                                                      \
+    const int64_t need = (items + kCmbWarps - 1) / kCmbWarps;                                                  \
     const unsigned cgrid = unsigned(need < int64_t(per_sm) * grid ? need : int64_t(per_sm) * grid);            \
-    kern<<<cgrid, 256, 0, stream>>>(sel, q_offset, kv_len, part_o, part_lse, rev, b, Nq, Nk, Hq, G, K, Bs, nblk, d, \
-                                    c0, cq, o16, lse);                                                         \
+    kern<<<cgrid, 256, csm, stream>>>(sel, q_offset, kv_len, part_o, part_lse, rev, b, Nq, Nk, Hq, G, K, Bs, nblk, \
+                                      d, c0, cq, o16, lse);                                                    \
   } while (0)
         if (nvec <= 32)
           MSA_CMB(1);
