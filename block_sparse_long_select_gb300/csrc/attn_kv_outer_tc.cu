@@ -91,10 +91,13 @@ __global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t
     if (hist[t]) atomicAdd(&cnt[g * nblk + t], hist[t]);
 }
 
-// Relative cost of the attention kernel's work, fitted to per-CTA cycle
-// counts: a tile, the first tile of a bin (its K/V load and the pipeline
-// bubble around it), a tile holding rows whose local block this is (masked).
+// Relative cost of a tile pass's work: a tile, the first tile of a bin (its
+// K/V load and the pipeline bubble around it), a tile holding rows whose
+// local block this is (masked). The forward attention's weights were fitted
+// to per-CTA cycle counts; the KL and backward tile passes (whose epilogues
+// bind) were measured faster with a lighter bin weight and no masked weight.
 constexpr int kCostTile = 32, kCostBin = 17, kCostMasked = 8;
+constexpr int kCostTileT = 32, kCostBinT = 8, kCostMaskedT = 0;
 constexpr int kMaxGrid = kKvoMaxGrid;  // persistent grid: one CTA per SM
 
 // The tile where a cost prefix reaches X, searching bins [blo, bhi] (the last
@@ -118,7 +121,8 @@ __device__ int split_tile(const int* __restrict__ cost_off, const int* __restric
 // entries per tile: every tile owns a full slot range), tile total, and the
 // persistent grid's splits:
 //  - cta_start: CTA j takes tiles [cta_start[j], cta_start[j+1]), contiguous
-//    runs of equal estimated cost (the KL and backward passes);
+//    runs of equal estimated cost under the training passes' weights (the KL
+//    and backward passes);
 //  - cta_seg [nph][grid + 1]: phase p (the bins of groups
 //    [p G / nph, (p+1) G / nph)) split the same way on its own, so that CTA j
 //    takes a 1/grid share of every phase, phase after phase (the forward
@@ -127,62 +131,74 @@ __global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__
                                                          int b, int nblk, int nbins, int per_tile, int Bs, int c0,
                                                          int cq, int grid, int G, int nph, int* __restrict__ entry_off,
                                                          int* __restrict__ tile_off, int* __restrict__ cost_off,
-                                                         int* __restrict__ total_tiles, int* __restrict__ cta_start,
-                                                         int* __restrict__ cta_seg) {
-  __shared__ int s_e[1024], s_t[1024], s_c[1024];
+                                                         int* __restrict__ cost_off2, int* __restrict__ total_tiles,
+                                                         int* __restrict__ cta_start, int* __restrict__ cta_seg) {
+  __shared__ int s_e[1024], s_t[1024], s_c[1024], s_c2[1024];
   const int tid = threadIdx.x;
   const int per = (nbins + 1023) / 1024;
   const int lo = min(nbins, tid * per), hi = min(nbins, lo + per);
   const int q0 = q_offset ? q_offset[b] : 0;
-  auto bin_cost = [&](int x, int nt) {
-    // queries of the chunk whose local block is this bin's block
+  // queries of the chunk whose local block is this bin's block
+  auto nloc_of = [&](int x) {
     const int t = x % nblk;
     const int a0 = max(c0, t * Bs - q0), a1 = min(c0 + cq, (t + 1) * Bs - q0);
-    const int nloc = max(0, a1 - a0);
-    return nt > 0 ? kCostTile * nt + kCostBin + kCostMasked * min(nt, nloc) : 0;
+    return max(0, a1 - a0);
   };
-  int se = 0, st = 0, sc = 0;
+  auto bin_cost = [&](int x, int nt) {  // forward attention
+    return nt > 0 ? kCostTile * nt + kCostBin + kCostMasked * min(nt, nloc_of(x)) : 0;
+  };
+  auto bin_cost2 = [&](int x, int nt) {  // KL and backward tile passes
+    return nt > 0 ? kCostTileT * nt + kCostBinT + kCostMaskedT * min(nt, nloc_of(x)) : 0;
+  };
+  int se = 0, st = 0, sc = 0, sc2 = 0;
   for (int x = lo; x < hi; ++x) {
     const int nt = (cnt[x] + per_tile - 1) / per_tile;
     se += cnt[x];
     st += nt;
     sc += bin_cost(x, nt);
+    sc2 += bin_cost2(x, nt);
   }
   s_e[tid] = se;
   s_t[tid] = st;
   s_c[tid] = sc;
+  s_c2[tid] = sc2;
   __syncthreads();
   for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scans
     const int ve = tid >= off ? s_e[tid - off] : 0;
     const int vt = tid >= off ? s_t[tid - off] : 0;
     const int vc = tid >= off ? s_c[tid - off] : 0;
+    const int vc2 = tid >= off ? s_c2[tid - off] : 0;
     __syncthreads();
     s_e[tid] += ve;
     s_t[tid] += vt;
     s_c[tid] += vc;
+    s_c2[tid] += vc2;
     __syncthreads();
   }
-  int bt = s_t[tid] - st, bc = s_c[tid] - sc;
+  int bt = s_t[tid] - st, bc = s_c[tid] - sc, bc2 = s_c2[tid] - sc2;
   for (int x = lo; x < hi; ++x) {
     const int nt = (cnt[x] + per_tile - 1) / per_tile;
     entry_off[x] = bt * per_tile;  // a bin's entries start on a tile boundary
     tile_off[x] = bt;
     cost_off[x] = bc;
+    cost_off2[x] = bc2;
     bt += nt;
     bc += bin_cost(x, nt);
+    bc2 += bin_cost2(x, nt);
   }
   if (tid == 1023) {
     entry_off[nbins] = s_t[1023] * per_tile;
     tile_off[nbins] = s_t[1023];
     cost_off[nbins] = s_c[1023];
+    cost_off2[nbins] = s_c2[1023];
     *total_tiles = s_t[1023];
   }
   __syncthreads();
   // CTA j starts at the tile where the cost prefix reaches total * j / grid
-  const int64_t ctot = s_c[1023];
+  const int64_t ctot = s_c2[1023];
   const int ttot = s_t[1023];
   for (int j = tid; j <= grid; j += 1024)
-    cta_start[j] = j == grid ? ttot : split_tile(cost_off, tile_off, 0, nbins - 1, ctot * j / grid);
+    cta_start[j] = j == grid ? ttot : split_tile(cost_off2, tile_off, 0, nbins - 1, ctot * j / grid);
   for (int x = tid; x < nph * (grid + 1); x += 1024) {
     const int ph = x / (grid + 1), j = x % (grid + 1);
     const int blo = (ph * G / nph) * nblk, bhi = ((ph + 1) * G / nph) * nblk;  // bins [blo, bhi)
@@ -277,18 +293,6 @@ struct AttnParams {
   float scale;
 };
 
-// A CTA's tiles: run r (one phase) holds its local tiles [pref[r], pref[r+1]),
-// which are the chunk's tiles lo[r] + (z - pref[r]). Each warp role walks its
-// local tile numbers in increasing order, so the lookup keeps its run.
-struct TileRuns {
-  const int* lo;
-  const int* pref;
-  int r = 0;
-  __device__ __forceinline__ int at(int z) {
-    while (z >= pref[r + 1]) ++r;
-    return lo[r] + (z - pref[r]);
-  }
-};
 
 constexpr int kRing = 4;  // gathered-query tile ring depth (tile z in slot z % kRing)
 static_assert(kMmaWarpA == kTmaWarp0 + kTmaWarps && kMmaWarpA < 4, "warpgroup 0: gather warps, then the MMA warp");
@@ -355,16 +359,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(never_bar, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
-    // this CTA's share of every phase, phase after phase
-    int acc = 0;
-    run_pref[0] = 0;
-    for (int ph = 0; ph < p.nph; ++ph) {
-      const int* seg = p.cta_seg + ph * (p.grid + 1);
-      const int lo = seg[blockIdx.x], hi = seg[blockIdx.x + 1];
-      run_lo[ph] = lo;
-      acc += hi - lo;
-      run_pref[ph + 1] = acc;
-    }
+    load_tile_runs(p.cta_seg, p.nph, p.grid, run_lo, run_pref);  // this CTA's share of every phase
   }
   if (warp == kMmaWarpA) {
     tc::tmem_alloc(tmem_slot, 512);
@@ -1145,6 +1140,8 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   o += a256((nbins + 1) * 4);
   L.cost_off = o;
   o += a256((nbins + 1) * 4);
+  L.cost_off2 = o;
+  o += a256((nbins + 1) * 4);
   L.total = o;
   o += 256;
   L.cta_start = o;
@@ -1197,7 +1194,8 @@ cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int3
   attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, q_offset, b, nblk, nbins, per_tile, Bs, c0, cq, grid, G,
                                            kvo_phases(G), reinterpret_cast<int*>(w + L.entry_off),
                                            reinterpret_cast<int*>(w + L.tile_off),
-                                           reinterpret_cast<int*>(w + L.cost_off), reinterpret_cast<int*>(w + L.total),
+                                           reinterpret_cast<int*>(w + L.cost_off),
+                                           reinterpret_cast<int*>(w + L.cost_off2), reinterpret_cast<int*>(w + L.total),
                                            reinterpret_cast<int*>(w + L.cta_start),
                                            reinterpret_cast<int*>(w + L.cta_seg));
   attn_tiles_kernel<<<(nbins + 255) / 256, 256, 0, stream>>>(cnt, reinterpret_cast<int*>(w + L.entry_off),

@@ -95,10 +95,35 @@ constexpr int kKvoMaxGrid = 1024;   // cta_start capacity
 constexpr int kKvoMaxPhases = 16;   // forward attention: group ranges processed one after another
 inline int kvo_phases(int G) { return G < kKvoMaxPhases ? G : kKvoMaxPhases; }
 struct KvoLayout {
-  size_t cnt, cursor, entry_off, tile_off, cost_off, total, cta_start, cta_seg, entries, rev, tiles, part_o, part_lse,
-      end;
+  size_t cnt, cursor, entry_off, tile_off, cost_off, cost_off2, total, cta_start, cta_seg, entries, rev, tiles, part_o,
+      part_lse, end;
   size_t max_tiles;
 };
+// A CTA's tiles under the per-phase split (cta_seg [nph][grid + 1]): run r
+// holds its local tiles [pref[r], pref[r+1]), which are the chunk's tiles
+// lo[r] + (z - pref[r]). A warp role that walks its local tile numbers in
+// increasing order keeps its run between lookups.
+struct TileRuns {
+  const int* lo;
+  const int* pref;
+  int r = 0;
+  __device__ __forceinline__ int at(int z) {
+    while (z >= pref[r + 1]) ++r;
+    return lo[r] + (z - pref[r]);
+  }
+};
+// One thread fills lo[nph] and pref[nph + 1] (shared memory) for this CTA.
+__device__ __forceinline__ void load_tile_runs(const int* cta_seg, int nph, int grid, int* lo, int* pref) {
+  int acc = 0;
+  pref[0] = 0;
+  for (int ph = 0; ph < nph; ++ph) {
+    const int* seg = cta_seg + ph * (grid + 1);
+    const int a = seg[blockIdx.x], b = seg[blockIdx.x + 1];
+    lo[ph] = a;
+    acc += b - a;
+    pref[ph + 1] = acc;
+  }
+}
 // query tokens per chunk (equal chunks; the forward's bf16 partials stay under ~6 GiB)
 int chunk_tokens(int Nq, int Hq, int K, int d);
 KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk);
