@@ -47,9 +47,16 @@ namespace {
 constexpr int kRows = 128;  // query rows per tile (M of both MMAs)
 constexpr int kAttnThreads = 512;
 constexpr int kLaunchRegs = 128;  // registers per thread at launch (checked on the host)
-// warpgroup 0: producers (K/V, gathers, MMA); 1: partial stores; 2-3: softmax
-constexpr int kProdRegs = 80, kStoreRegs = 96, kSoftRegs = 168;
-static_assert(128 * (kProdRegs + kStoreRegs + 2 * kSoftRegs) <= kAttnThreads * kLaunchRegs, "register split");
+// warpgroup 0: producers (K/V, gathers, MMA); 1: partial stores; 2-3: softmax.
+// A 128-key softmax holds its whole S row (128 registers) and takes a larger
+// share from the partial stores.
+constexpr int kProdRegs = 80;
+template <int BS>
+struct AttnRegs {
+  static constexpr int kStore = BS == 128 ? 80 : 96;
+  static constexpr int kSoft = BS == 128 ? 176 : 168;
+  static_assert(128 * (kProdRegs + kStore + 2 * kSoft) <= kAttnThreads * kLaunchRegs, "register split");
+};
 constexpr int kTmaWarp0 = 0;  // warps 0..2: query-row gathers (four-row TMA gathers)
 constexpr int kTmaWarps = 3;
 constexpr int kMmaWarpA = 3;  // MMA issuer, TMEM owner and K/V loads
@@ -207,14 +214,15 @@ __global__ void __launch_bounds__(1024) attn_scan_kernel(const int* __restrict__
   }
 }
 
-// one thread per bin: its tiles (bin, first entry, count)
+// one thread per bin: its tiles (bin, first entry, count, tiles of the bin
+// from this one on)
 __global__ void attn_tiles_kernel(const int* __restrict__ cnt, const int* __restrict__ entry_off,
                                   const int* __restrict__ tile_off, int nbins, int per_tile, int4* __restrict__ tiles) {
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= nbins) return;
   const int c = cnt[x], e0 = entry_off[x], t0 = tile_off[x];
-  for (int j = 0; j * per_tile < c; ++j)
-    tiles[t0 + j] = make_int4(x, e0 + j * per_tile, min(per_tile, c - j * per_tile), 0);
+  const int nt = (c + per_tile - 1) / per_tile;
+  for (int j = 0; j < nt; ++j) tiles[t0 + j] = make_int4(x, e0 + j * per_tile, min(per_tile, c - j * per_tile), nt - j);
 }
 
 // grid (row chunks, G); dynamic smem = 2 * nblk ints. Entry = local query * 64 + slot;
@@ -267,14 +275,43 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// paired fp32 arithmetic (one instruction for two lanes of a 64-bit register pair)
+__device__ __forceinline__ uint64_t f32x2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_bits(uint32_t a, uint32_t b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ uint32_t pack_bf16x2(uint64_t r) {
+  float a, b;
+  unpack_f32x2(r, a, b);
+  return pack_bf16(a, b);
 }
 
 struct AttnParams {
@@ -295,6 +332,9 @@ struct AttnParams {
 
 
 constexpr int kRing = 4;  // gathered-query tile ring depth (tile z in slot z % kRing)
+// V buffers: two where shared memory has room for them (blocks of up to 64
+// keys), so a block's V is loaded ahead like its K; one at 128 keys
+constexpr int attn_v_buffers(int bs) { return bs <= 64 ? 2 : 1; }
 static_assert(kMmaWarpA == kTmaWarp0 + kTmaWarps && kMmaWarpA < 4, "warpgroup 0: gather warps, then the MMA warp");
 // Query rows reach the ring by four-row TMA gathers (512 bytes each, 64 per
 // tile). Issuing one takes a warp about 100 cycles, so the gather rate grows
@@ -311,26 +351,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr uint32_t kKVHalf = BS * 128;            // one 64-wide half of a K or V block
   constexpr uint32_t kKBytes = BS * D * 2;
   constexpr int NH = D / 64;
+  constexpr int NV = attn_v_buffers(BS);
   constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, BS, false);
   constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, D, true);  // B = V is MN-major
+  constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, 2);           // 128B swizzle, 8-row groups 1024 B apart
   // TMEM columns: warpgroup w owns S at [256 w, 256 w + BS) and O at [256 w + 128, 256 w + 128 + D)
   static_assert(BS <= 128 && D <= 128, "TMEM plan: S <= 128 and O <= 128 columns per warpgroup");
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = tc::smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* k_buf = smem;                    // [NH][BS][128 B]
-  uint8_t* v_buf = k_buf + kKBytes;         // [NH][BS][128 B]
-  uint8_t* ring = v_buf + kKBytes;          // kRing x kSlot: gathered Q tiles
-  int* meta = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kRing][128] tiles' entries (query*64+slot) or -1
-  int* run_lo = meta + kRing * kRows;                       // [kKvoMaxPhases]
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (tc::smem_u32(smem_raw) & 1023u) {  // the swizzled operands need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, MSA_ERR_CUDA);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  uint8_t* k_buf = smem;                    // [2][NH][BS][128 B]: the current key block's K and the next one's
+  uint8_t* v_buf = k_buf + 2 * kKBytes;     // [NV][NH][BS][128 B]
+  uint8_t* ring = v_buf + NV * kKBytes;     // kRing x kSlot: gathered Q tiles
+  float* inv_l = reinterpret_cast<float*>(ring + kRing * kSlot);  // [kRing][128] 1 / row sum of tile z in z % kRing
+  int* run_lo = reinterpret_cast<int*>(inv_l + kRing * kRows);    // [kKvoMaxPhases]
   int* run_pref = run_lo + kKvoMaxPhases;                   // [kKvoMaxPhases + 1]
   // mbarriers need 8-byte alignment: round the barrier area up to 16 bytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(run_pref + kKvoMaxPhases + 1) + 15) & ~uintptr_t(15));
-  uint64_t* kv_full = bars + 0;
-  uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;                // [kRing]
+  uint64_t* k_full = bars + 0;   // [2] a key block's K has landed in K buffer i
+  uint64_t* k_empty = bars + 2;  // [2] the last QK of a block has read K buffer i
+  uint64_t* v_full = bars + 4;   // [2] a key block's V has landed in V buffer i (i < NV)
+  uint64_t* v_empty = bars + 6;  // [2] the last PV of a block has read V buffer i
+  uint64_t* q_full = bars + 8;                // [kRing]
   uint64_t* q_empty = q_full + kRing;         // [kRing]
   uint64_t* s_full = q_empty + kRing;         // [2]
   uint64_t* p_full = s_full + 2;              // [2]
@@ -343,8 +390,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    tc::mbar_init(kv_full, 1);
-    tc::mbar_init(kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&k_full[i], 1);
+      tc::mbar_init(&k_empty[i], 1);
+      tc::mbar_init(&v_full[i], 1);
+      tc::mbar_init(&v_empty[i], 1);
+    }
     for (int r = 0; r < kRing; ++r) {
       tc::mbar_init(&q_full[r], 1);  // the tile's gather warp (arrival with the expected bytes)
       tc::mbar_init(&q_empty[r], 1);
@@ -389,27 +440,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp >= kTmaWarp0 && warp < kTmaWarp0 + kTmaWarps) {
     // ------------------------------ query-row gather ------------------------------
     // Gather warp gi takes tiles z = gi, gi + kTmaWarps, ... (ring slot z %
-    // kRing); each tile's entries are fetched one of its tiles ahead. Lane l
-    // gathers rows [4 l, 4 l + 4) with one four-row TMA gather per 64-column
-    // half into the 128B-swizzled K-major layout (the swizzle is
-    // address-based); the bytes are counted on the slot's barrier with the
-    // warp's arrival. Rows of padding entries read the chunk's first query
-    // (finite values; their outputs are never read).
+    // kRing). Lane l gathers rows [4 l, 4 l + 4) with one four-row TMA
+    // gather per 64-column half into the 128B-swizzled K-major layout (the
+    // swizzle is address-based); the bytes are counted on the slot's barrier
+    // with the warp's arrival. A lane loads its rows' entries itself, one of
+    // its tiles ahead (one load when the rows share an entry, as they do
+    // when the heads per group are a multiple of 4). Rows of padding entries
+    // read the chunk's first query (finite values; their outputs are never
+    // read).
     const int gi = warp - kTmaWarp0;
-    constexpr int kEntPerLane = kRows / 32;
     static_assert(kRows == 32 * 4, "one lane per four rows");
     const int per_tile = kRows / p.hpg;
+    const bool one_entry = p.hpg % 4 == 0;  // rows 4 l .. 4 l + 3 belong to one entry
     int4 tl = make_int4(0, 0, 0, 0);
-    int ev[kEntPerLane];
+    int ev[4];  // the entries of this lane's four rows (-1 past the tile's count)
     TileRuns runs{run_lo, run_pref};
     const uint64_t pol_q = tc::policy_evict_last();  // the phase's query rows are reused by every CTA
     auto fetch = [&](int z) {  // independent loads: tile zt's entries start at zt * per_tile
       const int zt = runs.at(z);
       tl = p.tiles[zt];
+      const int* ent = p.entries + int64_t(zt) * per_tile;
+      if (one_entry) {
+        const int e = lane * 4 / p.hpg;
+        ev[0] = ev[1] = ev[2] = ev[3] = e < per_tile ? ent[e] : -1;
+      } else {
 #pragma unroll
-      for (int x = 0; x < kEntPerLane; ++x) {
-        const int e = lane + 32 * x;
-        ev[x] = e < per_tile ? p.entries[int64_t(zt) * per_tile + e] : -1;
+        for (int j = 0; j < 4; ++j) {
+          const int e = (lane * 4 + j) / p.hpg;
+          ev[j] = e < per_tile ? ent[e] : -1;
+        }
       }
     };
     if (gi < n) fetch(gi);
@@ -420,18 +479,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         fail();
         break;
       }
-      int* my_meta = meta + rs * kRows;
-#pragma unroll
-      for (int x = 0; x < kEntPerLane; ++x)
-        if (lane + 32 * x < per_tile) my_meta[lane + 32 * x] = lane + 32 * x < tl.z ? ev[x] : -1;
-      __syncwarp();
       const int g = tl.x / p.nblk;
       int rows[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int row = lane * 4 + j;
-        const int ent = my_meta[row / p.hpg];
-        const int il = ent >= 0 ? (ent >> 6) : 0;
+        const int il = row / p.hpg < tl.z && ev[j] >= 0 ? (ev[j] >> 6) : 0;
         rows[j] = (p.b * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg;
       }
       if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[rs], uint32_t(kRows) * D * 2);
@@ -446,7 +499,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ++issued;
       last = z;
       if (z + kTmaWarps < n) fetch(z + kTmaWarps);
-      __syncwarp();  // every lane has read my_meta before the slot comes round again
     }
     // drain after an abort: no gather may still be landing in shared memory
     // when the CTA exits. (In a full run the MMA warp has waited for every
@@ -461,58 +513,113 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
   } else if (warp == kMmaWarpA) {
     // ------------------------------- MMA issuer -------------------------------
+    // One thread issues every MMA, so its instructions per tile set the pace
+    // when blocks are short: the common path per tile is one wait for the Q
+    // tile, QK^T, the previous tile's PV and a few compares; block changes
+    // take a separate path. Key blocks are numbered in the order this CTA
+    // meets them (bi = 0, 1, ...). Block bi's K goes to K buffer bi & 1 and
+    // is loaded during the previous block's second tile (its first tile is
+    // known from the tile records, read one tile ahead), into the buffer the
+    // block before that has finished with; after a one-tile block it is
+    // loaded at the change. With two V buffers V is loaded with K. With one,
+    // a block's V is loaded right after the block's first QK, once the
+    // previous block's last PV (issued just before) has read the buffer, so
+    // the copy overlaps the first tile's softmax.
     if (lane == 0) {
       const uint64_t pol_kv = tc::policy_evict_first();  // each block's K/V is read by one or two CTAs
-      int prev_bin = -1, loads = 0;
+      // descriptor low words of the first ring slot, K buffer and V buffer
+      const uint32_t ring_lo0 = tc::smem_desc_lo(tc::smem_u32(ring), 16);
+      const uint32_t k_lo0 = tc::smem_desc_lo(tc::smem_u32(k_buf), 16);
+      const uint32_t v_lo0 = tc::smem_desc_lo(tc::smem_u32(v_buf), kKVHalf);
+      int kl = 0, vl = 0;  // K / V loads issued: block bi's K is K load bi, its V is V load bi
+      int vw = 0;          // blocks whose V has been waited for (once, before the block's first PV)
       bool alive = true;
-      auto issue_pv = [&](int z, bool last_of_bin) -> bool {
-        const int s = z & 1;
+      auto load_k = [&](int bin, int bi) -> bool {
+        const int kb = bi & 1;
+        // the buffer's previous block (bi - 2) must be done with it
+        if (bi >= 2 && !tc::mbar_wait(&k_empty[kb], ((bi >> 1) - 1) & 1, abort_flag)) return false;
+        const int g = bin / p.nblk, t = bin % p.nblk;
+        tc::mbar_arrive_expect_tx(&k_full[kb], kKBytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          tc::tma_load_4d_hint(k_buf + kb * kKBytes + h * kKVHalf, &tmK, &k_full[kb], h * 64, g, t * BS, p.b,
+                               pol_kv);
+        kl = bi + 1;
+        return true;
+      };
+      auto load_v = [&](int bin, int bi) -> bool {
+        const int vb = bi % NV;
+        // the buffer's previous block (bi - NV) must be done with it
+        if (bi >= NV && !tc::mbar_wait(&v_empty[vb], ((bi / NV) - 1) & 1, abort_flag)) return false;
+        const int g = bin / p.nblk, t = bin % p.nblk;
+        tc::mbar_arrive_expect_tx(&v_full[vb], kKBytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          tc::tma_load_4d_hint(v_buf + vb * kKBytes + h * kKVHalf, &tmV, &v_full[vb], h * 64, g, t * BS, p.b,
+                               pol_kv);
+        vl = bi + 1;
+        return true;
+      };
+      // PV of tile z (block bi), the block's last if last_of_bin
+      auto issue_pv = [&](int z, int bi, bool last_of_bin) -> bool {
+        const int s = z & 1, vb = bi % NV;
+        if (vw <= bi) {  // the block's first PV: its V must have landed
+          if (!tc::mbar_wait(&v_full[vb], (bi / NV) & 1, abort_flag)) return false;
+          vw = bi + 1;
+        }
         if (!tc::mbar_wait(&p_full[s], (z >> 1) & 1, abort_flag) ||
             !tc::mbar_wait(&o_empty[s], ((z >> 1) & 1) ^ 1, abort_flag))
           return false;
         tc::fence_after_sync();
-        const uint32_t va = tc::smem_u32(v_buf);
+        const uint32_t v_lo = v_lo0 + uint32_t(vb) * (kKBytes >> 4);
+        const uint32_t t_s = tmem + uint32_t(s) * 256u;
 #pragma unroll
         for (int kk = 0; kk < BS / 16; ++kk) {
           // P (bf16 pairs packed per 32-bit column) sits where S was: 16 keys = 8 columns
-          const uint32_t a_tmem = tmem + uint32_t(s) * 256u + uint32_t(kk) * 8u;
-          const uint64_t bd = tc::smem_desc(va + kk * 16 * 128, kKVHalf, 1024, 2);
-          tc::mma_f16_ts(tmem + uint32_t(s) * 256u + 128u, a_tmem, bd, kIdescPV, kk > 0 ? 1u : 0u);
+          tc::mma_f16_ts_lo<kDescHi>(t_s + 128u, t_s + uint32_t(kk) * 8u, v_lo + uint32_t(kk * 16 * 128 >> 4), kIdescPV,
+                                     kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&o_full[s]);
-        if (last_of_bin) tc::mma_commit(kv_empty);
+        if (last_of_bin) tc::mma_commit(&v_empty[vb]);
         return true;
       };
       if (p.inject_timeout && !tc::mbar_wait_for(never_bar, 0, abort_flag, tc::kInjectedWaitCycles)) {
         fail();
         alive = false;
       }
-      TileRuns runs{run_lo, run_pref};
-      int bin_next = n > 0 ? p.tiles[runs.at(0)].x : -1;
+      // the lookahead cursor: local tile z1 = z + 1 is chunk tile zg1 of run r1 (which ends at local end1)
+      int r1 = 0;
+      while (r1 < p.nph && run_pref[r1 + 1] == 0) ++r1;
+      int zg1 = n > 0 ? run_lo[r1] : 0, end1 = n > 0 ? run_pref[r1 + 1] : 0;
+      int4 rec_next = n > 0 ? p.tiles[zg1] : make_int4(-1, 0, 0, 0);
+      TileRuns peek{run_lo, run_pref};
+      int prev_bin = -1, bi = -1;
+      int pend_z = -1, pend_bin = -1;  // at local tile pend_z: load block bi + 1 (from pend_bin)
+      if (alive && n > 0 && !(load_k(rec_next.x, 0) && load_v(rec_next.x, 0))) {  // the first block
+        fail();
+        alive = false;
+      }
       for (int z = 0; z < n && alive; ++z) {
-        const int s = z & 1, rs = z % kRing;
-        const int bin = bin_next;
-        if (z + 1 < n) bin_next = p.tiles[runs.at(z + 1)].x;
-        if (bin != prev_bin) {
-          // a new key block: the previous block's last PV, then this block's
-          // K and V over the same buffers once that PV has read V
-          if (z > 0 && !issue_pv(z - 1, true)) {
-            fail();
-            break;
+        const int s = z & 1, rs = z & (kRing - 1);
+        const int4 rec = rec_next;
+        const int zg = zg1, end_z = end1;
+        if (z + 1 < n) {
+          if (z + 1 == end1) {  // the next tile opens the next non-empty run
+            do ++r1;
+            while (run_pref[r1 + 1] == z + 1);
+            zg1 = run_lo[r1];
+            end1 = run_pref[r1 + 1];
+          } else {
+            ++zg1;
           }
-          if (loads > 0 && !tc::mbar_wait(kv_empty, (loads - 1) & 1, abort_flag)) {
-            fail();
-            break;
-          }
-          const int g = bin / p.nblk, t = bin % p.nblk;
-          tc::mbar_arrive_expect_tx(kv_full, 2 * kKBytes);
-#pragma unroll
-          for (int h = 0; h < NH; ++h) {
-            tc::tma_load_4d_hint(k_buf + h * kKVHalf, &tmK, kv_full, h * 64, g, t * BS, p.b, pol_kv);
-            tc::tma_load_4d_hint(v_buf + h * kKVHalf, &tmV, kv_full, h * 64, g, t * BS, p.b, pol_kv);
-          }
-          ++loads;
-          if (!tc::mbar_wait(kv_full, (loads - 1) & 1, abort_flag)) {
+          rec_next = p.tiles[zg1];
+        }
+        const bool first_of_bin = rec.x != prev_bin;
+        if (first_of_bin) {
+          ++bi;
+          // not loaded ahead (the previous block had one tile here): load now
+          if ((kl <= bi && !load_k(rec.x, bi)) || (NV == 2 && vl <= bi && !load_v(rec.x, bi)) ||
+              !tc::mbar_wait(&k_full[bi & 1], (bi >> 1) & 1, abort_flag)) {
             fail();
             break;
           }
@@ -522,43 +629,72 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint32_t qa = tc::smem_u32(ring + rs * kSlot);
-        const uint32_t ka = tc::smem_u32(k_buf);
+        const uint32_t q_lo = ring_lo0 + uint32_t(rs) * (kSlot >> 4);
+        const uint32_t k_lo = k_lo0 + uint32_t(bi & 1) * (kKBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          const uint64_t ad = tc::smem_desc(qa + (kk >> 2) * (kRows * 128) + off, 16, 1024, 2);
-          const uint64_t bd = tc::smem_desc(ka + (kk >> 2) * kKVHalf + off, 16, 1024, 2);
-          tc::mma_f16_ss(tmem + uint32_t(s) * 256u, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes along the swizzled 128-byte rows
+          tc::mma_f16_ss_lo<kDescHi>(tmem + uint32_t(s) * 256u, q_lo + (((kk >> 2) * (kRows * 128) + off) >> 4),
+                                     k_lo + (((kk >> 2) * kKVHalf + off) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&s_full[s]);
         tc::mma_commit(&q_empty[rs]);  // the gathered Q tile is consumed
-        if (bin == prev_bin && z > 0) {
-          if (!issue_pv(z - 1, false)) {
+        // the previous tile's PV (the previous block's last at a block change)
+        if (z > 0 && !issue_pv(z - 1, first_of_bin ? bi - 1 : bi, first_of_bin)) {
+          fail();
+          alive = false;
+          break;
+        }
+        if (first_of_bin) {
+          // the previous block's K buffer is free once everything issued so
+          // far (its last QK among them) has completed
+          if (z > 0) tc::mma_commit(&k_empty[(bi - 1) & 1]);
+          // the next block: its first tile follows this block's rec.w tiles
+          // in this run, or opens the next run; its K (and V) are loaded
+          // during this block's second tile
+          const int zn = z + rec.w < end_z ? z + rec.w : end_z;
+          if (zn < n && zn > z + 1) {
+            pend_z = z + 1;
+            pend_bin = p.tiles[zn < end_z ? zg + (zn - z) : peek.at(zn)].x;
+          }
+          // one V buffer: this block's V now. The wait is for the previous
+          // block's last PV, issued just above, and ends well before this
+          // tile's P is ready
+          if (NV == 1 && bi >= 1 && vl == bi && !load_v(rec.x, bi)) {
+            fail();
+            alive = false;
+            break;
+          }
+        } else if (z == pend_z) {
+          if ((kl <= bi + 1 && !load_k(pend_bin, bi + 1)) || (NV == 2 && vl <= bi + 1 && !load_v(pend_bin, bi + 1))) {
             fail();
             alive = false;
             break;
           }
         }
-        prev_bin = bin;
+        prev_bin = rec.x;
       }
       if (alive && n > 0 && !*abort_flag) {
-        if (!issue_pv(n - 1, true)) fail();
+        if (!issue_pv(n - 1, bi, true)) fail();
       }
-      int zero = 0;
-      if (loads > 0) tc::mbar_wait(kv_full, (loads - 1) & 1, &zero);  // no K/V copy still landing
+      int zero = 0;  // no K or V copy may still be landing: the last load into each buffer
+      for (int b2 = kl - 1; b2 >= 0 && b2 >= kl - 2; --b2) tc::mbar_wait(&k_full[b2 & 1], (b2 >> 1) & 1, &zero);
+      for (int b2 = vl - 1; b2 >= 0 && b2 >= vl - NV; --b2) tc::mbar_wait(&v_full[b2 % NV], (b2 / NV) & 1, &zero);
       tc::mma_commit(done_bar);
       tc::mbar_wait(done_bar, 0, &zero);
     }
   }  // other warps of warpgroup 0: none
   } else if (warp < kEpiWarp0) {
-    tc::regs_dec<kStoreRegs>();
+    tc::regs_dec<AttnRegs<BS>::kStore>();
     // --------------------------- partial stores ---------------------------
     // Warpgroup 1 reads every tile's O (TMEM lanes of its warp's quarter)
     // and stores it as the tile's bf16 partial rows: 16-byte chunk c of row
     // r of tile zg at part_o[(zg * D/8 + c) * 128 + r], so each warp store
     // instruction writes 32 consecutive rows' chunk (512 contiguous bytes).
-    // P was normalised by the row sum before PV, so O is the partial itself.
+    // P is unnormalised: O is scaled by the row's 1 / sum that the softmax
+    // left in shared memory (slot z % kRing; the softmax overwrites it only
+    // for tile z + kRing, whose QK^T waits for PV(z + 2), which waits for
+    // this warpgroup's o_empty arrival below, made after the read).
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
@@ -572,6 +708,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       tc::fence_after_sync();
+      const float inv = inv_l[(z % kRing) * kRows + r];
+      const uint64_t inv2 = f32x2(inv, inv);
       const uint32_t o_addr = tmem + lane_base + uint32_t(s) * 256u + 128u;
       uint4* dst = p.part_o + int64_t(zg) * (D / 8) * kRows + r;
 #pragma unroll
@@ -587,22 +725,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint4 o;
-          o.x = pack_bf16(__uint_as_float(ov[c * 8 + 0]), __uint_as_float(ov[c * 8 + 1]));
-          o.y = pack_bf16(__uint_as_float(ov[c * 8 + 2]), __uint_as_float(ov[c * 8 + 3]));
-          o.z = pack_bf16(__uint_as_float(ov[c * 8 + 4]), __uint_as_float(ov[c * 8 + 5]));
-          o.w = pack_bf16(__uint_as_float(ov[c * 8 + 6]), __uint_as_float(ov[c * 8 + 7]));
+          o.x = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 0], ov[c * 8 + 1]), inv2));
+          o.y = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 2], ov[c * 8 + 3]), inv2));
+          o.z = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 4], ov[c * 8 + 5]), inv2));
+          o.w = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 6], ov[c * 8 + 7]), inv2));
           tc::st_v4_hint(dst + (c0 / 8 + c) * kRows, o, pol_part);
         }
       }
     }
   } else {
-    tc::regs_inc<kSoftRegs>();
+    tc::regs_inc<AttnRegs<BS>::kSoft>();
     // -------------------------------- softmax --------------------------------
     // Warpgroups 2 and 3 take alternate tiles (TMEM set s = z & 1): the whole
     // S row of a thread's TMEM lane in registers, causal mask in the local
-    // block, exact softmax with the row sum folded into P (bf16 pairs written
-    // back over S for the PV MMA), and the row's log-sum-exp stored for the
-    // combine.
+    // block, exact softmax with unnormalised probabilities as P (bf16 pairs
+    // written back over S for the PV MMA; the partial-store warps divide O by
+    // the row sum), and the row's log-sum-exp stored for the combine. The
+    // exponent arguments and the row sum use paired fp32 instructions.
     const int w = (warp - kEpiWarp0) >> 2;         // warpgroup: tiles z with z % 2 == w
     const int quarter = warp & 3;                  // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;             // tile row
@@ -648,30 +787,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j < BS; j += 2)
         m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
       const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      // probabilities (in place) and their sum in fp32
+      // probabilities, 32 keys at a time: packed to bf16 pairs and written
+      // back over S in TMEM at once (the PV MMA reads its A operand from
+      // there: keys 2c (low half) and 2c+1 (high half) in column c), their
+      // sum in fp32, two keys per instruction
       const float mneg = -mx * p.scale_log2;
-      float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < BS; ++j) {
-        const float pj = ex2(fmaf(__uint_as_float(v[j]), p.scale_log2, mneg));
-        l4[j & 3] += pj;
-        v[j] = __float_as_uint(pj);
-      }
-      const float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      // P / l as bf16 pairs written back over S in TMEM (the PV MMA reads its
-      // A operand from there): keys 2c (low half) and 2c+1 (high half) in column c
+      uint64_t l2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
       for (int c0 = 0; c0 < BS / 32; ++c0) {
-        uint32_t pk[16];
+        uint32_t* pk = v + c0 * 32;  // the packed pairs reuse the chunk's first 16 registers
 #pragma unroll
-        for (int j = 0; j < 32; j += 2)
-          pk[j >> 1] = pack_bf16(__uint_as_float(v[c0 * 32 + j]) * inv, __uint_as_float(v[c0 * 32 + j + 1]) * inv);
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j]), p.scale_log2, mneg));
+          const float p1 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j + 1]), p.scale_log2, mneg));
+          l2[(j >> 1) & 1] = add_f32x2(l2[(j >> 1) & 1], f32x2(p0, p1));
+          pk[j >> 1] = pack_bf16(p0, p1);
+        }
         tc::tmem_st_32x32b_x16(s_addr + c0 * 16, pk);
       }
+      float la, lb, lc, ld;
+      unpack_f32x2(l2[0], la, lb);
+      unpack_f32x2(l2[1], lc, ld);
+      const float l = (la + lb) + (lc + ld);
+      inv_l[(z % kRing) * kRows + r] = l > 0.f ? 1.f / l : 0.f;
       tc::tmem_st_wait();
       tc::fence_before_sync();
-      __syncwarp();
+      __syncwarp();  // (also orders every lane's 1 / sum before the arrival)
       if (lane == 0) tc::mbar_arrive(&p_full[s]);
       tc::st_f32_hint(p.part_lse + int64_t(zg) * kRows + r, valid ? mx * p.scale + logf(l) : 0.f, pol_part);
     }
@@ -1164,10 +1305,10 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
 }
 
 static size_t attn_smem_bytes(int d, int Bs) {
-  const size_t kv = size_t(Bs) * d * 2 * 2;
+  const size_t kv = size_t(Bs) * d * 2 * (2 + attn_v_buffers(Bs));  // two K buffers, one or two V buffers
   const size_t slot = size_t(kRows) * d * 2;
   const size_t meta = size_t(kRing) * kRows * 4 + size_t(2 * kKvoMaxPhases + 1) * 4 + 16;
-  return 1024 + kv + kRing * slot + meta + (2 + 2 * kRing + 8 + 2) * 8 + 16;
+  return kv + kRing * slot + meta + (8 + 2 * kRing + 8 + 2) * 8 + 16;  // the base is 1024-byte aligned
 }
 
 // selection -> per-(group, block) entry lists, tiles and the persistent

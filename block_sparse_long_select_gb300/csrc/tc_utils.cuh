@@ -252,6 +252,44 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// The same descriptor as two 32-bit words. The high word (stride offset,
+// version bit, swizzle mode) is fixed by the layout; the low word holds the
+// start address and the leading offset, so the descriptor of an address a
+// few KB further on is a base low word plus (byte offset >> 4), one integer
+// add. Issuing threads that keep only low words run far fewer instructions
+// per MMA.
+__host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo, uint32_t swizzle) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | ((swizzle & 0x7u) << 29);
+}
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+// D[tmem] (+)= A[smem] * B[smem]^T with both descriptors given by low words
+template <uint32_t HI>
+__device__ __forceinline__ void mma_f16_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %5};\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(HI)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T with B's descriptor given by its low word
+template <uint32_t HI>
+__device__ __forceinline__ void mma_f16_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(HI)
+      : "memory");
+}
+
 // 32 TMEM lanes x 32 consecutive 32-bit columns -> 32 registers per thread
 // (thread = lane of its warp's 32-lane quarter).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
