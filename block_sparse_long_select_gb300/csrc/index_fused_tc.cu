@@ -352,19 +352,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block maxima of the whole tile first (the accumulator is released
         // as soon as its last columns are in registers), offers afterwards
         float bm[kTileN / BS];
+        if constexpr (!REG || BS == 128) {
+          // each 32-column load returns the maximum of its columns as well
+          // (two loads in flight where the heap takes registers)
+          constexpr int kWave = REG ? kChunk / 32 : 2;
 #pragma unroll
-        for (int c = 0; c < kTileN / kChunk; ++c) {
-          uint32_t v[kChunk];
+          for (int c = 0; c < kTileN / kChunk; ++c) {
+            float m32[kChunk / 32];
 #pragma unroll
-          for (int q = 0; q < kChunk / 32; ++q) tc::tmem_ld_32x32b_x32(taddr + c * kChunk + q * 32, v + q * 32);
-          tc::tmem_ld_wait();
-          if (c == kTileN / kChunk - 1) {  // the whole accumulator is in registers: release it
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&acc_empty[m]);
+            for (int q0 = 0; q0 < kChunk / 32; q0 += kWave) {
+#pragma unroll
+              for (int q = q0; q < q0 + kWave; ++q) {
+                uint32_t v[32];  // the values themselves are not needed
+                m32[q] = tc::tmem_ld_max_32x32b_x32(taddr + c * kChunk + q * 32, v);
+              }
+              tc::tmem_ld_wait();
+            }
+            if (c == kTileN / kChunk - 1) {  // the whole accumulator has been read: release it
+              tc::fence_before_sync();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&acc_empty[m]);
+            }
+#pragma unroll
+            for (int bi = 0; bi < kChunk / BS; ++bi) {
+              float mx = m32[bi * (BS / 32)];
+#pragma unroll
+              for (int q = 1; q < BS / 32; ++q) mx = fmaxf(mx, m32[bi * (BS / 32) + q]);
+              bm[c * (kChunk / BS) + bi] = mx;
+            }
           }
+        } else {
+          // many block maxima per tile next to the register list: loaded
+          // values reduced by 3-input max chains keep the registers in bounds
 #pragma unroll
-          for (int bi = 0; bi < kChunk / BS; ++bi) bm[c * (kChunk / BS) + bi] = block_max<BS>(v + bi * BS);
+          for (int c = 0; c < kTileN / kChunk; ++c) {
+            uint32_t v[kChunk];
+#pragma unroll
+            for (int q = 0; q < kChunk / 32; ++q) tc::tmem_ld_32x32b_x32(taddr + c * kChunk + q * 32, v + q * 32);
+            tc::tmem_ld_wait();
+            if (c == kTileN / kChunk - 1) {  // the whole accumulator is in registers: release it
+              tc::fence_before_sync();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&acc_empty[m]);
+            }
+#pragma unroll
+            for (int bi = 0; bi < kChunk / BS; ++bi) bm[c * (kChunk / BS) + bi] = block_max<BS>(v + bi * BS);
+          }
         }
         if constexpr (REG) {
 #pragma unroll
