@@ -771,22 +771,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int nvalid = valid ? min(BS, pos - t * BS + 1) : BS;  // keys j <= pos inside the block
       const uint32_t s_addr = tmem + lane_base + uint32_t(s) * 256u;
       const bool full = nvalid >= BS;  // all keys visible (every block but the local one)
-      // the whole S row in registers: one TMEM round trip
+      // the whole S row in registers: one TMEM round trip; each 32-column
+      // load also returns the maximum of its columns
       uint32_t v[BS];
+      float m32[BS / 32];
 #pragma unroll
-      for (int c = 0; c < BS / 32; ++c) tc::tmem_ld_32x32b_x32(s_addr + c * 32, v + c * 32);
+      for (int c = 0; c < BS / 32; ++c) m32[c] = tc::tmem_ld_max_32x32b_x32(s_addr + c * 32, v + c * 32);
       tc::tmem_ld_wait();
-      if (!full) {
+      float mx = m32[0];
+#pragma unroll
+      for (int c = 1; c < BS / 32; ++c) mx = fmaxf(mx, m32[c]);
+      if (!full) {  // the local block: the row maximum over its visible keys only
 #pragma unroll
         for (int j = 0; j < BS; ++j)
           if (j >= nvalid) v[j] = __float_as_uint(-INFINITY);  // exp2(-inf) = 0 below
-      }
-      // row maximum (four independent chains)
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int j = 0; j < BS; j += 2)
-        m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        for (int j = 0; j < BS; j += 2)
+          m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
       // probabilities, 32 keys at a time: packed to bf16 pairs and written
       // back over S in TMEM at once (the PV MMA reads its A operand from
       // there: keys 2c (low half) and 2c+1 (high half) in column c), their
