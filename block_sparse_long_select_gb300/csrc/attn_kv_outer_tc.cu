@@ -47,10 +47,22 @@ namespace {
 constexpr int kRows = 128;  // query rows per tile (M of both MMAs)
 constexpr int kAttnThreads = 512;
 constexpr int kLaunchRegs = 128;  // registers per thread at launch (checked on the host)
-// warpgroup 0: producers (K/V, gathers, MMA); 1: partial stores; 2-3: softmax.
-// A 128-key softmax holds its whole S row (128 registers) and takes a larger
-// share from the partial stores.
-constexpr int kProdRegs = 80;
+// Two designs share this file. The two-issuer design (blocks of 64 and 32
+// keys). Warpgroups 0 and 1 (80 registers): warps 0, 1, 2 and 6 gather
+// query rows (one ring slot each), warp 3 loads K and V and owns TMEM, warps
+// 4 and 5 issue the MMAs of softmax warpgroup 0 and 1, warp 7 is idle.
+// Warpgroups 2 and 3 (176 registers: a 128-key row of S in registers): the
+// softmax of alternate tiles and the store of their O.
+constexpr int kProdRegs = 80, kSoftRegs = 176;
+static_assert(128 * (2 * kProdRegs + 2 * kSoftRegs) <= kAttnThreads * kLaunchRegs, "register split");
+constexpr int kLoadWarp = 3;   // K/V loads, TMEM allocation
+constexpr int kIssueWarp0 = 4;  // warps 4, 5: MMA issuers of softmax warpgroups 0, 1
+constexpr int kGatherWarpHi = 6;  // the fourth gather warp (with warps 0, 1, 2)
+constexpr int kEpiWarp0 = 8;    // warps 8..15 (warpgroups 2 and 3)
+// The single-issuer design (blocks of 128 keys): warpgroup 0 (80 registers):
+// warps 0-2 gather query rows, warp 3 issues the MMAs, loads K and V and owns
+// TMEM; warpgroup 1 (80) stores the partials; warpgroups 2 and 3 (176) run
+// the softmax of alternate tiles.
 template <int BS>
 struct AttnRegs {
   static constexpr int kStore = BS == 128 ? 80 : 96;
@@ -61,7 +73,6 @@ constexpr int kTmaWarp0 = 0;  // warps 0..2: query-row gathers (four-row TMA gat
 constexpr int kTmaWarps = 3;
 constexpr int kMmaWarpA = 3;  // MMA issuer, TMEM owner and K/V loads
 constexpr int kStoreWarp0 = 4;  // warps 4..7 (warpgroup 1)
-constexpr int kEpiWarp0 = 8;    // warps 8..15 (warpgroups 2 and 3)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -289,11 +300,6 @@ __device__ __forceinline__ uint64_t f32x2_bits(uint32_t a, uint32_t b) {
 __device__ __forceinline__ void unpack_f32x2(uint64_t r, float& a, float& b) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
 }
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -325,7 +331,7 @@ struct AttnParams {
   float* part_lse;        // [entries, hpg]: row (entry * hpg + head in group)
   uint32_t* status;
   int b, Nq, Nk, Hq, G, Bs, K, nblk, c0, hpg, nph, grid;
-  int inject_timeout;  // test hook: the MMA warp first waits on a barrier nothing completes
+  int inject_timeout;  // test hook: the kernel first waits on a barrier nothing completes
   float scale_log2;  // softmax scale * log2(e)
   float scale;
 };
@@ -335,13 +341,16 @@ constexpr int kRing = 4;  // gathered-query tile ring depth (tile z in slot z % 
 // V buffers: two where shared memory has room for them (blocks of up to 64
 // keys), so a block's V is loaded ahead like its K; one at 128 keys
 constexpr int attn_v_buffers(int bs) { return bs <= 64 ? 2 : 1; }
-static_assert(kMmaWarpA == kTmaWarp0 + kTmaWarps && kMmaWarpA < 4, "warpgroup 0: gather warps, then the MMA warp");
 // Query rows reach the ring by four-row TMA gathers (512 bytes each, 64 per
-// tile). Issuing one takes a warp about 100 cycles, so the gather rate grows
-// with the number of warps that issue them; measured alternatives were
-// slower: a cp.async warp issues about a third of that rate.
+// tile). Issuing one holds a warp about 70-90 cycles, so the gather rate grows
+// with the number of warps that issue them: four warps, one ring slot each.
+// Measured alternatives were slower: a cp.async warp issues about a third of
+// a TMA warp's rate.
 
 
+// The single-issuer design, used for blocks of 128 keys: one MMA thread,
+// three gather warps and a partial-store warpgroup (the 128-key softmax is
+// long enough to hide them); see the constants above.
 template <int D, int BS>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -829,6 +838,474 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
+// The two-issuer design, used for blocks of 64 and 32 keys (two to four
+// times the tiles per unit of work, each with a short softmax).
+template <int D, int BS>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kv_outer2_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmQ, const AttnParams p) {
+  constexpr uint32_t kQBytes = kRows * D * 2;       // one gathered query tile (= one bf16 O tile)
+  constexpr uint32_t kSlot = kQBytes;
+  constexpr uint32_t kKVHalf = BS * 128;            // one 64-wide half of a K or V block
+  constexpr uint32_t kKBytes = BS * D * 2;
+  constexpr int NH = D / 64;
+  constexpr int NV = attn_v_buffers(BS);
+  constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, BS, false);
+  constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, D, true);  // B = V is MN-major
+  constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, 2);           // 128B swizzle, 8-row groups 1024 B apart
+  // TMEM columns: softmax warpgroup w owns S at [256 w, 256 w + BS) and O at [256 w + 128, 256 w + 128 + D)
+  static_assert(BS <= 128 && D <= 128, "TMEM plan: S <= 128 and O <= 128 columns per warpgroup");
+  static_assert(kRing == 4, "four gather warps, one ring slot each");
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (tc::smem_u32(smem_raw) & 1023u) {  // the swizzled operands need 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, MSA_ERR_CUDA);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  uint8_t* k_buf = smem;                    // [2][NH][BS][128 B]: the current key block's K and the next one's
+  uint8_t* v_buf = k_buf + 2 * kKBytes;     // [NV][NH][BS][128 B]
+  uint8_t* ring = v_buf + NV * kKBytes;     // kRing x kSlot: gathered Q tiles
+  int* run_lo = reinterpret_cast<int*>(ring + kRing * kSlot);  // [kKvoMaxPhases]
+  int* run_pref = run_lo + kKvoMaxPhases;                      // [kKvoMaxPhases + 1]
+  // mbarriers need 8-byte alignment: round the barrier area up to 16 bytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(run_pref + kKvoMaxPhases + 1) + 15) & ~uintptr_t(15));
+  uint64_t* k_full = bars + 0;   // [2] a key block's K has landed in K buffer i
+  uint64_t* k_empty = bars + 2;  // [2] both issuers are done with K buffer i (2 arrivals)
+  uint64_t* v_full = bars + 4;   // [2] a key block's V has landed in V buffer i (i < NV)
+  uint64_t* v_empty = bars + 6;  // [2] both issuers are done with V buffer i (2 arrivals)
+  uint64_t* q_full = bars + 8;                // [kRing]
+  uint64_t* q_empty = q_full + kRing;         // [kRing]
+  uint64_t* s_full = q_empty + kRing;         // [2] per softmax warpgroup
+  uint64_t* p_full = s_full + 2;              // [2]
+  uint64_t* o_full = p_full + 2;              // [2]
+  uint64_t* done_bar = o_full + 2;            // [2] per issuer
+  uint64_t* never_bar = done_bar + 2;  // no thread arrives on it (timeout injection)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&k_full[i], 1);
+      tc::mbar_init(&k_empty[i], 2);
+      tc::mbar_init(&v_full[i], 1);
+      tc::mbar_init(&v_empty[i], 2);
+    }
+    for (int r = 0; r < kRing; ++r) {
+      tc::mbar_init(&q_full[r], 1);  // the slot's gather warp (arrival with the expected bytes)
+      tc::mbar_init(&q_empty[r], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&s_full[s], 1);
+      tc::mbar_init(&p_full[s], 4);
+      tc::mbar_init(&o_full[s], 1);
+      tc::mbar_init(&done_bar[s], 1);
+    }
+    tc::mbar_init(never_bar, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+    load_tile_runs(p.cta_seg, p.nph, p.grid, run_lo, run_pref);  // this CTA's share of every phase
+  }
+  if (warp == kLoadWarp) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tc::tma_prefetch(&tmK);
+    tc::tma_prefetch(&tmV);
+    tc::tma_prefetch(&tmQ);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  // this CTA's tiles: local numbers z in [0, n), mapped to the chunk's tiles by TileRuns
+  const int n = run_pref[p.nph];
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, MSA_ERR_TIMEOUT);
+  };
+
+  // Each register re-allocation sits at the top of its warpgroups' branch
+  // (one instruction for all warps of a warpgroup) so that the compiler
+  // budgets each branch with its own register count.
+  if (warp < kEpiWarp0) {
+  tc::regs_dec<kProdRegs>();
+  if (warp < kLoadWarp || warp == kGatherWarpHi) {
+    // ------------------------------ query-row gather ------------------------------
+    // Gather warp gw (warps 0, 1, 2, 6) takes tiles z = gw, gw + 4, ... into
+    // ring slot gw, so a warp has at most one tile in flight. Lane l gathers
+    // rows [4 l, 4 l + 4) with one four-row TMA gather per 64-column half
+    // into the 128B-swizzled K-major layout (the swizzle is address-based);
+    // the bytes are counted on the slot's barrier with the warp's arrival. A
+    // lane loads its rows' entries itself, one of its tiles ahead (one load
+    // when the rows share an entry, as they do when the heads per group are a
+    // multiple of 4). Rows of padding entries read the chunk's first query
+    // (finite values; their outputs are never read).
+    const int gw = warp < kLoadWarp ? warp : 3;
+    static_assert(kRows == 32 * 4, "one lane per four rows");
+    const int per_tile = kRows / p.hpg;
+    const bool one_entry = p.hpg % 4 == 0;  // rows 4 l .. 4 l + 3 belong to one entry
+    int4 tl = make_int4(0, 0, 0, 0);
+    int ev[4];  // the entries of this lane's four rows (-1 past the tile's count)
+    TileRuns runs{run_lo, run_pref};
+    const uint64_t pol_q = tc::policy_evict_last();  // the phase's query rows are reused by every CTA
+    auto fetch = [&](int z) {  // independent loads: tile zt's entries start at zt * per_tile
+      const int zt = runs.at(z);
+      tl = p.tiles[zt];
+      const int* ent = p.entries + int64_t(zt) * per_tile;
+      if (one_entry) {
+        const int e = lane * 4 / p.hpg;
+        ev[0] = ev[1] = ev[2] = ev[3] = e < per_tile ? ent[e] : -1;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = (lane * 4 + j) / p.hpg;
+          ev[j] = e < per_tile ? ent[e] : -1;
+        }
+      }
+    };
+    if (gw < n) fetch(gw);
+    int last = -1;  // the last tile this warp issued
+    for (int z = gw; z < n; z += kRing) {
+      if (!tc::mbar_wait(&q_empty[gw], ((z / kRing) & 1) ^ 1, abort_flag)) {
+        fail();
+        break;
+      }
+      const int g = tl.x / p.nblk;
+      int rows[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = lane * 4 + j;
+        const int il = row / p.hpg < tl.z && ev[j] >= 0 ? (ev[j] >> 6) : 0;
+        rows[j] = (p.b * p.Nq + p.c0 + il) * p.Hq + g * p.hpg + row % p.hpg;
+      }
+      if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[gw], uint32_t(kRows) * D * 2);
+      __syncwarp();
+      {
+        uint8_t* dst = ring + gw * kSlot + lane * 4 * 128;
+#pragma unroll
+        for (int hf = 0; hf < NH; ++hf)
+          tc::tma_gather4_hint(dst + hf * (kRows * 128), &tmQ, &q_full[gw], hf * 64, rows[0], rows[1], rows[2],
+                               rows[3], pol_q);
+      }
+      last = z;
+      if (z + kRing < n) fetch(z + kRing);
+    }
+    // drain after an abort: no gather may still be landing in shared memory
+    // when the CTA exits (the slot's earlier tiles were consumed before this
+    // one could be issued; in a full run the issuers consumed every tile)
+    int zero = 0;
+    if (*abort_flag && lane == 0 && last >= 0) tc::mbar_wait(&q_full[gw], (last / kRing) & 1, &zero);
+  } else if (warp == kLoadWarp) {
+    // ------------------------------ K/V loads ------------------------------
+    // Key blocks are numbered in the order this CTA meets them (bi = 0, 1,
+    // ...); block bi's K goes to K buffer bi & 1, its V to V buffer bi % NV.
+    // A block is loaded as soon as both issuers have released the block that
+    // used its buffers before, so K runs a block ahead (and V too with two V
+    // buffers). The walk visits each block's first tile: from there the
+    // next block starts rec.w tiles on in the same run, or opens the next run.
+    if (lane == 0) {
+      const uint64_t pol_kv = tc::policy_evict_first();  // each block's K/V is read by one or two CTAs
+      int kl = 0, vl = 0;  // K / V loads issued
+      bool alive = true;
+      if (p.inject_timeout && !tc::mbar_wait_for(never_bar, 0, abort_flag, tc::kInjectedWaitCycles)) {
+        fail();
+        alive = false;
+      }
+      TileRuns runs{run_lo, run_pref};
+      for (int z = 0, bi = 0; z < n && alive; ++bi) {
+        const int zg = runs.at(z);
+        const int e_run = runs.run_end(z);
+        const int4 rec = p.tiles[zg];
+        const int g = rec.x / p.nblk, t = rec.x % p.nblk;
+        const int kb = bi & 1, vb = bi % NV;
+        if (bi >= 2 && !tc::mbar_wait(&k_empty[kb], ((bi >> 1) - 1) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&k_full[kb], kKBytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          tc::tma_load_4d_hint(k_buf + kb * kKBytes + h * kKVHalf, &tmK, &k_full[kb], h * 64, g, t * BS, p.b,
+                               pol_kv);
+        kl = bi + 1;
+        if (bi >= NV && !tc::mbar_wait(&v_empty[vb], ((bi / NV) - 1) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&v_full[vb], kKBytes);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          tc::tma_load_4d_hint(v_buf + vb * kKBytes + h * kKVHalf, &tmV, &v_full[vb], h * 64, g, t * BS, p.b,
+                               pol_kv);
+        vl = bi + 1;
+        if (rec.w < 1) {  // a malformed tile record: stop rather than walk in place
+          set_status(p.status, MSA_ERR_BOUNDS);
+          *abort_flag = 1;
+          break;
+        }
+        z = z + rec.w < e_run ? z + rec.w : e_run;
+      }
+      // no K or V copy may still be landing when the CTA exits: the last load into each buffer
+      int zero = 0;
+      for (int b2 = kl - 1; b2 >= 0 && b2 >= kl - 2; --b2) tc::mbar_wait(&k_full[b2 & 1], (b2 >> 1) & 1, &zero);
+      for (int b2 = vl - 1; b2 >= 0 && b2 >= vl - NV; --b2) tc::mbar_wait(&v_full[b2 % NV], (b2 / NV) & 1, &zero);
+    }
+  } else if (warp < kIssueWarp0 + 2) {
+    // ------------------------------- MMA issuers -------------------------------
+    // Issuer w (one thread) issues QK^T and PV of the tiles z = w, w + 2, ...
+    // (softmax warpgroup w, TMEM set w): QK(z), then PV(z) once P(z) is
+    // ready, then QK(z + 2), which overwrites S(z) = P(z) after PV(z) has
+    // read it (one thread's MMAs run in issue order). Both issuers walk every
+    // tile record to number the key blocks; at each block change each
+    // releases the block it leaves (K and V buffers, two arrivals each: one
+    // per issuer, whether or not it had tiles there), after its K and V have
+    // landed.
+    const int w = warp - kIssueWarp0;
+    if (lane == 0) {
+      const uint32_t ring_lo0 = tc::smem_desc_lo(tc::smem_u32(ring), 16);
+      const uint32_t k_lo0 = tc::smem_desc_lo(tc::smem_u32(k_buf), 16);
+      const uint32_t v_lo0 = tc::smem_desc_lo(tc::smem_u32(v_buf), kKVHalf);
+      const uint32_t t_s = tmem + uint32_t(w) * 256u;  // this issuer's TMEM set: S at t_s, O at t_s + 128
+      int kw = 0, vw = 0;  // blocks whose K / V this issuer has waited for
+      // the lookahead cursor: local tile za is chunk tile zga of run ra (which
+      // ends at local enda); the bins of tiles z + 1 and z + 2 are in flight
+      int ra = 0;
+      while (ra < p.nph && run_pref[ra + 1] == 0) ++ra;
+      int za = 0, zga = n > 0 ? run_lo[ra] : 0, enda = n > 0 ? run_pref[ra + 1] : 0;
+      auto advance = [&]() {  // za -> za + 1 (< n)
+        ++za;
+        if (za == enda) {  // opens the next non-empty run
+          do ++ra;
+          while (run_pref[ra + 1] == za);
+          zga = run_lo[ra];
+          enda = run_pref[ra + 1];
+        } else {
+          ++zga;
+        }
+      };
+      int bin_n1 = n > 0 ? p.tiles[zga].x : -1, bin_n2 = -1;
+      if (n > 1) {
+        advance();
+        bin_n2 = p.tiles[zga].x;
+      }
+      int prev_bin = -1, bi = -1;
+      for (int z = 0; z < n; ++z) {
+        const int bin = bin_n1;
+        bin_n1 = bin_n2;
+        if (z + 2 < n) {
+          advance();
+          bin_n2 = p.tiles[zga].x;
+        }
+        if (bin != prev_bin) {  // a new key block: release the one left (all its MMAs of this issuer issued)
+          if (bi >= 0) {
+            // A block is released only once its K and V have been seen to
+            // land (waited for here if this issuer had no tile in it): they
+            // were loaded after both issuers released the block before it in
+            // the same buffers, so one issuer's releases cannot run a buffer
+            // phase ahead of the other's.
+            if ((kw <= bi && !tc::mbar_wait(&k_full[bi & 1], (bi >> 1) & 1, abort_flag)) ||
+                (vw <= bi && !tc::mbar_wait(&v_full[bi % NV], (bi / NV) & 1, abort_flag))) {
+              fail();
+              break;
+            }
+            kw = vw = bi + 1;
+            tc::mma_commit(&k_empty[bi & 1]);
+            tc::mma_commit(&v_empty[bi % NV]);
+          }
+          ++bi;
+          prev_bin = bin;
+        }
+        if ((z & 1) != w) continue;
+        const int rs = z & (kRing - 1);
+        if (kw <= bi) {  // this issuer's first tile in the block: its K must have landed
+          if (!tc::mbar_wait(&k_full[bi & 1], (bi >> 1) & 1, abort_flag)) {
+            fail();
+            break;
+          }
+          kw = bi + 1;
+        }
+        if (!tc::mbar_wait(&q_full[rs], (z / kRing) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t q_lo = ring_lo0 + uint32_t(rs) * (kSlot >> 4);
+        const uint32_t k_lo = k_lo0 + uint32_t(bi & 1) * (kKBytes >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes along the swizzled 128-byte rows
+          tc::mma_f16_ss_lo<kDescHi>(t_s, q_lo + (((kk >> 2) * (kRows * 128) + off) >> 4),
+                                     k_lo + (((kk >> 2) * kKVHalf + off) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&s_full[w]);
+        tc::mma_commit(&q_empty[rs]);  // the gathered Q tile is consumed
+        const int vb = bi % NV;
+        if (vw <= bi) {  // the block's first PV here: its V must have landed
+          if (!tc::mbar_wait(&v_full[vb], (bi / NV) & 1, abort_flag)) {
+            fail();
+            break;
+          }
+          vw = bi + 1;
+        }
+        if (!tc::mbar_wait(&p_full[w], (z >> 1) & 1, abort_flag)) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t v_lo = v_lo0 + uint32_t(vb) * (kKBytes >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BS / 16; ++kk) {
+          // P (bf16 pairs packed per 32-bit column) sits where S was: 16 keys = 8 columns
+          tc::mma_f16_ts_lo<kDescHi>(t_s + 128u, t_s + uint32_t(kk) * 8u, v_lo + uint32_t(kk * 16 * 128 >> 4), kIdescPV,
+                                     kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&o_full[w]);
+      }
+      // every issued MMA completes before TMEM is released
+      int zero = 0;
+      tc::mma_commit(&done_bar[w]);
+      tc::mbar_wait(&done_bar[w], 0, &zero);
+    }
+  }  // warp 7: idle
+  } else {
+    tc::regs_inc<kSoftRegs>();
+    // --------------------------- softmax and partial store ---------------------------
+    // Warpgroups 2 and 3 take alternate tiles (TMEM set w = z & 1): the whole
+    // S row of a thread's TMEM lane in registers, causal mask in the local
+    // block, exact softmax with unnormalised probabilities as P (bf16 pairs
+    // written back over S for the PV MMA), the exponent arguments and the row
+    // sum on paired fp32 instructions, and the row's log-sum-exp stored for
+    // the combine. Then, while the tensor core computes PV(z) and QK(z + 2),
+    // O(z) is read from TMEM, divided by the row sum and stored as the tile's
+    // bf16 partial: 16-byte chunk c of row r of tile zg at
+    // part_o[(zg * D/8 + c) * 128 + r], so each warp store instruction writes
+    // 32 consecutive rows' chunk (512 contiguous bytes). PV(z + 2), which
+    // overwrites O, waits for P(z + 2), written after O(z) was read.
+    const int w = (warp - kEpiWarp0) >> 2;         // warpgroup: tiles z with z % 2 == w
+    const int quarter = warp & 3;                  // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;             // tile row
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
+    TileRuns runs{run_lo, run_pref};
+    const uint64_t pol_part = tc::policy_evict_first();  // partials are read back once, by the combine
+    const uint32_t s_addr = tmem + lane_base + uint32_t(w) * 256u;
+    // a tile's metadata straight from global memory (the Q ring slot is
+    // recycled as soon as QK^T has consumed it), loaded one tile ahead
+    int zg_n = 0, e_n = -1;
+    int4 tl_n = make_int4(0, 0, 0, 0);
+    auto meta = [&](int z) {
+      zg_n = runs.at(z);
+      tl_n = p.tiles[zg_n];
+      e_n = p.entries[int64_t(zg_n) * (kRows / p.hpg) + r / p.hpg];
+    };
+    if (w < n) meta(w);
+    for (int z = w; z < n; z += 2) {
+      const int zg = zg_n;
+      const int4 tl = tl_n;
+      const int ent = r / p.hpg < tl.z ? e_n : -1;
+      if (!tc::mbar_wait(&s_full[w], (z >> 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      if (z + 2 < n) meta(z + 2);  // in flight during this tile
+      const int bin = tl.x;
+      const bool valid = ent >= 0;
+      const int t = bin % p.nblk;
+      const int il = ent >> 6;
+      const int pos = sv.q0 + p.c0 + il;
+      const int nvalid = valid ? min(BS, pos - t * BS + 1) : BS;  // keys j <= pos inside the block
+      const bool full = nvalid >= BS;  // all keys visible (every block but the local one)
+      float inv;
+      {
+        // the whole S row in registers: one TMEM round trip; each 32-column
+        // load also returns the maximum of its columns
+        uint32_t v[BS];
+        float m32[BS / 32];
+#pragma unroll
+        for (int c = 0; c < BS / 32; ++c) m32[c] = tc::tmem_ld_max_32x32b_x32(s_addr + c * 32, v + c * 32);
+        tc::tmem_ld_wait();
+        float mx = m32[0];
+#pragma unroll
+        for (int c = 1; c < BS / 32; ++c) mx = fmaxf(mx, m32[c]);
+        if (!full) {  // the local block: the row maximum over its visible keys only
+#pragma unroll
+          for (int j = 0; j < BS; ++j)
+            if (j >= nvalid) v[j] = __float_as_uint(-INFINITY);  // exp2(-inf) = 0 below
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int j = 0; j < BS; j += 2)
+            m4[(j >> 1) & 3] = tc::fmax3(m4[(j >> 1) & 3], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        }
+        // probabilities, 32 keys at a time: packed to bf16 pairs and written
+        // back over S in TMEM at once (the PV MMA reads its A operand from
+        // there: keys 2c (low half) and 2c+1 (high half) in column c), their
+        // sum in fp32, two keys per instruction
+        const float mneg = -mx * p.scale_log2;
+        uint64_t l2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+#pragma unroll
+        for (int c0 = 0; c0 < BS / 32; ++c0) {
+          uint32_t* pk = v + c0 * 32;  // the packed pairs reuse the chunk's first 16 registers
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j]), p.scale_log2, mneg));
+            const float p1 = ex2(fmaf(__uint_as_float(v[c0 * 32 + j + 1]), p.scale_log2, mneg));
+            l2[(j >> 1) & 1] = add_f32x2(l2[(j >> 1) & 1], f32x2(p0, p1));
+            pk[j >> 1] = pack_bf16(p0, p1);
+          }
+          tc::tmem_st_32x32b_x16(s_addr + c0 * 16, pk);
+        }
+        float la, lb, lc, ld;
+        unpack_f32x2(l2[0], la, lb);
+        unpack_f32x2(l2[1], lc, ld);
+        const float l = (la + lb) + (lc + ld);
+        inv = l > 0.f ? 1.f / l : 0.f;
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&p_full[w]);
+        tc::st_f32_hint(p.part_lse + int64_t(zg) * kRows + r, valid ? mx * p.scale + logf(l) : 0.f, pol_part);
+      }
+      // O(z) = P(z) V as the tile's partial, scaled by 1 / row sum
+      if (!tc::mbar_wait(&o_full[w], (z >> 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const uint64_t inv2 = f32x2(inv, inv);
+      uint4* dst = p.part_o + int64_t(zg) * (D / 8) * kRows + r;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        tc::tmem_ld_32x32b_x32(s_addr + 128u + c0, ov);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 o;
+          o.x = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 0], ov[c * 8 + 1]), inv2));
+          o.y = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 2], ov[c * 8 + 3]), inv2));
+          o.z = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 4], ov[c * 8 + 5]), inv2));
+          o.w = pack_bf16x2(mul_f32x2(f32x2_bits(ov[c * 8 + 6], ov[c * 8 + 7]), inv2));
+          tc::st_v4_hint(dst + (c0 / 8 + c) * kRows, o, pol_part);
+        }
+      }
+      // (the next tile's P store, which lets PV overwrite O, follows these loads in program order)
+      tc::fence_before_sync();
+    }
+  }
+
+  __syncthreads();
+  if (warp == kLoadWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // combine: persistent warps, each taking (query, group) items in a strided
 // loop. A slot's partials of the group's heads are hpg consecutive partial
@@ -1308,12 +1785,22 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   return L;
 }
 
-static size_t attn_smem_bytes(int d, int Bs) {
+static size_t attn1_smem_bytes(int d, int Bs) {  // the single-issuer design
   const size_t kv = size_t(Bs) * d * 2 * (2 + attn_v_buffers(Bs));  // two K buffers, one or two V buffers
   const size_t slot = size_t(kRows) * d * 2;
   const size_t meta = size_t(kRing) * kRows * 4 + size_t(2 * kKvoMaxPhases + 1) * 4 + 16;
   return kv + kRing * slot + meta + (8 + 2 * kRing + 8 + 2) * 8 + 16;  // the base is 1024-byte aligned
 }
+
+static size_t attn2_smem_bytes(int d, int Bs) {  // the two-issuer design
+  const size_t kv = size_t(Bs) * d * 2 * (2 + attn_v_buffers(Bs));  // two K buffers, one or two V buffers
+  const size_t slot = size_t(kRows) * d * 2;
+  const size_t runs = size_t(2 * kKvoMaxPhases + 1) * 4 + 16;  // run arrays, barrier alignment
+  return kv + kRing * slot + runs + (8 + 2 * kRing + 8 + 1) * 8 + 16;  // the base is 1024-byte aligned
+}
+
+// blocks of 128 keys take the single-issuer design, smaller blocks the two-issuer one
+static size_t attn_smem_bytes(int d, int Bs) { return Bs == 128 ? attn1_smem_bytes(d, Bs) : attn2_smem_bytes(d, Bs); }
 
 // selection -> per-(group, block) entry lists, tiles and the persistent
 // grid's cost split, for one query chunk [c0, c0 + cq) of sequence b
@@ -1446,26 +1933,27 @@ cudaError_t launch_attn_kv_outer(const void* q, const void* k, const void* v, co
       prm.c0 = c0;
       {
         ProfScope pf("attn_kv_outer_tc", stream);
-#define MSA_KVO(D_, BS_)                                                                  \
+#define MSA_KVO(KERN)                                                                     \
   do {                                                                                    \
-    auto kern = attn_kv_outer_kernel<D_, BS_>;                                           \
+    auto kern = KERN;                                                                     \
     if ((e = set_attr(kern)) != cudaSuccess) return e;                                   \
     kern<<<grid, kAttnThreads, smem, stream>>>(tmK, tmV, tmQ, prm);                      \
   } while (0)
+        // blocks of 128 keys: the single-issuer design; 64 and 32: the two-issuer design
         if (d == 128) {
           if (Bs == 128)
-            MSA_KVO(128, 128);
+            MSA_KVO((attn_kv_outer_kernel<128, 128>));
           else if (Bs == 64)
-            MSA_KVO(128, 64);
+            MSA_KVO((attn_kv_outer2_kernel<128, 64>));
           else
-            MSA_KVO(128, 32);
+            MSA_KVO((attn_kv_outer2_kernel<128, 32>));
         } else {
           if (Bs == 128)
-            MSA_KVO(64, 128);
+            MSA_KVO((attn_kv_outer_kernel<64, 128>));
           else if (Bs == 64)
-            MSA_KVO(64, 64);
+            MSA_KVO((attn_kv_outer2_kernel<64, 64>));
           else
-            MSA_KVO(64, 32);
+            MSA_KVO((attn_kv_outer2_kernel<64, 32>));
         }
 #undef MSA_KVO
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

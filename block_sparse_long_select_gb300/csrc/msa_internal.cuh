@@ -111,6 +111,11 @@ struct TileRuns {
     while (z >= pref[r + 1]) ++r;
     return lo[r] + (z - pref[r]);
   }
+  // the first local tile after the run that holds z
+  __device__ __forceinline__ int run_end(int z) {
+    while (z >= pref[r + 1]) ++r;
+    return pref[r + 1];
+  }
 };
 // One thread fills lo[nph] and pref[nph + 1] (shared memory) for this CTA.
 __device__ __forceinline__ void load_tile_runs(const int* cta_seg, int nph, int grid, int* lo, int* pref) {
