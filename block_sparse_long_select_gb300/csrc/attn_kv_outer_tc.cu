@@ -853,8 +853,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, BS, false);
   constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, D, true);  // B = V is MN-major
   constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, 2);           // 128B swizzle, 8-row groups 1024 B apart
-  // TMEM columns: softmax warpgroup w owns S at [256 w, 256 w + BS) and O at [256 w + 128, 256 w + 128 + D)
-  static_assert(BS <= 128 && D <= 128, "TMEM plan: S <= 128 and O <= 128 columns per warpgroup");
+  // TMEM columns: softmax warpgroup w owns two S buffers at [256 w, 256 w + 2 BS) and O at
+  // [256 w + 128, 256 w + 128 + D); tile z uses S buffer (z >> 1) & 1
+  static_assert(BS <= 64 && D <= 128, "TMEM plan: 2 BS <= 128 columns of S and O <= 128 columns per warpgroup");
   static_assert(kRing == 4, "four gather warps, one ring slot each");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -877,8 +878,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* v_empty = bars + 6;  // [2] both issuers are done with V buffer i (2 arrivals)
   uint64_t* q_full = bars + 8;                // [kRing]
   uint64_t* q_empty = q_full + kRing;         // [kRing]
-  uint64_t* s_full = q_empty + kRing;         // [2] per softmax warpgroup
-  uint64_t* p_full = s_full + 2;              // [2]
+  uint64_t* s_full = q_empty + kRing;         // [2][2] per softmax warpgroup and S buffer
+  uint64_t* p_full = s_full + 4;              // [2]
   uint64_t* o_full = p_full + 2;              // [2]
   uint64_t* done_bar = o_full + 2;            // [2] per issuer
   uint64_t* never_bar = done_bar + 2;  // no thread arrives on it (timeout injection)
@@ -897,8 +898,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc::mbar_init(&q_full[r], 1);  // the slot's gather warp (arrival with the expected bytes)
       tc::mbar_init(&q_empty[r], 1);
     }
+    for (int s = 0; s < 4; ++s) tc::mbar_init(&s_full[s], 1);
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&s_full[s], 1);
       tc::mbar_init(&p_full[s], 4);
       tc::mbar_init(&o_full[s], 1);
       tc::mbar_init(&done_bar[s], 1);
@@ -1092,78 +1093,124 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         advance();
         bin_n2 = p.tiles[zga].x;
       }
+      // The walk over the tile records numbers the key blocks; blocks left
+      // on the way are released once this issuer's MMAs on them are issued.
       int prev_bin = -1, bi = -1;
-      for (int z = 0; z < n; ++z) {
-        const int bin = bin_n1;
-        bin_n1 = bin_n2;
-        if (z + 2 < n) {
-          advance();
-          bin_n2 = p.tiles[zga].x;
-        }
-        if (bin != prev_bin) {  // a new key block: release the one left (all its MMAs of this issuer issued)
-          if (bi >= 0) {
-            // A block is released only once its K and V have been seen to
-            // land (waited for here if this issuer had no tile in it): they
-            // were loaded after both issuers released the block before it in
-            // the same buffers, so one issuer's releases cannot run a buffer
-            // phase ahead of the other's.
-            if ((kw <= bi && !tc::mbar_wait(&k_full[bi & 1], (bi >> 1) & 1, abort_flag)) ||
-                (vw <= bi && !tc::mbar_wait(&v_full[bi % NV], (bi / NV) & 1, abort_flag))) {
-              fail();
-              break;
+      int zw = 0;                        // the next tile to walk
+      int rel0 = 0, rel1 = 0, nrel = 0;  // blocks left during the walk (at most two), to release
+      auto walk_to = [&](int zt) {       // walk up to tile zt: bi is then its block
+        while (zw <= zt && zw < n) {
+          const int bin = bin_n1;
+          bin_n1 = bin_n2;
+          if (zw + 2 < n) {
+            advance();
+            bin_n2 = p.tiles[zga].x;
+          }
+          if (bin != prev_bin) {  // a new key block
+            if (bi >= 0) {
+              if (nrel == 0)
+                rel0 = bi;
+              else
+                rel1 = bi;
+              ++nrel;
             }
-            kw = vw = bi + 1;
-            tc::mma_commit(&k_empty[bi & 1]);
-            tc::mma_commit(&v_empty[bi % NV]);
+            ++bi;
+            prev_bin = bin;
           }
-          ++bi;
-          prev_bin = bin;
+          ++zw;
         }
-        if ((z & 1) != w) continue;
+      };
+      // A block is released only once its K and V have been seen to land
+      // (waited for here if this issuer had no tile in it): they were loaded
+      // after both issuers released the block before it in the same buffers,
+      // so one issuer's releases cannot run a buffer phase ahead of the
+      // other's.
+      auto release = [&]() -> bool {
+        for (int i = 0; i < nrel; ++i) {
+          const int b = i == 0 ? rel0 : rel1;
+          if ((kw <= b && !tc::mbar_wait(&k_full[b & 1], (b >> 1) & 1, abort_flag)) ||
+              (vw <= b && !tc::mbar_wait(&v_full[b % NV], (b / NV) & 1, abort_flag)))
+            return false;
+          if (kw <= b) kw = b + 1;
+          if (vw <= b) vw = b + 1;
+          tc::mma_commit(&k_empty[b & 1]);
+          tc::mma_commit(&v_empty[b % NV]);
+        }
+        nrel = 0;
+        return true;
+      };
+      // QK^T of tile z (block bz) into S buffer (z >> 1) & 1
+      auto issue_qk = [&](int z, int bz) -> bool {
         const int rs = z & (kRing - 1);
-        if (kw <= bi) {  // this issuer's first tile in the block: its K must have landed
-          if (!tc::mbar_wait(&k_full[bi & 1], (bi >> 1) & 1, abort_flag)) {
-            fail();
-            break;
-          }
-          kw = bi + 1;
+        if (kw <= bz) {  // this issuer's first tile in the block: its K must have landed
+          if (!tc::mbar_wait(&k_full[bz & 1], (bz >> 1) & 1, abort_flag)) return false;
+          kw = bz + 1;
         }
-        if (!tc::mbar_wait(&q_full[rs], (z / kRing) & 1, abort_flag)) {
-          fail();
-          break;
-        }
+        if (!tc::mbar_wait(&q_full[rs], (z / kRing) & 1, abort_flag)) return false;
         tc::fence_after_sync();
         const uint32_t q_lo = ring_lo0 + uint32_t(rs) * (kSlot >> 4);
-        const uint32_t k_lo = k_lo0 + uint32_t(bi & 1) * (kKBytes >> 4);
+        const uint32_t k_lo = k_lo0 + uint32_t(bz & 1) * (kKBytes >> 4);
+        const int sb = (z >> 1) & 1;
+        const uint32_t d = t_s + uint32_t(sb * BS);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;  // 16 columns = 32 bytes along the swizzled 128-byte rows
-          tc::mma_f16_ss_lo<kDescHi>(t_s, q_lo + (((kk >> 2) * (kRows * 128) + off) >> 4),
+          tc::mma_f16_ss_lo<kDescHi>(d, q_lo + (((kk >> 2) * (kRows * 128) + off) >> 4),
                                      k_lo + (((kk >> 2) * kKVHalf + off) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&s_full[w]);
+        tc::mma_commit(&s_full[w * 2 + sb]);
         tc::mma_commit(&q_empty[rs]);  // the gathered Q tile is consumed
-        const int vb = bi % NV;
-        if (vw <= bi) {  // the block's first PV here: its V must have landed
-          if (!tc::mbar_wait(&v_full[vb], (bi / NV) & 1, abort_flag)) {
-            fail();
-            break;
-          }
-          vw = bi + 1;
+        return true;
+      };
+      // PV of tile z (block bz): P(z) in S buffer (z >> 1) & 1, O of this warpgroup
+      auto issue_pv = [&](int z, int bz) -> bool {
+        const int vb = bz % NV;
+        if (vw <= bz) {  // the block's first PV here: its V must have landed
+          if (!tc::mbar_wait(&v_full[vb], (bz / NV) & 1, abort_flag)) return false;
+          vw = bz + 1;
         }
-        if (!tc::mbar_wait(&p_full[w], (z >> 1) & 1, abort_flag)) {
-          fail();
-          break;
-        }
+        if (!tc::mbar_wait(&p_full[w], (z >> 1) & 1, abort_flag)) return false;
         tc::fence_after_sync();
         const uint32_t v_lo = v_lo0 + uint32_t(vb) * (kKBytes >> 4);
+        const uint32_t a = t_s + uint32_t(((z >> 1) & 1) * BS);
 #pragma unroll
         for (int kk = 0; kk < BS / 16; ++kk) {
           // P (bf16 pairs packed per 32-bit column) sits where S was: 16 keys = 8 columns
-          tc::mma_f16_ts_lo<kDescHi>(t_s + 128u, t_s + uint32_t(kk) * 8u, v_lo + uint32_t(kk * 16 * 128 >> 4), kIdescPV,
+          tc::mma_f16_ts_lo<kDescHi>(t_s + 128u, a + uint32_t(kk) * 8u, v_lo + uint32_t(kk * 16 * 128 >> 4), kIdescPV,
                                      kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&o_full[w]);
+        return true;
+      };
+      // Order: QK(z + 2) goes ahead of PV(z) (the other S buffer), so S(z + 2)
+      // is ready when the softmax finishes tile z; PV(z) then QK(z + 4)
+      // keeps P(z) read before it is overwritten. Tile z + 2's K buffer must
+      // not wait on a release that only follows PV(z): a block two or more
+      // ahead takes the order PV(z), releases, QK(z + 2).
+      bool alive = true;
+      walk_to(w);
+      int bz = bi;
+      if (!release() || (w < n && !issue_qk(w, bz))) {
+        fail();
+        alive = false;
+      }
+      for (int z = w; z < n && alive; z += 2) {
+        int bz2 = -1;
+        bool early = false;
+        if (z + 2 < n) {
+          walk_to(z + 2);
+          bz2 = bi;
+          early = bz2 <= bz + 1;
+          if (early && !issue_qk(z + 2, bz2)) {
+            fail();
+            break;
+          }
+        }
+        if (!issue_pv(z, bz) || !release() || (z + 2 < n && !early && !issue_qk(z + 2, bz2))) {
+          fail();
+          break;
+        }
+        bz = bz2;
       }
       // every issued MMA completes before TMEM is released
       int zero = 0;
@@ -1192,7 +1239,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const SeqView sv = seq_view(p.q_offset, p.kv_len, p.b, p.Nq, p.Nk, false);
     TileRuns runs{run_lo, run_pref};
     const uint64_t pol_part = tc::policy_evict_first();  // partials are read back once, by the combine
-    const uint32_t s_addr = tmem + lane_base + uint32_t(w) * 256u;
+    const uint32_t t_wg = tmem + lane_base + uint32_t(w) * 256u;  // this warpgroup's TMEM set (own lanes)
     // a tile's metadata straight from global memory (the Q ring slot is
     // recycled as soon as QK^T has consumed it), loaded one tile ahead
     int zg_n = 0, e_n = -1;
@@ -1207,7 +1254,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int zg = zg_n;
       const int4 tl = tl_n;
       const int ent = r / p.hpg < tl.z ? e_n : -1;
-      if (!tc::mbar_wait(&s_full[w], (z >> 1) & 1, abort_flag)) {
+      const int sb = (z >> 1) & 1;  // S buffer of this tile
+      const uint32_t s_addr = t_wg + uint32_t(sb * BS);
+      if (!tc::mbar_wait(&s_full[w * 2 + sb], (z >> 2) & 1, abort_flag)) {
         fail();
         break;
       }
@@ -1282,7 +1331,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
-        tc::tmem_ld_32x32b_x32(s_addr + 128u + c0, ov);
+        tc::tmem_ld_32x32b_x32(t_wg + 128u + c0, ov);
         tc::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -1796,7 +1845,7 @@ static size_t attn2_smem_bytes(int d, int Bs) {  // the two-issuer design
   const size_t kv = size_t(Bs) * d * 2 * (2 + attn_v_buffers(Bs));  // two K buffers, one or two V buffers
   const size_t slot = size_t(kRows) * d * 2;
   const size_t runs = size_t(2 * kKvoMaxPhases + 1) * 4 + 16;  // run arrays, barrier alignment
-  return kv + kRing * slot + runs + (8 + 2 * kRing + 8 + 1) * 8 + 16;  // the base is 1024-byte aligned
+  return kv + kRing * slot + runs + (8 + 2 * kRing + 10 + 1) * 8 + 16;  // the base is 1024-byte aligned
 }
 
 // blocks of 128 keys take the single-issuer design, smaller blocks the two-issuer one
