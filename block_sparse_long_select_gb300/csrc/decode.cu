@@ -423,6 +423,8 @@ __global__ void __launch_bounds__(kDiThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, 2);  // 128B swizzle, 8-row groups 1024 B apart
+      const uint32_t stage_lo0 = tc::smem_desc_lo(tc::smem_u32(stages), 16);
       int n = 0;
       for (int x = x0; x < x1; ++x, ++n) {
         const int s = n % kDiStages, a = n % kDiAcc;
@@ -432,13 +434,12 @@ __global__ void __launch_bounds__(kDiThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        const uint32_t sa = tc::smem_u32(stages + s * kDiStage);
+        // descriptors from low words: the stage's first 16-column slice plus 32 bytes per slice
+        const uint32_t a_lo = stage_lo0 + uint32_t(s) * (kDiStage >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, 1024, 2);
-          const uint64_t bd = tc::smem_desc(sa + kDiA + kk * 32, 16, 1024, 2);
-          tc::mma_f16_ss(tmem + uint32_t(a) * 32u, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_f16_ss_lo<kDescHi>(tmem + uint32_t(a) * 32u, a_lo + uint32_t(kk * 2), a_lo + (kDiA >> 4) + uint32_t(kk * 2),
+                                     kIdesc, kk > 0 ? 1u : 0u);
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&acc_full[a]);
       }
