@@ -296,14 +296,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ncand = 0;
 #pragma unroll
       for (int k = 0; k < kRegList; ++k) L[k] = 0;
+      // Blocks are offered in ascending t, so a candidate ranks above a kept
+      // key exactly when its score word (the key's high 32 bits) is larger:
+      // on equal scores the earlier (lower) block ranks higher. The compares
+      // take 32-bit words; invalid candidates (key 0) rank above nothing.
       auto offer_reg = [&](int t, float mx) {
         const bool valid = cand_row && unsigned(t - fs) < unsigned(loc - fs);  // fs <= t < loc
         const uint64_t x = valid ? rank_key(mx, t) : 0ull;
+        const uint32_t xh = uint32_t(x >> 32);
         ncand += valid ? 1 : 0;
-        if (__any_sync(0xffffffffu, x > L[kRegList - 1])) {
+        if (__any_sync(0xffffffffu, xh > uint32_t(L[kRegList - 1] >> 32))) {
+          bool c[kRegList];  // the candidate ranks above L[k]
 #pragma unroll
-          for (int k = kRegList - 1; k > 0; --k) L[k] = x > L[k - 1] ? L[k - 1] : (x > L[k] ? x : L[k]);
-          L[0] = x > L[0] ? x : L[0];
+          for (int k = 0; k < kRegList; ++k) c[k] = xh > uint32_t(L[k] >> 32);
+#pragma unroll
+          for (int k = kRegList - 1; k > 0; --k) L[k] = c[k - 1] ? L[k - 1] : (c[k] ? x : L[k]);
+          L[0] = c[0] ? x : L[0];
         }
       };
       auto offer = [&](int t, float mx) {  // candidate block t with maximum mx
