@@ -38,6 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {  # kernel name -> source file (for the ncu traffic freshness check)
     "index_blockmax_table": "index_table.cu", "topk_from_table": "index_table.cu",
     "attn_query_outer": "attn_query_outer.cu", "index_fused_tc": "index_fused_tc.cu",
+    "index_topk_table": "index_fused_tc.cu",
     "attn_kv_outer_tc": "attn_kv_outer_tc.cu", "attn_invert": "attn_kv_outer_tc.cu",
     "attn_combine": "attn_kv_outer_tc.cu", "decode_index": "decode.cu", "decode_topk": "decode.cu",
     "decode_attn": "decode.cu", "kl_tile": "attn_kv_outer_tc.cu",
@@ -217,8 +218,13 @@ def prefill_work(w, sel, qo, kl):
     pos = qo[:, None].astype(np.int64) + np.arange(w.Nq)[None, :]
     visible = np.minimum(pos + 1, kl[:, None]).sum()
     att = attended_keys(sel, qo, kl, w.Bs)
+    # top-K over a block-max table: the candidate maxima t < loc of every row
+    # that ranks (more than K visible blocks) read once, the selection written
+    loc = pos // w.Bs
+    cand = np.where(loc + 1 > w.K, loc, 0).sum()
     return {"index_flops": 2.0 * w.di * w.G * float(visible),
             "attn_flops": 4.0 * w.d * (w.Hq // w.G) * float(att),
+            "topk_bytes": 4.0 * w.G * float(cand) + 4.0 * w.K * w.G * w.B * w.Nq,
             "attended_keys": att, "visible_keys": int(visible)}
 
 
@@ -265,6 +271,8 @@ def roofline_for(kernel, prof, work, peaks, peak_src, workload, steps, mode="pre
             return None
     elif kernel in ("index_fused_tc", "index_blockmax_table"):
         bound, unit, per_step = "tensor", "TFLOP/s", work["index_flops"]
+    elif kernel == "index_topk_table":
+        bound, unit, per_step = "hbm", "GB/s", work["topk_bytes"]
     elif kernel in ("attn_kv_outer_tc", "attn_query_outer"):
         bound, unit, per_step = "tensor", "TFLOP/s", work["attn_flops"]
     elif kernel in ("kl_tile", "kl_tile_tc"):

@@ -489,11 +489,6 @@ __global__ void __launch_bounds__(kDiThreads, 1)
   }
 }
 
-__device__ __forceinline__ uint32_t ord_f32(float m) {
-  uint32_t u = __float_as_uint(m);
-  if (u == 0x80000000u) u = 0u;  // -0 == +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // Exact top-K of one (sequence, group) row by one warp, from the row's 32-key
 // sub-block maxima. Candidates are the blocks t < loc; their maxima become

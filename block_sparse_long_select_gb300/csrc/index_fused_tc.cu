@@ -2,11 +2,15 @@
 //   index scores  S = iq . ik^T on tcgen05 (TMA-fed shared-memory operands,
 //                 fp32 accumulators in TMEM),
 //   block max     pooled straight out of TMEM in the epilogue,
-//   top-K         a running exact top-(K-1) per row over the candidate blocks
-//                 t < loc, then the local block appended (with the sequence
-//                 start forced as well: top-(K-2) over 1 <= t < loc, plus
-//                 block 0),
-// so neither the token-score matrix nor the block-max table ever reaches HBM.
+//   top-K         exact top-(K-1) per row over the candidate blocks t < loc,
+//                 then the local block appended (with the sequence start
+//                 forced as well: top-(K-2) over 1 <= t < loc, plus block 0).
+// For K - 1 <= 15 the top-K is a running list in registers inside the kernel,
+// so neither the token-score matrix nor the block-max table reaches HBM. For
+// larger K (many blocks per row at small block sizes) the kernel writes the
+// candidate block maxima of a chunk of rows to a workspace table, and
+// index_topk_table selects from it, one warp per row; the token scores still
+// never leave the chip.
 // (hyper.ai summary of paper 2606.13392, section "方法": per GQA group, dot-
 //  product scores of the index query against every visible key, Block Max
 //  Pooling, Top-K blocks, the block holding the query always included;
@@ -21,13 +25,16 @@
 // out in a static serpentine order, longest first, over a persistent grid of
 // one CTA per SM.
 //
-// Warp roles (320 threads): warps 0-7 epilogue (warpgroup m reads TMEM lanes
+// Warp roles (384 threads): warps 0-7 epilogue (warpgroup m reads TMEM lanes
 // of MMA tile m), warp 8 TMA producer, warp 9 TMEM owner + MMA issuer.
 // Pipelines: key tiles in an S-stage shared-memory ring; index-query tiles in
 // nA buffers; two TMEM accumulator sets of 2 x 128 columns (512 columns).
 // Every wait is bounded; on expiry the kernel records MSA_ERR_TIMEOUT, stops
 // issuing work, drains its copies and MMAs, frees TMEM and returns.
+#include <algorithm>
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 
 #include "msa_internal.cuh"
 #include "tc_utils.cuh"
@@ -47,14 +54,17 @@ static_assert(128 * kProdRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "regis
 constexpr int kRegList = 15;       // candidates kept in registers when K - 1 <= 15
 
 struct Unit {
-  int b, row0, nrows, q0, nt;
+  int gu, b, row0, nrows, q0, nt;
   bool ok;
 };
 
-__device__ __forceinline__ Unit get_unit(int u, int nunits, int nrb, int NqG, int G, int Nq, int Nk, int Bs, int K,
-                                         int fs, const int32_t* q_offset, const int32_t* kv_len) {
+// u-th unit of the launch's range [unit_lo, unit_lo + nunits) of the flat
+// (sequence, row block) units
+__device__ __forceinline__ Unit get_unit(int u, int unit_lo, int nunits, int nrb, int NqG, int G, int Nq, int Nk,
+                                         int Bs, int K, int fs, const int32_t* q_offset, const int32_t* kv_len) {
   Unit U;
-  const int gu = nunits - 1 - u;  // longest units (latest rows) first
+  const int gu = unit_lo + nunits - 1 - u;  // longest units (latest rows) first
+  U.gu = gu;
   U.b = gu / nrb;
   const int rb = gu % nrb;
   U.row0 = rb * kUnitRows;
@@ -89,11 +99,27 @@ __device__ __forceinline__ float block_max(const uint32_t* v) {
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
-template <int DI, int BS, bool REG>
+// Table rows are written by TMA tensor stores from shared memory where a
+// tile's blocks of one row fill at least 16 bytes (blocks of 32 / 64 keys):
+// each epilogue warp stages its 32 rows x (256 / Bs) maxima, double-buffered.
+template <int BS>
+constexpr bool table_tma() { return (kTileN / BS) * 4 >= 16; }
+template <int BS>
+constexpr size_t table_stage_bytes() { return table_tma<BS>() ? size_t(kEpiWarps) * 2 * 32 * (kTileN / BS) * 4 : 0; }
+
+// REG: top-K in a register list (K - 1 <= 15); TABLE: the candidate block
+// maxima of rows of units [unit_lo, unit_lo + nunits) go to table[row - first
+// row of unit_lo][t] (row stride tstride floats; tmT maps that chunk table),
+// and no selection is written.
+template <int DI, int BS, bool REG, bool TABLE>
 __global__ void __launch_bounds__(kThreads, 1)
     index_fused_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len, int B, int Nq,
-                          int Nk, int G, int K, int fs, int nA, int S, int32_t* __restrict__ sel, uint32_t* status) {
+                          const __grid_constant__ CUtensorMap tmT, const int32_t* __restrict__ q_offset,
+                          const int32_t* __restrict__ kv_len, int Nq, int Nk, int G, int K, int fs, int nA, int S,
+                          int unit_lo, int nunits, int32_t* __restrict__ sel, float* __restrict__ table, int tstride,
+                          uint32_t* status) {
+  static_assert(REG != TABLE, "one top-K form");
+  constexpr bool kTmaTable = TABLE && table_tma<BS>();
   constexpr uint32_t kABytes = kUnitRows * DI * 2;   // one unit of index queries
   constexpr uint32_t kATile = 128 * DI * 2;          // one 128-row MMA tile
   constexpr uint32_t kBBytes = kTileN * DI * 2;      // one key tile
@@ -110,8 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* b_buf = a_buf + size_t(nA) * kABytes;               // S x kBBytes
   const int Kl = K - 1;  // list slots per row (the host sizes shared memory for K - 1)
   const int Kc = K - 1 - fs;  // blocks ranked per row: fs = 1 keeps block 0 outright, like the local block
-  uint64_t* lists = reinterpret_cast<uint64_t*>(b_buf + size_t(S) * kBBytes);  // [Kl][256]
-  uint64_t* bars = lists + size_t(Kl > 0 ? Kl : 1) * kUnitRows;
+  float* stage = reinterpret_cast<float*>(b_buf + size_t(S) * kBBytes);  // [8 warps][2][32 rows][256 / BS]
+  uint64_t* lists = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(stage) + (TABLE ? table_stage_bytes<BS>() : 0));  // [Kl][256]
+  uint64_t* bars = lists + size_t(TABLE ? 0 : (Kl > 0 ? Kl : 1)) * kUnitRows;
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* a_full = empty + S;
@@ -125,7 +152,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NqG = Nq * G;
   const int nrb = (NqG + kUnitRows - 1) / kUnitRows;
-  const int nunits = B * nrb;
   const int ncta = gridDim.x, cta = blockIdx.x;
   const int rounds = (nunits + ncta - 1) / ncta;
 
@@ -175,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < rounds && alive; ++r) {
         const int u = unit_at(r, cta, ncta);
         if (u >= nunits) continue;
-        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
+        const Unit U = get_unit(u, unit_lo, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
         if (U.nt == 0) continue;
         const int x = jA % nA;
         if (!tc::mbar_wait(&a_empty[x], ((jA / nA) & 1) ^ 1, abort_flag)) {
@@ -215,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < rounds && alive; ++r) {
         const int u = unit_at(r, cta, ncta);
         if (u >= nunits) continue;
-        const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
+        const Unit U = get_unit(u, unit_lo, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
         if (U.nt == 0) continue;
         const int x = jA % nA;
         if (!tc::mbar_wait(&a_full[x], (jA / nA) & 1, abort_flag)) {
@@ -271,22 +297,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kAcc = 0;
     bool alive = true;
     uint64_t* my_list = lists + urow;  // entry k at my_list[k * 256]
+    int nstore = 0;  // this warp's staged table stores so far (buffer = parity)
     for (int r = 0; r < rounds && alive; ++r) {
       const int u = unit_at(r, cta, ncta);
       if (u >= nunits) continue;
-      const Unit U = get_unit(u, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
+      const Unit U = get_unit(u, unit_lo, nunits, nrb, NqG, G, Nq, Nk, BS, K, fs, q_offset, kv_len);
       const bool active = urow < U.nrows;
       const int row = U.row0 + urow;
       const int pos = U.q0 + row / G;
       const int loc = pos / BS;
       const bool dense = loc + 1 <= K;
       const bool cand_row = active && U.ok && !dense;
-      // This row's best Kc candidates so far, as a binary min-heap of rank
-      // keys (unique: the block id is part of the key) in its shared-memory
-      // slots; the root is the acceptance threshold once the heap is full.
-      // An accepted candidate costs at most log2(Kc) levels.
-      int cnt = 0;
-      uint64_t thr = 0;
       // REG (K - 1 <= 15): the best candidates so far in registers, sorted
       // descending and padded with key 0 (below every real key); an insertion
       // is a branch-free compare-and-shift over the list, taken by the whole
@@ -314,41 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           L[0] = c[0] ? x : L[0];
         }
       };
-      auto offer = [&](int t, float mx) {  // candidate block t with maximum mx
-        if (t >= loc || t < fs) return;
-        const uint64_t key = rank_key(mx, t);
-        if (cnt < Kc) {  // fill: sift up
-          int i = cnt++;
-          while (i > 0) {
-            const int pi = (i - 1) >> 1;
-            const uint64_t pv = my_list[pi * kUnitRows];
-            if (pv < key) break;
-            my_list[i * kUnitRows] = pv;
-            i = pi;
-          }
-          my_list[i * kUnitRows] = key;
-          if (cnt == Kc) thr = my_list[0];
-        } else if (key > thr) {  // replace the minimum: sift down
-          int i = 0;
-          while (true) {
-            int c = 2 * i + 1;
-            if (c >= Kc) break;
-            uint64_t cv = my_list[c * kUnitRows];
-            if (c + 1 < Kc) {
-              const uint64_t c2 = my_list[(c + 1) * kUnitRows];
-              if (c2 < cv) {
-                cv = c2;
-                ++c;
-              }
-            }
-            if (key < cv) break;
-            my_list[i * kUnitRows] = cv;
-            i = c;
-          }
-          my_list[i * kUnitRows] = key;
-          thr = my_list[0];
-        }
-      };
       for (int n = 0; n < U.nt; ++n, ++kAcc) {
         if (!tc::mbar_wait(&acc_full[m], kAcc & 1, abort_flag)) {
           fail();
@@ -360,22 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block maxima of the whole tile first (the accumulator is released
         // as soon as its last columns are in registers), offers afterwards
         float bm[kTileN / BS];
-        if constexpr (!REG || BS == 128) {
+        if constexpr (TABLE || BS == 128) {
           // each 32-column load returns the maximum of its columns as well
-          // (two loads in flight where the heap takes registers)
-          constexpr int kWave = REG ? kChunk / 32 : 2;
 #pragma unroll
           for (int c = 0; c < kTileN / kChunk; ++c) {
             float m32[kChunk / 32];
 #pragma unroll
-            for (int q0 = 0; q0 < kChunk / 32; q0 += kWave) {
-#pragma unroll
-              for (int q = q0; q < q0 + kWave; ++q) {
-                uint32_t v[32];  // the values themselves are not needed
-                m32[q] = tc::tmem_ld_max_32x32b_x32(taddr + c * kChunk + q * 32, v);
-              }
-              tc::tmem_ld_wait();
+            for (int q = 0; q < kChunk / 32; ++q) {
+              uint32_t v[32];  // the values themselves are not needed
+              m32[q] = tc::tmem_ld_max_32x32b_x32(taddr + c * kChunk + q * 32, v);
             }
+            tc::tmem_ld_wait();
             if (c == kTileN / kChunk - 1) {  // the whole accumulator has been read: release it
               tc::fence_before_sync();
               __syncwarp();
@@ -407,20 +388,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int bi = 0; bi < kChunk / BS; ++bi) bm[c * (kChunk / BS) + bi] = block_max<BS>(v + bi * BS);
           }
         }
-        if constexpr (REG) {
+        if constexpr (TABLE) {
+          // this tile's blocks t < loc, as one full-sector vector store per row
+          // where the whole tile is visible
+          constexpr int kPer = kTileN / BS;
+          const int t0 = n * kPer;
+          if constexpr (kTmaTable) {
+            // all 32 rows of the warp (rows that rank nothing hold values no
+            // one reads; columns past loc likewise, inside the padded row)
+            float* buf = stage + size_t(warp * 2 + (nstore & 1)) * 32 * kPer;
+            if (lane == 0) tc::bulk_wait_read_but_one();  // the store of two tiles ago has read this buffer
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < kPer; j += 4)
+              *reinterpret_cast<float4*>(buf + lane * kPer + j) = make_float4(bm[j], bm[j + 1], bm[j + 2], bm[j + 3]);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tc::tma_store_2d(&tmT, buf, t0, (U.gu - unit_lo) * kUnitRows + m * 128 + quarter * 32);
+              tc::bulk_commit();
+            }
+            ++nstore;
+          } else if (cand_row) {
+            float* dst = table + (int64_t(U.gu - unit_lo) * kUnitRows + urow) * tstride + t0;
+            if (t0 + kPer <= loc) {
+              if constexpr (kPer >= 4) {
+#pragma unroll
+                for (int j = 0; j < kPer; j += 4)
+                  *reinterpret_cast<float4*>(dst + j) = make_float4(bm[j], bm[j + 1], bm[j + 2], bm[j + 3]);
+              } else {
+                *reinterpret_cast<float2*>(dst) = make_float2(bm[0], bm[1]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < kPer; ++j)
+                if (t0 + j < loc) dst[j] = bm[j];
+            }
+          }
+        } else {
 #pragma unroll
           for (int j = 0; j < kTileN / BS; ++j) offer_reg(n * (kTileN / BS) + j, bm[j]);
-        } else if (cand_row) {
-#pragma unroll 1
-          for (int j = 0; j < kTileN / BS; ++j) offer(n * (kTileN / BS) + j, bm[j]);
         }
       }
-      if constexpr (REG) {  // the best min(candidates, Kc) keys go to the row's slots
-        cnt = ncand < Kc ? ncand : Kc;
+      if constexpr (TABLE) continue;  // the selection kernel writes this chunk's rows
+      // the best min(candidates, Kc) keys go to the row's slots
+      const int cnt = ncand < Kc ? ncand : Kc;
 #pragma unroll
-        for (int k = 0; k < kRegList; ++k)
-          if (k < cnt) my_list[k * kUnitRows] = L[k];
-      }
+      for (int k = 0; k < kRegList; ++k)
+        if (k < cnt) my_list[k * kUnitRows] = L[k];
       if (!alive || !active) continue;
       int32_t* out = sel + (int64_t(U.b) * NqG + row) * K;
       if (!U.ok) {
@@ -446,12 +461,219 @@ __global__ void __launch_bounds__(kThreads, 1)
           out[k] = k - fs < cnt ? int32_t(my_list[(k - fs) * kUnitRows]) : (k - fs == cnt ? loc : -1);
       }
     }
+    // the staged table stores are complete before the shared memory goes away
+    if constexpr (kTmaTable) {
+      if (lane == 0) tc::bulk_wait_all();
+      __syncwarp();
+    }
   }
 
   __syncthreads();
   if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// index_topk_table: the exact top-K of every row of a table chunk, one warp
+// per (token, group) row (the same selection rule as the fused top-K: the
+// K - 1 - fs best blocks fs <= t < loc by maximum, ties to the lower block,
+// then ascending, the local block after them and block 0 first if fs).
+//  1. Each lane keeps the NS largest of its candidates t = fs + lane + 32 j.
+//     Among those 32 NS sample values, T = the largest one with at least
+//     `need` sample values >= T: then at least `need` candidates are >= T, so
+//     the need-th largest candidate v* is >= T, and only candidates >= T can
+//     be chosen.
+//  2. The candidates >= T are compacted in ascending t into the warp's list
+//     (a second pass over the row, from L2).
+//  3. v* by bisection over the list's order-preserving 32-bit values (two bits
+//     per round, starting below the bits that T and the row maximum share;
+//     the three counts of a round are summed as one packed word), then every
+//     value above v* and the lowest-t values equal to v*, compacted in list
+//     order.
+// The two passes compare floats (the order of the 32-bit values, with -0 and
+// +0 equal); only listed candidates are converted. A list that would
+// overflow (many values tied at T) bisects over the row itself instead.
+// NS = 1 serves need <= 32, NS = 2 need <= 64.
+// ---------------------------------------------------------------------------
+constexpr int kSelWarps = 8;
+constexpr int kSelCap = 256;  // list entries per warp
+constexpr int kSelBatch = 8;  // row loads in flight per lane
+
+__device__ __forceinline__ uint32_t cand_value(const float* __restrict__ M, int t) {
+  const uint32_t v = ord_f32(__ldg(M + t));
+  return v > 1u ? v : 1u;  // 0 is kept for "no candidate"
+}
+__device__ __forceinline__ float ord_inv(uint32_t u) {  // the float of an order-preserving value
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+template <int NS>
+__global__ void __launch_bounds__(kSelWarps * 32) index_topk_table_kernel(
+    const float* __restrict__ table, int tstride, int unit_lo, int nrows, int nrb, int NqG, int G, int Nq, int Nk,
+    int Bs, int K, int fs, const int32_t* __restrict__ q_offset, const int32_t* __restrict__ kv_len,
+    int32_t* __restrict__ sel, uint32_t* status) {
+  __shared__ uint32_t list_v[kSelWarps][kSelCap];
+  __shared__ int list_t[kSelWarps][kSelCap];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  const int r = blockIdx.x * kSelWarps + warp;  // row of the chunk
+  if (r >= nrows) return;
+  const int gu = unit_lo + r / kUnitRows;
+  const int b = gu / nrb;
+  const int row = (gu % nrb) * kUnitRows + r % kUnitRows;
+  if (row >= NqG) return;  // past the last row of a sequence
+  int32_t* out = sel + (int64_t(b) * NqG + row) * K;
+  const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
+  if (!sv.ok) {
+    for (int k = lane; k < K; k += 32) out[k] = -1;
+    if (lane == 0 && row % kUnitRows == 0) set_status(status, MSA_ERR_BOUNDS);
+    return;
+  }
+  const int loc = (sv.q0 + row / G) / Bs;
+  if (loc + 1 <= K) {  // every visible block
+    for (int k = lane; k < K; k += 32) out[k] = k <= loc ? k : -1;
+    return;
+  }
+  const int need = K - 1 - fs;
+  if (lane == 0) {
+    if (fs) out[0] = 0;
+    out[K - 1] = loc;
+  }
+  if (need == 0) return;
+  out += fs;
+  const float* M = table + int64_t(r) * tstride;
+  // 1. per-lane sample (kSelBatch loads in flight per lane; -inf past the row)
+  float s0 = -INFINITY, s1 = -INFINITY;
+  for (int t0 = fs; t0 < loc; t0 += 32 * kSelBatch) {
+    float v[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int t = t0 + 32 * u + lane;
+      v[u] = t < loc ? __ldg(M + t) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      if constexpr (NS == 1) {
+        s0 = fmaxf(s0, v[u]);
+      } else {
+        s1 = fmaxf(s1, fminf(s0, v[u]));
+        s0 = fmaxf(s0, v[u]);
+      }
+    }
+  }
+  int c0 = 0, c1 = 0;
+#pragma unroll 8
+  for (int o = 0; o < 32; ++o) {
+    const float x0 = __shfl_sync(0xffffffffu, s0, o);
+    c0 += x0 >= s0;
+    if constexpr (NS == 2) {
+      const float x1 = __shfl_sync(0xffffffffu, s1, o);
+      c0 += x1 >= s0;
+      c1 += (x0 >= s1) + (x1 >= s1);
+    }
+  }
+  uint32_t mine = c0 >= need ? ord_f32(s0) : 0u;
+  if constexpr (NS == 2) mine = max(mine, c1 >= need ? ord_f32(s1) : 0u);
+  const uint32_t T = max(__reduce_max_sync(0xffffffffu, mine), 1u);
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, max(ord_f32(s0), 1u));  // the row maximum
+  const float Tf = ord_inv(T);
+  // 2. candidates >= T in ascending t
+  uint32_t* lv = list_v[warp];
+  int* ltb = list_t[warp];
+  int C = 0;
+  for (int t0 = fs; t0 < loc; t0 += 32 * kSelBatch) {
+    float v[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {
+      const int t = t0 + 32 * u + lane;
+      v[u] = t < loc ? __ldg(M + t) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u) {  // ascending t: batch by batch, then lane by lane
+      const bool f = v[u] >= Tf;
+      const unsigned fm = __ballot_sync(0xffffffffu, f);
+      if (fm) {
+        if (f) {
+          const int q = C + __popc(fm & lt);
+          if (q < kSelCap) {
+            lv[q] = max(ord_f32(v[u]), 1u);
+            ltb[q] = t0 + 32 * u + lane;
+          }
+        }
+        C += __popc(fm);
+      }
+    }
+  }
+  __syncwarp();
+  // 3. v*: the largest value with at least `need` values >= it
+  const bool listed = C <= kSelCap;
+  constexpr int kPerLane = kSelCap / 32;
+  uint32_t e[kPerLane];
+#pragma unroll
+  for (int k = 0; k < kPerLane; ++k) {
+    const int i = lane + 32 * k;
+    e[k] = (listed && i < C) ? lv[i] : 0u;
+  }
+  const uint32_t diff = T ^ hi;
+  const int nb = diff ? ((32 - __clz(int(diff))) + 1) & ~1 : 0;  // low bits to resolve (even)
+  uint32_t v = nb >= 32 ? 0u : (T & ~((1u << nb) - 1u));
+  for (int sh = nb - 2; sh >= 0; sh -= 2) {
+    const uint32_t c1v = v | (1u << sh), c2v = v | (2u << sh), c3v = v | (3u << sh);
+    int n1, n2, n3;
+    if (listed) {  // counts of at most kSelCap in 10-bit fields of one word
+      uint32_t n = 0;
+#pragma unroll
+      for (int k = 0; k < kPerLane; ++k)
+        if (32 * k < C) n += uint32_t(e[k] >= c1v) + (uint32_t(e[k] >= c2v) << 10) + (uint32_t(e[k] >= c3v) << 20);
+      n = __reduce_add_sync(0xffffffffu, n);
+      n1 = int(n & 1023u), n2 = int((n >> 10) & 1023u), n3 = int(n >> 20);
+    } else {
+      int a1 = 0, a2 = 0, a3 = 0;
+      for (int t = fs + lane; t < loc; t += 32) {
+        const uint32_t x = cand_value(M, t);
+        a1 += x >= c1v;
+        a2 += x >= c2v;
+        a3 += x >= c3v;
+      }
+      n1 = __reduce_add_sync(0xffffffffu, a1);
+      n2 = __reduce_add_sync(0xffffffffu, a2);
+      n3 = __reduce_add_sync(0xffffffffu, a3);
+    }
+    const uint32_t best = n3 >= need ? 3u : (n2 >= need ? 2u : (n1 >= need ? 1u : 0u));
+    v |= best << sh;
+  }
+  // everything above v*, then the lowest-t values equal to v*
+  int gt = 0;
+  if (listed) {
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) gt += e[k] > v;
+  } else {
+    for (int t = fs + lane; t < loc; t += 32) gt += cand_value(M, t) > v;
+  }
+  const int ties = need - __reduce_add_sync(0xffffffffu, gt);
+  int base = 0, eq_seen = 0;
+  auto emit = [&](uint32_t x, int t, bool have) {
+    const bool eq = have && x == v;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+    const bool take = have && (x > v || (eq && eq_seen + __popc(eqm & lt) < ties));
+    const unsigned tm = __ballot_sync(0xffffffffu, take);
+    if (take) out[base + __popc(tm & lt)] = t;
+    base += __popc(tm);
+    eq_seen += __popc(eqm);
+  };
+  if (listed) {
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) {
+      const int i = lane + 32 * k;
+      if (32 * k < C) emit(e[k], i < C ? ltb[i] : 0, i < C);
+    }
+  } else {
+    for (int t0 = fs; t0 < loc; t0 += 32) {
+      const int t = t0 + lane;
+      emit(t < loc ? cand_value(M, t) : 0u, t, t < loc);
+    }
   }
 }
 
@@ -471,6 +693,32 @@ int num_sms() {
 
 }  // namespace
 
+namespace {
+// Chunk table: rows of whole units, row stride a multiple of 8 floats (32-byte
+// rows for the vector stores), at most ~4 GiB unless that leaves fewer than
+// four units per SM. MSA_INDEX_TABLE_UNITS (environment, read once per
+// process) sets the units per chunk instead.
+constexpr size_t kTableBudget = size_t(4) << 30;
+int table_stride(int Nk, int Bs) { return (((Nk + Bs - 1) / Bs) + 7) & ~7; }
+int table_chunk_units(int B, int Nq, int Nk, int G, int Bs) {
+  static int env = -1;
+  if (env < 0) {
+    const char* e = getenv("MSA_INDEX_TABLE_UNITS");
+    env = e ? atoi(e) : 0;
+  }
+  const int64_t total = int64_t(B) * ((int64_t(Nq) * G + kUnitRows - 1) / kUnitRows);
+  const size_t unit_bytes = size_t(kUnitRows) * table_stride(Nk, Bs) * sizeof(float);
+  int64_t cu = env > 0 ? env : std::max<int64_t>(4 * kNumSMs, int64_t(kTableBudget / unit_bytes));
+  return int(std::min<int64_t>(cu, total));
+}
+bool uses_table(int K) { return K - 1 > kRegList; }
+}  // namespace
+
+size_t index_fused_table_bytes(int B, int Nq, int Nk, int G, int Bs, int K) {
+  if (!uses_table(K)) return 0;
+  return size_t(table_chunk_units(B, Nq, Nk, G, Bs)) * kUnitRows * table_stride(Nk, Bs) * sizeof(float);
+}
+
 bool index_fused_supported(int dtype, int Nq, int G, int di, int Bs, int K) {
   if (dtype != MSA_BF16 || (di != 32 && di != 64)) return false;
   if (Bs != 32 && Bs != 64 && Bs != 128) return false;
@@ -481,8 +729,10 @@ bool index_fused_supported(int dtype, int Nq, int G, int di, int Bs, int K) {
 
 cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len,
                                   int B, int Nq, int Nk, int G, int di, int Bs, int K, int fs, int32_t* sel,
-                                  uint32_t* status, cudaStream_t stream) {
+                                  float* table, size_t table_bytes, uint32_t* status, cudaStream_t stream) {
   const int NqG = Nq * G;
+  const bool tab = uses_table(K);
+  if (tab && (!table || table_bytes < index_fused_table_bytes(B, Nq, Nk, G, Bs, K))) return cudaErrorInvalidValue;
   CUtensorMap tmA, tmB;
   {
     const uint64_t dims[3] = {uint64_t(di), uint64_t(NqG), uint64_t(B)};
@@ -502,8 +752,9 @@ cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t*
   }
   const size_t a_bytes = size_t(kUnitRows) * di * 2, b_bytes = size_t(kTileN) * di * 2;
   const int Kc = K - 1 > 0 ? K - 1 : 1;
-  const size_t lists = size_t(Kc) * kUnitRows * 8;
-  const size_t fixed = 1024 /*alignment slack*/ + lists + 256 /*barriers, flags*/;
+  const size_t lists = tab ? 0 : size_t(Kc) * kUnitRows * 8;
+  const size_t stage = !tab ? 0 : Bs == 32 ? table_stage_bytes<32>() : Bs == 64 ? table_stage_bytes<64>() : table_stage_bytes<128>();
+  const size_t fixed = 1024 /*alignment slack*/ + lists + stage + 256 /*barriers, flags*/;
   const size_t budget = 227 * 1024;
   int nA = 2, S = 8;
   while (S > 2 && fixed + nA * a_bytes + S * b_bytes > budget) --S;
@@ -514,47 +765,77 @@ cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t*
   // barriers must fit in the 256 reserved bytes
   if ((2 * S + 2 * nA + 5) * 8 + 8 > 256) return cudaErrorInvalidValue;
 
-  const int nunits = B * ((NqG + kUnitRows - 1) / kUnitRows);
-  const int grid = nunits < num_sms() ? nunits : num_sms();
-  ProfScope prof("index_fused_tc", stream);
+  const int nrb = (NqG + kUnitRows - 1) / kUnitRows;
+  const int total = B * nrb;
+  const int tstride = table_stride(Nk, Bs);
+  const int chunk = tab ? table_chunk_units(B, Nq, Nk, G, Bs) : total;
+  // the chunk table for TMA stores: (tstride, chunk rows) fp32, boxes of 32
+  // rows x (256 / Bs) blocks (unused by the other forms)
+  CUtensorMap tmT;
+  std::memset(&tmT, 0, sizeof(tmT));
+  if (tab && 256 / Bs * 4 >= 16) {
+    const uint64_t dims[2] = {uint64_t(tstride), uint64_t(chunk) * kUnitRows};
+    const uint64_t strides[1] = {uint64_t(tstride) * 4};
+    const uint32_t box[2] = {uint32_t(256 / Bs), 32};
+    if (!make_tmap_f32(&tmT, table, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+  }
+  const int need = K - 1 - fs;
   // The register split re-allocates exactly the launch allocation: a build
   // that launches with another register count must not run (the increase
   // would wait for registers that are never released).
-#define MSA_FUSED(DI_, BS_, REG_)                                                                               \
+#define MSA_FUSED(DI_, BS_, REG_, TAB_)                                                                         \
   do {                                                                                                          \
-    auto kern = index_fused_tc_kernel<DI_, BS_, REG_>;                                                         \
+    auto kern = index_fused_tc_kernel<DI_, BS_, REG_, TAB_>;                                                   \
     cudaFuncAttributes fa;                                                                                      \
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);                                                           \
     if (e != cudaSuccess) return e;                                                                            \
     if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads) return cudaErrorInvalidConfiguration;  \
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));                    \
     if (e != cudaSuccess) return e;                                                                            \
-    kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, q_offset, kv_len, B, Nq, Nk, G, K, fs, nA, S, sel, status); \
+    ProfScope prof("index_fused_tc", stream);                                                                  \
+    kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, tmT, q_offset, kv_len, Nq, Nk, G, K, fs, nA, S, lo, n,     \
+                                           sel, table, tstride, status);                                      \
   } while (0)
-#define MSA_FUSED_BS(DI_, REG_) \
-  do {                          \
-    if (Bs == 128)              \
-      MSA_FUSED(DI_, 128, REG_); \
-    else if (Bs == 64)          \
-      MSA_FUSED(DI_, 64, REG_);  \
-    else                        \
-      MSA_FUSED(DI_, 32, REG_);  \
+#define MSA_FUSED_BS(DI_, REG_, TAB_)  \
+  do {                                 \
+    if (Bs == 128)                     \
+      MSA_FUSED(DI_, 128, REG_, TAB_); \
+    else if (Bs == 64)                 \
+      MSA_FUSED(DI_, 64, REG_, TAB_);  \
+    else                               \
+      MSA_FUSED(DI_, 32, REG_, TAB_);  \
   } while (0)
-  const bool reg = K - 1 <= kRegList;
-  if (di == 64) {
-    if (reg)
-      MSA_FUSED_BS(64, true);
+  for (int lo = 0; lo < total; lo += chunk) {
+    const int n = std::min(chunk, total - lo);
+    const int grid = n < num_sms() ? n : num_sms();
+    if (di == 64) {
+      if (tab)
+        MSA_FUSED_BS(64, false, true);
+      else
+        MSA_FUSED_BS(64, true, false);
+    } else {
+      if (tab)
+        MSA_FUSED_BS(32, false, true);
+      else
+        MSA_FUSED_BS(32, true, false);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !tab) return e;
+    const int rows = n * kUnitRows;
+    const unsigned sgrid = unsigned((rows + kSelWarps - 1) / kSelWarps);
+    ProfScope prof("index_topk_table", stream);
+    if (need <= 32)
+      index_topk_table_kernel<1><<<sgrid, kSelWarps * 32, 0, stream>>>(table, tstride, lo, rows, nrb, NqG, G, Nq, Nk,
+                                                                       Bs, K, fs, q_offset, kv_len, sel, status);
     else
-      MSA_FUSED_BS(64, false);
-  } else {
-    if (reg)
-      MSA_FUSED_BS(32, true);
-    else
-      MSA_FUSED_BS(32, false);
+      index_topk_table_kernel<2><<<sgrid, kSelWarps * 32, 0, stream>>>(table, tstride, lo, rows, nrb, NqG, G, Nq, Nk,
+                                                                       Bs, K, fs, q_offset, kv_len, sel, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
 #undef MSA_FUSED_BS
 #undef MSA_FUSED
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace msa

@@ -15,7 +15,7 @@ bool dtype_ok(int dtype) { return dtype == MSA_BF16 || dtype == MSA_FP32; }
 // ---- Index Branch planning ---------------------------------------------------
 struct IndexPlan {
   bool ok = false;
-  bool fused = false;  // tcgen05 kernel (no table) when no block_max is requested
+  bool fused = false;  // tcgen05 kernel when no block_max is requested
   msa_status_t err = MSA_ERR_INVALID_ARG;
   size_t table_off = 0, table_bytes = 0;  // table region inside ws (0 if none)
   size_t ws_bytes = 0;
@@ -38,10 +38,12 @@ IndexPlan plan_index(int B, int Nq, int Nk, int G, int di, int Bs, int K, int dt
   // the one-query (decode) path keeps 32-key sub-block maxima instead
   if (decode_index_supported(dtype, B, Nq, G, di, Bs, K)) table = std::max(table, decode_index_ws_bytes(B, G, Nk));
   p.fused = index_fused_supported(dtype, Nq, G, di, Bs, K);
+  // the fused kernel's chunk table (large K only), else the full table
+  if (p.fused) table = index_fused_table_bytes(B, Nq, Nk, G, Bs, K);
   p.table_off = kWsHeader;
-  p.table_bytes = (have_block_max || p.fused) ? 0 : align256(table);
+  p.table_bytes = have_block_max ? 0 : align256(table);
   // size for the call without block_max
-  p.ws_bytes = kWsHeader + (p.fused ? 0 : align256(table));
+  p.ws_bytes = kWsHeader + align256(table);
   p.ok = true;
   p.err = MSA_OK;
   return p;
@@ -190,8 +192,9 @@ extern "C" msa_status_t msa_index_select_v(const void* iq, const void* ik, const
   if (w != MSA_OK) return w;
   uint32_t* status = status_word(ws);
   if (p.fused && !block_max) {
-    return cuda_status(launch_index_fused_tc(iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, K, fs, sel, status,
-                                             stream));
+    float* tab = reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);
+    return cuda_status(launch_index_fused_tc(iq, ik, q_offset, kv_len, B, Nq, Nk, G, di, Bs, K, fs, sel, tab,
+                                             p.table_bytes, status, stream));
   }
   if (!block_max && decode_index_supported(dtype, B, Nq, G, di, Bs, K)) {
     float* tab = reinterpret_cast<float*>(static_cast<char*>(ws) + p.table_off);

@@ -38,15 +38,18 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-// Order-preserving map of a float block maximum and its block id to one
-// unsigned 64-bit key: a larger key means a larger maximum, and among equal
-// maxima the lower block id. -0 is folded onto +0 so that the two compare
-// equal, as they do in floating point.
-__device__ __forceinline__ uint64_t rank_key(float m, int t) {
+// Order-preserving map of a float to an unsigned 32-bit value (a larger float
+// gives a larger value). -0 is folded onto +0 so that the two compare equal,
+// as they do in floating point.
+__device__ __forceinline__ uint32_t ord_f32(float m) {
   uint32_t u = __float_as_uint(m);
   if (u == 0x80000000u) u = 0u;
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (uint64_t(u) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(t));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// A block maximum and its block id as one unsigned 64-bit key: a larger key
+// means a larger maximum, and among equal maxima the lower block id.
+__device__ __forceinline__ uint64_t rank_key(float m, int t) {
+  return (uint64_t(ord_f32(m)) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(t));
 }
 __device__ __forceinline__ int rank_key_block(uint64_t key) { return int(0xFFFFFFFFu - uint32_t(key)); }
 
@@ -147,13 +150,19 @@ msa_status_t index_select_empty_status(int Nk, int G, int di, int Bs, int K, int
 cudaError_t launch_index_blockmax_table(int dtype, const void* iq, const void* ik, const int32_t* q_offset,
                                         const int32_t* kv_len, int B, int Nq, int Nk, int G, int di, int Bs,
                                         float* table, uint32_t* status, cudaStream_t stream);
-// Index Branch, fused tcgen05 path (bf16): scores + block max + top-K in one
-// persistent kernel; no table.
+// Index Branch, fused tcgen05 path (bf16): scores + block max on the tensor
+// cores. For K - 1 <= 15 the top-K runs in the same persistent kernel (no
+// table); for larger K the kernel writes the candidate block maxima of a chunk
+// of rows to a workspace table and a warp-per-row selection kernel follows,
+// chunk after chunk.
 bool index_fused_supported(int dtype, int Nq, int G, int di, int Bs, int K);
-// fs = 1 keeps block 0 as well as the local block (K - 2 blocks ranked)
+// Workspace bytes of the chunk table (0 when the top-K stays in the kernel).
+size_t index_fused_table_bytes(int B, int Nq, int Nk, int G, int Bs, int K);
+// fs = 1 keeps block 0 as well as the local block (K - 2 blocks ranked);
+// table / table_bytes: the chunk table (index_fused_table_bytes of it)
 cudaError_t launch_index_fused_tc(const void* iq, const void* ik, const int32_t* q_offset, const int32_t* kv_len,
                                   int B, int Nq, int Nk, int G, int di, int Bs, int K, int fs, int32_t* sel,
-                                  uint32_t* status, cudaStream_t stream);
+                                  float* table, size_t table_bytes, uint32_t* status, cudaStream_t stream);
 // Exact top-K over a block-max table (warp per row).
 cudaError_t launch_topk_from_table(const float* table, const int32_t* q_offset, const int32_t* kv_len, int B, int Nq,
                                    int Nk, int G, int Bs, int K, int fs, int32_t* sel, uint32_t* status,

@@ -13,8 +13,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 }  // namespace
 
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                    const uint32_t* box, CUtensorMapSwizzle swizzle) {
+namespace {
+bool make_tmap(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -33,10 +34,21 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t
     e[i] = 1;
   }
   for (int i = 0; i + 1 < rank; ++i) s[i] = cuuint64_t(strides[i]);
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void*>(base), d, s, b, e,
+  CUresult r = g_encode(map, dtype, cuuint32_t(rank), const_cast<void*>(base), d, s, b, e,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                    const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box, swizzle);
+}
+
+bool make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                   const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides, box, swizzle);
 }
 
 }  // namespace msa

@@ -55,6 +55,27 @@ def test_workspace_size(lib):
     assert msa.msa_workspace_size(7, 1, 64, 64, 2, 8, 64, 32, 32, 4, 1) == 0
 
 
+def test_index_workspace_holds_the_chunk_table(lib):
+    """Tensor-core index path: the top-K for K - 1 <= 15 stays in the kernel
+    (status header only); larger K needs the block-max table of one chunk of
+    whole 256-row units, rows padded to a multiple of 8 floats, ~4 GiB at most
+    unless that leaves fewer than 608 units (four per SM), never more rows
+    than the call has."""
+    bf16 = msa.MSA_BF16
+    idx = msa.MSA_OP_INDEX_SELECT
+    assert msa.msa_workspace_size(idx, 1, 131072, 131072, 8, 0, 0, 64, 128, 16, bf16) == 256
+    unit = lambda nblk: 256 * ((nblk + 7) // 8 * 8) * 4  # noqa: E731
+    # 128K tokens, Bs 32, K 64: 4096 blocks per row, 1024 units of 4 MiB per 4 GiB chunk
+    assert msa.msa_workspace_size(idx, 1, 131072, 131072, 8, 0, 0, 64, 32, 64, bf16) == 256 + 1024 * unit(4096)
+    # Bs 64, K 32: 2048 units of 2 MiB
+    assert msa.msa_workspace_size(idx, 1, 131072, 131072, 8, 0, 0, 64, 64, 32, bf16) == 256 + 2048 * unit(2048)
+    # a small call: all of its 40 units (10000 x 1 rows, 313 blocks padded to 320)
+    assert msa.msa_workspace_size(idx, 1, 10000, 10000, 1, 0, 0, 32, 32, 20, bf16) == 256 + 40 * unit(313)
+    # 1M tokens at Bs 32: 32768 blocks (32 MiB units) -> the four-per-SM floor, 608 units
+    ws = msa.msa_workspace_size(idx, 1, 1048576, 1048576, 8, 0, 0, 64, 32, 64, bf16)
+    assert ws == 256 + 608 * unit(32768)
+
+
 FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails host validation
 
 
