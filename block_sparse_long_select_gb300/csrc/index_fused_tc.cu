@@ -488,13 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  2. The candidates >= T are compacted in ascending t into the warp's list
 //     (a second pass over the row, from L2).
 //  3. v* by bisection over the list's order-preserving 32-bit values (two bits
-//     per round, starting below the bits that T and the row maximum share;
-//     the three counts of a round are summed as one packed word), then every
-//     value above v* and the lowest-t values equal to v*, compacted in list
-//     order.
+//     per round, starting below the bits that T and the list maximum share;
+//     the three counts of a round are summed as one packed word) until the
+//     bucket holding v* has at most 32 values, which are then ranked among
+//     themselves by shuffles; then every value above v* and the lowest-t
+//     values equal to v*, compacted in list order.
 // The two passes compare floats (the order of the 32-bit values, with -0 and
-// +0 equal); only listed candidates are converted. A list that would
-// overflow (many values tied at T) bisects over the row itself instead.
+// +0 equal); only listed candidates are converted. A list that overflows
+// gives a tighter bound (the need-th largest of its kSelCap entries) and the
+// compaction runs again; ties at the bound that make no progress bisect over
+// the row itself.
 // NS = 1 serves need <= 32, NS = 2 need <= 64.
 // ---------------------------------------------------------------------------
 constexpr int kSelWarps = 8;
@@ -576,60 +579,128 @@ __global__ void __launch_bounds__(kSelWarps * 32) index_topk_table_kernel(
   }
   uint32_t mine = c0 >= need ? ord_f32(s0) : 0u;
   if constexpr (NS == 2) mine = max(mine, c1 >= need ? ord_f32(s1) : 0u);
-  const uint32_t T = max(__reduce_max_sync(0xffffffffu, mine), 1u);
+  uint32_t T = max(__reduce_max_sync(0xffffffffu, mine), 1u);
   const uint32_t hi = __reduce_max_sync(0xffffffffu, max(ord_f32(s0), 1u));  // the row maximum
-  const float Tf = ord_inv(T);
-  // 2. candidates >= T in ascending t
+  // 2. candidates >= T in ascending t (a list of the first kSelCap; C counts all)
   uint32_t* lv = list_v[warp];
   int* ltb = list_t[warp];
   int C = 0;
-  for (int t0 = fs; t0 < loc; t0 += 32 * kSelBatch) {
-    float v[kSelBatch];
+  auto compact = [&](float Tf) {
+    C = 0;
+    for (int t0 = fs; t0 < loc; t0 += 32 * kSelBatch) {
+      float v[kSelBatch];
 #pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {
-      const int t = t0 + 32 * u + lane;
-      v[u] = t < loc ? __ldg(M + t) : -INFINITY;
-    }
+      for (int u = 0; u < kSelBatch; ++u) {
+        const int t = t0 + 32 * u + lane;
+        v[u] = t < loc ? __ldg(M + t) : -INFINITY;
+      }
 #pragma unroll
-    for (int u = 0; u < kSelBatch; ++u) {  // ascending t: batch by batch, then lane by lane
-      const bool f = v[u] >= Tf;
-      const unsigned fm = __ballot_sync(0xffffffffu, f);
-      if (fm) {
-        if (f) {
-          const int q = C + __popc(fm & lt);
-          if (q < kSelCap) {
-            lv[q] = max(ord_f32(v[u]), 1u);
-            ltb[q] = t0 + 32 * u + lane;
+      for (int u = 0; u < kSelBatch; ++u) {  // ascending t: batch by batch, then lane by lane
+        const bool f = v[u] >= Tf;
+        const unsigned fm = __ballot_sync(0xffffffffu, f);
+        if (fm) {
+          if (f) {
+            const int q = C + __popc(fm & lt);
+            if (q < kSelCap) {  // the float's bits; converted when loaded below
+              lv[q] = __float_as_uint(v[u]);
+              ltb[q] = t0 + 32 * u + lane;
+            }
           }
+          C += __popc(fm);
         }
-        C += __popc(fm);
       }
     }
-  }
-  __syncwarp();
-  // 3. v*: the largest value with at least `need` values >= it
-  const bool listed = C <= kSelCap;
+    __syncwarp();
+  };
   constexpr int kPerLane = kSelCap / 32;
-  uint32_t e[kPerLane];
+  uint32_t e[kPerLane];  // list entry lane + 32 k, order-preserving (0 past the list)
+  auto load_list = [&](int n) {
 #pragma unroll
-  for (int k = 0; k < kPerLane; ++k) {
-    const int i = lane + 32 * k;
-    e[k] = (listed && i < C) ? lv[i] : 0u;
-  }
-  const uint32_t diff = T ^ hi;
-  const int nb = diff ? ((32 - __clz(int(diff))) + 1) & ~1 : 0;  // low bits to resolve (even)
-  uint32_t v = nb >= 32 ? 0u : (T & ~((1u << nb) - 1u));
-  for (int sh = nb - 2; sh >= 0; sh -= 2) {
-    const uint32_t c1v = v | (1u << sh), c2v = v | (2u << sh), c3v = v | (3u << sh);
-    int n1, n2, n3;
-    if (listed) {  // counts of at most kSelCap in 10-bit fields of one word
-      uint32_t n = 0;
+    for (int k = 0; k < kPerLane; ++k) {
+      const int i = lane + 32 * k;
+      e[k] = i < n ? max(ord_f32(__uint_as_float(lv[i])), 1u) : 0u;
+    }
+  };
+  // The need-th largest of the n list values (all >= lo, n >= need): bisection
+  // (two bits per round, from below the bits that lo and the list maximum
+  // share; the three counts of a round summed as one packed word) while the
+  // bucket [v, v + 2^w) holding it has more than 32 values, then those values
+  // ranked among themselves. ge = values >= v, above = values >= v + 2^w.
+  auto list_kth = [&](int n, uint32_t lo) -> uint32_t {
+    uint32_t hl = 0;
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) hl = max(hl, e[k]);
+    hl = __reduce_max_sync(0xffffffffu, hl);
+    const uint32_t diff = lo ^ hl;
+    int w = diff ? ((32 - __clz(int(diff))) + 1) & ~1 : 0;  // low bits to resolve (even)
+    uint32_t v = w >= 32 ? 0u : (lo & ~((1u << w) - 1u));
+    int ge = n, above = 0;
+    while (w > 0 && ge - above > 32) {
+      const int sh = w - 2;
+      const uint32_t c1v = v | (1u << sh), c2v = v | (2u << sh), c3v = v | (3u << sh);
+      uint32_t cnt = 0;  // counts of at most kSelCap in 10-bit fields
 #pragma unroll
       for (int k = 0; k < kPerLane; ++k)
-        if (32 * k < C) n += uint32_t(e[k] >= c1v) + (uint32_t(e[k] >= c2v) << 10) + (uint32_t(e[k] >= c3v) << 20);
-      n = __reduce_add_sync(0xffffffffu, n);
-      n1 = int(n & 1023u), n2 = int((n >> 10) & 1023u), n3 = int(n >> 20);
-    } else {
+        if (32 * k < n) cnt += uint32_t(e[k] >= c1v) + (uint32_t(e[k] >= c2v) << 10) + (uint32_t(e[k] >= c3v) << 20);
+      cnt = __reduce_add_sync(0xffffffffu, cnt);
+      const int n1 = int(cnt & 1023u), n2 = int((cnt >> 10) & 1023u), n3 = int(cnt >> 20);
+      const uint32_t best = n3 >= need ? 3u : (n2 >= need ? 2u : (n1 >= need ? 1u : 0u));
+      above = best == 3u ? above : (best == 2u ? n3 : (best == 1u ? n2 : n1));
+      ge = best == 3u ? n3 : (best == 2u ? n2 : (best == 1u ? n1 : ge));
+      v |= best << sh;
+      w = sh;
+    }
+    if (w == 0) return v;
+    const uint64_t vend = uint64_t(v) + (uint64_t(1) << w);
+    int nbk = 0;
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) {
+      if (32 * k >= n) break;
+      const bool in = e[k] >= v && uint64_t(e[k]) < vend;
+      const unsigned im = __ballot_sync(0xffffffffu, in);
+      if (in) lv[nbk + __popc(im & lt)] = e[k];  // the list's float bits are in e[] by now
+      nbk += __popc(im);
+    }
+    __syncwarp();
+    const uint32_t x = lane < nbk ? lv[lane] : 0u;
+    int cgt = 0, cge = 0;
+#pragma unroll 8
+    for (int o = 0; o < 32; ++o) {
+      const uint32_t y = __shfl_sync(0xffffffffu, x, o);
+      const bool real = o < nbk;
+      cgt += real && y > x;
+      cge += real && y >= x;
+    }
+    const int m = need - above;  // v* is the m-th largest bucket value
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < nbk && cgt < m && cge >= m);
+    const uint32_t r = __shfl_sync(0xffffffffu, x, __ffs(hit) - 1);
+    __syncwarp();
+    return r;
+  };
+  // 3. A list that overflows still holds kSelCap candidates: their need-th
+  // largest value is a tighter bound, and the compaction runs again. Ties at
+  // the bound that make no progress bisect over the row itself.
+  bool listed = false;
+  for (int attempt = 0; attempt < 3; ++attempt) {
+    compact(ord_inv(T));
+    load_list(min(C, kSelCap));
+    if (C <= kSelCap) {
+      listed = true;
+      break;
+    }
+    const uint32_t T2 = list_kth(kSelCap, T);
+    if (T2 <= T) break;
+    T = T2;
+  }
+  uint32_t v;
+  if (listed) {
+    v = list_kth(C, T);
+  } else {
+    const uint32_t diff = T ^ hi;
+    const int nb = diff ? ((32 - __clz(int(diff))) + 1) & ~1 : 0;
+    v = nb >= 32 ? 0u : (T & ~((1u << nb) - 1u));
+    for (int sh = nb - 2; sh >= 0; sh -= 2) {
+      const uint32_t c1v = v | (1u << sh), c2v = v | (2u << sh), c3v = v | (3u << sh);
       int a1 = 0, a2 = 0, a3 = 0;
       for (int t = fs + lane; t < loc; t += 32) {
         const uint32_t x = cand_value(M, t);
@@ -637,12 +708,12 @@ __global__ void __launch_bounds__(kSelWarps * 32) index_topk_table_kernel(
         a2 += x >= c2v;
         a3 += x >= c3v;
       }
-      n1 = __reduce_add_sync(0xffffffffu, a1);
-      n2 = __reduce_add_sync(0xffffffffu, a2);
-      n3 = __reduce_add_sync(0xffffffffu, a3);
+      const int n1 = __reduce_add_sync(0xffffffffu, a1);
+      const int n2 = __reduce_add_sync(0xffffffffu, a2);
+      const int n3 = __reduce_add_sync(0xffffffffu, a3);
+      const uint32_t best = n3 >= need ? 3u : (n2 >= need ? 2u : (n1 >= need ? 1u : 0u));
+      v |= best << sh;
     }
-    const uint32_t best = n3 >= need ? 3u : (n2 >= need ? 2u : (n1 >= need ? 1u : 0u));
-    v |= best << sh;
   }
   // everything above v*, then the lowest-t values equal to v*
   int gt = 0;
