@@ -226,7 +226,7 @@ def msa_index_select_dev(t, w, qo, kl):
 # forced sequence-start variant (block 0 kept with the local block), one case per top-K implementation
 FORCE_START_PREFILL = {
     "fused_registers": synth.scaled(BASE, B=1, Nq=1500, Nk=1500, Bs=64, K=8),
-    "fused_heap": synth.scaled(BASE, B=1, Nq=1200, Nk=1200, Bs=32, K=20),
+    "fused_table": synth.scaled(BASE, B=1, Nq=1200, Nk=1200, Bs=32, K=20),
     "fused_k2_nothing_ranked": synth.scaled(BASE, B=1, Nq=800, Nk=800, Bs=32, K=2),
     "table_fp32": synth.WORKLOADS["tiny_fp32"],
 }
