@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kKSteps = DI / 16;
   constexpr int kChunk = 128;  // TMEM columns read per epilogue step (one load round)
   constexpr uint32_t kIdesc = tc::idesc_bf16_f32(128, kTileN);
+  constexpr uint32_t kDescHi = tc::smem_desc_hi(kSbo, kSwz);  // the descriptors' constant high word
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
@@ -249,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ++jA;
-        const uint32_t a_addr = tc::smem_u32(a_buf + size_t(x) * kABytes);
+        // descriptor low words (start address, leading offset): one add per operand and MMA
+        const uint32_t a_lo = tc::smem_desc_lo(tc::smem_u32(a_buf + size_t(x) * kABytes), 16);
         for (int n = 0; n < U.nt; ++n, ++kB, ++kAcc) {
           const int s = kB % S;
           if (!tc::mbar_wait(&full[s], (kB / S) & 1, abort_flag)) {
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             alive = false;
             break;
           }
-          const uint32_t b_addr = tc::smem_u32(b_buf + size_t(s) * kBBytes);
+          const uint32_t b_lo = tc::smem_desc_lo(tc::smem_u32(b_buf + size_t(s) * kBBytes), 16);
           // ping-pong: tile m's accumulator is drained by warpgroup m while the
           // tensor core works on the other tile
 #pragma unroll
@@ -270,11 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             const uint32_t d = tmem + uint32_t(m * kTileN);
 #pragma unroll
-            for (int kk = 0; kk < kKSteps; ++kk) {
-              const uint64_t ad = tc::smem_desc(a_addr + m * kATile + kk * 32, 16, kSbo, kSwz);
-              const uint64_t bd = tc::smem_desc(b_addr + kk * 32, 16, kSbo, kSwz);
-              tc::mma_f16_ss(d, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kKSteps; ++kk)
+              tc::mma_f16_ss_lo<kDescHi>(d, a_lo + ((m * kATile + kk * 32) >> 4), b_lo + ((kk * 32) >> 4), kIdesc,
+                                         kk > 0 ? 1u : 0u);
             tc::mma_commit(&acc_full[m]);
           }
           if (!alive) break;
