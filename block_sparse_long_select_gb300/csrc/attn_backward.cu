@@ -746,6 +746,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int kv_uses = 0, nbins = 0, prev_bin = -1;
       const uint32_t ka = tc::smem_u32(k_buf), va = tc::smem_u32(v_buf), dsa = tc::smem_u32(ds_buf);
+      // Descriptors from 32-bit low words (start address, leading offset) with
+      // one constant high word (8-row groups 1024 B apart, 128B swizzle): one
+      // add per operand and MMA instead of building two 64-bit descriptors
+      constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, 2);
+      const uint32_t ka16 = tc::smem_desc_lo(ka, 16), va16 = tc::smem_desc_lo(va, 16);
+      const uint32_t kaH = tc::smem_desc_lo(ka, SM::kHalf), dsaH = tc::smem_desc_lo(dsa, SM::kHalf);
       int bin_n = n > 0 ? p.tiles[z0].x : -1;
       for (int z = 0; z < n; ++z) {
         const int slot = z & 1;
@@ -767,20 +773,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_after_sync();
         const uint32_t qa = tc::smem_u32(ring + slot * SM::kSlot), oa = qa + SM::kRowsT;
+        const uint32_t qa16 = tc::smem_desc_lo(qa, 16), oa16 = tc::smem_desc_lo(oa, 16);
+        const uint32_t qaL = tc::smem_desc_lo(qa, kBwdRows * 128), oaL = tc::smem_desc_lo(oa, kBwdRows * 128);
         // S^T = K Q^T, dP^T = V dO^T (both operands K-major along d)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          const uint64_t kd = tc::smem_desc(ka + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
-          const uint64_t qd = tc::smem_desc(qa + (kk >> 2) * (kBwdRows * 128) + off, 16, 1024, 2);
-          tc::mma_f16_ss(tmem, kd, qd, kIdS, kk > 0 ? 1u : 0u);
+          tc::mma_f16_ss_lo<kDescHi>(tmem, ka16 + (((kk >> 2) * SM::kHalf + off) >> 4),
+                                     qa16 + (((kk >> 2) * (kBwdRows * 128) + off) >> 4), kIdS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk & 3) * 32;
-          const uint64_t vd = tc::smem_desc(va + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
-          const uint64_t od = tc::smem_desc(oa + (kk >> 2) * (kBwdRows * 128) + off, 16, 1024, 2);
-          tc::mma_f16_ss(tmem + 128u, vd, od, kIdS, kk > 0 ? 1u : 0u);
+          tc::mma_f16_ss_lo<kDescHi>(tmem + 128u, va16 + (((kk >> 2) * SM::kHalf + off) >> 4),
+                                     oa16 + (((kk >> 2) * (kBwdRows * 128) + off) >> 4), kIdS, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(s_full);
         if (!tc::mbar_wait(p_full, z & 1, abort_flag) ||
@@ -791,24 +797,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_after_sync();
         // dV += P^T dO, dK += dS^T Q: A from TMEM (16 rows = 8 packed columns per step), B MN-major
 #pragma unroll
-        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
-          const uint64_t od = tc::smem_desc(oa + kk * 16 * 128, kBwdRows * 128, 1024, 2);
-          tc::mma_f16_ts(tmem + kColDv, tmem + uint32_t(kk) * 8u, od, kIdKV, (first && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < kBwdRows / 16; ++kk)
+          tc::mma_f16_ts_lo<kDescHi>(tmem + kColDv, tmem + uint32_t(kk) * 8u, oaL + ((kk * 16 * 128) >> 4), kIdKV,
+                                     (first && kk == 0) ? 0u : 1u);
 #pragma unroll
-        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
-          const uint64_t qd = tc::smem_desc(qa + kk * 16 * 128, kBwdRows * 128, 1024, 2);
-          tc::mma_f16_ts(tmem + kColDk, tmem + 128u + uint32_t(kk) * 8u, qd, kIdKV, (first && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < kBwdRows / 16; ++kk)
+          tc::mma_f16_ts_lo<kDescHi>(tmem + kColDk, tmem + 128u + uint32_t(kk) * 8u, qaL + ((kk * 16 * 128) >> 4),
+                                     kIdKV, (first && kk == 0) ? 0u : 1u);
         // dQ = dS K, one 64-column half of d at a time (A = dS MN-major over the tile rows)
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
 #pragma unroll
-          for (int kk = 0; kk < kTcBs / 16; ++kk) {
-            const uint64_t sd = tc::smem_desc(dsa + kk * 16 * 128, SM::kHalf, 1024, 2);
-            const uint64_t kd = tc::smem_desc(ka + h * SM::kHalf + kk * 16 * 128, SM::kHalf, 1024, 2);
-            tc::mma_f16_ss(tmem + (h == 0 ? 64u : 192u), sd, kd, kIdQ, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kTcBs / 16; ++kk)
+            tc::mma_f16_ss_lo<kDescHi>(tmem + (h == 0 ? 64u : 192u), dsaH + ((kk * 16 * 128) >> 4),
+                                       kaH + ((h * SM::kHalf + kk * 16 * 128) >> 4), kIdQ, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(dq_full);
         tc::mma_commit(&q_empty[slot]);

@@ -425,6 +425,10 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
     if (lane == 0) {
       int kv_uses = 0, prev_bin = -1;
       const uint32_t ka = tc::smem_u32(k_buf), ika = tc::smem_u32(ik_buf);
+      // descriptors from 32-bit low words with one constant high word (8-row
+      // groups 1024 B apart, 128B swizzle): one add per operand and MMA
+      constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, 2);
+      const uint32_t ka16 = tc::smem_desc_lo(ka, 16), ika16 = tc::smem_desc_lo(ika, 16);
       int bin_n = n > 0 ? p.tiles[z0].x : -1;
       for (int z = 0; z < n; ++z) {
         const int set = z % NS, slot = set, ph = (z / NS) & 1;
@@ -446,20 +450,17 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
         }
         tc::fence_after_sync();
         const uint32_t qa = tc::smem_u32(ring + slot * SM::kSlot), iqa = qa + SM::kQ;
+        const uint32_t qa16 = tc::smem_desc_lo(qa, 16), iqa16 = tc::smem_desc_lo(iqa, 16);
         const uint32_t d_s = tmem + uint32_t(set) * kSet;
 #pragma unroll
         for (int kk = 0; kk < kKtD / 16; ++kk) {  // S^T = K q^T
-          const uint32_t off = (kk & 3) * 32;
-          const uint64_t kd = tc::smem_desc(ka + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
-          const uint64_t qd = tc::smem_desc(qa + (kk >> 2) * SM::kHalf + off, 16, 1024, 2);
-          tc::mma_f16_ss(d_s, kd, qd, kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * SM::kHalf + (kk & 3) * 32) >> 4;
+          tc::mma_f16_ss_lo<kDescHi>(d_s, ka16 + off, qa16 + off, kIdS, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < kKtDI / 16; ++kk) {  // I^T = IK iq^T
-          const uint32_t off = kk * 32;
-          const uint64_t kd = tc::smem_desc(ika + off, 16, 1024, 2);
-          const uint64_t qd = tc::smem_desc(iqa + off, 16, 1024, 2);
-          tc::mma_f16_ss(d_s + 128u, kd, qd, kIdI, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk * 32) >> 4;
+          tc::mma_f16_ss_lo<kDescHi>(d_s + 128u, ika16 + off, iqa16 + off, kIdI, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(&s_full[set]);
         tc::mma_commit(&q_empty[slot]);
