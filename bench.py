@@ -815,6 +815,21 @@ def cpu_baseline(w, rows_n, full_legs=True):
         full[wd.name] = {"value": round(wd.B / sec, 2), "unit": "tokens/s", "seconds": round(sec, 3), "rows": wd.B,
                          "what": "every sequence's new token, index select over its cache + attention"}
         res["full"] = full
+        # sampled rows of the other prefill workloads (the block-size sweep
+        # and 1M tokens): evenly spaced rows, so rows / seconds estimates the
+        # oracle's tokens/s over the whole sequence
+        sampled = {}
+        for name, n in (("prefill_128k_bs64", 512), ("prefill_128k_bs32", 512), ("prefill_1m", 16)):
+            wl = synth.WORKLOADS[name]
+            ikl = synth.host_tensor(wl, "ik")
+            rl = sample_rows(wl, n)
+            sec = oracle_prefill_rows(wl, rl, ikl)
+            del ikl
+            sampled[name] = {"value": round(len(rl) / sec, 2), "unit": "tokens/s", "seconds": round(sec, 3),
+                             "rows": len(rl), "what": f"{len(rl)} query rows evenly spaced over {wl.Nq} tokens, "
+                                                      "index select + attention"}
+        _KV_HOST.clear()
+        res["sampled"] = sampled
     return res
 
 
