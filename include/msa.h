@@ -110,6 +110,13 @@ size_t msa_workspace_size(int op, int B, int Nq, int Nk, int G, int Hq, int d, i
  *            0..loc and is padded with -1.
  *  block_max [B, Nq, G, ceil(Nk/Bs)] fp32 or NULL, out (diagnostic): the
  *            block maxima of the visible keys, NaN for blocks t > loc.
+ *  ws        msa_workspace_size(MSA_OP_INDEX_SELECT, ...) bytes. For bf16
+ *            prefill on the tensor cores it is the 256-byte status header
+ *            when K <= 16; for K > 16 it also holds the block-max table of
+ *            one chunk of rows (whole units of 256 (row, group) rows, about
+ *            4 GiB at most unless that leaves fewer than 608 units;
+ *            MSA_INDEX_TABLE_UNITS in the environment, read once per process,
+ *            sets the units per chunk, and the size follows it).
  *  Supported: dtype BF16 or FP32; di in {32, 64}; 1 <= Bs <= 1024; 1 <= K <= 64.
  *  Selection is exact when the index scores are exact in fp32 (for example
  *  integer-valued index q/k with |score| < 2^24). */
