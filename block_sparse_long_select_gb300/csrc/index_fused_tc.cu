@@ -566,20 +566,40 @@ __global__ void __launch_bounds__(kSelWarps * 32) index_topk_table_kernel(
       }
     }
   }
-  int c0 = 0, c1 = 0;
-#pragma unroll 8
-  for (int o = 0; o < 32; ++o) {
-    const float x0 = __shfl_sync(0xffffffffu, s0, o);
-    c0 += x0 >= s0;
-    if constexpr (NS == 2) {
-      const float x1 = __shfl_sync(0xffffffffu, s1, o);
-      c0 += x1 >= s0;
-      c1 += (x0 >= s1) + (x1 >= s1);
+  // T is the (32 NS - need + 1)-th smallest sample value. When that is one
+  // of the few smallest, take it by repeated minimum extraction (a lane's
+  // values are in ascending order: lo, then hi2); otherwise rank the sample
+  // values by shuffles.
+  uint32_t T;
+  const int below = 32 * NS - need;  // sample values below T in the sorted order
+  if (below <= 3) {
+    uint32_t lo = ord_f32(NS == 1 ? s0 : s1), hi2 = NS == 1 ? 0xFFFFFFFFu : ord_f32(s0);
+    for (int x = 0; x < below; ++x) {
+      const uint32_t m = __reduce_min_sync(0xffffffffu, lo);
+      const unsigned who = __ballot_sync(0xffffffffu, lo == m);
+      if (lane == __ffs(who) - 1) {
+        lo = hi2;
+        hi2 = 0xFFFFFFFFu;
+      }
     }
+    T = __reduce_min_sync(0xffffffffu, lo);
+  } else {
+    int c0 = 0, c1 = 0;
+#pragma unroll 8
+    for (int o = 0; o < 32; ++o) {
+      const float x0 = __shfl_sync(0xffffffffu, s0, o);
+      c0 += x0 >= s0;
+      if constexpr (NS == 2) {
+        const float x1 = __shfl_sync(0xffffffffu, s1, o);
+        c0 += x1 >= s0;
+        c1 += (x0 >= s1) + (x1 >= s1);
+      }
+    }
+    uint32_t mine = c0 >= need ? ord_f32(s0) : 0u;
+    if constexpr (NS == 2) mine = max(mine, c1 >= need ? ord_f32(s1) : 0u);
+    T = __reduce_max_sync(0xffffffffu, mine);
   }
-  uint32_t mine = c0 >= need ? ord_f32(s0) : 0u;
-  if constexpr (NS == 2) mine = max(mine, c1 >= need ? ord_f32(s1) : 0u);
-  uint32_t T = max(__reduce_max_sync(0xffffffffu, mine), 1u);
+  T = max(T, 1u);
   const uint32_t hi = __reduce_max_sync(0xffffffffu, max(ord_f32(s0), 1u));  // the row maximum
   // 2. candidates >= T in ascending t (a list of the first kSelCap; C counts all)
   uint32_t* lv = list_v[warp];
