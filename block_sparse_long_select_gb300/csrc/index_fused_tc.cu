@@ -682,18 +682,20 @@ __global__ void __launch_bounds__(kSelWarps * 32) index_topk_table_kernel(
       nbk += __popc(im);
     }
     __syncwarp();
-    const uint32_t x = lane < nbk ? lv[lane] : 0u;
-    int cgt = 0, cge = 0;
-#pragma unroll 8
-    for (int o = 0; o < 32; ++o) {
-      const uint32_t y = __shfl_sync(0xffffffffu, x, o);
-      const bool real = o < nbk;
-      cgt += real && y > x;
-      cge += real && y >= x;
+    // v* is the m-th largest bucket value: a descending bitonic sort across
+    // the lanes (lanes past the bucket hold 0, below every value), then lane m - 1
+    uint32_t x = lane < nbk ? lv[lane] : 0u;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+        x = keep_max ? max(x, y) : min(x, y);
+      }
     }
-    const int m = need - above;  // v* is the m-th largest bucket value
-    const unsigned hit = __ballot_sync(0xffffffffu, lane < nbk && cgt < m && cge >= m);
-    const uint32_t r = __shfl_sync(0xffffffffu, x, __ffs(hit) - 1);
+    const int m = need - above;
+    const uint32_t r = __shfl_sync(0xffffffffu, x, m - 1);
     __syncwarp();
     return r;
   };
