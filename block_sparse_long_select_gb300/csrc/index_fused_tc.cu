@@ -21,14 +21,15 @@
 // of (Nq*G) x Nk per sequence serves every group (the index key is shared by
 // all groups). A work unit is 256 stacked rows (two 128-row MMA tiles that
 // share each key tile, which halves the key traffic per flop); it sweeps key
-// tiles of 128 keys over the blocks before its local block. Units are handed
+// tiles of 256 keys over the blocks before its local block. Units are handed
 // out in a static serpentine order, longest first, over a persistent grid of
 // one CTA per SM.
 //
 // Warp roles (384 threads): warps 0-7 epilogue (warpgroup m reads TMEM lanes
 // of MMA tile m), warp 8 TMA producer, warp 9 TMEM owner + MMA issuer.
 // Pipelines: key tiles in an S-stage shared-memory ring; index-query tiles in
-// nA buffers; two TMEM accumulator sets of 2 x 128 columns (512 columns).
+// nA buffers; two TMEM accumulators of 256 columns (one per 128-row MMA tile,
+// 512 columns), drained by their warpgroups in turn.
 // Every wait is bounded; on expiry the kernel records MSA_ERR_TIMEOUT, stops
 // issuing work, drains its copies and MMAs, frees TMEM and returns.
 #include <algorithm>
@@ -484,15 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 //     Among those 32 NS sample values, T = the largest one with at least
 //     `need` sample values >= T: then at least `need` candidates are >= T, so
 //     the need-th largest candidate v* is >= T, and only candidates >= T can
-//     be chosen.
+//     be chosen. (T is the sample's (32 NS - need + 1)-th smallest value:
+//     found by repeated minimum extraction when that is one of the four
+//     smallest, else by ranking the sample with shuffles.)
 //  2. The candidates >= T are compacted in ascending t into the warp's list
 //     (a second pass over the row, from L2).
 //  3. v* by bisection over the list's order-preserving 32-bit values (two bits
 //     per round, starting below the bits that T and the list maximum share;
 //     the three counts of a round are summed as one packed word) until the
-//     bucket holding v* has at most 32 values, which are then ranked among
-//     themselves by shuffles; then every value above v* and the lowest-t
-//     values equal to v*, compacted in list order.
+//     bucket holding v* has at most 32 values, which a warp bitonic sort
+//     puts in order; then every value above v* and the lowest-t values equal
+//     to v*, compacted in list order.
 // The two passes compare floats (the order of the 32-bit values, with -0 and
 // +0 equal); only listed candidates are converted. A list that overflows
 // gives a tighter bound (the need-th largest of its kSelCap entries) and the
