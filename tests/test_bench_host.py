@@ -55,6 +55,14 @@ def test_prefill_and_decode_work_counts():
     assert work["attended_keys"] == att
     assert work["attn_flops"] == 4.0 * w.d * (w.Hq // w.G) * att
     assert bench.kl_work(w, work)["kl_flops"] == 2.0 * w.d * (w.Hq // w.G) * att + 2.0 * w.di * att
+    # top-K over a block-max table: rows with more than K visible blocks read
+    # their loc candidate maxima (blocks t < loc), every row writes K ids
+    cand = 0
+    for b in range(w.B):
+        for i in range(w.Nq):
+            loc = (int(qo[b]) + i) // w.Bs
+            cand += loc if loc + 1 > w.K else 0
+    assert work["topk_bytes"] == 4.0 * w.G * cand + 4.0 * w.K * w.G * w.B * w.Nq
     assert bench.backward_work(w, work)["bwd_flops"] == 10.0 * w.d * (w.Hq // w.G) * att
 
     wd = synth.scaled(synth.WORKLOADS["decode_b64"], B=2, Nk=40, Hq=8, Hkv=2, d=64, di=32, Bs=8, K=2)
@@ -85,6 +93,10 @@ def test_roofline_arithmetic():
                            "decode")
     assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(6.0e8 / 1.0e-4 / 1e9, abs=0.01)
     assert bench.roofline_for("attn_invert", {"attn_invert": (1, 1.0)}, work, peaks, "m", "w", 1) is None
+    # the large-K selection pass: table bytes over time against the copy bandwidth
+    r = bench.roofline_for("index_topk_table", {"index_topk_table": (4, 2.0)}, dict(work, topk_bytes=8.0e9), peaks,
+                           "measured", "nowhere", 1)
+    assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(8.0e9 / 4 / 0.5e-3 / 1e9, abs=0.01)
 
 
 def test_ncu_traffic_needs_the_current_source(tmp_path, monkeypatch):
