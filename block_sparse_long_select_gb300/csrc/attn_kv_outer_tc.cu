@@ -87,7 +87,7 @@ __device__ __forceinline__ bool entry_valid(int t, int pos, int Bs, int nblk) {
 __global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
                                   const int32_t* __restrict__ kv_len, int b, int Nq, int Nk, int G, int K, int Bs,
                                   int nblk, int c0, int cq, int rows_per_cta, int* __restrict__ cnt,
-                                  uint32_t* status) {
+                                  int* __restrict__ hist_g, uint32_t* status) {
   extern __shared__ int hist[];
   const int g = blockIdx.y;
   for (int t = threadIdx.x; t < nblk; t += blockDim.x) hist[t] = 0;
@@ -105,8 +105,12 @@ __global__ void attn_count_kernel(const int32_t* __restrict__ sel, const int32_t
     }
   }
   __syncthreads();
-  for (int t = threadIdx.x; t < nblk; t += blockDim.x)
+  // the CTA's histogram is kept for attn_fill (same CTA decomposition)
+  int* keep = hist_g + (int64_t(g) * gridDim.x + blockIdx.x) * nblk;
+  for (int t = threadIdx.x; t < nblk; t += blockDim.x) {
+    keep[t] = hist[t];
     if (hist[t]) atomicAdd(&cnt[g * nblk + t], hist[t]);
+  }
 }
 
 // Relative cost of a tile pass's work: a tile, the first tile of a bin (its
@@ -241,26 +245,19 @@ __global__ void attn_tiles_kernel(const int* __restrict__ cnt, const int* __rest
 __global__ void attn_fill_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ q_offset,
                                  const int32_t* __restrict__ kv_len, int b, int Nq, int Nk, int G, int K, int Bs,
                                  int nblk, int c0, int cq, int rows_per_cta, const int* __restrict__ entry_off,
-                                 int* __restrict__ cursor, int* __restrict__ entries, int* __restrict__ rev) {
+                                 const int* __restrict__ hist_g, int* __restrict__ cursor, int* __restrict__ entries,
+                                 int* __restrict__ rev) {
   extern __shared__ int sm[];
   int* hist = sm;
   int* base = sm + nblk;
   const int g = blockIdx.y;
-  for (int t = threadIdx.x; t < nblk; t += blockDim.x) hist[t] = 0;
-  __syncthreads();
   const SeqView sv = seq_view(q_offset, kv_len, b, Nq, Nk, false);
   const int r0 = blockIdx.x * rows_per_cta;
   const int r1 = min(cq, r0 + rows_per_cta);
-  if (sv.ok) {
-    for (int e = threadIdx.x; e < (r1 - r0) * K; e += blockDim.x) {
-      const int il = r0 + e / K, k = e % K;
-      const int t = sel[((int64_t(b) * Nq + c0 + il) * G + g) * K + k];
-      if (entry_valid(t, sv.q0 + c0 + il, Bs, nblk)) atomicAdd(&hist[t], 1);
-    }
-  }
-  __syncthreads();
+  // this CTA's range of every bin, from the histogram attn_count kept
+  const int* keep = hist_g + (int64_t(g) * gridDim.x + blockIdx.x) * nblk;
   for (int t = threadIdx.x; t < nblk; t += blockDim.x) {
-    const int h = hist[t];
+    const int h = keep[t];
     base[t] = h ? entry_off[g * nblk + t] + atomicAdd(&cursor[g * nblk + t], h) : 0;
     hist[t] = 0;
   }
@@ -1778,6 +1775,7 @@ int sm_count() {
 }
 
 static inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr int kInvRows = 1024;  // query rows per inversion CTA (one group each)
 
 int chunk_tokens(int Nq, int Hq, int K, int d) {
   static int env = -1;
@@ -1826,6 +1824,8 @@ KvoLayout kvo_layout(int Nq, int Hq, int G, int d, int Bs, int K, int Nk) {
   o += a256(size_t(kMaxGrid + 1) * 4);
   L.cta_seg = o;
   o += a256(size_t(kKvoMaxPhases) * (kMaxGrid + 1) * 4);
+  L.hist = o;  // [G][count CTAs][nblk]: each inversion CTA's histogram
+  o += a256(size_t(G) * ((cq + kInvRows - 1) / kInvRows) * nblk * 4);
   L.max_tiles = max_tiles;
   L.entries = o;
   o += a256(max_tiles * per_tile * 4);  // bins padded to whole tiles
@@ -1863,7 +1863,7 @@ static size_t attn_smem_bytes(int d, int Bs) { return Bs == 128 ? attn1_smem_byt
 cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int32_t* kv_len, int b, int Nq, int Nk,
                          int G, int K, int Bs, int per_tile, int c0, int cq, int grid, char* w, const KvoLayout& L,
                          uint32_t* status, cudaStream_t stream) {
-  const int nblk = (Nk + Bs - 1) / Bs, nbins = G * nblk, rows_per_cta = 1024;
+  const int nblk = (Nk + Bs - 1) / Bs, nbins = G * nblk, rows_per_cta = kInvRows;
   const size_t hist_smem = size_t(nblk) * 4 * 2;
   if (hist_smem > 200 * 1024) return cudaErrorInvalidValue;
   cudaError_t e;
@@ -1877,8 +1877,9 @@ cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int3
   const dim3 igrid((cq + rows_per_cta - 1) / rows_per_cta, G);
   if ((e = cudaMemsetAsync(w + L.cnt, 0, L.entry_off - L.cnt, stream)) != cudaSuccess) return e;
   ProfScope pf("attn_invert", stream);
+  int* hist_g = reinterpret_cast<int*>(w + L.hist);
   attn_count_kernel<<<igrid, 256, size_t(nblk) * 4, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0,
-                                                              cq, rows_per_cta, cnt, status);
+                                                              cq, rows_per_cta, cnt, hist_g, status);
   attn_scan_kernel<<<1, 1024, 0, stream>>>(cnt, q_offset, b, nblk, nbins, per_tile, Bs, c0, cq, grid, G,
                                            kvo_phases(G), reinterpret_cast<int*>(w + L.entry_off),
                                            reinterpret_cast<int*>(w + L.tile_off),
@@ -1890,7 +1891,7 @@ cudaError_t invert_chunk(const int32_t* sel, const int32_t* q_offset, const int3
                                                              reinterpret_cast<int*>(w + L.tile_off), nbins, per_tile,
                                                              reinterpret_cast<int4*>(w + L.tiles));
   attn_fill_kernel<<<igrid, 256, hist_smem, stream>>>(sel, q_offset, kv_len, b, Nq, Nk, G, K, Bs, nblk, c0, cq,
-                                                      rows_per_cta, reinterpret_cast<int*>(w + L.entry_off),
+                                                      rows_per_cta, reinterpret_cast<int*>(w + L.entry_off), hist_g,
                                                       reinterpret_cast<int*>(w + L.cursor),
                                                       reinterpret_cast<int*>(w + L.entries),
                                                       reinterpret_cast<int*>(w + L.rev));

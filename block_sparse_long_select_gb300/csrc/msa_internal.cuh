@@ -98,8 +98,8 @@ constexpr int kKvoMaxGrid = 1024;   // cta_start capacity
 constexpr int kKvoMaxPhases = 16;   // forward attention: group ranges processed one after another
 inline int kvo_phases(int G) { return G < kKvoMaxPhases ? G : kKvoMaxPhases; }
 struct KvoLayout {
-  size_t cnt, cursor, entry_off, tile_off, cost_off, cost_off2, total, cta_start, cta_seg, entries, rev, tiles, part_o,
-      part_lse, end;
+  size_t cnt, cursor, entry_off, tile_off, cost_off, cost_off2, total, cta_start, cta_seg, hist, entries, rev, tiles,
+      part_o, part_lse, end;
   size_t max_tiles;
 };
 // A CTA's tiles under the per-phase split (cta_seg [nph][grid + 1]): run r
