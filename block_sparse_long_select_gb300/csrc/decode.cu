@@ -260,21 +260,67 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
   if (tid == 0) arrivals[bg] = 0;  // ready for the next call
   const float* po = part_o + int64_t(bg) * K * kOut;
   const float* pm = part_ml + int64_t(bg) * K * HPG * 2;
-  for (int o = tid; o < kOut; o += kDecThreads) {
-    const int hh = o / D, c = o % D;
-    float M = -INFINITY;
-    for (int kk = 0; kk < K; ++kk) M = fmaxf(M, __ldcg(pm + (kk * HPG + hh) * 2));
-    float acc = 0.f, den = 0.f;
-    if (M > -INFINITY) {
-      for (int kk = 0; kk < K; ++kk) {
-        const float w = ex2f(__ldcg(pm + (kk * HPG + hh) * 2) - M);  // 0 for empty slots
-        den = fmaf(w, __ldcg(pm + (kk * HPG + hh) * 2 + 1), den);
-        acc = fmaf(w, __ldcg(po + int64_t(kk) * kOut + o), acc);
-      }
+  // Weights first, one warp per head: every slot's (max, sum) in one round of
+  // loads, the head's maximum M and denominator, and each slot's normalised
+  // weight exp(m - M) / den into shared memory (the K tile's space, which
+  // this CTA no longer reads). Then every output sums its slots with all of
+  // a thread's loads of a round in flight at once.
+  float* wts = reinterpret_cast<float*>(kt);  // [K][HPG]
+  float* hstat = wts + K * HPG;               // [HPG][2]: M, den
+  static_assert(kMaxK <= 64 && HPG <= kDecThreads / 32, "two slots per lane, one warp per head");
+  if (warp < HPG) {
+    const int hh = warp;
+    float mv[2], lv[2], M = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int kk = lane + 32 * x;
+      mv[x] = kk < K ? __ldcg(pm + (kk * HPG + hh) * 2) : -INFINITY;
+      lv[x] = kk < K ? __ldcg(pm + (kk * HPG + hh) * 2 + 1) : 0.f;
+      M = fmaxf(M, mv[x]);
     }
+    M = tc::warp_max_f32(M);
+    float w[2], den = 0.f;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      w[x] = M > -INFINITY ? ex2f(mv[x] - M) : 0.f;  // 0 for empty slots
+      den = fmaf(w[x], lv[x], den);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (lane + 32 * x < K) wts[(lane + 32 * x) * HPG + hh] = w[x] * inv;
+    if (lane == 0) {
+      hstat[2 * hh] = M;
+      hstat[2 * hh + 1] = den;
+    }
+  }
+  __syncthreads();
+  constexpr int kPer = (kOut + kDecThreads - 1) / kDecThreads;  // outputs per thread
+  float acc[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
+#pragma unroll 4
+  for (int kk = 0; kk < K; ++kk) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int o = tid + j * kDecThreads;
+      if (kPer * kDecThreads == kOut || o < kOut)
+        acc[j] = fmaf(wts[kk * HPG + o / D], __ldcg(po + int64_t(kk) * kOut + o), acc[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int o = tid + j * kDecThreads;
+    if (kPer * kDecThreads != kOut && o >= kOut) continue;
+    const int hh = o / D, c = o % D;
     const int h = g * HPG + hh;
-    out[(int64_t(b) * Hq + h) * D + c] = __float2bfloat16_rn(den > 0.f ? acc / den : 0.f);
-    if (lse && c == 0) lse[int64_t(b) * Hq + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+    out[(int64_t(b) * Hq + h) * D + c] = __float2bfloat16_rn(acc[j]);  // weights are 0 when den = 0
+    if (lse && c == 0) {
+      const float den = hstat[2 * hh + 1];
+      lse[int64_t(b) * Hq + h] = den > 0.f ? (hstat[2 * hh] + log2f(den)) * kLn2 : -INFINITY;
+    }
   }
 }
 
