@@ -16,8 +16,11 @@
 // in-thread). The sums over keys are a reduce-scatter across the warp's lanes
 // (lanes l and l + 16 end with entry l of a group of 16) and a four-warp
 // merge in shared memory. NS epilogue warpgroups (NS = 3 when three TMEM sets of
-// 128 + E columns fit, else 2) take tiles in turn, each with its own TMEM set
-// and gather ring slot, so the MMAs of the next tiles run under the epilogues.
+// 128 + E columns fit, else 2) take tiles in turn, each with its own TMEM set,
+// so the MMAs of the next tiles run under the epilogues. The gather ring has
+// one slot more than there are TMEM sets: tile z's rows are copied while the
+// epilogue of tile z - NS still holds the TMEM set that tile z's MMA needs,
+// which keeps the copy latency off the path from one epilogue to the next.
 // Warps 0..4 NS - 1 epilogue (warpgroup z % NS takes tile z), then two warps
 // gathering q rows, index-query rows and row data (cp.async, 128B-swizzled
 // K-major; tile records and entries fetched a tile ahead), one TMA warp for K
@@ -51,6 +54,8 @@ __device__ __forceinline__ void kt_cp16(uint32_t dst, const void* src, bool in) 
 
 __device__ __forceinline__ void cp_async_commit_kt() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all_kt() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// all but the most recently committed group have landed
+__device__ __forceinline__ void cp_async_wait_but_one_kt() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 __host__ __device__ constexpr uint32_t kt_idesc(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
@@ -83,7 +88,8 @@ __device__ __forceinline__ void kt_lse_merge(float& m, float& l, float m2, float
 template <int HPG>
 struct KtSmem {
   static constexpr int E = kKtRows / HPG;                  // entries per tile
-  static constexpr int NS = 512 / (128 + E) >= 3 ? 3 : 2;  // TMEM sets = epilogue warpgroups = ring slots
+  static constexpr int NS = 512 / (128 + E) >= 3 ? 3 : 2;  // TMEM sets = epilogue warpgroups
+  static constexpr int NR = NS + 1;                         // gather ring slots
   static constexpr int kThreads = (4 * NS + 4) * 32;
   static constexpr uint32_t kHalf = kKtRows * 128;         // one 64-wide half of a 128-row operand
   static constexpr uint32_t kK = kKtBs * kKtD * 2;         // K block (two halves)
@@ -92,12 +98,13 @@ struct KtSmem {
   static constexpr uint32_t kIQ = E * kKtDI * 2;           // gathered index-query rows (E x 128 B)
   static constexpr uint32_t kSlot = kQ + kIQ;              // multiple of 1024
   static constexpr uint32_t oK = 0, oIK = kK, oRing = kK + kIK;
-  static constexpr uint32_t oLse = oRing + NS * kSlot;     // [NS][128] lse * log2(e)
-  static constexpr uint32_t oLim = oLse + NS * kKtRows * 4;  // [NS][E] last visible key - t * 128 (-1: none)
-  static constexpr uint32_t oRed = oLim + NS * E * 4;       // [NS warpgroups][2][4 warps][16] float4 per-warp sums
+  static constexpr uint32_t oLse = oRing + NR * kSlot;     // [NR][128] lse * log2(e)
+  static constexpr uint32_t oLim = oLse + NR * kKtRows * 4;  // [NR][E] last visible key - t * 128 (-1: none)
+  static constexpr uint32_t oRed = oLim + NR * E * 4;       // [NS warpgroups][2][4 warps][16] float4 per-warp sums
   static constexpr uint32_t oBar = oRed + NS * 2 * 4 * kKtEG * 16;
-  static constexpr uint32_t kBars = 3 + 8 * NS;
+  static constexpr uint32_t kBars = 3 + 3 * NR + 6 * NS;
   static constexpr uint32_t kTotal = oBar + kBars * 8 + 16;
+  static_assert(kTotal <= 227u * 1024u && kSlot % 1024 == 0, "shared memory window; 1024-byte aligned slots");
 };
 
 template <int HPG>
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
     kl_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmIK,
                  const KlTcArgs p) {
   using SM = KtSmem<HPG>;
-  constexpr int E = SM::E, NS = SM::NS;
+  constexpr int E = SM::E, NS = SM::NS, NR = SM::NR;
   constexpr uint32_t kSet = 128 + E;  // TMEM columns per set: S^T, then I^T
   constexpr int EG = kKtEG;    // entries per reduce-scatter group
   constexpr int NG = E / EG;
@@ -127,9 +134,10 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* done_bar = bars + 2;
-  uint64_t* q_full = bars + 3;               // [NS] ring slots
-  uint64_t* q_empty = q_full + NS;           // [NS]
-  uint64_t* s_full = q_empty + NS;           // [NS] TMEM sets
+  uint64_t* q_full = bars + 3;               // [NR] ring slots: rows and row data landed
+  uint64_t* q_empty = q_full + NR;           // [NR]: the MMA has read the rows
+  uint64_t* rd_empty = q_empty + NR;         // [NR]: the epilogue has read the row data
+  uint64_t* s_full = rd_empty + NR;          // [NS] TMEM sets
   uint64_t* tm_empty = s_full + NS;          // [NS]
   uint64_t* red_full = tm_empty + NS;        // [NS][2]: a warpgroup's four warps' sums of a group are in red
   uint64_t* red_empty = red_full + 2 * NS;   // [NS][2]: its warp 0 has merged them
@@ -141,9 +149,12 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
-    for (int r = 0; r < NS; ++r) {
+    for (int r = 0; r < NR; ++r) {
       tc::mbar_init(&q_full[r], 2);
       tc::mbar_init(&q_empty[r], 1);
+      tc::mbar_init(&rd_empty[r], 4);
+    }
+    for (int r = 0; r < NS; ++r) {
       tc::mbar_init(&s_full[r], 1);
       tc::mbar_init(&tm_empty[r], 4);
     }
@@ -176,7 +187,7 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
 
   if (warp < kGather0) {
     // ------------------------------ epilogue ------------------------------
-    const int wg = warp >> 2;  // takes tiles z with z % NS == wg (TMEM set and ring slot wg)
+    const int wg = warp >> 2;  // takes tiles z with z % NS == wg (TMEM set wg, ring slot z % NR)
     const int quarter = warp & 3;
     const int key = quarter * 32 + lane;  // TMEM lane = key of the block
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
@@ -186,16 +197,17 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
     int4 tl_n = wg < n ? p.tiles[z0 + wg] : make_int4(0, 0, 0, 0);
     for (int z = wg; z < n && alive; z += NS) {
       const int set = wg, ph = (z / NS) & 1;
+      const int slot = z % NR, phr = (z / NR) & 1;
       const int4 tl = tl_n;
       if (z + NS < n) tl_n = p.tiles[z0 + z + NS];  // in flight during this tile
       if (!tc::mbar_wait(&s_full[set], ph, abort_flag) ||
-          !tc::mbar_wait(&q_full[set], ph, abort_flag)) {  // row data of the slot (already complete)
+          !tc::mbar_wait(&q_full[slot], phr, abort_flag)) {  // row data of the slot (already complete)
         fail();
         break;
       }
       tc::fence_after_sync();
-      const float* lse_r = lse_s + set * kKtRows;
-      const int* lim = lim_s + set * E;
+      const float* lse_r = lse_s + slot * kKtRows;
+      const int* lim = lim_s + slot * E;
       const uint32_t s_col = tmem + lane_base + uint32_t(set) * kSet;
 #pragma unroll 1
       for (int eg = 0; eg < NG; ++eg) {
@@ -251,7 +263,10 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
         if (eg + 1 == NG) {  // every TMEM column of this tile is in registers
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&tm_empty[set]);
+          if (lane == 0) {
+            tc::mbar_arrive(&tm_empty[set]);
+            tc::mbar_arrive(&rd_empty[slot]);  // its row data has been read too
+          }
         }
         kt_rs_sum(va, lane);
         kt_rs_sum(vb, lane);
@@ -327,9 +342,15 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
       const int eL = gw * (E / 2) + lane;
       entL_n = (lane < E / 2 && eL < tl_n.z) ? p.entries[tl_n.y + eL] : -1;
     };
-    if (n > 0) fetch(0);
-    for (int z = 0; z < n; ++z) {
-      const int slot = z % NS, ph = (z / NS) & 1;
+    // a slot is free once the MMA has read its rows and the epilogue of tile
+    // z - NR (same slot) has read its row data
+    auto slot_free = [&](int zz) {
+      const int sl = zz % NR;
+      const uint32_t par = ((zz / NR) & 1) ^ 1;
+      return tc::mbar_wait(&q_empty[sl], par, abort_flag) && tc::mbar_wait(&rd_empty[sl], par, abort_flag);
+    };
+    auto issue = [&](int z) {  // tile z's copies and row data (its records were fetched one tile ahead)
+      const int slot = z % NR;
       const int4 tl = tl_n;
       int ent2[2], entI[kItI];
 #pragma unroll
@@ -338,13 +359,6 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
       for (int it = 0; it < kItI; ++it) entI[it] = entI_n[it];
       const int entL = entL_n;
       if (z + 1 < n) fetch(z + 1);
-      // the slot is free once the MMA has read its rows and the epilogue of
-      // tile z - NS (same slot and TMEM set) has read its row data
-      if (!tc::mbar_wait(&q_empty[slot], ph ^ 1, abort_flag) ||
-          !tc::mbar_wait(&tm_empty[slot], ph ^ 1, abort_flag)) {
-        fail();
-        break;
-      }
       const int g = tl.x / p.nblk, t = tl.x % p.nblk;
       const uint32_t qs = tc::smem_u32(ring + slot * SM::kSlot), iqs = qs + SM::kQ;
       // this lane's two rows of the warp's 64 (row data)
@@ -389,12 +403,41 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
         if (entL >= 0 && sv.ok) lm = min(min(sv.q0 + p.c0 + (entL >> 6), sv.L - 1) - t * kKtBs, kKtBs - 1);
         lim_s[slot * E + gw * (E / 2) + lane] = lm;
       }
-      cp_async_wait_all_kt();
+    };
+    auto finish = [&](int z) {  // tile z's copies have landed: scale its lse, publish the slot
+      const int slot = z % NR;
 #pragma unroll
       for (int x = 0; x < 2; ++x) lse_s[slot * kKtRows + gw * 64 + x * 32 + lane] *= kKtLog2e;  // log2 units
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&q_full[slot]);
+    };
+    // Two tiles in flight: tile z + 1's copies go out before tile z's are
+    // waited for. Its slot frees when the epilogue of tile z + 1 - NR (that
+    // is, z - NS) has read its row data, the point at which that epilogue also
+    // releases the TMEM set tile z's MMA needs, so publishing tile z after
+    // that wait delays no MMA.
+    bool ok = true;
+    if (n > 0) {
+      fetch(0);
+      ok = slot_free(0);
+      if (ok)
+        issue(0);
+      else
+        fail();
+    }
+    for (int z = 0; ok && z < n; ++z) {
+      if (z + 1 < n) {
+        if (!slot_free(z + 1)) {
+          fail();
+          break;
+        }
+        issue(z + 1);
+        cp_async_wait_but_one_kt();  // tile z's group
+      } else {
+        cp_async_wait_all_kt();
+      }
+      finish(z);
     }
     cp_async_wait_all_kt();
   } else if (warp == kTmaWarp) {
@@ -431,7 +474,8 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
       const uint32_t ka16 = tc::smem_desc_lo(ka, 16), ika16 = tc::smem_desc_lo(ika, 16);
       int bin_n = n > 0 ? p.tiles[z0].x : -1;
       for (int z = 0; z < n; ++z) {
-        const int set = z % NS, slot = set, ph = (z / NS) & 1;
+        const int set = z % NS, ph = (z / NS) & 1;
+        const int slot = z % NR, phr = (z / NR) & 1;
         const int bin = bin_n;
         bin_n = z + 1 < n ? p.tiles[z0 + z + 1].x : -1;  // one tile ahead
         const bool first = bin != prev_bin;
@@ -444,7 +488,7 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
           }
           ++kv_uses;
         }
-        if (!tc::mbar_wait(&q_full[slot], ph, abort_flag) || !tc::mbar_wait(&tm_empty[set], ph ^ 1, abort_flag)) {
+        if (!tc::mbar_wait(&q_full[slot], phr, abort_flag) || !tc::mbar_wait(&tm_empty[set], ph ^ 1, abort_flag)) {
           fail();
           break;
         }
