@@ -17,10 +17,11 @@
 // (lanes l and l + 16 end with entry l of a group of 16) and a four-warp
 // merge in shared memory. NS epilogue warpgroups (NS = 3 when three TMEM sets of
 // 128 + E columns fit, else 2) take tiles in turn, each with its own TMEM set,
-// so the MMAs of the next tiles run under the epilogues. The gather ring has
-// one slot more than there are TMEM sets: tile z's rows are copied while the
-// epilogue of tile z - NS still holds the TMEM set that tile z's MMA needs,
-// which keeps the copy latency off the path from one epilogue to the next.
+// so the MMAs of the next tiles run under the epilogues. The gathered rows and
+// a tile's row data (lse, visibility limits) sit in separate rings: a row slot
+// is free once the MMA has read it, a row-data slot once the epilogue has, so
+// the copies of tile z start as soon as the MMA of tile z - NR is done, well
+// before the epilogue of tile z - NS releases the TMEM set tile z needs.
 // Warps 0..4 NS - 1 epilogue (warpgroup z % NS takes tile z), then two warps
 // gathering q rows, index-query rows and row data (cp.async, 128B-swizzled
 // K-major; tile records and entries fetched a tile ahead), one TMA warp for K
@@ -89,7 +90,8 @@ template <int HPG>
 struct KtSmem {
   static constexpr int E = kKtRows / HPG;                  // entries per tile
   static constexpr int NS = 512 / (128 + E) >= 3 ? 3 : 2;  // TMEM sets = epilogue warpgroups
-  static constexpr int NR = NS + 1;                         // gather ring slots
+  static constexpr int NR = NS + 1;                         // gathered-row ring slots
+  static constexpr int ND = 8;                              // row-data ring slots
   static constexpr int kThreads = (4 * NS + 4) * 32;
   static constexpr uint32_t kHalf = kKtRows * 128;         // one 64-wide half of a 128-row operand
   static constexpr uint32_t kK = kKtBs * kKtD * 2;         // K block (two halves)
@@ -98,11 +100,11 @@ struct KtSmem {
   static constexpr uint32_t kIQ = E * kKtDI * 2;           // gathered index-query rows (E x 128 B)
   static constexpr uint32_t kSlot = kQ + kIQ;              // multiple of 1024
   static constexpr uint32_t oK = 0, oIK = kK, oRing = kK + kIK;
-  static constexpr uint32_t oLse = oRing + NR * kSlot;     // [NR][128] lse * log2(e)
-  static constexpr uint32_t oLim = oLse + NR * kKtRows * 4;  // [NR][E] last visible key - t * 128 (-1: none)
-  static constexpr uint32_t oRed = oLim + NR * E * 4;       // [NS warpgroups][2][4 warps][16] float4 per-warp sums
+  static constexpr uint32_t oLse = oRing + NR * kSlot;     // [ND][128] lse * log2(e)
+  static constexpr uint32_t oLim = oLse + ND * kKtRows * 4;  // [ND][E] last visible key - t * 128 (-1: none)
+  static constexpr uint32_t oRed = oLim + ND * E * 4;       // [NS warpgroups][2][4 warps][16] float4 per-warp sums
   static constexpr uint32_t oBar = oRed + NS * 2 * 4 * kKtEG * 16;
-  static constexpr uint32_t kBars = 3 + 3 * NR + 6 * NS;
+  static constexpr uint32_t kBars = 3 + 2 * NR + 2 * ND + 6 * NS;
   static constexpr uint32_t kTotal = oBar + kBars * 8 + 16;
   static_assert(kTotal <= 227u * 1024u && kSlot % 1024 == 0, "shared memory window; 1024-byte aligned slots");
 };
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
     kl_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmIK,
                  const KlTcArgs p) {
   using SM = KtSmem<HPG>;
-  constexpr int E = SM::E, NS = SM::NS, NR = SM::NR;
+  constexpr int E = SM::E, NS = SM::NS, NR = SM::NR, ND = SM::ND;
   constexpr uint32_t kSet = 128 + E;  // TMEM columns per set: S^T, then I^T
   constexpr int EG = kKtEG;    // entries per reduce-scatter group
   constexpr int NG = E / EG;
@@ -134,10 +136,11 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* done_bar = bars + 2;
-  uint64_t* q_full = bars + 3;               // [NR] ring slots: rows and row data landed
-  uint64_t* q_empty = q_full + NR;           // [NR]: the MMA has read the rows
-  uint64_t* rd_empty = q_empty + NR;         // [NR]: the epilogue has read the row data
-  uint64_t* s_full = rd_empty + NR;          // [NS] TMEM sets
+  uint64_t* q_full = bars + 3;               // [NR] row slots: the rows have landed
+  uint64_t* q_empty = q_full + NR;           // [NR]: the MMA has read them
+  uint64_t* rd_full = q_empty + NR;          // [ND] row-data slots: written
+  uint64_t* rd_empty = rd_full + ND;         // [ND]: the epilogue has read them
+  uint64_t* s_full = rd_empty + ND;          // [NS] TMEM sets
   uint64_t* tm_empty = s_full + NS;          // [NS]
   uint64_t* red_full = tm_empty + NS;        // [NS][2]: a warpgroup's four warps' sums of a group are in red
   uint64_t* red_empty = red_full + 2 * NS;   // [NS][2]: its warp 0 has merged them
@@ -152,6 +155,9 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
     for (int r = 0; r < NR; ++r) {
       tc::mbar_init(&q_full[r], 2);
       tc::mbar_init(&q_empty[r], 1);
+    }
+    for (int r = 0; r < ND; ++r) {
+      tc::mbar_init(&rd_full[r], 2);
       tc::mbar_init(&rd_empty[r], 4);
     }
     for (int r = 0; r < NS; ++r) {
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
 
   if (warp < kGather0) {
     // ------------------------------ epilogue ------------------------------
-    const int wg = warp >> 2;  // takes tiles z with z % NS == wg (TMEM set wg, ring slot z % NR)
+    const int wg = warp >> 2;  // takes tiles z with z % NS == wg (TMEM set wg, row-data slot z % ND)
     const int quarter = warp & 3;
     const int key = quarter * 32 + lane;  // TMEM lane = key of the block
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
@@ -197,11 +203,11 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
     int4 tl_n = wg < n ? p.tiles[z0 + wg] : make_int4(0, 0, 0, 0);
     for (int z = wg; z < n && alive; z += NS) {
       const int set = wg, ph = (z / NS) & 1;
-      const int slot = z % NR, phr = (z / NR) & 1;
+      const int slot = z % ND, phr = (z / ND) & 1;
       const int4 tl = tl_n;
       if (z + NS < n) tl_n = p.tiles[z0 + z + NS];  // in flight during this tile
       if (!tc::mbar_wait(&s_full[set], ph, abort_flag) ||
-          !tc::mbar_wait(&q_full[slot], phr, abort_flag)) {  // row data of the slot (already complete)
+          !tc::mbar_wait(&rd_full[slot], phr, abort_flag)) {  // the tile's row data (already complete)
         fail();
         break;
       }
@@ -342,15 +348,14 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
       const int eL = gw * (E / 2) + lane;
       entL_n = (lane < E / 2 && eL < tl_n.z) ? p.entries[tl_n.y + eL] : -1;
     };
-    // a slot is free once the MMA has read its rows and the epilogue of tile
-    // z - NR (same slot) has read its row data
+    // tile z's row slot is free once the MMA of tile z - NR has read it, its
+    // row-data slot once the epilogue of tile z - ND has
     auto slot_free = [&](int zz) {
-      const int sl = zz % NR;
-      const uint32_t par = ((zz / NR) & 1) ^ 1;
-      return tc::mbar_wait(&q_empty[sl], par, abort_flag) && tc::mbar_wait(&rd_empty[sl], par, abort_flag);
+      return tc::mbar_wait(&q_empty[zz % NR], ((zz / NR) & 1) ^ 1, abort_flag) &&
+             tc::mbar_wait(&rd_empty[zz % ND], ((zz / ND) & 1) ^ 1, abort_flag);
     };
     auto issue = [&](int z) {  // tile z's copies and row data (its records were fetched one tile ahead)
-      const int slot = z % NR;
+      const int slot = z % NR, dslot = z % ND;
       const int4 tl = tl_n;
       int ent2[2], entI[kItI];
 #pragma unroll
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const int r = gw * 64 + x * 32 + lane;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(lse_s + slot * kKtRows + r)),
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(lse_s + dslot * kKtRows + r)),
                      "l"(p.lse + qrow2[x]), "r"(ent2[x] >= 0 ? 4u : 0u)
                      : "memory");
       }
@@ -401,22 +406,24 @@ __global__ void __launch_bounds__(KtSmem<HPG>::kThreads, 1)
       if (lane < E / 2) {
         int lm = -1;
         if (entL >= 0 && sv.ok) lm = min(min(sv.q0 + p.c0 + (entL >> 6), sv.L - 1) - t * kKtBs, kKtBs - 1);
-        lim_s[slot * E + gw * (E / 2) + lane] = lm;
+        lim_s[dslot * E + gw * (E / 2) + lane] = lm;
       }
     };
-    auto finish = [&](int z) {  // tile z's copies have landed: scale its lse, publish the slot
-      const int slot = z % NR;
+    auto finish = [&](int z) {  // tile z's copies have landed: scale its lse, publish both slots
+      const int dslot = z % ND;
 #pragma unroll
-      for (int x = 0; x < 2; ++x) lse_s[slot * kKtRows + gw * 64 + x * 32 + lane] *= kKtLog2e;  // log2 units
+      for (int x = 0; x < 2; ++x) lse_s[dslot * kKtRows + gw * 64 + x * 32 + lane] *= kKtLog2e;  // log2 units
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&q_full[slot]);
+      if (lane == 0) {
+        tc::mbar_arrive(&q_full[z % NR]);
+        tc::mbar_arrive(&rd_full[dslot]);
+      }
     };
     // Two tiles in flight: tile z + 1's copies go out before tile z's are
-    // waited for. Its slot frees when the epilogue of tile z + 1 - NR (that
-    // is, z - NS) has read its row data, the point at which that epilogue also
-    // releases the TMEM set tile z's MMA needs, so publishing tile z after
-    // that wait delays no MMA.
+    // waited for. Its slots free when the MMA of tile z + 1 - NR and the
+    // epilogue of tile z + 1 - ND are done, both of which precede tile z's
+    // MMA, so publishing tile z after that wait delays no MMA.
     bool ok = true;
     if (n > 0) {
       fetch(0);
