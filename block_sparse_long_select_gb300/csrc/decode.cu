@@ -248,9 +248,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(
     }
   }
   // ---- the last of the K slot CTAs of (b, g) merges the partials ----
-  __threadfence();
+  // The barrier orders every thread's partial stores before thread 0's
+  // device-scope fence, which (being cumulative) publishes them all before
+  // its arrival; one fence instead of one per thread.
   __syncthreads();
   if (tid == 0) {
+    __threadfence();
     const int old = atomicAdd(&arrivals[bg], 1);
     last_s = old == K - 1;
   }
